@@ -1,0 +1,206 @@
+"""Plain fp64 CPU oracle for scaled-dot-product attention, forward and backward.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py``; never by the CUDA library or its binding.
+
+Sources (web pages, cited by title and section):
+
+* [PyTensor-SDPA] "PERF: detect scaled-dot-product-attention pattern and lower to
+  mx.fast.scaled_dot_product_attention" (pymc-devs/pytensor issue 2090), section
+  "Proposed change": the NumPy ``perform`` sketch computes scores = (Q Kᵀ)·scale,
+  subtracts the row maximum, exponentiates, divides by the row sum and multiplies by V.
+  The forward here is that definition, with the causal mask and grouped KV heads added.
+* [MPS-SDPA] "MPS scaled_dot_product_attention (SDPA)" (PyTorch issue, stepcodex
+  mirror), section "Problem - Unused second output tensor": the forward's second
+  output (the per-row logsumexp) is what the backward needs.
+* [MLX-VJP] "[Metal] Add Flash Attention VJP for training" (ml-explore/mlx PR 2995),
+  sections "Implementation Notes" and "Key Features": logsumexp cached by the forward,
+  GQA (several query heads share one KV head), causal masking; and the maintainer
+  comment listing the backward's steps (recompute scores, load logsumexp,
+  P = exp(S - LSE), gradients).
+* [mps-flash-sdpa] "mps-flash-sdpa 0.1.0" (PyPI), section "Quick Start": the
+  ``is_causal`` flag of ``F.scaled_dot_product_attention``.
+
+Readings of points the pages leave open (each also listed in the design notes):
+
+* logsumexp is the natural log of the row sum of exp(scale·q·k) over visible keys,
+  including the scale; stored in fp32 by the GPU, fp64 here.
+* causal is top-left aligned: key j is masked for query i when j > i, for any Lq, Lkv.
+  Key 0 is always visible, so no row is ever fully masked.
+* GQA groups are contiguous: query head h reads KV head h // (Hq // Hkv).
+* The backward is the textbook vector-Jacobian product of the forward with
+  delta = rowsum(dO * O) taken from this oracle's own fp64 O.
+* The oracle does not clamp exponent arguments (the clamp mentioned in [MLX-VJP]
+  "Implementation Notes" only guards the GPU's exp2 against overflow; after the row
+  maximum is subtracted every argument is <= 0 already).
+
+Arrays are NumPy, layout [B, H, L, D].  Inputs may be any float dtype; they are upcast
+exactly to float64 (bf16/fp16 values are exactly representable).  Work goes one
+(batch, head) at a time, and in blocks of whole query rows when ``row_block`` is given
+so that long sequences fit in memory; every row is still computed over all its keys at
+once, exactly as the definition says.
+
+Parity: every function here is pinned by ``tests/test_oracle.py`` (finite differences,
+closed forms, invariants, a hand-derived fixture under ``tests/golden/`` and a library
+cross-check), so none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "head_forward",
+    "head_backward",
+    "group_backward",
+    "sdpa_forward",
+    "sdpa_backward",
+]
+
+
+def _f64(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+def _scores(q_rows, k, scale, is_causal, row_idx):
+    """Scores of a block of query rows against all keys, masked.
+
+    [PyTensor-SDPA] "Proposed change": scores = (q @ kᵀ) * scale.
+    Causal ([mps-flash-sdpa] "Quick Start" ``is_causal``; top-left reading): the score of
+    key j for absolute query row i = row_idx[r] is -inf when j > i.
+    """
+    s = (q_rows @ k.T) * scale
+    if is_causal:
+        j = np.arange(k.shape[0])[None, :]
+        s = np.where(j > np.asarray(row_idx)[:, None], -np.inf, s)
+    return s
+
+
+def _softmax_rows(s):
+    """Row softmax as [PyTensor-SDPA] "Proposed change" writes it, plus the logsumexp.
+
+    Subtract the row maximum, exponentiate, divide by the row sum.  The logsumexp of
+    the row ([MPS-SDPA] "Problem - Unused second output tensor") is max + log(sum).
+    """
+    m = s.max(axis=1, keepdims=True)
+    e = np.exp(s - m)
+    l = e.sum(axis=1, keepdims=True)
+    p = e / l
+    lse = (m + np.log(l))[:, 0]
+    return p, lse
+
+
+def _blocks(n, row_block):
+    step = n if not row_block else int(row_block)
+    for r0 in range(0, n, step):
+        yield r0, min(n, r0 + step)
+
+
+def head_forward(q, k, v, scale, is_causal, rows=None, row_block=None):
+    """Forward of one head: O = softmax(scale·q kᵀ [+ causal mask]) v and its logsumexp.
+
+    q: [Lq, D], k, v: [Lkv, D].  ``rows`` (optional, sorted or not) selects which query
+    rows to compute; by default all.  Returns (O [n, D], lse [n]) in float64.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    idx = np.arange(q.shape[0]) if rows is None else np.asarray(rows, dtype=np.int64)
+    o = np.empty((idx.size, v.shape[1]))
+    lse = np.empty(idx.size)
+    for a, b in _blocks(idx.size, row_block):
+        sel = idx[a:b]
+        p, lse[a:b] = _softmax_rows(_scores(q[sel], k, scale, is_causal, sel))
+        o[a:b] = p @ v
+    return o, lse
+
+
+def head_backward(q, k, v, dout, scale, is_causal, row_block=None):
+    """Backward of one head (textbook VJP).  Returns (dq, dk_part, dv_part) in float64.
+
+    Steps, per [MLX-VJP]'s description (recompute S, P = exp(S - LSE), then gradients)
+    written as the plain chain rule of the forward:
+        P   = softmax(S)                         (recomputed from q, k)
+        O   = P v
+        dV  = Pᵀ dO
+        dP  = dO vᵀ
+        δ   = rowsum(dO ∘ O)
+        dS  = P ∘ (dP − δ)
+        dQ  = scale · dS k
+        dK  = scale · dSᵀ q
+    dk_part and dv_part are this head's contribution to its KV head; the caller sums
+    them over the query heads of the group.
+    """
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    dq = np.empty_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for a, b in _blocks(q.shape[0], row_block):
+        p, _ = _softmax_rows(_scores(q[a:b], k, scale, is_causal, np.arange(a, b)))
+        o = p @ v
+        dv += p.T @ dout[a:b]
+        dp = dout[a:b] @ v.T
+        delta = (dout[a:b] * o).sum(axis=1, keepdims=True)
+        ds = p * (dp - delta)
+        dq[a:b] = scale * (ds @ k)
+        dk += scale * (ds.T @ q[a:b])
+    return dq, dk, dv
+
+
+def _check(q, k, v):
+    if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
+        raise ValueError("expected [B, H, L, D] arrays")
+    B, Hq, _, D = q.shape
+    if k.shape[0] != B or v.shape[:3] != k.shape[:3] or k.shape[3] != D:
+        raise ValueError("q, k, v shapes disagree")
+    Hkv = k.shape[1]
+    if Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    return B, Hq, Hkv, Hq // Hkv
+
+
+def sdpa_forward(q, k, v, scale, is_causal, row_block=None):
+    """Forward over [B, H, L, D] arrays with GQA ([MLX-VJP] "Key Features").
+
+    Query head h reads KV head h // G with G = Hq // Hkv.  Returns (O [B,Hq,Lq,D],
+    lse [B,Hq,Lq]) in float64.
+    """
+    B, Hq, Hkv, G = _check(q, k, v)
+    o = np.empty(q.shape[:3] + (v.shape[3],))
+    lse = np.empty(q.shape[:3])
+    for b in range(B):
+        for h in range(Hq):
+            g = h // G
+            o[b, h], lse[b, h] = head_forward(q[b, h], k[b, g], v[b, g], scale,
+                                              is_causal, row_block=row_block)
+    return o, lse
+
+
+def group_backward(q, k, v, dout, scale, is_causal, b, g, row_block=None):
+    """Backward for KV head g of batch b: dQ of its G query heads, and dK, dV of g.
+
+    dK and dV sum the contributions of every query head that reads KV head g
+    ([MLX-VJP] "Implementation Notes": several query heads share one KV head).
+    Returns (dq [G, Lq, D], dk [Lkv, D], dv [Lkv, D]).
+    """
+    B, Hq, Hkv, G = _check(q, k, v)
+    dq = np.empty((G,) + q.shape[2:])
+    dk = np.zeros(k.shape[2:])
+    dv = np.zeros(v.shape[2:])
+    for t in range(G):
+        h = g * G + t
+        dq[t], dk_h, dv_h = head_backward(q[b, h], k[b, g], v[b, g], dout[b, h], scale,
+                                          is_causal, row_block=row_block)
+        dk += dk_h
+        dv += dv_h
+    return dq, dk, dv
+
+
+def sdpa_backward(q, k, v, dout, scale, is_causal, row_block=None):
+    """Backward over [B, H, L, D] arrays.  Returns (dq, dk, dv) in float64."""
+    B, Hq, Hkv, G = _check(q, k, v)
+    dq = np.empty(q.shape, dtype=np.float64)
+    dk = np.empty(k.shape, dtype=np.float64)
+    dv = np.empty(v.shape, dtype=np.float64)
+    for b in range(B):
+        for g in range(Hkv):
+            dq[b, g * G:(g + 1) * G], dk[b, g], dv[b, g] = group_backward(
+                q, k, v, dout, scale, is_causal, b, g, row_block=row_block)
+    return dq, dk, dv

@@ -1,0 +1,395 @@
+"""Pins for the CPU oracle: checks against facts that do not come from the oracle itself.
+
+Each test names the fact it uses: hand-derived closed forms (``tests/golden``), central
+finite differences of the forward, special cases with closed forms, invariants of
+softmax attention, and an independent library routine (PyTorch's CPU SDPA in float64,
+as a second opinion only).  ``test_planted_mistakes_are_caught`` plants plausible bugs
+in a copy of the oracle and checks that at least one pin fails for each.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import ref
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def rnd(rng, *shape):
+    return rng.standard_normal(shape)
+
+
+def make(rng, B=1, Hq=2, Hkv=1, Lq=5, Lkv=6, D=4):
+    q = rnd(rng, B, Hq, Lq, D)
+    k = rnd(rng, B, Hkv, Lkv, D)
+    v = rnd(rng, B, Hkv, Lkv, D)
+    do = rnd(rng, B, Hq, Lq, D)
+    return q, k, v, do
+
+
+# ----------------------------------------------------------------------------- golden
+def _exact(x):
+    """[num, den] -> num/den ; [num, den, c] -> num/den * ln(c); nested lists recurse."""
+    if isinstance(x, list) and x and not isinstance(x[0], list):
+        val = x[0] / x[1]
+        return val * math.log(x[2]) if len(x) == 3 else val
+    return [_exact(y) for y in x]
+
+
+def _cases():
+    with open(os.path.join(HERE, "golden", "closed_form_cases.json")) as f:
+        return json.load(f)["cases"]
+
+
+@pytest.mark.parametrize("case", _cases(), ids=lambda c: c["name"])
+def test_closed_form_fixtures(case):
+    q = np.array(case["q"])
+    k = np.array(_exact(case["k_exact"]))
+    v = np.array(case["v"])
+    do = np.array(case["dout"])
+    assert np.allclose(k, np.array(case["k"]), atol=1e-15)
+    o, lse = oracle.sdpa_forward(q, k, v, case["scale"], case["is_causal"])
+    dq, dk, dv = oracle.sdpa_backward(q, k, v, do, case["scale"], case["is_causal"])
+    np.testing.assert_allclose(o, np.array(_exact(case["o"])), atol=1e-13)
+    np.testing.assert_allclose(lse, np.array(_exact(case["lse"])), atol=1e-13)
+    np.testing.assert_allclose(dq, np.array(_exact(case["dq"])), atol=1e-13)
+    np.testing.assert_allclose(dk, np.array(_exact(case["dk"])), atol=1e-13)
+    np.testing.assert_allclose(dv, np.array(_exact(case["dv"])), atol=1e-13)
+
+
+# ----------------------------------------------------------------- finite differences
+def _loss(q, k, v, do, scale, causal, impl=None):
+    impl = impl or oracle
+    o, _ = impl.sdpa_forward(q, k, v, scale, causal)
+    return float((o * do).sum())
+
+
+def _fd_grad(x, f, h=1e-6):
+    g = np.zeros_like(x)
+    it = np.nditer(x, flags=["multi_index"])
+    for _ in it:
+        i = it.multi_index
+        old = x[i]
+        x[i] = old + h
+        fp = f()
+        x[i] = old - h
+        fm = f()
+        x[i] = old
+        g[i] = (fp - fm) / (2 * h)
+    return g
+
+
+FD_CASES = [
+    dict(B=1, Hq=2, Hkv=1, Lq=5, Lkv=6, D=4, causal=False),
+    dict(B=1, Hq=2, Hkv=1, Lq=5, Lkv=6, D=4, causal=True),
+    dict(B=2, Hq=3, Hkv=3, Lq=4, Lkv=4, D=3, causal=True),
+    dict(B=1, Hq=4, Hkv=2, Lq=7, Lkv=3, D=2, causal=True),
+    dict(B=1, Hq=1, Hkv=1, Lq=1, Lkv=5, D=3, causal=False),
+]
+
+
+@pytest.mark.parametrize("case", FD_CASES, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
+def test_backward_matches_finite_differences(case, impl=None):
+    impl = impl or oracle
+    rng = np.random.default_rng(11)
+    c = dict(case)
+    causal = c.pop("causal")
+    q, k, v, do = make(rng, **c)
+    scale = 0.7
+    dq, dk, dv = impl.sdpa_backward(q, k, v, do, scale, causal)
+    f = lambda: _loss(q, k, v, do, scale, causal, impl)  # noqa: E731
+    np.testing.assert_allclose(dq, _fd_grad(q, f), atol=1e-7, rtol=1e-6)
+    np.testing.assert_allclose(dk, _fd_grad(k, f), atol=1e-7, rtol=1e-6)
+    np.testing.assert_allclose(dv, _fd_grad(v, f), atol=1e-7, rtol=1e-6)
+
+
+# ----------------------------------------------------------------- special cases
+def test_rows_of_p_sum_to_one(impl=None):
+    """With V = identity (Lkv <= D), O is P itself: every row is a probability vector."""
+    impl = impl or oracle
+    rng = np.random.default_rng(1)
+    for causal in (False, True):
+        q = rnd(rng, 1, 2, 9, 8)
+        k = rnd(rng, 1, 2, 8, 8)
+        v = np.broadcast_to(np.eye(8), (1, 2, 8, 8)).copy()
+        o, lse = impl.sdpa_forward(q, k, v, 0.9, causal)
+        assert (o >= 0).all()
+        np.testing.assert_allclose(o.sum(-1), 1.0, atol=1e-14)
+        if causal:  # masked entries are exactly zero
+            for i in range(8):
+                assert (o[..., i, i + 1:] == 0).all()
+        # lse is log of the row sum of exp(scores): check against P's definition
+        s = np.einsum("bhid,bhjd->bhij", q, k) * 0.9
+        j = np.arange(8)
+        for i in range(9):
+            vis = j <= i if causal else np.ones(8, bool)
+            np.testing.assert_allclose(o[..., i, vis], np.exp(s[..., i, vis] - lse[..., i, None]),
+                                       atol=1e-13)
+
+
+def test_constant_v_gives_constant_output(impl=None):
+    impl = impl or oracle
+    rng = np.random.default_rng(2)
+    q, k, _, _ = make(rng, B=2, Hq=4, Hkv=2, Lq=6, Lkv=9, D=5)
+    c = rnd(rng, 5)
+    v = np.broadcast_to(c, (2, 2, 9, 5)).copy()
+    for causal in (False, True):
+        o, _ = impl.sdpa_forward(q, k, v, 0.3, causal)
+        np.testing.assert_allclose(o, np.broadcast_to(c, o.shape), atol=1e-13)
+
+
+def test_causal_first_row_attends_only_to_key0(impl=None):
+    impl = impl or oracle
+    rng = np.random.default_rng(3)
+    q, k, v, do = make(rng, B=1, Hq=4, Hkv=2, Lq=6, Lkv=6, D=5)
+    scale = 0.45
+    o, lse = impl.sdpa_forward(q, k, v, scale, True)
+    dq, _, _ = impl.sdpa_backward(q, k, v, do, scale, True)
+    for h in range(4):
+        g = h // 2
+        np.testing.assert_allclose(o[0, h, 0], v[0, g, 0], atol=1e-14)
+        np.testing.assert_allclose(lse[0, h, 0], scale * q[0, h, 0] @ k[0, g, 0], atol=1e-14)
+        np.testing.assert_allclose(dq[0, h, 0], 0.0, atol=1e-14)
+
+
+def test_single_key(impl=None):
+    """Lkv = 1: O = v0, lse = scale q.k0, dQ = dK = 0, dV0 = sum of dO over the group."""
+    impl = impl or oracle
+    rng = np.random.default_rng(4)
+    q, k, v, do = make(rng, B=2, Hq=6, Hkv=2, Lq=5, Lkv=1, D=3)
+    for causal in (False, True):
+        o, lse = impl.sdpa_forward(q, k, v, 1.3, causal)
+        dq, dk, dv = impl.sdpa_backward(q, k, v, do, 1.3, causal)
+        kk = np.repeat(k, 3, axis=1)
+        np.testing.assert_allclose(o, np.repeat(v, 3, axis=1).repeat(5, axis=2), atol=1e-14)
+        np.testing.assert_allclose(lse, 1.3 * np.einsum("bhid,bhjd->bhi", q, kk), atol=1e-13)
+        np.testing.assert_allclose(dq, 0.0, atol=1e-13)
+        np.testing.assert_allclose(dk, 0.0, atol=1e-13)
+        np.testing.assert_allclose(dv[:, :, 0], do.reshape(2, 2, 3 * 5, 3).sum(2), atol=1e-13)
+
+
+def test_zero_scale_is_uniform_attention(impl=None):
+    """scale = 0: O is the mean of V (causal: the prefix mean); lse = log(#visible keys)."""
+    impl = impl or oracle
+    rng = np.random.default_rng(5)
+    q, k, v, _ = make(rng, B=1, Hq=2, Hkv=1, Lq=7, Lkv=5, D=3)
+    o, lse = impl.sdpa_forward(q, k, v, 0.0, False)
+    np.testing.assert_allclose(o, np.broadcast_to(v.mean(2, keepdims=True), o.shape), atol=1e-14)
+    np.testing.assert_allclose(lse, math.log(5), atol=1e-14)
+    o, lse = impl.sdpa_forward(q, k, v, 0.0, True)
+    for i in range(7):
+        n = min(i + 1, 5)
+        np.testing.assert_allclose(o[0, :, i], np.broadcast_to(v[0, 0, :n].mean(0), (2, 3)),
+                                   atol=1e-14)
+        np.testing.assert_allclose(lse[0, :, i], math.log(n), atol=1e-14)
+
+
+# ----------------------------------------------------------------- invariants
+def test_gradient_sums(impl=None):
+    """Rows of dS sum to 0, so dK sums to 0 over keys; dV sums to the sum of dO."""
+    impl = impl or oracle
+    rng = np.random.default_rng(6)
+    q, k, v, do = make(rng, B=2, Hq=4, Hkv=2, Lq=8, Lkv=11, D=6)
+    for causal in (False, True):
+        dq, dk, dv = impl.sdpa_backward(q, k, v, do, 0.6, causal)
+        np.testing.assert_allclose(dk.sum(2), 0.0, atol=1e-12)
+        np.testing.assert_allclose(dv.sum(2), do.reshape(2, 2, 2 * 8, 6).sum(2), atol=1e-12)
+
+
+def test_key_shift_invariance(impl=None):
+    """K <- K + c: O and dQ unchanged (every score of row i shifts by scale q_i.c),
+    lse shifts by scale q_i.c."""
+    impl = impl or oracle
+    rng = np.random.default_rng(7)
+    q, k, v, do = make(rng, B=1, Hq=4, Hkv=2, Lq=6, Lkv=7, D=5)
+    c = rnd(rng, 5)
+    for causal in (False, True):
+        o0, l0 = impl.sdpa_forward(q, k, v, 0.8, causal)
+        o1, l1 = impl.sdpa_forward(q, k + c, v, 0.8, causal)
+        dq0, dk0, dv0 = impl.sdpa_backward(q, k, v, do, 0.8, causal)
+        dq1, dk1, dv1 = impl.sdpa_backward(q, k + c, v, do, 0.8, causal)
+        np.testing.assert_allclose(o1, o0, atol=1e-12)
+        np.testing.assert_allclose(l1 - l0, 0.8 * q @ c, atol=1e-12)
+        np.testing.assert_allclose(dq1, dq0, atol=1e-12)
+        np.testing.assert_allclose(dk1, dk0, atol=1e-12)
+        np.testing.assert_allclose(dv1, dv0, atol=1e-12)
+
+
+def test_gqa_equals_repeated_kv_heads(impl=None):
+    """GQA = MHA on KV heads repeated G times in place (contiguous groups), with dK/dV
+    summed over each group."""
+    impl = impl or oracle
+    rng = np.random.default_rng(8)
+    q, k, v, do = make(rng, B=2, Hq=6, Hkv=2, Lq=5, Lkv=7, D=4)
+    for causal in (False, True):
+        o, lse = impl.sdpa_forward(q, k, v, 0.5, causal)
+        dq, dk, dv = impl.sdpa_backward(q, k, v, do, 0.5, causal)
+        kr, vr = np.repeat(k, 3, axis=1), np.repeat(v, 3, axis=1)
+        o2, lse2 = impl.sdpa_forward(q, kr, vr, 0.5, causal)
+        dq2, dk2, dv2 = impl.sdpa_backward(q, kr, vr, do, 0.5, causal)
+        np.testing.assert_allclose(o, o2, atol=1e-14)
+        np.testing.assert_allclose(lse, lse2, atol=1e-14)
+        np.testing.assert_allclose(dq, dq2, atol=1e-13)
+        np.testing.assert_allclose(dk, dk2.reshape(2, 2, 3, 7, 4).sum(2), atol=1e-13)
+        np.testing.assert_allclose(dv, dv2.reshape(2, 2, 3, 7, 4).sum(2), atol=1e-13)
+
+
+def test_mha_equals_independent_heads(impl=None):
+    """Hq = Hkv: every head is an independent attention problem."""
+    impl = impl or oracle
+    rng = np.random.default_rng(9)
+    q, k, v, do = make(rng, B=2, Hq=3, Hkv=3, Lq=4, Lkv=6, D=3)
+    o, lse = impl.sdpa_forward(q, k, v, 0.5, True)
+    dq, dk, dv = impl.sdpa_backward(q, k, v, do, 0.5, True)
+    for b in range(2):
+        for h in range(3):
+            oh, lh = impl.sdpa_forward(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1],
+                                       v[b:b + 1, h:h + 1], 0.5, True)
+            gh = impl.sdpa_backward(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1],
+                                    v[b:b + 1, h:h + 1], do[b:b + 1, h:h + 1], 0.5, True)
+            np.testing.assert_allclose(o[b, h], oh[0, 0], atol=1e-14)
+            np.testing.assert_allclose(lse[b, h], lh[0, 0], atol=1e-14)
+            for full, part in zip((dq, dk, dv), gh):
+                np.testing.assert_allclose(full[b, h], part[0, 0], atol=1e-14)
+
+
+def test_row_blocks_and_sampled_rows_agree():
+    rng = np.random.default_rng(10)
+    q, k, v, do = make(rng, B=1, Hq=4, Hkv=2, Lq=37, Lkv=29, D=4)
+    for causal in (False, True):
+        o, lse = oracle.sdpa_forward(q, k, v, 0.4, causal)
+        o2, lse2 = oracle.sdpa_forward(q, k, v, 0.4, causal, row_block=8)
+        g = oracle.sdpa_backward(q, k, v, do, 0.4, causal)
+        g2 = oracle.sdpa_backward(q, k, v, do, 0.4, causal, row_block=5)
+        np.testing.assert_allclose(o, o2, atol=1e-14)
+        np.testing.assert_allclose(lse, lse2, atol=1e-14)
+        for a, b in zip(g, g2):
+            np.testing.assert_allclose(a, b, atol=1e-13)
+        rows = np.array([36, 0, 17, 5])
+        orow, lrow = oracle.head_forward(q[0, 3], k[0, 1], v[0, 1], 0.4, causal, rows=rows)
+        np.testing.assert_allclose(orow, o[0, 3, rows], atol=1e-14)
+        np.testing.assert_allclose(lrow, lse[0, 3, rows], atol=1e-14)
+
+
+def test_float32_inputs_are_upcast_exactly():
+    rng = np.random.default_rng(12)
+    q, k, v, do = (x.astype(np.float32) for x in make(rng))
+    o, _ = oracle.sdpa_forward(q, k, v, 0.5, False)
+    o64, _ = oracle.sdpa_forward(q.astype(np.float64), k.astype(np.float64),
+                                 v.astype(np.float64), 0.5, False)
+    assert o.dtype == np.float64
+    np.testing.assert_array_equal(o, o64)
+
+
+# ----------------------------------------------------------------- library second opinion
+def test_matches_torch_cpu_float64():
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    rng = np.random.default_rng(13)
+    q, k, v, do = make(rng, B=2, Hq=4, Hkv=2, Lq=9, Lkv=9, D=8)
+    for causal in (False, True):
+        tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+        kr = tk.repeat_interleave(2, dim=1)
+        vr = tv.repeat_interleave(2, dim=1)
+        o = F.scaled_dot_product_attention(tq, kr, vr, is_causal=causal, scale=0.35)
+        o.backward(torch.tensor(do))
+        oo, _ = oracle.sdpa_forward(q, k, v, 0.35, causal)
+        dq, dk, dv = oracle.sdpa_backward(q, k, v, do, 0.35, causal)
+        np.testing.assert_allclose(oo, o.detach().numpy(), atol=1e-12)
+        np.testing.assert_allclose(dq, tq.grad.numpy(), atol=1e-12)
+        np.testing.assert_allclose(dk, tk.grad.numpy(), atol=1e-12)
+        np.testing.assert_allclose(dv, tv.grad.numpy(), atol=1e-12)
+
+
+# ----------------------------------------------------------------- pins have teeth
+PINS = [
+    test_rows_of_p_sum_to_one,
+    test_constant_v_gives_constant_output,
+    test_causal_first_row_attends_only_to_key0,
+    test_single_key,
+    test_zero_scale_is_uniform_attention,
+    test_gradient_sums,
+    test_key_shift_invariance,
+    test_gqa_equals_repeated_kv_heads,
+    test_mha_equals_independent_heads,
+]
+
+
+def _mutant(name):
+    """A copy of the oracle module with one plausible mistake planted (CPU only)."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("oracle_mutant_" + name, ref.__file__)
+    m = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(m)
+    if name in ("causal_diag_masked", "causal_off_by_one"):
+        shift = 0 if name == "causal_diag_masked" else 2
+
+        def _scores(q_rows, k, scale, is_causal, row_idx):
+            s = (q_rows @ k.T) * scale
+            if is_causal:
+                j = np.arange(k.shape[0])[None, :]
+                s = np.where(j >= np.asarray(row_idx)[:, None] + shift, -np.inf, s)
+            return s
+        m._scores = _scores
+    elif name == "lse_log2":
+        orig = m._softmax_rows
+
+        def _softmax_rows(s):
+            p, lse = orig(s)
+            return p, lse / math.log(2.0)
+        m._softmax_rows = _softmax_rows
+    elif name == "gqa_modulo":
+        def sdpa_forward(q, k, v, scale, is_causal, row_block=None):
+            B, Hq, Hkv, G = m._check(q, k, v)
+            o = np.empty(q.shape[:3] + (v.shape[3],))
+            lse = np.empty(q.shape[:3])
+            for b in range(B):
+                for h in range(Hq):
+                    g = h % Hkv
+                    o[b, h], lse[b, h] = m.head_forward(q[b, h], k[b, g], v[b, g], scale, is_causal)
+            return o, lse
+        m.sdpa_forward = sdpa_forward
+    elif name == "no_scale_in_dq":
+        orig = m.head_backward
+
+        def head_backward(q, k, v, dout, scale, is_causal, row_block=None):
+            dq, dk, dv = orig(q, k, v, dout, scale, is_causal, row_block)
+            return (dq / scale if scale else dq), dk, dv
+        m.head_backward = head_backward
+    elif name == "delta_dropped":
+        def head_backward(q, k, v, dout, scale, is_causal, row_block=None):
+            q, k, v, dout = (np.asarray(x, float) for x in (q, k, v, dout))
+            p, _ = m._softmax_rows(m._scores(q, k, scale, is_causal, np.arange(q.shape[0])))
+            ds = p * (dout @ v.T)
+            return scale * ds @ k, scale * ds.T @ q, p.T @ dout
+        m.head_backward = head_backward
+    elif name == "dk_transposed_operand":
+        orig = m.head_backward
+
+        def head_backward(q, k, v, dout, scale, is_causal, row_block=None):
+            dq, dk, dv = orig(q, k, v, dout, scale, is_causal, row_block)
+            return dq, dk[::-1].copy(), dv
+        m.head_backward = head_backward
+    else:
+        raise KeyError(name)
+    return m
+
+
+@pytest.mark.parametrize("name", ["causal_diag_masked", "causal_off_by_one", "lse_log2", "gqa_modulo",
+                                  "no_scale_in_dq", "delta_dropped", "dk_transposed_operand"])
+def test_planted_mistakes_are_caught(name):
+    mutant = _mutant(name)
+    failures = 0
+    checks = PINS + [lambda impl: [test_backward_matches_finite_differences(c, impl)
+                                   for c in FD_CASES]]
+    with np.errstate(all="ignore"):
+        for pin in checks:
+            try:
+                pin(impl=mutant)
+            except (AssertionError, FloatingPointError, ValueError):
+                failures += 1
+    assert failures > 0, f"no pin caught the planted mistake {name!r}"
