@@ -1,0 +1,488 @@
+#!/usr/bin/env python
+"""Benchmark: SDPA forward and forward+backward TFLOP/s on one GB300.
+
+Headline workload: bf16 GQA causal attention, B=2, Hq=32, Hkv=8, Lq=Lkv=4096, D=128,
+scale=1/sqrt(128), logsumexp cached by the forward for the backward; inputs iid N(0,1)
+from seed 3 (rank r adds 1000·r), rounded to bf16.  One step = sdpa_fwd + sdpa_bwd
+(forward, δ pre-pass, dK/dV kernel, dQ kernel) through the C ABI, inputs resident in HBM.
+FLOPs are algorithmic: 4·B·Hq·Lq·Lkv·D forward, 2.5× that backward, halved for causal.
+
+Timing: W untimed warm-up steps, then exactly K steps, each bracketed by CUDA events on
+the launching stream; L2 is flushed (a 256 MiB write) before every step, outside the
+step's events.  Per-kernel durations come from the library's own event brackets
+(sdpa_timing_*), recorded during the same timed steps.  SM clocks and throttle reasons
+are sampled with nvidia-smi during the timed region.  Also measured in the same run:
+the same step end to end from pinned host buffers (copies inside the timed region), the
+short-query (vector) path and the δ pre-pass against the HBM roofline, and the CPU
+oracle on a bounded sample of the workload (the reported CPU baseline).
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the path needs no
+exchange between GPUs); value = all ranks' FLOPs / the slowest rank's time; weak scaling.
+`--impl reference` times the CPU oracle instead (rank 0 only), each step one query head
+of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = dict(B=2, Hq=32, Hkv=8, Lq=4096, Lkv=4096, D=128)
+CAUSAL = True
+SEED = 3
+METRIC = "SDPA fwd and fwd+bwd TFLOP/s on 1 GB300 & % of dense bf16 tensor peak"
+WORKLOAD_NAME = "bf16 GQA causal SDPA fwd+bwd, B=2 Hq=32 Hkv=8 Lq=Lkv=4096 D=128"
+SHORT_QUERY = dict(B=4, Hq=32, Hkv=8, Lq=8, Lkv=8192, D=128)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def fwd_flops(B, Hq, Hkv, Lq, Lkv, D, causal):
+    f = 4.0 * B * Hq * Lq * Lkv * D
+    return f / 2 if causal else f
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest(name):
+    p = os.path.join(ROOT, "scaled_dot_product_flash_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """DRAM bytes per launch from a committed ncu capture, or None if absent or stale."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f).get(kernel)
+    if not d:
+        return None
+    if source_digest(d["source"]) != d["source_sha"]:
+        return None
+    return d["bytes_per_launch"]
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples, timestamped on the host."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(index), "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.perf_counter(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not inside:  # region shorter than the sampling period: nearest sample after t0
+            inside = [min(self.samples, key=lambda s: abs(s[0] - (t0 + t1) / 2))]
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for _, p in inside if num(p[1]) is not None]
+        mx = [num(p[2]) for _, p in inside if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for _, p in inside for n, v in zip(names, p[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside),
+                "power_w_max": max((num(p[3]) or 0.0) for _, p in inside)}
+
+
+def cpu_baseline_sample(q, k, v, do, scale, heads):
+    """Time the oracle (as it stands) on the first `heads` query heads of batch 0."""
+    import numpy as np  # noqa: F401
+    import oracle
+    from scaled_dot_product_flash_gb300.inputs import as_f64
+    G = q.shape[1] // k.shape[1]
+    t0 = time.perf_counter()
+    for h in range(heads):
+        g = h // G
+        qh, kg, vg, dh = (as_f64(t) for t in (q[0, h], k[0, g], v[0, g], do[0, h]))
+        oracle.head_forward(qh, kg, vg, scale, CAUSAL, row_block=1024)
+        oracle.head_backward(qh, kg, vg, dh, scale, CAUSAL, row_block=1024)
+    dt = time.perf_counter() - t0
+    W = WORKLOAD
+    flops = 3.5 * fwd_flops(1, heads, 1, W["Lq"], W["Lkv"], W["D"], CAUSAL)
+    return flops / dt / 1e12, dt
+
+
+def run_reference(args):
+    """CPU oracle arm: each step is one query head of the workload, fwd + bwd."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    import numpy as np
+    import oracle
+    from scaled_dot_product_flash_gb300.inputs import Shape, as_f64, draw
+    W = WORKLOAD
+    q, k, v, do = draw(Shape(**W), SEED, "bf16")
+    scale = 1.0 / math.sqrt(W["D"])
+    G = W["Hq"] // W["Hkv"]
+    times = []
+    for step in range(args.warmup + args.steps):
+        h = step % W["Hq"]
+        qh, kg, vg, dh = (as_f64(t) for t in (q[0, h], k[0, h // G], v[0, h // G], do[0, h]))
+        t0 = time.perf_counter()
+        oracle.head_forward(qh, kg, vg, scale, CAUSAL, row_block=1024)
+        oracle.head_backward(qh, kg, vg, dh, scale, CAUSAL, row_block=1024)
+        if step >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    del np
+    flops = 3.5 * fwd_flops(1, 1, 1, W["Lq"], W["Lkv"], W["D"], CAUSAL)
+    ms = 1e3 * sum(times) / len(times)
+    value = flops / (ms / 1e3) / 1e12
+    cores = len(os.sched_getaffinity(0))
+    sample = "one query head (Lq=Lkv=4096, D=128, causal) fwd+bwd per step, fp64 NumPy oracle"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAME, **W, "causal": CAUSAL, "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        args.steps = args.steps or 20
+        run_reference(args)
+        return
+    args.warmup = max(3, args.warmup)
+
+    import torch
+    import torch.distributed as dist
+    from scaled_dot_product_flash_gb300 import _lib, api
+    from scaled_dot_product_flash_gb300 import build as libbuild
+    from scaled_dot_product_flash_gb300.inputs import Shape, draw
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0:
+        libbuild.build()
+    if world > 1:
+        dist.barrier()
+    _lib.load()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    W = WORKLOAD
+    shape = Shape(**W)
+    scale = 1.0 / math.sqrt(W["D"])
+    q_h, k_h, v_h, do_h = draw(shape, SEED + 1000 * rank, "bf16")
+    q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+    out = torch.empty_like(q)
+    lse = torch.empty((W["B"], W["Hq"], W["Lq"]), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(max(16, api.workspace_bytes(q, k)), device=dev, dtype=torch.uint8)
+    flush = torch.empty(L2_FLUSH_BYTES, device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        api.attention_forward(q, k, v, scale=scale, is_causal=CAUSAL, out=out, lse=lse)
+        e_mid = torch.cuda.Event(enable_timing=True)
+        e_mid.record(stream)
+        api.attention_backward(q, k, v, out, do, lse, scale=scale, is_causal=CAUSAL,
+                               workspace=ws, dq=dq, dk=dk, dv=dv)
+        return e_mid
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    api.poll_status()
+    # Default step count: about two seconds of timed work.
+    if args.steps is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        args.steps = int(min(2000, max(10, 2000.0 / max(e0.elapsed_time(e1), 1e-3))))
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = []
+    _lib.sdpa_timing_reset()
+    _lib.sdpa_timing_enable(True)
+    barrier()
+    launches0 = _lib.sdpa_launch_count()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        mids.append(step())
+        ends[i].record(stream)
+    barrier()
+    t1 = time.perf_counter()
+    launches = _lib.sdpa_launch_count() - launches0
+    _lib.sdpa_timing_enable(False)
+    api.poll_status()
+    clocks = sampler.summary(t0, t1) if sampler else None
+    if sampler:
+        sampler.stop()
+
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    fwd_ms = [s.elapsed_time(m) for s, m in zip(starts, mids)]
+    tot = torch.tensor([sum(step_ms), sum(fwd_ms)], device=dev, dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(tot, op=dist.ReduceOp.MAX)
+    total_ms, total_fwd_ms = float(tot[0]), float(tot[1])
+    ms_per_step = total_ms / args.steps
+    F = fwd_flops(**W, causal=CAUSAL)
+    step_flops = 3.5 * F
+    value = world * step_flops * args.steps / (total_ms / 1e3) / 1e12
+    fwd_tflops = world * F * args.steps / (total_fwd_ms / 1e3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    bf16_peak = peaks["bf16_tflops"]
+    hbm_peak = peaks["hbm_gbs"]
+
+    # Per-kernel achieved rates from the library's event brackets (same timed steps).
+    kern = {}
+    work = {"fwd": F, "dkdv": 2.0 * F, "dq": 0.5 * F}
+    for name, kid in _lib.KERNELS.items():
+        ms, n = _lib.sdpa_timing_read(kid)
+        if n == 0:
+            continue
+        avg = ms / n
+        entry = {"launches": n, "avg_ms": avg, "share": None}
+        if name in work:
+            entry["tflops"] = work[name] / (avg / 1e3) / 1e12
+        if name == "delta":
+            rows = W["B"] * W["Hq"] * W["Lq"]
+            entry["gbs"] = (2 * rows * W["D"] * 2 + 4 * rows) / (avg / 1e3) / 1e9
+        kern[name] = entry
+    tot_k = sum(e["avg_ms"] * e["launches"] for e in kern.values())
+    for e in kern.values():
+        e["share"] = e["avg_ms"] * e["launches"] / tot_k if tot_k else None
+    dom = max((n for n in kern if n in work), key=lambda n: kern[n]["avg_ms"] * kern[n]["launches"])
+    path_is_tensor = _tensor_available()
+    dom_src = {"fwd": "tc_fwd.cu", "dkdv": "tc_bwd.cu", "dq": "tc_bwd.cu"}[dom] \
+        if path_is_tensor else "simt_kernels.cu"
+    traffic = ncu_traffic(f"{dom}:{dom_src}")
+    if path_is_tensor:
+        roof = {"bound": "tensor", "achieved": kern[dom]["tflops"], "peak": bf16_peak,
+                "unit": "TFLOP/s", "frac": kern[dom]["tflops"] / bf16_peak, "traffic": traffic,
+                "kernel": dom, "peak_source": f"{peak_src} (burst bf16)"}
+    else:
+        alu_peak = alu_peak_tflops(clocks)
+        roof = {"bound": "alu", "achieved": kern[dom]["tflops"], "peak": alu_peak,
+                "unit": "TFLOP/s", "frac": kern[dom]["tflops"] / alu_peak, "traffic": traffic,
+                "kernel": dom, "peak_source": "152 SMs x 128 fp32 FMA/clk x 2 x 2.07 GHz"}
+
+    # End to end through the public API from pinned host buffers.
+    e2e = run_e2e(torch, api, dev, stream, (q_h, k_h, v_h, do_h), scale, args.steps, step_flops,
+                  world, barrier, dist if world > 1 else None)
+
+    extras = {}
+    if rank == 0:
+        extras["short_query"] = run_short_query(torch, api, _lib, dev, stream, hbm_peak)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        heads = 16
+        val, dt = cpu_baseline_sample(q_h, k_h, v_h, do_h, scale, heads)
+        cpu = {"value": val, "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
+               "kind": "oracle",
+               "sample": f"first {heads} query heads of batch 0, fwd+bwd, fp64 NumPy, {dt:.1f} s"}
+
+    if world > 1:
+        dist.barrier()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD_NAME, **W, "causal": CAUSAL,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "flushed before every step (256 MiB write, outside step events)"},
+            "frac_of_bf16_peak": value / bf16_peak,
+            "fwd": {"tflops": fwd_tflops, "ms": total_fwd_ms / args.steps,
+                    "frac_of_bf16_peak": fwd_tflops / bf16_peak},
+            "roofline": roof,
+            "kernels": kern,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "clocks": clocks,
+            "gpu_launches": launches,
+            "peaks": {"source": peak_src, "bf16_tflops": bf16_peak, "hbm_gbs": hbm_peak},
+            **extras,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def _tensor_available():
+    """True when the tiled forward of the headline workload runs on the tensor-core path."""
+    import torch
+    from scaled_dot_product_flash_gb300 import _lib, api
+    q = torch.zeros(1, 1, 128, 128, device="cuda", dtype=torch.bfloat16)
+    try:
+        with api.force_path(_lib.PATH_TENSOR):
+            api.attention_forward(q, q, q, need_lse=False)
+        return True
+    except _lib.SdpaError:
+        return False
+
+
+def alu_peak_tflops(clocks):
+    return 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def run_e2e(torch, api, dev, stream, host_inputs, scale, steps, step_flops, world, barrier, dist):
+    """Same step from pinned host memory: H2D of q, k, v, dO; fwd + bwd; D2H of out, lse,
+    dq, dk, dv; all inside the timed region."""
+    pin = [t.pin_memory() for t in host_inputs]
+    q, k, v, do = (torch.empty_like(t, device=dev) for t in pin)
+    W = WORKLOAD
+    out_h = torch.empty_like(pin[0]).pin_memory()
+    lse_h = torch.empty((W["B"], W["Hq"], W["Lq"]), dtype=torch.float32).pin_memory()
+    dq_h = torch.empty_like(pin[0]).pin_memory()
+    dk_h = torch.empty_like(pin[1]).pin_memory()
+    dv_h = torch.empty_like(pin[2]).pin_memory()
+    ws = torch.empty(max(16, api.workspace_bytes(q, k)), device=dev, dtype=torch.uint8)
+
+    def one():
+        for d, h in zip((q, k, v, do), pin):
+            d.copy_(h, non_blocking=True)
+        out, lse = api.attention_forward(q, k, v, scale=scale, is_causal=CAUSAL)
+        dq, dk, dv = api.attention_backward(q, k, v, out, do, lse, scale=scale,
+                                            is_causal=CAUSAL, workspace=ws)
+        for h, d in ((out_h, out), (lse_h, lse), (dq_h, dq), (dk_h, dk), (dv_h, dv)):
+            h.copy_(d, non_blocking=True)
+
+    n = max(3, min(steps, 20))
+    for _ in range(3):
+        one()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        one()
+    e1.record(stream)
+    barrier()
+    ms = e0.elapsed_time(e1)
+    t = torch.tensor([ms], device=dev, dtype=torch.float64)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms = float(t[0])
+    h2d = sum(t.numel() * t.element_size() for t in pin)
+    d2h = sum(t.numel() * t.element_size() for t in (out_h, lse_h, dq_h, dk_h, dv_h))
+    return {"value": world * step_flops * n / (ms / 1e3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / n,
+            "steps": n}
+
+
+def run_short_query(torch, api, _lib, dev, stream, hbm_peak):
+    """Short-query (vector) path, Lq=8, Lkv=8192, bf16: HBM GB/s of fwd and bwd."""
+    from scaled_dot_product_flash_gb300.inputs import Shape, draw
+    S = SHORT_QUERY
+    q, k, v, do = (t.to(dev) for t in draw(Shape(**S), 4, "bf16"))
+    scale = 1.0 / math.sqrt(S["D"])
+    flush = torch.empty(L2_FLUSH_BYTES, device=dev, dtype=torch.uint8)
+    out, lse = api.attention_forward(q, k, v, scale=scale)
+    dq, dk, dv = api.attention_backward(q, k, v, out, do, lse, scale=scale)
+    fwd_t, bwd_t = [], []
+    for i in range(23):
+        flush.zero_()
+        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a.record(stream)
+        api.attention_forward(q, k, v, scale=scale, out=out, lse=lse)
+        b.record(stream)
+        api.attention_backward(q, k, v, out, do, lse, scale=scale, dq=dq, dk=dk, dv=dv)
+        c.record(stream)
+        if i >= 3:
+            fwd_t.append((a, b))
+            bwd_t.append((b, c))
+    torch.cuda.synchronize()
+    api.poll_status()
+    fms = statistics.median(a.elapsed_time(b) for a, b in fwd_t)
+    bms = statistics.median(a.elapsed_time(b) for a, b in bwd_t)
+    kv = S["B"] * S["Hkv"] * S["Lkv"] * S["D"] * 2
+    qb = S["B"] * S["Hq"] * S["Lq"] * S["D"] * 2
+    rows = S["B"] * S["Hq"] * S["Lq"] * 4
+    fwd_bytes = 2 * kv + 2 * qb + rows
+    bwd_bytes = 4 * kv + 4 * qb + rows
+    F = fwd_flops(**S, causal=False)
+    return {"workload": "bf16 short-query B=4 Hq=32 Hkv=8 Lq=8 Lkv=8192 D=128 non-causal",
+            "fwd_ms": fms, "bwd_ms": bms,
+            "fwd_gbs": fwd_bytes / (fms / 1e3) / 1e9, "bwd_gbs": bwd_bytes / (bms / 1e3) / 1e9,
+            "fwd_frac_hbm": fwd_bytes / (fms / 1e3) / 1e9 / hbm_peak,
+            "bwd_frac_hbm": bwd_bytes / (bms / 1e3) / 1e9 / hbm_peak,
+            "fwd_tflops": F / (fms / 1e3) / 1e12, "bwd_tflops": 2.5 * F / (bms / 1e3) / 1e12,
+            "algorithmic_bytes": {"fwd": fwd_bytes, "bwd": bwd_bytes}}
+
+
+if __name__ == "__main__":
+    main()

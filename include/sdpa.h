@@ -1,0 +1,156 @@
+/*
+ * sdpa.h — C ABI of the GB300 fused scaled-dot-product attention library (libsdpa.so).
+ *
+ * The operation.  For query head h of batch b, with G = Hq / Hkv and KV head g = h / G:
+ *     S   = scale · Q[b,h] · K[b,g]ᵀ                 (Lq × Lkv scores)
+ *     S_ij = −∞ where is_causal and j > i            (top-left aligned causal mask)
+ *     P   = softmax of each row of S
+ *     O[b,h]   = P · V[b,g]
+ *     lse[b,h,i] = ln Σ_j exp(S_ij)                  (natural log, scale included)
+ * This is the definition in the NumPy "perform" sketch of the PyTensor issue "PERF: detect
+ * scaled-dot-product-attention pattern and lower to mx.fast.scaled_dot_product_attention"
+ * (section "Proposed change"), with the causal flag of F.scaled_dot_product_attention
+ * ("mps-flash-sdpa 0.1.0", section "Quick Start") and grouped KV heads ("[Metal] Add Flash
+ * Attention VJP for training", section "Key Features").  The logsumexp is the forward's
+ * second output that the backward needs ("MPS scaled_dot_product_attention (SDPA)", section
+ * "Problem - Unused second output tensor").  The backward is the vector-Jacobian product:
+ *     dV[b,g] = Σ_{h in group g} Pᵀ·dO[b,h]
+ *     dP = dO·Vᵀ,  δ_i = Σ_d dO_id·O_id,  dS = P ∘ (dP − δ)
+ *     dQ[b,h] = scale · dS·K[b,g],   dK[b,g] = scale · Σ_{h in group g} dSᵀ·Q[b,h]
+ * recomputing P from the cached logsumexp ("[Metal] Add Flash Attention VJP for training",
+ * sections "Implementation Notes" and "Limitations": the backward requires the forward's
+ * logsumexp).
+ *
+ * Conventions shared by every entry point:
+ *  - Layout: every tensor is a dense, contiguous row-major [B, H, L, D] array of `dtype`
+ *    (H = Hq for q, out, dout, dq; H = Hkv for k, v, dk, dv).  lse is a dense fp32
+ *    [B, Hq, Lq] array.  All pointers are DEVICE pointers (or managed memory) on the
+ *    current CUDA device, and must be 16-byte aligned.
+ *  - Ownership: the caller allocates and owns every buffer.  The library keeps only a
+ *    static device error word and host-side counters.
+ *  - Execution: every call enqueues work on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and returns without synchronising, except sdpa_poll_status.
+ *  - Outputs are fully overwritten; they need no zeroing.  Inputs must not overlap
+ *    outputs.
+ *  - Errors: argument errors are detected on the host before anything is launched and
+ *    return SDPA_ERR_INVALID_ARG or SDPA_ERR_UNSUPPORTED; a failed launch returns
+ *    SDPA_ERR_CUDA.  Kernels never trap: a wait that runs out of its iteration limit sets
+ *    the device error word and the kernel returns; sdpa_poll_status reports it.
+ *  - Supported: dtype in {SDPA_F32, SDPA_F16, SDPA_BF16}; D in {32, 64, 96, 128};
+ *    B, Hq, Hkv, Lq, Lkv >= 1; Hq % Hkv == 0; Hq, B <= 65535; scale finite (0 allowed).
+ */
+#ifndef SDPA_GB300_H
+#define SDPA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SDPA_F32 = 0,
+  SDPA_F16 = 1,
+  SDPA_BF16 = 2
+} sdpa_dtype_t;
+
+typedef enum {
+  SDPA_OK = 0,
+  SDPA_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad size, overlap, bad scale */
+  SDPA_ERR_UNSUPPORTED = 2,    /* valid but unsupported dtype / head dim / shape */
+  SDPA_ERR_CUDA = 3,           /* a CUDA runtime call or kernel launch failed */
+  SDPA_ERR_DEVICE_TIMEOUT = 4, /* a kernel's bounded wait ran out (reported by poll) */
+  SDPA_ERR_WORKSPACE = 5       /* workspace missing or smaller than required */
+} sdpa_status_t;
+
+/*
+ * Forward.  Computes out = softmax(scale·q·kᵀ [causal]) · v and, when lse != NULL, the
+ * per-row logsumexp.  Pass lse = NULL when no gradient will be taken: it is then neither
+ * computed nor written (the "second output only when needed" of "MPS
+ * scaled_dot_product_attention (SDPA)", section "Problem - Unused second output tensor").
+ *   q   [B,Hq,Lq,D]  dtype, read        k, v [B,Hkv,Lkv,D] dtype, read
+ *   out [B,Hq,Lq,D]  dtype, written     lse  [B,Hq,Lq] fp32, written (nullable)
+ * Needs no workspace.  Returns an sdpa_status_t.
+ */
+int sdpa_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+             int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale, int is_causal,
+             int dtype, void* stream);
+
+/*
+ * Bytes of device workspace sdpa_bwd needs for these sizes (the fp32 δ = rowsum(dO∘O)
+ * vector, [B,Hq,Lq], rounded up to 256 bytes).  Returns 0 for invalid arguments.
+ */
+size_t sdpa_bwd_workspace_size(int B, int Hq, int Hkv, int Lq, int Lkv, int D, int dtype);
+
+/*
+ * Backward.  Given the forward's inputs, its output `out` and logsumexp `lse` (both as
+ * written by sdpa_fwd with the same arguments) and the output gradient `dout`, writes
+ * dq, dk, dv.  dk and dv sum over the Hq/Hkv query heads that share each KV head; every
+ * KV row is owned by one thread block, so no atomics are used and results are bitwise
+ * reproducible run to run.
+ *   q, out, dout, dq [B,Hq,Lq,D]  dtype      k, v, dk, dv [B,Hkv,Lkv,D]  dtype
+ *   lse [B,Hq,Lq] fp32 (required)
+ *   workspace: device buffer of at least sdpa_bwd_workspace_size(...) bytes, 16-byte
+ *   aligned, owned by the caller, contents irrelevant on entry; it must stay untouched
+ *   until the work enqueued by this call has finished.
+ * Returns an sdpa_status_t (SDPA_ERR_WORKSPACE if the workspace is NULL or too small).
+ */
+int sdpa_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv,
+             int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale, int is_causal,
+             int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word that kernels set
+ * when a bounded wait gives up.  Returns SDPA_OK, SDPA_ERR_DEVICE_TIMEOUT, or
+ * SDPA_ERR_CUDA if the synchronisation itself reported an error.
+ */
+int sdpa_poll_status(void* stream);
+
+/* A static, human-readable name for a status code. */
+const char* sdpa_status_string(int status);
+
+/*
+ * Kernel family selection, for tests and measurements.  SDPA_PATH_AUTO (the default)
+ * picks by shape and dtype: the vector path when Lq <= 8 and (Hq/Hkv)·Lq <= 32, else the
+ * tensor-core tiled path for fp16/bf16 with D in {64, 128}, else the CUDA-core tiled path.
+ * A forced path that cannot serve a call makes that call return SDPA_ERR_UNSUPPORTED.
+ * Process-wide setting; not thread-safe against concurrent calls.
+ */
+typedef enum {
+  SDPA_PATH_AUTO = 0,
+  SDPA_PATH_TENSOR = 1,  /* TMA + tcgen05 tiled kernels (fp16/bf16, D in {64,128}) */
+  SDPA_PATH_SIMT = 2,    /* CUDA-core (FFMA) tiled kernels, every dtype and D */
+  SDPA_PATH_VECTOR = 3   /* short-query kernels (Lq <= 8, (Hq/Hkv)·Lq <= 32) */
+} sdpa_path_t;
+int sdpa_set_path(int path); /* SDPA_OK, or SDPA_ERR_INVALID_ARG for an unknown path */
+
+/* Number of kernels this library has launched since load (host-side counter). */
+uint64_t sdpa_launch_count(void);
+
+/*
+ * Per-kernel device timing, for measurements.  While enabled, every kernel the library
+ * launches is bracketed by two CUDA events recorded on the launch's stream;
+ * sdpa_timing_read waits for the recorded events, adds their elapsed times into
+ * per-kernel totals, and returns the total milliseconds and the number of timed launches
+ * of one kernel kind since the last sdpa_timing_reset.  Process-wide, guarded by a mutex.
+ * sdpa_timing_enable/read return an sdpa_status_t.
+ */
+typedef enum {
+  SDPA_KERNEL_FWD = 0,      /* tiled forward (tensor-core or CUDA-core) */
+  SDPA_KERNEL_DELTA = 1,    /* δ = rowsum(dO∘O) pre-pass */
+  SDPA_KERNEL_DQ = 2,       /* tiled dQ kernel */
+  SDPA_KERNEL_DKDV = 3,     /* tiled dK/dV kernel */
+  SDPA_KERNEL_VEC_FWD = 4,  /* short-query forward */
+  SDPA_KERNEL_VEC_BWD = 5,  /* short-query backward */
+  SDPA_KERNEL_COUNT = 6
+} sdpa_kernel_t;
+int sdpa_timing_enable(int on);
+int sdpa_timing_read(int kernel, double* total_ms, uint64_t* launches);
+void sdpa_timing_reset(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SDPA_GB300_H */

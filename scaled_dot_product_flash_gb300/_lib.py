@@ -1,0 +1,123 @@
+"""ctypes binding of libsdpa.so: the C entry points under the same names.
+
+Argument marshalling only.  Every step of the computation runs in the library's CUDA
+kernels; there is no fallback of any kind.  If the library has not been built, loading
+fails with an error that says how to build it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsdpa.so")
+
+OK = 0
+STATUS_NAMES = {
+    0: "SDPA_OK",
+    1: "SDPA_ERR_INVALID_ARG",
+    2: "SDPA_ERR_UNSUPPORTED",
+    3: "SDPA_ERR_CUDA",
+    4: "SDPA_ERR_DEVICE_TIMEOUT",
+    5: "SDPA_ERR_WORKSPACE",
+}
+PATH_AUTO, PATH_TENSOR, PATH_SIMT, PATH_VECTOR = 0, 1, 2, 3
+
+# Every symbol include/sdpa.h declares, with its ctypes signature.
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "sdpa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
+    "sdpa_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i]),
+    "sdpa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                      _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp, _sz, _vp]),
+    "sdpa_poll_status": (_i, [_vp]),
+    "sdpa_status_string": (ctypes.c_char_p, [_i]),
+    "sdpa_set_path": (_i, [_i]),
+    "sdpa_launch_count": (ctypes.c_uint64, []),
+    "sdpa_timing_enable": (_i, [_i]),
+    "sdpa_timing_read": (_i, [_i, ctypes.POINTER(ctypes.c_double),
+                              ctypes.POINTER(ctypes.c_uint64)]),
+    "sdpa_timing_reset": (None, []),
+}
+KERNELS = {"fwd": 0, "delta": 1, "dq": 2, "dkdv": 3, "vec_fwd": 4, "vec_bwd": 5}
+
+_lib = None
+
+
+class SdpaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} "
+                         f"({status_string(status) if _lib else ''})")
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libsdpa.so (once) and declare its signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} is missing: build it first with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` "
+            "or `python scaled_dot_product_flash_gb300/build.py`")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def sdpa_fwd(q, k, v, out, lse, B, Hq, Hkv, Lq, Lkv, D, scale, is_causal, dtype, stream):
+    return load().sdpa_fwd(q, k, v, out, lse, B, Hq, Hkv, Lq, Lkv, D, scale, is_causal,
+                           dtype, stream)
+
+
+def sdpa_bwd_workspace_size(B, Hq, Hkv, Lq, Lkv, D, dtype):
+    return load().sdpa_bwd_workspace_size(B, Hq, Hkv, Lq, Lkv, D, dtype)
+
+
+def sdpa_bwd(q, k, v, out, dout, lse, dq, dk, dv, B, Hq, Hkv, Lq, Lkv, D, scale, is_causal,
+             dtype, workspace, workspace_bytes, stream):
+    return load().sdpa_bwd(q, k, v, out, dout, lse, dq, dk, dv, B, Hq, Hkv, Lq, Lkv, D, scale,
+                           is_causal, dtype, workspace, workspace_bytes, stream)
+
+
+def sdpa_poll_status(stream):
+    return load().sdpa_poll_status(stream)
+
+
+def status_string(status: int) -> str:
+    return load().sdpa_status_string(status).decode()
+
+
+def sdpa_status_string(status: int) -> str:
+    return status_string(status)
+
+
+def sdpa_set_path(path: int) -> int:
+    return load().sdpa_set_path(path)
+
+
+def sdpa_launch_count() -> int:
+    return int(load().sdpa_launch_count())
+
+
+def sdpa_timing_enable(on: bool) -> int:
+    return load().sdpa_timing_enable(int(bool(on)))
+
+
+def sdpa_timing_read(kernel: int):
+    """(total_ms, launches) of one kernel kind since the last reset."""
+    ms = ctypes.c_double(0.0)
+    n = ctypes.c_uint64(0)
+    st = load().sdpa_timing_read(kernel, ctypes.byref(ms), ctypes.byref(n))
+    if st != OK:
+        raise SdpaError(st, "sdpa_timing_read")
+    return ms.value, int(n.value)
+
+
+def sdpa_timing_reset() -> None:
+    load().sdpa_timing_reset()

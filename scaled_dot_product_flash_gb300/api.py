@@ -1,0 +1,118 @@
+"""Tensor-level convenience calls over the C ABI (marshalling only).
+
+PyTorch is used here for device memory and streams: outputs are allocated with torch,
+their raw device pointers and the current stream's handle are passed to libsdpa.so, and
+a non-OK status is raised as ``SdpaError``.  All arithmetic runs in the library.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _lib
+
+DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+
+
+def _check(name, t, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous [B, H, L, D]")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dims(q, k):
+    B, Hq, Lq, D = q.shape
+    Bk, Hkv, Lkv, Dk = k.shape
+    if Bk != B or Dk != D:
+        raise ValueError("q and k disagree in batch or head dim")
+    return B, Hq, Hkv, Lq, Lkv, D
+
+
+def attention_forward(q, k, v, scale=None, is_causal=False, need_lse=True, out=None,
+                      lse=None, stream=None):
+    """out = softmax(scale·q·kᵀ [causal]) · v; also the fp32 logsumexp when need_lse.
+
+    q [B,Hq,Lq,D], k/v [B,Hkv,Lkv,D] CUDA tensors of one dtype (fp32/fp16/bf16).
+    Returns (out, lse or None).
+    """
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check(n, t, q.dtype)
+    B, Hq, Hkv, Lq, Lkv, D = _dims(q, k)
+    if v.shape != k.shape:
+        raise ValueError("k and v shapes differ")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if need_lse and lse is None:
+        lse = torch.empty((B, Hq, Lq), device=q.device, dtype=torch.float32)
+    if not need_lse:
+        lse = None
+    st = _lib.sdpa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                       lse.data_ptr() if lse is not None else None,
+                       B, Hq, Hkv, Lq, Lkv, D, scale, int(bool(is_causal)),
+                       DTYPE_CODE[q.dtype], _stream(stream))
+    if st != _lib.OK:
+        raise _lib.SdpaError(st, "sdpa_fwd")
+    return out, lse
+
+
+def workspace_bytes(q, k):
+    B, Hq, Hkv, Lq, Lkv, D = _dims(q, k)
+    return _lib.sdpa_bwd_workspace_size(B, Hq, Hkv, Lq, Lkv, D, DTYPE_CODE[q.dtype])
+
+
+def attention_backward(q, k, v, out, dout, lse, scale=None, is_causal=False, workspace=None,
+                       dq=None, dk=None, dv=None, stream=None):
+    """(dq, dk, dv) of the forward, from its output ``out`` and logsumexp ``lse``."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
+        _check(n, t, q.dtype)
+    _check("lse", lse, torch.float32)
+    B, Hq, Hkv, Lq, Lkv, D = _dims(q, k)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = workspace_bytes(q, k)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    st = _lib.sdpa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                       dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                       dv.data_ptr(), B, Hq, Hkv, Lq, Lkv, D, scale, int(bool(is_causal)),
+                       DTYPE_CODE[q.dtype], workspace.data_ptr(), workspace.numel(),
+                       _stream(stream))
+    if st != _lib.OK:
+        raise _lib.SdpaError(st, "sdpa_bwd")
+    return dq, dk, dv
+
+
+def poll_status(stream=None):
+    """Synchronise the stream; raise if a kernel reported a timed-out wait."""
+    st = _lib.sdpa_poll_status(_stream(stream))
+    if st != _lib.OK:
+        raise _lib.SdpaError(st, "sdpa_poll_status")
+
+
+class force_path:
+    """Context manager selecting one kernel family (tests and measurements)."""
+
+    def __init__(self, path: int):
+        self.path = path
+
+    def __enter__(self):
+        st = _lib.sdpa_set_path(self.path)
+        if st != _lib.OK:
+            raise _lib.SdpaError(st, "sdpa_set_path")
+        return self
+
+    def __exit__(self, *exc):
+        _lib.sdpa_set_path(_lib.PATH_AUTO)
+        return False

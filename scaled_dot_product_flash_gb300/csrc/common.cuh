@@ -1,0 +1,80 @@
+// Shared device helpers: element conversion, launch parameters, error reporting.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace sdpa {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Error codes written into the device error word (low 16 bits: code, high: kernel id).
+enum DeviceError : unsigned {
+  kDevErrNone = 0,
+  kDevErrTimeout = 1,
+};
+
+// Kernel ids for the error word.
+enum KernelId : unsigned {
+  kKidSimtFwd = 1,
+  kKidSimtDq = 2,
+  kKidSimtDkdv = 3,
+  kKidDelta = 4,
+  kKidVecFwd = 5,
+  kKidVecBwd = 6,
+  kKidTcFwd = 7,
+  kKidTcDq = 8,
+  kKidTcDkdv = 9,
+};
+
+__device__ __forceinline__ void report_error(unsigned* err, unsigned code, unsigned kid) {
+  if (err) atomicCAS(err, 0u, (kid << 16) | code);
+}
+
+// Element <-> fp32 conversion (round-to-nearest-even on the way down).
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static __device__ __forceinline__ float to_f(float x) { return x; }
+  static __device__ __forceinline__ float from_f(float x) { return x; }
+};
+template <> struct Elem<__half> {
+  static __device__ __forceinline__ float to_f(__half x) { return __half2float(x); }
+  static __device__ __forceinline__ __half from_f(float x) { return __float2half_rn(x); }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+  static __device__ __forceinline__ __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+};
+
+// Sizes and pointers of one call, passed by value to every kernel.
+struct Problem {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;     // forward output (backward input)
+  const void* dout;
+  void* out;         // forward output
+  float* lse;        // natural-log logsumexp [B,Hq,Lq] (nullable in the forward)
+  void* dq;
+  void* dk;
+  void* dv;
+  float* delta;      // δ = rowsum(dO∘O) [B,Hq,Lq]
+  int B, Hq, Hkv, Lq, Lkv, D;
+  int G;             // Hq / Hkv
+  float scale;
+  float scale_log2;  // scale · log2(e)
+  int causal;
+  unsigned* err;     // device error word
+};
+
+__host__ __device__ __forceinline__ int64_t q_row(const Problem& p, int b, int h, int i) {
+  return ((int64_t)b * p.Hq + h) * p.Lq + i;
+}
+__host__ __device__ __forceinline__ int64_t kv_row(const Problem& p, int b, int g, int j) {
+  return ((int64_t)b * p.Hkv + g) * p.Lkv + j;
+}
+
+}  // namespace sdpa

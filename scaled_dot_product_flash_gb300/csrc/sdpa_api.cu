@@ -1,0 +1,329 @@
+// C ABI of libsdpa.so: argument validation, kernel-family choice and launches.
+// The operation and every convention are documented in include/sdpa.h.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "launch.h"
+#include "../../include/sdpa.h"
+
+namespace sdpa {
+namespace {
+
+__device__ unsigned g_device_error = 0;
+
+std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_path{SDPA_PATH_AUTO};
+
+constexpr int kMaxDevices = 64;
+unsigned* g_err_ptr[kMaxDevices] = {};
+
+// Device address of the error word on the current device (looked up once per device).
+int error_word(unsigned** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SDPA_ERR_CUDA;
+  if (!g_err_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_device_error) != cudaSuccess) return SDPA_ERR_CUDA;
+    g_err_ptr[dev] = static_cast<unsigned*>(ptr);
+  }
+  *out = g_err_ptr[dev];
+  return SDPA_OK;
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+size_t elem_size(int dtype) { return dtype == SDPA_F32 ? 4 : 2; }
+
+// Checks sizes, dtype and scale; fills the size fields of *p.
+int check_sizes(int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale, int dtype,
+                Problem* p) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lkv < 1 || D < 1) return SDPA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return SDPA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return SDPA_ERR_INVALID_ARG;
+  if (dtype != SDPA_F32 && dtype != SDPA_F16 && dtype != SDPA_BF16) return SDPA_ERR_UNSUPPORTED;
+  if (D != 32 && D != 64 && D != 96 && D != 128) return SDPA_ERR_UNSUPPORTED;
+  if (B > 65535 || Hq > 65535) return SDPA_ERR_UNSUPPORTED;
+  // Keep every element index comfortably inside int64 (and far above any real HBM size).
+  const double qe = (double)B * Hq * Lq * D, ke = (double)B * Hkv * Lkv * D;
+  if (qe > 4.0e12 || ke > 4.0e12) return SDPA_ERR_UNSUPPORTED;
+  std::memset(p, 0, sizeof(*p));
+  p->B = B;
+  p->Hq = Hq;
+  p->Hkv = Hkv;
+  p->Lq = Lq;
+  p->Lkv = Lkv;
+  p->D = D;
+  p->G = Hq / Hkv;
+  p->scale = scale;
+  p->scale_log2 = scale * kLog2e;
+  return SDPA_OK;
+}
+
+enum class Family { kTensor, kSimt, kVector };
+
+int choose(const Problem& p, int dtype, Family* f) {
+  const int forced = g_path.load();
+  switch (forced) {
+    case SDPA_PATH_TENSOR:
+      if (!tensor_supported(p, dtype)) return SDPA_ERR_UNSUPPORTED;
+      *f = Family::kTensor;
+      return SDPA_OK;
+    case SDPA_PATH_SIMT:
+      *f = Family::kSimt;
+      return SDPA_OK;
+    case SDPA_PATH_VECTOR:
+      if (!vector_supported(p, dtype)) return SDPA_ERR_UNSUPPORTED;
+      *f = Family::kVector;
+      return SDPA_OK;
+    default:
+      break;
+  }
+  if (vector_supported(p, dtype)) *f = Family::kVector;
+  else if (tensor_supported(p, dtype)) *f = Family::kTensor;
+  else *f = Family::kSimt;
+  return SDPA_OK;
+}
+
+// ---- optional per-kernel device timing (CUDA events bracketing each launch) ----
+struct EventPair {
+  cudaEvent_t start = nullptr, stop = nullptr;
+};
+struct PendingTiming {
+  int kernel;
+  EventPair ev;
+};
+std::mutex g_timing_mu;
+std::atomic<bool> g_timing_on{false};
+std::vector<EventPair> g_event_pool;
+std::vector<PendingTiming> g_pending;
+double g_total_ms[SDPA_KERNEL_COUNT] = {};
+uint64_t g_timed_launches[SDPA_KERNEL_COUNT] = {};
+
+bool take_pair(EventPair* ev) {
+  std::lock_guard<std::mutex> lock(g_timing_mu);
+  if (!g_event_pool.empty()) {
+    *ev = g_event_pool.back();
+    g_event_pool.pop_back();
+    return true;
+  }
+  if (cudaEventCreate(&ev->start) != cudaSuccess) return false;
+  if (cudaEventCreate(&ev->stop) != cudaSuccess) {
+    cudaEventDestroy(ev->start);
+    return false;
+  }
+  return true;
+}
+
+// Launches one kernel through `fn`, counting it and, when timing is on, bracketing it with
+// events on its stream.
+template <typename Fn>
+cudaError_t launch_one(int kernel, cudaStream_t s, Fn fn) {
+  EventPair ev;
+  const bool timed = g_timing_on.load() && take_pair(&ev);
+  if (timed) cudaEventRecord(ev.start, s);
+  cudaError_t e = fn();
+  if (e == cudaSuccess) g_launches.fetch_add(1);
+  if (timed) {
+    cudaEventRecord(ev.stop, s);
+    std::lock_guard<std::mutex> lock(g_timing_mu);
+    if (e == cudaSuccess) g_pending.push_back({kernel, ev});
+    else g_event_pool.push_back(ev);
+  }
+  return e;
+}
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA; }
+
+}  // namespace
+}  // namespace sdpa
+
+using namespace sdpa;
+
+extern "C" int sdpa_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                        int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale,
+                        int is_causal, int dtype, void* stream) {
+  Problem p;
+  int st = check_sizes(B, Hq, Hkv, Lq, Lkv, D, scale, dtype, &p);
+  if (st != SDPA_OK) return st;
+  if (!q || !k || !v || !out) return SDPA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return SDPA_ERR_INVALID_ARG;
+  const size_t es = elem_size(dtype);
+  const size_t qb = (size_t)B * Hq * Lq * D * es, kb = (size_t)B * Hkv * Lkv * D * es;
+  const size_t lb = lse ? (size_t)B * Hq * Lq * sizeof(float) : 0;
+  if (overlaps(out, qb, q, qb) || overlaps(out, qb, k, kb) || overlaps(out, qb, v, kb) ||
+      overlaps(lse, lb, q, qb) || overlaps(lse, lb, k, kb) || overlaps(lse, lb, v, kb) ||
+      overlaps(lse, lb, out, qb))
+    return SDPA_ERR_INVALID_ARG;
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.lse = lse;
+  p.causal = is_causal ? 1 : 0;
+  Family f;
+  if ((st = choose(p, dtype, &f)) != SDPA_OK) return st;
+  if ((st = error_word(&p.err)) != SDPA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  switch (f) {
+    case Family::kVector:
+      e = launch_one(SDPA_KERNEL_VEC_FWD, s, [&] { return launch_vector_fwd(p, dtype, s); });
+      break;
+    case Family::kTensor:
+      e = launch_one(SDPA_KERNEL_FWD, s, [&] { return launch_tc_fwd(p, dtype, s); });
+      break;
+    default:
+      e = launch_one(SDPA_KERNEL_FWD, s, [&] { return launch_simt_fwd(p, dtype, s); });
+      break;
+  }
+  return status_of(e);
+}
+
+extern "C" size_t sdpa_bwd_workspace_size(int B, int Hq, int Hkv, int Lq, int Lkv, int D,
+                                          int dtype) {
+  Problem p;
+  if (check_sizes(B, Hq, Hkv, Lq, Lkv, D, 1.0f, dtype, &p) != SDPA_OK) return 0;
+  const size_t bytes = (size_t)B * Hq * Lq * sizeof(float);
+  return (bytes + 255) / 256 * 256;
+}
+
+extern "C" int sdpa_bwd(const void* q, const void* k, const void* v, const void* out,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                        int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale,
+                        int is_causal, int dtype, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  Problem p;
+  int st = check_sizes(B, Hq, Hkv, Lq, Lkv, D, scale, dtype, &p);
+  if (st != SDPA_OK) return st;
+  if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return SDPA_ERR_INVALID_ARG;
+  const void* all[] = {q, k, v, out, dout, lse, dq, dk, dv};
+  for (const void* ptr : all)
+    if (!aligned16(ptr)) return SDPA_ERR_INVALID_ARG;
+  const size_t need = sdpa_bwd_workspace_size(B, Hq, Hkv, Lq, Lkv, D, dtype);
+  if (!workspace || workspace_bytes < need) return SDPA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return SDPA_ERR_INVALID_ARG;
+  const size_t es = elem_size(dtype);
+  const size_t qb = (size_t)B * Hq * Lq * D * es, kb = (size_t)B * Hkv * Lkv * D * es;
+  const size_t lb = (size_t)B * Hq * Lq * sizeof(float);
+  const void* ins[] = {q, k, v, out, dout, lse};
+  const size_t in_bytes[] = {qb, kb, kb, qb, qb, lb};
+  void* outs[] = {dq, dk, dv, workspace};
+  const size_t out_bytes[] = {qb, kb, kb, need};
+  for (int a = 0; a < 4; ++a) {
+    for (int c = 0; c < 6; ++c)
+      if (overlaps(outs[a], out_bytes[a], ins[c], in_bytes[c])) return SDPA_ERR_INVALID_ARG;
+    for (int c = a + 1; c < 4; ++c)
+      if (overlaps(outs[a], out_bytes[a], outs[c], out_bytes[c])) return SDPA_ERR_INVALID_ARG;
+  }
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = out;
+  p.dout = dout;
+  p.lse = const_cast<float*>(lse);
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.delta = static_cast<float*>(workspace);
+  p.causal = is_causal ? 1 : 0;
+  Family f;
+  if ((st = choose(p, dtype, &f)) != SDPA_OK) return st;
+  if ((st = error_word(&p.err)) != SDPA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (f == Family::kVector)
+    return status_of(launch_one(SDPA_KERNEL_VEC_BWD, s, [&] { return launch_vector_bwd(p, dtype, s); }));
+  cudaError_t e = launch_one(SDPA_KERNEL_DELTA, s, [&] { return launch_delta(p, dtype, s); });
+  if (e != cudaSuccess) return status_of(e);
+  const bool tc = f == Family::kTensor;
+  e = launch_one(SDPA_KERNEL_DKDV, s, [&] {
+    return tc ? launch_tc_dkdv(p, dtype, s) : launch_simt_dkdv(p, dtype, s);
+  });
+  if (e != cudaSuccess) return status_of(e);
+  e = launch_one(SDPA_KERNEL_DQ, s, [&] {
+    return tc ? launch_tc_dq(p, dtype, s) : launch_simt_dq(p, dtype, s);
+  });
+  return status_of(e);
+}
+
+extern "C" int sdpa_poll_status(void* stream) {
+  unsigned* err = nullptr;
+  int st = error_word(&err);
+  if (st != SDPA_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SDPA_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return SDPA_ERR_CUDA;
+  if (word == 0) return SDPA_OK;
+  const unsigned zero = 0;
+  if (cudaMemcpy(err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return SDPA_ERR_CUDA;
+  return SDPA_ERR_DEVICE_TIMEOUT;
+}
+
+extern "C" const char* sdpa_status_string(int status) {
+  switch (status) {
+    case SDPA_OK: return "ok";
+    case SDPA_ERR_INVALID_ARG: return "invalid argument";
+    case SDPA_ERR_UNSUPPORTED: return "unsupported dtype, head dim or shape";
+    case SDPA_ERR_CUDA: return "CUDA error";
+    case SDPA_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait timed out";
+    case SDPA_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int sdpa_set_path(int path) {
+  if (path < SDPA_PATH_AUTO || path > SDPA_PATH_VECTOR) return SDPA_ERR_INVALID_ARG;
+  g_path.store(path);
+  return SDPA_OK;
+}
+
+extern "C" uint64_t sdpa_launch_count(void) { return g_launches.load(); }
+
+extern "C" int sdpa_timing_enable(int on) {
+  g_timing_on.store(on != 0);
+  return SDPA_OK;
+}
+
+extern "C" int sdpa_timing_read(int kernel, double* total_ms, uint64_t* launches) {
+  if (kernel < 0 || kernel >= SDPA_KERNEL_COUNT || !total_ms || !launches) return SDPA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_timing_mu);
+  int st = SDPA_OK;
+  for (PendingTiming& pt : g_pending) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(pt.ev.stop) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, pt.ev.start, pt.ev.stop) != cudaSuccess) {
+      st = SDPA_ERR_CUDA;
+    } else {
+      g_total_ms[pt.kernel] += ms;
+      g_timed_launches[pt.kernel] += 1;
+    }
+    g_event_pool.push_back(pt.ev);
+  }
+  g_pending.clear();
+  *total_ms = g_total_ms[kernel];
+  *launches = g_timed_launches[kernel];
+  return st;
+}
+
+extern "C" void sdpa_timing_reset(void) {
+  std::lock_guard<std::mutex> lock(g_timing_mu);
+  for (PendingTiming& pt : g_pending) {
+    cudaEventSynchronize(pt.ev.stop);
+    g_event_pool.push_back(pt.ev);
+  }
+  g_pending.clear();
+  for (int k = 0; k < SDPA_KERNEL_COUNT; ++k) {
+    g_total_ms[k] = 0.0;
+    g_timed_launches[k] = 0;
+  }
+}

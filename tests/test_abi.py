@@ -1,0 +1,130 @@
+"""C-ABI checks that need no GPU: the library loads, exports every declared symbol, and
+rejects bad arguments on the host with the documented status codes before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from scaled_dot_product_flash_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sdpa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sdpa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_documented_calls():
+    names = declared_functions()
+    for n in ("sdpa_fwd", "sdpa_bwd", "sdpa_bwd_workspace_size", "sdpa_poll_status",
+              "sdpa_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert _lib.status_string(code) not in ("", "unknown status")
+    assert _lib.status_string(99) == "unknown status"
+
+
+def test_workspace_size(lib):
+    # fp32 delta per query row, rounded up to 256 bytes
+    assert _lib.sdpa_bwd_workspace_size(2, 32, 8, 4096, 4096, 128, 2) == 2 * 32 * 4096 * 4
+    assert _lib.sdpa_bwd_workspace_size(1, 1, 1, 1, 1, 64, 0) == 256
+    assert _lib.sdpa_bwd_workspace_size(1, 3, 2, 8, 8, 64, 0) == 0   # Hq % Hkv != 0
+    assert _lib.sdpa_bwd_workspace_size(1, 2, 2, 8, 8, 48, 0) == 0   # unsupported D
+
+
+# Fake, 16-byte aligned, non-overlapping "device" addresses: every case below must be
+# rejected by host-side validation, so nothing is ever dereferenced or launched.
+Q, K, V, O, L, DO, DQ, DK, DV, WS = (0x10000000 * (n + 1) for n in range(10))
+GOOD = dict(B=1, Hq=2, Hkv=1, Lq=64, Lkv=64, D=64, scale=0.125, causal=0, dtype=2)
+
+
+def fwd(lib, q=Q, k=K, v=V, o=O, lse=L, **kw):
+    a = dict(GOOD, **kw)
+    return _lib.sdpa_fwd(q, k, v, o, lse, a["B"], a["Hq"], a["Hkv"], a["Lq"], a["Lkv"], a["D"],
+                         a["scale"], a["causal"], a["dtype"], None)
+
+
+def bwd(lib, ws=WS, ws_bytes=1 << 20, dq=DQ, lse=L, **kw):
+    a = dict(GOOD, **kw)
+    return _lib.sdpa_bwd(Q, K, V, O, DO, lse, dq, DK, DV, a["B"], a["Hq"], a["Hkv"], a["Lq"],
+                         a["Lkv"], a["D"], a["scale"], a["causal"], a["dtype"], ws, ws_bytes,
+                         None)
+
+
+INVALID, UNSUPPORTED, WORKSPACE = 1, 2, 5
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), INVALID),
+    (dict(o=0), INVALID),
+    (dict(k=K + 8), INVALID),                 # misaligned
+    (dict(lse=L + 4), INVALID),               # misaligned
+    (dict(B=0), INVALID),
+    (dict(Lq=0), INVALID),
+    (dict(Lkv=0), INVALID),
+    (dict(Hq=3, Hkv=2), INVALID),             # Hq % Hkv
+    (dict(scale=float("nan")), INVALID),
+    (dict(scale=float("inf")), INVALID),
+    (dict(D=48), UNSUPPORTED),
+    (dict(D=256), UNSUPPORTED),
+    (dict(dtype=3), UNSUPPORTED),
+    (dict(B=70000), UNSUPPORTED),
+    (dict(o=Q + 64), INVALID),                # out overlaps q
+    (dict(lse=O), INVALID),                   # lse overlaps out
+])
+def test_forward_rejects(lib, kw, code):
+    assert fwd(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ws=0), WORKSPACE),
+    (dict(ws_bytes=100), WORKSPACE),
+    (dict(lse=0), INVALID),
+    (dict(dq=Q), INVALID),                    # dq aliases q
+    (dict(dq=DQ + 2), INVALID),
+    (dict(ws=DK), INVALID),                   # workspace overlaps dk
+    (dict(Hq=4, Hkv=3), INVALID),
+    (dict(D=80), UNSUPPORTED),
+])
+def test_backward_rejects(lib, kw, code):
+    assert bwd(lib, **kw) == code
+
+
+def test_set_path(lib):
+    assert _lib.sdpa_set_path(7) == INVALID
+    assert _lib.sdpa_set_path(-1) == INVALID
+    for p in (_lib.PATH_TENSOR, _lib.PATH_SIMT, _lib.PATH_VECTOR, _lib.PATH_AUTO):
+        assert _lib.sdpa_set_path(p) == 0
+
+
+def test_launch_counter_is_readable(lib):
+    assert isinstance(_lib.sdpa_launch_count(), int)
+
+
+def test_product_path_has_no_oracle_dependency():
+    """The library binding and the CUDA sources never touch the oracle package."""
+    pkg = os.path.join(ROOT, "scaled_dot_product_flash_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"\b(import|from)\s+oracle\b|oracle[./]", text), f
