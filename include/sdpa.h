@@ -150,6 +150,16 @@ int sdpa_timing_enable(int on);
 int sdpa_timing_read(int kernel, double* total_ms, uint64_t* launches);
 void sdpa_timing_reset(void);
 
+/*
+ * Failure-detection test hook.  Sets the time limit of every bounded wait inside the
+ * kernels launched from now on (default 2 s) and, when `on` is non-zero, makes the next
+ * tensor-core forward launch withhold its first K tile, so that the block's wait for it
+ * runs out: the kernel then records SDPA_ERR_DEVICE_TIMEOUT in the device error word and
+ * returns (no trap, no fault), and sdpa_poll_status reports it.  Returns SDPA_OK, or
+ * SDPA_ERR_INVALID_ARG if wait_limit_ns is 0.
+ */
+int sdpa_debug_inject_timeout(int on, uint64_t wait_limit_ns);
+
 #ifdef __cplusplus
 }
 #endif

@@ -38,6 +38,7 @@ SIGNATURES = {
     "sdpa_timing_read": (_i, [_i, ctypes.POINTER(ctypes.c_double),
                               ctypes.POINTER(ctypes.c_uint64)]),
     "sdpa_timing_reset": (None, []),
+    "sdpa_debug_inject_timeout": (_i, [_i, ctypes.c_uint64]),
 }
 KERNELS = {"fwd": 0, "delta": 1, "dq": 2, "dkdv": 3, "vec_fwd": 4, "vec_bwd": 5}
 
@@ -121,3 +122,7 @@ def sdpa_timing_read(kernel: int):
 
 def sdpa_timing_reset() -> None:
     load().sdpa_timing_reset()
+
+
+def sdpa_debug_inject_timeout(on: bool, wait_limit_ns: int) -> int:
+    return load().sdpa_debug_inject_timeout(int(bool(on)), int(wait_limit_ns))

@@ -68,6 +68,8 @@ struct Problem {
   float scale_log2;  // scale · log2(e)
   int causal;
   unsigned* err;     // device error word
+  uint64_t wait_limit_ns;  // time limit of any single bounded wait inside a kernel
+  int inject;        // test hook: 1 = the tensor-core forward never delivers its first K tile
 };
 
 __host__ __device__ __forceinline__ int64_t q_row(const Problem& p, int b, int h, int i) {

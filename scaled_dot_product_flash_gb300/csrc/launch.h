@@ -21,6 +21,7 @@ cudaError_t launch_vector_bwd(const Problem& p, int dtype, cudaStream_t s);
 
 // Tensor-core path (TMA + tcgen05), fp16/bf16 with D in {64, 128}.
 bool tensor_supported(const Problem& p, int dtype);
+bool tensor_bwd_supported(const Problem& p, int dtype);
 cudaError_t launch_tc_fwd(const Problem& p, int dtype, cudaStream_t s);
 cudaError_t launch_tc_dq(const Problem& p, int dtype, cudaStream_t s);
 cudaError_t launch_tc_dkdv(const Problem& p, int dtype, cudaStream_t s);

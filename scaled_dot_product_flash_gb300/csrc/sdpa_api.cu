@@ -17,6 +17,8 @@ __device__ unsigned g_device_error = 0;
 
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_path{SDPA_PATH_AUTO};
+std::atomic<int> g_inject{0};
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 
 constexpr int kMaxDevices = 64;
 unsigned* g_err_ptr[kMaxDevices] = {};
@@ -66,6 +68,7 @@ int check_sizes(int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale, int
   p->G = Hq / Hkv;
   p->scale = scale;
   p->scale_log2 = scale * kLog2e;
+  p->wait_limit_ns = g_wait_limit_ns.load();
   return SDPA_OK;
 }
 
@@ -181,6 +184,7 @@ extern "C" int sdpa_fwd(const void* q, const void* k, const void* v, void* out, 
       e = launch_one(SDPA_KERNEL_VEC_FWD, s, [&] { return launch_vector_fwd(p, dtype, s); });
       break;
     case Family::kTensor:
+      p.inject = g_inject.exchange(0);
       e = launch_one(SDPA_KERNEL_FWD, s, [&] { return launch_tc_fwd(p, dtype, s); });
       break;
     default:
@@ -245,7 +249,7 @@ extern "C" int sdpa_bwd(const void* q, const void* k, const void* v, const void*
     return status_of(launch_one(SDPA_KERNEL_VEC_BWD, s, [&] { return launch_vector_bwd(p, dtype, s); }));
   cudaError_t e = launch_one(SDPA_KERNEL_DELTA, s, [&] { return launch_delta(p, dtype, s); });
   if (e != cudaSuccess) return status_of(e);
-  const bool tc = f == Family::kTensor;
+  const bool tc = f == Family::kTensor && tensor_bwd_supported(p, dtype);
   e = launch_one(SDPA_KERNEL_DKDV, s, [&] {
     return tc ? launch_tc_dkdv(p, dtype, s) : launch_simt_dkdv(p, dtype, s);
   });
@@ -326,4 +330,11 @@ extern "C" void sdpa_timing_reset(void) {
     g_total_ms[k] = 0.0;
     g_timed_launches[k] = 0;
   }
+}
+
+extern "C" int sdpa_debug_inject_timeout(int on, uint64_t wait_limit_ns) {
+  if (wait_limit_ns == 0) return SDPA_ERR_INVALID_ARG;
+  g_inject.store(on ? 1 : 0);
+  g_wait_limit_ns.store(wait_limit_ns);
+  return SDPA_OK;
 }

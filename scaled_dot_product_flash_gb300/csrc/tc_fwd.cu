@@ -1,0 +1,428 @@
+// Tensor-core forward (fp16/bf16, D in {64, 128}): TMA + tcgen05 + TMEM.
+//
+// One block computes 256 query rows (two 128-row Q tiles) of one (batch, head) against
+// the keys of its KV head (h / G).  Warp roles:
+//   warps 0-3 / 4-7  softmax warpgroup of Q tile 0 / 1: thread = one query row = one TMEM
+//                    lane; online softmax in the log2 domain ("[Metal] Add Flash Attention
+//                    VJP for training", section "Implementation Notes": log2 domain)
+//   warp 8           TMA producer: Q tiles once, then K_j, V_j tiles into a 4-stage ring
+//   warp 9           tcgen05 issuer (one thread) and TMEM owner
+// Each softmax thread reads its 128 scores twice from TMEM (pass 1: row maximum; pass 2:
+// exponentials), which keeps it far below the register limit of a 320-thread block.
+// Tensor memory (512 columns, fp32): S_w = Q_w·K_jᵀ at columns [128w, 128w+128); P_w is
+// written back over the first 64 columns of S_w as packed 16-bit pairs and read from TMEM
+// as the A operand of O_w += P_w·V_j, with O_w at columns [256 + D·w, 256 + D·(w+1)).
+// The running maximum is raised lazily: O and l are rescaled only when a row's maximum
+// grows by more than 2^8, so exponentials stay <= 256 while O and l use one consistent
+// maximum, which keeps the result exact up to rounding.
+// Rows with few visible keys (the first Q tile under the causal mask, or every row when
+// Lkv <= 128) can have |O| near the largest inputs, where rounding P to 16 bits would
+// add an error comparable to the output's own rounding.  For that one KV tile P is split
+// into a 16-bit head and a 16-bit remainder (written to S columns [64, 128)) and both
+// are multiplied into O, so P enters O with ~16 extra bits.
+// Epilogue: O / l rounded to the element type, lse = ln2·(m + log2 l) (natural log).
+#include "launch.h"
+#include "tc_common.cuh"
+
+namespace sdpa {
+namespace {
+using namespace tc;
+
+constexpr int kBM = 128;      // rows per Q tile
+constexpr int kBN = 128;      // keys per KV tile
+constexpr int kQTiles = 2;    // Q tiles per block
+constexpr int kStages = 4;    // K/V ring stages (each one [kBN x D] tile)
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kRescale = 8.f;  // log2 of the largest exponential allowed before rescaling
+
+template <int D>
+struct FwdLayout {
+  static constexpr int kTileBytes = kBM * D * 2;
+  static constexpr int kQOff = 0;
+  static constexpr int kRingOff = kQTiles * kTileBytes;
+  static constexpr int kBytes = kRingOff + kStages * kTileBytes;
+  static constexpr int kSCol = 0;    // S_w at column 128·w
+  static constexpr int kOCol = 256;  // O_w at column 256 + D·w
+};
+
+struct FwdBars {
+  uint64_t q_full;
+  uint64_t kv_full[kStages];
+  uint64_t kv_empty[kStages];
+  uint64_t s_full[kQTiles];
+  uint64_t p_full[kQTiles];
+  uint64_t o_done[kQTiles];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <typename T>
+struct IsBf16 { static constexpr bool value = false; };
+template <>
+struct IsBf16<__nv_bfloat16> { static constexpr bool value = true; };
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+// KV tile j of Q tile starting at tile_row0 gets the split (head + remainder) P.
+__device__ __forceinline__ bool split_tile(const Problem& p, int j, int tile_row0) {
+  return j == 0 && (tile_row0 == 0 || p.Lkv <= kBN);
+}
+
+__device__ __forceinline__ bool visible(const Problem& p, int key, int i) {
+  return key < p.Lkv && (!p.causal || key <= i);
+}
+
+// Second softmax pass of one row over a 128-key tile: exponentials, their sum (returned),
+// and P packed to 16 bits into TMEM columns [0, 64) of the S tile.
+template <typename T>
+__device__ __forceinline__ float softmax_pass2(uint32_t s_addr, float c, float neg_m, bool need_mask,
+                                               int k0, int i, const Problem& p) {
+  float sum = 0.f;
+#pragma unroll
+  for (int cq = 0; cq < 4; ++cq) {
+    uint32_t sr[32];
+    tmem_ld32(s_addr + cq * 32, sr);
+    tmem_ld_wait();
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      float x0 = fmaf(__uint_as_float(sr[2 * e]), c, neg_m);
+      float x1 = fmaf(__uint_as_float(sr[2 * e + 1]), c, neg_m);
+      if (need_mask) {
+        const int key = k0 + cq * 32 + 2 * e;
+        if (!visible(p, key, i)) x0 = neg_inf();
+        if (!visible(p, key + 1, i)) x1 = neg_inf();
+      }
+      const float p0 = ex2(x0), p1 = ex2(x1);
+      sum += p0 + p1;
+      pk[e] = pack2<T>(p0, p1);
+    }
+    tmem_st16(s_addr + cq * 16, pk);
+  }
+  return sum;
+}
+
+// As softmax_pass2, and also the remainder P − head(P), packed to 16 bits into columns
+// [64, 128).  Scores are read 16 columns at a time; the remainder of chunk q goes to
+// columns [64 + 8q, 72 + 8q), which hold the scores of chunk 4 + q/2, so it is kept in
+// registers until that chunk has been read.
+template <typename T>
+__device__ __forceinline__ float softmax_pass2_split(uint32_t s_addr, float c, float neg_m, int k0, int i,
+                                                     const Problem& p) {
+  float sum = 0.f;
+  uint32_t rem[8][8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    uint32_t sr[16];
+    tmem_ld16(s_addr + q * 16, sr);
+    tmem_ld_wait();
+    uint32_t pk[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int key = k0 + q * 16 + 2 * e;
+      float x0 = fmaf(__uint_as_float(sr[2 * e]), c, neg_m);
+      float x1 = fmaf(__uint_as_float(sr[2 * e + 1]), c, neg_m);
+      if (!visible(p, key, i)) x0 = neg_inf();
+      if (!visible(p, key + 1, i)) x1 = neg_inf();
+      const float p0 = ex2(x0), p1 = ex2(x1);
+      sum += p0 + p1;
+      pk[e] = pack2<T>(p0, p1);
+      float h0, h1;
+      unpack2<T>(pk[e], h0, h1);
+      rem[q][e] = pack2<T>(p0 - h0, p1 - h1);
+    }
+    tmem_st8(s_addr + q * 8, pk);
+#pragma unroll
+    for (int q2 = 0; q2 <= q; ++q2)
+      if (4 + q2 / 2 == q) tmem_st8(s_addr + 64 + q2 * 8, rem[q2]);
+  }
+  return sum;
+}
+
+// Bounded wait that ignores the abort flag (used to drain in-flight work at teardown).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > limit_ns) return;
+  }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, Problem p) {
+  using L = FwdLayout<D>;
+  constexpr int kCB = D / 64;
+  constexpr bool kBf16 = IsBf16<T>::value;
+  constexpr uint32_t kIdS = idesc_f16(kBM, kBN, kBf16, false, false);
+  constexpr uint32_t kIdO = idesc_f16(kBM, D, kBf16, false, true);
+  extern __shared__ unsigned char smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ FwdBars bars;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int b = blockIdx.z, h = blockIdx.y, g = h / p.G;
+  const int qb = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;  // heavy first
+  const int row0 = qb * kBM * kQTiles;
+  int nkv[kQTiles];
+#pragma unroll
+  for (int w = 0; w < kQTiles; ++w) {
+    const int r0 = row0 + w * kBM;
+    if (r0 >= p.Lq) {
+      nkv[w] = 0;
+    } else {
+      const int kend = p.causal ? min(p.Lkv, min(p.Lq, r0 + kBM)) : p.Lkv;
+      nkv[w] = (kend + kBN - 1) / kBN;
+    }
+  }
+  const int nmax = max(nkv[0], nkv[1]);
+
+  if (threadIdx.x == 0) {
+    bars.abort = 0;
+    mbar_init(&bars.q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars.kv_full[s], 1);
+      mbar_init(&bars.kv_empty[s], 1);
+    }
+    for (int w = 0; w < kQTiles; ++w) {
+      mbar_init(&bars.s_full[w], 1);
+      mbar_init(&bars.p_full[w], kBM);
+      mbar_init(&bars.o_done[w], 1);
+    }
+    mbar_init(&bars.mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&bars.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = bars.tmem_base;
+  const WaitCtx wc{&bars.abort, 0, p.wait_limit_ns, p.err, kKidTcFwd};
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      const int nq = nkv[1] > 0 ? 2 : 1;
+      mbar_arrive_expect_tx(&bars.q_full, nq * L::kTileBytes);
+      for (int w = 0; w < nq; ++w)
+        for (int cb = 0; cb < kCB; ++cb)
+          tma_load_3d(sm + L::kQOff + w * L::kTileBytes + cb * 16384, &tq, &bars.q_full, cb * 64,
+                      row0 + w * kBM, b * p.Hq + h);
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; ok && j < nmax; ++j) {
+        for (int kv = 0; kv < 2; ++kv) {
+          const int it = 2 * j + kv, s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1;
+          if (!(ok = mbar_wait(&bars.kv_empty[s], ph ^ 1, wc))) break;
+          if (p.inject == 1 && it == 0) continue;  // test hook: never deliver the first K tile
+          mbar_arrive_expect_tx(&bars.kv_full[s], L::kTileBytes);
+          for (int cb = 0; cb < kCB; ++cb)
+            tma_load_3d(sm + L::kRingOff + s * L::kTileBytes + cb * 16384, kv ? &tv : &tk,
+                        &bars.kv_full[s], cb * 64, j * kBN, b * p.Hkv + g);
+          issued = it + 1;
+        }
+      }
+      if (!ok || bars.abort) {  // let copies still in flight land before the block exits
+        for (int it = max(0, issued - kStages); it < issued; ++it)
+          drain_wait(&bars.kv_full[it % kStages], (it / kStages) & 1, 100000000ull);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      bool ok = mbar_wait(&bars.q_full, 0, wc);
+      tc_fence_after();
+      const uint32_t q_s = smem_u32(sm + L::kQOff);
+      const uint32_t ring_s = smem_u32(sm + L::kRingOff);
+      for (int j = 0; ok && j < nmax; ++j) {
+        const int sk = (2 * j) % kStages, sv = (2 * j + 1) % kStages;
+        const uint32_t phk = ((2 * j) / kStages) & 1, phv = ((2 * j + 1) / kStages) & 1;
+        if (!(ok = mbar_wait(&bars.kv_full[sk], phk, wc))) break;
+        tc_fence_after();
+        for (int w = 0; ok && w < kQTiles; ++w) {
+          if (j >= nkv[w]) continue;
+          if (j > 0) {  // P_w(j-1) consumed: S_w may be overwritten
+            if (!(ok = mbar_wait(&bars.o_done[w], (j - 1) & 1, wc))) break;
+            tc_fence_after();
+          }
+          const uint32_t qa = q_s + w * L::kTileBytes, kb = ring_s + sk * L::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+            mma_ss(tbase + L::kSCol + w * 128, sdesc_sw128(qa + off, 16, 1024),
+                   sdesc_sw128(kb + off, 16, 1024), kIdS, kk > 0);
+          }
+          mma_commit(&bars.s_full[w]);
+        }
+        if (!ok) break;
+        mma_commit(&bars.kv_empty[sk]);
+        if (!(ok = mbar_wait(&bars.kv_full[sv], phv, wc))) break;
+        tc_fence_after();
+        for (int w = 0; ok && w < kQTiles; ++w) {
+          if (j >= nkv[w]) continue;
+          if (!(ok = mbar_wait(&bars.p_full[w], j & 1, wc))) break;
+          tc_fence_after();
+          const uint32_t vb = ring_s + sv * L::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ts(tbase + L::kOCol + w * D, tbase + L::kSCol + w * 128 + kk * 8,
+                   sdesc_sw128(vb + kk * 2048, 16384, 1024), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+          if (split_tile(p, j, row0 + w * kBM)) {  // remainder of P, columns [64, 128)
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              mma_ts(tbase + L::kOCol + w * D, tbase + L::kSCol + w * 128 + 64 + kk * 8,
+                     sdesc_sw128(vb + kk * 2048, 16384, 1024), kIdO, 1u);
+          }
+          mma_commit(&bars.o_done[w]);
+        }
+        if (!ok) break;
+        mma_commit(&bars.kv_empty[sv]);
+      }
+      mma_commit(&bars.mma_done);
+      drain_wait(&bars.mma_done, 0, 100000000ull);
+    }
+  } else if (warp < 8) {
+    // Softmax warpgroups.
+    const int w = warp / 4, quarter = warp % 4;
+    const int r = quarter * 32 + lane;
+    const int i = row0 + w * kBM + r;
+    const uint32_t s_addr = tmem_addr(tbase, quarter * 32, L::kSCol + w * 128);
+    const uint32_t o_addr = tmem_addr(tbase, quarter * 32, L::kOCol + w * D);
+    const float c = p.scale_log2;
+    const int tile_row0 = row0 + w * kBM;
+    float m = neg_inf(), l = 0.f;
+    bool ok = true;
+    const bool cpos = c >= 0.f;
+    for (int j = 0; j < nkv[w]; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[w], j & 1, wc));
+      if (!ok) break;
+      tc_fence_after();
+      const int k0 = j * kBN;
+      const bool need_mask = (k0 + kBN > p.Lkv) || (p.causal && k0 + kBN - 1 > tile_row0);
+      // Pass 1: the row maximum of the scaled scores of this tile.
+      float mt = neg_inf();
+#pragma unroll
+      for (int cq = 0; cq < 4; ++cq) {
+        uint32_t sr[32];
+        tmem_ld32(s_addr + cq * 32, sr);
+        tmem_ld_wait();
+        if (need_mask) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int key = k0 + cq * 32 + e;
+            mt = fmaxf(mt, visible(p, key, i) ? __uint_as_float(sr[e]) * c : neg_inf());
+          }
+        } else if (cpos) {
+          float mx = neg_inf();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[e]));
+          mt = fmaxf(mt, mx * c);
+        } else {
+          float mn = -neg_inf();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mn = fminf(mn, __uint_as_float(sr[e]));
+          mt = fmaxf(mt, mn * c);
+        }
+      }
+      const float m_new = fmaxf(m, mt);
+      const bool resc = m_new > m + kRescale;  // always true on the first tile (m = -inf)
+      const float alpha = resc ? ex2(m - m_new) : 1.f;
+      if (resc) {
+        l *= alpha;
+        m = m_new;
+      }
+      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        // Some row of this warp raised its maximum: rescale O once PV(j-1) has landed.
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_done[w], (j - 1) & 1, wc));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c32 = 0; c32 < D / 32; ++c32) {
+          uint32_t orr[32];
+          tmem_ld32(o_addr + c32 * 32, orr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+          tmem_st32(o_addr + c32 * 32, orr);
+        }
+        tmem_st_wait();
+      }
+      // Pass 2: P = exp2(c·s − m), row sum, P packed to 16 bits over S's first 64 columns.
+      if (split_tile(p, j, tile_row0))
+        l += softmax_pass2_split<T>(s_addr, c, -m, k0, i, p);
+      else
+        l += softmax_pass2<T>(s_addr, c, -m, need_mask, k0, i, p);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars.p_full[w]);
+    }
+    if (ok && nkv[w] > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_done[w], (nkv[w] - 1) & 1, wc));
+    if (ok && nkv[w] > 0) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+      const bool valid = i < p.Lq;
+      T* orow = static_cast<T*>(p.out) + q_row(p, b, h, valid ? i : 0) * D;
+#pragma unroll
+      for (int c32 = 0; c32 < D / 32; ++c32) {
+        uint32_t orr[32];
+        tmem_ld32(o_addr + c32 * 32, orr);
+        tmem_ld_wait();
+        uint32_t packed[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          packed[e] = pack2<T>(__uint_as_float(orr[2 * e]) * inv, __uint_as_float(orr[2 * e + 1]) * inv);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c32 * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(packed[4 * v4], packed[4 * v4 + 1], packed[4 * v4 + 2], packed[4 * v4 + 3]);
+        }
+      }
+      if (valid && p.lse) p.lse[q_row(p, b, h, i)] = (m + __log2f(l)) * kLn2;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <typename T, int D>
+cudaError_t tc_fwd_t(const Problem& p, cudaStream_t s) {
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_3d(&tq, p.q, D, p.Lq, p.B * p.Hq, kBM) ||
+      !make_tmap_3d(&tk, p.k, D, p.Lkv, p.B * p.Hkv, kBN) ||
+      !make_tmap_3d(&tv, p.v, D, p.Lkv, p.B * p.Hkv, kBN))
+    return cudaErrorInvalidValue;
+  const int smem = FwdLayout<D>::kBytes + 1024;
+  auto kern = tc_fwd_kernel<T, D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((p.Lq + kBM * kQTiles - 1) / (kBM * kQTiles), p.Hq, p.B);
+  kern<<<grid, kThreads, smem, s>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tensor_supported(const Problem& p, int dtype) {
+  return (dtype == 1 || dtype == 2) && (p.D == 64 || p.D == 128);
+}
+
+cudaError_t launch_tc_fwd(const Problem& p, int dtype, cudaStream_t s) {
+  if (dtype == 2) return p.D == 128 ? tc_fwd_t<__nv_bfloat16, 128>(p, s) : tc_fwd_t<__nv_bfloat16, 64>(p, s);
+  return p.D == 128 ? tc_fwd_t<__half, 128>(p, s) : tc_fwd_t<__half, 64>(p, s);
+}
+
+}  // namespace sdpa
