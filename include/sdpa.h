@@ -102,6 +102,35 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* out, const
              int dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Backward without a workspace argument: sdpa_bwd for callers that cannot allocate device
+ * memory.  Such callers include code running inside a host application or framework that
+ * owns every device allocation and hands its plugins nothing but their inputs and outputs,
+ * code on a latency-critical path that must not call cudaMalloc (which can synchronise
+ * the whole device), and code that runs while its own memory pool is locked.  The pages
+ * this library follows have no counterpart to this call; it exists for those callers.
+ *
+ * Arguments, layouts and results are those of sdpa_bwd, minus the workspace.  The fp32 δ
+ * scratch that sdpa_bwd keeps in the caller's workspace lives instead in a static device
+ * array of SDPA_BWD_NOALLOC_MAX_ROWS floats (4 MiB) inside this library, which every GPU
+ * that loads the library holds until the process exits.  The call allocates nothing: no
+ * cudaMalloc, cudaFree or allocating library routine.
+ *  - Limit: B·Hq·Lq must not exceed SDPA_BWD_NOALLOC_MAX_ROWS; larger problems return
+ *    SDPA_ERR_WORKSPACE before anything is launched (use sdpa_bwd with a workspace).
+ *  - The first call on each device looks up the array's device address (with that device
+ *    current); make that first call before any stream capture begins.
+ *  - Every call shares the one array and it keeps the previous call's contents.  The
+ *    backward writes every δ it reads before reading it, so nothing needs clearing, but
+ *    calls whose work overlaps on the GPU (other streams, other host threads) race on the
+ *    array: order them, e.g. on a single stream.
+ * Returns an sdpa_status_t.
+ */
+#define SDPA_BWD_NOALLOC_MAX_ROWS (1u << 20)
+int sdpa_bwd_noalloc(const void* q, const void* k, const void* v, const void* out,
+                     const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                     int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale, int is_causal,
+                     int dtype, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device error word that kernels set
  * when a bounded wait gives up.  Returns SDPA_OK, SDPA_ERR_DEVICE_TIMEOUT, or
  * SDPA_ERR_CUDA if the synchronisation itself reported an error.

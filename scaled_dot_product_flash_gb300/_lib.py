@@ -39,7 +39,10 @@ SIGNATURES = {
                               ctypes.POINTER(ctypes.c_uint64)]),
     "sdpa_timing_reset": (None, []),
     "sdpa_debug_inject_timeout": (_i, [_i, ctypes.c_uint64]),
+    "sdpa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                              _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
 }
+BWD_NOALLOC_MAX_ROWS = 1 << 20
 KERNELS = {"fwd": 0, "delta": 1, "dq": 2, "dkdv": 3, "vec_fwd": 4, "vec_bwd": 5}
 
 _lib = None
@@ -84,6 +87,13 @@ def sdpa_bwd(q, k, v, out, dout, lse, dq, dk, dv, B, Hq, Hkv, Lq, Lkv, D, scale,
              dtype, workspace, workspace_bytes, stream):
     return load().sdpa_bwd(q, k, v, out, dout, lse, dq, dk, dv, B, Hq, Hkv, Lq, Lkv, D, scale,
                            is_causal, dtype, workspace, workspace_bytes, stream)
+
+
+def sdpa_bwd_noalloc(q, k, v, out, dout, lse, dq, dk, dv, B, Hq, Hkv, Lq, Lkv, D, scale,
+                     is_causal, dtype, stream):
+    """sdpa_bwd with its scratch in the library's static device array (no workspace)."""
+    return load().sdpa_bwd_noalloc(q, k, v, out, dout, lse, dq, dk, dv, B, Hq, Hkv, Lq, Lkv, D,
+                                   scale, is_causal, dtype, stream)
 
 
 def sdpa_poll_status(stream):
