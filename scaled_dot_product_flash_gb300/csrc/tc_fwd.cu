@@ -76,33 +76,38 @@ __device__ __forceinline__ bool visible(const Problem& p, int key, int i) {
 }
 
 // Second softmax pass of one row over a 128-key tile: exponentials, their sum (returned),
-// and P packed to 16 bits into TMEM columns [0, 64) of the S tile.
+// and P packed to 16 bits into TMEM columns [0, 64) of the S tile.  Each round trip reads
+// 64 score columns and writes the 32 packed columns they produce (columns already read).
 template <typename T>
 __device__ __forceinline__ float softmax_pass2(uint32_t s_addr, float c, float neg_m, bool need_mask,
                                                int k0, int i, const Problem& p) {
-  float sum = 0.f;
-#pragma unroll
-  for (int cq = 0; cq < 4; ++cq) {
-    uint32_t sr[32];
-    tmem_ld32(s_addr + cq * 32, sr);
+  float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll 1
+  for (int h2 = 0; h2 < 2; ++h2) {
+    uint32_t sa[32], sb[32];
+    tmem_ld32(s_addr + h2 * 64, sa);
+    tmem_ld32(s_addr + h2 * 64 + 32, sb);
     tmem_ld_wait();
-    uint32_t pk[16];
+    uint32_t pk[32];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      float x0 = fmaf(__uint_as_float(sr[2 * e]), c, neg_m);
-      float x1 = fmaf(__uint_as_float(sr[2 * e + 1]), c, neg_m);
+    for (int e = 0; e < 32; ++e) {
+      const uint32_t* src = e < 16 ? sa : sb;
+      const int ee = e % 16;
+      float x0 = fmaf(__uint_as_float(src[2 * ee]), c, neg_m);
+      float x1 = fmaf(__uint_as_float(src[2 * ee + 1]), c, neg_m);
       if (need_mask) {
-        const int key = k0 + cq * 32 + 2 * e;
+        const int key = k0 + h2 * 64 + 2 * e;
         if (!visible(p, key, i)) x0 = neg_inf();
         if (!visible(p, key + 1, i)) x1 = neg_inf();
       }
       const float p0 = ex2(x0), p1 = ex2(x1);
-      sum += p0 + p1;
+      sum0 += p0;
+      sum1 += p1;
       pk[e] = pack2<T>(p0, p1);
     }
-    tmem_st16(s_addr + cq * 16, pk);
+    tmem_st32(s_addr + h2 * 32, pk);
   }
-  return sum;
+  return sum0 + sum1;
 }
 
 // As softmax_pass2, and also the remainder P − head(P), packed to 16 bits into columns
@@ -307,30 +312,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int k0 = j * kBN;
       const bool need_mask = (k0 + kBN > p.Lkv) || (p.causal && k0 + kBN - 1 > tile_row0);
-      // Pass 1: the row maximum of the scaled scores of this tile.
-      float mt = neg_inf();
+      // Pass 1: the row maximum of the scaled scores of this tile (64 columns per TMEM
+      // round trip, eight independent maxima to keep the dependency chains short).
+      float mt;
+      {
+        float acc[8];
 #pragma unroll
-      for (int cq = 0; cq < 4; ++cq) {
-        uint32_t sr[32];
-        tmem_ld32(s_addr + cq * 32, sr);
-        tmem_ld_wait();
-        if (need_mask) {
+        for (int e = 0; e < 8; ++e) acc[e] = neg_inf();
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t sa[32], sb[32];
+          tmem_ld32(s_addr + h2 * 64, sa);
+          tmem_ld32(s_addr + h2 * 64 + 32, sb);
+          tmem_ld_wait();
+          if (!need_mask && cpos) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int key = k0 + cq * 32 + e;
-            mt = fmaxf(mt, visible(p, key, i) ? __uint_as_float(sr[e]) * c : neg_inf());
+            for (int e = 0; e < 32; ++e) {
+              acc[e % 8] = fmaxf(acc[e % 8], __uint_as_float(sa[e]));
+              acc[e % 8] = fmaxf(acc[e % 8], __uint_as_float(sb[e]));
+            }
+          } else {
+            const int kb = k0 + h2 * 64;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const float xa = __uint_as_float(sa[e]) * c, xb = __uint_as_float(sb[e]) * c;
+              acc[e % 8] = fmaxf(acc[e % 8], (!need_mask || visible(p, kb + e, i)) ? xa : neg_inf());
+              acc[e % 8] = fmaxf(acc[e % 8], (!need_mask || visible(p, kb + 32 + e, i)) ? xb : neg_inf());
+            }
           }
-        } else if (cpos) {
-          float mx = neg_inf();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(sr[e]));
-          mt = fmaxf(mt, mx * c);
-        } else {
-          float mn = -neg_inf();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) mn = fminf(mn, __uint_as_float(sr[e]));
-          mt = fmaxf(mt, mn * c);
         }
+        mt = fmaxf(fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3])),
+                   fmaxf(fmaxf(acc[4], acc[5]), fmaxf(acc[6], acc[7])));
+        if (!need_mask && cpos) mt *= c;
       }
       const float m_new = fmaxf(m, mt);
       const bool resc = m_new > m + kRescale;  // always true on the first tile (m = -inf)
@@ -344,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_done[w], (j - 1) & 1, wc));
         if (!ok) break;
         tc_fence_after();
-#pragma unroll
+#pragma unroll 1
         for (int c32 = 0; c32 < D / 32; ++c32) {
           uint32_t orr[32];
           tmem_ld32(o_addr + c32 * 32, orr);
