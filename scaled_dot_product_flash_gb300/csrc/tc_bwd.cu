@@ -47,6 +47,83 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
   }
 }
 
+// Element work of the dK/dV kernel for one key row and a 64-query block: Pᵀ and dSᵀ from
+// Sᵀ and dPᵀ in TMEM, written back as packed 16-bit pairs over the first 32 columns of
+// each (columns already read).  Per pair of queries: one packed FMA, two exponentials, one
+// packed add and one packed multiply, two conversions.
+template <typename T, bool kCausalMask>
+__device__ __forceinline__ void dkdv_elements(uint32_t s_addr, float c, const float* nlse2,
+                                              const float* ndelta, int j, int i0) {
+  const uint32_t dp_addr = s_addr + 64;
+  const uint64_t cc = f2pack(c, c);
+#pragma unroll 1
+  for (int half = 0; half < 2; ++half) {
+    uint32_t sr[32], dr[32];
+    tmem_ld32(s_addr + half * 32, sr);
+    tmem_ld32(dp_addr + half * 32, dr);
+    tmem_ld_wait();
+    const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(nlse2 + half * 32);
+    const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(ndelta + half * 32);
+    uint32_t pk[16], dk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      float p0, p1;
+      f2unpack(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl2[e]), p0, p1);
+      p0 = ex2(p0);
+      p1 = ex2(p1);
+      if constexpr (kCausalMask) {
+        const int q0 = i0 + half * 32 + 2 * e;
+        if (j > q0) p0 = 0.f;
+        if (j > q0 + 1) p1 = 0.f;
+      }
+      const uint64_t pp = f2pack(p0, p1);
+      const uint64_t t = fadd2(f2pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), nd2[e]);
+      float d0, d1;
+      f2unpack(fmul2(pp, t), d0, d1);
+      pk[e] = pack2<T>(p0, p1);
+      dk[e] = pack2<T>(d0, d1);
+    }
+    tmem_st16(s_addr + half * 16, pk);
+    tmem_st16(dp_addr + half * 16, dk);
+  }
+}
+
+// Element work of the dQ kernel for one query row and a 64-key block: dS = P∘(dP − δ) with
+// P = exp2(c·S − log2e·lse), packed into the first 32 columns of S (all of S read first).
+template <typename T, bool kMask>
+__device__ __forceinline__ void dq_elements(uint32_t s_addr, float c, float nlse2, float ndl, int k0,
+                                            int i, const Problem& p) {
+  const uint32_t dp_addr = s_addr + 64;
+  const uint64_t cc = f2pack(c, c), nl = f2pack(nlse2, nlse2), nd = f2pack(ndl, ndl);
+  uint32_t dsk[32];
+#pragma unroll 1
+  for (int half = 0; half < 2; ++half) {
+    uint32_t sr[32], dr[32];
+    tmem_ld32(s_addr + half * 32, sr);
+    tmem_ld32(dp_addr + half * 32, dr);
+    tmem_ld_wait();
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      float p0, p1;
+      f2unpack(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl), p0, p1);
+      p0 = ex2(p0);
+      p1 = ex2(p1);
+      if constexpr (kMask) {
+        const int key = k0 + half * 32 + 2 * e;
+        if (key >= p.Lkv || (p.causal && key > i)) p0 = 0.f;
+        if (key + 1 >= p.Lkv || (p.causal && key + 1 > i)) p1 = 0.f;
+      }
+      const uint64_t t = fadd2(f2pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), nd);
+      float d0, d1;
+      f2unpack(fmul2(f2pack(p0, p1), t), d0, d1);
+      const uint32_t v = pack2<T>(d0, d1);
+      if (half == 0) dsk[e] = v;
+      else dsk[16 + e] = v;
+    }
+  }
+  tmem_st32(s_addr, dsk);
+}
+
 // Shared-memory plan (offsets from a 1024-byte aligned base).
 template <int D>
 struct BwdLayout {
@@ -74,8 +151,8 @@ struct BwdBars {
   uint64_t acc_done;
   uint32_t tmem_base;
   int abort;
-  float lse2[kStages][kBlk];
-  float delta[kStages][kBlk];
+  alignas(16) float nlse2[kStages][kBlk];   // −log2e·lse per query (−inf past Lq: P = 0 there)
+  alignas(16) float ndelta[kStages][kBlk];  // −δ per query
 };
 
 // ================================================================== dK / dV
@@ -157,15 +234,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                       b * p.Hq + h);
         }
       }
-      // Per-query vectors of the block: log2-domain logsumexp (+inf past Lq, so P = 0
-      // there) and δ.
+      // Per-query vectors of the block, negated for the packed FMA/ADD of the element
+      // warps: −log2e·lse (−inf past Lq, so P = 0 there) and −δ.
       const float* lsep = p.lse + q_row(p, b, h, 0);
       const float* dlp = p.delta + q_row(p, b, h, 0);
 #pragma unroll
       for (int e = lane; e < kBlk; e += 32) {
         const int i = i0 + e;
-        bars.lse2[s][e] = i < p.Lq ? lsep[i] * kLog2e : pos_inf();
-        bars.delta[s][e] = i < p.Lq ? dlp[i] : 0.f;
+        bars.nlse2[s][e] = i < p.Lq ? -lsep[i] * kLog2e : -pos_inf();
+        bars.ndelta[s][e] = i < p.Lq ? -dlp[i] : 0.f;
       }
       mbar_arrive(&bars.vec_full[s]);
       issued = n + 1;
@@ -240,34 +317,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const int i0 = i_begin + (n % nqb) * kBlk;
-      const bool need_mask = (i0 + kBlk > p.Lq) || (p.causal && j0 + kRows - 1 > i0);
+      const bool diag = p.causal && j0 + kRows - 1 > i0;  // some key of this block is after some query
       const uint32_t s_addr = tmem_addr(tbase, quarter * 32, L::kBuf + w * 128);
-      const uint32_t dp_addr = s_addr + 64;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(s_addr + half * 32, sr);
-        tmem_ld32(dp_addr + half * 32, dr);
-        tmem_ld_wait();
-        uint32_t pk[16], dk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int q0 = half * 32 + 2 * e;
-          float p0 = ex2(fmaf(__uint_as_float(sr[2 * e]), c, -bars.lse2[s][q0]));
-          float p1 = ex2(fmaf(__uint_as_float(sr[2 * e + 1]), c, -bars.lse2[s][q0 + 1]));
-          if (need_mask && p.causal) {
-            if (j > i0 + q0) p0 = 0.f;
-            if (j > i0 + q0 + 1) p1 = 0.f;
-          }
-          const float d0 = p0 * (__uint_as_float(dr[2 * e]) - bars.delta[s][q0]);
-          const float d1 = p1 * (__uint_as_float(dr[2 * e + 1]) - bars.delta[s][q0 + 1]);
-          pk[e] = pack2<T>(p0, p1);
-          dk[e] = pack2<T>(d0, d1);
-        }
-        // Columns [16·half, 16·half + 16) were read in this or an earlier half.
-        tmem_st16(s_addr + half * 16, pk);
-        tmem_st16(dp_addr + half * 16, dk);
-      }
+      if (diag)
+        dkdv_elements<T, true>(s_addr, c, bars.nlse2[s], bars.ndelta[s], j, i0);
+      else
+        dkdv_elements<T, false>(s_addr, c, bars.nlse2[s], bars.ndelta[s], j, i0);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars.p_full[w]);
@@ -450,29 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int k0 = n * kBlk;
       const bool need_mask = (k0 + kBlk > p.Lkv) || (p.causal && k0 + kBlk - 1 > i0);
       const uint32_t s_addr = tmem_addr(tbase, quarter * 32, L::kBuf + w * 128);
-      const uint32_t dp_addr = s_addr + 64;
-      uint32_t dsk[32];
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(s_addr + half * 32, sr);
-        tmem_ld32(dp_addr + half * 32, dr);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int key = k0 + half * 32 + 2 * e;
-          float p0 = ex2(fmaf(__uint_as_float(sr[2 * e]), c, -lse2));
-          float p1 = ex2(fmaf(__uint_as_float(sr[2 * e + 1]), c, -lse2));
-          if (need_mask) {
-            if (key >= p.Lkv || (p.causal && key > i)) p0 = 0.f;
-            if (key + 1 >= p.Lkv || (p.causal && key + 1 > i)) p1 = 0.f;
-          }
-          dsk[half * 16 + e] = pack2<T>(p0 * (__uint_as_float(dr[2 * e]) - dl),
-                                        p1 * (__uint_as_float(dr[2 * e + 1]) - dl));
-        }
-      }
-      // dS packed over S's first 32 columns (all of S has been read).
-      tmem_st32(s_addr, dsk);
+      if (need_mask)
+        dq_elements<T, true>(s_addr, c, -lse2, -dl, k0, i, p);
+      else
+        dq_elements<T, false>(s_addr, c, -lse2, -dl, k0, i, p);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars.p_full[w]);

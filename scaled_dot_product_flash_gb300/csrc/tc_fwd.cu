@@ -75,13 +75,52 @@ __device__ __forceinline__ bool visible(const Problem& p, int key, int i) {
   return key < p.Lkv && (!p.causal || key <= i);
 }
 
+// First softmax pass of one row over a 128-key tile: the maximum of the scaled scores
+// (64 score columns per TMEM round trip; three-input max to halve the instructions).
+// Without a mask the raw maximum (or minimum, for a negative scale) is scaled once.
+template <bool kMask>
+__device__ __forceinline__ float row_max(uint32_t s_addr, float c, int k0, int i, const Problem& p) {
+  float acc[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
+  const bool cpos = c >= 0.f;
+#pragma unroll 1
+  for (int h2 = 0; h2 < 2; ++h2) {
+    uint32_t sa[32], sb[32];
+    tmem_ld32(s_addr + h2 * 64, sa);
+    tmem_ld32(s_addr + h2 * 64 + 32, sb);
+    tmem_ld_wait();
+    if constexpr (kMask) {
+      const int kb = k0 + h2 * 64;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const float xa = visible(p, kb + e, i) ? __uint_as_float(sa[e]) * c : neg_inf();
+        const float xb = visible(p, kb + 32 + e, i) ? __uint_as_float(sb[e]) * c : neg_inf();
+        acc[e % 4] = fmax3(acc[e % 4], xa, xb);
+      }
+    } else if (cpos) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        acc[e % 4] = fmax3(acc[e % 4], __uint_as_float(sa[e]), __uint_as_float(sb[e]));
+    } else {
+      if (h2 == 0) acc[0] = acc[1] = acc[2] = acc[3] = -neg_inf();
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        acc[e % 4] = fmin3(acc[e % 4], __uint_as_float(sa[e]), __uint_as_float(sb[e]));
+    }
+  }
+  if constexpr (kMask) return fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3]));
+  if (cpos) return fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3])) * c;
+  return fminf(fminf(acc[0], acc[1]), fminf(acc[2], acc[3])) * c;
+}
+
 // Second softmax pass of one row over a 128-key tile: exponentials, their sum (returned),
 // and P packed to 16 bits into TMEM columns [0, 64) of the S tile.  Each round trip reads
 // 64 score columns and writes the 32 packed columns they produce (columns already read).
-template <typename T>
-__device__ __forceinline__ float softmax_pass2(uint32_t s_addr, float c, float neg_m, bool need_mask,
-                                               int k0, int i, const Problem& p) {
-  float sum0 = 0.f, sum1 = 0.f;
+// Pairs of columns go through packed f32x2 FMA/ADD: about 2.5 instructions per score.
+template <typename T, bool kMask>
+__device__ __forceinline__ float softmax_pass2(uint32_t s_addr, float c, float neg_m, int k0, int i,
+                                               const Problem& p) {
+  const uint64_t cc = f2pack(c, c), nm = f2pack(neg_m, neg_m);
+  uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll 1
   for (int h2 = 0; h2 < 2; ++h2) {
     uint32_t sa[32], sb[32];
@@ -93,21 +132,24 @@ __device__ __forceinline__ float softmax_pass2(uint32_t s_addr, float c, float n
     for (int e = 0; e < 32; ++e) {
       const uint32_t* src = e < 16 ? sa : sb;
       const int ee = e % 16;
-      float x0 = fmaf(__uint_as_float(src[2 * ee]), c, neg_m);
-      float x1 = fmaf(__uint_as_float(src[2 * ee + 1]), c, neg_m);
-      if (need_mask) {
+      float x0, x1;
+      f2unpack(ffma2(f2pack(__uint_as_float(src[2 * ee]), __uint_as_float(src[2 * ee + 1])), cc, nm), x0, x1);
+      if constexpr (kMask) {
         const int key = k0 + h2 * 64 + 2 * e;
         if (!visible(p, key, i)) x0 = neg_inf();
         if (!visible(p, key + 1, i)) x1 = neg_inf();
       }
       const float p0 = ex2(x0), p1 = ex2(x1);
-      sum0 += p0;
-      sum1 += p1;
+      if (e % 2 == 0) acc0 = fadd2(acc0, f2pack(p0, p1));
+      else acc1 = fadd2(acc1, f2pack(p0, p1));
       pk[e] = pack2<T>(p0, p1);
     }
     tmem_st32(s_addr + h2 * 32, pk);
   }
-  return sum0 + sum1;
+  float a, b, c2, d;
+  f2unpack(acc0, a, b);
+  f2unpack(acc1, c2, d);
+  return (a + b) + (c2 + d);
 }
 
 // As softmax_pass2, and also the remainder P − head(P), packed to 16 bits into columns
@@ -305,46 +347,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tile_row0 = row0 + w * kBM;
     float m = neg_inf(), l = 0.f;
     bool ok = true;
-    const bool cpos = c >= 0.f;
     for (int j = 0; j < nkv[w]; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[w], j & 1, wc));
       if (!ok) break;
       tc_fence_after();
       const int k0 = j * kBN;
       const bool need_mask = (k0 + kBN > p.Lkv) || (p.causal && k0 + kBN - 1 > tile_row0);
-      // Pass 1: the row maximum of the scaled scores of this tile (64 columns per TMEM
-      // round trip, eight independent maxima to keep the dependency chains short).
-      float mt;
-      {
-        float acc[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = neg_inf();
-#pragma unroll 1
-        for (int h2 = 0; h2 < 2; ++h2) {
-          uint32_t sa[32], sb[32];
-          tmem_ld32(s_addr + h2 * 64, sa);
-          tmem_ld32(s_addr + h2 * 64 + 32, sb);
-          tmem_ld_wait();
-          if (!need_mask && cpos) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              acc[e % 8] = fmaxf(acc[e % 8], __uint_as_float(sa[e]));
-              acc[e % 8] = fmaxf(acc[e % 8], __uint_as_float(sb[e]));
-            }
-          } else {
-            const int kb = k0 + h2 * 64;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const float xa = __uint_as_float(sa[e]) * c, xb = __uint_as_float(sb[e]) * c;
-              acc[e % 8] = fmaxf(acc[e % 8], (!need_mask || visible(p, kb + e, i)) ? xa : neg_inf());
-              acc[e % 8] = fmaxf(acc[e % 8], (!need_mask || visible(p, kb + 32 + e, i)) ? xb : neg_inf());
-            }
-          }
-        }
-        mt = fmaxf(fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3])),
-                   fmaxf(fmaxf(acc[4], acc[5]), fmaxf(acc[6], acc[7])));
-        if (!need_mask && cpos) mt *= c;
-      }
+      // Pass 1: the row maximum of the scaled scores of this tile.
+      const float mt = need_mask ? row_max<true>(s_addr, c, k0, i, p) : row_max<false>(s_addr, c, k0, i, p);
       const float m_new = fmaxf(m, mt);
       const bool resc = m_new > m + kRescale;  // always true on the first tile (m = -inf)
       const float alpha = resc ? ex2(m - m_new) : 1.f;
@@ -371,8 +381,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Pass 2: P = exp2(c·s − m), row sum, P packed to 16 bits over S's first 64 columns.
       if (split_tile(p, j, tile_row0))
         l += softmax_pass2_split<T>(s_addr, c, -m, k0, i, p);
+      else if (need_mask)
+        l += softmax_pass2<T, true>(s_addr, c, -m, k0, i, p);
       else
-        l += softmax_pass2<T>(s_addr, c, -m, need_mask, k0, i, p);
+        l += softmax_pass2<T, false>(s_addr, c, -m, k0, i, p);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars.p_full[w]);
