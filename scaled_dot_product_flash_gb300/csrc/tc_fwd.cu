@@ -211,8 +211,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ FwdBars bars;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int b = blockIdx.z, h = blockIdx.y, g = h / p.G;
-  const int qb = p.causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;  // heavy first
+  // Block order: all heads of one query block, then the next block; under the causal mask
+  // the last (heaviest) query blocks go first so that the tail of the grid is light.
+  const int units = p.B * p.Hq;
+  const int unit = blockIdx.x % units, rank = blockIdx.x / units;
+  const int b = unit / p.Hq, h = unit % p.Hq, g = h / p.G;
+  const int nqb = (p.Lq + kBM * kQTiles - 1) / (kBM * kQTiles);
+  const int qb = p.causal ? nqb - 1 - rank : rank;
   const int row0 = qb * kBM * kQTiles;
   int nkv[kQTiles];
 #pragma unroll
@@ -434,8 +439,8 @@ cudaError_t tc_fwd_t(const Problem& p, cudaStream_t s) {
   auto kern = tc_fwd_kernel<T, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((p.Lq + kBM * kQTiles - 1) / (kBM * kQTiles), p.Hq, p.B);
-  kern<<<grid, kThreads, smem, s>>>(tq, tk, tv, p);
+  const unsigned nqb = (p.Lq + kBM * kQTiles - 1) / (kBM * kQTiles);
+  kern<<<nqb * p.Hq * p.B, kThreads, smem, s>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
