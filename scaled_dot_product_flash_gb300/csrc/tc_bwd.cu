@@ -23,8 +23,8 @@
 // the shared-memory operand traffic exceed what one SM's shared memory can deliver.
 // Warps 0-3 and 4-7 split each 128-column block of scores into two 64-column halves
 // (warpgroup w owns columns [64w, 64w+64) and writes its packed results to its own
-// columns [64w, 64w+32)), warp 8 is the TMA producer, warp 9 issues the MMAs and owns the
-// 512 TMEM columns.
+// columns [64w, 64w+32)), warp 8 is the TMA producer, warps 9 and 10 issue the MMAs (two
+// independent chains each) and warp 9 owns the 512 TMEM columns.
 #include "launch.h"
 #include "tc_common.cuh"
 
@@ -32,7 +32,7 @@ namespace sdpa {
 namespace {
 using namespace tc;
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kRows = 128;  // rows owned by a block (keys for dK/dV, queries for dQ)
@@ -94,7 +94,7 @@ __device__ __forceinline__ void init_bars(BwdBars& bars) {
   mbar_init(&bars.own_full, 1);
   for (int s = 0; s < kStages; ++s) {
     mbar_init(&bars.ring_full[s], 1);
-    mbar_init(&bars.ring_empty[s], 1);
+    mbar_init(&bars.ring_empty[s], 2);  // released by both MMA issuers
     mbar_init(&bars.vec_full[s], 32);
   }
   mbar_init(&bars.s_full[0], 1);
@@ -106,7 +106,7 @@ __device__ __forceinline__ void init_bars(BwdBars& bars) {
   mbar_init(&bars.y_free, 1);
   mbar_init(&bars.dq_done[0], 1);
   mbar_init(&bars.dq_done[1], 1);
-  mbar_init(&bars.acc_done, 1);
+  mbar_init(&bars.acc_done, 2);  // one commit per MMA issuer
   fence_mbar_init();
 }
 
@@ -214,34 +214,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int n = max(0, issued - kStages); n < issued; ++n)
         drain_wait(&bars.ring_full[n % kStages], (n / kStages) & 1, 100000000ull);
     }
-  } else if (warp == kMmaWarp) {
-    // ---------------------------------------------------------------- MMA issuer
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    // ---------------------------------------------------------------- MMA issuers
+    // Two independent chains, one issuer each: warp 9 issues Sᵀ and dV (TMEM region X),
+    // warp 10 issues dPᵀ and dK (region Y), so Sᵀ of the next block can start as soon as
+    // dV has consumed Pᵀ even while dK still waits for dSᵀ.
+    const bool chain_x = warp == kMmaWarp;
     if (lane == 0) {
       bool ok = mbar_wait(&bars.own_full, 0, wc);
       tc_fence_after();
-      const uint32_t k_s = smem_u32(sm + L::kOwnA), v_s = smem_u32(sm + L::kOwnB);
+      const uint32_t own_s = smem_u32(sm + (chain_x ? L::kOwnA : L::kOwnB));  // K or V
+      const uint32_t col = chain_x ? kColX : kColY;
+      const uint32_t acc = chain_x ? kColDv : kColDk;
+      uint64_t* freed = chain_x ? &bars.x_free : &bars.y_free;
+      uint64_t* ready = chain_x ? &bars.p_ready : &bars.ds_ready;
+      uint64_t* scores_done = chain_x ? &bars.s_full[0] : &bars.dp_full;
       for (int n = 0; ok && n < total; ++n) {
         const int s = n % kStages;
-        const uint32_t par = (n - 1) & 1;
         const uint32_t q_s = smem_u32(sm + L::kRing + s * L::kStageBytes), do_s = q_s + L::kTileBytes;
         if (!(ok = mbar_wait(&bars.ring_full[s], (n / kStages) & 1, wc))) break;
-        if (n > 0 && !(ok = mbar_wait(&bars.x_free, par, wc))) break;
+        if (n > 0 && !(ok = mbar_wait(freed, (n - 1) & 1, wc))) break;
         tc_fence_after();
-        mma_scores<D>(tbase + kColX, k_s, q_s, kIdS);  // Sᵀ = K·Qᵀ
-        mma_commit(&bars.s_full[0]);
-        if (n > 0 && !(ok = mbar_wait(&bars.y_free, par, wc))) break;
+        mma_scores<D>(tbase + col, own_s, chain_x ? q_s : do_s, kIdS);  // Sᵀ = K·Qᵀ or dPᵀ = V·dOᵀ
+        mma_commit(scores_done);
+        if (!(ok = mbar_wait(ready, n & 1, wc))) break;
         tc_fence_after();
-        mma_scores<D>(tbase + kColY, v_s, do_s, kIdS);  // dPᵀ = V·dOᵀ
-        mma_commit(&bars.dp_full);
-        if (!(ok = mbar_wait(&bars.p_ready, n & 1, wc))) break;
-        tc_fence_after();
-        mma_accumulate<D>(tbase + kColDv, tbase + kColX, do_s, kIdAcc, n == 0);  // dV += Pᵀ·dO
-        mma_commit(&bars.x_free);
-        if (!(ok = mbar_wait(&bars.ds_ready, n & 1, wc))) break;
-        tc_fence_after();
-        mma_accumulate<D>(tbase + kColDk, tbase + kColY, q_s, kIdAcc, n == 0);  // dK += dSᵀ·Q
-        mma_commit(&bars.y_free);
-        mma_commit(&bars.ring_empty[s]);
+        // dV += Pᵀ·dO or dK += dSᵀ·Q
+        mma_accumulate<D>(tbase + acc, tbase + col, chain_x ? do_s : q_s, kIdAcc, n == 0);
+        mma_commit(freed);
+        mma_commit(&bars.ring_empty[s]);  // one of the stage's two arrivals
       }
       mma_commit(&bars.acc_done);
       drain_wait(&bars.acc_done, 0, 100000000ull);
@@ -264,32 +265,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool diag = p.causal && j0 + kRows - 1 > i0;
       const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(&bars.nlse2[s][64 * w]);
       const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(&bars.ndelta[s][64 * w]);
-      // Pᵀ for this half: 64 queries, kept in registers for dSᵀ and packed over Sᵀ.
-      float pr[64];
-      {
-        uint32_t sa[32], sb[32];
-        tmem_ld32(x_addr, sa);
-        tmem_ld32(x_addr + 32, sb);
-        tmem_ld_wait();
-        uint32_t pk[32];
+      // Pᵀ for this half (64 queries), 32 per TMEM round trip; the packed 16-bit values
+      // are written over Sᵀ and kept in registers for dSᵀ (which therefore uses the same
+      // rounded Pᵀ that dV is multiplied with).
+      uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const uint32_t* src = e < 16 ? sa : sb;
-          const int ee = e % 16;
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t sr[32];
+        tmem_ld32(x_addr + 32 * hh, sr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int q = 32 * hh + 2 * e;
           float p0, p1;
-          f2unpack(ffma2(f2pack(__uint_as_float(src[2 * ee]), __uint_as_float(src[2 * ee + 1])), cc, nl2[e]),
-                   p0, p1);
-          p0 = ex2(p0);
-          p1 = ex2(p1);
+          ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl2[q / 2]), p0,
+                   p1);
           if (diag) {
-            if (j > i0 + 2 * e) p0 = 0.f;
-            if (j > i0 + 2 * e + 1) p1 = 0.f;
+            if (j > i0 + q) p0 = 0.f;
+            if (j > i0 + q + 1) p1 = 0.f;
           }
-          pr[2 * e] = p0;
-          pr[2 * e + 1] = p1;
-          pk[e] = pack2<T>(p0, p1);
+          pk[16 * hh + e] = pack2<T>(p0, p1);
         }
-        tmem_st32(x_addr, pk);
+        tmem_st16(x_addr + 16 * hh, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * hh]));
       }
       tmem_st_wait();
       tc_fence_before();
@@ -307,8 +304,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int q = 32 * hh + 2 * e;
-          float d0, d1;
-          f2unpack(fmul2(f2pack(pr[q], pr[q + 1]),
+          float p0, p1, d0, d1;
+          unpack2<T>(pk[16 * hh + e], p0, p1);
+          f2unpack(fmul2(f2pack(p0, p1),
                          fadd2(f2pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), nd2[q / 2])),
                    d0, d1);
           dk[e] = pack2<T>(d0, d1);
@@ -359,13 +357,45 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ================================================================== dQ
+// K blocks live until dQ has used them, V blocks only until dP has, so they have rings of
+// their own: three K stages let the next K block load while dQ still reads the current one.
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
+
+template <int D>
+struct DqLayout {
+  static constexpr int kTileBytes = kRows * D * 2;
+  static constexpr int kQ = 0;
+  static constexpr int kDo = kTileBytes;
+  static constexpr int kK = 2 * kTileBytes;                       // kKStages K blocks
+  static constexpr int kV = kK + kKStages * kTileBytes;           // kVStages V blocks
+  static constexpr int kBytes = kV + kVStages * kTileBytes;
+};
+
+struct DqBars {
+  uint64_t own_full;
+  uint64_t k_full[kKStages];
+  uint64_t k_empty[kKStages];
+  uint64_t v_full[kVStages];
+  uint64_t v_empty[kVStages];
+  uint64_t s_full[2];   // one per S buffer
+  uint64_t dp_full;
+  uint64_t dp_free;     // the element warps have read dP (its buffer may be refilled)
+  uint64_t ds_ready;    // dS packed
+  uint64_t dq_done[2];  // dQ MMA of the block in S buffer i has finished
+  uint64_t acc_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                  Problem p) {
-  using L = BwdLayout<D>;
+  using L = DqLayout<D>;
   constexpr int kCB = D / 64;
+  constexpr int kCbStride = kRows * 128;
   constexpr bool kBf16 = IsBf16<T>::value;
   constexpr uint32_t kIdS = idesc_f16(kRows, kBlk, kBf16, false, false);
   constexpr uint32_t kIdAcc = idesc_f16(kRows, D, kBf16, false, true);
@@ -373,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kColDq = 0, kColS0 = D, kColDp = D + 256;
   extern __shared__ unsigned char smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ BwdBars bars;
+  __shared__ DqBars bars;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // Block order: all heads of one query tile, then the next; causal: heaviest tiles first.
@@ -386,7 +416,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kend = p.causal ? min(p.Lkv, min(p.Lq, i0 + kRows)) : p.Lkv;
   const int total = (kend + kBlk - 1) / kBlk;  // KV blocks visited
 
-  if (threadIdx.x == 0) init_bars(bars);
+  if (threadIdx.x == 0) {
+    bars.abort = 0;
+    mbar_init(&bars.own_full, 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&bars.k_full[s], 1);
+      mbar_init(&bars.k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&bars.v_full[s], 1);
+      mbar_init(&bars.v_empty[s], 1);
+    }
+    mbar_init(&bars.s_full[0], 1);
+    mbar_init(&bars.s_full[1], 1);
+    mbar_init(&bars.dp_full, 1);
+    mbar_init(&bars.dp_free, 256);
+    mbar_init(&bars.ds_ready, 256);
+    mbar_init(&bars.dq_done[0], 1);
+    mbar_init(&bars.dq_done[1], 1);
+    mbar_init(&bars.acc_done, 2);  // one commit per MMA issuer
+    fence_mbar_init();
+  }
   if (warp == kMmaWarp) {
     tmem_alloc(&bars.tmem_base, 512);
     tmem_relinquish();
@@ -403,61 +453,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tv);
       mbar_arrive_expect_tx(&bars.own_full, 2 * L::kTileBytes);
       for (int cb = 0; cb < kCB; ++cb) {
-        tma_load_3d(sm + L::kOwnA + cb * L::kCbStride, &tq, &bars.own_full, cb * 64, i0, b * p.Hq + h);
-        tma_load_3d(sm + L::kOwnB + cb * L::kCbStride, &tdo, &bars.own_full, cb * 64, i0, b * p.Hq + h);
+        tma_load_3d(sm + L::kQ + cb * kCbStride, &tq, &bars.own_full, cb * 64, i0, b * p.Hq + h);
+        tma_load_3d(sm + L::kDo + cb * kCbStride, &tdo, &bars.own_full, cb * 64, i0, b * p.Hq + h);
       }
-      int issued = 0;
+      int k_issued = 0, v_issued = 0;
       bool ok = true;
       for (int n = 0; ok && n < total; ++n) {
-        const int s = n % kStages;
-        if (!(ok = mbar_wait(&bars.ring_empty[s], ((n / kStages) & 1) ^ 1, wc))) break;
-        mbar_arrive_expect_tx(&bars.ring_full[s], 2 * L::kTileBytes);
-        uint8_t* st = sm + L::kRing + s * L::kStageBytes;
-        for (int cb = 0; cb < kCB; ++cb) {
-          tma_load_3d(st + cb * L::kCbStride, &tk, &bars.ring_full[s], cb * 64, n * kBlk, b * p.Hkv + g);
-          tma_load_3d(st + L::kTileBytes + cb * L::kCbStride, &tv, &bars.ring_full[s], cb * 64, n * kBlk,
-                      b * p.Hkv + g);
-        }
-        issued = n + 1;
+        const int sk = n % kKStages, sv = n % kVStages;
+        if (!(ok = mbar_wait(&bars.k_empty[sk], ((n / kKStages) & 1) ^ 1, wc))) break;
+        mbar_arrive_expect_tx(&bars.k_full[sk], L::kTileBytes);
+        for (int cb = 0; cb < kCB; ++cb)
+          tma_load_3d(sm + L::kK + sk * L::kTileBytes + cb * kCbStride, &tk, &bars.k_full[sk], cb * 64,
+                      n * kBlk, b * p.Hkv + g);
+        k_issued = n + 1;
+        if (!(ok = mbar_wait(&bars.v_empty[sv], ((n / kVStages) & 1) ^ 1, wc))) break;
+        mbar_arrive_expect_tx(&bars.v_full[sv], L::kTileBytes);
+        for (int cb = 0; cb < kCB; ++cb)
+          tma_load_3d(sm + L::kV + sv * L::kTileBytes + cb * kCbStride, &tv, &bars.v_full[sv], cb * 64,
+                      n * kBlk, b * p.Hkv + g);
+        v_issued = n + 1;
       }
       if (!ok || bars.abort) {
-        for (int n = max(0, issued - kStages); n < issued; ++n)
-          drain_wait(&bars.ring_full[n % kStages], (n / kStages) & 1, 100000000ull);
+        for (int n = max(0, k_issued - kKStages); n < k_issued; ++n)
+          drain_wait(&bars.k_full[n % kKStages], (n / kKStages) & 1, 100000000ull);
+        for (int n = max(0, v_issued - kVStages); n < v_issued; ++n)
+          drain_wait(&bars.v_full[n % kVStages], (n / kVStages) & 1, 100000000ull);
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    // Two issuers: warp 9 issues S and dQ, warp 10 issues dP, each at its own pace.
     if (lane == 0) {
       bool ok = mbar_wait(&bars.own_full, 0, wc);
       tc_fence_after();
-      const uint32_t q_s = smem_u32(sm + L::kOwnA), do_s = smem_u32(sm + L::kOwnB);
-      auto stage = [&](int n) { return smem_u32(sm + L::kRing + (n % kStages) * L::kStageBytes); };
-      // S(n) = Q·K(n)ᵀ into S buffer n % 2 (free once dQ(n-2) has read dS(n-2) from it).
-      auto issue_s = [&](int n) -> bool {
-        if (!mbar_wait(&bars.ring_full[n % kStages], (n / kStages) & 1, wc)) return false;
-        if (n >= 2 && !mbar_wait(&bars.dq_done[n % 2], ((n - 2) / 2) & 1, wc)) return false;
-        tc_fence_after();
-        mma_scores<D>(tbase + kColS0 + 128 * (n % 2), q_s, stage(n), kIdS);
-        mma_commit(&bars.s_full[n % 2]);
-        return true;
-      };
-      // dP(n) = dO·V(n)ᵀ into the dP buffer (free once the element warps finished block n-1).
-      auto issue_dp = [&](int n) {
-        mma_scores<D>(tbase + kColDp, do_s, stage(n) + L::kTileBytes, kIdS);
-        mma_commit(&bars.dp_full);
-      };
-      if (ok && total > 0) {
-        ok = issue_s(0);
-        if (ok) issue_dp(0);
+      const uint32_t q_s = smem_u32(sm + L::kQ), do_s = smem_u32(sm + L::kDo);
+      const uint32_t k_s = smem_u32(sm + L::kK), v_s = smem_u32(sm + L::kV);
+      if (warp == kMmaWarp) {
+        // S(n) = Q·K(n)ᵀ into S buffer n % 2 (free once dQ(n-2) has read dS(n-2) from it).
+        auto issue_s = [&](int n) -> bool {
+          if (!mbar_wait(&bars.k_full[n % kKStages], (n / kKStages) & 1, wc)) return false;
+          if (n >= 2 && !mbar_wait(&bars.dq_done[n % 2], ((n - 2) / 2) & 1, wc)) return false;
+          tc_fence_after();
+          mma_scores<D>(tbase + kColS0 + 128 * (n % 2), q_s, k_s + (n % kKStages) * L::kTileBytes, kIdS);
+          mma_commit(&bars.s_full[n % 2]);
+          return true;
+        };
+        if (ok && total > 0) ok = issue_s(0);
         if (ok && total > 1) ok = issue_s(1);
-      }
-      for (int n = 0; ok && n < total; ++n) {
-        if (!(ok = mbar_wait(&bars.ds_ready, n & 1, wc))) break;
-        tc_fence_after();
-        if (n + 1 < total) issue_dp(n + 1);  // its ring stage was waited for in issue_s(n+1)
-        mma_accumulate<D>(tbase + kColDq, tbase + kColS0 + 128 * (n % 2), stage(n), kIdAcc, n == 0);
-        mma_commit(&bars.dq_done[n % 2]);
-        mma_commit(&bars.ring_empty[n % kStages]);
-        if (n + 2 < total && !(ok = issue_s(n + 2))) break;
+        for (int n = 0; ok && n < total; ++n) {
+          if (!(ok = mbar_wait(&bars.ds_ready, n & 1, wc))) break;
+          tc_fence_after();
+          // dQ += dS·K: B = the K block read MN-major.
+          mma_accumulate<D>(tbase + kColDq, tbase + kColS0 + 128 * (n % 2),
+                            k_s + (n % kKStages) * L::kTileBytes, kIdAcc, n == 0);
+          mma_commit(&bars.dq_done[n % 2]);
+          mma_commit(&bars.k_empty[n % kKStages]);
+          if (n + 2 < total && !(ok = issue_s(n + 2))) break;
+        }
+      } else {
+        // dP(n) = dO·V(n)ᵀ into the dP buffer (free once the element warps have read dP(n-1)).
+        for (int n = 0; ok && n < total; ++n) {
+          if (!(ok = mbar_wait(&bars.v_full[n % kVStages], (n / kVStages) & 1, wc))) break;
+          if (n >= 1 && !(ok = mbar_wait(&bars.dp_free, (n - 1) & 1, wc))) break;
+          tc_fence_after();
+          mma_scores<D>(tbase + kColDp, do_s, v_s + (n % kVStages) * L::kTileBytes, kIdS);
+          mma_commit(&bars.dp_full);
+          mma_commit(&bars.v_empty[n % kVStages]);
+        }
       }
       mma_commit(&bars.acc_done);
       drain_wait(&bars.acc_done, 0, 100000000ull);
@@ -480,27 +541,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool need_mask = (k0 + 64 > p.Lkv) || (p.causal && k0 + 63 > i0);
       const uint32_t s_addr = tmem_addr(tbase, quarter * 32, kColS0 + 128 * (n % 2) + 64 * w);
       const uint32_t dp_addr = tmem_addr(tbase, quarter * 32, kColDp + 64 * w);
+      // dP first, so that the next block's dP can be computed during this block's math.
+      uint32_t dr[64];
+      tmem_ld32(dp_addr, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+      tmem_ld32(dp_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&bars.dp_free);
       uint32_t dsk[32];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        uint32_t sr[32], dr[32];
+        uint32_t sr[32];
         tmem_ld32(s_addr + 32 * hh, sr);
-        tmem_ld32(dp_addr + 32 * hh, dr);
         tmem_ld_wait();
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           float p0, p1;
-          f2unpack(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl), p0, p1);
-          p0 = ex2(p0);
-          p1 = ex2(p1);
+          ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl), p0, p1);
           if (need_mask) {
             const int key = k0 + 32 * hh + 2 * e;
             if (key >= p.Lkv || (p.causal && key > i)) p0 = 0.f;
             if (key + 1 >= p.Lkv || (p.causal && key + 1 > i)) p1 = 0.f;
           }
+          const int q = 32 * hh + 2 * e;
           float d0, d1;
-          f2unpack(fmul2(f2pack(p0, p1),
-                         fadd2(f2pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), nd)),
+          f2unpack(fmul2(f2pack(p0, p1), fadd2(f2pack(__uint_as_float(dr[q]), __uint_as_float(dr[q + 1])), nd)),
                    d0, d1);
           dsk[16 * hh + e] = pack2<T>(d0, d1);
         }
@@ -574,7 +639,7 @@ template <typename T, int D>
 cudaError_t dq_t(const Problem& p, cudaStream_t s) {
   Maps m;
   if (!make_maps(p, D, &m)) return cudaErrorInvalidValue;
-  const int smem = BwdLayout<D>::kBytes + 1024;
+  const int smem = DqLayout<D>::kBytes + 1024;
   auto kern = tc_dq_kernel<T, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;

@@ -301,6 +301,14 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// 2^x for both halves of a packed pair (two exponential-unit instructions).
+__device__ __forceinline__ void ex2_pair(uint64_t x, float& p0, float& p1) {
+  float x0, x1;
+  f2unpack(x, x0, x1);
+  p0 = ex2(x0);
+  p1 = ex2(x1);
+}
+
 }  // namespace tc
 
 // ------------------------------------------------------------------ host: tensor maps

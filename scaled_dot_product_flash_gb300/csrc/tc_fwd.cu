@@ -6,7 +6,7 @@
 //                    lane; online softmax in the log2 domain ("[Metal] Add Flash Attention
 //                    VJP for training", section "Implementation Notes": log2 domain)
 //   warp 8           TMA producer: Q tiles once, then K_j, V_j tiles into a 4-stage ring
-//   warp 9           tcgen05 issuer (one thread) and TMEM owner
+//   warps 9 / 10     tcgen05 issuers (one thread each) for Q tile 0 / 1; warp 9 owns TMEM
 // Each softmax thread reads its 128 scores twice from TMEM (pass 1: row maximum; pass 2:
 // exponentials), which keeps it far below the register limit of a 320-thread block.
 // Tensor memory (512 columns, fp32): S_w = Q_w·K_jᵀ at columns [128w, 128w+128); P_w is
@@ -32,7 +32,7 @@ constexpr int kBM = 128;      // rows per Q tile
 constexpr int kBN = 128;      // keys per KV tile
 constexpr int kQTiles = 2;    // Q tiles per block
 constexpr int kStages = 4;    // K/V ring stages (each one [kBN x D] tile)
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr float kRescale = 8.f;  // log2 of the largest exponential allowed before rescaling
@@ -54,7 +54,7 @@ struct FwdBars {
   uint64_t s_full[kQTiles];
   uint64_t p_full[kQTiles];
   uint64_t o_done[kQTiles];
-  uint64_t mma_done;
+  uint64_t mma_done[kQTiles];
   uint32_t tmem_base;
   int abort;
 };
@@ -132,14 +132,17 @@ __device__ __forceinline__ float softmax_pass2(uint32_t s_addr, float c, float n
     for (int e = 0; e < 32; ++e) {
       const uint32_t* src = e < 16 ? sa : sb;
       const int ee = e % 16;
-      float x0, x1;
-      f2unpack(ffma2(f2pack(__uint_as_float(src[2 * ee]), __uint_as_float(src[2 * ee + 1])), cc, nm), x0, x1);
+      uint64_t xx = ffma2(f2pack(__uint_as_float(src[2 * ee]), __uint_as_float(src[2 * ee + 1])), cc, nm);
       if constexpr (kMask) {
         const int key = k0 + h2 * 64 + 2 * e;
+        float x0, x1;
+        f2unpack(xx, x0, x1);
         if (!visible(p, key, i)) x0 = neg_inf();
         if (!visible(p, key + 1, i)) x1 = neg_inf();
+        xx = f2pack(x0, x1);
       }
-      const float p0 = ex2(x0), p1 = ex2(x1);
+      float p0, p1;
+      ex2_pair(xx, p0, p1);
       if (e % 2 == 0) acc0 = fadd2(acc0, f2pack(p0, p1));
       else acc1 = fadd2(acc1, f2pack(p0, p1));
       pk[e] = pack2<T>(p0, p1);
@@ -237,14 +240,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars.q_full, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars.kv_full[s], 1);
-      mbar_init(&bars.kv_empty[s], 1);
+      mbar_init(&bars.kv_empty[s], kQTiles);  // released by both MMA issuers
     }
     for (int w = 0; w < kQTiles; ++w) {
       mbar_init(&bars.s_full[w], 1);
       mbar_init(&bars.p_full[w], kBM);
       mbar_init(&bars.o_done[w], 1);
     }
-    mbar_init(&bars.mma_done, 1);
+    mbar_init(&bars.mma_done[0], 1);
+    mbar_init(&bars.mma_done[1], 1);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -288,24 +292,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           drain_wait(&bars.kv_full[it % kStages], (it / kStages) & 1, 100000000ull);
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    // One MMA issuer per Q tile, so that each tile's chain S → softmax → PV → S advances
+    // at its own pace and neither issuer waits on the other tile's softmax.
+    const int w = warp - kMmaWarp;
     if (lane == 0) {
       bool ok = mbar_wait(&bars.q_full, 0, wc);
       tc_fence_after();
-      const uint32_t q_s = smem_u32(sm + L::kQOff);
+      const uint32_t qa = smem_u32(sm + L::kQOff) + w * L::kTileBytes;
       const uint32_t ring_s = smem_u32(sm + L::kRingOff);
       for (int j = 0; ok && j < nmax; ++j) {
         const int sk = (2 * j) % kStages, sv = (2 * j + 1) % kStages;
         const uint32_t phk = ((2 * j) / kStages) & 1, phv = ((2 * j + 1) / kStages) & 1;
+        // Every stage use gets exactly one arrival from each issuer, made only after the
+        // stage was filled for this use, even by an issuer whose tile needs no MMA here.
         if (!(ok = mbar_wait(&bars.kv_full[sk], phk, wc))) break;
-        tc_fence_after();
-        for (int w = 0; ok && w < kQTiles; ++w) {
-          if (j >= nkv[w]) continue;
-          if (j > 0) {  // P_w(j-1) consumed: S_w may be overwritten
-            if (!(ok = mbar_wait(&bars.o_done[w], (j - 1) & 1, wc))) break;
-            tc_fence_after();
-          }
-          const uint32_t qa = q_s + w * L::kTileBytes, kb = ring_s + sk * L::kTileBytes;
+        if (j < nkv[w]) {
+          if (j > 0 && !(ok = mbar_wait(&bars.o_done[w], (j - 1) & 1, wc))) break;  // P_w(j-1) consumed
+          tc_fence_after();
+          const uint32_t kb = ring_s + sk * L::kTileBytes;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
@@ -314,12 +319,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(&bars.s_full[w]);
         }
-        if (!ok) break;
-        mma_commit(&bars.kv_empty[sk]);
+        mma_commit(&bars.kv_empty[sk]);  // one of the stage's two arrivals
         if (!(ok = mbar_wait(&bars.kv_full[sv], phv, wc))) break;
-        tc_fence_after();
-        for (int w = 0; ok && w < kQTiles; ++w) {
-          if (j >= nkv[w]) continue;
+        if (j < nkv[w]) {
           if (!(ok = mbar_wait(&bars.p_full[w], j & 1, wc))) break;
           tc_fence_after();
           const uint32_t vb = ring_s + sv * L::kTileBytes;
@@ -335,11 +337,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(&bars.o_done[w]);
         }
-        if (!ok) break;
         mma_commit(&bars.kv_empty[sv]);
       }
-      mma_commit(&bars.mma_done);
-      drain_wait(&bars.mma_done, 0, 100000000ull);
+      mma_commit(&bars.mma_done[w]);
+      drain_wait(&bars.mma_done[w], 0, 100000000ull);
     }
   } else if (warp < 8) {
     // Softmax warpgroups.
