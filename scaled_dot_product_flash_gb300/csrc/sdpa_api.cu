@@ -181,7 +181,9 @@ extern "C" int sdpa_fwd(const void* q, const void* k, const void* v, void* out, 
   cudaError_t e;
   switch (f) {
     case Family::kVector:
-      e = launch_one(SDPA_KERNEL_VEC_FWD, s, [&] { return launch_vector_fwd(p, dtype, s); });
+      e = launch_one(SDPA_KERNEL_VEC_FWD, s, [&] {
+        return vector_mma_supported(p, dtype) ? launch_vector_mma_fwd(p, dtype, s) : launch_vector_fwd(p, dtype, s);
+      });
       break;
     case Family::kTensor:
       p.inject = g_inject.exchange(0);

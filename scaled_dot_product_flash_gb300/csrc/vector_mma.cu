@@ -1,0 +1,376 @@
+// Short-query ("vector") forward for fp16/bf16 with D in {64, 128}, on warp-level MMAs.
+//
+// Lq <= 8 and G·Lq <= 32 rows per KV head: the work is a stream over the KV rows, and the
+// kernel is meant to run at HBM speed.  The arithmetic per key byte (up to 32 rows × 2
+// FLOP per element) is beyond what fp32 FMAs sustain at that speed, so both products use
+// warp-level mma.sync (m16n8k16, fp32 accumulate); everything else is the short-sequence
+// design of "[Metal] Add Flash Attention VJP for training" (section "Implementation Notes",
+// item 3): per-row reductions by warp shuffles, fp32 accumulators, and shared-memory
+// reductions to merge partial results.
+//
+// One cluster of 8 blocks per (batch, KV head); block c owns a contiguous chunk of keys,
+// streamed by TMA in 64-key tiles through a 3-stage ring (each K/V byte read once).
+// Warp (mt, kq) of a block takes rows [16mt, 16mt+16) of the group and keys
+// [16kq, 16kq+16) of every tile, keeping its own online-softmax state (row maximum, row
+// sum, O).  At the end the four key quarters are merged in shared memory and the eight
+// blocks of the cluster through distributed shared memory (log-sum-exp merge), so no
+// workspace is needed.  Row r of the group is query r % Lq of head g·G + r / Lq.
+#include <cooperative_groups.h>
+
+#include "launch.h"
+#include "tc_common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace sdpa {
+namespace {
+using namespace tc;
+
+constexpr int kCs = 8;        // blocks per cluster
+constexpr int kKeys = 64;     // keys per streamed tile
+constexpr int kRing = 3;      // ring stages
+
+__device__ __forceinline__ float ninf() { return __int_as_float(0xff800000); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+template <typename T>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1);
+template <>
+__device__ __forceinline__ void mma16816<__nv_bfloat16>(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+template <>
+__device__ __forceinline__ void mma16816<__half>(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Shared-memory address of (row, 16-byte chunk) in a [64 rows x D] 16-bit tile stored by
+// TMA with 128-byte swizzle as D/64 column blocks of [64 rows][64 elements].
+template <int D>
+__device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int chunk) {
+  return tile + (chunk >> 3) * (kKeys * 128) + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+}
+
+template <int D, int MT>
+struct VmLayout {
+  static constexpr int kTileBytes = kKeys * D * 2;
+  static constexpr int kStageBytes = 2 * kTileBytes;            // K tile, V tile
+  static constexpr int kRingBytes = kRing * kStageBytes;
+  static constexpr int kWarps = 4 * MT;
+  static constexpr int kRows = 16 * MT;
+  // after the loop the ring is reused for the merges:
+  static constexpr int kPartO = 0;                               // [warps][16][D] fp32
+  static constexpr int kPartM = kPartO + kWarps * 16 * D * 4;    // [warps][16]
+  static constexpr int kPartL = kPartM + kWarps * 16 * 4;
+  static constexpr int kCtaO = kPartL + kWarps * 16 * 4;         // [rows][D] fp32
+  static constexpr int kCtaM = kCtaO + kRows * D * 4;            // [rows]
+  static constexpr int kCtaL = kCtaM + kRows * 4;
+  static constexpr int kMergeBytes = kCtaL + kRows * 4;
+  static constexpr int kBytes = kRingBytes > kMergeBytes ? kRingBytes : kMergeBytes;
+};
+
+template <typename T, int D, int MT>
+__global__ void __launch_bounds__(128 * MT) vec_mma_fwd_kernel(const __grid_constant__ CUtensorMap tk,
+                                                              const __grid_constant__ CUtensorMap tv, Problem p,
+                                                              int chunk) {
+  using L = VmLayout<D, MT>;
+  constexpr int kWarps = L::kWarps;
+  extern __shared__ unsigned char smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t full[kRing], empty[kRing];
+  __shared__ int abort_flag;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int c = (int)cluster.block_rank();
+  const int b = blockIdx.z, g = blockIdx.y;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int mt = warp % MT, kq = warp / MT;
+  const int R = p.G * p.Lq;
+  const int kv_end = p.causal ? min(p.Lkv, p.Lq) : p.Lkv;  // query i sees keys 0..i only
+  const int j_begin = c * chunk, j_end = min(kv_end, j_begin + chunk);
+  const int ntiles = j_end > j_begin ? (j_end - j_begin + kKeys - 1) / kKeys : 0;
+  const WaitCtx wc{&abort_flag, 0, p.wait_limit_ns, p.err, kKidVecFwd};
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const uint32_t ring = smem_u32(sm);
+  auto issue = [&](int t) {
+    const int s = t % kRing;
+    mbar_arrive_expect_tx(&full[s], L::kStageBytes);
+    for (int cb = 0; cb < D / 64; ++cb) {
+      tma_load_3d(sm + s * L::kStageBytes + cb * (kKeys * 128), &tk, &full[s], cb * 64, j_begin + t * kKeys,
+                  b * p.Hkv + g);
+      tma_load_3d(sm + s * L::kStageBytes + L::kTileBytes + cb * (kKeys * 128), &tv, &full[s], cb * 64,
+                  j_begin + t * kKeys, b * p.Hkv + g);
+    }
+  };
+  int issued = 0;  // tiles whose loads thread 0 has issued
+  if (threadIdx.x == 0)
+    for (; issued < min(kRing, ntiles); ++issued) issue(issued);
+
+  // Q fragments (rows r0 = 16mt + lane/4 and r1 = r0 + 8 of the group).
+  const int r0 = 16 * mt + lane / 4, r1 = r0 + 8;
+  uint32_t qf[D / 16][4];
+  {
+    const T* q = static_cast<const T*>(p.q);
+    const int64_t row0 = r0 < R ? q_row(p, b, g * p.G + r0 / p.Lq, r0 % p.Lq) : -1;
+    const int64_t row1 = r1 < R ? q_row(p, b, g * p.G + r1 / p.Lq, r1 % p.Lq) : -1;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int col = 16 * kk + 2 * (lane % 4);
+      qf[kk][0] = row0 >= 0 ? *reinterpret_cast<const uint32_t*>(q + row0 * D + col) : 0u;
+      qf[kk][1] = row1 >= 0 ? *reinterpret_cast<const uint32_t*>(q + row1 * D + col) : 0u;
+      qf[kk][2] = row0 >= 0 ? *reinterpret_cast<const uint32_t*>(q + row0 * D + col + 8) : 0u;
+      qf[kk][3] = row1 >= 0 ? *reinterpret_cast<const uint32_t*>(q + row1 * D + col + 8) : 0u;
+    }
+  }
+  const int i0 = r0 < R ? r0 % p.Lq : 0, i1 = r1 < R ? r1 % p.Lq : 0;
+  const float c2 = p.scale_log2;
+  const bool split = p.causal || p.Lkv <= 256;  // rows see few keys
+  float m0 = ninf(), m1 = ninf(), l0 = 0.f, l1 = 0.f;
+  float o[D / 8][4];
+#pragma unroll
+  for (int dn = 0; dn < D / 8; ++dn) o[dn][0] = o[dn][1] = o[dn][2] = o[dn][3] = 0.f;
+
+  bool ok = true;
+  for (int t = 0; t < ntiles; ++t) {
+    const int s = t % kRing;
+    ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (t / kRing) & 1, wc));
+    if (!ok) break;
+    const uint32_t kt = ring + s * L::kStageBytes, vt = kt + L::kTileBytes;
+    // S = Q·Kᵀ for this warp's 16 keys (two n-tiles of 8).
+    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int mm = lane / 8;
+      const int key = 16 * kq + (mm / 2) * 8 + (lane % 8);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(swz<D>(kt, key, 2 * kk + (mm % 2)), b0, b1, b2, b3);
+      mma16816<T>(sc[0], qf[kk], b0, b1);
+      mma16816<T>(sc[1], qf[kk], b2, b3);
+    }
+    // Scale, mask, online softmax (rows r0: elements 0,1; r1: elements 2,3).
+    const int kbase = j_begin + t * kKeys + 16 * kq + 2 * (lane % 4);
+    float x[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = kbase + 8 * nt + (e & 1);
+        const int ir = e < 2 ? i0 : i1, rr = e < 2 ? r0 : r1;
+        const bool vis = j < j_end && rr < R && (!p.causal || j <= ir);
+        x[nt][e] = vis ? sc[nt][e] * c2 : ninf();
+      }
+    float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+    float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+#pragma unroll
+    for (int off = 1; off <= 2; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float a0 = mn0 == ninf() ? 1.f : ex2(m0 - mn0), a1 = mn1 == ninf() ? 1.f : ex2(m1 - mn1);
+    m0 = mn0;
+    m1 = mn1;
+    float pr[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      pr[nt][0] = mn0 == ninf() ? 0.f : ex2(x[nt][0] - mn0);
+      pr[nt][1] = mn0 == ninf() ? 0.f : ex2(x[nt][1] - mn0);
+      pr[nt][2] = mn1 == ninf() ? 0.f : ex2(x[nt][2] - mn1);
+      pr[nt][3] = mn1 == ninf() ? 0.f : ex2(x[nt][3] - mn1);
+    }
+    l0 = l0 * a0 + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+    l1 = l1 * a1 + (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
+    if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
+#pragma unroll
+      for (int dn = 0; dn < D / 8; ++dn) {
+        o[dn][0] *= a0;
+        o[dn][1] *= a0;
+        o[dn][2] *= a1;
+        o[dn][3] *= a1;
+      }
+    }
+    // O += P·V (P as the A fragment: the C layout of S, repacked to 16 bits).  With few
+    // visible keys per row |O| can be as large as |V|; then P also enters as its 16-bit
+    // remainder P − head(P), so that rounding P adds nothing measurable to O's own rounding.
+    const uint32_t pa[4] = {pack2<T>(pr[0][0], pr[0][1]), pack2<T>(pr[0][2], pr[0][3]),
+                            pack2<T>(pr[1][0], pr[1][1]), pack2<T>(pr[1][2], pr[1][3])};
+    uint32_t pl[4];
+    if (split) {
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        float h0, h1;
+        unpack2<T>(pa[a], h0, h1);
+        pl[a] = pack2<T>(pr[a / 2][2 * (a % 2)] - h0, pr[a / 2][2 * (a % 2) + 1] - h1);
+      }
+    }
+#pragma unroll
+    for (int dn2 = 0; dn2 < D / 16; ++dn2) {
+      const int mm = lane / 8;
+      const int key = 16 * kq + (mm % 2) * 8 + (lane % 8);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(swz<D>(vt, key, 2 * dn2 + mm / 2), b0, b1, b2, b3);
+      mma16816<T>(o[2 * dn2], pa, b0, b1);
+      mma16816<T>(o[2 * dn2 + 1], pa, b2, b3);
+      if (split) {
+        mma16816<T>(o[2 * dn2], pl, b0, b1);
+        mma16816<T>(o[2 * dn2 + 1], pl, b2, b3);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (threadIdx.x == 0 && t + kRing < ntiles) {
+      if (!mbar_wait(&empty[s], (t / kRing) & 1, wc)) ok = false;
+      else issue(issued++);
+    }
+  }
+  if (threadIdx.x == 0 && (!ok || abort_flag)) {  // let copies still in flight land
+    for (int t = max(0, issued - kRing); t < issued; ++t) {
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(&full[t % kRing], (t / kRing) & 1) && globaltimer() - t0 < 100000000ull) {
+      }
+    }
+  }
+  // Row sums were kept per lane: finish them across the quad.
+#pragma unroll
+  for (int off = 1; off <= 2; off <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+  }
+  __syncthreads();  // every stage consumed: the ring is free for the merges
+  float* part_o = reinterpret_cast<float*>(sm + L::kPartO);
+  float* part_m = reinterpret_cast<float*>(sm + L::kPartM);
+  float* part_l = reinterpret_cast<float*>(sm + L::kPartL);
+  {
+    const int lr = lane / 4;
+#pragma unroll
+    for (int dn = 0; dn < D / 8; ++dn) {
+      const int d = 8 * dn + 2 * (lane % 4);
+      part_o[(warp * 16 + lr) * D + d] = o[dn][0];
+      part_o[(warp * 16 + lr) * D + d + 1] = o[dn][1];
+      part_o[(warp * 16 + lr + 8) * D + d] = o[dn][2];
+      part_o[(warp * 16 + lr + 8) * D + d + 1] = o[dn][3];
+    }
+    if (lane % 4 == 0) {
+      part_m[warp * 16 + lr] = m0;
+      part_m[warp * 16 + lr + 8] = m1;
+      part_l[warp * 16 + lr] = l0;
+      part_l[warp * 16 + lr + 8] = l1;
+    }
+  }
+  __syncthreads();
+  // Merge the four key quarters of each row block: this block's partial (M, L, O).
+  float* cta_o = reinterpret_cast<float*>(sm + L::kCtaO);
+  float* cta_m = reinterpret_cast<float*>(sm + L::kCtaM);
+  float* cta_l = reinterpret_cast<float*>(sm + L::kCtaL);
+  for (int e = threadIdx.x; e < L::kRows * D; e += blockDim.x) {
+    const int r = e / D, d = e % D, mtr = r / 16, lr = r % 16;
+    float M = ninf();
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) M = fmaxf(M, part_m[(mtr + MT * q4) * 16 + lr]);
+    float Lsum = 0.f, O = 0.f;
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const int w = mtr + MT * q4;
+      const float mw = part_m[w * 16 + lr];
+      const float wgt = mw == ninf() ? 0.f : ex2(mw - M);
+      Lsum = fmaf(part_l[w * 16 + lr], wgt, Lsum);
+      O = fmaf(part_o[(w * 16 + lr) * D + d], wgt, O);
+    }
+    cta_o[r * D + d] = O;
+    if (d == 0) {
+      cta_m[r] = M;
+      cta_l[r] = Lsum;
+    }
+  }
+  cluster.sync();
+  // Merge the cluster's blocks; block c finalises head-dim slice [c·D/8, (c+1)·D/8).
+  constexpr int kSlice = D / kCs;
+  for (int e = threadIdx.x; e < R * kSlice; e += blockDim.x) {
+    const int r = e / kSlice, d = c * kSlice + e % kSlice;
+    float M = ninf();
+    for (int cc = 0; cc < kCs; ++cc) M = fmaxf(M, cluster.map_shared_rank(cta_m, cc)[r]);
+    float Lsum = 0.f, O = 0.f;
+    for (int cc = 0; cc < kCs; ++cc) {
+      const float mc = cluster.map_shared_rank(cta_m, cc)[r];
+      const float wgt = mc == ninf() ? 0.f : ex2(mc - M);
+      Lsum = fmaf(cluster.map_shared_rank(cta_l, cc)[r], wgt, Lsum);
+      O = fmaf(cluster.map_shared_rank(cta_o, cc)[r * D + d], wgt, O);
+    }
+    const int64_t row = q_row(p, b, g * p.G + r / p.Lq, r % p.Lq);
+    static_cast<T*>(p.out)[row * D + d] = Elem<T>::from_f(O / Lsum);
+    if (p.lse && d == 0) p.lse[row] = (M + __log2f(Lsum)) * kLn2;
+  }
+  cluster.sync();  // peers may still be reading this block's shared memory
+  (void)ok;
+}
+
+template <typename T, int D, int MT>
+cudaError_t vec_mma_fwd_t(const Problem& p, cudaStream_t s) {
+  CUtensorMap tk, tv;
+  if (!make_tmap_3d(&tk, p.k, D, p.Lkv, p.B * p.Hkv, kKeys) || !make_tmap_3d(&tv, p.v, D, p.Lkv, p.B * p.Hkv, kKeys))
+    return cudaErrorInvalidValue;
+  const int smem = VmLayout<D, MT>::kBytes + 1024;
+  auto kern = vec_mma_fwd_kernel<T, D, MT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int chunk = ((p.Lkv + kCs - 1) / kCs + kKeys - 1) / kKeys * kKeys;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kCs, p.Hkv, p.B);
+  cfg.blockDim = dim3(128 * MT, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, p, chunk);
+}
+
+template <typename T>
+cudaError_t vec_mma_fwd_any(const Problem& p, cudaStream_t s) {
+  const bool two = p.G * p.Lq > 16;
+  if (p.D == 128) return two ? vec_mma_fwd_t<T, 128, 2>(p, s) : vec_mma_fwd_t<T, 128, 1>(p, s);
+  return two ? vec_mma_fwd_t<T, 64, 2>(p, s) : vec_mma_fwd_t<T, 64, 1>(p, s);
+}
+
+}  // namespace
+
+bool vector_mma_supported(const Problem& p, int dtype) {
+  return (dtype == 1 || dtype == 2) && (p.D == 64 || p.D == 128) && p.Lq <= 8 && p.G * p.Lq <= 32;
+}
+
+cudaError_t launch_vector_mma_fwd(const Problem& p, int dtype, cudaStream_t s) {
+  return dtype == 2 ? vec_mma_fwd_any<__nv_bfloat16>(p, s) : vec_mma_fwd_any<__half>(p, s);
+}
+
+}  // namespace sdpa
