@@ -18,9 +18,10 @@ cudaError_t launch_delta(const Problem& p, int dtype, cudaStream_t s);
 bool vector_supported(const Problem& p, int dtype);
 cudaError_t launch_vector_fwd(const Problem& p, int dtype, cudaStream_t s);
 cudaError_t launch_vector_bwd(const Problem& p, int dtype, cudaStream_t s);
-// Its warp-level-MMA forward for fp16/bf16 with D in {64, 128}.
+// Its warp-level-MMA kernels for fp16/bf16 with D in {64, 128}.
 bool vector_mma_supported(const Problem& p, int dtype);
 cudaError_t launch_vector_mma_fwd(const Problem& p, int dtype, cudaStream_t s);
+cudaError_t launch_vector_mma_bwd(const Problem& p, int dtype, cudaStream_t s);
 
 // Tensor-core path (TMA + tcgen05), fp16/bf16 with D in {64, 128}.
 bool tensor_supported(const Problem& p, int dtype);

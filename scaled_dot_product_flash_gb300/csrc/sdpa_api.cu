@@ -248,7 +248,9 @@ extern "C" int sdpa_bwd(const void* q, const void* k, const void* v, const void*
   if ((st = error_word(&p.err)) != SDPA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (f == Family::kVector)
-    return status_of(launch_one(SDPA_KERNEL_VEC_BWD, s, [&] { return launch_vector_bwd(p, dtype, s); }));
+    return status_of(launch_one(SDPA_KERNEL_VEC_BWD, s, [&] {
+      return vector_mma_supported(p, dtype) ? launch_vector_mma_bwd(p, dtype, s) : launch_vector_bwd(p, dtype, s);
+    }));
   cudaError_t e = launch_one(SDPA_KERNEL_DELTA, s, [&] { return launch_delta(p, dtype, s); });
   if (e != cudaSuccess) return status_of(e);
   const bool tc = f == Family::kTensor && tensor_bwd_supported(p, dtype);

@@ -1,4 +1,5 @@
-// Short-query ("vector") forward for fp16/bf16 with D in {64, 128}, on warp-level MMAs.
+// Short-query ("vector") forward and backward for fp16/bf16 with D in {64, 128}, on
+// warp-level MMAs.
 //
 // Lq <= 8 and G·Lq <= 32 rows per KV head: the work is a stream over the KV rows, and the
 // kernel is meant to run at HBM speed.  The arithmetic per key byte (up to 32 rows × 2
@@ -10,11 +11,12 @@
 //
 // One cluster of 8 blocks per (batch, KV head); block c owns a contiguous chunk of keys,
 // streamed by TMA in 64-key tiles through a 3-stage ring (each K/V byte read once).
-// Warp (mt, kq) of a block takes rows [16mt, 16mt+16) of the group and keys
-// [16kq, 16kq+16) of every tile, keeping its own online-softmax state (row maximum, row
-// sum, O).  At the end the four key quarters are merged in shared memory and the eight
-// blocks of the cluster through distributed shared memory (log-sum-exp merge), so no
-// workspace is needed.  Row r of the group is query r % Lq of head g·G + r / Lq.
+// A block has four warps; with MT row blocks of 16 (MT = 1 or 2), warp (mt, kq) takes rows
+// [16mt, 16mt+16) of the group and the 64/(4/MT)-key slice kq of every tile, in 16-key
+// steps, keeping its own online-softmax state (row maximum, row sum, O).  At the end the
+// key slices are merged in shared memory and the eight blocks of the cluster through
+// distributed shared memory (log-sum-exp merge), so no workspace is needed.  Row r of the
+// group is query r % Lq of head g·G + r / Lq.
 #include <cooperative_groups.h>
 
 #include "launch.h"
@@ -75,7 +77,8 @@ struct VmLayout {
   static constexpr int kTileBytes = kKeys * D * 2;
   static constexpr int kStageBytes = 2 * kTileBytes;            // K tile, V tile
   static constexpr int kRingBytes = kRing * kStageBytes;
-  static constexpr int kWarps = 4 * MT;
+  static constexpr int kWarps = 4;
+  static constexpr int kSlices = 4 / MT;           // key slices per tile (one per warp of a row block)
   static constexpr int kRows = 16 * MT;
   // after the loop the ring is reused for the merges:
   static constexpr int kPartO = 0;                               // [warps][16][D] fp32
@@ -89,7 +92,7 @@ struct VmLayout {
 };
 
 template <typename T, int D, int MT>
-__global__ void __launch_bounds__(128 * MT) vec_mma_fwd_kernel(const __grid_constant__ CUtensorMap tk,
+__global__ void __launch_bounds__(128) vec_mma_fwd_kernel(const __grid_constant__ CUtensorMap tk,
                                                               const __grid_constant__ CUtensorMap tv, Problem p,
                                                               int chunk) {
   using L = VmLayout<D, MT>;
@@ -102,7 +105,8 @@ __global__ void __launch_bounds__(128 * MT) vec_mma_fwd_kernel(const __grid_cons
   const int c = (int)cluster.block_rank();
   const int b = blockIdx.z, g = blockIdx.y;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int mt = warp % MT, kq = warp / MT;
+  const int mt = warp % MT, kq = warp / MT;  // row block, key slice
+  constexpr int kSliceKeys = kKeys / L::kSlices;
   const int R = p.G * p.Lq;
   const int kv_end = p.causal ? min(p.Lkv, p.Lq) : p.Lkv;  // query i sees keys 0..i only
   const int j_begin = c * chunk, j_end = min(kv_end, j_begin + chunk);
@@ -163,84 +167,88 @@ __global__ void __launch_bounds__(128 * MT) vec_mma_fwd_kernel(const __grid_cons
     ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (t / kRing) & 1, wc));
     if (!ok) break;
     const uint32_t kt = ring + s * L::kStageBytes, vt = kt + L::kTileBytes;
-    // S = Q·Kᵀ for this warp's 16 keys (two n-tiles of 8).
-    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll 1
+    for (int ch = 0; ch < kSliceKeys / 16; ++ch) {
+      const int koff = kq * kSliceKeys + 16 * ch;  // first key of this 16-key step within the tile
+      // S = Q·Kᵀ for this warp's 16 keys (two n-tiles of 8).
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const int mm = lane / 8;
-      const int key = 16 * kq + (mm / 2) * 8 + (lane % 8);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(swz<D>(kt, key, 2 * kk + (mm % 2)), b0, b1, b2, b3);
-      mma16816<T>(sc[0], qf[kk], b0, b1);
-      mma16816<T>(sc[1], qf[kk], b2, b3);
-    }
-    // Scale, mask, online softmax (rows r0: elements 0,1; r1: elements 2,3).
-    const int kbase = j_begin + t * kKeys + 16 * kq + 2 * (lane % 4);
-    float x[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int j = kbase + 8 * nt + (e & 1);
-        const int ir = e < 2 ? i0 : i1, rr = e < 2 ? r0 : r1;
-        const bool vis = j < j_end && rr < R && (!p.causal || j <= ir);
-        x[nt][e] = vis ? sc[nt][e] * c2 : ninf();
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const int mm = lane / 8;
+        const int key = koff + (mm / 2) * 8 + (lane % 8);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(swz<D>(kt, key, 2 * kk + (mm % 2)), b0, b1, b2, b3);
+        mma16816<T>(sc[0], qf[kk], b0, b1);
+        mma16816<T>(sc[1], qf[kk], b2, b3);
       }
-    float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-    float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
+      // Scale, mask, online softmax (rows r0: elements 0,1; r1: elements 2,3).
+      const int kbase = j_begin + t * kKeys + koff + 2 * (lane % 4);
+      float x[2][4];
 #pragma unroll
-    for (int off = 1; off <= 2; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-    }
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float a0 = mn0 == ninf() ? 1.f : ex2(m0 - mn0), a1 = mn1 == ninf() ? 1.f : ex2(m1 - mn1);
-    m0 = mn0;
-    m1 = mn1;
-    float pr[2][4];
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      pr[nt][0] = mn0 == ninf() ? 0.f : ex2(x[nt][0] - mn0);
-      pr[nt][1] = mn0 == ninf() ? 0.f : ex2(x[nt][1] - mn0);
-      pr[nt][2] = mn1 == ninf() ? 0.f : ex2(x[nt][2] - mn1);
-      pr[nt][3] = mn1 == ninf() ? 0.f : ex2(x[nt][3] - mn1);
-    }
-    l0 = l0 * a0 + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
-    l1 = l1 * a1 + (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
-    if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
+        for (int e = 0; e < 4; ++e) {
+          const int j = kbase + 8 * nt + (e & 1);
+          const int ir = e < 2 ? i0 : i1, rr = e < 2 ? r0 : r1;
+          const bool vis = j < j_end && rr < R && (!p.causal || j <= ir);
+          x[nt][e] = vis ? sc[nt][e] * c2 : ninf();
+        }
+      float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
+      float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
 #pragma unroll
-      for (int dn = 0; dn < D / 8; ++dn) {
-        o[dn][0] *= a0;
-        o[dn][1] *= a0;
-        o[dn][2] *= a1;
-        o[dn][3] *= a1;
+      for (int off = 1; off <= 2; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
       }
-    }
-    // O += P·V (P as the A fragment: the C layout of S, repacked to 16 bits).  With few
-    // visible keys per row |O| can be as large as |V|; then P also enters as its 16-bit
-    // remainder P − head(P), so that rounding P adds nothing measurable to O's own rounding.
-    const uint32_t pa[4] = {pack2<T>(pr[0][0], pr[0][1]), pack2<T>(pr[0][2], pr[0][3]),
-                            pack2<T>(pr[1][0], pr[1][1]), pack2<T>(pr[1][2], pr[1][3])};
-    uint32_t pl[4];
-    if (split) {
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float a0 = mn0 == ninf() ? 1.f : ex2(m0 - mn0), a1 = mn1 == ninf() ? 1.f : ex2(m1 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+      float pr[2][4];
 #pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        float h0, h1;
-        unpack2<T>(pa[a], h0, h1);
-        pl[a] = pack2<T>(pr[a / 2][2 * (a % 2)] - h0, pr[a / 2][2 * (a % 2) + 1] - h1);
+      for (int nt = 0; nt < 2; ++nt) {
+        pr[nt][0] = mn0 == ninf() ? 0.f : ex2(x[nt][0] - mn0);
+        pr[nt][1] = mn0 == ninf() ? 0.f : ex2(x[nt][1] - mn0);
+        pr[nt][2] = mn1 == ninf() ? 0.f : ex2(x[nt][2] - mn1);
+        pr[nt][3] = mn1 == ninf() ? 0.f : ex2(x[nt][3] - mn1);
       }
-    }
+      l0 = l0 * a0 + (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+      l1 = l1 * a1 + (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
+      if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
-    for (int dn2 = 0; dn2 < D / 16; ++dn2) {
-      const int mm = lane / 8;
-      const int key = 16 * kq + (mm % 2) * 8 + (lane % 8);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(swz<D>(vt, key, 2 * dn2 + mm / 2), b0, b1, b2, b3);
-      mma16816<T>(o[2 * dn2], pa, b0, b1);
-      mma16816<T>(o[2 * dn2 + 1], pa, b2, b3);
+        for (int dn = 0; dn < D / 8; ++dn) {
+          o[dn][0] *= a0;
+          o[dn][1] *= a0;
+          o[dn][2] *= a1;
+          o[dn][3] *= a1;
+        }
+      }
+      // O += P·V (P as the A fragment: the C layout of S, repacked to 16 bits).  With few
+      // visible keys per row |O| can be as large as |V|; then P also enters as its 16-bit
+      // remainder P − head(P), so that rounding P adds nothing measurable to O's own rounding.
+      const uint32_t pa[4] = {pack2<T>(pr[0][0], pr[0][1]), pack2<T>(pr[0][2], pr[0][3]),
+                              pack2<T>(pr[1][0], pr[1][1]), pack2<T>(pr[1][2], pr[1][3])};
+      uint32_t pl[4];
       if (split) {
-        mma16816<T>(o[2 * dn2], pl, b0, b1);
-        mma16816<T>(o[2 * dn2 + 1], pl, b2, b3);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          float h0, h1;
+          unpack2<T>(pa[a], h0, h1);
+          pl[a] = pack2<T>(pr[a / 2][2 * (a % 2)] - h0, pr[a / 2][2 * (a % 2) + 1] - h1);
+        }
+      }
+#pragma unroll
+      for (int dn2 = 0; dn2 < D / 16; ++dn2) {
+        const int mm = lane / 8;
+        const int key = koff + (mm % 2) * 8 + (lane % 8);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(swz<D>(vt, key, 2 * dn2 + mm / 2), b0, b1, b2, b3);
+        mma16816<T>(o[2 * dn2], pa, b0, b1);
+        mma16816<T>(o[2 * dn2 + 1], pa, b2, b3);
+        if (split) {
+          mma16816<T>(o[2 * dn2], pl, b0, b1);
+          mma16816<T>(o[2 * dn2 + 1], pl, b2, b3);
+        }
       }
     }
     __syncwarp();
@@ -285,7 +293,7 @@ __global__ void __launch_bounds__(128 * MT) vec_mma_fwd_kernel(const __grid_cons
     }
   }
   __syncthreads();
-  // Merge the four key quarters of each row block: this block's partial (M, L, O).
+  // Merge the key slices of each row block: this block's partial (M, L, O).
   float* cta_o = reinterpret_cast<float*>(sm + L::kCtaO);
   float* cta_m = reinterpret_cast<float*>(sm + L::kCtaM);
   float* cta_l = reinterpret_cast<float*>(sm + L::kCtaL);
@@ -293,10 +301,10 @@ __global__ void __launch_bounds__(128 * MT) vec_mma_fwd_kernel(const __grid_cons
     const int r = e / D, d = e % D, mtr = r / 16, lr = r % 16;
     float M = ninf();
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) M = fmaxf(M, part_m[(mtr + MT * q4) * 16 + lr]);
+    for (int q4 = 0; q4 < L::kSlices; ++q4) M = fmaxf(M, part_m[(mtr + MT * q4) * 16 + lr]);
     float Lsum = 0.f, O = 0.f;
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
+    for (int q4 = 0; q4 < L::kSlices; ++q4) {
       const int w = mtr + MT * q4;
       const float mw = part_m[w * 16 + lr];
       const float wgt = mw == ninf() ? 0.f : ex2(mw - M);
@@ -343,7 +351,7 @@ cudaError_t vec_mma_fwd_t(const Problem& p, cudaStream_t s) {
   const int chunk = ((p.Lkv + kCs - 1) / kCs + kKeys - 1) / kKeys * kKeys;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kCs, p.Hkv, p.B);
-  cfg.blockDim = dim3(128 * MT, 1, 1);
+  cfg.blockDim = dim3(128, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -363,6 +371,306 @@ cudaError_t vec_mma_fwd_any(const Problem& p, cudaStream_t s) {
   return two ? vec_mma_fwd_t<T, 64, 2>(p, s) : vec_mma_fwd_t<T, 64, 1>(p, s);
 }
 
+
+// ------------------------------------------------------------------ backward
+// Per 64-key tile (keys owned by this block; all G·Lq rows of the group):
+//   phase A (warp w: keys [16w, 16w+16)): S = Q·Kᵀ, dP = dO·Vᵀ on mma.sync;
+//            P = exp2(c·S − log2e·lse), dS = P∘(dP − δ) → shared memory (16-bit)
+//   phase C (warp w): dV = Pᵀ·dO and dK = scale·dSᵀ·Q for keys [16w, 16w+16), complete
+//            for these keys (every row of the group is here) and stored at once;
+//            dQ[:, w·D/4 : (w+1)·D/4) += dS·K accumulated in registers across tiles.
+// The dQ partials of the cluster's blocks are summed through distributed shared memory.
+constexpr int kBwdRing = 2;
+
+template <int D, int MT>
+struct VbLayout {
+  static constexpr int kTileBytes = kKeys * D * 2;
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kRows = 16 * MT;
+  static constexpr int kRowStride = (D + 8) * 2;          // padded: conflict-free ldmatrix
+  static constexpr int kPStride = (kKeys + 8) * 2;
+  static constexpr int kQ = kBwdRing * kStageBytes;       // [rows][D+8] 16-bit
+  static constexpr int kDo = kQ + kRows * kRowStride;
+  static constexpr int kP = kDo + kRows * kRowStride;     // [rows][64+8] 16-bit
+  static constexpr int kDs = kP + kRows * kPStride;
+  static constexpr int kVec = kDs + kRows * kPStride;     // nlse2[rows], ndelta[rows]
+  static constexpr int kBytes = kVec + 2 * kRows * 4;
+  static constexpr int kDq = 0;                           // after the loop: [rows][D] fp32
+  static_assert(kRows * D * 4 <= kBwdRing * kStageBytes, "dQ merge buffer must fit in the ring");
+};
+
+template <typename T, int D, int MT>
+__global__ void __launch_bounds__(128) vec_mma_bwd_kernel(const __grid_constant__ CUtensorMap tk,
+                                                         const __grid_constant__ CUtensorMap tv, Problem p,
+                                                         int chunk) {
+  using L = VbLayout<D, MT>;
+  constexpr int kWarps = 4;
+  extern __shared__ unsigned char smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t full[kBwdRing], empty[kBwdRing];
+  __shared__ int abort_flag;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int c = (int)cluster.block_rank();
+  const int b = blockIdx.z, g = blockIdx.y;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int R = p.G * p.Lq;
+  const int kv_end = p.causal ? min(p.Lkv, p.Lq) : p.Lkv;
+  const int j_begin = c * chunk, j_own_end = min(p.Lkv, j_begin + chunk);
+  const int j_end = min(kv_end, j_own_end);
+  const int ntiles = j_end > j_begin ? (j_end - j_begin + kKeys - 1) / kKeys : 0;
+  const WaitCtx wc{&abort_flag, 0, p.wait_limit_ns, p.err, kKidVecBwd};
+  const uint32_t ring = smem_u32(sm);
+  const uint32_t qs = smem_u32(sm + L::kQ), dos = smem_u32(sm + L::kDo);
+  const uint32_t ps = smem_u32(sm + L::kP), dss = smem_u32(sm + L::kDs);
+  float* nlse2 = reinterpret_cast<float*>(sm + L::kVec);
+  float* ndelta = nlse2 + L::kRows;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < kBwdRing; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  auto issue = [&](int t) {
+    const int s = t % kBwdRing;
+    mbar_arrive_expect_tx(&full[s], L::kStageBytes);
+    for (int cb = 0; cb < D / 64; ++cb) {
+      tma_load_3d(sm + s * L::kStageBytes + cb * (kKeys * 128), &tk, &full[s], cb * 64, j_begin + t * kKeys,
+                  b * p.Hkv + g);
+      tma_load_3d(sm + s * L::kStageBytes + L::kTileBytes + cb * (kKeys * 128), &tv, &full[s], cb * 64,
+                  j_begin + t * kKeys, b * p.Hkv + g);
+    }
+  };
+  int issued = 0;
+  if (threadIdx.x == 0)
+    for (; issued < min(kBwdRing, ntiles); ++issued) issue(issued);
+
+  // Stage Q and dO (zero rows past R); δ_r = Σ_d dO·O and −log2e·lse per row.
+  {
+    const T* qg = static_cast<const T*>(p.q);
+    const T* dog = static_cast<const T*>(p.dout);
+    for (int e = threadIdx.x; e < L::kRows * (D / 2); e += blockDim.x) {
+      const int r = e / (D / 2), d = 2 * (e % (D / 2));
+      uint32_t qv = 0u, dv = 0u;
+      if (r < R) {
+        const int64_t row = q_row(p, b, g * p.G + r / p.Lq, r % p.Lq);
+        qv = *reinterpret_cast<const uint32_t*>(qg + row * D + d);
+        dv = *reinterpret_cast<const uint32_t*>(dog + row * D + d);
+      }
+      *reinterpret_cast<uint32_t*>(sm + L::kQ + r * L::kRowStride + d * 2) = qv;
+      *reinterpret_cast<uint32_t*>(sm + L::kDo + r * L::kRowStride + d * 2) = dv;
+    }
+    for (int r = warp; r < L::kRows; r += kWarps) {
+      float acc = 0.f, nl = -__int_as_float(0x7f800000);
+      if (r < R) {
+        const int64_t row = q_row(p, b, g * p.G + r / p.Lq, r % p.Lq);
+        const T* op = static_cast<const T*>(p.o) + row * D;
+        for (int d = lane; d < D; d += 32) acc = fmaf(Elem<T>::to_f(op[d]), Elem<T>::to_f(dog[row * D + d]), acc);
+        nl = -p.lse[row] * kLog2e;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (lane == 0) {
+        ndelta[r] = -acc;
+        nlse2[r] = nl;
+      }
+    }
+  }
+  __syncthreads();
+
+  const float c2 = p.scale_log2;
+  constexpr int kDqTiles = D / 32;  // n-tiles of 8 dims in this warp's quarter of D
+  float dq[MT][kDqTiles][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < kDqTiles; ++nt) dq[mt][nt][0] = dq[mt][nt][1] = dq[mt][nt][2] = dq[mt][nt][3] = 0.f;
+  T* dkg = static_cast<T*>(p.dk) + kv_row(p, b, g, 0) * D;
+  T* dvg = static_cast<T*>(p.dv) + kv_row(p, b, g, 0) * D;
+  const int mm = lane / 8;
+
+  bool ok = true;
+  for (int t = 0; t < ntiles; ++t) {
+    const int s = t % kBwdRing;
+    ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (t / kBwdRing) & 1, wc));
+    if (!ok) break;
+    const uint32_t kt = ring + s * L::kStageBytes, vt = kt + L::kTileBytes;
+    const int tile_key0 = j_begin + t * kKeys;
+    // ---- phase A: S, dP for keys [16w, 16w+16) of the tile, all rows
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      float dp[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const int arow = 16 * mt + (mm % 2) * 8 + (lane % 8), acol = 16 * kk + (mm / 2) * 8;
+        uint32_t qa[4], da[4];
+        ldsm_x4(qs + arow * L::kRowStride + acol * 2, qa[0], qa[1], qa[2], qa[3]);
+        ldsm_x4(dos + arow * L::kRowStride + acol * 2, da[0], da[1], da[2], da[3]);
+        const int key = 16 * warp + (mm / 2) * 8 + (lane % 8);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(swz<D>(kt, key, 2 * kk + (mm % 2)), b0, b1, b2, b3);
+        mma16816<T>(sc[0], qa, b0, b1);
+        mma16816<T>(sc[1], qa, b2, b3);
+        ldsm_x4(swz<D>(vt, key, 2 * kk + (mm % 2)), b0, b1, b2, b3);
+        mma16816<T>(dp[0], da, b0, b1);
+        mma16816<T>(dp[1], da, b2, b3);
+      }
+      const int ra = 16 * mt + lane / 4, rb = ra + 8;
+      const float nla = nlse2[ra], nlb = nlse2[rb], nda = ndelta[ra], ndb = ndelta[rb];
+      const int ia = ra < R ? ra % p.Lq : 0, ib = rb < R ? rb % p.Lq : 0;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int kl = 16 * warp + 8 * nt + 2 * (lane % 4);  // key within the tile
+        float pv[4], dsv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = tile_key0 + kl + (e & 1);
+          const bool first = e < 2;
+          const bool vis = j < j_end && (!p.causal || j <= (first ? ia : ib));
+          const float x = fmaf(sc[nt][e], c2, first ? nla : nlb);
+          pv[e] = vis ? ex2(x) : 0.f;
+          dsv[e] = pv[e] * (dp[nt][e] + (first ? nda : ndb));
+        }
+        *reinterpret_cast<uint32_t*>(sm + L::kP + ra * L::kPStride + kl * 2) = pack2<T>(pv[0], pv[1]);
+        *reinterpret_cast<uint32_t*>(sm + L::kP + rb * L::kPStride + kl * 2) = pack2<T>(pv[2], pv[3]);
+        *reinterpret_cast<uint32_t*>(sm + L::kDs + ra * L::kPStride + kl * 2) = pack2<T>(dsv[0], dsv[1]);
+        *reinterpret_cast<uint32_t*>(sm + L::kDs + rb * L::kPStride + kl * 2) = pack2<T>(dsv[2], dsv[3]);
+      }
+    }
+    __syncthreads();
+    // ---- phase C (i): dV = Pᵀ·dO and dK = scale·dSᵀ·Q for keys [16w, 16w+16)
+#pragma unroll 1
+    for (int which = 0; which < 2; ++which) {
+      const uint32_t a_s = which == 0 ? ps : dss;
+      const uint32_t b_s = which == 0 ? dos : qs;
+      float acc[D / 8][4];
+#pragma unroll
+      for (int dn = 0; dn < D / 8; ++dn) acc[dn][0] = acc[dn][1] = acc[dn][2] = acc[dn][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < MT; ++ks) {
+        uint32_t a[4];
+        const int prow = 16 * ks + (mm / 2) * 8 + (lane % 8), pcol = 16 * warp + (mm % 2) * 8;
+        ldsm_x4_t(a_s + prow * L::kPStride + pcol * 2, a[0], a[1], a[2], a[3]);
+#pragma unroll
+        for (int dn2 = 0; dn2 < D / 16; ++dn2) {
+          const int brow = 16 * ks + (mm % 2) * 8 + (lane % 8), bcol = 16 * dn2 + (mm / 2) * 8;
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(b_s + brow * L::kRowStride + bcol * 2, b0, b1, b2, b3);
+          mma16816<T>(acc[2 * dn2], a, b0, b1);
+          mma16816<T>(acc[2 * dn2 + 1], a, b2, b3);
+        }
+      }
+      const float mul = which == 0 ? 1.f : p.scale;
+      T* dst = which == 0 ? dvg : dkg;
+      const int ja = tile_key0 + 16 * warp + lane / 4, jb = ja + 8;
+#pragma unroll
+      for (int dn = 0; dn < D / 8; ++dn) {
+        const int d = 8 * dn + 2 * (lane % 4);
+        if (ja < j_own_end)
+          *reinterpret_cast<uint32_t*>(dst + (int64_t)ja * D + d) = pack2<T>(acc[dn][0] * mul, acc[dn][1] * mul);
+        if (jb < j_own_end)
+          *reinterpret_cast<uint32_t*>(dst + (int64_t)jb * D + d) = pack2<T>(acc[dn][2] * mul, acc[dn][3] * mul);
+      }
+    }
+    // ---- phase C (ii): dQ[:, w·D/4 : (w+1)·D/4) += dS·K over this tile's 64 keys
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+      for (int kk = 0; kk < kKeys / 16; ++kk) {
+        uint32_t a[4];
+        const int arow = 16 * mt + (mm % 2) * 8 + (lane % 8), acol = 16 * kk + (mm / 2) * 8;
+        ldsm_x4(dss + arow * L::kPStride + acol * 2, a[0], a[1], a[2], a[3]);
+#pragma unroll
+        for (int np = 0; np < kDqTiles / 2; ++np) {
+          const int key = 16 * kk + (mm % 2) * 8 + (lane % 8);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(swz<D>(kt, key, (warp * D / 4) / 8 + 2 * np + mm / 2), b0, b1, b2, b3);
+          mma16816<T>(dq[mt][2 * np], a, b0, b1);
+          mma16816<T>(dq[mt][2 * np + 1], a, b2, b3);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (threadIdx.x == 0 && t + kBwdRing < ntiles) {
+      if (!mbar_wait(&empty[s], (t / kBwdRing) & 1, wc)) ok = false;
+      else issue(issued++);
+    }
+    __syncthreads();  // phase A of the next tile rewrites P and dS
+  }
+  if (threadIdx.x == 0 && (!ok || abort_flag)) {  // let copies still in flight land
+    for (int t = max(0, issued - kBwdRing); t < issued; ++t) {
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(&full[t % kBwdRing], (t / kBwdRing) & 1) && globaltimer() - t0 < 100000000ull) {
+      }
+    }
+  }
+  // Keys this block owns that no query can see (causal, j >= Lq) get zero gradients.
+  for (int64_t e = (int64_t)max(j_begin + ntiles * kKeys, j_begin) * D + threadIdx.x; e < (int64_t)j_own_end * D;
+       e += blockDim.x) {
+    dkg[e] = Elem<T>::from_f(0.f);
+    dvg[e] = Elem<T>::from_f(0.f);
+  }
+  __syncthreads();  // the ring is free: reuse it for the dQ partial of this block
+  float* cta_dq = reinterpret_cast<float*>(sm + L::kDq);
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < kDqTiles; ++nt) {
+      const int r = 16 * mt + lane / 4, d = warp * D / 4 + 8 * nt + 2 * (lane % 4);
+      cta_dq[r * D + d] = dq[mt][nt][0];
+      cta_dq[r * D + d + 1] = dq[mt][nt][1];
+      cta_dq[(r + 8) * D + d] = dq[mt][nt][2];
+      cta_dq[(r + 8) * D + d + 1] = dq[mt][nt][3];
+    }
+  cluster.sync();
+  constexpr int kSlice = D / kCs;
+  for (int e = threadIdx.x; e < R * kSlice; e += blockDim.x) {
+    const int r = e / kSlice, d = c * kSlice + e % kSlice;
+    float acc = 0.f;
+    for (int cc = 0; cc < kCs; ++cc) acc += cluster.map_shared_rank(cta_dq, cc)[r * D + d];
+    const int64_t row = q_row(p, b, g * p.G + r / p.Lq, r % p.Lq);
+    static_cast<T*>(p.dq)[row * D + d] = Elem<T>::from_f(acc * p.scale);
+  }
+  cluster.sync();
+}
+
+template <typename T, int D, int MT>
+cudaError_t vec_mma_bwd_t(const Problem& p, cudaStream_t s) {
+  CUtensorMap tk, tv;
+  if (!make_tmap_3d(&tk, p.k, D, p.Lkv, p.B * p.Hkv, kKeys) || !make_tmap_3d(&tv, p.v, D, p.Lkv, p.B * p.Hkv, kKeys))
+    return cudaErrorInvalidValue;
+  const int smem = VbLayout<D, MT>::kBytes + 1024;
+  auto kern = vec_mma_bwd_kernel<T, D, MT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int chunk = ((p.Lkv + kCs - 1) / kCs + kKeys - 1) / kKeys * kKeys;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kCs, p.Hkv, p.B);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, p, chunk);
+}
+
+template <typename T>
+cudaError_t vec_mma_bwd_any(const Problem& p, cudaStream_t s) {
+  const bool two = p.G * p.Lq > 16;
+  if (p.D == 128) return two ? vec_mma_bwd_t<T, 128, 2>(p, s) : vec_mma_bwd_t<T, 128, 1>(p, s);
+  return two ? vec_mma_bwd_t<T, 64, 2>(p, s) : vec_mma_bwd_t<T, 64, 1>(p, s);
+}
+
 }  // namespace
 
 bool vector_mma_supported(const Problem& p, int dtype) {
@@ -371,6 +679,10 @@ bool vector_mma_supported(const Problem& p, int dtype) {
 
 cudaError_t launch_vector_mma_fwd(const Problem& p, int dtype, cudaStream_t s) {
   return dtype == 2 ? vec_mma_fwd_any<__nv_bfloat16>(p, s) : vec_mma_fwd_any<__half>(p, s);
+}
+
+cudaError_t launch_vector_mma_bwd(const Problem& p, int dtype, cudaStream_t s) {
+  return dtype == 2 ? vec_mma_bwd_any<__nv_bfloat16>(p, s) : vec_mma_bwd_any<__half>(p, s);
 }
 
 }  // namespace sdpa
