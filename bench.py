@@ -401,36 +401,70 @@ def alu_peak_tflops(clocks):
 
 
 def run_e2e(torch, api, dev, stream, host_inputs, scale, steps, step_flops, world, barrier, dist):
-    """Same step from pinned host memory: H2D of q, k, v, dO; fwd + bwd; D2H of out, lse,
-    dq, dk, dv; all inside the timed region."""
+    """Same step end to end from pinned host memory through the public API: every step
+    copies q, k, v, dO host→device, runs forward + backward, and copies out, lse, dq, dk,
+    dv device→host, all inside the timed region.  Steps are software-pipelined over three
+    streams (copy in, compute, copy out) with two device buffer sets, so the copies of
+    one step overlap the compute of its neighbours."""
     pin = [t.pin_memory() for t in host_inputs]
-    q, k, v, do = (torch.empty_like(t, device=dev) for t in pin)
     W = WORKLOAD
-    out_h = torch.empty_like(pin[0]).pin_memory()
-    lse_h = torch.empty((W["B"], W["Hq"], W["Lq"]), dtype=torch.float32).pin_memory()
-    dq_h = torch.empty_like(pin[0]).pin_memory()
-    dk_h = torch.empty_like(pin[1]).pin_memory()
-    dv_h = torch.empty_like(pin[2]).pin_memory()
-    ws = torch.empty(max(16, api.workspace_bytes(q, k)), device=dev, dtype=torch.uint8)
-
-    def one():
-        for d, h in zip((q, k, v, do), pin):
-            d.copy_(h, non_blocking=True)
-        out, lse = api.attention_forward(q, k, v, scale=scale, is_causal=CAUSAL)
-        dq, dk, dv = api.attention_backward(q, k, v, out, do, lse, scale=scale,
-                                            is_causal=CAUSAL, workspace=ws)
-        for h, d in ((out_h, out), (lse_h, lse), (dq_h, dq), (dk_h, dk), (dv_h, dv)):
-            h.copy_(d, non_blocking=True)
-
+    outs_h = [torch.empty_like(pin[0]).pin_memory(),
+              torch.empty((W["B"], W["Hq"], W["Lq"]), dtype=torch.float32).pin_memory(),
+              torch.empty_like(pin[0]).pin_memory(), torch.empty_like(pin[1]).pin_memory(),
+              torch.empty_like(pin[2]).pin_memory()]
+    sets = []
+    for _ in range(2):
+        ins = [torch.empty_like(t, device=dev) for t in pin]
+        outs = [torch.empty_like(ins[0]), torch.empty((W["B"], W["Hq"], W["Lq"]), device=dev),
+                torch.empty_like(ins[0]), torch.empty_like(ins[1]), torch.empty_like(ins[2])]
+        ws = torch.empty(max(16, api.workspace_bytes(ins[0], ins[1])), device=dev, dtype=torch.uint8)
+        sets.append((ins, outs, ws))
+    s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     n = max(3, min(steps, 20))
-    for _ in range(3):
-        one()
+
+    def run(count, start_ev=None, end_ev=None):
+        comp_done, out_done = {}, {}
+        if start_ev is not None:
+            start_ev.record(s_in)
+            s_cmp.wait_event(start_ev)
+            s_out.wait_event(start_ev)
+        for i in range(count):
+            ins, outs, ws = sets[i % 2]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(comp_done[i - 2])
+                for d, h in zip(ins, pin):
+                    d.copy_(h, non_blocking=True)
+                in_done = torch.cuda.Event()
+                in_done.record(s_in)
+            with torch.cuda.stream(s_cmp):
+                s_cmp.wait_event(in_done)
+                if i >= 2:
+                    s_cmp.wait_event(out_done[i - 2])
+                q, k, v, do = ins
+                api.attention_forward(q, k, v, scale=scale, is_causal=CAUSAL, out=outs[0], lse=outs[1],
+                                      stream=s_cmp)
+                api.attention_backward(q, k, v, outs[0], do, outs[1], scale=scale, is_causal=CAUSAL,
+                                       workspace=ws, dq=outs[2], dk=outs[3], dv=outs[4], stream=s_cmp)
+                comp_done[i] = torch.cuda.Event()
+                comp_done[i].record(s_cmp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[i])
+                for h, d in zip(outs_h, outs):
+                    h.copy_(d, non_blocking=True)
+                out_done[i] = torch.cuda.Event()
+                out_done[i].record(s_out)
+        if end_ev is not None:
+            s_out.wait_event(comp_done[count - 1])
+            s_out.wait_stream(s_in)
+            end_ev.record(s_out)
+
+    run(3)
+    torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(n):
-        one()
-    e1.record(stream)
+    run(n, e0, e1)
+    torch.cuda.synchronize()
     barrier()
     ms = e0.elapsed_time(e1)
     t = torch.tensor([ms], device=dev, dtype=torch.float64)
@@ -438,50 +472,58 @@ def run_e2e(torch, api, dev, stream, host_inputs, scale, steps, step_flops, worl
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
     ms = float(t[0])
     h2d = sum(t.numel() * t.element_size() for t in pin)
-    d2h = sum(t.numel() * t.element_size() for t in (out_h, lse_h, dq_h, dk_h, dv_h))
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
     return {"value": world * step_flops * n / (ms / 1e3) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / n,
-            "steps": n}
+            "steps": n, "pipelined": "copy-in / compute / copy-out streams, 2 buffer sets"}
 
 
 def run_short_query(torch, api, _lib, dev, stream, hbm_peak):
-    """Short-query (vector) path, Lq=8, Lkv=8192, bf16: HBM GB/s of fwd and bwd."""
+    """Short-query (vector) path, B=4 Hq=32 Hkv=8 Lkv=8192 D=128 bf16, Lq in {1, 4, 8}:
+    HBM GB/s of forward and backward against the measured copy peak."""
     from scaled_dot_product_flash_gb300.inputs import Shape, draw
-    S = SHORT_QUERY
-    q, k, v, do = (t.to(dev) for t in draw(Shape(**S), 4, "bf16"))
-    scale = 1.0 / math.sqrt(S["D"])
+    res = {"workload": "bf16 short-query B=4 Hq=32 Hkv=8 Lkv=8192 D=128 non-causal, Lq in {1,4,8}",
+           "timing": "median of 20 calls, L2 flushed before each"}
     flush = torch.empty(L2_FLUSH_BYTES, device=dev, dtype=torch.uint8)
-    out, lse = api.attention_forward(q, k, v, scale=scale)
-    dq, dk, dv = api.attention_backward(q, k, v, out, do, lse, scale=scale)
-    fwd_t, bwd_t = [], []
-    for i in range(23):
-        flush.zero_()
-        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-        a.record(stream)
-        api.attention_forward(q, k, v, scale=scale, out=out, lse=lse)
-        b.record(stream)
-        api.attention_backward(q, k, v, out, do, lse, scale=scale, dq=dq, dk=dk, dv=dv)
-        c.record(stream)
-        if i >= 3:
-            fwd_t.append((a, b))
-            bwd_t.append((b, c))
-    torch.cuda.synchronize()
-    api.poll_status()
-    fms = statistics.median(a.elapsed_time(b) for a, b in fwd_t)
-    bms = statistics.median(a.elapsed_time(b) for a, b in bwd_t)
-    kv = S["B"] * S["Hkv"] * S["Lkv"] * S["D"] * 2
-    qb = S["B"] * S["Hq"] * S["Lq"] * S["D"] * 2
-    rows = S["B"] * S["Hq"] * S["Lq"] * 4
-    fwd_bytes = 2 * kv + 2 * qb + rows
-    bwd_bytes = 4 * kv + 4 * qb + rows
-    F = fwd_flops(**S, causal=False)
-    return {"workload": "bf16 short-query B=4 Hq=32 Hkv=8 Lq=8 Lkv=8192 D=128 non-causal",
+    for lq in (1, 4, 8):
+        S = dict(SHORT_QUERY, Lq=lq)
+        q, k, v, do = (t.to(dev) for t in draw(Shape(**S), 4, "bf16"))
+        scale = 1.0 / math.sqrt(S["D"])
+        out, lse = api.attention_forward(q, k, v, scale=scale)
+        dq, dk, dv = api.attention_backward(q, k, v, out, do, lse, scale=scale)
+        fwd_t, bwd_t = [], []
+        for i in range(23):
+            flush.zero_()
+            a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            a.record(stream)
+            api.attention_forward(q, k, v, scale=scale, out=out, lse=lse)
+            b.record(stream)
+            flush.zero_()
+            c0 = torch.cuda.Event(enable_timing=True)
+            c0.record(stream)
+            api.attention_backward(q, k, v, out, do, lse, scale=scale, dq=dq, dk=dk, dv=dv)
+            c.record(stream)
+            if i >= 3:
+                fwd_t.append((a, b))
+                bwd_t.append((c0, c))
+        torch.cuda.synchronize()
+        api.poll_status()
+        fms = statistics.median(a.elapsed_time(b) for a, b in fwd_t)
+        bms = statistics.median(a.elapsed_time(b) for a, b in bwd_t)
+        kv = S["B"] * S["Hkv"] * S["Lkv"] * S["D"] * 2
+        qb = S["B"] * S["Hq"] * S["Lq"] * S["D"] * 2
+        rows = S["B"] * S["Hq"] * S["Lq"] * 4
+        fwd_bytes = 2 * kv + 2 * qb + rows
+        bwd_bytes = 4 * kv + 4 * qb + rows
+        F = fwd_flops(**S, causal=False)
+        res[f"Lq{lq}"] = {
             "fwd_ms": fms, "bwd_ms": bms,
             "fwd_gbs": fwd_bytes / (fms / 1e3) / 1e9, "bwd_gbs": bwd_bytes / (bms / 1e3) / 1e9,
             "fwd_frac_hbm": fwd_bytes / (fms / 1e3) / 1e9 / hbm_peak,
             "bwd_frac_hbm": bwd_bytes / (bms / 1e3) / 1e9 / hbm_peak,
             "fwd_tflops": F / (fms / 1e3) / 1e12, "bwd_tflops": 2.5 * F / (bms / 1e3) / 1e12,
             "algorithmic_bytes": {"fwd": fwd_bytes, "bwd": bwd_bytes}}
+    return res
 
 
 if __name__ == "__main__":
