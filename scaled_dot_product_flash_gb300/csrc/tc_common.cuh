@@ -184,6 +184,13 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The same descriptor with its start address moved by `bytes` (a multiple of 16).  The start
+// field holds (address & 0x3FFFF) >> 4 in the low 14 bits, so for shared-memory addresses
+// below 256 KB the sum never carries out of the field.
+__device__ __forceinline__ uint64_t sdesc_advance(uint64_t desc, uint32_t bytes) {
+  return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
 // Instruction descriptor of tcgen05.mma .kind::f16 with fp32 accumulation:
 //   bits 4..5 D format (1 = f32); bits 7..9 A format, 10..12 B format (0 = f16, 1 = bf16);
 //   bit 15 A MN-major, bit 16 B MN-major; bits 17..22 N >> 3; bits 24..28 M >> 4.
@@ -217,6 +224,35 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
                : "memory");
+}
+
+// Warp-wide forms: every lane of the warp executes the call with the same operands and one
+// lane, picked by elect.sync (the same lane on every call while the whole warp is active),
+// issues the instruction.  Keeping the issuing loop on all 32 lanes lets the operands
+// stay warp-uniform; issuing from inside a lane-0 branch measured at 150-160 cycles per
+// 128x128x16 MMA once any operand varied at run time, against 64 cycles in this form.
+__device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_w(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar))
+      : "memory");
 }
 
 // ------------------------------------------------------------------ register split

@@ -55,6 +55,7 @@ struct FwdBars {
   uint64_t p_full[kQTiles];
   uint64_t o_done[kQTiles];
   uint64_t mma_done[kQTiles];
+  uint64_t turn[kQTiles];  // exponential pass of Q tile w may start (alternates 0, 1, 0, ...)
   uint32_t tmem_base;
   int abort;
 };
@@ -249,6 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bars.mma_done[0], 1);
     mbar_init(&bars.mma_done[1], 1);
+    mbar_init(&bars.turn[0], 4);  // one arrival per warp of the other warpgroup
+    mbar_init(&bars.turn[1], 4);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -293,55 +296,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-    // One MMA issuer per Q tile, so that each tile's chain S → softmax → PV → S advances
-    // at its own pace and neither issuer waits on the other tile's softmax.
-    const int w = warp - kMmaWarp;
-    if (lane == 0) {
-      bool ok = mbar_wait(&bars.q_full, 0, wc);
-      tc_fence_after();
-      const uint32_t qa = smem_u32(sm + L::kQOff) + w * L::kTileBytes;
-      const uint32_t ring_s = smem_u32(sm + L::kRingOff);
-      for (int j = 0; ok && j < nmax; ++j) {
-        const int sk = (2 * j) % kStages, sv = (2 * j + 1) % kStages;
-        const uint32_t phk = ((2 * j) / kStages) & 1, phv = ((2 * j + 1) / kStages) & 1;
-        // Every stage use gets exactly one arrival from each issuer, made only after the
-        // stage was filled for this use, even by an issuer whose tile needs no MMA here.
-        if (!(ok = mbar_wait(&bars.kv_full[sk], phk, wc))) break;
-        if (j < nkv[w]) {
-          if (j > 0 && !(ok = mbar_wait(&bars.o_done[w], (j - 1) & 1, wc))) break;  // P_w(j-1) consumed
-          tc_fence_after();
-          const uint32_t kb = ring_s + sk * L::kTileBytes;
+    // One MMA issuer warp per Q tile, so that each tile's chain S → softmax → PV → S
+    // advances at its own pace.  The whole warp runs the loop; one lane issues.
+    constexpr unsigned kAll = 0xffffffffu;
+    const int w = __shfl_sync(kAll, warp - kMmaWarp, 0);
+    const int nkv_w = w == 0 ? nkv[0] : nkv[1];
+    bool ok = __all_sync(kAll, mbar_wait(&bars.q_full, 0, wc));
+    tc_fence_after();
+    const uint64_t qd = sdesc_sw128(smem_u32(sm + L::kQOff) + w * L::kTileBytes, 16, 1024);
+    const uint32_t ring_s = smem_u32(sm + L::kRingOff);
+    const uint32_t s_tm = tbase + L::kSCol + w * 128, o_tm = tbase + L::kOCol + w * D;
+    const int tile_row0 = row0 + w * kBM;
+    for (int j = 0; ok && j < nmax; ++j) {
+      const int sk = (2 * j) % kStages, sv = (2 * j + 1) % kStages;
+      const uint32_t phk = ((2 * j) / kStages) & 1, phv = ((2 * j + 1) / kStages) & 1;
+      // Every stage use gets exactly one arrival from each issuer, made only after the
+      // stage was filled for this use, even by an issuer whose tile needs no MMA here.
+      if (!(ok = __all_sync(kAll, mbar_wait(&bars.kv_full[sk], phk, wc)))) break;
+      if (j < nkv_w) {
+        if (j > 0 && !(ok = __all_sync(kAll, mbar_wait(&bars.o_done[w], (j - 1) & 1, wc)))) break;
+        tc_fence_after();  // P_w(j-1) consumed: S_w may be overwritten
+        const uint64_t kd = sdesc_sw128(ring_s + sk * L::kTileBytes, 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-            mma_ss(tbase + L::kSCol + w * 128, sdesc_sw128(qa + off, 16, 1024),
-                   sdesc_sw128(kb + off, 16, 1024), kIdS, kk > 0);
-          }
-          mma_commit(&bars.s_full[w]);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+          mma_ss_w(s_tm, sdesc_advance(qd, off), sdesc_advance(kd, off), kIdS, kk > 0);
         }
-        mma_commit(&bars.kv_empty[sk]);  // one of the stage's two arrivals
-        if (!(ok = mbar_wait(&bars.kv_full[sv], phv, wc))) break;
-        if (j < nkv[w]) {
-          if (!(ok = mbar_wait(&bars.p_full[w], j & 1, wc))) break;
-          tc_fence_after();
-          const uint32_t vb = ring_s + sv * L::kTileBytes;
+        mma_commit_w(&bars.s_full[w]);
+      }
+      mma_commit_w(&bars.kv_empty[sk]);  // one of the stage's two arrivals
+      if (!(ok = __all_sync(kAll, mbar_wait(&bars.kv_full[sv], phv, wc)))) break;
+      if (j < nkv_w) {
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.p_full[w], j & 1, wc)))) break;
+        tc_fence_after();
+        const uint64_t vd = sdesc_sw128(ring_s + sv * L::kTileBytes, 16384, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts_w(o_tm, s_tm + kk * 8, sdesc_advance(vd, kk * 2048), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+        if (split_tile(p, j, tile_row0)) {  // remainder of P, columns [64, 128)
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
-            mma_ts(tbase + L::kOCol + w * D, tbase + L::kSCol + w * 128 + kk * 8,
-                   sdesc_sw128(vb + kk * 2048, 16384, 1024), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-          if (split_tile(p, j, row0 + w * kBM)) {  // remainder of P, columns [64, 128)
-#pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk)
-              mma_ts(tbase + L::kOCol + w * D, tbase + L::kSCol + w * 128 + 64 + kk * 8,
-                     sdesc_sw128(vb + kk * 2048, 16384, 1024), kIdO, 1u);
-          }
-          mma_commit(&bars.o_done[w]);
+            mma_ts_w(o_tm, s_tm + 64 + kk * 8, sdesc_advance(vd, kk * 2048), kIdO, 1u);
         }
-        mma_commit(&bars.kv_empty[sv]);
+        mma_commit_w(&bars.o_done[w]);
       }
-      mma_commit(&bars.mma_done[w]);
-      drain_wait(&bars.mma_done[w], 0, 100000000ull);
+      mma_commit_w(&bars.kv_empty[sv]);
     }
+    mma_commit_w(&bars.mma_done[w]);
+    drain_wait(&bars.mma_done[w], 0, 100000000ull);
   } else if (warp < 8) {
     // Softmax warpgroups.
     const int w = warp / 4, quarter = warp % 4;
@@ -353,6 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tile_row0 = row0 + w * kBM;
     float m = neg_inf(), l = 0.f;
     bool ok = true;
+    // The two warpgroups take turns at the exponential pass (0, 1, 0, 1, ... while both
+    // tiles have KV tiles left), so the pass of one tile has the multi-function units to
+    // itself while the tensor core works on the other tile's PV and next S.
+    const int nboth = min(nkv[0], nkv[1]);
     for (int j = 0; j < nkv[w]; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[w], j & 1, wc));
       if (!ok) break;
@@ -384,6 +390,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tmem_st_wait();
       }
+      if (j < nboth && (w == 1 || j > 0)) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars.turn[w], (w == 1 ? j : j - 1) & 1, wc));
+        if (!ok) break;
+      }
       // Pass 2: P = exp2(c·s − m), row sum, P packed to 16 bits over S's first 64 columns.
       if (split_tile(p, j, tile_row0))
         l += softmax_pass2_split<T>(s_addr, c, -m, k0, i, p);
@@ -394,6 +404,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars.p_full[w]);
+      if (j < nboth - w) {  // hand the turn to the other tile
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.turn[1 - w]);
+      }
     }
     if (ok && nkv[w] > 0)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_done[w], (nkv[w] - 1) & 1, wc));
