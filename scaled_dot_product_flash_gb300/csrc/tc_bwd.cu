@@ -111,12 +111,14 @@ __device__ __forceinline__ void init_bars(BwdBars& bars) {
 }
 
 // Issues C[tmem] = A·Bᵀ for two [128 x D] K-major tiles in shared memory (N = 128).
+// Called by all 32 lanes of the issuing warp; one elected lane issues.
 template <int D>
 __device__ __forceinline__ void mma_scores(uint32_t c_tmem, uint32_t a_s, uint32_t b_s, uint32_t idesc) {
+  const uint64_t ad = sdesc_sw128(a_s, 16, 1024), bd = sdesc_sw128(b_s, 16, 1024);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = (kk / 4) * BwdLayout<D>::kCbStride + (kk % 4) * 32;
-    mma_ss(c_tmem, sdesc_sw128(a_s + off, 16, 1024), sdesc_sw128(b_s + off, 16, 1024), idesc, kk > 0);
+    mma_ss_w(c_tmem, sdesc_advance(ad, off), sdesc_advance(bd, off), idesc, kk > 0);
   }
 }
 
@@ -125,10 +127,11 @@ __device__ __forceinline__ void mma_scores(uint32_t c_tmem, uint32_t a_s, uint32
 template <int D>
 __device__ __forceinline__ void mma_accumulate(uint32_t acc_tmem, uint32_t a_tmem, uint32_t b_s,
                                                uint32_t idesc, bool first) {
+  const uint64_t bd = sdesc_sw128(b_s, BwdLayout<D>::kCbStride, 1024);
 #pragma unroll
   for (int kk = 0; kk < kBlk / 16; ++kk)
-    mma_ts(acc_tmem, a_tmem + packed_col(kk), sdesc_sw128(b_s + kk * 2048, BwdLayout<D>::kCbStride, 1024),
-           idesc, (!first || kk > 0) ? 1u : 0u);
+    mma_ts_w(acc_tmem, a_tmem + packed_col(kk), sdesc_advance(bd, kk * 2048), idesc,
+             (!first || kk > 0) ? 1u : 0u);
 }
 
 // ================================================================== dK / dV
@@ -219,34 +222,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Two independent chains, one issuer each: warp 9 issues Sᵀ and dV (TMEM region X),
     // warp 10 issues dPᵀ and dK (region Y), so Sᵀ of the next block can start as soon as
     // dV has consumed Pᵀ even while dK still waits for dSᵀ.
-    const bool chain_x = warp == kMmaWarp;
-    if (lane == 0) {
-      bool ok = mbar_wait(&bars.own_full, 0, wc);
+    constexpr unsigned kAll = 0xffffffffu;
+    const bool chain_x = __shfl_sync(kAll, warp, 0) == kMmaWarp;
+    bool ok = __all_sync(kAll, mbar_wait(&bars.own_full, 0, wc));
+    tc_fence_after();
+    const uint32_t own_s = smem_u32(sm + (chain_x ? L::kOwnA : L::kOwnB));  // K or V
+    const uint32_t col = chain_x ? kColX : kColY;
+    const uint32_t acc = chain_x ? kColDv : kColDk;
+    uint64_t* freed = chain_x ? &bars.x_free : &bars.y_free;
+    uint64_t* ready = chain_x ? &bars.p_ready : &bars.ds_ready;
+    uint64_t* scores_done = chain_x ? &bars.s_full[0] : &bars.dp_full;
+    for (int n = 0; ok && n < total; ++n) {
+      const int s = n % kStages;
+      const uint32_t q_s = smem_u32(sm + L::kRing + s * L::kStageBytes), do_s = q_s + L::kTileBytes;
+      if (!(ok = __all_sync(kAll, mbar_wait(&bars.ring_full[s], (n / kStages) & 1, wc)))) break;
+      if (n > 0 && !(ok = __all_sync(kAll, mbar_wait(freed, (n - 1) & 1, wc)))) break;
       tc_fence_after();
-      const uint32_t own_s = smem_u32(sm + (chain_x ? L::kOwnA : L::kOwnB));  // K or V
-      const uint32_t col = chain_x ? kColX : kColY;
-      const uint32_t acc = chain_x ? kColDv : kColDk;
-      uint64_t* freed = chain_x ? &bars.x_free : &bars.y_free;
-      uint64_t* ready = chain_x ? &bars.p_ready : &bars.ds_ready;
-      uint64_t* scores_done = chain_x ? &bars.s_full[0] : &bars.dp_full;
-      for (int n = 0; ok && n < total; ++n) {
-        const int s = n % kStages;
-        const uint32_t q_s = smem_u32(sm + L::kRing + s * L::kStageBytes), do_s = q_s + L::kTileBytes;
-        if (!(ok = mbar_wait(&bars.ring_full[s], (n / kStages) & 1, wc))) break;
-        if (n > 0 && !(ok = mbar_wait(freed, (n - 1) & 1, wc))) break;
-        tc_fence_after();
-        mma_scores<D>(tbase + col, own_s, chain_x ? q_s : do_s, kIdS);  // Sᵀ = K·Qᵀ or dPᵀ = V·dOᵀ
-        mma_commit(scores_done);
-        if (!(ok = mbar_wait(ready, n & 1, wc))) break;
-        tc_fence_after();
-        // dV += Pᵀ·dO or dK += dSᵀ·Q
-        mma_accumulate<D>(tbase + acc, tbase + col, chain_x ? do_s : q_s, kIdAcc, n == 0);
-        mma_commit(freed);
-        mma_commit(&bars.ring_empty[s]);  // one of the stage's two arrivals
-      }
-      mma_commit(&bars.acc_done);
-      drain_wait(&bars.acc_done, 0, 100000000ull);
+      mma_scores<D>(tbase + col, own_s, chain_x ? q_s : do_s, kIdS);  // Sᵀ = K·Qᵀ or dPᵀ = V·dOᵀ
+      mma_commit_w(scores_done);
+      if (!(ok = __all_sync(kAll, mbar_wait(ready, n & 1, wc)))) break;
+      tc_fence_after();
+      // dV += Pᵀ·dO or dK += dSᵀ·Q
+      mma_accumulate<D>(tbase + acc, tbase + col, chain_x ? do_s : q_s, kIdAcc, n == 0);
+      mma_commit_w(freed);
+      mma_commit_w(&bars.ring_empty[s]);  // one of the stage's two arrivals
     }
+    mma_commit_w(&bars.acc_done);
+    drain_wait(&bars.acc_done, 0, 100000000ull);
   } else {
     // ---------------------------------------------------------------- element warps
     const int w = warp / 4, quarter = warp % 4;
@@ -481,48 +483,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-    // Two issuers: warp 9 issues S and dQ, warp 10 issues dP, each at its own pace.
-    if (lane == 0) {
-      bool ok = mbar_wait(&bars.own_full, 0, wc);
-      tc_fence_after();
-      const uint32_t q_s = smem_u32(sm + L::kQ), do_s = smem_u32(sm + L::kDo);
-      const uint32_t k_s = smem_u32(sm + L::kK), v_s = smem_u32(sm + L::kV);
-      if (warp == kMmaWarp) {
-        // S(n) = Q·K(n)ᵀ into S buffer n % 2 (free once dQ(n-2) has read dS(n-2) from it).
-        auto issue_s = [&](int n) -> bool {
-          if (!mbar_wait(&bars.k_full[n % kKStages], (n / kKStages) & 1, wc)) return false;
-          if (n >= 2 && !mbar_wait(&bars.dq_done[n % 2], ((n - 2) / 2) & 1, wc)) return false;
-          tc_fence_after();
-          mma_scores<D>(tbase + kColS0 + 128 * (n % 2), q_s, k_s + (n % kKStages) * L::kTileBytes, kIdS);
-          mma_commit(&bars.s_full[n % 2]);
-          return true;
-        };
-        if (ok && total > 0) ok = issue_s(0);
-        if (ok && total > 1) ok = issue_s(1);
-        for (int n = 0; ok && n < total; ++n) {
-          if (!(ok = mbar_wait(&bars.ds_ready, n & 1, wc))) break;
-          tc_fence_after();
-          // dQ += dS·K: B = the K block read MN-major.
-          mma_accumulate<D>(tbase + kColDq, tbase + kColS0 + 128 * (n % 2),
-                            k_s + (n % kKStages) * L::kTileBytes, kIdAcc, n == 0);
-          mma_commit(&bars.dq_done[n % 2]);
-          mma_commit(&bars.k_empty[n % kKStages]);
-          if (n + 2 < total && !(ok = issue_s(n + 2))) break;
-        }
-      } else {
-        // dP(n) = dO·V(n)ᵀ into the dP buffer (free once the element warps have read dP(n-1)).
-        for (int n = 0; ok && n < total; ++n) {
-          if (!(ok = mbar_wait(&bars.v_full[n % kVStages], (n / kVStages) & 1, wc))) break;
-          if (n >= 1 && !(ok = mbar_wait(&bars.dp_free, (n - 1) & 1, wc))) break;
-          tc_fence_after();
-          mma_scores<D>(tbase + kColDp, do_s, v_s + (n % kVStages) * L::kTileBytes, kIdS);
-          mma_commit(&bars.dp_full);
-          mma_commit(&bars.v_empty[n % kVStages]);
-        }
+    // Two issuers: warp 9 issues S and dQ, warp 10 issues dP, each at its own pace.  All
+    // lanes of an issuer warp run its loop; one elected lane issues.
+    constexpr unsigned kAll = 0xffffffffu;
+    bool ok = __all_sync(kAll, mbar_wait(&bars.own_full, 0, wc));
+    tc_fence_after();
+    const uint32_t q_s = smem_u32(sm + L::kQ), do_s = smem_u32(sm + L::kDo);
+    const uint32_t k_s = smem_u32(sm + L::kK), v_s = smem_u32(sm + L::kV);
+    if (__shfl_sync(kAll, warp, 0) == kMmaWarp) {
+      // S(n) = Q·K(n)ᵀ into S buffer n % 2 (free once dQ(n-2) has read dS(n-2) from it).
+      auto issue_s = [&](int n) -> bool {
+        if (!__all_sync(kAll, mbar_wait(&bars.k_full[n % kKStages], (n / kKStages) & 1, wc))) return false;
+        if (n >= 2 && !__all_sync(kAll, mbar_wait(&bars.dq_done[n % 2], ((n - 2) / 2) & 1, wc))) return false;
+        tc_fence_after();
+        mma_scores<D>(tbase + kColS0 + 128 * (n % 2), q_s, k_s + (n % kKStages) * L::kTileBytes, kIdS);
+        mma_commit_w(&bars.s_full[n % 2]);
+        return true;
+      };
+      if (ok && total > 0) ok = issue_s(0);
+      if (ok && total > 1) ok = issue_s(1);
+      for (int n = 0; ok && n < total; ++n) {
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.ds_ready, n & 1, wc)))) break;
+        tc_fence_after();
+        // dQ += dS·K: B = the K block read MN-major.
+        mma_accumulate<D>(tbase + kColDq, tbase + kColS0 + 128 * (n % 2),
+                          k_s + (n % kKStages) * L::kTileBytes, kIdAcc, n == 0);
+        mma_commit_w(&bars.dq_done[n % 2]);
+        mma_commit_w(&bars.k_empty[n % kKStages]);
+        if (n + 2 < total && !(ok = issue_s(n + 2))) break;
       }
-      mma_commit(&bars.acc_done);
-      drain_wait(&bars.acc_done, 0, 100000000ull);
+    } else {
+      // dP(n) = dO·V(n)ᵀ into the dP buffer (free once the element warps have read dP(n-1)).
+      for (int n = 0; ok && n < total; ++n) {
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.v_full[n % kVStages], (n / kVStages) & 1, wc)))) break;
+        if (n >= 1 && !(ok = __all_sync(kAll, mbar_wait(&bars.dp_free, (n - 1) & 1, wc)))) break;
+        tc_fence_after();
+        mma_scores<D>(tbase + kColDp, do_s, v_s + (n % kVStages) * L::kTileBytes, kIdS);
+        mma_commit_w(&bars.dp_full);
+        mma_commit_w(&bars.v_empty[n % kVStages]);
+      }
     }
+    mma_commit_w(&bars.acc_done);
+    drain_wait(&bars.acc_done, 0, 100000000ull);
   } else {
     const int w = warp / 4, quarter = warp % 4;
     const int i = i0 + quarter * 32 + lane;  // this thread's query
