@@ -1,14 +1,18 @@
 // Tensor-core forward (fp16/bf16, D in {64, 128}): TMA + tcgen05 + TMEM.
 //
 // One block computes 256 query rows (two 128-row Q tiles) of one (batch, head) against
-// the keys of its KV head (h / G).  Warp roles:
+// the keys of its KV head (h / G).  Warp roles (384 threads):
 //   warps 0-3 / 4-7  softmax warpgroup of Q tile 0 / 1: thread = one query row = one TMEM
 //                    lane; online softmax in the log2 domain ("[Metal] Add Flash Attention
 //                    VJP for training", section "Implementation Notes": log2 domain)
 //   warp 8           TMA producer: Q tiles once, then K_j, V_j tiles into a 4-stage ring
-//   warps 9 / 10     tcgen05 issuers (one thread each) for Q tile 0 / 1; warp 9 owns TMEM
-// Each softmax thread reads its 128 scores twice from TMEM (pass 1: row maximum; pass 2:
-// exponentials), which keeps it far below the register limit of a 320-thread block.
+//   warps 9 / 10     tcgen05 issuers for Q tile 0 / 1 (whole warp runs the loop, one
+//                    elected lane issues); warp 9 owns TMEM
+//   warp 11          idle (completes warpgroup 2 for the register split)
+// setmaxnreg moves registers from warpgroup 2 to the softmax warpgroups, so a softmax
+// thread holds its row's 128 scores in registers after one TMEM round trip and computes
+// the row maximum and the exponentials from there.  The two softmax warpgroups take turns
+// at the exponential pass, so one tile's pass overlaps the other tile's MMAs.
 // Tensor memory (512 columns, fp32): S_w = Q_w·K_jᵀ at columns [128w, 128w+128); P_w is
 // written back over the first 64 columns of S_w as packed 16-bit pairs and read from TMEM
 // as the A operand of O_w += P_w·V_j, with O_w at columns [256 + D·w, 256 + D·(w+1)).
@@ -20,7 +24,8 @@
 // add an error comparable to the output's own rounding.  For that one KV tile P is split
 // into a 16-bit head and a 16-bit remainder (written to S columns [64, 128)) and both
 // are multiplied into O, so P enters O with ~16 extra bits.
-// Epilogue: O / l rounded to the element type, lse = ln2·(m + log2 l) (natural log).
+// Epilogue: O / l rounded to the element type and staged in the tile's (now unused) Q
+// buffer, then written by bulk tensor stores; lse = ln2·(m + log2 l) (natural log).
 #include "launch.h"
 #include "tc_common.cuh"
 
@@ -32,9 +37,15 @@ constexpr int kBM = 128;      // rows per Q tile
 constexpr int kBN = 128;      // keys per KV tile
 constexpr int kQTiles = 2;    // Q tiles per block
 constexpr int kStages = 4;    // K/V ring stages (each one [kBN x D] tile)
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;    // warps 0-7 softmax, 8 producer, 9-10 MMA issuers, 11 idle
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+// Register split (setmaxnreg): the block launches with 168 registers a thread (65,536 / 384
+// rounded down to a multiple of 8, 64,512 in all); warpgroup 2 (producer, issuers, idle
+// warp) drops to 56 and the softmax warpgroups rise to 224: 128·56 + 256·224 = 64,512.
+constexpr int kRegsLow = 56;
+constexpr int kRegsHigh = 224;
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * 168, "register split exceeds the launch");
 constexpr float kRescale = 8.f;  // log2 of the largest exponential allowed before rescaling
 
 template <int D>
@@ -72,74 +83,61 @@ __device__ __forceinline__ bool split_tile(const Problem& p, int j, int tile_row
   return j == 0 && (tile_row0 == 0 || p.Lkv <= kBN);
 }
 
-__device__ __forceinline__ bool visible(const Problem& p, int key, int i) {
-  return key < p.Lkv && (!p.causal || key <= i);
+// Number of leading keys of the tile starting at k0 that row i may see: key k0 + e is
+// visible iff e < lim (keys past Lkv are padding; under the causal mask key <= i).
+__device__ __forceinline__ int visible_keys(const Problem& p, int k0, int i) {
+  int lim = min(p.Lkv - k0, kBN);
+  if (p.causal) lim = min(lim, i - k0 + 1);
+  return lim;
 }
 
-// First softmax pass of one row over a 128-key tile: the maximum of the scaled scores
-// (64 score columns per TMEM round trip; three-input max to halve the instructions).
-// Without a mask the raw maximum (or minimum, for a negative scale) is scaled once.
+// Row maximum of the scaled scores of a 128-key tile held in registers (three-input max):
+// the maximum raw score (the minimum for a negative scale) over the visible keys e < lim,
+// scaled once.  A row that sees no key of the tile gets -inf.
 template <bool kMask>
-__device__ __forceinline__ float row_max(uint32_t s_addr, float c, int k0, int i, const Problem& p) {
-  float acc[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
-  const bool cpos = c >= 0.f;
-#pragma unroll 1
-  for (int h2 = 0; h2 < 2; ++h2) {
-    uint32_t sa[32], sb[32];
-    tmem_ld32(s_addr + h2 * 64, sa);
-    tmem_ld32(s_addr + h2 * 64 + 32, sb);
-    tmem_ld_wait();
-    if constexpr (kMask) {
-      const int kb = k0 + h2 * 64;
+__device__ __forceinline__ float tile_max(const uint32_t (&sv)[kBN], float c, int lim) {
+  constexpr int kH = kBN / 2;
+  if (kMask && lim <= 0) return neg_inf();
+  float acc[4];
+  if (c >= 0.f) {
+    acc[0] = acc[1] = acc[2] = acc[3] = neg_inf();
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const float xa = visible(p, kb + e, i) ? __uint_as_float(sa[e]) * c : neg_inf();
-        const float xb = visible(p, kb + 32 + e, i) ? __uint_as_float(sb[e]) * c : neg_inf();
-        acc[e % 4] = fmax3(acc[e % 4], xa, xb);
-      }
-    } else if (cpos) {
-#pragma unroll
-      for (int e = 0; e < 32; ++e)
-        acc[e % 4] = fmax3(acc[e % 4], __uint_as_float(sa[e]), __uint_as_float(sb[e]));
-    } else {
-      if (h2 == 0) acc[0] = acc[1] = acc[2] = acc[3] = -neg_inf();
-#pragma unroll
-      for (int e = 0; e < 32; ++e)
-        acc[e % 4] = fmin3(acc[e % 4], __uint_as_float(sa[e]), __uint_as_float(sb[e]));
+    for (int e = 0; e < kH; ++e) {
+      const float xa = (!kMask || e < lim) ? __uint_as_float(sv[e]) : neg_inf();
+      const float xb = (!kMask || kH + e < lim) ? __uint_as_float(sv[kH + e]) : neg_inf();
+      acc[e % 4] = fmax3(acc[e % 4], xa, xb);
     }
+    return fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3])) * c;
   }
-  if constexpr (kMask) return fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3]));
-  if (cpos) return fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3])) * c;
+  acc[0] = acc[1] = acc[2] = acc[3] = -neg_inf();
+#pragma unroll
+  for (int e = 0; e < kH; ++e) {
+    const float xa = (!kMask || e < lim) ? __uint_as_float(sv[e]) : -neg_inf();
+    const float xb = (!kMask || kH + e < lim) ? __uint_as_float(sv[kH + e]) : -neg_inf();
+    acc[e % 4] = fmin3(acc[e % 4], xa, xb);
+  }
   return fminf(fminf(acc[0], acc[1]), fminf(acc[2], acc[3])) * c;
 }
 
-// Second softmax pass of one row over a 128-key tile: exponentials, their sum (returned),
-// and P packed to 16 bits into TMEM columns [0, 64) of the S tile.  Each round trip reads
-// 64 score columns and writes the 32 packed columns they produce (columns already read).
-// Pairs of columns go through packed f32x2 FMA/ADD: about 2.5 instructions per score.
+// Exponentials of a 128-key tile held in registers: returns their sum and writes P packed
+// to 16 bits into TMEM columns [0, 64) of the S tile (column q holds keys 2q and 2q + 1).
 template <typename T, bool kMask>
-__device__ __forceinline__ float softmax_pass2(uint32_t s_addr, float c, float neg_m, int k0, int i,
-                                               const Problem& p) {
+__device__ __forceinline__ float exp_pass(const uint32_t (&sv)[kBN], uint32_t s_addr, float c, float neg_m,
+                                          int lim) {
   const uint64_t cc = f2pack(c, c), nm = f2pack(neg_m, neg_m);
   uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
-#pragma unroll 1
-  for (int h2 = 0; h2 < 2; ++h2) {
-    uint32_t sa[32], sb[32];
-    tmem_ld32(s_addr + h2 * 64, sa);
-    tmem_ld32(s_addr + h2 * 64 + 32, sb);
-    tmem_ld_wait();
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
     uint32_t pk[32];
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
-      const uint32_t* src = e < 16 ? sa : sb;
-      const int ee = e % 16;
-      uint64_t xx = ffma2(f2pack(__uint_as_float(src[2 * ee]), __uint_as_float(src[2 * ee + 1])), cc, nm);
+      const int col = 64 * h + 2 * e;
+      uint64_t xx = ffma2(f2pack(__uint_as_float(sv[col]), __uint_as_float(sv[col + 1])), cc, nm);
       if constexpr (kMask) {
-        const int key = k0 + h2 * 64 + 2 * e;
         float x0, x1;
         f2unpack(xx, x0, x1);
-        if (!visible(p, key, i)) x0 = neg_inf();
-        if (!visible(p, key + 1, i)) x1 = neg_inf();
+        if (col >= lim) x0 = neg_inf();
+        if (col + 1 >= lim) x1 = neg_inf();
         xx = f2pack(x0, x1);
       }
       float p0, p1;
@@ -148,7 +146,7 @@ __device__ __forceinline__ float softmax_pass2(uint32_t s_addr, float c, float n
       else acc1 = fadd2(acc1, f2pack(p0, p1));
       pk[e] = pack2<T>(p0, p1);
     }
-    tmem_st32(s_addr + h2 * 32, pk);
+    tmem_st32(s_addr + 32 * h, pk);
   }
   float a, b, c2, d;
   f2unpack(acc0, a, b);
@@ -161,8 +159,7 @@ __device__ __forceinline__ float softmax_pass2(uint32_t s_addr, float c, float n
 // columns [64 + 8q, 72 + 8q), which hold the scores of chunk 4 + q/2, so it is kept in
 // registers until that chunk has been read.
 template <typename T>
-__device__ __forceinline__ float softmax_pass2_split(uint32_t s_addr, float c, float neg_m, int k0, int i,
-                                                     const Problem& p) {
+__device__ __forceinline__ float softmax_pass2_split(uint32_t s_addr, float c, float neg_m, int lim) {
   float sum = 0.f;
   uint32_t rem[8][8];
 #pragma unroll
@@ -173,11 +170,11 @@ __device__ __forceinline__ float softmax_pass2_split(uint32_t s_addr, float c, f
     uint32_t pk[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const int key = k0 + q * 16 + 2 * e;
+      const int col = q * 16 + 2 * e;
       float x0 = fmaf(__uint_as_float(sr[2 * e]), c, neg_m);
       float x1 = fmaf(__uint_as_float(sr[2 * e + 1]), c, neg_m);
-      if (!visible(p, key, i)) x0 = neg_inf();
-      if (!visible(p, key + 1, i)) x1 = neg_inf();
+      if (col >= lim) x0 = neg_inf();
+      if (col + 1 >= lim) x1 = neg_inf();
       const float p0 = ex2(x0), p1 = ex2(x1);
       sum += p0 + p1;
       pk[e] = pack2<T>(p0, p1);
@@ -204,7 +201,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                  const __grid_constant__ CUtensorMap tv, Problem p) {
+                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to, Problem p) {
   using L = FwdLayout<D>;
   constexpr int kCB = D / 64;
   constexpr bool kBf16 = IsBf16<T>::value;
@@ -263,12 +260,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = bars.tmem_base;
   const WaitCtx wc{&bars.abort, 0, p.wait_limit_ns, p.err, kKidTcFwd};
+  if (warp >= 8) regs_dec<kRegsLow>();
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
+      prefetch_tmap(&to);
       const int nq = nkv[1] > 0 ? 2 : 1;
       mbar_arrive_expect_tx(&bars.q_full, nq * L::kTileBytes);
       for (int w = 0; w < nq; ++w)
@@ -346,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     drain_wait(&bars.mma_done[w], 0, 100000000ull);
   } else if (warp < 8) {
     // Softmax warpgroups.
+    regs_inc<kRegsHigh>();
     const int w = warp / 4, quarter = warp % 4;
     const int r = quarter * 32 + lane;
     const int i = row0 + w * kBM + r;
@@ -365,8 +365,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int k0 = j * kBN;
       const bool need_mask = (k0 + kBN > p.Lkv) || (p.causal && k0 + kBN - 1 > tile_row0);
-      // Pass 1: the row maximum of the scaled scores of this tile.
-      const float mt = need_mask ? row_max<true>(s_addr, c, k0, i, p) : row_max<false>(s_addr, c, k0, i, p);
+      // The row's 128 scores in registers (one TMEM round trip), then its maximum.
+      uint32_t sv[kBN];
+#pragma unroll
+      for (int q4 = 0; q4 < kBN / 32; ++q4)
+        tmem_ld32(s_addr + 32 * q4, *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * q4]));
+      tmem_ld_wait();
+      const int lim = visible_keys(p, k0, i);
+      const float mt = need_mask ? tile_max<true>(sv, c, lim) : tile_max<false>(sv, c, lim);
       const float m_new = fmaxf(m, mt);
       const bool resc = m_new > m + kRescale;  // always true on the first tile (m = -inf)
       const float alpha = resc ? ex2(m - m_new) : 1.f;
@@ -396,11 +402,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Pass 2: P = exp2(c·s − m), row sum, P packed to 16 bits over S's first 64 columns.
       if (split_tile(p, j, tile_row0))
-        l += softmax_pass2_split<T>(s_addr, c, -m, k0, i, p);
+        l += softmax_pass2_split<T>(s_addr, c, -m, lim);
       else if (need_mask)
-        l += softmax_pass2<T, true>(s_addr, c, -m, k0, i, p);
+        l += exp_pass<T, true>(sv, s_addr, c, -m, lim);
       else
-        l += softmax_pass2<T, false>(s_addr, c, -m, k0, i, p);
+        l += exp_pass<T, false>(sv, s_addr, c, -m, lim);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars.p_full[w]);
@@ -413,9 +419,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_done[w], (nkv[w] - 1) & 1, wc));
     if (ok && nkv[w] > 0) {
       tc_fence_after();
+      // O / l is staged in this tile's Q buffer (its last reader, S_w(nkv-1), has finished)
+      // in the swizzled layout of the Q tile, then written by one bulk tensor store per
+      // 64-column block; rows at or past Lq are clipped by the store.
       const float inv = 1.f / l;
-      const bool valid = i < p.Lq;
-      T* orow = static_cast<T*>(p.out) + q_row(p, b, h, valid ? i : 0) * D;
+      uint8_t* stage = sm + L::kQOff + w * L::kTileBytes;
 #pragma unroll
       for (int c32 = 0; c32 < D / 32; ++c32) {
         uint32_t orr[32];
@@ -425,14 +433,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           packed[e] = pack2<T>(__uint_as_float(orr[2 * e]) * inv, __uint_as_float(orr[2 * e + 1]) * inv);
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c32 * 32);
+        uint8_t* blk = stage + (c32 / 2) * 16384;
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            dst[v4] = make_uint4(packed[4 * v4], packed[4 * v4 + 1], packed[4 * v4 + 2], packed[4 * v4 + 3]);
-        }
+        for (int v4 = 0; v4 < 4; ++v4)
+          *reinterpret_cast<uint4*>(blk + sw128_off(r, (c32 % 2) * 4 + v4)) =
+              make_uint4(packed[4 * v4], packed[4 * v4 + 1], packed[4 * v4 + 2], packed[4 * v4 + 3]);
       }
-      if (valid && p.lse) p.lse[q_row(p, b, h, i)] = (m + __log2f(l)) * kLn2;
+      fence_async_smem();
+      named_sync(1 + w, kBM);
+      if (r == 0) {
+        for (int cb = 0; cb < kCB; ++cb) tma_store_3d(&to, stage + cb * 16384, cb * 64, tile_row0, b * p.Hq + h);
+        bulk_commit();
+        bulk_wait_read();
+      }
+      if (i < p.Lq && p.lse) p.lse[q_row(p, b, h, i)] = (m + __log2f(l)) * kLn2;
     }
   }
   tc_fence_before();
@@ -445,8 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <typename T, int D>
 cudaError_t tc_fwd_t(const Problem& p, cudaStream_t s) {
-  CUtensorMap tq, tk, tv;
-  if (!make_tmap_3d(&tq, p.q, D, p.Lq, p.B * p.Hq, kBM) ||
+  CUtensorMap tq, tk, tv, to;
+  if (!make_tmap_3d(&tq, p.q, D, p.Lq, p.B * p.Hq, kBM) || !make_tmap_3d(&to, p.out, D, p.Lq, p.B * p.Hq, kBM) ||
       !make_tmap_3d(&tk, p.k, D, p.Lkv, p.B * p.Hkv, kBN) ||
       !make_tmap_3d(&tv, p.v, D, p.Lkv, p.B * p.Hkv, kBN))
     return cudaErrorInvalidValue;
@@ -455,7 +469,7 @@ cudaError_t tc_fwd_t(const Problem& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned nqb = (p.Lq + kBM * kQTiles - 1) / (kBM * kQTiles);
-  kern<<<nqb * p.Hq * p.B, kThreads, smem, s>>>(tq, tk, tv, p);
+  kern<<<nqb * p.Hq * p.B, kThreads, smem, s>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
