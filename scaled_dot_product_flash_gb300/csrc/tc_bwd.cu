@@ -32,7 +32,14 @@ namespace sdpa {
 namespace {
 using namespace tc;
 
-constexpr int kThreads = 352;
+constexpr int kThreads = 352;    // dK/dV: warps 0-7 element work, 8 producer, 9-10 MMA issuers
+constexpr int kDqThreads = 384;  // dQ: the same plus an idle warp 11 for the register split
+// dQ register split (setmaxnreg): launched at 168 registers a thread (65,536 / 384 rounded
+// down to a multiple of 8, 64,512 in all); warpgroup 2 drops to 56 and the element
+// warpgroups rise to 224: 128·56 + 256·224 = 64,512.
+constexpr int kRegsLow = 56;
+constexpr int kRegsHigh = 224;
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= kDqThreads * 168, "register split exceeds the launch");
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kRows = 128;  // rows owned by a block (keys for dK/dV, queries for dQ)
@@ -139,6 +146,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                   const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv,
                    Problem p) {
   using L = BwdLayout<D>;
   constexpr int kCB = D / 64;
@@ -319,12 +327,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&bars.ds_ready);
     }
-    // Epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK·scale.
-    if (ok) ok = __all_sync(0xffffffffu, total == 0 || mbar_wait(&bars.acc_done, 0, wc));
+    // Epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK·scale.  Each is staged in the
+    // block's own V or K buffer (no MMA reads them once acc_done has completed) in the
+    // swizzled tile layout and written by bulk tensor stores (keys past Lkv are clipped).
+    // The staging buffer is one the block's own TMA load fills; with no MMA (total == 0)
+    // nothing else has waited for that load, so wait for it here too.
+    if (ok)
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.own_full, 0, wc) && (total == 0 || mbar_wait(&bars.acc_done, 0, wc)));
+    const int r = quarter * 32 + lane;
+    uint8_t* stage = sm + (w == 0 ? L::kOwnB : L::kOwnA);
     if (ok) {
       tc_fence_after();
-      const bool valid = j < p.Lkv;
-      T* dst = static_cast<T*>(w == 0 ? p.dv : p.dk) + kv_row(p, b, g, valid ? j : 0) * D;
       const float mul = w == 0 ? 1.f : p.scale;
       const uint32_t a_addr = tmem_addr(tbase, quarter * 32, w == 0 ? kColDv : kColDk);
 #pragma unroll 1
@@ -341,13 +354,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           packed[e] = pack2<T>(__uint_as_float(acc[2 * e]) * mul, __uint_as_float(acc[2 * e + 1]) * mul);
-        if (valid) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c32 * 32);
+        uint8_t* blk = stage + (c32 / 2) * L::kCbStride;
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            d4[v4] = make_uint4(packed[4 * v4], packed[4 * v4 + 1], packed[4 * v4 + 2], packed[4 * v4 + 3]);
-        }
+        for (int v4 = 0; v4 < 4; ++v4)
+          *reinterpret_cast<uint4*>(blk + sw128_off(r, (c32 % 2) * 4 + v4)) =
+              make_uint4(packed[4 * v4], packed[4 * v4 + 1], packed[4 * v4 + 2], packed[4 * v4 + 3]);
       }
+      fence_async_smem();
+    }
+    if (named_sync_and(1 + w, 128, ok) && r == 0) {
+      for (int cb = 0; cb < kCB; ++cb)
+        tma_store_3d(w == 0 ? &tdv : &tdk, stage + cb * L::kCbStride, cb * 64, j0, b * p.Hkv + g);
+      bulk_commit();
+      bulk_wait_read();
     }
   }
   tc_fence_before();
@@ -391,10 +410,10 @@ struct DqBars {
 };
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kDqThreads, 1)
     tc_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                 Problem p) {
+                 const __grid_constant__ CUtensorMap tdq, Problem p) {
   using L = DqLayout<D>;
   constexpr int kCB = D / 64;
   constexpr int kCbStride = kRows * 128;
@@ -448,6 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = bars.tmem_base;
   const WaitCtx wc{&bars.abort, 0, p.wait_limit_ns, p.err, kKidTcDq};
+  if (warp >= 8) regs_dec<kRegsLow>();
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
@@ -525,7 +545,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mma_commit_w(&bars.acc_done);
     drain_wait(&bars.acc_done, 0, 100000000ull);
-  } else {
+  } else if (warp < 8) {
+    regs_inc<kRegsHigh>();
     const int w = warp / 4, quarter = warp % 4;
     const int i = i0 + quarter * 32 + lane;  // this thread's query
     const bool valid = i < p.Lq;
@@ -541,67 +562,79 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int k0 = n * kBlk + 64 * w;  // first key of this half
       const bool need_mask = (k0 + 64 > p.Lkv) || (p.causal && k0 + 63 > i0);
+      // keys k0 + e with e < lim are visible to this query
+      const int lim = min(p.Lkv - k0, p.causal ? i - k0 + 1 : 64);
       const uint32_t s_addr = tmem_addr(tbase, quarter * 32, kColS0 + 128 * (n % 2) + 64 * w);
       const uint32_t dp_addr = tmem_addr(tbase, quarter * 32, kColDp + 64 * w);
-      // dP first, so that the next block's dP can be computed during this block's math.
-      uint32_t dr[64];
+      // dP and S of this half in one TMEM round trip; the dP buffer is released at once so
+      // that the next block's dP can be computed during this block's math.
+      uint32_t dr[64], sr[64];
       tmem_ld32(dp_addr, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
       tmem_ld32(dp_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+      tmem_ld32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&bars.dp_free);
       uint32_t dsk[32];
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t sr[32];
-        tmem_ld32(s_addr + 32 * hh, sr);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float p0, p1;
-          ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl), p0, p1);
-          if (need_mask) {
-            const int key = k0 + 32 * hh + 2 * e;
-            if (key >= p.Lkv || (p.causal && key > i)) p0 = 0.f;
-            if (key + 1 >= p.Lkv || (p.causal && key + 1 > i)) p1 = 0.f;
-          }
-          const int q = 32 * hh + 2 * e;
-          float d0, d1;
-          f2unpack(fmul2(f2pack(p0, p1), fadd2(f2pack(__uint_as_float(dr[q]), __uint_as_float(dr[q + 1])), nd)),
-                   d0, d1);
-          dsk[16 * hh + e] = pack2<T>(d0, d1);
+      for (int e = 0; e < 32; ++e) {
+        float p0, p1;
+        ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl), p0, p1);
+        if (need_mask) {
+          if (2 * e >= lim) p0 = 0.f;
+          if (2 * e + 1 >= lim) p1 = 0.f;
         }
+        float d0, d1;
+        f2unpack(fmul2(f2pack(p0, p1), fadd2(f2pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), nd)),
+                 d0, d1);
+        dsk[e] = pack2<T>(d0, d1);
       }
       tmem_st32(s_addr, dsk);  // dS over this half's first 32 columns (all of it read)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars.ds_ready);
     }
-    if (ok) ok = __all_sync(0xffffffffu, total == 0 || mbar_wait(&bars.acc_done, 0, wc));
-    if (ok && w == 0) {
-      tc_fence_after();
-      T* dst = static_cast<T*>(p.dq) + row * D;
-      const uint32_t a_addr = tmem_addr(tbase, quarter * 32, kColDq);
+    // Epilogue: dQ·scale staged in the block's Q buffer (the last S MMA has read it) and
+    // written by bulk tensor stores; warpgroup w handles the 64-column blocks cb ≡ w (mod 2).
+    // The staging buffer is one the block's own TMA load fills; with no MMA (total == 0)
+    // nothing else has waited for that load, so wait for it here too.
+    if (ok)
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.own_full, 0, wc) && (total == 0 || mbar_wait(&bars.acc_done, 0, wc)));
+    if (w < kCB) {  // the same for every thread of the warpgroup
+      const int r = quarter * 32 + lane;
+      if (ok) {
+        tc_fence_after();
+        const uint32_t a_addr = tmem_addr(tbase, quarter * 32, kColDq);
 #pragma unroll 1
-      for (int c32 = 0; c32 < D / 32; ++c32) {
-        uint32_t acc[32];
-        if (total > 0) {
-          tmem_ld32(a_addr + c32 * 32, acc);
-          tmem_ld_wait();
-        } else {
+        for (int cb = w; cb < kCB; cb += 2) {
+          uint8_t* blk = sm + L::kQ + cb * kCbStride;
 #pragma unroll
-          for (int e = 0; e < 32; ++e) acc[e] = 0u;
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t acc[32];
+            if (total > 0) {
+              tmem_ld32(a_addr + cb * 64 + h2 * 32, acc);
+              tmem_ld_wait();
+            } else {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) acc[e] = 0u;
+            }
+            uint32_t packed[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              packed[e] = pack2<T>(__uint_as_float(acc[2 * e]) * p.scale, __uint_as_float(acc[2 * e + 1]) * p.scale);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              *reinterpret_cast<uint4*>(blk + sw128_off(r, h2 * 4 + v4)) =
+                  make_uint4(packed[4 * v4], packed[4 * v4 + 1], packed[4 * v4 + 2], packed[4 * v4 + 3]);
+          }
         }
-        uint32_t packed[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          packed[e] = pack2<T>(__uint_as_float(acc[2 * e]) * p.scale, __uint_as_float(acc[2 * e + 1]) * p.scale);
-        if (valid) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c32 * 32);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            d4[v4] = make_uint4(packed[4 * v4], packed[4 * v4 + 1], packed[4 * v4 + 2], packed[4 * v4 + 3]);
-        }
+        fence_async_smem();
+      }
+      if (named_sync_and(1 + w, 128, ok) && r == 0) {
+        for (int cb = w; cb < kCB; cb += 2) tma_store_3d(&tdq, sm + L::kQ + cb * kCbStride, cb * 64, i0, b * p.Hq + h);
+        bulk_commit();
+        bulk_wait_read();
       }
     }
   }
@@ -614,11 +647,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 struct Maps {
-  CUtensorMap q, k, v, dout;
+  CUtensorMap q, k, v, dout, dq, dk, dv;
 };
 
 bool make_maps(const Problem& p, int D, Maps* m) {
   return make_tmap_3d(&m->q, p.q, D, p.Lq, p.B * p.Hq, kRows) &&
+         make_tmap_3d(&m->dq, p.dq, D, p.Lq, p.B * p.Hq, kRows) &&
+         make_tmap_3d(&m->dk, p.dk, D, p.Lkv, p.B * p.Hkv, kRows) &&
+         make_tmap_3d(&m->dv, p.dv, D, p.Lkv, p.B * p.Hkv, kRows) &&
          make_tmap_3d(&m->dout, p.dout, D, p.Lq, p.B * p.Hq, kRows) &&
          make_tmap_3d(&m->k, p.k, D, p.Lkv, p.B * p.Hkv, kRows) &&
          make_tmap_3d(&m->v, p.v, D, p.Lkv, p.B * p.Hkv, kRows);
@@ -633,7 +669,7 @@ cudaError_t dkdv_t(const Problem& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned nkt = (p.Lkv + kRows - 1) / kRows;
-  kern<<<nkt * p.Hkv * p.B, kThreads, smem, s>>>(m.q, m.k, m.v, m.dout, p);
+  kern<<<nkt * p.Hkv * p.B, kThreads, smem, s>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv, p);
   return cudaGetLastError();
 }
 
@@ -646,7 +682,7 @@ cudaError_t dq_t(const Problem& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned nqt = (p.Lq + kRows - 1) / kRows;
-  kern<<<nqt * p.Hq * p.B, kThreads, smem, s>>>(m.q, m.k, m.v, m.dout, p);
+  kern<<<nqt * p.Hq * p.B, kDqThreads, smem, s>>>(m.q, m.k, m.v, m.dout, m.dq, p);
   return cudaGetLastError();
 }
 

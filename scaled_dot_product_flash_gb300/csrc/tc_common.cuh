@@ -99,8 +99,20 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // Makes this thread's generic-proxy shared-memory writes visible to the async proxy (TMA).
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-// Barrier over `n` threads (a multiple of 32) on hardware barrier `id` (1..15; 0 is __syncthreads).
-__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+// Barrier over `n` threads (a multiple of 32) on hardware barrier `id` (1..15; 0 is
+// __syncthreads) that returns the AND of `pred` over those threads.  Every one of the n
+// threads must reach it, whatever its own pred, so callers place it outside their error
+// branches.
+__device__ __forceinline__ bool named_sync_and(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
 // Byte offset of 16-byte chunk `c` (0..7) of row `r` in a 128-byte-swizzled [rows x 128 B] box.
 __device__ __forceinline__ uint32_t sw128_off(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
 

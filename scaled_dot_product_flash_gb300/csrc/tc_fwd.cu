@@ -417,36 +417,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok && nkv[w] > 0)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_done[w], (nkv[w] - 1) & 1, wc));
-    if (ok && nkv[w] > 0) {
-      tc_fence_after();
+    if (nkv[w] > 0) {  // the same for every thread of the warpgroup
       // O / l is staged in this tile's Q buffer (its last reader, S_w(nkv-1), has finished)
       // in the swizzled layout of the Q tile, then written by one bulk tensor store per
       // 64-column block; rows at or past Lq are clipped by the store.
-      const float inv = 1.f / l;
       uint8_t* stage = sm + L::kQOff + w * L::kTileBytes;
+      if (ok) {
+        tc_fence_after();
+        const float inv = 1.f / l;
 #pragma unroll
-      for (int c32 = 0; c32 < D / 32; ++c32) {
-        uint32_t orr[32];
-        tmem_ld32(o_addr + c32 * 32, orr);
-        tmem_ld_wait();
-        uint32_t packed[16];
+        for (int c32 = 0; c32 < D / 32; ++c32) {
+          uint32_t orr[32];
+          tmem_ld32(o_addr + c32 * 32, orr);
+          tmem_ld_wait();
+          uint32_t packed[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          packed[e] = pack2<T>(__uint_as_float(orr[2 * e]) * inv, __uint_as_float(orr[2 * e + 1]) * inv);
-        uint8_t* blk = stage + (c32 / 2) * 16384;
+          for (int e = 0; e < 16; ++e)
+            packed[e] = pack2<T>(__uint_as_float(orr[2 * e]) * inv, __uint_as_float(orr[2 * e + 1]) * inv);
+          uint8_t* blk = stage + (c32 / 2) * 16384;
 #pragma unroll
-        for (int v4 = 0; v4 < 4; ++v4)
-          *reinterpret_cast<uint4*>(blk + sw128_off(r, (c32 % 2) * 4 + v4)) =
-              make_uint4(packed[4 * v4], packed[4 * v4 + 1], packed[4 * v4 + 2], packed[4 * v4 + 3]);
+          for (int v4 = 0; v4 < 4; ++v4)
+            *reinterpret_cast<uint4*>(blk + sw128_off(r, (c32 % 2) * 4 + v4)) =
+                make_uint4(packed[4 * v4], packed[4 * v4 + 1], packed[4 * v4 + 2], packed[4 * v4 + 3]);
+        }
+        fence_async_smem();
+        if (i < p.Lq && p.lse) p.lse[q_row(p, b, h, i)] = (m + __log2f(l)) * kLn2;
       }
-      fence_async_smem();
-      named_sync(1 + w, kBM);
-      if (r == 0) {
+      if (named_sync_and(1 + w, kBM, ok) && r == 0) {
         for (int cb = 0; cb < kCB; ++cb) tma_store_3d(&to, stage + cb * 16384, cb * 64, tile_row0, b * p.Hq + h);
         bulk_commit();
         bulk_wait_read();
       }
-      if (i < p.Lq && p.lse) p.lse[q_row(p, b, h, i)] = (m + __log2f(l)) * kLn2;
     }
   }
   tc_fence_before();
