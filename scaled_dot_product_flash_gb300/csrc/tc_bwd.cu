@@ -11,7 +11,8 @@
 //   dV += Pᵀ·dO, dK += dSᵀ·Q                         (tcgen05, accumulators stay in TMEM)
 // and finally dK·scale and dV are rounded and stored.  The element warps publish Pᵀ as
 // soon as it is ready, so dV runs while dSᵀ is computed, and Sᵀ of the next block starts
-// as soon as dV has consumed Pᵀ.
+// as soon as dV has consumed Pᵀ.  dSᵀ is formed from Pᵀ in fp32 (dV uses Pᵀ rounded to
+// the element type, as the A operand of a 16-bit MMA must be).
 //
 // dQ kernel: one block owns 128 query rows of one head and loops over 128-row KV blocks:
 //   S = Q·Kᵀ, dP = dO·Vᵀ, P = exp2(c·S − log2e·lse_i), dS = P∘(dP − δ_i), dQ += dS·K,
@@ -275,28 +276,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool diag = p.causal && j0 + kRows - 1 > i0;
       const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(&bars.nlse2[s][64 * w]);
       const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(&bars.ndelta[s][64 * w]);
-      // Pᵀ for this half (64 queries), 32 per TMEM round trip; the packed 16-bit values
-      // are written over Sᵀ and kept in registers for dSᵀ (which therefore uses the same
-      // rounded Pᵀ that dV is multiplied with).
-      uint32_t pk[32];
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t sr[32];
-        tmem_ld32(x_addr + 32 * hh, sr);
+      // Pᵀ for this half (64 queries) from one TMEM round trip; the packed 16-bit values
+      // are written over Sᵀ for dV, and Pᵀ stays in registers in fp32 for dSᵀ.
+      uint64_t pf[32];  // fp32 pairs
+      {
+        uint32_t sr[64];
+        tmem_ld32(x_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        tmem_ld32(x_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
         tmem_ld_wait();
+        uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int q = 32 * hh + 2 * e;
+        for (int e = 0; e < 32; ++e) {
           float p0, p1;
-          ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl2[q / 2]), p0,
-                   p1);
+          ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl2[e]), p0, p1);
           if (diag) {
-            if (j > i0 + q) p0 = 0.f;
-            if (j > i0 + q + 1) p1 = 0.f;
+            if (j > i0 + 2 * e) p0 = 0.f;
+            if (j > i0 + 2 * e + 1) p1 = 0.f;
           }
-          pk[16 * hh + e] = pack2<T>(p0, p1);
+          pf[e] = f2pack(p0, p1);
+          pk[e] = pack2<T>(p0, p1);
         }
-        tmem_st16(x_addr + 16 * hh, *reinterpret_cast<uint32_t(*)[16]>(&pk[16 * hh]));
+        tmem_st32(x_addr, pk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -304,24 +304,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_full, n & 1, wc));
       if (!ok) break;
       tc_fence_after();
-      // dSᵀ = Pᵀ∘(dPᵀ − δ), 32 queries per TMEM round trip.
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t dr[32];
-        tmem_ld32(y_addr + 32 * hh, dr);
+      // dSᵀ = Pᵀ∘(dPᵀ − δ), one TMEM round trip.
+      {
+        uint32_t dr[64];
+        tmem_ld32(y_addr, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+        tmem_ld32(y_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
         tmem_ld_wait();
-        uint32_t dk[16];
+        uint32_t dk[32];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int q = 32 * hh + 2 * e;
-          float p0, p1, d0, d1;
-          unpack2<T>(pk[16 * hh + e], p0, p1);
-          f2unpack(fmul2(f2pack(p0, p1),
-                         fadd2(f2pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), nd2[q / 2])),
-                   d0, d1);
+        for (int e = 0; e < 32; ++e) {
+          float d0, d1;
+          f2unpack(fmul2(pf[e], fadd2(f2pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), nd2[e])), d0,
+                   d1);
           dk[e] = pack2<T>(d0, d1);
         }
-        tmem_st16(y_addr + 16 * hh, dk);
+        tmem_st32(y_addr, dk);
       }
       tmem_st_wait();
       tc_fence_before();
