@@ -5,6 +5,8 @@ declared in ``include/sdpa.h``).  This package is its thin Python binding:
 
 * ``_lib``: ctypes entry points under the C names (``sdpa_fwd``, ``sdpa_bwd``, ...).
 * ``api``: tensor-level calls that allocate outputs with PyTorch and pass raw pointers.
+* ``autograd``: ``SDPAFunction`` (torch autograd over the forward and fused backward) and a
+  ``scaled_dot_product_attention`` drop-in for the cases the kernels cover.
 * ``inputs``: seeded synthetic inputs.
 * ``build``: nvcc build of the library.
 """
