@@ -154,40 +154,41 @@ __device__ __forceinline__ float exp_pass(const uint32_t (&sv)[kBN], uint32_t s_
   return (a + b) + (c2 + d);
 }
 
-// As softmax_pass2, and also the remainder P − head(P), packed to 16 bits into columns
-// [64, 128).  Scores are read 16 columns at a time; the remainder of chunk q goes to
-// columns [64 + 8q, 72 + 8q), which hold the scores of chunk 4 + q/2, so it is kept in
-// registers until that chunk has been read.
+// As exp_pass, and also the remainder P − head(P), packed to 16 bits into columns
+// [64, 128) (their scores are already in registers), so that P enters O with about 16
+// more bits.  Written 16 keys at a time to keep few packed values live.
 template <typename T>
-__device__ __forceinline__ float softmax_pass2_split(uint32_t s_addr, float c, float neg_m, int lim) {
-  float sum = 0.f;
-  uint32_t rem[8][8];
+__device__ __forceinline__ float exp_pass_split(const uint32_t (&sv)[kBN], uint32_t s_addr, float c, float neg_m,
+                                                int lim) {
+  const uint64_t cc = f2pack(c, c), nm = f2pack(neg_m, neg_m);
+  uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    uint32_t sr[16];
-    tmem_ld16(s_addr + q * 16, sr);
-    tmem_ld_wait();
-    uint32_t pk[8];
+  for (int q = 0; q < kBN / 16; ++q) {
+    uint32_t pk[8], rk[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const int col = q * 16 + 2 * e;
-      float x0 = fmaf(__uint_as_float(sr[2 * e]), c, neg_m);
-      float x1 = fmaf(__uint_as_float(sr[2 * e + 1]), c, neg_m);
+      const int col = 16 * q + 2 * e;
+      uint64_t xx = ffma2(f2pack(__uint_as_float(sv[col]), __uint_as_float(sv[col + 1])), cc, nm);
+      float x0, x1;
+      f2unpack(xx, x0, x1);
       if (col >= lim) x0 = neg_inf();
       if (col + 1 >= lim) x1 = neg_inf();
-      const float p0 = ex2(x0), p1 = ex2(x1);
-      sum += p0 + p1;
+      float p0, p1;
+      ex2_pair(f2pack(x0, x1), p0, p1);
+      if (e % 2 == 0) acc0 = fadd2(acc0, f2pack(p0, p1));
+      else acc1 = fadd2(acc1, f2pack(p0, p1));
       pk[e] = pack2<T>(p0, p1);
       float h0, h1;
       unpack2<T>(pk[e], h0, h1);
-      rem[q][e] = pack2<T>(p0 - h0, p1 - h1);
+      rk[e] = pack2<T>(p0 - h0, p1 - h1);
     }
-    tmem_st8(s_addr + q * 8, pk);
-#pragma unroll
-    for (int q2 = 0; q2 <= q; ++q2)
-      if (4 + q2 / 2 == q) tmem_st8(s_addr + 64 + q2 * 8, rem[q2]);
+    tmem_st8(s_addr + 8 * q, pk);
+    tmem_st8(s_addr + 64 + 8 * q, rk);
   }
-  return sum;
+  float a, b, c2, d;
+  f2unpack(acc0, a, b);
+  f2unpack(acc1, c2, d);
+  return (a + b) + (c2 + d);
 }
 
 // Bounded wait that ignores the abort flag (used to drain in-flight work at teardown).
@@ -402,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Pass 2: P = exp2(c·s − m), row sum, P packed to 16 bits over S's first 64 columns.
       if (split_tile(p, j, tile_row0))
-        l += softmax_pass2_split<T>(s_addr, c, -m, lim);
+        l += exp_pass_split<T>(sv, s_addr, c, -m, lim);
       else if (need_mask)
         l += exp_pass<T, true>(sv, s_addr, c, -m, lim);
       else
