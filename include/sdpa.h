@@ -102,6 +102,39 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* out, const
              int dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Strided layouts.  sdpa_fwd and sdpa_bwd take contiguous [B,H,L,D] tensors.  These two
+ * calls take every [B,H,L,D] tensor with its own element strides for the batch, head and
+ * row dimensions (the D elements of a row stay contiguous), so that tensors stored as
+ * [B,L,H,D] (one row per token holding all heads), or views into a fused [B,L,3,H,D]
+ * projection output, are read and written in place instead of being copied to [B,H,L,D]
+ * first (the pages' Metal kernel pays such transposes: "mps-flash-sdpa 0.1.0", section
+ * "How It Works").  The operation, the other arguments and every other rule are those of
+ * sdpa_fwd / sdpa_bwd; lse and the workspace stay contiguous [B,Hq,Lq] fp32.
+ *  - Each stride, in bytes, must be a positive multiple of 16 (TMA and 16-byte vector
+ *    access), and the layout must not map two elements of a tensor to the same address
+ *    (checked: sorted by stride, each stride covers the extent of the smaller ones).
+ *    Otherwise SDPA_ERR_INVALID_ARG.
+ *  - Inputs may overlap one another (q, k, v as views of one buffer); outputs may overlap
+ *    nothing, judged by each tensor's address range [base, base + extent).
+ * sdpa_fwd_strided reads strides->q, k, v and writes with strides->o; sdpa_bwd_strided
+ * uses all eight (o is the forward output it reads).
+ */
+typedef struct {
+  int64_t batch, head, row; /* element strides; the D elements of a row are contiguous */
+} sdpa_layout_t;
+typedef struct {
+  sdpa_layout_t q, k, v, o, dout, dq, dk, dv;
+} sdpa_strides_t;
+int sdpa_fwd_strided(const void* q, const void* k, const void* v, void* out, float* lse,
+                     int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale, int is_causal,
+                     int dtype, const sdpa_strides_t* strides, void* stream);
+int sdpa_bwd_strided(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv,
+                     int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale, int is_causal,
+                     int dtype, const sdpa_strides_t* strides, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/*
  * Backward without a workspace argument: sdpa_bwd for callers that cannot allocate device
  * memory.  Such callers include code running inside a host application or framework that
  * owns every device allocation and hands its plugins nothing but their inputs and outputs,

@@ -25,6 +25,19 @@ PATH_AUTO, PATH_TENSOR, PATH_SIMT, PATH_VECTOR = 0, 1, 2, 3
 
 # Every symbol include/sdpa.h declares, with its ctypes signature.
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+
+class Layout(ctypes.Structure):
+    """sdpa_layout_t: element strides of the batch, head and row dimensions."""
+    _fields_ = [("batch", ctypes.c_int64), ("head", ctypes.c_int64), ("row", ctypes.c_int64)]
+
+
+class Strides(ctypes.Structure):
+    """sdpa_strides_t: one layout per tensor."""
+    _fields_ = [(n, Layout) for n in ("q", "k", "v", "o", "dout", "dq", "dk", "dv")]
+
+
+_sp = ctypes.POINTER(Strides)
 SIGNATURES = {
     "sdpa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
     "sdpa_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i]),
@@ -41,6 +54,10 @@ SIGNATURES = {
     "sdpa_debug_inject_timeout": (_i, [_i, ctypes.c_uint64]),
     "sdpa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                               _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
+    "sdpa_fwd_strided": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _sp,
+                              _vp]),
+    "sdpa_bwd_strided": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                              _i, _i, _i, _i, _i, _i, _f, _i, _i, _sp, _vp, _sz, _vp]),
 }
 BWD_NOALLOC_MAX_ROWS = 1 << 20
 KERNELS = {"fwd": 0, "delta": 1, "dq": 2, "dkdv": 3, "vec_fwd": 4, "vec_bwd": 5}
@@ -87,6 +104,28 @@ def sdpa_bwd(q, k, v, out, dout, lse, dq, dk, dv, B, Hq, Hkv, Lq, Lkv, D, scale,
              dtype, workspace, workspace_bytes, stream):
     return load().sdpa_bwd(q, k, v, out, dout, lse, dq, dk, dv, B, Hq, Hkv, Lq, Lkv, D, scale,
                            is_causal, dtype, workspace, workspace_bytes, stream)
+
+
+def make_strides(**layouts) -> Strides:
+    """Strides from (batch, head, row) element-stride triples keyed q, k, v, o, dout, dq,
+    dk, dv (missing tensors get zeros, which the library rejects if it reads them)."""
+    st = Strides()
+    for name, (b, h, r) in layouts.items():
+        setattr(st, name, Layout(int(b), int(h), int(r)))
+    return st
+
+
+def sdpa_fwd_strided(q, k, v, out, lse, B, Hq, Hkv, Lq, Lkv, D, scale, is_causal, dtype, strides,
+                     stream):
+    return load().sdpa_fwd_strided(q, k, v, out, lse, B, Hq, Hkv, Lq, Lkv, D, scale, is_causal,
+                                   dtype, ctypes.byref(strides), stream)
+
+
+def sdpa_bwd_strided(q, k, v, out, dout, lse, dq, dk, dv, B, Hq, Hkv, Lq, Lkv, D, scale,
+                     is_causal, dtype, strides, workspace, workspace_bytes, stream):
+    return load().sdpa_bwd_strided(q, k, v, out, dout, lse, dq, dk, dv, B, Hq, Hkv, Lq, Lkv, D,
+                                   scale, is_causal, dtype, ctypes.byref(strides), workspace,
+                                   workspace_bytes, stream)
 
 
 def sdpa_bwd_noalloc(q, k, v, out, dout, lse, dq, dk, dv, B, Hq, Hkv, Lq, Lkv, D, scale,

@@ -18,10 +18,18 @@ DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 def _check(name, t, dtype=None):
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
-    if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous [B, H, L, D]")
+    if t.dim() == 4 and t.stride(-1) != 1:
+        raise ValueError(f"{name} must have contiguous rows (stride 1 along D)")
+    if t.dim() != 4 and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+
+
+def _layout(t):
+    """(batch, head, row) element strides of a [B, H, L, D] tensor: any layout whose rows
+    are contiguous, e.g. a [B, L, H, D] buffer seen through .transpose(1, 2)."""
+    return (t.stride(0), t.stride(1), t.stride(2))
 
 
 def _stream(stream):
@@ -41,7 +49,9 @@ def attention_forward(q, k, v, scale=None, is_causal=False, need_lse=True, out=N
                       lse=None, stream=None):
     """out = softmax(scale·q·kᵀ [causal]) · v; also the fp32 logsumexp when need_lse.
 
-    q [B,Hq,Lq,D], k/v [B,Hkv,Lkv,D] CUDA tensors of one dtype (fp32/fp16/bf16).
+    q [B,Hq,Lq,D], k/v [B,Hkv,Lkv,D] CUDA tensors of one dtype (fp32/fp16/bf16), in any
+    layout with contiguous rows (e.g. [B,L,H,D] storage seen through .transpose(1, 2));
+    the strides go to the library, nothing is copied.  `out` defaults to q's layout.
     Returns (out, lse or None).
     """
     for n, t in (("q", q), ("k", k), ("v", v)):
@@ -51,15 +61,17 @@ def attention_forward(q, k, v, scale=None, is_causal=False, need_lse=True, out=N
         raise ValueError("k and v shapes differ")
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty_like(q)  # same layout as q
     if need_lse and lse is None:
         lse = torch.empty((B, Hq, Lq), device=q.device, dtype=torch.float32)
     if not need_lse:
         lse = None
-    st = _lib.sdpa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                       lse.data_ptr() if lse is not None else None,
-                       B, Hq, Hkv, Lq, Lkv, D, scale, int(bool(is_causal)),
-                       DTYPE_CODE[q.dtype], _stream(stream))
+    _check("out", out, q.dtype)
+    strides = _lib.make_strides(q=_layout(q), k=_layout(k), v=_layout(v), o=_layout(out))
+    st = _lib.sdpa_fwd_strided(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                               lse.data_ptr() if lse is not None else None,
+                               B, Hq, Hkv, Lq, Lkv, D, scale, int(bool(is_causal)),
+                               DTYPE_CODE[q.dtype], strides, _stream(stream))
     if st != _lib.OK:
         raise _lib.SdpaError(st, "sdpa_fwd")
     return out, lse
@@ -84,11 +96,16 @@ def attention_backward(q, k, v, out, dout, lse, scale=None, is_causal=False, wor
     need = workspace_bytes(q, k)
     if workspace is None:
         workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
-    st = _lib.sdpa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                       dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                       dv.data_ptr(), B, Hq, Hkv, Lq, Lkv, D, scale, int(bool(is_causal)),
-                       DTYPE_CODE[q.dtype], workspace.data_ptr(), workspace.numel(),
-                       _stream(stream))
+    for n, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check(n, t, q.dtype)
+    strides = _lib.make_strides(q=_layout(q), k=_layout(k), v=_layout(v), o=_layout(out),
+                                dout=_layout(dout), dq=_layout(dq), dk=_layout(dk),
+                                dv=_layout(dv))
+    st = _lib.sdpa_bwd_strided(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                               dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                               dv.data_ptr(), B, Hq, Hkv, Lq, Lkv, D, scale,
+                               int(bool(is_causal)), DTYPE_CODE[q.dtype], strides,
+                               workspace.data_ptr(), workspace.numel(), _stream(stream))
     if st != _lib.OK:
         raise _lib.SdpaError(st, "sdpa_bwd")
     return dq, dk, dv

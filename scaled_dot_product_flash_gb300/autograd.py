@@ -8,7 +8,8 @@ sections "Key Features" and "Limitations": the backward needs the forward's logs
 tensor": the logsumexp is only produced when a gradient will be taken).  As in the rest of
 the package, this module only marshals tensors; all arithmetic runs in ``libsdpa.so``.
 
-Supported: q [B, Hq, Lq, D], k and v [B, Hkv, Lkv, D] on CUDA, one dtype of fp32/fp16/bf16,
+Supported: q [B, Hq, Lq, D], k and v [B, Hkv, Lkv, D] on CUDA (any layout whose rows are
+contiguous, e.g. [B, L, H, D] storage through .transpose(1, 2)), one dtype of fp32/fp16/bf16,
 Hq a multiple of Hkv (grouped-query attention: query head h uses KV head h // (Hq/Hkv)),
 D in {32, 64, 96, 128}, optional top-left causal mask, any finite scale.  Attention masks,
 dropout and other head layouts raise ``NotImplementedError``.
@@ -39,8 +40,10 @@ class SDPAFunction(torch.autograd.Function):
     @staticmethod
     def backward(ctx, dout):
         q, k, v, out, lse = ctx.saved_tensors
-        dq, dk, dv = api.attention_backward(q, k, v, out, dout.contiguous(), lse,
-                                            scale=ctx.scale, is_causal=ctx.is_causal)
+        if dout.stride(-1) != 1:
+            dout = dout.contiguous()
+        dq, dk, dv = api.attention_backward(q, k, v, out, dout, lse, scale=ctx.scale,
+                                            is_causal=ctx.is_causal)
         return dq, dk, dv, None, None
 
 
@@ -73,5 +76,7 @@ def scaled_dot_product_attention(query, key, value, attn_mask=None, dropout_p=0.
     if not math.isfinite(1.0 / math.sqrt(D) if scale is None else float(scale)):
         raise ValueError("scale must be finite")
     s = 1.0 / math.sqrt(D) if scale is None else float(scale)
-    return SDPAFunction.apply(query.contiguous(), key.contiguous(), value.contiguous(), s,
-                              bool(is_causal))
+    # Any layout with contiguous rows is passed through as is (its strides go to the
+    # library); others are copied to [B, H, L, D] first.
+    q, k, v = (t if t.stride(-1) == 1 else t.contiguous() for t in (query, key, value))
+    return SDPAFunction.apply(q, k, v, s, bool(is_causal))

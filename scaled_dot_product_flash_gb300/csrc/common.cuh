@@ -49,6 +49,11 @@ template <> struct Elem<__nv_bfloat16> {
   static __device__ __forceinline__ __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
 };
 
+// Element strides of a [B, H, L, D] tensor whose D elements are contiguous.
+struct Layout {
+  int64_t sb, sh, sl;  // batch, head, row
+};
+
 // Sizes and pointers of one call, passed by value to every kernel.
 struct Problem {
   const void* q;
@@ -70,13 +75,25 @@ struct Problem {
   unsigned* err;     // device error word
   uint64_t wait_limit_ns;  // time limit of any single bounded wait inside a kernel
   int inject;        // test hook: 1 = the tensor-core forward never delivers its first K tile
+  // Layouts of q, k, v, o (forward output / backward input), dout, dq, dk, dv.
+  Layout lq, lk, lv, lo, ldo, ldq, ldk, ldv;
 };
 
+// Index of query row (b, h, i) in the contiguous [B, Hq, Lq] arrays lse and δ.
 __host__ __device__ __forceinline__ int64_t q_row(const Problem& p, int b, int h, int i) {
   return ((int64_t)b * p.Hq + h) * p.Lq + i;
 }
-__host__ __device__ __forceinline__ int64_t kv_row(const Problem& p, int b, int g, int j) {
-  return ((int64_t)b * p.Hkv + g) * p.Lkv + j;
+// Element offset of row (b, h, i) of a tensor with layout l.
+__host__ __device__ __forceinline__ int64_t row_off(const Layout& l, int b, int h, int64_t i) {
+  return (int64_t)b * l.sb + (int64_t)h * l.sh + i * l.sl;
+}
+template <typename T>
+__host__ __device__ __forceinline__ const T* row_ptr(const void* base, const Layout& l, int b, int h, int64_t i) {
+  return static_cast<const T*>(base) + row_off(l, b, h, i);
+}
+template <typename T>
+__host__ __device__ __forceinline__ T* row_ptr(void* base, const Layout& l, int b, int h, int64_t i) {
+  return static_cast<T*>(base) + row_off(l, b, h, i);
 }
 
 }  // namespace sdpa

@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "launch.h"
@@ -45,6 +46,40 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 size_t elem_size(int dtype) { return dtype == SDPA_F32 ? 4 : 2; }
+
+sdpa_layout_t contiguous(int H, int L, int D) {
+  return sdpa_layout_t{(int64_t)H * L * D, (int64_t)L * D, (int64_t)D};
+}
+
+sdpa_strides_t contiguous_strides(int Hq, int Hkv, int Lq, int Lkv, int D) {
+  const sdpa_layout_t lq = contiguous(Hq, Lq, D), lk = contiguous(Hkv, Lkv, D);
+  return sdpa_strides_t{lq, lk, lk, lq, lq, lq, lk, lk};
+}
+
+// Validates the layout of one [B, H, L, D] tensor (strides positive, multiples of 16
+// bytes, no two elements at one address: sorted by stride, each stride covers the extent
+// of the smaller dimensions) and returns its byte extent in *bytes.
+bool check_layout(const sdpa_layout_t& l, int B, int H, int L, int D, size_t es, Layout* out, size_t* bytes) {
+  const int64_t st[3] = {l.batch, l.head, l.row};
+  const int64_t n[3] = {B, H, L};
+  for (int a = 0; a < 3; ++a)
+    if (st[a] < 1 || (st[a] * (int64_t)es) % 16 != 0 || st[a] > ((int64_t)1 << 40)) return false;
+  int order[3] = {0, 1, 2};
+  for (int a = 0; a < 3; ++a)
+    for (int c = a + 1; c < 3; ++c)
+      if (st[order[c]] < st[order[a]]) std::swap(order[a], order[c]);
+  int64_t covered = D;  // extent of the dimensions below, in elements
+  for (int a = 0; a < 3; ++a) {
+    const int dim = order[a];
+    if (n[dim] == 1) continue;
+    if (st[dim] < covered) return false;
+    covered = st[dim] * (n[dim] - 1) + covered;
+  }
+  *bytes = (size_t)(((int64_t)(B - 1) * l.batch + (int64_t)(H - 1) * l.head + (int64_t)(L - 1) * l.row + D) *
+                    (int64_t)es);
+  *out = Layout{l.batch, l.head, l.row};
+  return true;
+}
 
 // Checks sizes, dtype and scale; fills the size fields of *p.
 int check_sizes(int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale, int dtype,
@@ -152,21 +187,24 @@ int status_of(cudaError_t e) { return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA
 
 using namespace sdpa;
 
-extern "C" int sdpa_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
-                        int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale,
-                        int is_causal, int dtype, void* stream) {
+extern "C" int sdpa_fwd_strided(const void* q, const void* k, const void* v, void* out, float* lse,
+                                int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale,
+                                int is_causal, int dtype, const sdpa_strides_t* strides, void* stream) {
   Problem p;
   int st = check_sizes(B, Hq, Hkv, Lq, Lkv, D, scale, dtype, &p);
   if (st != SDPA_OK) return st;
-  if (!q || !k || !v || !out) return SDPA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !out || !strides) return SDPA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
     return SDPA_ERR_INVALID_ARG;
   const size_t es = elem_size(dtype);
-  const size_t qb = (size_t)B * Hq * Lq * D * es, kb = (size_t)B * Hkv * Lkv * D * es;
+  size_t qb, kb, vb, ob;
+  if (!check_layout(strides->q, B, Hq, Lq, D, es, &p.lq, &qb) || !check_layout(strides->k, B, Hkv, Lkv, D, es, &p.lk, &kb) ||
+      !check_layout(strides->v, B, Hkv, Lkv, D, es, &p.lv, &vb) || !check_layout(strides->o, B, Hq, Lq, D, es, &p.lo, &ob))
+    return SDPA_ERR_INVALID_ARG;
   const size_t lb = lse ? (size_t)B * Hq * Lq * sizeof(float) : 0;
-  if (overlaps(out, qb, q, qb) || overlaps(out, qb, k, kb) || overlaps(out, qb, v, kb) ||
-      overlaps(lse, lb, q, qb) || overlaps(lse, lb, k, kb) || overlaps(lse, lb, v, kb) ||
-      overlaps(lse, lb, out, qb))
+  if (overlaps(out, ob, q, qb) || overlaps(out, ob, k, kb) || overlaps(out, ob, v, vb) ||
+      overlaps(lse, lb, q, qb) || overlaps(lse, lb, k, kb) || overlaps(lse, lb, v, vb) ||
+      overlaps(lse, lb, out, ob))
     return SDPA_ERR_INVALID_ARG;
   p.q = q;
   p.k = k;
@@ -196,6 +234,14 @@ extern "C" int sdpa_fwd(const void* q, const void* k, const void* v, void* out, 
   return status_of(e);
 }
 
+extern "C" int sdpa_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                        int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale,
+                        int is_causal, int dtype, void* stream) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lkv < 1 || D < 1) return SDPA_ERR_INVALID_ARG;
+  const sdpa_strides_t st = contiguous_strides(Hq, Hkv, Lq, Lkv, D);
+  return sdpa_fwd_strided(q, k, v, out, lse, B, Hq, Hkv, Lq, Lkv, D, scale, is_causal, dtype, &st, stream);
+}
+
 extern "C" size_t sdpa_bwd_workspace_size(int B, int Hq, int Hkv, int Lq, int Lkv, int D,
                                           int dtype) {
   Problem p;
@@ -204,15 +250,15 @@ extern "C" size_t sdpa_bwd_workspace_size(int B, int Hq, int Hkv, int Lq, int Lk
   return (bytes + 255) / 256 * 256;
 }
 
-extern "C" int sdpa_bwd(const void* q, const void* k, const void* v, const void* out,
-                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
-                        int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale,
-                        int is_causal, int dtype, void* workspace, size_t workspace_bytes,
-                        void* stream) {
+extern "C" int sdpa_bwd_strided(const void* q, const void* k, const void* v, const void* out,
+                                const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                                int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale,
+                                int is_causal, int dtype, const sdpa_strides_t* strides,
+                                void* workspace, size_t workspace_bytes, void* stream) {
   Problem p;
   int st = check_sizes(B, Hq, Hkv, Lq, Lkv, D, scale, dtype, &p);
   if (st != SDPA_OK) return st;
-  if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return SDPA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv || !strides) return SDPA_ERR_INVALID_ARG;
   const void* all[] = {q, k, v, out, dout, lse, dq, dk, dv};
   for (const void* ptr : all)
     if (!aligned16(ptr)) return SDPA_ERR_INVALID_ARG;
@@ -220,12 +266,19 @@ extern "C" int sdpa_bwd(const void* q, const void* k, const void* v, const void*
   if (!workspace || workspace_bytes < need) return SDPA_ERR_WORKSPACE;
   if (!aligned16(workspace)) return SDPA_ERR_INVALID_ARG;
   const size_t es = elem_size(dtype);
-  const size_t qb = (size_t)B * Hq * Lq * D * es, kb = (size_t)B * Hkv * Lkv * D * es;
+  size_t qb, kb, vb, ob, dob, dqb, dkb, dvb;
+  if (!check_layout(strides->q, B, Hq, Lq, D, es, &p.lq, &qb) || !check_layout(strides->k, B, Hkv, Lkv, D, es, &p.lk, &kb) ||
+      !check_layout(strides->v, B, Hkv, Lkv, D, es, &p.lv, &vb) || !check_layout(strides->o, B, Hq, Lq, D, es, &p.lo, &ob) ||
+      !check_layout(strides->dout, B, Hq, Lq, D, es, &p.ldo, &dob) ||
+      !check_layout(strides->dq, B, Hq, Lq, D, es, &p.ldq, &dqb) ||
+      !check_layout(strides->dk, B, Hkv, Lkv, D, es, &p.ldk, &dkb) ||
+      !check_layout(strides->dv, B, Hkv, Lkv, D, es, &p.ldv, &dvb))
+    return SDPA_ERR_INVALID_ARG;
   const size_t lb = (size_t)B * Hq * Lq * sizeof(float);
   const void* ins[] = {q, k, v, out, dout, lse};
-  const size_t in_bytes[] = {qb, kb, kb, qb, qb, lb};
+  const size_t in_bytes[] = {qb, kb, vb, ob, dob, lb};
   void* outs[] = {dq, dk, dv, workspace};
-  const size_t out_bytes[] = {qb, kb, kb, need};
+  const size_t out_bytes[] = {dqb, dkb, dvb, need};
   for (int a = 0; a < 4; ++a) {
     for (int c = 0; c < 6; ++c)
       if (overlaps(outs[a], out_bytes[a], ins[c], in_bytes[c])) return SDPA_ERR_INVALID_ARG;
@@ -262,6 +315,17 @@ extern "C" int sdpa_bwd(const void* q, const void* k, const void* v, const void*
     return tc ? launch_tc_dq(p, dtype, s) : launch_simt_dq(p, dtype, s);
   });
   return status_of(e);
+}
+
+extern "C" int sdpa_bwd(const void* q, const void* k, const void* v, const void* out,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                        int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale,
+                        int is_causal, int dtype, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lkv < 1 || D < 1) return SDPA_ERR_INVALID_ARG;
+  const sdpa_strides_t st = contiguous_strides(Hq, Hkv, Lq, Lkv, D);
+  return sdpa_bwd_strided(q, k, v, out, dout, lse, dq, dk, dv, B, Hq, Hkv, Lq, Lkv, D, scale, is_causal,
+                          dtype, &st, workspace, workspace_bytes, stream);
 }
 
 extern "C" int sdpa_poll_status(void* stream) {

@@ -28,14 +28,14 @@ __device__ __forceinline__ float reduce4(float x) {
   return x;
 }
 
-// Cooperative load of rows [r0, r0 + kTile) of a [rows, D] slab into fp32 smem;
-// rows at or beyond `nrows` are zero.
+// Cooperative load of rows [r0, r0 + kTile) of a slab of rows `rs` elements apart into
+// fp32 smem; rows at or beyond `nrows` are zero.
 template <typename T, int D>
-__device__ __forceinline__ void load_tile(float (*dst)[D], const T* src, int r0, int nrows) {
+__device__ __forceinline__ void load_tile(float (*dst)[D], const T* src, int64_t rs, int r0, int nrows) {
   for (int e = threadIdx.x; e < kTile * D; e += kThreads) {
     const int rr = e / D, d = e % D;
     const int r = r0 + rr;
-    dst[rr][d] = r < nrows ? Elem<T>::to_f(src[(int64_t)r * D + d]) : 0.f;
+    dst[rr][d] = r < nrows ? Elem<T>::to_f(src[(int64_t)r * rs + d]) : 0.f;
   }
 }
 
@@ -48,9 +48,9 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Problem p) {
   const int b = blockIdx.z, h = blockIdx.y, g = h / p.G;
   const int i = blockIdx.x * kRows + r;
   const bool valid = i < p.Lq;
-  const T* qp = (const T*)p.q + q_row(p, b, h, valid ? i : 0) * D;
-  const T* kp = (const T*)p.k + kv_row(p, b, g, 0) * D;
-  const T* vp = (const T*)p.v + kv_row(p, b, g, 0) * D;
+  const T* qp = row_ptr<T>(p.q, p.lq, b, h, valid ? i : 0);
+  const T* kp = row_ptr<T>(p.k, p.lk, b, g, 0);
+  const T* vp = row_ptr<T>(p.v, p.lv, b, g, 0);
 
   float qr[DPT], o[DPT];
 #pragma unroll
@@ -64,8 +64,8 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Problem p) {
 
   for (int j0 = 0; j0 < kv_end; j0 += kTile) {
     __syncthreads();
-    load_tile<T, D>(ks, kp, j0, p.Lkv);
-    load_tile<T, D>(vs, vp, j0, p.Lkv);
+    load_tile<T, D>(ks, kp, p.lk.sl, j0, p.Lkv);
+    load_tile<T, D>(vs, vp, p.lv.sl, j0, p.Lkv);
     __syncthreads();
     float s[kTile];
     float tmax = neg_inf();
@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Problem p) {
   }
   if (!valid) return;
   const float inv = 1.f / l;
-  T* op = (T*)p.out + q_row(p, b, h, i) * D;
+  T* op = row_ptr<T>(p.out, p.lo, b, h, i);
 #pragma unroll
   for (int t = 0; t < DPT; ++t) op[sub + kTpr * t] = Elem<T>::from_f(o[t] * inv);
   if (p.lse && sub == 0) p.lse[q_row(p, b, h, i)] = (m + log2f(l)) * kLn2;
@@ -113,10 +113,10 @@ __global__ void __launch_bounds__(kThreads) simt_dq_kernel(Problem p) {
   const int i = blockIdx.x * kRows + r;
   const bool valid = i < p.Lq;
   const int64_t row = q_row(p, b, h, valid ? i : 0);
-  const T* qp = (const T*)p.q + row * D;
-  const T* dop = (const T*)p.dout + row * D;
-  const T* kp = (const T*)p.k + kv_row(p, b, g, 0) * D;
-  const T* vp = (const T*)p.v + kv_row(p, b, g, 0) * D;
+  const T* qp = row_ptr<T>(p.q, p.lq, b, h, valid ? i : 0);
+  const T* dop = row_ptr<T>(p.dout, p.ldo, b, h, valid ? i : 0);
+  const T* kp = row_ptr<T>(p.k, p.lk, b, g, 0);
+  const T* vp = row_ptr<T>(p.v, p.lv, b, g, 0);
 
   float qr[DPT], dor[DPT], dq[DPT];
 #pragma unroll
@@ -132,8 +132,8 @@ __global__ void __launch_bounds__(kThreads) simt_dq_kernel(Problem p) {
 
   for (int j0 = 0; j0 < kv_end; j0 += kTile) {
     __syncthreads();
-    load_tile<T, D>(ks, kp, j0, p.Lkv);
-    load_tile<T, D>(vs, vp, j0, p.Lkv);
+    load_tile<T, D>(ks, kp, p.lk.sl, j0, p.Lkv);
+    load_tile<T, D>(vs, vp, p.lv.sl, j0, p.Lkv);
     __syncthreads();
 #pragma unroll 4
     for (int jj = 0; jj < kTile; ++jj) {
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kThreads) simt_dq_kernel(Problem p) {
     }
   }
   if (!valid) return;
-  T* out = (T*)p.dq + row * D;
+  T* out = row_ptr<T>(p.dq, p.ldq, b, h, i);
 #pragma unroll
   for (int t = 0; t < DPT; ++t) out[sub + kTpr * t] = Elem<T>::from_f(dq[t] * p.scale);
 }
@@ -170,9 +170,8 @@ __global__ void __launch_bounds__(kThreads) simt_dkdv_kernel(Problem p) {
   const int b = blockIdx.z, g = blockIdx.y;
   const int j = blockIdx.x * kRows + r;
   const bool valid = j < p.Lkv;
-  const int64_t krow = kv_row(p, b, g, valid ? j : 0);
-  const T* kp = (const T*)p.k + krow * D;
-  const T* vp = (const T*)p.v + krow * D;
+  const T* kp = row_ptr<T>(p.k, p.lk, b, g, valid ? j : 0);
+  const T* vp = row_ptr<T>(p.v, p.lv, b, g, valid ? j : 0);
 
   float kr[DPT], vr[DPT], dk[DPT], dv[DPT];
 #pragma unroll
@@ -187,14 +186,14 @@ __global__ void __launch_bounds__(kThreads) simt_dkdv_kernel(Problem p) {
 
   for (int hh = 0; hh < p.G; ++hh) {
     const int h = g * p.G + hh;
-    const T* qp = (const T*)p.q + q_row(p, b, h, 0) * D;
-    const T* dop = (const T*)p.dout + q_row(p, b, h, 0) * D;
+    const T* qp = row_ptr<T>(p.q, p.lq, b, h, 0);
+    const T* dop = row_ptr<T>(p.dout, p.ldo, b, h, 0);
     const float* lsep = p.lse + q_row(p, b, h, 0);
     const float* dlp = p.delta + q_row(p, b, h, 0);
     for (int i0 = i_begin; i0 < p.Lq; i0 += kTile) {
       __syncthreads();
-      load_tile<T, D>(qs, qp, i0, p.Lq);
-      load_tile<T, D>(dos, dop, i0, p.Lq);
+      load_tile<T, D>(qs, qp, p.lq.sl, i0, p.Lq);
+      load_tile<T, D>(dos, dop, p.ldo.sl, i0, p.Lq);
       if (threadIdx.x < kTile) {
         const int i = i0 + threadIdx.x;
         lse2s[threadIdx.x] = i < p.Lq ? lsep[i] * kLog2e : 0.f;
@@ -224,8 +223,8 @@ __global__ void __launch_bounds__(kThreads) simt_dkdv_kernel(Problem p) {
     }
   }
   if (!valid) return;
-  T* dkp = (T*)p.dk + krow * D;
-  T* dvp = (T*)p.dv + krow * D;
+  T* dkp = row_ptr<T>(p.dk, p.ldk, b, g, j);
+  T* dvp = row_ptr<T>(p.dv, p.ldv, b, g, j);
 #pragma unroll
   for (int t = 0; t < DPT; ++t) {
     dkp[sub + kTpr * t] = Elem<T>::from_f(dk[t] * p.scale);
@@ -263,24 +262,24 @@ __device__ __forceinline__ void load_elems(const T* src, float (&dst)[N]) {
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kDeltaThreads) delta_kernel(const T* __restrict__ o,
-                                                               const T* __restrict__ dout,
-                                                               float* __restrict__ delta,
-                                                               int64_t rows) {
+__global__ void __launch_bounds__(kDeltaThreads) delta_kernel(Problem p, int64_t rows) {
   constexpr int EPT = D / kDeltaTpr;
-  const int64_t row = ((int64_t)blockIdx.x * kDeltaThreads + threadIdx.x) / kDeltaTpr;
+  const int64_t row = ((int64_t)blockIdx.x * kDeltaThreads + threadIdx.x) / kDeltaTpr;  // (b·Hq + h)·Lq + i
   const int sub = threadIdx.x % kDeltaTpr;
   float acc = 0.f;
   if (row < rows) {
+    const int i = (int)(row % p.Lq);
+    const int64_t bh = row / p.Lq;
+    const int b = (int)(bh / p.Hq), h = (int)(bh % p.Hq);
     float a[EPT], c[EPT];
-    load_elems<T, EPT>(o + row * D + sub * EPT, a);
-    load_elems<T, EPT>(dout + row * D + sub * EPT, c);
+    load_elems<T, EPT>(row_ptr<T>(p.o, p.lo, b, h, i) + sub * EPT, a);
+    load_elems<T, EPT>(row_ptr<T>(p.dout, p.ldo, b, h, i) + sub * EPT, c);
 #pragma unroll
     for (int n = 0; n < EPT; ++n) acc = fmaf(a[n], c[n], acc);
   }
 #pragma unroll
   for (int off = kDeltaTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (row < rows && sub == 0) delta[row] = acc;
+  if (row < rows && sub == 0) p.delta[row] = acc;
 }
 
 template <typename T, int D>
@@ -309,8 +308,7 @@ cudaError_t delta_t(const Problem& p, cudaStream_t s) {
   const int64_t rows = (int64_t)p.B * p.Hq * p.Lq;
   const int64_t rows_per_block = kDeltaThreads / kDeltaTpr;
   const int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
-  delta_kernel<T, D><<<(unsigned)blocks, kDeltaThreads, 0, s>>>((const T*)p.o, (const T*)p.dout,
-                                                                  p.delta, rows);
+  delta_kernel<T, D><<<(unsigned)blocks, kDeltaThreads, 0, s>>>(p, rows);
   return cudaGetLastError();
 }
 

@@ -189,8 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tdo);
       mbar_arrive_expect_tx(&bars.own_full, 2 * L::kTileBytes);
       for (int cb = 0; cb < kCB; ++cb) {
-        tma_load_3d(sm + L::kOwnA + cb * L::kCbStride, &tk, &bars.own_full, cb * 64, j0, b * p.Hkv + g);
-        tma_load_3d(sm + L::kOwnB + cb * L::kCbStride, &tv, &bars.own_full, cb * 64, j0, b * p.Hkv + g);
+        tma_load_4d(sm + L::kOwnA + cb * L::kCbStride, &tk, &bars.own_full, cb * 64, j0, g, b);
+        tma_load_4d(sm + L::kOwnB + cb * L::kCbStride, &tv, &bars.own_full, cb * 64, j0, g, b);
       }
     }
     int issued = 0;
@@ -205,9 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&bars.ring_full[s], 2 * L::kTileBytes);
         uint8_t* st = sm + L::kRing + s * L::kStageBytes;
         for (int cb = 0; cb < kCB; ++cb) {
-          tma_load_3d(st + cb * L::kCbStride, &tq, &bars.ring_full[s], cb * 64, i0, b * p.Hq + h);
-          tma_load_3d(st + L::kTileBytes + cb * L::kCbStride, &tdo, &bars.ring_full[s], cb * 64, i0,
-                      b * p.Hq + h);
+          tma_load_4d(st + cb * L::kCbStride, &tq, &bars.ring_full[s], cb * 64, i0, h, b);
+          tma_load_4d(st + L::kTileBytes + cb * L::kCbStride, &tdo, &bars.ring_full[s], cb * 64, i0, h, b);
         }
       }
       // Per-query vectors, negated for the packed math of the element warps.
@@ -361,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (named_sync_and(1 + w, 128, ok) && r == 0) {
       for (int cb = 0; cb < kCB; ++cb)
-        tma_store_3d(w == 0 ? &tdv : &tdk, stage + cb * L::kCbStride, cb * 64, j0, b * p.Hkv + g);
+        tma_store_4d(w == 0 ? &tdv : &tdk, stage + cb * L::kCbStride, cb * 64, j0, g, b);
       bulk_commit();
       bulk_wait_read();
     }
@@ -472,8 +471,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       prefetch_tmap(&tv);
       mbar_arrive_expect_tx(&bars.own_full, 2 * L::kTileBytes);
       for (int cb = 0; cb < kCB; ++cb) {
-        tma_load_3d(sm + L::kQ + cb * kCbStride, &tq, &bars.own_full, cb * 64, i0, b * p.Hq + h);
-        tma_load_3d(sm + L::kDo + cb * kCbStride, &tdo, &bars.own_full, cb * 64, i0, b * p.Hq + h);
+        tma_load_4d(sm + L::kQ + cb * kCbStride, &tq, &bars.own_full, cb * 64, i0, h, b);
+        tma_load_4d(sm + L::kDo + cb * kCbStride, &tdo, &bars.own_full, cb * 64, i0, h, b);
       }
       int k_issued = 0, v_issued = 0;
       bool ok = true;
@@ -482,14 +481,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         if (!(ok = mbar_wait(&bars.k_empty[sk], ((n / kKStages) & 1) ^ 1, wc))) break;
         mbar_arrive_expect_tx(&bars.k_full[sk], L::kTileBytes);
         for (int cb = 0; cb < kCB; ++cb)
-          tma_load_3d(sm + L::kK + sk * L::kTileBytes + cb * kCbStride, &tk, &bars.k_full[sk], cb * 64,
-                      n * kBlk, b * p.Hkv + g);
+          tma_load_4d(sm + L::kK + sk * L::kTileBytes + cb * kCbStride, &tk, &bars.k_full[sk], cb * 64,
+                      n * kBlk, g, b);
         k_issued = n + 1;
         if (!(ok = mbar_wait(&bars.v_empty[sv], ((n / kVStages) & 1) ^ 1, wc))) break;
         mbar_arrive_expect_tx(&bars.v_full[sv], L::kTileBytes);
         for (int cb = 0; cb < kCB; ++cb)
-          tma_load_3d(sm + L::kV + sv * L::kTileBytes + cb * kCbStride, &tv, &bars.v_full[sv], cb * 64,
-                      n * kBlk, b * p.Hkv + g);
+          tma_load_4d(sm + L::kV + sv * L::kTileBytes + cb * kCbStride, &tv, &bars.v_full[sv], cb * 64,
+                      n * kBlk, g, b);
         v_issued = n + 1;
       }
       if (!ok || bars.abort) {
@@ -629,7 +628,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         fence_async_smem();
       }
       if (named_sync_and(1 + w, 128, ok) && r == 0) {
-        for (int cb = w; cb < kCB; cb += 2) tma_store_3d(&tdq, sm + L::kQ + cb * kCbStride, cb * 64, i0, b * p.Hq + h);
+        for (int cb = w; cb < kCB; cb += 2) tma_store_4d(&tdq, sm + L::kQ + cb * kCbStride, cb * 64, i0, h, b);
         bulk_commit();
         bulk_wait_read();
       }
@@ -648,13 +647,13 @@ struct Maps {
 };
 
 bool make_maps(const Problem& p, int D, Maps* m) {
-  return make_tmap_3d(&m->q, p.q, D, p.Lq, p.B * p.Hq, kRows) &&
-         make_tmap_3d(&m->dq, p.dq, D, p.Lq, p.B * p.Hq, kRows) &&
-         make_tmap_3d(&m->dk, p.dk, D, p.Lkv, p.B * p.Hkv, kRows) &&
-         make_tmap_3d(&m->dv, p.dv, D, p.Lkv, p.B * p.Hkv, kRows) &&
-         make_tmap_3d(&m->dout, p.dout, D, p.Lq, p.B * p.Hq, kRows) &&
-         make_tmap_3d(&m->k, p.k, D, p.Lkv, p.B * p.Hkv, kRows) &&
-         make_tmap_3d(&m->v, p.v, D, p.Lkv, p.B * p.Hkv, kRows);
+  return make_tmap_4d(&m->q, p.q, D, p.Lq, p.Hq, p.B, p.lq, kRows) &&
+         make_tmap_4d(&m->dq, p.dq, D, p.Lq, p.Hq, p.B, p.ldq, kRows) &&
+         make_tmap_4d(&m->dk, p.dk, D, p.Lkv, p.Hkv, p.B, p.ldk, kRows) &&
+         make_tmap_4d(&m->dv, p.dv, D, p.Lkv, p.Hkv, p.B, p.ldv, kRows) &&
+         make_tmap_4d(&m->dout, p.dout, D, p.Lq, p.Hq, p.B, p.ldo, kRows) &&
+         make_tmap_4d(&m->k, p.k, D, p.Lkv, p.Hkv, p.B, p.lk, kRows) &&
+         make_tmap_4d(&m->v, p.v, D, p.Lkv, p.Hkv, p.B, p.lv, kRows);
 }
 
 template <typename T, int D>

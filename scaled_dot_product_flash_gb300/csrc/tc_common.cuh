@@ -79,20 +79,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
 }
 
 // ------------------------------------------------------------------ TMA
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
-                                            int y, int z) {
+// Tiled load of box {64 elements, rows, 1, 1} at (x = element column, y = row, h = head,
+// b = batch) of a map made by make_tmap_4d.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
+                                            int y, int h, int b) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(h), "r"(b)
       : "memory");
 }
 // Tiled bulk store shared → global (rows past the tensor's extent are not written).  The
 // caller commits the group and waits for its reads before the shared memory is reused.
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y, int z) {
-  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void* src, int x, int y, int h,
+                                             int b) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
-               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(h), "r"(b)
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
@@ -377,8 +380,11 @@ __device__ __forceinline__ void ex2_pair(uint64_t x, float& p0, float& p1) {
 }  // namespace tc
 
 // ------------------------------------------------------------------ host: tensor maps
-// 3-D tiled map over a [planes, rows, D] 16-bit tensor, box {64, box_rows, 1}, 128-byte
-// swizzle, zero fill out of bounds.  Returns false if the driver refuses it.
-bool make_tmap_3d(CUtensorMap* map, const void* base, int D, int rows, int planes, int box_rows);
+// 4-D tiled map over a [batch, heads, rows, D] 16-bit tensor with element strides l (D
+// contiguous; the strides must be multiples of 8 elements), box {64, box_rows, 1, 1},
+// 128-byte swizzle, zero fill out of bounds on loads and clipping on stores.  Returns
+// false if the driver refuses it.
+bool make_tmap_4d(CUtensorMap* map, const void* base, int D, int rows, int heads, int batch, const Layout& l,
+                  int box_rows);
 
 }  // namespace sdpa

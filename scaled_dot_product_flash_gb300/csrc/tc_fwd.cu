@@ -273,8 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(&bars.q_full, nq * L::kTileBytes);
       for (int w = 0; w < nq; ++w)
         for (int cb = 0; cb < kCB; ++cb)
-          tma_load_3d(sm + L::kQOff + w * L::kTileBytes + cb * 16384, &tq, &bars.q_full, cb * 64,
-                      row0 + w * kBM, b * p.Hq + h);
+          tma_load_4d(sm + L::kQOff + w * L::kTileBytes + cb * 16384, &tq, &bars.q_full, cb * 64,
+                      row0 + w * kBM, h, b);
       int issued = 0;
       bool ok = true;
       for (int j = 0; ok && j < nmax; ++j) {
@@ -285,8 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (p.inject == 1 && it == 0) continue;  // test hook: never deliver the first K tile
           mbar_arrive_expect_tx(&bars.kv_full[s], L::kTileBytes);
           for (int cb = 0; cb < kCB; ++cb)
-            tma_load_3d(sm + L::kRingOff + s * L::kTileBytes + cb * 16384, kv ? &tv : &tk,
-                        &bars.kv_full[s], cb * 64, j * kBN, b * p.Hkv + g);
+            tma_load_4d(sm + L::kRingOff + s * L::kTileBytes + cb * 16384, kv ? &tv : &tk,
+                        &bars.kv_full[s], cb * 64, j * kBN, g, b);
           issued = it + 1;
         }
       }
@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i < p.Lq && p.lse) p.lse[q_row(p, b, h, i)] = (m + __log2f(l)) * kLn2;
       }
       if (named_sync_and(1 + w, kBM, ok) && r == 0) {
-        for (int cb = 0; cb < kCB; ++cb) tma_store_3d(&to, stage + cb * 16384, cb * 64, tile_row0, b * p.Hq + h);
+        for (int cb = 0; cb < kCB; ++cb) tma_store_4d(&to, stage + cb * 16384, cb * 64, tile_row0, h, b);
         bulk_commit();
         bulk_wait_read();
       }
@@ -462,9 +462,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <typename T, int D>
 cudaError_t tc_fwd_t(const Problem& p, cudaStream_t s) {
   CUtensorMap tq, tk, tv, to;
-  if (!make_tmap_3d(&tq, p.q, D, p.Lq, p.B * p.Hq, kBM) || !make_tmap_3d(&to, p.out, D, p.Lq, p.B * p.Hq, kBM) ||
-      !make_tmap_3d(&tk, p.k, D, p.Lkv, p.B * p.Hkv, kBN) ||
-      !make_tmap_3d(&tv, p.v, D, p.Lkv, p.B * p.Hkv, kBN))
+  if (!make_tmap_4d(&tq, p.q, D, p.Lq, p.Hq, p.B, p.lq, kBM) || !make_tmap_4d(&to, p.out, D, p.Lq, p.Hq, p.B, p.lo, kBM) ||
+      !make_tmap_4d(&tk, p.k, D, p.Lkv, p.Hkv, p.B, p.lk, kBN) ||
+      !make_tmap_4d(&tv, p.v, D, p.Lkv, p.Hkv, p.B, p.lv, kBN))
     return cudaErrorInvalidValue;
   const int smem = FwdLayout<D>::kBytes + 1024;
   auto kern = tc_fwd_kernel<T, D>;

@@ -36,14 +36,14 @@ __device__ __forceinline__ float reduce_lanes(float x) {
   return x;
 }
 
-// Copy rows [r0, r0 + n) (n <= NB) of a contiguous [*, D] slab into a float tile; rows
-// past `nrows` are zero.
+// Copy rows [r0, r0 + n) (n <= NB) of a slab of rows `rs` elements apart into a float
+// tile; rows past `nrows` are zero.
 template <typename T, int D, int NB>
-__device__ __forceinline__ void stage_rows(float (*dst)[D], const T* src, int r0, int nrows) {
+__device__ __forceinline__ void stage_rows(float (*dst)[D], const T* src, int64_t rs, int r0, int nrows) {
   for (int e = threadIdx.x; e < NB * D; e += kThreads) {
     const int rr = e / D, d = e % D;
     const int r = r0 + rr;
-    dst[rr][d] = r < nrows ? Elem<T>::to_f(src[(int64_t)r * D + d]) : 0.f;
+    dst[rr][d] = r < nrows ? Elem<T>::to_f(src[(int64_t)r * rs + d]) : 0.f;
   }
 }
 
@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(kThreads) vec_fwd_kernel(Problem p, int chunk)
 
   float qv[DPL], ov[DPL];
   {
-    const T* qp = (const T*)p.q + q_row(p, b, h, i) * D + d0;
+    const T* qp = row_ptr<T>(p.q, p.lq, b, h, i) + d0;
 #pragma unroll
     for (int t = 0; t < DPL; ++t) {
       qv[t] = row_ok ? Elem<T>::to_f(qp[t]) : 0.f;
@@ -103,13 +103,13 @@ __global__ void __launch_bounds__(kThreads) vec_fwd_kernel(Problem p, int chunk)
   int kv_end = p.Lkv;
   if (p.causal) kv_end = min(p.Lkv, p.Lq);  // query i sees keys 0..i only
   const int j_begin = c * chunk, j_end = min(kv_end, j_begin + chunk);
-  const T* kp = (const T*)p.k + kv_row(p, b, g, 0) * D;
-  const T* vp = (const T*)p.v + kv_row(p, b, g, 0) * D;
+  const T* kp = row_ptr<T>(p.k, p.lk, b, g, 0);
+  const T* vp = row_ptr<T>(p.v, p.lv, b, g, 0);
 
   for (int j0 = j_begin; j0 < j_end; j0 += NB) {
     __syncthreads();
-    stage_rows<T, D, NB>(sm.ks, kp, j0, j_end);
-    stage_rows<T, D, NB>(sm.vs, vp, j0, j_end);
+    stage_rows<T, D, NB>(sm.ks, kp, p.lk.sl, j0, j_end);
+    stage_rows<T, D, NB>(sm.vs, vp, p.lv.sl, j0, j_end);
     __syncthreads();
     // Phase 1: partial scores over this warp's head-dim slice.
 #pragma unroll 4
@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(kThreads) vec_fwd_kernel(Problem p, int chunk)
     }
     const int hh2 = r2 / p.Lq, i2 = r2 % p.Lq;
     const int64_t row = q_row(p, b, g * p.G + hh2, i2);
-    ((T*)p.out)[row * D + d] = Elem<T>::from_f(O / L);
+    row_ptr<T>(p.out, p.lo, b, g * p.G + hh2, i2)[d] = Elem<T>::from_f(O / L);
     if (p.lse && d == 0) p.lse[row] = (M + log2f(L)) * kLn2;
   }
   cluster.sync();  // peers may still be reading this block's shared memory
@@ -239,9 +239,9 @@ __global__ void __launch_bounds__(kThreads) vec_bwd_kernel(Problem p, int chunk)
     const int r2 = e / D, d = e % D;
     float qv = 0.f, dov = 0.f;
     if (r2 < R) {
-      const int64_t row = q_row(p, b, g * p.G + r2 / p.Lq, r2 % p.Lq);
-      qv = Elem<T>::to_f(((const T*)p.q)[row * D + d]);
-      dov = Elem<T>::to_f(((const T*)p.dout)[row * D + d]);
+      const int h2 = g * p.G + r2 / p.Lq, i2 = r2 % p.Lq;
+      qv = Elem<T>::to_f(row_ptr<T>(p.q, p.lq, b, h2, i2)[d]);
+      dov = Elem<T>::to_f(row_ptr<T>(p.dout, p.ldo, b, h2, i2)[d]);
     }
     sm.qs[r2][d] = qv;
     sm.dos[r2][d] = dov;
@@ -249,9 +249,10 @@ __global__ void __launch_bounds__(kThreads) vec_bwd_kernel(Problem p, int chunk)
   for (int r2 = warp; r2 < RP; r2 += kWarps) {
     float acc = 0.f, l2 = 0.f;
     if (r2 < R) {
-      const int64_t row = q_row(p, b, g * p.G + r2 / p.Lq, r2 % p.Lq);
-      const T* op = (const T*)p.o + row * D;
-      const T* dop = (const T*)p.dout + row * D;
+      const int h2 = g * p.G + r2 / p.Lq, i2 = r2 % p.Lq;
+      const int64_t row = q_row(p, b, h2, i2);
+      const T* op = row_ptr<T>(p.o, p.lo, b, h2, i2);
+      const T* dop = row_ptr<T>(p.dout, p.ldo, b, h2, i2);
       for (int d = lane; d < D; d += 32) acc = fmaf(Elem<T>::to_f(op[d]), Elem<T>::to_f(dop[d]), acc);
       l2 = p.lse[row] * kLog2e;
     }
@@ -274,15 +275,15 @@ __global__ void __launch_bounds__(kThreads) vec_bwd_kernel(Problem p, int chunk)
   if (p.causal) kv_end = min(p.Lkv, p.Lq);
   const int j_begin = c * chunk, j_own_end = min(p.Lkv, j_begin + chunk);
   const int j_end = min(kv_end, j_own_end);
-  const T* kp = (const T*)p.k + kv_row(p, b, g, 0) * D;
-  const T* vp = (const T*)p.v + kv_row(p, b, g, 0) * D;
-  T* dkp = (T*)p.dk + kv_row(p, b, g, 0) * D;
-  T* dvp = (T*)p.dv + kv_row(p, b, g, 0) * D;
+  const T* kp = row_ptr<T>(p.k, p.lk, b, g, 0);
+  const T* vp = row_ptr<T>(p.v, p.lv, b, g, 0);
+  T* dkp = row_ptr<T>(p.dk, p.ldk, b, g, 0);
+  T* dvp = row_ptr<T>(p.dv, p.ldv, b, g, 0);
 
   for (int j0 = j_begin; j0 < j_end; j0 += NB) {
     __syncthreads();
-    stage_rows<T, D, NB>(sm.ks, kp, j0, j_end);
-    stage_rows<T, D, NB>(sm.vs, vp, j0, j_end);
+    stage_rows<T, D, NB>(sm.ks, kp, p.lk.sl, j0, j_end);
+    stage_rows<T, D, NB>(sm.vs, vp, p.lv.sl, j0, j_end);
     __syncthreads();
     // Phase 1: partial S = Q·Kᵀ and dP = dO·Vᵀ over this warp's head-dim slice.
 #pragma unroll 4
@@ -345,8 +346,8 @@ __global__ void __launch_bounds__(kThreads) vec_bwd_kernel(Problem p, int chunk)
       if (j < j_end) {
 #pragma unroll
         for (int t = 0; t < kDims; ++t) {
-          dkp[(int64_t)j * D + dd + t] = Elem<T>::from_f(dk[t] * p.scale);
-          dvp[(int64_t)j * D + dd + t] = Elem<T>::from_f(dv[t]);
+          dkp[(int64_t)j * p.ldk.sl + dd + t] = Elem<T>::from_f(dk[t] * p.scale);
+          dvp[(int64_t)j * p.ldv.sl + dd + t] = Elem<T>::from_f(dv[t]);
         }
       }
     }
@@ -354,8 +355,9 @@ __global__ void __launch_bounds__(kThreads) vec_bwd_kernel(Problem p, int chunk)
   // Keys this block owns but no query can see (causal, j >= Lq) get zero gradients.
   for (int64_t e = (int64_t)max(j_end, j_begin) * D + threadIdx.x; e < (int64_t)j_own_end * D;
        e += kThreads) {
-    dkp[e] = Elem<T>::from_f(0.f);
-    dvp[e] = Elem<T>::from_f(0.f);
+    const int64_t jj = e / D, d = e % D;
+    dkp[jj * p.ldk.sl + d] = Elem<T>::from_f(0.f);
+    dvp[jj * p.ldv.sl + d] = Elem<T>::from_f(0.f);
   }
   // Merge the dQ partials of the cluster's blocks.
 #pragma unroll
@@ -367,8 +369,7 @@ __global__ void __launch_bounds__(kThreads) vec_bwd_kernel(Problem p, int chunk)
     if (r2 >= R) continue;
     float acc = 0.f;
     for (int cc = 0; cc < kCs; ++cc) acc += cluster.map_shared_rank(&sm, cc)->dqacc[r2][d];
-    const int64_t row = q_row(p, b, g * p.G + r2 / p.Lq, r2 % p.Lq);
-    ((T*)p.dq)[row * D + d] = Elem<T>::from_f(acc * p.scale);
+    row_ptr<T>(p.dq, p.ldq, b, g * p.G + r2 / p.Lq, r2 % p.Lq)[d] = Elem<T>::from_f(acc * p.scale);
   }
   cluster.sync();
 }

@@ -127,10 +127,10 @@ __global__ void __launch_bounds__(128) vec_mma_fwd_kernel(const __grid_constant_
     const int s = t % kRing;
     mbar_arrive_expect_tx(&full[s], L::kStageBytes);
     for (int cb = 0; cb < D / 64; ++cb) {
-      tma_load_3d(sm + s * L::kStageBytes + cb * (kKeys * 128), &tk, &full[s], cb * 64, j_begin + t * kKeys,
-                  b * p.Hkv + g);
-      tma_load_3d(sm + s * L::kStageBytes + L::kTileBytes + cb * (kKeys * 128), &tv, &full[s], cb * 64,
-                  j_begin + t * kKeys, b * p.Hkv + g);
+      tma_load_4d(sm + s * L::kStageBytes + cb * (kKeys * 128), &tk, &full[s], cb * 64, j_begin + t * kKeys, g,
+                  b);
+      tma_load_4d(sm + s * L::kStageBytes + L::kTileBytes + cb * (kKeys * 128), &tv, &full[s], cb * 64,
+                  j_begin + t * kKeys, g, b);
     }
   };
   int issued = 0;  // tiles whose loads thread 0 has issued
@@ -141,16 +141,15 @@ __global__ void __launch_bounds__(128) vec_mma_fwd_kernel(const __grid_constant_
   const int r0 = 16 * mt + lane / 4, r1 = r0 + 8;
   uint32_t qf[D / 16][4];
   {
-    const T* q = static_cast<const T*>(p.q);
-    const int64_t row0 = r0 < R ? q_row(p, b, g * p.G + r0 / p.Lq, r0 % p.Lq) : -1;
-    const int64_t row1 = r1 < R ? q_row(p, b, g * p.G + r1 / p.Lq, r1 % p.Lq) : -1;
+    const T* q0 = r0 < R ? row_ptr<T>(p.q, p.lq, b, g * p.G + r0 / p.Lq, r0 % p.Lq) : nullptr;
+    const T* q1 = r1 < R ? row_ptr<T>(p.q, p.lq, b, g * p.G + r1 / p.Lq, r1 % p.Lq) : nullptr;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const int col = 16 * kk + 2 * (lane % 4);
-      qf[kk][0] = row0 >= 0 ? *reinterpret_cast<const uint32_t*>(q + row0 * D + col) : 0u;
-      qf[kk][1] = row1 >= 0 ? *reinterpret_cast<const uint32_t*>(q + row1 * D + col) : 0u;
-      qf[kk][2] = row0 >= 0 ? *reinterpret_cast<const uint32_t*>(q + row0 * D + col + 8) : 0u;
-      qf[kk][3] = row1 >= 0 ? *reinterpret_cast<const uint32_t*>(q + row1 * D + col + 8) : 0u;
+      qf[kk][0] = q0 ? *reinterpret_cast<const uint32_t*>(q0 + col) : 0u;
+      qf[kk][1] = q1 ? *reinterpret_cast<const uint32_t*>(q1 + col) : 0u;
+      qf[kk][2] = q0 ? *reinterpret_cast<const uint32_t*>(q0 + col + 8) : 0u;
+      qf[kk][3] = q1 ? *reinterpret_cast<const uint32_t*>(q1 + col + 8) : 0u;
     }
   }
   const int i0 = r0 < R ? r0 % p.Lq : 0, i1 = r1 < R ? r1 % p.Lq : 0;
@@ -332,7 +331,7 @@ __global__ void __launch_bounds__(128) vec_mma_fwd_kernel(const __grid_constant_
       O = fmaf(cluster.map_shared_rank(cta_o, cc)[r * D + d], wgt, O);
     }
     const int64_t row = q_row(p, b, g * p.G + r / p.Lq, r % p.Lq);
-    static_cast<T*>(p.out)[row * D + d] = Elem<T>::from_f(O / Lsum);
+    row_ptr<T>(p.out, p.lo, b, g * p.G + r / p.Lq, r % p.Lq)[d] = Elem<T>::from_f(O / Lsum);
     if (p.lse && d == 0) p.lse[row] = (M + __log2f(Lsum)) * kLn2;
   }
   cluster.sync();  // peers may still be reading this block's shared memory
@@ -342,7 +341,7 @@ __global__ void __launch_bounds__(128) vec_mma_fwd_kernel(const __grid_constant_
 template <typename T, int D, int MT>
 cudaError_t vec_mma_fwd_t(const Problem& p, cudaStream_t s) {
   CUtensorMap tk, tv;
-  if (!make_tmap_3d(&tk, p.k, D, p.Lkv, p.B * p.Hkv, kKeys) || !make_tmap_3d(&tv, p.v, D, p.Lkv, p.B * p.Hkv, kKeys))
+  if (!make_tmap_4d(&tk, p.k, D, p.Lkv, p.Hkv, p.B, p.lk, kKeys) || !make_tmap_4d(&tv, p.v, D, p.Lkv, p.Hkv, p.B, p.lv, kKeys))
     return cudaErrorInvalidValue;
   const int smem = VmLayout<D, MT>::kBytes + 1024;
   auto kern = vec_mma_fwd_kernel<T, D, MT>;
@@ -438,10 +437,10 @@ __global__ void __launch_bounds__(128) vec_mma_bwd_kernel(const __grid_constant_
     const int s = t % kBwdRing;
     mbar_arrive_expect_tx(&full[s], L::kStageBytes);
     for (int cb = 0; cb < D / 64; ++cb) {
-      tma_load_3d(sm + s * L::kStageBytes + cb * (kKeys * 128), &tk, &full[s], cb * 64, j_begin + t * kKeys,
-                  b * p.Hkv + g);
-      tma_load_3d(sm + s * L::kStageBytes + L::kTileBytes + cb * (kKeys * 128), &tv, &full[s], cb * 64,
-                  j_begin + t * kKeys, b * p.Hkv + g);
+      tma_load_4d(sm + s * L::kStageBytes + cb * (kKeys * 128), &tk, &full[s], cb * 64, j_begin + t * kKeys, g,
+                  b);
+      tma_load_4d(sm + s * L::kStageBytes + L::kTileBytes + cb * (kKeys * 128), &tv, &full[s], cb * 64,
+                  j_begin + t * kKeys, g, b);
     }
   };
   int issued = 0;
@@ -450,15 +449,13 @@ __global__ void __launch_bounds__(128) vec_mma_bwd_kernel(const __grid_constant_
 
   // Stage Q and dO (zero rows past R); δ_r = Σ_d dO·O and −log2e·lse per row.
   {
-    const T* qg = static_cast<const T*>(p.q);
-    const T* dog = static_cast<const T*>(p.dout);
     for (int e = threadIdx.x; e < L::kRows * (D / 2); e += blockDim.x) {
       const int r = e / (D / 2), d = 2 * (e % (D / 2));
       uint32_t qv = 0u, dv = 0u;
       if (r < R) {
-        const int64_t row = q_row(p, b, g * p.G + r / p.Lq, r % p.Lq);
-        qv = *reinterpret_cast<const uint32_t*>(qg + row * D + d);
-        dv = *reinterpret_cast<const uint32_t*>(dog + row * D + d);
+        const int h2 = g * p.G + r / p.Lq, i2 = r % p.Lq;
+        qv = *reinterpret_cast<const uint32_t*>(row_ptr<T>(p.q, p.lq, b, h2, i2) + d);
+        dv = *reinterpret_cast<const uint32_t*>(row_ptr<T>(p.dout, p.ldo, b, h2, i2) + d);
       }
       *reinterpret_cast<uint32_t*>(sm + L::kQ + r * L::kRowStride + d * 2) = qv;
       *reinterpret_cast<uint32_t*>(sm + L::kDo + r * L::kRowStride + d * 2) = dv;
@@ -466,9 +463,11 @@ __global__ void __launch_bounds__(128) vec_mma_bwd_kernel(const __grid_constant_
     for (int r = warp; r < L::kRows; r += kWarps) {
       float acc = 0.f, nl = -__int_as_float(0x7f800000);
       if (r < R) {
-        const int64_t row = q_row(p, b, g * p.G + r / p.Lq, r % p.Lq);
-        const T* op = static_cast<const T*>(p.o) + row * D;
-        for (int d = lane; d < D; d += 32) acc = fmaf(Elem<T>::to_f(op[d]), Elem<T>::to_f(dog[row * D + d]), acc);
+        const int h2 = g * p.G + r / p.Lq, i2 = r % p.Lq;
+        const int64_t row = q_row(p, b, h2, i2);
+        const T* op = row_ptr<T>(p.o, p.lo, b, h2, i2);
+        const T* dop = row_ptr<T>(p.dout, p.ldo, b, h2, i2);
+        for (int d = lane; d < D; d += 32) acc = fmaf(Elem<T>::to_f(op[d]), Elem<T>::to_f(dop[d]), acc);
         nl = -p.lse[row] * kLog2e;
       }
 #pragma unroll
@@ -488,8 +487,8 @@ __global__ void __launch_bounds__(128) vec_mma_bwd_kernel(const __grid_constant_
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
     for (int nt = 0; nt < kDqTiles; ++nt) dq[mt][nt][0] = dq[mt][nt][1] = dq[mt][nt][2] = dq[mt][nt][3] = 0.f;
-  T* dkg = static_cast<T*>(p.dk) + kv_row(p, b, g, 0) * D;
-  T* dvg = static_cast<T*>(p.dv) + kv_row(p, b, g, 0) * D;
+  T* dkg = row_ptr<T>(p.dk, p.ldk, b, g, 0);
+  T* dvg = row_ptr<T>(p.dv, p.ldv, b, g, 0);
   const int mm = lane / 8;
 
   bool ok = true;
@@ -566,14 +565,15 @@ __global__ void __launch_bounds__(128) vec_mma_bwd_kernel(const __grid_constant_
       }
       const float mul = which == 0 ? 1.f : p.scale;
       T* dst = which == 0 ? dvg : dkg;
+      const int64_t rs = which == 0 ? p.ldv.sl : p.ldk.sl;
       const int ja = tile_key0 + 16 * warp + lane / 4, jb = ja + 8;
 #pragma unroll
       for (int dn = 0; dn < D / 8; ++dn) {
         const int d = 8 * dn + 2 * (lane % 4);
         if (ja < j_own_end)
-          *reinterpret_cast<uint32_t*>(dst + (int64_t)ja * D + d) = pack2<T>(acc[dn][0] * mul, acc[dn][1] * mul);
+          *reinterpret_cast<uint32_t*>(dst + (int64_t)ja * rs + d) = pack2<T>(acc[dn][0] * mul, acc[dn][1] * mul);
         if (jb < j_own_end)
-          *reinterpret_cast<uint32_t*>(dst + (int64_t)jb * D + d) = pack2<T>(acc[dn][2] * mul, acc[dn][3] * mul);
+          *reinterpret_cast<uint32_t*>(dst + (int64_t)jb * rs + d) = pack2<T>(acc[dn][2] * mul, acc[dn][3] * mul);
       }
     }
     // ---- phase C (ii): dQ[:, w·D/4 : (w+1)·D/4) += dS·K over this tile's 64 keys
@@ -612,8 +612,9 @@ __global__ void __launch_bounds__(128) vec_mma_bwd_kernel(const __grid_constant_
   // Keys this block owns that no query can see (causal, j >= Lq) get zero gradients.
   for (int64_t e = (int64_t)max(j_begin + ntiles * kKeys, j_begin) * D + threadIdx.x; e < (int64_t)j_own_end * D;
        e += blockDim.x) {
-    dkg[e] = Elem<T>::from_f(0.f);
-    dvg[e] = Elem<T>::from_f(0.f);
+    const int64_t jj = e / D, d = e % D;
+    dkg[jj * p.ldk.sl + d] = Elem<T>::from_f(0.f);
+    dvg[jj * p.ldv.sl + d] = Elem<T>::from_f(0.f);
   }
   __syncthreads();  // the ring is free: reuse it for the dQ partial of this block
   float* cta_dq = reinterpret_cast<float*>(sm + L::kDq);
@@ -633,8 +634,7 @@ __global__ void __launch_bounds__(128) vec_mma_bwd_kernel(const __grid_constant_
     const int r = e / kSlice, d = c * kSlice + e % kSlice;
     float acc = 0.f;
     for (int cc = 0; cc < kCs; ++cc) acc += cluster.map_shared_rank(cta_dq, cc)[r * D + d];
-    const int64_t row = q_row(p, b, g * p.G + r / p.Lq, r % p.Lq);
-    static_cast<T*>(p.dq)[row * D + d] = Elem<T>::from_f(acc * p.scale);
+    row_ptr<T>(p.dq, p.ldq, b, g * p.G + r / p.Lq, r % p.Lq)[d] = Elem<T>::from_f(acc * p.scale);
   }
   cluster.sync();
 }
@@ -642,7 +642,7 @@ __global__ void __launch_bounds__(128) vec_mma_bwd_kernel(const __grid_constant_
 template <typename T, int D, int MT>
 cudaError_t vec_mma_bwd_t(const Problem& p, cudaStream_t s) {
   CUtensorMap tk, tv;
-  if (!make_tmap_3d(&tk, p.k, D, p.Lkv, p.B * p.Hkv, kKeys) || !make_tmap_3d(&tv, p.v, D, p.Lkv, p.B * p.Hkv, kKeys))
+  if (!make_tmap_4d(&tk, p.k, D, p.Lkv, p.Hkv, p.B, p.lk, kKeys) || !make_tmap_4d(&tv, p.v, D, p.Lkv, p.Hkv, p.B, p.lv, kKeys))
     return cudaErrorInvalidValue;
   const int smem = VbLayout<D, MT>::kBytes + 1024;
   auto kern = vec_mma_bwd_kernel<T, D, MT>;

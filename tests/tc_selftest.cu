@@ -40,8 +40,8 @@ __global__ void __launch_bounds__(128) selftest_kernel(const __grid_constant__ C
   if (tid == 0) {
     mbar_arrive_expect_tx(&bar_load, 65536);
     for (int cb = 0; cb < 2; ++cb) {
-      tma_load_3d(sa + cb * 16384, &map_a, &bar_load, cb * 64, 0, 0);
-      tma_load_3d(sb + cb * 16384, &map_b, &bar_load, cb * 64, 0, 0);
+      tma_load_4d(sa + cb * 16384, &map_a, &bar_load, cb * 64, 0, 0, 0);
+      tma_load_4d(sb + cb * 16384, &map_b, &bar_load, cb * 64, 0, 0, 0);
     }
   }
   if (variant == 2) {
@@ -104,7 +104,8 @@ __global__ void __launch_bounds__(128) selftest_kernel(const __grid_constant__ C
 // a, b: device bf16 [128 x 128] row-major.  out: device fp32 [128 x 128].  err: device word.
 extern "C" int selftest_mma(int variant, const void* a, const void* b, float* out, unsigned* err) {
   CUtensorMap ma, mb;
-  if (!make_tmap_3d(&ma, a, 128, 128, 1, 128) || !make_tmap_3d(&mb, b, 128, 128, 1, 128)) return 1;
+  const Layout l{128 * 128, 128 * 128, 128};
+  if (!make_tmap_4d(&ma, a, 128, 128, 1, 1, l, 128) || !make_tmap_4d(&mb, b, 128, 128, 1, 1, l, 128)) return 1;
   const int smem = 65536 + 1024;
   if (cudaFuncSetAttribute(selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return 2;

@@ -128,3 +128,38 @@ def test_product_path_has_no_oracle_dependency():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"\b(import|from)\s+oracle\b|oracle[./]", text), f
+
+
+# ---- strided entry points: every case below is rejected before anything is launched.
+def _cont(H, L, D):
+    return (H * L * D, L * D, D)
+
+
+def fwd_strided(lib, out_ptr=O, **lay):
+    a = GOOD
+    B, Hq, Hkv, Lq, Lkv, D = a["B"], a["Hq"], a["Hkv"], a["Lq"], a["Lkv"], a["D"]
+    layouts = dict(q=_cont(Hq, Lq, D), k=_cont(Hkv, Lkv, D), v=_cont(Hkv, Lkv, D),
+                   o=_cont(Hq, Lq, D))
+    layouts.update(lay)
+    st = _lib.make_strides(**layouts)
+    return _lib.sdpa_fwd_strided(Q, K, V, out_ptr, L, B, Hq, Hkv, Lq, Lkv, D, a["scale"],
+                                 a["causal"], a["dtype"], st, None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q=(8192, 4096, 65)),          # row stride not a multiple of 16 bytes
+    dict(q=(8192, 4096, 32)),          # rows overlap (row stride < D)
+    dict(k=(4096, 0, 64)),             # zero stride
+    dict(v=(4096, 4096, -64)),         # negative stride
+    dict(q=(8192, 64, 64)),            # heads and rows share addresses
+    dict(o=(8192, 64, 128), q=(8192, 64, 128)),     # [B, L, H, D] out at q's address: overlap
+])
+def test_forward_strided_rejects(lib, kw):
+    out_ptr = Q + 16 if "o" in kw else O
+    assert fwd_strided(lib, out_ptr=out_ptr, **kw) == INVALID
+
+
+def test_strided_null_strides_rejected(lib):
+    a = GOOD
+    assert lib.sdpa_fwd_strided(Q, K, V, O, L, a["B"], a["Hq"], a["Hkv"], a["Lq"], a["Lkv"],
+                                a["D"], a["scale"], a["causal"], a["dtype"], None, None) == INVALID
