@@ -262,15 +262,14 @@ __device__ __forceinline__ void load_elems(const T* src, float (&dst)[N]) {
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kDeltaThreads) delta_kernel(Problem p, int64_t rows) {
+__global__ void __launch_bounds__(kDeltaThreads) delta_kernel(Problem p) {
+  // Grid (row blocks, Hq, B): rows i of head h of batch b, kDeltaThreads / kDeltaTpr per block.
   constexpr int EPT = D / kDeltaTpr;
-  const int64_t row = ((int64_t)blockIdx.x * kDeltaThreads + threadIdx.x) / kDeltaTpr;  // (b·Hq + h)·Lq + i
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int i = blockIdx.x * (kDeltaThreads / kDeltaTpr) + threadIdx.x / kDeltaTpr;
   const int sub = threadIdx.x % kDeltaTpr;
   float acc = 0.f;
-  if (row < rows) {
-    const int i = (int)(row % p.Lq);
-    const int64_t bh = row / p.Lq;
-    const int b = (int)(bh / p.Hq), h = (int)(bh % p.Hq);
+  if (i < p.Lq) {
     float a[EPT], c[EPT];
     load_elems<T, EPT>(row_ptr<T>(p.o, p.lo, b, h, i) + sub * EPT, a);
     load_elems<T, EPT>(row_ptr<T>(p.dout, p.ldo, b, h, i) + sub * EPT, c);
@@ -279,7 +278,7 @@ __global__ void __launch_bounds__(kDeltaThreads) delta_kernel(Problem p, int64_t
   }
 #pragma unroll
   for (int off = kDeltaTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (row < rows && sub == 0) p.delta[row] = acc;
+  if (i < p.Lq && sub == 0) p.delta[q_row(p, b, h, i)] = acc;
 }
 
 template <typename T, int D>
@@ -305,10 +304,9 @@ cudaError_t simt_dkdv_t(const Problem& p, cudaStream_t s) {
 
 template <typename T, int D>
 cudaError_t delta_t(const Problem& p, cudaStream_t s) {
-  const int64_t rows = (int64_t)p.B * p.Hq * p.Lq;
-  const int64_t rows_per_block = kDeltaThreads / kDeltaTpr;
-  const int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
-  delta_kernel<T, D><<<(unsigned)blocks, kDeltaThreads, 0, s>>>(p, rows);
+  constexpr int rows_per_block = kDeltaThreads / kDeltaTpr;
+  const dim3 grid((p.Lq + rows_per_block - 1) / rows_per_block, p.Hq, p.B);
+  delta_kernel<T, D><<<grid, kDeltaThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
