@@ -1,4 +1,4 @@
-// Tensor-core backward (fp16/bf16, D in {64, 128}): a dK/dV kernel and a dQ kernel, both
+// Tensor-core backward (fp16/bf16, D in {64, 96, 128}): a dK/dV kernel and a dQ kernel, both
 // TMA + tcgen05 + TMEM, recomputing P from the forward's logsumexp ("[Metal] Add Flash
 // Attention VJP for training", sections "Implementation Notes" and "Limitations").
 //
@@ -69,7 +69,8 @@ __device__ __forceinline__ uint32_t packed_col(int kk) { return kk < 4 ? kk * 8 
 // Shared-memory plan (offsets from a 1024-byte aligned base).
 template <int D>
 struct BwdLayout {
-  static constexpr int kTileBytes = kRows * D * 2;     // one [128 x D] tile
+  static constexpr int kCB = (D + 63) / 64;            // 64-column blocks (D = 96 padded to 128)
+  static constexpr int kTileBytes = kRows * kCB * 64 * 2;  // one [128 x D] tile
   static constexpr int kOwnA = 0;                      // K (dK/dV) or Q (dQ)
   static constexpr int kOwnB = kTileBytes;             // V (dK/dV) or dO (dQ)
   static constexpr int kRing = 2 * kTileBytes;         // stages of {A block, B block}
@@ -150,12 +151,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv,
                    Problem p) {
   using L = BwdLayout<D>;
-  constexpr int kCB = D / 64;
+  constexpr int kCB = L::kCB;
   constexpr bool kBf16 = IsBf16<T>::value;
   constexpr uint32_t kIdS = idesc_f16(kRows, kBlk, kBf16, false, false);
   constexpr uint32_t kIdAcc = idesc_f16(kRows, D, kBf16, false, true);
   // TMEM columns: dV, dK, Sᵀ (→ Pᵀ), dPᵀ (→ dSᵀ)
-  constexpr uint32_t kColDv = 0, kColDk = D, kColX = 2 * D, kColY = 2 * D + 128;
+  constexpr uint32_t kColDv = 0, kColDk = 128, kColX = 256, kColY = 384;
   extern __shared__ unsigned char smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ BwdBars bars;
@@ -381,7 +382,8 @@ constexpr int kVStages = 2;
 
 template <int D>
 struct DqLayout {
-  static constexpr int kTileBytes = kRows * D * 2;
+  static constexpr int kCB = (D + 63) / 64;  // 64-column blocks (D = 96 padded to 128)
+  static constexpr int kTileBytes = kRows * kCB * 64 * 2;
   static constexpr int kQ = 0;
   static constexpr int kDo = kTileBytes;
   static constexpr int kK = 2 * kTileBytes;                       // kKStages K blocks
@@ -411,13 +413,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                  const __grid_constant__ CUtensorMap tdq, Problem p) {
   using L = DqLayout<D>;
-  constexpr int kCB = D / 64;
+  constexpr int kCB = L::kCB;
   constexpr int kCbStride = kRows * 128;
   constexpr bool kBf16 = IsBf16<T>::value;
   constexpr uint32_t kIdS = idesc_f16(kRows, kBlk, kBf16, false, false);
   constexpr uint32_t kIdAcc = idesc_f16(kRows, D, kBf16, false, true);
   // TMEM columns: dQ, two S buffers (→ dS), dP
-  constexpr uint32_t kColDq = 0, kColS0 = D, kColDp = D + 256;
+  constexpr uint32_t kColDq = 0, kColS0 = 128, kColDp = 384;
   extern __shared__ unsigned char smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ DqBars bars;
@@ -687,13 +689,25 @@ cudaError_t dq_t(const Problem& p, cudaStream_t s) {
 bool tensor_bwd_supported(const Problem& p, int dtype) { return tensor_supported(p, dtype); }
 
 cudaError_t launch_tc_dkdv(const Problem& p, int dtype, cudaStream_t s) {
-  if (dtype == 2) return p.D == 128 ? dkdv_t<__nv_bfloat16, 128>(p, s) : dkdv_t<__nv_bfloat16, 64>(p, s);
-  return p.D == 128 ? dkdv_t<__half, 128>(p, s) : dkdv_t<__half, 64>(p, s);
+  if (dtype == 2) {
+    if (p.D == 128) return dkdv_t<__nv_bfloat16, 128>(p, s);
+    if (p.D == 96) return dkdv_t<__nv_bfloat16, 96>(p, s);
+    return dkdv_t<__nv_bfloat16, 64>(p, s);
+  }
+  if (p.D == 128) return dkdv_t<__half, 128>(p, s);
+  if (p.D == 96) return dkdv_t<__half, 96>(p, s);
+  return dkdv_t<__half, 64>(p, s);
 }
 
 cudaError_t launch_tc_dq(const Problem& p, int dtype, cudaStream_t s) {
-  if (dtype == 2) return p.D == 128 ? dq_t<__nv_bfloat16, 128>(p, s) : dq_t<__nv_bfloat16, 64>(p, s);
-  return p.D == 128 ? dq_t<__half, 128>(p, s) : dq_t<__half, 64>(p, s);
+  if (dtype == 2) {
+    if (p.D == 128) return dq_t<__nv_bfloat16, 128>(p, s);
+    if (p.D == 96) return dq_t<__nv_bfloat16, 96>(p, s);
+    return dq_t<__nv_bfloat16, 64>(p, s);
+  }
+  if (p.D == 128) return dq_t<__half, 128>(p, s);
+  if (p.D == 96) return dq_t<__half, 96>(p, s);
+  return dq_t<__half, 64>(p, s);
 }
 
 }  // namespace sdpa

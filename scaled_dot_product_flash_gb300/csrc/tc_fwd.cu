@@ -1,4 +1,4 @@
-// Tensor-core forward (fp16/bf16, D in {64, 128}): TMA + tcgen05 + TMEM.
+// Tensor-core forward (fp16/bf16, D in {64, 96, 128}): TMA + tcgen05 + TMEM.
 //
 // One block computes 256 query rows (two 128-row Q tiles) of one (batch, head) against
 // the keys of its KV head (h / G).  Warp roles (384 threads):
@@ -15,7 +15,7 @@
 // at the exponential pass, so one tile's pass overlaps the other tile's MMAs.
 // Tensor memory (512 columns, fp32): S_w = Q_w·K_jᵀ at columns [128w, 128w+128); P_w is
 // written back over the first 64 columns of S_w as packed 16-bit pairs and read from TMEM
-// as the A operand of O_w += P_w·V_j, with O_w at columns [256 + D·w, 256 + D·(w+1)).
+// as the A operand of O_w += P_w·V_j, with O_w at columns [256 + 128w, 256 + 128w + D).
 // The running maximum is raised lazily: O and l are rescaled only when a row's maximum
 // grows by more than 2^8, so exponentials stay <= 256 while O and l use one consistent
 // maximum, which keeps the result exact up to rounding.
@@ -50,12 +50,15 @@ constexpr float kRescale = 8.f;  // log2 of the largest exponential allowed befo
 
 template <int D>
 struct FwdLayout {
-  static constexpr int kTileBytes = kBM * D * 2;
+  // Tiles hold ceil(D/64) 64-column blocks (D = 96 is padded to 128 columns: TMA fills
+  // the missing columns with zeros on loads and clips them on stores).
+  static constexpr int kCB = (D + 63) / 64;
+  static constexpr int kTileBytes = kBM * kCB * 64 * 2;
   static constexpr int kQOff = 0;
   static constexpr int kRingOff = kQTiles * kTileBytes;
   static constexpr int kBytes = kRingOff + kStages * kTileBytes;
   static constexpr int kSCol = 0;    // S_w at column 128·w
-  static constexpr int kOCol = 256;  // O_w at column 256 + D·w
+  static constexpr int kOCol = 256;  // O_w at column 256 + 128·w
 };
 
 struct FwdBars {
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to, Problem p) {
   using L = FwdLayout<D>;
-  constexpr int kCB = D / 64;
+  constexpr int kCB = L::kCB;
   constexpr bool kBf16 = IsBf16<T>::value;
   constexpr uint32_t kIdS = idesc_f16(kBM, kBN, kBf16, false, false);
   constexpr uint32_t kIdO = idesc_f16(kBM, D, kBf16, false, true);
@@ -305,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint64_t qd = sdesc_sw128(smem_u32(sm + L::kQOff) + w * L::kTileBytes, 16, 1024);
     const uint32_t ring_s = smem_u32(sm + L::kRingOff);
-    const uint32_t s_tm = tbase + L::kSCol + w * 128, o_tm = tbase + L::kOCol + w * D;
+    const uint32_t s_tm = tbase + L::kSCol + w * 128, o_tm = tbase + L::kOCol + w * 128;
     const int tile_row0 = row0 + w * kBM;
     for (int j = 0; ok && j < nmax; ++j) {
       const int sk = (2 * j) % kStages, sv = (2 * j + 1) % kStages;
@@ -351,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;
     const int i = row0 + w * kBM + r;
     const uint32_t s_addr = tmem_addr(tbase, quarter * 32, L::kSCol + w * 128);
-    const uint32_t o_addr = tmem_addr(tbase, quarter * 32, L::kOCol + w * D);
+    const uint32_t o_addr = tmem_addr(tbase, quarter * 32, L::kOCol + w * 128);
     const float c = p.scale_log2;
     const int tile_row0 = row0 + w * kBM;
     float m = neg_inf(), l = 0.f;
@@ -478,12 +481,18 @@ cudaError_t tc_fwd_t(const Problem& p, cudaStream_t s) {
 }  // namespace
 
 bool tensor_supported(const Problem& p, int dtype) {
-  return (dtype == 1 || dtype == 2) && (p.D == 64 || p.D == 128);
+  return (dtype == 1 || dtype == 2) && (p.D == 64 || p.D == 96 || p.D == 128);
 }
 
 cudaError_t launch_tc_fwd(const Problem& p, int dtype, cudaStream_t s) {
-  if (dtype == 2) return p.D == 128 ? tc_fwd_t<__nv_bfloat16, 128>(p, s) : tc_fwd_t<__nv_bfloat16, 64>(p, s);
-  return p.D == 128 ? tc_fwd_t<__half, 128>(p, s) : tc_fwd_t<__half, 64>(p, s);
+  if (dtype == 2) {
+    if (p.D == 128) return tc_fwd_t<__nv_bfloat16, 128>(p, s);
+    if (p.D == 96) return tc_fwd_t<__nv_bfloat16, 96>(p, s);
+    return tc_fwd_t<__nv_bfloat16, 64>(p, s);
+  }
+  if (p.D == 128) return tc_fwd_t<__half, 128>(p, s);
+  if (p.D == 96) return tc_fwd_t<__half, 96>(p, s);
+  return tc_fwd_t<__half, 64>(p, s);
 }
 
 }  // namespace sdpa

@@ -102,6 +102,8 @@ FORCED = [
     (_lib.PATH_VECTOR, Shape(1, 4, 1, 8, 1000, 128), "bf16", True),
     (_lib.PATH_VECTOR, Shape(2, 8, 2, 8, 513, 32), "f32", False),
     (_lib.PATH_VECTOR, Shape(1, 32, 1, 1, 2000, 96), "f16", False),
+    (_lib.PATH_TENSOR, Shape(2, 8, 2, 300, 260, 96), "bf16", True),    # D = 96 on tcgen05
+    (_lib.PATH_TENSOR, Shape(1, 4, 4, 257, 129, 96), "f16", False),
 ]
 
 

@@ -36,6 +36,7 @@ CASES = [
     (Shape(1, 4, 2, 40, 70, 32), "f32", True, _lib.PATH_AUTO),         # CUDA cores
     (Shape(1, 2, 2, 5, 90, 96), "f32", False, _lib.PATH_AUTO),         # short query, CUDA cores
     (Shape(1, 4, 2, 130, 130, 64), "bf16", True, _lib.PATH_SIMT),      # forced CUDA cores, bf16
+    (Shape(1, 4, 2, 200, 330, 96), "bf16", True, _lib.PATH_AUTO),      # tensor cores, D = 96
 ]
 
 
