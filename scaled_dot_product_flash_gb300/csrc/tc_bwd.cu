@@ -1,4 +1,4 @@
-// Tensor-core backward (fp16/bf16, D in {64, 96, 128}): a dK/dV kernel and a dQ kernel, both
+// Tensor-core backward (fp16/bf16, D in {32, 64, 96, 128}): a dK/dV kernel and a dQ kernel, both
 // TMA + tcgen05 + TMEM, recomputing P from the forward's logsumexp ("[Metal] Add Flash
 // Attention VJP for training", sections "Implementation Notes" and "Limitations").
 //
@@ -692,10 +692,12 @@ cudaError_t launch_tc_dkdv(const Problem& p, int dtype, cudaStream_t s) {
   if (dtype == 2) {
     if (p.D == 128) return dkdv_t<__nv_bfloat16, 128>(p, s);
     if (p.D == 96) return dkdv_t<__nv_bfloat16, 96>(p, s);
+    if (p.D == 32) return dkdv_t<__nv_bfloat16, 32>(p, s);
     return dkdv_t<__nv_bfloat16, 64>(p, s);
   }
   if (p.D == 128) return dkdv_t<__half, 128>(p, s);
   if (p.D == 96) return dkdv_t<__half, 96>(p, s);
+  if (p.D == 32) return dkdv_t<__half, 32>(p, s);
   return dkdv_t<__half, 64>(p, s);
 }
 
@@ -703,10 +705,12 @@ cudaError_t launch_tc_dq(const Problem& p, int dtype, cudaStream_t s) {
   if (dtype == 2) {
     if (p.D == 128) return dq_t<__nv_bfloat16, 128>(p, s);
     if (p.D == 96) return dq_t<__nv_bfloat16, 96>(p, s);
+    if (p.D == 32) return dq_t<__nv_bfloat16, 32>(p, s);
     return dq_t<__nv_bfloat16, 64>(p, s);
   }
   if (p.D == 128) return dq_t<__half, 128>(p, s);
   if (p.D == 96) return dq_t<__half, 96>(p, s);
+  if (p.D == 32) return dq_t<__half, 32>(p, s);
   return dq_t<__half, 64>(p, s);
 }
 

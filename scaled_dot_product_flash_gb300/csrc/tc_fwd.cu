@@ -1,4 +1,4 @@
-// Tensor-core forward (fp16/bf16, D in {64, 96, 128}): TMA + tcgen05 + TMEM.
+// Tensor-core forward (fp16/bf16, D in {32, 64, 96, 128}): TMA + tcgen05 + TMEM.
 //
 // One block computes 256 query rows (two 128-row Q tiles) of one (batch, head) against
 // the keys of its KV head (h / G).  Warp roles (384 threads):
@@ -481,17 +481,19 @@ cudaError_t tc_fwd_t(const Problem& p, cudaStream_t s) {
 }  // namespace
 
 bool tensor_supported(const Problem& p, int dtype) {
-  return (dtype == 1 || dtype == 2) && (p.D == 64 || p.D == 96 || p.D == 128);
+  return (dtype == 1 || dtype == 2) && (p.D == 32 || p.D == 64 || p.D == 96 || p.D == 128);
 }
 
 cudaError_t launch_tc_fwd(const Problem& p, int dtype, cudaStream_t s) {
   if (dtype == 2) {
     if (p.D == 128) return tc_fwd_t<__nv_bfloat16, 128>(p, s);
     if (p.D == 96) return tc_fwd_t<__nv_bfloat16, 96>(p, s);
+    if (p.D == 32) return tc_fwd_t<__nv_bfloat16, 32>(p, s);
     return tc_fwd_t<__nv_bfloat16, 64>(p, s);
   }
   if (p.D == 128) return tc_fwd_t<__half, 128>(p, s);
   if (p.D == 96) return tc_fwd_t<__half, 96>(p, s);
+  if (p.D == 32) return tc_fwd_t<__half, 32>(p, s);
   return tc_fwd_t<__half, 64>(p, s);
 }
 

@@ -104,6 +104,8 @@ FORCED = [
     (_lib.PATH_VECTOR, Shape(1, 32, 1, 1, 2000, 96), "f16", False),
     (_lib.PATH_TENSOR, Shape(2, 8, 2, 300, 260, 96), "bf16", True),    # D = 96 on tcgen05
     (_lib.PATH_TENSOR, Shape(1, 4, 4, 257, 129, 96), "f16", False),
+    (_lib.PATH_TENSOR, Shape(2, 4, 2, 300, 200, 32), "bf16", True),    # D = 32 on tcgen05
+    (_lib.PATH_TENSOR, Shape(1, 2, 2, 140, 390, 32), "f16", False),
 ]
 
 
