@@ -26,7 +26,10 @@ Readings of points the pages leave open (each also listed in the design notes):
 * logsumexp is the natural log of the row sum of exp(scale·q·k) over visible keys,
   including the scale; stored in fp32 by the GPU, fp64 here.
 * causal is top-left aligned: key j is masked for query i when j > i, for any Lq, Lkv.
-  Key 0 is always visible, so no row is ever fully masked.
+  Key 0 is always visible, so no row is ever fully masked.  ``is_causal = 2`` selects the
+  bottom-right alignment instead (the last query sees every key): key j is masked for
+  query i when j > i + (Lkv - Lq); it is defined for Lq <= Lkv only, where again key 0
+  is always visible.
 * GQA groups are contiguous: query head h reads KV head h // (Hq // Hkv).
 * The backward is the textbook vector-Jacobian product of the forward with
   delta = rowsum(dO * O) taken from this oracle's own fp64 O.
@@ -61,17 +64,32 @@ def _f64(x):
     return np.asarray(x, dtype=np.float64)
 
 
-def _scores(q_rows, k, scale, is_causal, row_idx):
+BOTTOM_RIGHT = 2
+
+
+def _causal_offset(is_causal, lq, lkv):
+    """None without a mask; otherwise the c for which key j is hidden from query i when
+    j > i + c: 0 for the top-left mask, Lkv - Lq for the bottom-right one."""
+    if not is_causal:
+        return None
+    if is_causal == BOTTOM_RIGHT:
+        if lq > lkv:
+            raise ValueError("the bottom-right causal mask needs Lq <= Lkv")
+        return lkv - lq
+    return 0
+
+
+def _scores(q_rows, k, scale, offset, row_idx):
     """Scores of a block of query rows against all keys, masked.
 
     [PyTensor-SDPA] "Proposed change": scores = (q @ kᵀ) * scale.
-    Causal ([mps-flash-sdpa] "Quick Start" ``is_causal``; top-left reading): the score of
-    key j for absolute query row i = row_idx[r] is -inf when j > i.
+    Causal ([mps-flash-sdpa] "Quick Start" ``is_causal``): the score of key j for absolute
+    query row i = row_idx[r] is -inf when j > i + offset (offset None: no mask).
     """
     s = (q_rows @ k.T) * scale
-    if is_causal:
+    if offset is not None:
         j = np.arange(k.shape[0])[None, :]
-        s = np.where(j > np.asarray(row_idx)[:, None], -np.inf, s)
+        s = np.where(j > np.asarray(row_idx)[:, None] + offset, -np.inf, s)
     return s
 
 
@@ -102,12 +120,13 @@ def head_forward(q, k, v, scale, is_causal, rows=None, row_block=None):
     rows to compute; by default all.  Returns (O [n, D], lse [n]) in float64.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
+    off = _causal_offset(is_causal, q.shape[0], k.shape[0])
     idx = np.arange(q.shape[0]) if rows is None else np.asarray(rows, dtype=np.int64)
     o = np.empty((idx.size, v.shape[1]))
     lse = np.empty(idx.size)
     for a, b in _blocks(idx.size, row_block):
         sel = idx[a:b]
-        p, lse[a:b] = _softmax_rows(_scores(q[sel], k, scale, is_causal, sel))
+        p, lse[a:b] = _softmax_rows(_scores(q[sel], k, scale, off, sel))
         o[a:b] = p @ v
     return o, lse
 
@@ -129,11 +148,12 @@ def head_backward(q, k, v, dout, scale, is_causal, row_block=None):
     them over the query heads of the group.
     """
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    off = _causal_offset(is_causal, q.shape[0], k.shape[0])
     dq = np.empty_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
     for a, b in _blocks(q.shape[0], row_block):
-        p, _ = _softmax_rows(_scores(q[a:b], k, scale, is_causal, np.arange(a, b)))
+        p, _ = _softmax_rows(_scores(q[a:b], k, scale, off, np.arange(a, b)))
         o = p @ v
         dv += p.T @ dout[a:b]
         dp = dout[a:b] @ v.T

@@ -89,6 +89,7 @@ FD_CASES = [
     dict(B=2, Hq=3, Hkv=3, Lq=4, Lkv=4, D=3, causal=True),
     dict(B=1, Hq=4, Hkv=2, Lq=7, Lkv=3, D=2, causal=True),
     dict(B=1, Hq=1, Hkv=1, Lq=1, Lkv=5, D=3, causal=False),
+    dict(B=1, Hq=2, Hkv=1, Lq=4, Lkv=7, D=3, causal=2),      # bottom-right causal
 ]
 
 
@@ -305,6 +306,47 @@ def test_matches_torch_cpu_float64():
         np.testing.assert_allclose(dv, tv.grad.numpy(), atol=1e-12)
 
 
+# ----------------------------------------------------------------- bottom-right causal
+def test_bottom_right_equals_padded_top_left(impl=None):
+    """The bottom-right mask (key j hidden from query i when j > i + Lkv - Lq) is the
+    top-left mask of a problem with Lkv - Lq extra query rows in front: its rows are the
+    last Lq rows of that problem, and with zero output gradient on the extra rows the
+    gradients of K and V are the same."""
+    impl = impl or oracle
+    rng = np.random.default_rng(41)
+    B, Hq, Hkv, Lq, Lkv, D = 1, 4, 2, 5, 9, 3
+    q = rng.standard_normal((B, Hq, Lq, D))
+    k = rng.standard_normal((B, Hkv, Lkv, D))
+    v = rng.standard_normal((B, Hkv, Lkv, D))
+    do = rng.standard_normal((B, Hq, Lq, D))
+    pad = Lkv - Lq
+    qf = np.concatenate([rng.standard_normal((B, Hq, pad, D)), q], axis=2)
+    dof = np.concatenate([np.zeros((B, Hq, pad, D)), do], axis=2)
+    o, lse = impl.sdpa_forward(q, k, v, 0.7, 2)
+    of, lsef = impl.sdpa_forward(qf, k, v, 0.7, True)
+    np.testing.assert_allclose(o, of[:, :, pad:], atol=1e-13)
+    np.testing.assert_allclose(lse, lsef[:, :, pad:], atol=1e-13)
+    dq, dk, dv = impl.sdpa_backward(q, k, v, do, 0.7, 2)
+    dqf, dkf, dvf = impl.sdpa_backward(qf, k, v, dof, 0.7, True)
+    np.testing.assert_allclose(dq, dqf[:, :, pad:], atol=1e-12)
+    np.testing.assert_allclose(dk, dkf, atol=1e-12)
+    np.testing.assert_allclose(dv, dvf, atol=1e-12)
+
+
+def test_bottom_right_square_and_single_query(impl=None):
+    """Lq = Lkv: bottom-right is top-left.  Lq = 1: the single query sees every key."""
+    impl = impl or oracle
+    rng = np.random.default_rng(42)
+    q, k, v = (rng.standard_normal((1, 2, 6, 4)) for _ in range(3))
+    for a, b in zip(impl.sdpa_forward(q, k, v, 0.5, 2), impl.sdpa_forward(q, k, v, 0.5, True)):
+        np.testing.assert_allclose(a, b, atol=1e-14)
+    q1 = q[:, :, :1]
+    for a, b in zip(impl.sdpa_forward(q1, k, v, 0.5, 2), impl.sdpa_forward(q1, k, v, 0.5, False)):
+        np.testing.assert_allclose(a, b, atol=1e-14)
+    with pytest.raises(ValueError):
+        impl.sdpa_forward(q, k[:, :, :3], v[:, :, :3], 0.5, 2)  # Lq > Lkv
+
+
 # ----------------------------------------------------------------- pins have teeth
 PINS = [
     test_rows_of_p_sum_to_one,
@@ -316,6 +358,8 @@ PINS = [
     test_key_shift_invariance,
     test_gqa_equals_repeated_kv_heads,
     test_mha_equals_independent_heads,
+    test_bottom_right_equals_padded_top_left,
+    test_bottom_right_square_and_single_query,
 ]
 
 
@@ -328,13 +372,20 @@ def _mutant(name):
     if name in ("causal_diag_masked", "causal_off_by_one"):
         shift = 0 if name == "causal_diag_masked" else 2
 
-        def _scores(q_rows, k, scale, is_causal, row_idx):
+        def _scores(q_rows, k, scale, offset, row_idx):
             s = (q_rows @ k.T) * scale
-            if is_causal:
+            if offset is not None:
                 j = np.arange(k.shape[0])[None, :]
-                s = np.where(j >= np.asarray(row_idx)[:, None] + shift, -np.inf, s)
+                s = np.where(j >= np.asarray(row_idx)[:, None] + offset + shift, -np.inf, s)
             return s
         m._scores = _scores
+    elif name == "bottom_right_offset_off_by_one":
+        orig = m._causal_offset
+
+        def _causal_offset(is_causal, lq, lkv):
+            off = orig(is_causal, lq, lkv)
+            return off - 1 if is_causal == m.BOTTOM_RIGHT else off
+        m._causal_offset = _causal_offset
     elif name == "lse_log2":
         orig = m._softmax_rows
 
@@ -363,7 +414,8 @@ def _mutant(name):
     elif name == "delta_dropped":
         def head_backward(q, k, v, dout, scale, is_causal, row_block=None):
             q, k, v, dout = (np.asarray(x, float) for x in (q, k, v, dout))
-            p, _ = m._softmax_rows(m._scores(q, k, scale, is_causal, np.arange(q.shape[0])))
+            off = m._causal_offset(is_causal, q.shape[0], k.shape[0])
+            p, _ = m._softmax_rows(m._scores(q, k, scale, off, np.arange(q.shape[0])))
             ds = p * (dout @ v.T)
             return scale * ds @ k, scale * ds.T @ q, p.T @ dout
         m.head_backward = head_backward
@@ -380,7 +432,8 @@ def _mutant(name):
 
 
 @pytest.mark.parametrize("name", ["causal_diag_masked", "causal_off_by_one", "lse_log2", "gqa_modulo",
-                                  "no_scale_in_dq", "delta_dropped", "dk_transposed_operand"])
+                                  "no_scale_in_dq", "delta_dropped", "dk_transposed_operand",
+                                  "bottom_right_offset_off_by_one"])
 def test_planted_mistakes_are_caught(name):
     mutant = _mutant(name)
     failures = 0
