@@ -3,7 +3,8 @@
  *
  * The operation.  For query head h of batch b, with G = Hq / Hkv and KV head g = h / G:
  *     S   = scale · Q[b,h] · K[b,g]ᵀ                 (Lq × Lkv scores)
- *     S_ij = −∞ where is_causal and j > i            (top-left aligned causal mask)
+ *     S_ij = −∞ where is_causal and j > i + c        (causal mask; c = 0 top-left,
+ *                                                   c = Lkv − Lq bottom-right)
  *     P   = softmax of each row of S
  *     O[b,h]   = P · V[b,g]
  *     lse[b,h,i] = ln Σ_j exp(S_ij)                  (natural log, scale included)
@@ -22,6 +23,11 @@
  * logsumexp).
  *
  * Conventions shared by every entry point:
+ *  - is_causal: SDPA_CAUSAL_NONE (0), SDPA_CAUSAL_TOP_LEFT (1: key j hidden from query i
+ *    when j > i, as the is_causal flag of F.scaled_dot_product_attention), or
+ *    SDPA_CAUSAL_BOTTOM_RIGHT (2: hidden when j > i + Lkv − Lq, so the last query sees
+ *    every key, the alignment a query chunk at the end of a longer KV sequence needs;
+ *    requires Lq <= Lkv, else SDPA_ERR_UNSUPPORTED).  Other values: SDPA_ERR_INVALID_ARG.
  *  - Layout: every tensor is a dense, contiguous row-major [B, H, L, D] array of `dtype`
  *    (H = Hq for q, out, dout, dq; H = Hkv for k, v, dk, dv).  lse is a dense fp32
  *    [B, Hq, Lq] array.  All pointers are DEVICE pointers (or managed memory) on the
@@ -54,6 +60,12 @@ typedef enum {
   SDPA_F16 = 1,
   SDPA_BF16 = 2
 } sdpa_dtype_t;
+
+typedef enum {
+  SDPA_CAUSAL_NONE = 0,
+  SDPA_CAUSAL_TOP_LEFT = 1,
+  SDPA_CAUSAL_BOTTOM_RIGHT = 2
+} sdpa_causal_t;
 
 typedef enum {
   SDPA_OK = 0,

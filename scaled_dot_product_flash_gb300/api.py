@@ -14,6 +14,25 @@ from . import _lib
 
 DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
+# is_causal values: False/0, True/1 (top-left: key j hidden from query i when j > i) or
+# CAUSAL_BOTTOM_RIGHT / "bottom_right" (hidden when j > i + Lkv - Lq; needs Lq <= Lkv).
+CAUSAL_NONE, CAUSAL_TOP_LEFT, CAUSAL_BOTTOM_RIGHT = 0, 1, 2
+
+
+def _causal(c):
+    if c is None or c is False:
+        return CAUSAL_NONE
+    if c is True:
+        return CAUSAL_TOP_LEFT
+    if c == "bottom_right":
+        return CAUSAL_BOTTOM_RIGHT
+    if c == "top_left":
+        return CAUSAL_TOP_LEFT
+    c = int(c)
+    if c not in (CAUSAL_NONE, CAUSAL_TOP_LEFT, CAUSAL_BOTTOM_RIGHT):
+        raise ValueError(f"is_causal must be False, True or 'bottom_right', not {c}")
+    return c
+
 
 def _check(name, t, dtype=None):
     if not t.is_cuda:
@@ -70,7 +89,7 @@ def attention_forward(q, k, v, scale=None, is_causal=False, need_lse=True, out=N
     strides = _lib.make_strides(q=_layout(q), k=_layout(k), v=_layout(v), o=_layout(out))
     st = _lib.sdpa_fwd_strided(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                lse.data_ptr() if lse is not None else None,
-                               B, Hq, Hkv, Lq, Lkv, D, scale, int(bool(is_causal)),
+                               B, Hq, Hkv, Lq, Lkv, D, scale, _causal(is_causal),
                                DTYPE_CODE[q.dtype], strides, _stream(stream))
     if st != _lib.OK:
         raise _lib.SdpaError(st, "sdpa_fwd")
@@ -104,7 +123,7 @@ def attention_backward(q, k, v, out, dout, lse, scale=None, is_causal=False, wor
     st = _lib.sdpa_bwd_strided(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
                                dv.data_ptr(), B, Hq, Hkv, Lq, Lkv, D, scale,
-                               int(bool(is_causal)), DTYPE_CODE[q.dtype], strides,
+                               _causal(is_causal), DTYPE_CODE[q.dtype], strides,
                                workspace.data_ptr(), workspace.numel(), _stream(stream))
     if st != _lib.OK:
         raise _lib.SdpaError(st, "sdpa_bwd")

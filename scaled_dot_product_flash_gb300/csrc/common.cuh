@@ -72,6 +72,8 @@ struct Problem {
   float scale;
   float scale_log2;  // scale · log2(e)
   int causal;
+  int coff;          // causal: key j is hidden from query i when j > i + coff (0 top-left,
+                     // Lkv - Lq bottom-right)
   unsigned* err;     // device error word
   uint64_t wait_limit_ns;  // time limit of any single bounded wait inside a kernel
   int inject;        // test hook: 1 = the tensor-core forward never delivers its first K tile

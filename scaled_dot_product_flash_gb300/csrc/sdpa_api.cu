@@ -107,6 +107,19 @@ int check_sizes(int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale, int
   return SDPA_OK;
 }
 
+// Causal mode: none, top-left (key j hidden from query i when j > i) or bottom-right
+// (hidden when j > i + Lkv - Lq; needs Lq <= Lkv so that every query sees key 0).
+int set_causal(Problem* p, int is_causal) {
+  if (is_causal < SDPA_CAUSAL_NONE || is_causal > SDPA_CAUSAL_BOTTOM_RIGHT) return SDPA_ERR_INVALID_ARG;
+  p->causal = is_causal != SDPA_CAUSAL_NONE ? 1 : 0;
+  p->coff = 0;
+  if (is_causal == SDPA_CAUSAL_BOTTOM_RIGHT) {
+    if (p->Lq > p->Lkv) return SDPA_ERR_UNSUPPORTED;
+    p->coff = p->Lkv - p->Lq;
+  }
+  return SDPA_OK;
+}
+
 enum class Family { kTensor, kSimt, kVector };
 
 int choose(const Problem& p, int dtype, Family* f) {
@@ -211,7 +224,7 @@ extern "C" int sdpa_fwd_strided(const void* q, const void* k, const void* v, voi
   p.v = v;
   p.out = out;
   p.lse = lse;
-  p.causal = is_causal ? 1 : 0;
+  if ((st = set_causal(&p, is_causal)) != SDPA_OK) return st;
   Family f;
   if ((st = choose(p, dtype, &f)) != SDPA_OK) return st;
   if ((st = error_word(&p.err)) != SDPA_OK) return st;
@@ -295,7 +308,7 @@ extern "C" int sdpa_bwd_strided(const void* q, const void* k, const void* v, con
   p.dk = dk;
   p.dv = dv;
   p.delta = static_cast<float*>(workspace);
-  p.causal = is_causal ? 1 : 0;
+  if ((st = set_causal(&p, is_causal)) != SDPA_OK) return st;
   Family f;
   if ((st = choose(p, dtype, &f)) != SDPA_OK) return st;
   if ((st = error_word(&p.err)) != SDPA_OK) return st;

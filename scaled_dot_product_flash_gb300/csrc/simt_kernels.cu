@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Problem p) {
   }
   float m = neg_inf(), l = 0.f;
   int kv_end = p.Lkv;
-  if (p.causal) kv_end = min(p.Lkv, (int)blockIdx.x * kRows + kRows);
+  if (p.causal) kv_end = min(p.Lkv, (int)blockIdx.x * kRows + kRows + p.coff);
 
   for (int j0 = 0; j0 < kv_end; j0 += kTile) {
     __syncthreads();
@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Problem p) {
       for (int t = 0; t < DPT; ++t) acc = fmaf(qr[t], ks[jj][sub + kTpr * t], acc);
       acc = reduce4(acc);
       const int j = j0 + jj;
-      const bool vis = j < p.Lkv && (!p.causal || j <= i);
+      const bool vis = j < p.Lkv && (!p.causal || j <= i + p.coff);
       s[jj] = vis ? acc * p.scale_log2 : neg_inf();
       tmax = fmaxf(tmax, s[jj]);
     }
@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kThreads) simt_dq_kernel(Problem p) {
   const float lse2 = valid ? p.lse[row] * kLog2e : 0.f;
   const float dl = valid ? p.delta[row] : 0.f;
   int kv_end = p.Lkv;
-  if (p.causal) kv_end = min(p.Lkv, (int)blockIdx.x * kRows + kRows);
+  if (p.causal) kv_end = min(p.Lkv, (int)blockIdx.x * kRows + kRows + p.coff);
 
   for (int j0 = 0; j0 < kv_end; j0 += kTile) {
     __syncthreads();
@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kThreads) simt_dq_kernel(Problem p) {
       s = reduce4(s);
       dp = reduce4(dp);
       const int j = j0 + jj;
-      const bool vis = valid && j < p.Lkv && (!p.causal || j <= i);
+      const bool vis = valid && j < p.Lkv && (!p.causal || j <= i + p.coff);
       const float pj = vis ? exp2f(s * p.scale_log2 - lse2) : 0.f;
       const float ds = pj * (dp - dl);
 #pragma unroll
@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(kThreads) simt_dkdv_kernel(Problem p) {
     dv[t] = 0.f;
   }
   // Under the causal mask, queries before this block's first key see none of its keys.
-  const int i_begin = p.causal ? (int)blockIdx.x * kRows : 0;
+  const int i_begin = p.causal ? max(0, (int)blockIdx.x * kRows - p.coff) : 0;
 
   for (int hh = 0; hh < p.G; ++hh) {
     const int h = g * p.G + hh;
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kThreads) simt_dkdv_kernel(Problem p) {
         s = reduce4(s);
         dp = reduce4(dp);
         const int i = i0 + ii;
-        const bool vis = valid && i < p.Lq && (!p.causal || j <= i);
+        const bool vis = valid && i < p.Lq && (!p.causal || j <= i + p.coff);
         const float pj = vis ? exp2f(s * p.scale_log2 - lse2s[ii]) : 0.f;
         const float ds = pj * (dp - dls[ii]);
 #pragma unroll

@@ -168,7 +168,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int unit = blockIdx.x % units;
   const int b = unit / p.Hkv, g = unit % p.Hkv;
   const int j0 = (blockIdx.x / units) * kRows;  // first key of this block
-  const int i_begin = p.causal ? j0 : 0;        // queries before j0 see none of these keys
+  // Queries before j0 - coff see none of these keys.
+  const int i_begin = p.causal ? max(0, j0 - p.coff) : 0;
   const int nqb = i_begin < p.Lq ? (p.Lq - i_begin + kBlk - 1) / kBlk : 0;
   const int total = p.G * nqb;
 
@@ -273,7 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const int i0 = i_begin + (n % nqb) * kBlk + 64 * w;  // first query of this half
-      const bool diag = p.causal && j0 + kRows - 1 > i0;
+      const int ic = i0 + p.coff;  // key j is hidden from query i0 + q when j > ic + q
+      const bool diag = p.causal && j0 + kRows - 1 > ic;
       const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(&bars.nlse2[s][64 * w]);
       const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(&bars.ndelta[s][64 * w]);
       // Pᵀ for this half (64 queries) from one TMEM round trip; the packed 16-bit values
@@ -290,8 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float p0, p1;
           ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl2[e]), p0, p1);
           if (diag) {
-            if (j > i0 + 2 * e) p0 = 0.f;
-            if (j > i0 + 2 * e + 1) p1 = 0.f;
+            if (j > ic + 2 * e) p0 = 0.f;
+            if (j > ic + 2 * e + 1) p1 = 0.f;
           }
           pf[e] = f2pack(p0, p1);
           pk[e] = pack2<T>(p0, p1);
@@ -432,7 +434,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   const int nqt = (p.Lq + kRows - 1) / kRows;
   const int qt = p.causal ? nqt - 1 - rank : rank;
   const int i0 = qt * kRows;
-  const int kend = p.causal ? min(p.Lkv, min(p.Lq, i0 + kRows)) : p.Lkv;
+  const int kend = p.causal ? min(p.Lkv, min(p.Lq, i0 + kRows) + p.coff) : p.Lkv;
   const int total = (kend + kBlk - 1) / kBlk;  // KV blocks visited
 
   if (threadIdx.x == 0) {
@@ -559,9 +561,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const int k0 = n * kBlk + 64 * w;  // first key of this half
-      const bool need_mask = (k0 + 64 > p.Lkv) || (p.causal && k0 + 63 > i0);
+      const bool need_mask = (k0 + 64 > p.Lkv) || (p.causal && k0 + 63 > i0 + p.coff);
       // keys k0 + e with e < lim are visible to this query
-      const int lim = min(p.Lkv - k0, p.causal ? i - k0 + 1 : 64);
+      const int lim = min(p.Lkv - k0, p.causal ? i + p.coff - k0 + 1 : 64);
       const uint32_t s_addr = tmem_addr(tbase, quarter * 32, kColS0 + 128 * (n % 2) + 64 * w);
       const uint32_t dp_addr = tmem_addr(tbase, quarter * 32, kColDp + 64 * w);
       // dP and S of this half in one TMEM round trip; the dP buffer is released at once so

@@ -87,10 +87,10 @@ __device__ __forceinline__ bool split_tile(const Problem& p, int j, int tile_row
 }
 
 // Number of leading keys of the tile starting at k0 that row i may see: key k0 + e is
-// visible iff e < lim (keys past Lkv are padding; under the causal mask key <= i).
+// visible iff e < lim (keys past Lkv are padding; under the causal mask key <= i + coff).
 __device__ __forceinline__ int visible_keys(const Problem& p, int k0, int i) {
   int lim = min(p.Lkv - k0, kBN);
-  if (p.causal) lim = min(lim, i - k0 + 1);
+  if (p.causal) lim = min(lim, i + p.coff - k0 + 1);
   return lim;
 }
 
@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (r0 >= p.Lq) {
       nkv[w] = 0;
     } else {
-      const int kend = p.causal ? min(p.Lkv, min(p.Lq, r0 + kBM)) : p.Lkv;
+      const int kend = p.causal ? min(p.Lkv, min(p.Lq, r0 + kBM) + p.coff) : p.Lkv;
       nkv[w] = (kend + kBN - 1) / kBN;
     }
   }
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const int k0 = j * kBN;
-      const bool need_mask = (k0 + kBN > p.Lkv) || (p.causal && k0 + kBN - 1 > tile_row0);
+      const bool need_mask = (k0 + kBN > p.Lkv) || (p.causal && k0 + kBN - 1 > tile_row0 + p.coff);
       // The row's 128 scores in registers (one TMEM round trip), then its maximum.
       uint32_t sv[kBN];
 #pragma unroll

@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(kThreads) vec_fwd_kernel(Problem p, int chunk)
     sm.lrow[threadIdx.x] = 0.f;
   }
   int kv_end = p.Lkv;
-  if (p.causal) kv_end = min(p.Lkv, p.Lq);  // query i sees keys 0..i only
+  if (p.causal) kv_end = min(p.Lkv, p.Lq + p.coff);  // query i sees keys 0..i+coff only
   const int j_begin = c * chunk, j_end = min(kv_end, j_begin + chunk);
   const T* kp = row_ptr<T>(p.k, p.lk, b, g, 0);
   const T* vp = row_ptr<T>(p.v, p.lv, b, g, 0);
@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kThreads) vec_fwd_kernel(Problem p, int chunk)
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) acc += sm.spart[w][r2][jj];
         const int j = j0 + jj;
-        const bool vis = r2 < R && j < j_end && (!p.causal || j <= i2);
+        const bool vis = r2 < R && j < j_end && (!p.causal || j <= i2 + p.coff);
         s[e] = vis ? acc * p.scale_log2 : neg_inf();
         bmax = fmaxf(bmax, s[e]);
       }
@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(kThreads) vec_bwd_kernel(Problem p, int chunk)
     dq[t] = 0.f;
   }
   int kv_end = p.Lkv;
-  if (p.causal) kv_end = min(p.Lkv, p.Lq);
+  if (p.causal) kv_end = min(p.Lkv, p.Lq + p.coff);
   const int j_begin = c * chunk, j_own_end = min(p.Lkv, j_begin + chunk);
   const int j_end = min(kv_end, j_own_end);
   const T* kp = row_ptr<T>(p.k, p.lk, b, g, 0);
@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(kThreads) vec_bwd_kernel(Problem p, int chunk)
         dp += sm.dppart[w][r2][jj];
       }
       const int j = j0 + jj;
-      const bool vis = r2 < R && j < j_end && (!p.causal || j <= r2 % p.Lq);
+      const bool vis = r2 < R && j < j_end && (!p.causal || j <= r2 % p.Lq + p.coff);
       const float pe = vis ? exp2f(s * p.scale_log2 - sm.lse2[r2]) : 0.f;
       sm.pr[r2][jj] = pe;
       sm.dsr[r2][jj] = pe * (dp - sm.delta[r2]);
@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(kThreads) vec_bwd_kernel(Problem p, int chunk)
       }
     }
   }
-  // Keys this block owns but no query can see (causal, j >= Lq) get zero gradients.
+  // Keys this block owns but no query can see (causal, j >= Lq + coff) get zero gradients.
   for (int64_t e = (int64_t)max(j_end, j_begin) * D + threadIdx.x; e < (int64_t)j_own_end * D;
        e += kThreads) {
     const int64_t jj = e / D, d = e % D;

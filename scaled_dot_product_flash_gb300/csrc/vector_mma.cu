@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(128) vec_mma_fwd_kernel(const __grid_constant_
   const int mt = warp % MT, kq = warp / MT;  // row block, key slice
   constexpr int kSliceKeys = kKeys / L::kSlices;
   const int R = p.G * p.Lq;
-  const int kv_end = p.causal ? min(p.Lkv, p.Lq) : p.Lkv;  // query i sees keys 0..i only
+  const int kv_end = p.causal ? min(p.Lkv, p.Lq + p.coff) : p.Lkv;  // query i sees keys 0..i+coff
   const int j_begin = c * chunk, j_end = min(kv_end, j_begin + chunk);
   const int ntiles = j_end > j_begin ? (j_end - j_begin + kKeys - 1) / kKeys : 0;
   const WaitCtx wc{&abort_flag, 0, p.wait_limit_ns, p.err, kKidVecFwd};
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(128) vec_mma_fwd_kernel(const __grid_constant_
         for (int e = 0; e < 4; ++e) {
           const int j = kbase + 8 * nt + (e & 1);
           const int ir = e < 2 ? i0 : i1, rr = e < 2 ? r0 : r1;
-          const bool vis = j < j_end && rr < R && (!p.causal || j <= ir);
+          const bool vis = j < j_end && rr < R && (!p.causal || j <= ir + p.coff);
           x[nt][e] = vis ? sc[nt][e] * c2 : ninf();
         }
       float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
@@ -413,7 +413,7 @@ __global__ void __launch_bounds__(128) vec_mma_bwd_kernel(const __grid_constant_
   const int b = blockIdx.z, g = blockIdx.y;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int R = p.G * p.Lq;
-  const int kv_end = p.causal ? min(p.Lkv, p.Lq) : p.Lkv;
+  const int kv_end = p.causal ? min(p.Lkv, p.Lq + p.coff) : p.Lkv;
   const int j_begin = c * chunk, j_own_end = min(p.Lkv, j_begin + chunk);
   const int j_end = min(kv_end, j_own_end);
   const int ntiles = j_end > j_begin ? (j_end - j_begin + kKeys - 1) / kKeys : 0;
@@ -529,7 +529,7 @@ __global__ void __launch_bounds__(128) vec_mma_bwd_kernel(const __grid_constant_
         for (int e = 0; e < 4; ++e) {
           const int j = tile_key0 + kl + (e & 1);
           const bool first = e < 2;
-          const bool vis = j < j_end && (!p.causal || j <= (first ? ia : ib));
+          const bool vis = j < j_end && (!p.causal || j <= (first ? ia : ib) + p.coff);
           const float x = fmaf(sc[nt][e], c2, first ? nla : nlb);
           pv[e] = vis ? ex2(x) : 0.f;
           dsv[e] = pv[e] * (dp[nt][e] + (first ? nda : ndb));
@@ -609,7 +609,7 @@ __global__ void __launch_bounds__(128) vec_mma_bwd_kernel(const __grid_constant_
       }
     }
   }
-  // Keys this block owns that no query can see (causal, j >= Lq) get zero gradients.
+  // Keys this block owns that no query can see (causal, j >= Lq + coff) get zero gradients.
   for (int64_t e = (int64_t)max(j_begin + ntiles * kKeys, j_begin) * D + threadIdx.x; e < (int64_t)j_own_end * D;
        e += blockDim.x) {
     const int64_t jj = e / D, d = e % D;

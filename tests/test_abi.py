@@ -90,6 +90,9 @@ INVALID, UNSUPPORTED, WORKSPACE = 1, 2, 5
     (dict(B=70000), UNSUPPORTED),
     (dict(o=Q + 64), INVALID),                # out overlaps q
     (dict(lse=O), INVALID),                   # lse overlaps out
+    (dict(causal=3), INVALID),                # unknown causal mode
+    (dict(causal=-1), INVALID),
+    (dict(causal=2, Lq=65, Lkv=64), UNSUPPORTED),   # bottom-right needs Lq <= Lkv
 ])
 def test_forward_rejects(lib, kw, code):
     assert fwd(lib, **kw) == code

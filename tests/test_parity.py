@@ -94,6 +94,25 @@ def test_matrix(shape, dtype, causal):
     full_parity(shape, dtype, causal, seed=100 + shape.Lq + shape.D)
 
 
+# ------------------------------------------------------------------ bottom-right causal
+BOTTOM_RIGHT = [
+    (_lib.PATH_AUTO, Shape(1, 8, 2, 200, 700, 128), "bf16"),    # tensor cores, Lq < Lkv
+    (_lib.PATH_AUTO, Shape(2, 4, 4, 130, 131, 64), "f16"),      # tensor cores, offset 1
+    (_lib.PATH_AUTO, Shape(1, 4, 1, 300, 300, 96), "bf16"),     # tensor cores, Lq = Lkv
+    (_lib.PATH_AUTO, Shape(2, 8, 2, 4, 500, 128), "bf16"),      # short query, warp MMA
+    (_lib.PATH_AUTO, Shape(1, 4, 2, 40, 130, 32), "f32"),       # CUDA cores
+    (_lib.PATH_AUTO, Shape(1, 2, 2, 3, 90, 64), "f32"),         # short query, CUDA cores
+    (_lib.PATH_SIMT, Shape(1, 4, 2, 70, 200, 64), "bf16"),      # forced CUDA cores
+]
+
+
+@pytest.mark.parametrize("path,shape,dtype", BOTTOM_RIGHT)
+def test_bottom_right_causal(path, shape, dtype):
+    """Key j hidden from query i when j > i + Lkv - Lq (the last query sees every key)."""
+    with api.force_path(path):
+        full_parity(shape, dtype, 2, seed=11)
+
+
 # ------------------------------------------------------------------ each family forced
 FORCED = [
     (_lib.PATH_SIMT, Shape(1, 4, 2, 200, 150, 128), "bf16", True),
