@@ -28,10 +28,12 @@
  *    SDPA_CAUSAL_BOTTOM_RIGHT (2: hidden when j > i + Lkv − Lq, so the last query sees
  *    every key, the alignment a query chunk at the end of a longer KV sequence needs;
  *    requires Lq <= Lkv, else SDPA_ERR_UNSUPPORTED).  Other values: SDPA_ERR_INVALID_ARG.
- *  - Layout: every tensor is a dense, contiguous row-major [B, H, L, D] array of `dtype`
- *    (H = Hq for q, out, dout, dq; H = Hkv for k, v, dk, dv).  lse is a dense fp32
- *    [B, Hq, Lq] array.  All pointers are DEVICE pointers (or managed memory) on the
- *    current CUDA device, and must be 16-byte aligned.
+ *  - Layout: for sdpa_fwd, sdpa_bwd and sdpa_bwd_noalloc every tensor is a dense,
+ *    contiguous row-major [B, H, L, D] array of `dtype` (H = Hq for q, out, dout, dq;
+ *    H = Hkv for k, v, dk, dv); sdpa_fwd_strided and sdpa_bwd_strided take the same
+ *    tensors with per-tensor strides (see there).  lse is a dense fp32 [B, Hq, Lq] array.
+ *    All pointers are DEVICE pointers (or managed memory) on the current CUDA device, and
+ *    must be 16-byte aligned.
  *  - Ownership: the caller allocates and owns every buffer.  The library keeps only a
  *    static device error word and host-side counters.
  *  - Execution: every call enqueues work on `stream` (a cudaStream_t; NULL = the legacy
