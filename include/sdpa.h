@@ -129,7 +129,7 @@ int sdpa_bwd(const void* q, const void* k, const void* v, const void* out, const
  *    (checked: sorted by stride, each stride covers the extent of the smaller ones).
  *    Otherwise SDPA_ERR_INVALID_ARG.
  *  - Inputs may overlap one another (q, k, v as views of one buffer); outputs may overlap
- *    nothing, judged by each tensor's address range [base, base + extent).
+ *    nothing, as measured by each tensor's address range [base, base + extent).
  * sdpa_fwd_strided reads strides->q, k, v and writes with strides->o; sdpa_bwd_strided
  * uses all eight (o is the forward output it reads).
  */
