@@ -33,6 +33,11 @@ Readings of points the pages leave open (each also listed in the design notes):
 * GQA groups are contiguous: query head h reads KV head h // (Hq // Hkv).
 * The backward is the textbook vector-Jacobian product of the forward with
   delta = rowsum(dO * O) taken from this oracle's own fp64 O.
+* Attention sinks (optional, one logit per query head): the sink joins every row's
+  softmax as one more entry with score ``sink[h]`` (natural-log units, like scale·q·k)
+  and a zero value vector, so it enlarges the row sum and the logsumexp but adds nothing
+  to O.  The backward is the same chain rule; the sink's own gradient is
+  -sum_i p_sink,i · delta_i (its dP entry is zero because its value is zero).
 * The oracle does not clamp exponent arguments (the clamp mentioned in [MLX-VJP]
   "Implementation Notes" only guards the GPU's exp2 against overflow; after the row
   maximum is subtracted every argument is <= 0 already).
@@ -93,17 +98,26 @@ def _scores(q_rows, k, scale, offset, row_idx):
     return s
 
 
-def _softmax_rows(s):
+def _softmax_rows(s, sink=None):
     """Row softmax as [PyTensor-SDPA] "Proposed change" writes it, plus the logsumexp.
 
     Subtract the row maximum, exponentiate, divide by the row sum.  The logsumexp of
     the row ([MPS-SDPA] "Problem - Unused second output tensor") is max + log(sum).
+    With a sink logit, the row is the scores plus one more entry equal to the sink; the
+    returned P leaves that entry out, and p_sink (one per row) is returned as well.
     """
     m = s.max(axis=1, keepdims=True)
+    if sink is not None:
+        m = np.maximum(m, sink)
     e = np.exp(s - m)
     l = e.sum(axis=1, keepdims=True)
+    if sink is not None:
+        es = np.exp(sink - m)
+        l = l + es
     p = e / l
     lse = (m + np.log(l))[:, 0]
+    if sink is not None:
+        return p, lse, (es / l)[:, 0]
     return p, lse
 
 
@@ -113,11 +127,12 @@ def _blocks(n, row_block):
         yield r0, min(n, r0 + step)
 
 
-def head_forward(q, k, v, scale, is_causal, rows=None, row_block=None):
+def head_forward(q, k, v, scale, is_causal, rows=None, row_block=None, sink=None):
     """Forward of one head: O = softmax(scale·q kᵀ [+ causal mask]) v and its logsumexp.
 
     q: [Lq, D], k, v: [Lkv, D].  ``rows`` (optional, sorted or not) selects which query
-    rows to compute; by default all.  Returns (O [n, D], lse [n]) in float64.
+    rows to compute; by default all.  ``sink``: this head's sink logit, or None.
+    Returns (O [n, D], lse [n]) in float64.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     off = _causal_offset(is_causal, q.shape[0], k.shape[0])
@@ -126,12 +141,12 @@ def head_forward(q, k, v, scale, is_causal, rows=None, row_block=None):
     lse = np.empty(idx.size)
     for a, b in _blocks(idx.size, row_block):
         sel = idx[a:b]
-        p, lse[a:b] = _softmax_rows(_scores(q[sel], k, scale, off, sel))
+        p, lse[a:b] = _softmax_rows(_scores(q[sel], k, scale, off, sel), sink)[:2]
         o[a:b] = p @ v
     return o, lse
 
 
-def head_backward(q, k, v, dout, scale, is_causal, row_block=None):
+def head_backward(q, k, v, dout, scale, is_causal, row_block=None, sink=None):
     """Backward of one head (textbook VJP).  Returns (dq, dk_part, dv_part) in float64.
 
     Steps, per [MLX-VJP]'s description (recompute S, P = exp(S - LSE), then gradients)
@@ -145,15 +160,18 @@ def head_backward(q, k, v, dout, scale, is_causal, row_block=None):
         dQ  = scale · dS k
         dK  = scale · dSᵀ q
     dk_part and dv_part are this head's contribution to its KV head; the caller sums
-    them over the query heads of the group.
+    them over the query heads of the group.  With a sink logit, a fourth value is
+    returned: the sink's gradient, -sum_i p_sink,i · δ_i.
     """
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     off = _causal_offset(is_causal, q.shape[0], k.shape[0])
     dq = np.empty_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
+    dsink = 0.0
     for a, b in _blocks(q.shape[0], row_block):
-        p, _ = _softmax_rows(_scores(q[a:b], k, scale, off, np.arange(a, b)))
+        sm = _softmax_rows(_scores(q[a:b], k, scale, off, np.arange(a, b)), sink)
+        p = sm[0]
         o = p @ v
         dv += p.T @ dout[a:b]
         dp = dout[a:b] @ v.T
@@ -161,6 +179,10 @@ def head_backward(q, k, v, dout, scale, is_causal, row_block=None):
         ds = p * (dp - delta)
         dq[a:b] = scale * (ds @ k)
         dk += scale * (ds.T @ q[a:b])
+        if sink is not None:
+            dsink -= float((sm[2] * delta[:, 0]).sum())
+    if sink is not None:
+        return dq, dk, dv, dsink
     return dq, dk, dv
 
 
@@ -176,11 +198,11 @@ def _check(q, k, v):
     return B, Hq, Hkv, Hq // Hkv
 
 
-def sdpa_forward(q, k, v, scale, is_causal, row_block=None):
+def sdpa_forward(q, k, v, scale, is_causal, row_block=None, sinks=None):
     """Forward over [B, H, L, D] arrays with GQA ([MLX-VJP] "Key Features").
 
-    Query head h reads KV head h // G with G = Hq // Hkv.  Returns (O [B,Hq,Lq,D],
-    lse [B,Hq,Lq]) in float64.
+    Query head h reads KV head h // G with G = Hq // Hkv; ``sinks`` ([Hq] or None) adds
+    one sink logit per query head.  Returns (O [B,Hq,Lq,D], lse [B,Hq,Lq]) in float64.
     """
     B, Hq, Hkv, G = _check(q, k, v)
     o = np.empty(q.shape[:3] + (v.shape[3],))
@@ -189,38 +211,53 @@ def sdpa_forward(q, k, v, scale, is_causal, row_block=None):
         for h in range(Hq):
             g = h // G
             o[b, h], lse[b, h] = head_forward(q[b, h], k[b, g], v[b, g], scale,
-                                              is_causal, row_block=row_block)
+                                              is_causal, row_block=row_block,
+                                              sink=None if sinks is None else float(sinks[h]))
     return o, lse
 
 
-def group_backward(q, k, v, dout, scale, is_causal, b, g, row_block=None):
+def group_backward(q, k, v, dout, scale, is_causal, b, g, row_block=None, sinks=None):
     """Backward for KV head g of batch b: dQ of its G query heads, and dK, dV of g.
 
     dK and dV sum the contributions of every query head that reads KV head g
     ([MLX-VJP] "Implementation Notes": several query heads share one KV head).
-    Returns (dq [G, Lq, D], dk [Lkv, D], dv [Lkv, D]).
+    Returns (dq [G, Lq, D], dk [Lkv, D], dv [Lkv, D]), and with ``sinks`` also the
+    gradients of the group's G sink logits (batch b only).
     """
     B, Hq, Hkv, G = _check(q, k, v)
     dq = np.empty((G,) + q.shape[2:])
     dk = np.zeros(k.shape[2:])
     dv = np.zeros(v.shape[2:])
+    dsink = np.zeros(G)
     for t in range(G):
         h = g * G + t
-        dq[t], dk_h, dv_h = head_backward(q[b, h], k[b, g], v[b, g], dout[b, h], scale,
-                                          is_causal, row_block=row_block)
+        r = head_backward(q[b, h], k[b, g], v[b, g], dout[b, h], scale, is_causal,
+                          row_block=row_block, sink=None if sinks is None else float(sinks[h]))
+        dq[t], dk_h, dv_h = r[:3]
+        if sinks is not None:
+            dsink[t] = r[3]
         dk += dk_h
         dv += dv_h
+    if sinks is not None:
+        return dq, dk, dv, dsink
     return dq, dk, dv
 
 
-def sdpa_backward(q, k, v, dout, scale, is_causal, row_block=None):
-    """Backward over [B, H, L, D] arrays.  Returns (dq, dk, dv) in float64."""
+def sdpa_backward(q, k, v, dout, scale, is_causal, row_block=None, sinks=None):
+    """Backward over [B, H, L, D] arrays.  Returns (dq, dk, dv) in float64, and with
+    ``sinks`` ([Hq]) also dsinks [Hq], each summed over the batch."""
     B, Hq, Hkv, G = _check(q, k, v)
     dq = np.empty(q.shape, dtype=np.float64)
     dk = np.empty(k.shape, dtype=np.float64)
     dv = np.empty(v.shape, dtype=np.float64)
+    dsinks = np.zeros(Hq)
     for b in range(B):
         for g in range(Hkv):
-            dq[b, g * G:(g + 1) * G], dk[b, g], dv[b, g] = group_backward(
-                q, k, v, dout, scale, is_causal, b, g, row_block=row_block)
+            r = group_backward(q, k, v, dout, scale, is_causal, b, g, row_block=row_block,
+                               sinks=sinks)
+            dq[b, g * G:(g + 1) * G], dk[b, g], dv[b, g] = r[:3]
+            if sinks is not None:
+                dsinks[g * G:(g + 1) * G] += r[3]
+    if sinks is not None:
+        return dq, dk, dv, dsinks
     return dq, dk, dv

@@ -347,6 +347,125 @@ def test_bottom_right_square_and_single_query(impl=None):
         impl.sdpa_forward(q, k[:, :, :3], v[:, :, :3], 0.5, 2)  # Lq > Lkv
 
 
+# ----------------------------------------------------------------- attention sinks
+def test_sink_at_minus_infinity_is_no_sink(impl=None):
+    """exp(-inf) = 0: a sink of -inf leaves every output as without a sink and its own
+    gradient is zero."""
+    impl = impl or oracle
+    rng = np.random.default_rng(51)
+    q, k, v, do = make(rng, B=2, Hq=4, Hkv=2, Lq=5, Lkv=7, D=3)
+    sinks = np.full(4, -np.inf)
+    for causal in (False, True):
+        for a, b in zip(impl.sdpa_forward(q, k, v, 0.6, causal, sinks=sinks),
+                        impl.sdpa_forward(q, k, v, 0.6, causal)):
+            np.testing.assert_allclose(a, b, atol=1e-14)
+        r = impl.sdpa_backward(q, k, v, do, 0.6, causal, sinks=sinks)
+        for a, b in zip(r[:3], impl.sdpa_backward(q, k, v, do, 0.6, causal)):
+            np.testing.assert_allclose(a, b, atol=1e-14)
+        np.testing.assert_array_equal(r[3], 0.0)
+
+
+def test_sink_single_key_closed_form(impl=None):
+    """One key with score s and a sink σ: O = v0 · e^s / (e^s + e^σ),
+    lse = log(e^s + e^σ), and dσ = -Σ_i e^σ / (e^s_i + e^σ) · (dO_i · O_i)."""
+    impl = impl or oracle
+    rng = np.random.default_rng(52)
+    q, k, v, do = make(rng, B=1, Hq=2, Hkv=1, Lq=3, Lkv=1, D=4)
+    sinks = np.array([0.3, -1.2])
+    o, lse = impl.sdpa_forward(q, k, v, 0.8, False, sinks=sinks)
+    _, _, _, dsinks = impl.sdpa_backward(q, k, v, do, 0.8, False, sinks=sinks)
+    for h in range(2):
+        sc = 0.8 * q[0, h] @ k[0, 0, 0]
+        w = 1.0 / (1.0 + np.exp(sinks[h] - sc))
+        np.testing.assert_allclose(o[0, h], w[:, None] * v[0, 0, 0][None, :], atol=1e-14)
+        np.testing.assert_allclose(lse[0, h], np.logaddexp(sc, sinks[h]), atol=1e-14)
+        want = -np.sum((1.0 - w) * w * (do[0, h] @ v[0, 0, 0]))
+        np.testing.assert_allclose(dsinks[h], want, atol=1e-13)
+
+
+def test_sink_is_an_extra_key_with_zero_value(impl=None):
+    """A sink σ behaves as one more key whose score is σ for every row and whose value is
+    zero.  Build that key explicitly: append a coordinate 1 to every query and 0 to every
+    key, and put a key (0, …, 0, σ/scale) with value 0 in front of the keys.  Without a
+    mask, and with the bottom-right mask (which the extra front key leaves in place for
+    the old keys and keeps visible to every row), the sink problem's outputs, logsumexp
+    and gradients are those of the bigger problem, and dσ = dK_extra[D] / scale."""
+    impl = impl or oracle
+    rng = np.random.default_rng(53)
+    B, Hq, Hkv, Lq, Lkv, D, scale = 2, 4, 2, 5, 7, 3, 0.7
+    q, k, v, do = make(rng, B=B, Hq=Hq, Hkv=Hkv, Lq=Lq, Lkv=Lkv, D=D)
+    sinks = np.array([0.4, -0.9, 1.3, 0.0])
+    G = Hq // Hkv
+    qa = np.concatenate([q, np.ones((B, Hq, Lq, 1))], axis=3)
+    for causal in (False, 2):
+        o, lse = impl.sdpa_forward(q, k, v, scale, causal, sinks=sinks)
+        dq, dk, dv, dsinks = impl.sdpa_backward(q, k, v, do, scale, causal, sinks=sinks)
+        for h in range(Hq):
+            g = h // G
+            ka = np.concatenate([k[:, g:g + 1], np.zeros((B, 1, Lkv, 1))], axis=3)
+            extra = np.zeros((B, 1, 1, D + 1))
+            extra[..., D] = sinks[h] / scale
+            ka = np.concatenate([extra, ka], axis=2)
+            va = np.concatenate([np.zeros((B, 1, 1, D)), v[:, g:g + 1]], axis=2)
+            qh, doh = qa[:, h:h + 1], do[:, h:h + 1]
+            oa, lsea = impl.sdpa_forward(qh, ka, va, scale, causal)
+            np.testing.assert_allclose(o[:, h:h + 1], oa, atol=1e-13)
+            np.testing.assert_allclose(lse[:, h:h + 1], lsea, atol=1e-13)
+            dqa, dka, _ = impl.sdpa_backward(qh, ka, va, doh, scale, causal)
+            np.testing.assert_allclose(dq[:, h:h + 1], dqa[..., :D], atol=1e-12)
+            np.testing.assert_allclose(dsinks[h], dka[:, 0, 0, D].sum() / scale, atol=1e-12)
+        # dK and dV of a KV head sum over its query heads; check them on the G = 1 view.
+        for g in range(Hkv):
+            hs = range(g * G, (g + 1) * G)
+            dk_sum = np.zeros_like(k[:, g])
+            dv_sum = np.zeros_like(v[:, g])
+            for h in hs:
+                ka = np.concatenate([k[:, g:g + 1], np.zeros((B, 1, Lkv, 1))], axis=3)
+                extra = np.zeros((B, 1, 1, D + 1))
+                extra[..., D] = sinks[h] / scale
+                ka = np.concatenate([extra, ka], axis=2)
+                va = np.concatenate([np.zeros((B, 1, 1, D)), v[:, g:g + 1]], axis=2)
+                _, dka, dva = impl.sdpa_backward(qa[:, h:h + 1], ka, va, do[:, h:h + 1], scale,
+                                                 causal)
+                dk_sum += dka[:, 0, 1:, :D]
+                dv_sum += dva[:, 0, 1:]
+            np.testing.assert_allclose(dk[:, g], dk_sum, atol=1e-12)
+            np.testing.assert_allclose(dv[:, g], dv_sum, atol=1e-12)
+
+
+SINK_FD_CASES = [
+    dict(B=2, Hq=2, Hkv=1, Lq=5, Lkv=6, D=4, causal=False),
+    dict(B=1, Hq=4, Hkv=2, Lq=6, Lkv=4, D=3, causal=True),
+    dict(B=1, Hq=2, Hkv=2, Lq=3, Lkv=6, D=2, causal=2),
+]
+
+
+@pytest.mark.parametrize("case", SINK_FD_CASES,
+                         ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
+def test_sink_gradients_match_finite_differences(case, impl=None):
+    impl = impl or oracle
+    rng = np.random.default_rng(54)
+    c = dict(case)
+    causal = c.pop("causal")
+    q, k, v, do = make(rng, **c)
+    sinks = rng.standard_normal(c["Hq"])
+    scale = 0.7
+
+    def f():
+        o, _ = impl.sdpa_forward(q, k, v, scale, causal, sinks=sinks)
+        return float((o * do).sum())
+    dq, dk, dv, dsinks = impl.sdpa_backward(q, k, v, do, scale, causal, sinks=sinks)
+    np.testing.assert_allclose(dq, _fd_grad(q, f), atol=1e-7, rtol=1e-6)
+    np.testing.assert_allclose(dk, _fd_grad(k, f), atol=1e-7, rtol=1e-6)
+    np.testing.assert_allclose(dv, _fd_grad(v, f), atol=1e-7, rtol=1e-6)
+    np.testing.assert_allclose(dsinks, _fd_grad(sinks, f), atol=1e-7, rtol=1e-6)
+
+
+def _sink_fd_all(impl):
+    for c in SINK_FD_CASES:
+        test_sink_gradients_match_finite_differences(c, impl)
+
+
 # ----------------------------------------------------------------- pins have teeth
 PINS = [
     test_rows_of_p_sum_to_one,
@@ -360,6 +479,10 @@ PINS = [
     test_mha_equals_independent_heads,
     test_bottom_right_equals_padded_top_left,
     test_bottom_right_square_and_single_query,
+    test_sink_at_minus_infinity_is_no_sink,
+    test_sink_single_key_closed_form,
+    test_sink_is_an_extra_key_with_zero_value,
+    _sink_fd_all,
 ]
 
 
@@ -389,43 +512,70 @@ def _mutant(name):
     elif name == "lse_log2":
         orig = m._softmax_rows
 
-        def _softmax_rows(s):
-            p, lse = orig(s)
-            return p, lse / math.log(2.0)
+        def _softmax_rows(s, sink=None):
+            r = orig(s, sink)
+            return (r[0], r[1] / math.log(2.0)) + tuple(r[2:])
         m._softmax_rows = _softmax_rows
     elif name == "gqa_modulo":
-        def sdpa_forward(q, k, v, scale, is_causal, row_block=None):
+        def sdpa_forward(q, k, v, scale, is_causal, row_block=None, sinks=None):
             B, Hq, Hkv, G = m._check(q, k, v)
             o = np.empty(q.shape[:3] + (v.shape[3],))
             lse = np.empty(q.shape[:3])
             for b in range(B):
                 for h in range(Hq):
                     g = h % Hkv
-                    o[b, h], lse[b, h] = m.head_forward(q[b, h], k[b, g], v[b, g], scale, is_causal)
+                    o[b, h], lse[b, h] = m.head_forward(
+                        q[b, h], k[b, g], v[b, g], scale, is_causal,
+                        sink=None if sinks is None else float(sinks[h]))
             return o, lse
         m.sdpa_forward = sdpa_forward
     elif name == "no_scale_in_dq":
         orig = m.head_backward
 
-        def head_backward(q, k, v, dout, scale, is_causal, row_block=None):
-            dq, dk, dv = orig(q, k, v, dout, scale, is_causal, row_block)
-            return (dq / scale if scale else dq), dk, dv
+        def head_backward(q, k, v, dout, scale, is_causal, row_block=None, sink=None):
+            r = orig(q, k, v, dout, scale, is_causal, row_block, sink)
+            return ((r[0] / scale if scale else r[0]),) + tuple(r[1:])
         m.head_backward = head_backward
     elif name == "delta_dropped":
-        def head_backward(q, k, v, dout, scale, is_causal, row_block=None):
+        def head_backward(q, k, v, dout, scale, is_causal, row_block=None, sink=None):
             q, k, v, dout = (np.asarray(x, float) for x in (q, k, v, dout))
             off = m._causal_offset(is_causal, q.shape[0], k.shape[0])
-            p, _ = m._softmax_rows(m._scores(q, k, scale, off, np.arange(q.shape[0])))
+            sm = m._softmax_rows(m._scores(q, k, scale, off, np.arange(q.shape[0])), sink)
+            p = sm[0]
             ds = p * (dout @ v.T)
-            return scale * ds @ k, scale * ds.T @ q, p.T @ dout
+            r = (scale * ds @ k, scale * ds.T @ q, p.T @ dout)
+            return r if sink is None else r + (0.0,)
         m.head_backward = head_backward
     elif name == "dk_transposed_operand":
         orig = m.head_backward
 
-        def head_backward(q, k, v, dout, scale, is_causal, row_block=None):
-            dq, dk, dv = orig(q, k, v, dout, scale, is_causal, row_block)
-            return dq, dk[::-1].copy(), dv
+        def head_backward(q, k, v, dout, scale, is_causal, row_block=None, sink=None):
+            r = orig(q, k, v, dout, scale, is_causal, row_block, sink)
+            return (r[0], r[1][::-1].copy()) + tuple(r[2:])
         m.head_backward = head_backward
+    elif name == "sink_missing_from_lse":
+        orig = m._softmax_rows
+
+        def _softmax_rows(s, sink=None):
+            r = orig(s, sink)
+            return (r[0], orig(s)[1]) + tuple(r[2:])
+        m._softmax_rows = _softmax_rows
+    elif name == "sink_gradient_sign":
+        orig = m.head_backward
+
+        def head_backward(q, k, v, dout, scale, is_causal, row_block=None, sink=None):
+            r = orig(q, k, v, dout, scale, is_causal, row_block, sink)
+            return r if sink is None else r[:3] + (-r[3],)
+        m.head_backward = head_backward
+    elif name == "sink_given_a_value":
+        orig = m.head_forward
+
+        def head_forward(q, k, v, scale, is_causal, rows=None, row_block=None, sink=None):
+            o, lse = orig(q, k, v, scale, is_causal, rows, row_block, sink)
+            if sink is not None:
+                o = o + np.exp(sink - lse)[:, None] * np.asarray(v, float)[0][None, :]
+            return o, lse
+        m.head_forward = head_forward
     else:
         raise KeyError(name)
     return m
@@ -433,7 +583,8 @@ def _mutant(name):
 
 @pytest.mark.parametrize("name", ["causal_diag_masked", "causal_off_by_one", "lse_log2", "gqa_modulo",
                                   "no_scale_in_dq", "delta_dropped", "dk_transposed_operand",
-                                  "bottom_right_offset_off_by_one"])
+                                  "bottom_right_offset_off_by_one", "sink_missing_from_lse",
+                                  "sink_gradient_sign", "sink_given_a_value"])
 def test_planted_mistakes_are_caught(name):
     mutant = _mutant(name)
     failures = 0
