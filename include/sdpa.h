@@ -149,6 +149,38 @@ int sdpa_bwd_strided(const void* q, const void* k, const void* v, const void* ou
                      size_t workspace_bytes, void* stream);
 
 /*
+ * Attention sinks.  The strided calls plus one learned logit per query head, sinks[h],
+ * that joins the softmax of every row of head h as one more entry with a zero value
+ * vector: it enlarges each row's normaliser but contributes nothing to O.  In the notation
+ * above, with σ = sinks[h]:
+ *     P_ij = exp(S_ij) / (exp(σ) + Σ_j' exp(S_ij'))      O = P · V
+ *     lse[b,h,i] = ln(exp(σ) + Σ_j exp(S_ij))
+ *     dσ_h = −Σ_{b,i} exp(σ − lse[b,h,i]) · δ_{b,h,i}    (δ_i = Σ_d dO_id·O_id)
+ * and dQ, dK, dV keep their formulas, with P recomputed from this lse.  The pages name
+ * sinks, and their gradients, only as something the Metal backward leaves to unfused
+ * operations ("[Metal] Add Flash Attention VJP for training", section "Limitations"); the
+ * definition here is the usual one of a per-head sink logit.  Here they are fused: the
+ * forward folds σ into each row's maximum and sum after its last key tile, the backward
+ * kernels are unchanged, and dσ comes from one small kernel over lse and δ that sums in a
+ * fixed order (bitwise reproducible).
+ *   sinks  [Hq] fp32, natural-log units like S (read; NULL = no sink, the strided call);
+ *          −inf means no sink for that head; +inf and NaN are not checked (NaN
+ *          propagates to the head's outputs).
+ *   dsinks [Hq] fp32, written with the sum over the batch (nullable; needs sinks).
+ * Pointers are device pointers, 4-byte aligned; sinks may overlap no output, dsinks
+ * nothing.  The backward's lse must be the one that sdpa_fwd_sinks wrote with the same
+ * sinks.  Other arguments and rules are those of sdpa_fwd_strided / sdpa_bwd_strided.
+ */
+int sdpa_fwd_sinks(const void* q, const void* k, const void* v, void* out, float* lse,
+                   const float* sinks, int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale,
+                   int is_causal, int dtype, const sdpa_strides_t* strides, void* stream);
+int sdpa_bwd_sinks(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                   const float* lse, const float* sinks, void* dq, void* dk, void* dv, float* dsinks,
+                   int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale, int is_causal,
+                   int dtype, const sdpa_strides_t* strides, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/*
  * Backward without a workspace argument: sdpa_bwd for callers that cannot allocate device
  * memory.  Such callers include code running inside a host application or framework that
  * owns every device allocation and hands its plugins nothing but their inputs and outputs,
@@ -220,7 +252,8 @@ typedef enum {
   SDPA_KERNEL_DKDV = 3,     /* tiled dK/dV kernel */
   SDPA_KERNEL_VEC_FWD = 4,  /* short-query forward */
   SDPA_KERNEL_VEC_BWD = 5,  /* short-query backward */
-  SDPA_KERNEL_COUNT = 6
+  SDPA_KERNEL_SINK_GRAD = 6, /* sink-logit gradients */
+  SDPA_KERNEL_COUNT = 7
 } sdpa_kernel_t;
 int sdpa_timing_enable(int on);
 int sdpa_timing_read(int kernel, double* total_ms, uint64_t* launches);

@@ -58,9 +58,13 @@ SIGNATURES = {
                               _vp]),
     "sdpa_bwd_strided": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                               _i, _i, _i, _i, _i, _i, _f, _i, _i, _sp, _vp, _sz, _vp]),
+    "sdpa_fwd_sinks": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i,
+                            _sp, _vp]),
+    "sdpa_bwd_sinks": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                            _i, _i, _i, _i, _i, _i, _f, _i, _i, _sp, _vp, _sz, _vp]),
 }
 BWD_NOALLOC_MAX_ROWS = 1 << 20
-KERNELS = {"fwd": 0, "delta": 1, "dq": 2, "dkdv": 3, "vec_fwd": 4, "vec_bwd": 5}
+KERNELS = {"fwd": 0, "delta": 1, "dq": 2, "dkdv": 3, "vec_fwd": 4, "vec_bwd": 5, "sink_grad": 6}
 
 _lib = None
 
@@ -126,6 +130,21 @@ def sdpa_bwd_strided(q, k, v, out, dout, lse, dq, dk, dv, B, Hq, Hkv, Lq, Lkv, D
     return load().sdpa_bwd_strided(q, k, v, out, dout, lse, dq, dk, dv, B, Hq, Hkv, Lq, Lkv, D,
                                    scale, is_causal, dtype, ctypes.byref(strides), workspace,
                                    workspace_bytes, stream)
+
+
+def sdpa_fwd_sinks(q, k, v, out, lse, sinks, B, Hq, Hkv, Lq, Lkv, D, scale, is_causal, dtype,
+                   strides, stream):
+    """sdpa_fwd_strided with one sink logit per query head (sinks: fp32 [Hq] or None)."""
+    return load().sdpa_fwd_sinks(q, k, v, out, lse, sinks, B, Hq, Hkv, Lq, Lkv, D, scale,
+                                 is_causal, dtype, ctypes.byref(strides), stream)
+
+
+def sdpa_bwd_sinks(q, k, v, out, dout, lse, sinks, dq, dk, dv, dsinks, B, Hq, Hkv, Lq, Lkv, D,
+                   scale, is_causal, dtype, strides, workspace, workspace_bytes, stream):
+    """sdpa_bwd_strided that also writes the sink-logit gradients dsinks (fp32 [Hq])."""
+    return load().sdpa_bwd_sinks(q, k, v, out, dout, lse, sinks, dq, dk, dv, dsinks, B, Hq, Hkv,
+                                 Lq, Lkv, D, scale, is_causal, dtype, ctypes.byref(strides),
+                                 workspace, workspace_bytes, stream)
 
 
 def sdpa_bwd_noalloc(q, k, v, out, dout, lse, dq, dk, dv, B, Hq, Hkv, Lq, Lkv, D, scale,

@@ -64,13 +64,21 @@ def _dims(q, k):
     return B, Hq, Hkv, Lq, Lkv, D
 
 
+def _check_sinks(name, t, Hq):
+    _check(name, t, torch.float32)
+    if t.dim() != 1 or t.numel() != Hq:
+        raise ValueError(f"{name} must be a 1-D fp32 tensor of Hq = {Hq} sink logits")
+
+
 def attention_forward(q, k, v, scale=None, is_causal=False, need_lse=True, out=None,
-                      lse=None, stream=None):
+                      lse=None, stream=None, sinks=None):
     """out = softmax(scale·q·kᵀ [causal]) · v; also the fp32 logsumexp when need_lse.
 
     q [B,Hq,Lq,D], k/v [B,Hkv,Lkv,D] CUDA tensors of one dtype (fp32/fp16/bf16), in any
     layout with contiguous rows (e.g. [B,L,H,D] storage seen through .transpose(1, 2));
     the strides go to the library, nothing is copied.  `out` defaults to q's layout.
+    ``sinks``: optional fp32 [Hq] sink logits, one extra softmax entry per row of each
+    query head with a zero value vector (the lse then includes it).
     Returns (out, lse or None).
     """
     for n, t in (("q", q), ("k", k), ("v", v)):
@@ -86,11 +94,14 @@ def attention_forward(q, k, v, scale=None, is_causal=False, need_lse=True, out=N
     if not need_lse:
         lse = None
     _check("out", out, q.dtype)
+    if sinks is not None:
+        _check_sinks("sinks", sinks, Hq)
     strides = _lib.make_strides(q=_layout(q), k=_layout(k), v=_layout(v), o=_layout(out))
-    st = _lib.sdpa_fwd_strided(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                               lse.data_ptr() if lse is not None else None,
-                               B, Hq, Hkv, Lq, Lkv, D, scale, _causal(is_causal),
-                               DTYPE_CODE[q.dtype], strides, _stream(stream))
+    st = _lib.sdpa_fwd_sinks(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                             lse.data_ptr() if lse is not None else None,
+                             sinks.data_ptr() if sinks is not None else None,
+                             B, Hq, Hkv, Lq, Lkv, D, scale, _causal(is_causal),
+                             DTYPE_CODE[q.dtype], strides, _stream(stream))
     if st != _lib.OK:
         raise _lib.SdpaError(st, "sdpa_fwd")
     return out, lse
@@ -102,8 +113,12 @@ def workspace_bytes(q, k):
 
 
 def attention_backward(q, k, v, out, dout, lse, scale=None, is_causal=False, workspace=None,
-                       dq=None, dk=None, dv=None, stream=None):
-    """(dq, dk, dv) of the forward, from its output ``out`` and logsumexp ``lse``."""
+                       dq=None, dk=None, dv=None, stream=None, sinks=None, dsinks=None):
+    """(dq, dk, dv) of the forward, from its output ``out`` and logsumexp ``lse``.
+
+    With ``sinks`` (the forward's fp32 [Hq] sink logits), returns (dq, dk, dv, dsinks),
+    dsinks being the fp32 [Hq] gradient of the sink logits summed over the batch.
+    """
     for n, t in (("q", q), ("k", k), ("v", v), ("out", out), ("dout", dout)):
         _check(n, t, q.dtype)
     _check("lse", lse, torch.float32)
@@ -117,16 +132,27 @@ def attention_backward(q, k, v, out, dout, lse, scale=None, is_causal=False, wor
         workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
     for n, t in (("dq", dq), ("dk", dk), ("dv", dv)):
         _check(n, t, q.dtype)
+    if sinks is not None:
+        _check_sinks("sinks", sinks, Hq)
+        dsinks = torch.empty_like(sinks) if dsinks is None else dsinks
+        _check_sinks("dsinks", dsinks, Hq)
+    elif dsinks is not None:
+        raise ValueError("dsinks needs sinks")
     strides = _lib.make_strides(q=_layout(q), k=_layout(k), v=_layout(v), o=_layout(out),
                                 dout=_layout(dout), dq=_layout(dq), dk=_layout(dk),
                                 dv=_layout(dv))
-    st = _lib.sdpa_bwd_strided(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                               dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                               dv.data_ptr(), B, Hq, Hkv, Lq, Lkv, D, scale,
-                               _causal(is_causal), DTYPE_CODE[q.dtype], strides,
-                               workspace.data_ptr(), workspace.numel(), _stream(stream))
+    st = _lib.sdpa_bwd_sinks(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                             dout.data_ptr(), lse.data_ptr(),
+                             sinks.data_ptr() if sinks is not None else None,
+                             dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                             dsinks.data_ptr() if dsinks is not None else None,
+                             B, Hq, Hkv, Lq, Lkv, D, scale, _causal(is_causal),
+                             DTYPE_CODE[q.dtype], strides, workspace.data_ptr(),
+                             workspace.numel(), _stream(stream))
     if st != _lib.OK:
         raise _lib.SdpaError(st, "sdpa_bwd")
+    if sinks is not None:
+        return dq, dk, dv, dsinks
     return dq, dk, dv
 
 

@@ -67,6 +67,8 @@ struct Problem {
   void* dk;
   void* dv;
   float* delta;      // δ = rowsum(dO∘O) [B,Hq,Lq]
+  const float* sinks;  // per-query-head sink logits [Hq] (natural log), or null
+  float* dsinks;       // their gradients [Hq] (backward), or null
   int B, Hq, Hkv, Lq, Lkv, D;
   int G;             // Hq / Hkv
   float scale;
@@ -89,6 +91,25 @@ __host__ __device__ __forceinline__ int64_t q_row(const Problem& p, int b, int h
 __host__ __device__ __forceinline__ int64_t row_off(const Layout& l, int b, int h, int64_t i) {
   return (int64_t)b * l.sb + (int64_t)h * l.sh + i * l.sl;
 }
+// Attention sink of query head h: one more softmax entry per row with logit sinks[h] and
+// a zero value vector.  Folds it into a finished row whose running maximum m and sum l are
+// in the log2 domain (P = exp2(c·s − m)) and returns the factor a by which the row's
+// unnormalised output must be scaled before the division by the updated l (1 without a
+// sink, so the no-sink arithmetic is unchanged).  m and l then describe the row with the
+// sink, so lse = ln2·(m + log2 l) includes it.  A NaN sink gives NaN outputs.
+__device__ __forceinline__ float fold_sink(const Problem& p, int h, float& m, float& l) {
+  if (!p.sinks) return 1.f;
+  const float s2 = p.sinks[h] * kLog2e;
+  if (s2 <= m) {
+    l += exp2f(s2 - m);
+    return 1.f;
+  }
+  const float a = exp2f(m - s2);
+  l = fmaf(l, a, 1.f);
+  m = s2;
+  return a;
+}
+
 template <typename T>
 __host__ __device__ __forceinline__ const T* row_ptr(const void* base, const Layout& l, int b, int h, int64_t i) {
   return static_cast<const T*>(base) + row_off(l, b, h, i);

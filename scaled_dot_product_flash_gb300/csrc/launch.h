@@ -14,6 +14,9 @@ cudaError_t launch_simt_dkdv(const Problem& p, int dtype, cudaStream_t s);
 // δ = rowsum(dO ∘ O) pre-pass, every dtype and D.
 cudaError_t launch_delta(const Problem& p, int dtype, cudaStream_t s);
 
+// Sink-logit gradients from lse and δ (any dtype: both are fp32).
+cudaError_t launch_sink_grad(const Problem& p, cudaStream_t s);
+
 // Short-query path (Lq <= 8, G·Lq <= 32): thread-block clusters split Lkv.
 bool vector_supported(const Problem& p, int dtype);
 cudaError_t launch_vector_fwd(const Problem& p, int dtype, cudaStream_t s);

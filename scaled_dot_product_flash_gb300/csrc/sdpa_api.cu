@@ -38,6 +38,7 @@ int error_word(unsigned** out) {
 }
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+bool aligned4(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 3u) == 0; }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   if (!a || !b || na == 0 || nb == 0) return false;
@@ -200,14 +201,16 @@ int status_of(cudaError_t e) { return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA
 
 using namespace sdpa;
 
-extern "C" int sdpa_fwd_strided(const void* q, const void* k, const void* v, void* out, float* lse,
-                                int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale,
-                                int is_causal, int dtype, const sdpa_strides_t* strides, void* stream) {
+extern "C" int sdpa_fwd_sinks(const void* q, const void* k, const void* v, void* out, float* lse,
+                              const float* sinks, int B, int Hq, int Hkv, int Lq, int Lkv, int D,
+                              float scale, int is_causal, int dtype, const sdpa_strides_t* strides,
+                              void* stream) {
   Problem p;
   int st = check_sizes(B, Hq, Hkv, Lq, Lkv, D, scale, dtype, &p);
   if (st != SDPA_OK) return st;
   if (!q || !k || !v || !out || !strides) return SDPA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) ||
+      !aligned4(sinks))
     return SDPA_ERR_INVALID_ARG;
   const size_t es = elem_size(dtype);
   size_t qb, kb, vb, ob;
@@ -219,11 +222,14 @@ extern "C" int sdpa_fwd_strided(const void* q, const void* k, const void* v, voi
       overlaps(lse, lb, q, qb) || overlaps(lse, lb, k, kb) || overlaps(lse, lb, v, vb) ||
       overlaps(lse, lb, out, ob))
     return SDPA_ERR_INVALID_ARG;
+  const size_t sb = (size_t)Hq * sizeof(float);
+  if (overlaps(out, ob, sinks, sb) || overlaps(lse, lb, sinks, sb)) return SDPA_ERR_INVALID_ARG;
   p.q = q;
   p.k = k;
   p.v = v;
   p.out = out;
   p.lse = lse;
+  p.sinks = sinks;
   if ((st = set_causal(&p, is_causal)) != SDPA_OK) return st;
   Family f;
   if ((st = choose(p, dtype, &f)) != SDPA_OK) return st;
@@ -247,6 +253,13 @@ extern "C" int sdpa_fwd_strided(const void* q, const void* k, const void* v, voi
   return status_of(e);
 }
 
+extern "C" int sdpa_fwd_strided(const void* q, const void* k, const void* v, void* out, float* lse,
+                                int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale,
+                                int is_causal, int dtype, const sdpa_strides_t* strides, void* stream) {
+  return sdpa_fwd_sinks(q, k, v, out, lse, nullptr, B, Hq, Hkv, Lq, Lkv, D, scale, is_causal, dtype,
+                        strides, stream);
+}
+
 extern "C" int sdpa_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
                         int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale,
                         int is_causal, int dtype, void* stream) {
@@ -263,18 +276,21 @@ extern "C" size_t sdpa_bwd_workspace_size(int B, int Hq, int Hkv, int Lq, int Lk
   return (bytes + 255) / 256 * 256;
 }
 
-extern "C" int sdpa_bwd_strided(const void* q, const void* k, const void* v, const void* out,
-                                const void* dout, const float* lse, void* dq, void* dk, void* dv,
-                                int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale,
-                                int is_causal, int dtype, const sdpa_strides_t* strides,
-                                void* workspace, size_t workspace_bytes, void* stream) {
+extern "C" int sdpa_bwd_sinks(const void* q, const void* k, const void* v, const void* out,
+                              const void* dout, const float* lse, const float* sinks, void* dq,
+                              void* dk, void* dv, float* dsinks, int B, int Hq, int Hkv, int Lq,
+                              int Lkv, int D, float scale, int is_causal, int dtype,
+                              const sdpa_strides_t* strides, void* workspace, size_t workspace_bytes,
+                              void* stream) {
   Problem p;
   int st = check_sizes(B, Hq, Hkv, Lq, Lkv, D, scale, dtype, &p);
   if (st != SDPA_OK) return st;
   if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv || !strides) return SDPA_ERR_INVALID_ARG;
+  if (dsinks && !sinks) return SDPA_ERR_INVALID_ARG;
   const void* all[] = {q, k, v, out, dout, lse, dq, dk, dv};
   for (const void* ptr : all)
     if (!aligned16(ptr)) return SDPA_ERR_INVALID_ARG;
+  if (!aligned4(sinks) || !aligned4(dsinks)) return SDPA_ERR_INVALID_ARG;
   const size_t need = sdpa_bwd_workspace_size(B, Hq, Hkv, Lq, Lkv, D, dtype);
   if (!workspace || workspace_bytes < need) return SDPA_ERR_WORKSPACE;
   if (!aligned16(workspace)) return SDPA_ERR_INVALID_ARG;
@@ -287,15 +303,15 @@ extern "C" int sdpa_bwd_strided(const void* q, const void* k, const void* v, con
       !check_layout(strides->dk, B, Hkv, Lkv, D, es, &p.ldk, &dkb) ||
       !check_layout(strides->dv, B, Hkv, Lkv, D, es, &p.ldv, &dvb))
     return SDPA_ERR_INVALID_ARG;
-  const size_t lb = (size_t)B * Hq * Lq * sizeof(float);
-  const void* ins[] = {q, k, v, out, dout, lse};
-  const size_t in_bytes[] = {qb, kb, vb, ob, dob, lb};
-  void* outs[] = {dq, dk, dv, workspace};
-  const size_t out_bytes[] = {dqb, dkb, dvb, need};
-  for (int a = 0; a < 4; ++a) {
-    for (int c = 0; c < 6; ++c)
+  const size_t lb = (size_t)B * Hq * Lq * sizeof(float), sb = (size_t)Hq * sizeof(float);
+  const void* ins[] = {q, k, v, out, dout, lse, sinks};
+  const size_t in_bytes[] = {qb, kb, vb, ob, dob, lb, sb};
+  void* outs[] = {dq, dk, dv, workspace, dsinks};
+  const size_t out_bytes[] = {dqb, dkb, dvb, need, sb};
+  for (int a = 0; a < 5; ++a) {
+    for (int c = 0; c < 7; ++c)
       if (overlaps(outs[a], out_bytes[a], ins[c], in_bytes[c])) return SDPA_ERR_INVALID_ARG;
-    for (int c = a + 1; c < 4; ++c)
+    for (int c = a + 1; c < 5; ++c)
       if (overlaps(outs[a], out_bytes[a], outs[c], out_bytes[c])) return SDPA_ERR_INVALID_ARG;
   }
   p.q = q;
@@ -308,17 +324,28 @@ extern "C" int sdpa_bwd_strided(const void* q, const void* k, const void* v, con
   p.dk = dk;
   p.dv = dv;
   p.delta = static_cast<float*>(workspace);
+  p.sinks = sinks;
+  p.dsinks = dsinks;
   if ((st = set_causal(&p, is_causal)) != SDPA_OK) return st;
   Family f;
   if ((st = choose(p, dtype, &f)) != SDPA_OK) return st;
   if ((st = error_word(&p.err)) != SDPA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  // The short-query backward computes δ inside its own kernel; the sink gradients need it
+  // in the workspace, so then the δ pre-pass runs for them.
+  if (f != Family::kVector || dsinks) {
+    e = launch_one(SDPA_KERNEL_DELTA, s, [&] { return launch_delta(p, dtype, s); });
+    if (e != cudaSuccess) return status_of(e);
+  }
+  if (dsinks) {
+    e = launch_one(SDPA_KERNEL_SINK_GRAD, s, [&] { return launch_sink_grad(p, s); });
+    if (e != cudaSuccess) return status_of(e);
+  }
   if (f == Family::kVector)
     return status_of(launch_one(SDPA_KERNEL_VEC_BWD, s, [&] {
       return vector_mma_supported(p, dtype) ? launch_vector_mma_bwd(p, dtype, s) : launch_vector_bwd(p, dtype, s);
     }));
-  cudaError_t e = launch_one(SDPA_KERNEL_DELTA, s, [&] { return launch_delta(p, dtype, s); });
-  if (e != cudaSuccess) return status_of(e);
   const bool tc = f == Family::kTensor && tensor_bwd_supported(p, dtype);
   e = launch_one(SDPA_KERNEL_DKDV, s, [&] {
     return tc ? launch_tc_dkdv(p, dtype, s) : launch_simt_dkdv(p, dtype, s);
@@ -328,6 +355,15 @@ extern "C" int sdpa_bwd_strided(const void* q, const void* k, const void* v, con
     return tc ? launch_tc_dq(p, dtype, s) : launch_simt_dq(p, dtype, s);
   });
   return status_of(e);
+}
+
+extern "C" int sdpa_bwd_strided(const void* q, const void* k, const void* v, const void* out,
+                                const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                                int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale,
+                                int is_causal, int dtype, const sdpa_strides_t* strides,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  return sdpa_bwd_sinks(q, k, v, out, dout, lse, nullptr, dq, dk, dv, nullptr, B, Hq, Hkv, Lq, Lkv, D,
+                        scale, is_causal, dtype, strides, workspace, workspace_bytes, stream);
 }
 
 extern "C" int sdpa_bwd(const void* q, const void* k, const void* v, const void* out,

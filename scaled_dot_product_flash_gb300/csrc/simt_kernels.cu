@@ -96,7 +96,8 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Problem p) {
     m = m_new;
   }
   if (!valid) return;
-  const float inv = 1.f / l;
+  const float a = fold_sink(p, h, m, l);
+  const float inv = a / l;
   T* op = row_ptr<T>(p.out, p.lo, b, h, i);
 #pragma unroll
   for (int t = 0; t < DPT; ++t) op[sub + kTpr * t] = Elem<T>::from_f(o[t] * inv);
@@ -281,6 +282,43 @@ __global__ void __launch_bounds__(kDeltaThreads) delta_kernel(Problem p) {
   if (i < p.Lq && sub == 0) p.delta[q_row(p, b, h, i)] = acc;
 }
 
+// Gradient of each query head's sink logit.  The sink is one more entry of every row's
+// softmax with a zero value vector, so its dP entry is zero and its dS entry is
+// −p_sink·δ with p_sink = exp(sink − lse) (lse includes the sink).  Summed over the batch
+// and the rows: dsink_h = −Σ_{b,i} exp(sink_h − lse_bhi)·δ_bhi.  One block per head; the
+// rows are split over the threads in a fixed order and reduced by a fixed tree, so the
+// result is the same bits on every run.
+constexpr int kSinkThreads = 256;
+
+__global__ void __launch_bounds__(kSinkThreads) sink_grad_kernel(Problem p) {
+  const int h = blockIdx.x;
+  const float sk = p.sinks[h];
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int b = 0; b < p.B; ++b) {
+    const float* lse = p.lse + q_row(p, b, h, 0);
+    const float* dl = p.delta + q_row(p, b, h, 0);
+    int i = threadIdx.x;
+    for (; i + 3 * kSinkThreads < p.Lq; i += 4 * kSinkThreads) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        acc[u] = fmaf(expf(sk - lse[i + u * kSinkThreads]), dl[i + u * kSinkThreads], acc[u]);
+    }
+    for (; i < p.Lq; i += kSinkThreads) acc[0] = fmaf(expf(sk - lse[i]), dl[i], acc[0]);
+  }
+  float t = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+  __shared__ float part[kSinkThreads / 32];
+  if (threadIdx.x % 32 == 0) part[threadIdx.x / 32] = t;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kSinkThreads / 32; ++w) sum += part[w];
+    p.dsinks[h] = -sum;
+  }
+}
+
 template <typename T, int D>
 cudaError_t simt_fwd_t(const Problem& p, cudaStream_t s) {
   dim3 grid((p.Lq + kRows - 1) / kRows, p.Hq, p.B);
@@ -352,5 +390,10 @@ cudaError_t launch_simt_fwd(const Problem& p, int dtype, cudaStream_t s) { retur
 cudaError_t launch_simt_dq(const Problem& p, int dtype, cudaStream_t s) { return simt_dq_any(p, dtype, s); }
 cudaError_t launch_simt_dkdv(const Problem& p, int dtype, cudaStream_t s) { return simt_dkdv_any(p, dtype, s); }
 cudaError_t launch_delta(const Problem& p, int dtype, cudaStream_t s) { return delta_any(p, dtype, s); }
+
+cudaError_t launch_sink_grad(const Problem& p, cudaStream_t s) {
+  sink_grad_kernel<<<p.Hq, kSinkThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
 
 }  // namespace sdpa

@@ -428,7 +428,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* stage = sm + L::kQOff + w * L::kTileBytes;
       if (ok) {
         tc_fence_after();
-        const float inv = 1.f / l;
+        const float a = fold_sink(p, h, m, l);
+        const float inv = a / l;
 #pragma unroll
         for (int c32 = 0; c32 < D / 32; ++c32) {
           uint32_t orr[32];

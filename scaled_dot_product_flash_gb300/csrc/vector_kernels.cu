@@ -193,7 +193,8 @@ __global__ void __launch_bounds__(kThreads) vec_fwd_kernel(Problem p, int chunk)
     }
     const int hh2 = r2 / p.Lq, i2 = r2 % p.Lq;
     const int64_t row = q_row(p, b, g * p.G + hh2, i2);
-    row_ptr<T>(p.out, p.lo, b, g * p.G + hh2, i2)[d] = Elem<T>::from_f(O / L);
+    const float a = fold_sink(p, g * p.G + hh2, M, L);
+    row_ptr<T>(p.out, p.lo, b, g * p.G + hh2, i2)[d] = Elem<T>::from_f(O * a / L);
     if (p.lse && d == 0) p.lse[row] = (M + log2f(L)) * kLn2;
   }
   cluster.sync();  // peers may still be reading this block's shared memory

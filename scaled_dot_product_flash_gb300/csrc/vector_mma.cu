@@ -331,7 +331,8 @@ __global__ void __launch_bounds__(128) vec_mma_fwd_kernel(const __grid_constant_
       O = fmaf(cluster.map_shared_rank(cta_o, cc)[r * D + d], wgt, O);
     }
     const int64_t row = q_row(p, b, g * p.G + r / p.Lq, r % p.Lq);
-    row_ptr<T>(p.out, p.lo, b, g * p.G + r / p.Lq, r % p.Lq)[d] = Elem<T>::from_f(O / Lsum);
+    const float a = fold_sink(p, g * p.G + r / p.Lq, M, Lsum);
+    row_ptr<T>(p.out, p.lo, b, g * p.G + r / p.Lq, r % p.Lq)[d] = Elem<T>::from_f(O * a / Lsum);
     if (p.lse && d == 0) p.lse[row] = (M + __log2f(Lsum)) * kLn2;
   }
   cluster.sync();  // peers may still be reading this block's shared memory

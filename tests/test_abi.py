@@ -166,3 +166,46 @@ def test_strided_null_strides_rejected(lib):
     a = GOOD
     assert lib.sdpa_fwd_strided(Q, K, V, O, L, a["B"], a["Hq"], a["Hkv"], a["Lq"], a["Lkv"],
                                 a["D"], a["scale"], a["causal"], a["dtype"], None, None) == INVALID
+
+
+# ---- sink entry points: every case below is rejected before anything is launched.
+SK, DSK = 0x10000000 * 11, 0x10000000 * 12
+
+
+def _all_cont():
+    a = GOOD
+    q = _cont(a["Hq"], a["Lq"], a["D"])
+    k = _cont(a["Hkv"], a["Lkv"], a["D"])
+    return _lib.make_strides(q=q, k=k, v=k, o=q, dout=q, dq=q, dk=k, dv=k)
+
+
+def fwd_sinks(sinks):
+    a = GOOD
+    return _lib.sdpa_fwd_sinks(Q, K, V, O, L, sinks, a["B"], a["Hq"], a["Hkv"], a["Lq"],
+                               a["Lkv"], a["D"], a["scale"], a["causal"], a["dtype"], _all_cont(),
+                               None)
+
+
+def bwd_sinks(sinks, dsinks):
+    a = GOOD
+    return _lib.sdpa_bwd_sinks(Q, K, V, O, DO, L, sinks, DQ, DK, DV, dsinks, a["B"], a["Hq"],
+                               a["Hkv"], a["Lq"], a["Lkv"], a["D"], a["scale"], a["causal"],
+                               a["dtype"], _all_cont(), WS, 1 << 20, None)
+
+
+@pytest.mark.parametrize("sinks", [SK + 2, O + 64, L + 4])   # misaligned, in out, in lse
+def test_forward_sinks_rejects(lib, sinks):
+    assert fwd_sinks(sinks) == INVALID
+
+
+@pytest.mark.parametrize("sinks,dsinks", [
+    (None, DSK),          # a sink gradient without sinks
+    (SK, DSK + 1),        # misaligned
+    (SK, DQ + 16),        # dsinks inside dq
+    (SK, SK),             # dsinks aliases sinks
+    (SK, L + 8),          # dsinks inside lse
+    (SK + 2, DSK),        # misaligned sinks
+    (WS + 4, DSK),        # sinks inside the workspace
+])
+def test_backward_sinks_rejects(lib, sinks, dsinks):
+    assert bwd_sinks(sinks, dsinks) == INVALID
