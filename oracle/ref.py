@@ -38,6 +38,12 @@ Readings of points the pages leave open (each also listed in the design notes):
   and a zero value vector, so it enlarges the row sum and the logsumexp but adds nothing
   to O.  The backward is the same chain rule; the sink's own gradient is
   -sum_i p_sink,i · delta_i (its dP entry is zero because its value is zero).
+* Attention masks (optional): an array broadcastable to [B, Hq, Lq, Lkv], indexed by the
+  query head.  A boolean mask keeps key j for query i where it is True (the convention of
+  ``F.scaled_dot_product_attention``'s ``attn_mask``); a float mask is added to
+  scale·q·k before the softmax (−inf hides the key).  It combines with the causal mask.
+  A row that sees no key at all (possible only with such a mask) has O = 0,
+  lse = −inf and zero gradients (with a sink, the sink alone fills the row's softmax).
 * The oracle does not clamp exponent arguments (the clamp mentioned in [MLX-VJP]
   "Implementation Notes" only guards the GPU's exp2 against overflow; after the row
   maximum is subtracted every argument is <= 0 already).
@@ -84,14 +90,25 @@ def _causal_offset(is_causal, lq, lkv):
     return 0
 
 
-def _scores(q_rows, k, scale, offset, row_idx):
+def _mask_values(mask):
+    """A mask as additive fp64 values: boolean True -> 0, False -> -inf; floats as they are."""
+    mask = np.asarray(mask)
+    if mask.dtype == np.bool_:
+        return np.where(mask, 0.0, -np.inf)
+    return mask.astype(np.float64)
+
+
+def _scores(q_rows, k, scale, offset, row_idx, mask_rows=None):
     """Scores of a block of query rows against all keys, masked.
 
-    [PyTensor-SDPA] "Proposed change": scores = (q @ kᵀ) * scale.
-    Causal ([mps-flash-sdpa] "Quick Start" ``is_causal``): the score of key j for absolute
-    query row i = row_idx[r] is -inf when j > i + offset (offset None: no mask).
+    [PyTensor-SDPA] "Proposed change": scores = (q @ kᵀ) * scale.  ``mask_rows`` (the
+    additive mask of these rows, or None) is added.  Causal ([mps-flash-sdpa] "Quick
+    Start" ``is_causal``): the score of key j for absolute query row i = row_idx[r] is
+    -inf when j > i + offset (offset None: no causal mask).
     """
     s = (q_rows @ k.T) * scale
+    if mask_rows is not None:
+        s = s + mask_rows
     if offset is not None:
         j = np.arange(k.shape[0])[None, :]
         s = np.where(j > np.asarray(row_idx)[:, None] + offset, -np.inf, s)
@@ -105,17 +122,20 @@ def _softmax_rows(s, sink=None):
     the row ([MPS-SDPA] "Problem - Unused second output tensor") is max + log(sum).
     With a sink logit, the row is the scores plus one more entry equal to the sink; the
     returned P leaves that entry out, and p_sink (one per row) is returned as well.
+    A row with no finite entry (every key hidden, no sink) gets P = 0 and lse = -inf.
     """
     m = s.max(axis=1, keepdims=True)
     if sink is not None:
         m = np.maximum(m, sink)
+    m = np.where(np.isfinite(m), m, 0.0)  # rows with nothing visible: any finite shift
     e = np.exp(s - m)
     l = e.sum(axis=1, keepdims=True)
     if sink is not None:
         es = np.exp(sink - m)
         l = l + es
-    p = e / l
-    lse = (m + np.log(l))[:, 0]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        p = np.where(l > 0, e / l, 0.0)
+        lse = (m + np.log(l))[:, 0]
     if sink is not None:
         return p, lse, (es / l)[:, 0]
     return p, lse
@@ -127,26 +147,30 @@ def _blocks(n, row_block):
         yield r0, min(n, r0 + step)
 
 
-def head_forward(q, k, v, scale, is_causal, rows=None, row_block=None, sink=None):
-    """Forward of one head: O = softmax(scale·q kᵀ [+ causal mask]) v and its logsumexp.
+def head_forward(q, k, v, scale, is_causal, rows=None, row_block=None, sink=None, mask=None):
+    """Forward of one head: O = softmax(scale·q kᵀ [+ masks]) v and its logsumexp.
 
     q: [Lq, D], k, v: [Lkv, D].  ``rows`` (optional, sorted or not) selects which query
     rows to compute; by default all.  ``sink``: this head's sink logit, or None.
+    ``mask``: this head's [Lq, Lkv] mask (boolean or additive), or None.
     Returns (O [n, D], lse [n]) in float64.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
+    if mask is not None:
+        mask = np.broadcast_to(_mask_values(mask), (q.shape[0], k.shape[0]))
     off = _causal_offset(is_causal, q.shape[0], k.shape[0])
     idx = np.arange(q.shape[0]) if rows is None else np.asarray(rows, dtype=np.int64)
     o = np.empty((idx.size, v.shape[1]))
     lse = np.empty(idx.size)
     for a, b in _blocks(idx.size, row_block):
         sel = idx[a:b]
-        p, lse[a:b] = _softmax_rows(_scores(q[sel], k, scale, off, sel), sink)[:2]
+        mrows = None if mask is None else mask[sel]
+        p, lse[a:b] = _softmax_rows(_scores(q[sel], k, scale, off, sel, mrows), sink)[:2]
         o[a:b] = p @ v
     return o, lse
 
 
-def head_backward(q, k, v, dout, scale, is_causal, row_block=None, sink=None):
+def head_backward(q, k, v, dout, scale, is_causal, row_block=None, sink=None, mask=None):
     """Backward of one head (textbook VJP).  Returns (dq, dk_part, dv_part) in float64.
 
     Steps, per [MLX-VJP]'s description (recompute S, P = exp(S - LSE), then gradients)
@@ -161,16 +185,19 @@ def head_backward(q, k, v, dout, scale, is_causal, row_block=None, sink=None):
         dK  = scale · dSᵀ q
     dk_part and dv_part are this head's contribution to its KV head; the caller sums
     them over the query heads of the group.  With a sink logit, a fourth value is
-    returned: the sink's gradient, -sum_i p_sink,i · δ_i.
+    returned: the sink's gradient, -sum_i p_sink,i · δ_i.  ``mask``: as in head_forward.
     """
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    if mask is not None:
+        mask = np.broadcast_to(_mask_values(mask), (q.shape[0], k.shape[0]))
     off = _causal_offset(is_causal, q.shape[0], k.shape[0])
     dq = np.empty_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
     dsink = 0.0
     for a, b in _blocks(q.shape[0], row_block):
-        sm = _softmax_rows(_scores(q[a:b], k, scale, off, np.arange(a, b)), sink)
+        mrows = None if mask is None else mask[a:b]
+        sm = _softmax_rows(_scores(q[a:b], k, scale, off, np.arange(a, b), mrows), sink)
         p = sm[0]
         o = p @ v
         dv += p.T @ dout[a:b]
@@ -198,13 +225,22 @@ def _check(q, k, v):
     return B, Hq, Hkv, Hq // Hkv
 
 
-def sdpa_forward(q, k, v, scale, is_causal, row_block=None, sinks=None):
+def _full_mask(mask, q, k):
+    """The mask broadcast (without copying) to [B, Hq, Lq, Lkv], or None."""
+    if mask is None:
+        return None
+    return np.broadcast_to(_mask_values(mask), q.shape[:3] + (k.shape[2],))
+
+
+def sdpa_forward(q, k, v, scale, is_causal, row_block=None, sinks=None, mask=None):
     """Forward over [B, H, L, D] arrays with GQA ([MLX-VJP] "Key Features").
 
     Query head h reads KV head h // G with G = Hq // Hkv; ``sinks`` ([Hq] or None) adds
-    one sink logit per query head.  Returns (O [B,Hq,Lq,D], lse [B,Hq,Lq]) in float64.
+    one sink logit per query head; ``mask`` (broadcastable to [B, Hq, Lq, Lkv], boolean
+    or additive, or None) masks scores.  Returns (O [B,Hq,Lq,D], lse [B,Hq,Lq]) in float64.
     """
     B, Hq, Hkv, G = _check(q, k, v)
+    mask = _full_mask(mask, q, k)
     o = np.empty(q.shape[:3] + (v.shape[3],))
     lse = np.empty(q.shape[:3])
     for b in range(B):
@@ -212,11 +248,13 @@ def sdpa_forward(q, k, v, scale, is_causal, row_block=None, sinks=None):
             g = h // G
             o[b, h], lse[b, h] = head_forward(q[b, h], k[b, g], v[b, g], scale,
                                               is_causal, row_block=row_block,
-                                              sink=None if sinks is None else float(sinks[h]))
+                                              sink=None if sinks is None else float(sinks[h]),
+                                              mask=None if mask is None else mask[b, h])
     return o, lse
 
 
-def group_backward(q, k, v, dout, scale, is_causal, b, g, row_block=None, sinks=None):
+def group_backward(q, k, v, dout, scale, is_causal, b, g, row_block=None, sinks=None,
+                   mask=None):
     """Backward for KV head g of batch b: dQ of its G query heads, and dK, dV of g.
 
     dK and dV sum the contributions of every query head that reads KV head g
@@ -225,6 +263,7 @@ def group_backward(q, k, v, dout, scale, is_causal, b, g, row_block=None, sinks=
     gradients of the group's G sink logits (batch b only).
     """
     B, Hq, Hkv, G = _check(q, k, v)
+    mask = _full_mask(mask, q, k)
     dq = np.empty((G,) + q.shape[2:])
     dk = np.zeros(k.shape[2:])
     dv = np.zeros(v.shape[2:])
@@ -232,7 +271,8 @@ def group_backward(q, k, v, dout, scale, is_causal, b, g, row_block=None, sinks=
     for t in range(G):
         h = g * G + t
         r = head_backward(q[b, h], k[b, g], v[b, g], dout[b, h], scale, is_causal,
-                          row_block=row_block, sink=None if sinks is None else float(sinks[h]))
+                          row_block=row_block, sink=None if sinks is None else float(sinks[h]),
+                          mask=None if mask is None else mask[b, h])
         dq[t], dk_h, dv_h = r[:3]
         if sinks is not None:
             dsink[t] = r[3]
@@ -243,10 +283,12 @@ def group_backward(q, k, v, dout, scale, is_causal, b, g, row_block=None, sinks=
     return dq, dk, dv
 
 
-def sdpa_backward(q, k, v, dout, scale, is_causal, row_block=None, sinks=None):
+def sdpa_backward(q, k, v, dout, scale, is_causal, row_block=None, sinks=None, mask=None):
     """Backward over [B, H, L, D] arrays.  Returns (dq, dk, dv) in float64, and with
-    ``sinks`` ([Hq]) also dsinks [Hq], each summed over the batch."""
+    ``sinks`` ([Hq]) also dsinks [Hq], each summed over the batch.  ``mask``: as in
+    sdpa_forward."""
     B, Hq, Hkv, G = _check(q, k, v)
+    mask = _full_mask(mask, q, k)
     dq = np.empty(q.shape, dtype=np.float64)
     dk = np.empty(k.shape, dtype=np.float64)
     dv = np.empty(v.shape, dtype=np.float64)
@@ -254,7 +296,7 @@ def sdpa_backward(q, k, v, dout, scale, is_causal, row_block=None, sinks=None):
     for b in range(B):
         for g in range(Hkv):
             r = group_backward(q, k, v, dout, scale, is_causal, b, g, row_block=row_block,
-                               sinks=sinks)
+                               sinks=sinks, mask=mask)
             dq[b, g * G:(g + 1) * G], dk[b, g], dv[b, g] = r[:3]
             if sinks is not None:
                 dsinks[g * G:(g + 1) * G] += r[3]

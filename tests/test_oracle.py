@@ -466,6 +466,186 @@ def _sink_fd_all(impl):
         test_sink_gradients_match_finite_differences(c, impl)
 
 
+# ----------------------------------------------------------------- attention masks
+def test_zero_and_all_true_masks_are_no_mask(impl=None):
+    impl = impl or oracle
+    rng = np.random.default_rng(61)
+    q, k, v, do = make(rng, B=2, Hq=4, Hkv=2, Lq=5, Lkv=7, D=3)
+    want_f = impl.sdpa_forward(q, k, v, 0.6, True)
+    want_b = impl.sdpa_backward(q, k, v, do, 0.6, True)
+    for mask in (np.zeros((5, 7)), np.ones((2, 4, 5, 7), dtype=bool)):
+        for a, b in zip(impl.sdpa_forward(q, k, v, 0.6, True, mask=mask), want_f):
+            np.testing.assert_allclose(a, b, atol=1e-14)
+        for a, b in zip(impl.sdpa_backward(q, k, v, do, 0.6, True, mask=mask), want_b):
+            np.testing.assert_allclose(a, b, atol=1e-14)
+
+
+def test_lower_triangular_bool_mask_is_the_causal_flag(impl=None):
+    """A boolean mask that keeps key j for query i iff j <= i + c is the causal mask with
+    offset c (c = 0 top-left, Lkv - Lq bottom-right)."""
+    impl = impl or oracle
+    rng = np.random.default_rng(62)
+    q, k, v, do = make(rng, B=1, Hq=2, Hkv=1, Lq=4, Lkv=7, D=3)
+    for flag, c in ((True, 0), (2, 3)):
+        mask = np.tril(np.ones((4, 7), dtype=bool), k=c)
+        for a, b in zip(impl.sdpa_forward(q, k, v, 0.8, False, mask=mask),
+                        impl.sdpa_forward(q, k, v, 0.8, flag)):
+            np.testing.assert_allclose(a, b, atol=1e-14)
+        for a, b in zip(impl.sdpa_backward(q, k, v, do, 0.8, False, mask=mask),
+                        impl.sdpa_backward(q, k, v, do, 0.8, flag)):
+            np.testing.assert_allclose(a, b, atol=1e-14)
+
+
+def test_key_padding_mask_equals_truncated_keys(impl=None):
+    """A [B, 1, 1, Lkv] boolean mask hiding keys n_b.. of batch b is the problem with K and V
+    cut to their first n_b rows; the hidden keys get zero dK and dV."""
+    impl = impl or oracle
+    rng = np.random.default_rng(63)
+    q, k, v, do = make(rng, B=2, Hq=4, Hkv=2, Lq=5, Lkv=8, D=3)
+    ns = (3, 8)
+    mask = np.zeros((2, 1, 1, 8), dtype=bool)
+    for b, n in enumerate(ns):
+        mask[b, :, :, :n] = True
+    o, lse = impl.sdpa_forward(q, k, v, 0.7, False, mask=mask)
+    dq, dk, dv = impl.sdpa_backward(q, k, v, do, 0.7, False, mask=mask)
+    for b, n in enumerate(ns):
+        sl = slice(b, b + 1)
+        ot, lt = impl.sdpa_forward(q[sl], k[sl, :, :n], v[sl, :, :n], 0.7, False)
+        np.testing.assert_allclose(o[sl], ot, atol=1e-13)
+        np.testing.assert_allclose(lse[sl], lt, atol=1e-13)
+        gq, gk, gv = impl.sdpa_backward(q[sl], k[sl, :, :n], v[sl, :, :n], do[sl], 0.7, False)
+        np.testing.assert_allclose(dq[sl], gq, atol=1e-12)
+        np.testing.assert_allclose(dk[sl, :, :n], gk, atol=1e-12)
+        np.testing.assert_allclose(dv[sl, :, :n], gv, atol=1e-12)
+        np.testing.assert_array_equal(dk[sl, :, n:], 0.0)
+        np.testing.assert_array_equal(dv[sl, :, n:], 0.0)
+
+
+def test_log_two_mask_equals_a_duplicated_key(impl=None):
+    """Adding ln 2 to the score of key j gives it the weight of two copies of itself: the
+    problem with key j (and its value) duplicated.  dQ is the same; key j's dK and dV are the
+    sums over the two copies."""
+    impl = impl or oracle
+    rng = np.random.default_rng(64)
+    q, k, v, do = make(rng, B=1, Hq=2, Hkv=1, Lq=5, Lkv=6, D=3)
+    j = 2
+    mask = np.zeros((5, 6))
+    mask[:, j] = np.log(2.0)
+    kd = np.concatenate([k, k[:, :, j:j + 1]], axis=2)
+    vd = np.concatenate([v, v[:, :, j:j + 1]], axis=2)
+    for a, b in zip(impl.sdpa_forward(q, k, v, 0.9, False, mask=mask),
+                    impl.sdpa_forward(q, kd, vd, 0.9, False)):
+        np.testing.assert_allclose(a, b, atol=1e-13)
+    dq, dk, dv = impl.sdpa_backward(q, k, v, do, 0.9, False, mask=mask)
+    gq, gk, gv = impl.sdpa_backward(q, kd, vd, do, 0.9, False)
+    np.testing.assert_allclose(dq, gq, atol=1e-12)
+    gk[:, :, j] += gk[:, :, 6]
+    gv[:, :, j] += gv[:, :, 6]
+    np.testing.assert_allclose(dk, gk[:, :, :6], atol=1e-12)
+    np.testing.assert_allclose(dv, gv[:, :, :6], atol=1e-12)
+
+
+def test_row_constant_mask_shifts_only_the_logsumexp(impl=None):
+    """Softmax is invariant to a per-row constant: a mask c_i on every key of row i leaves O
+    and every gradient unchanged and adds c_i to lse_i."""
+    impl = impl or oracle
+    rng = np.random.default_rng(65)
+    q, k, v, do = make(rng, B=1, Hq=2, Hkv=1, Lq=5, Lkv=6, D=3)
+    c = rng.standard_normal((1, 2, 5, 1)) * 3.0
+    mask = np.broadcast_to(c, (1, 2, 5, 6))
+    o, lse = impl.sdpa_forward(q, k, v, 0.9, True, mask=mask)
+    o0, lse0 = impl.sdpa_forward(q, k, v, 0.9, True)
+    np.testing.assert_allclose(o, o0, atol=1e-13)
+    np.testing.assert_allclose(lse, lse0 + c[..., 0], atol=1e-13)
+    for a, b in zip(impl.sdpa_backward(q, k, v, do, 0.9, True, mask=mask),
+                    impl.sdpa_backward(q, k, v, do, 0.9, True)):
+        np.testing.assert_allclose(a, b, atol=1e-12)
+
+
+def test_per_query_head_masks_under_gqa(impl=None):
+    """The mask is indexed by the query head: with GQA, each query head with its own mask
+    equals that head run alone against its KV head."""
+    impl = impl or oracle
+    rng = np.random.default_rng(66)
+    q, k, v, do = make(rng, B=1, Hq=4, Hkv=2, Lq=5, Lkv=6, D=3)
+    mask = rng.standard_normal((1, 4, 5, 6))
+    o, lse = impl.sdpa_forward(q, k, v, 0.8, False, mask=mask)
+    dq, _, _ = impl.sdpa_backward(q, k, v, do, 0.8, False, mask=mask)
+    for h in range(4):
+        g = h // 2
+        oh, lh = impl.sdpa_forward(q[:, h:h + 1], k[:, g:g + 1], v[:, g:g + 1], 0.8, False,
+                                   mask=mask[:, h:h + 1])
+        np.testing.assert_allclose(o[:, h:h + 1], oh, atol=1e-13)
+        np.testing.assert_allclose(lse[:, h:h + 1], lh, atol=1e-13)
+        gq, _, _ = impl.sdpa_backward(q[:, h:h + 1], k[:, g:g + 1], v[:, g:g + 1],
+                                      do[:, h:h + 1], 0.8, False, mask=mask[:, h:h + 1])
+        np.testing.assert_allclose(dq[:, h:h + 1], gq, atol=1e-12)
+
+
+def test_fully_masked_row(impl=None):
+    """A row that sees no key (reading: O = 0, lse = -inf, zero gradients) leaves the other
+    rows, and dK and dV, as in the problem without that row; with a sink the sink alone
+    fills the row: O = 0 and lse = the sink."""
+    impl = impl or oracle
+    rng = np.random.default_rng(67)
+    q, k, v, do = make(rng, B=1, Hq=2, Hkv=1, Lq=5, Lkv=6, D=3)
+    mask = np.ones((5, 6), dtype=bool)
+    mask[3] = False
+    keep = [0, 1, 2, 4]
+    with np.errstate(all="raise"):
+        o, lse = impl.sdpa_forward(q, k, v, 0.7, False, mask=mask)
+        dq, dk, dv = impl.sdpa_backward(q, k, v, do, 0.7, False, mask=mask)
+    np.testing.assert_array_equal(o[:, :, 3], 0.0)
+    assert np.all(lse[:, :, 3] == -np.inf)
+    np.testing.assert_array_equal(dq[:, :, 3], 0.0)
+    o4, l4 = impl.sdpa_forward(q[:, :, keep], k, v, 0.7, False)
+    np.testing.assert_allclose(o[:, :, keep], o4, atol=1e-13)
+    np.testing.assert_allclose(lse[:, :, keep], l4, atol=1e-13)
+    g4 = impl.sdpa_backward(q[:, :, keep], k, v, do[:, :, keep], 0.7, False)
+    np.testing.assert_allclose(dq[:, :, keep], g4[0], atol=1e-12)
+    np.testing.assert_allclose(dk, g4[1], atol=1e-12)
+    np.testing.assert_allclose(dv, g4[2], atol=1e-12)
+    sinks = np.array([0.5, -1.0])
+    o, lse = impl.sdpa_forward(q, k, v, 0.7, False, mask=mask, sinks=sinks)
+    np.testing.assert_array_equal(o[:, :, 3], 0.0)
+    np.testing.assert_allclose(lse[0, :, 3], sinks, atol=1e-15)
+
+
+MASK_FD_CASES = [
+    dict(B=1, Hq=2, Hkv=1, Lq=5, Lkv=6, D=3, causal=False),
+    dict(B=2, Hq=4, Hkv=2, Lq=4, Lkv=7, D=2, causal=True),
+    dict(B=1, Hq=2, Hkv=2, Lq=3, Lkv=6, D=3, causal=2),
+]
+
+
+@pytest.mark.parametrize("case", MASK_FD_CASES,
+                         ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
+def test_masked_gradients_match_finite_differences(case, impl=None):
+    """A random additive mask with some hidden keys (key 0 stays visible to every row)."""
+    impl = impl or oracle
+    rng = np.random.default_rng(68)
+    c = dict(case)
+    causal = c.pop("causal")
+    q, k, v, do = make(rng, **c)
+    mask = rng.standard_normal((c["B"], c["Hq"], c["Lq"], c["Lkv"]))
+    mask[rng.random(mask.shape) < 0.3] = -np.inf
+    mask[..., 0] = 0.0
+    scale = 0.7
+
+    def f():
+        o, _ = impl.sdpa_forward(q, k, v, scale, causal, mask=mask)
+        return float((o * do).sum())
+    dq, dk, dv = impl.sdpa_backward(q, k, v, do, scale, causal, mask=mask)
+    np.testing.assert_allclose(dq, _fd_grad(q, f), atol=1e-7, rtol=1e-6)
+    np.testing.assert_allclose(dk, _fd_grad(k, f), atol=1e-7, rtol=1e-6)
+    np.testing.assert_allclose(dv, _fd_grad(v, f), atol=1e-7, rtol=1e-6)
+
+
+def _mask_fd_all(impl):
+    for c in MASK_FD_CASES:
+        test_masked_gradients_match_finite_differences(c, impl)
+
+
 # ----------------------------------------------------------------- pins have teeth
 PINS = [
     test_rows_of_p_sum_to_one,
@@ -483,6 +663,14 @@ PINS = [
     test_sink_single_key_closed_form,
     test_sink_is_an_extra_key_with_zero_value,
     _sink_fd_all,
+    test_zero_and_all_true_masks_are_no_mask,
+    test_lower_triangular_bool_mask_is_the_causal_flag,
+    test_key_padding_mask_equals_truncated_keys,
+    test_log_two_mask_equals_a_duplicated_key,
+    test_row_constant_mask_shifts_only_the_logsumexp,
+    test_per_query_head_masks_under_gqa,
+    test_fully_masked_row,
+    _mask_fd_all,
 ]
 
 
@@ -495,8 +683,10 @@ def _mutant(name):
     if name in ("causal_diag_masked", "causal_off_by_one"):
         shift = 0 if name == "causal_diag_masked" else 2
 
-        def _scores(q_rows, k, scale, offset, row_idx):
+        def _scores(q_rows, k, scale, offset, row_idx, mask_rows=None):
             s = (q_rows @ k.T) * scale
+            if mask_rows is not None:
+                s = s + mask_rows
             if offset is not None:
                 j = np.arange(k.shape[0])[None, :]
                 s = np.where(j >= np.asarray(row_idx)[:, None] + offset + shift, -np.inf, s)
@@ -517,8 +707,9 @@ def _mutant(name):
             return (r[0], r[1] / math.log(2.0)) + tuple(r[2:])
         m._softmax_rows = _softmax_rows
     elif name == "gqa_modulo":
-        def sdpa_forward(q, k, v, scale, is_causal, row_block=None, sinks=None):
+        def sdpa_forward(q, k, v, scale, is_causal, row_block=None, sinks=None, mask=None):
             B, Hq, Hkv, G = m._check(q, k, v)
+            mask = m._full_mask(mask, q, k)
             o = np.empty(q.shape[:3] + (v.shape[3],))
             lse = np.empty(q.shape[:3])
             for b in range(B):
@@ -526,21 +717,23 @@ def _mutant(name):
                     g = h % Hkv
                     o[b, h], lse[b, h] = m.head_forward(
                         q[b, h], k[b, g], v[b, g], scale, is_causal,
-                        sink=None if sinks is None else float(sinks[h]))
+                        sink=None if sinks is None else float(sinks[h]),
+                        mask=None if mask is None else mask[b, h])
             return o, lse
         m.sdpa_forward = sdpa_forward
     elif name == "no_scale_in_dq":
         orig = m.head_backward
 
-        def head_backward(q, k, v, dout, scale, is_causal, row_block=None, sink=None):
-            r = orig(q, k, v, dout, scale, is_causal, row_block, sink)
+        def head_backward(q, k, v, dout, scale, is_causal, row_block=None, sink=None, mask=None):
+            r = orig(q, k, v, dout, scale, is_causal, row_block, sink, mask)
             return ((r[0] / scale if scale else r[0]),) + tuple(r[1:])
         m.head_backward = head_backward
     elif name == "delta_dropped":
-        def head_backward(q, k, v, dout, scale, is_causal, row_block=None, sink=None):
+        def head_backward(q, k, v, dout, scale, is_causal, row_block=None, sink=None, mask=None):
             q, k, v, dout = (np.asarray(x, float) for x in (q, k, v, dout))
             off = m._causal_offset(is_causal, q.shape[0], k.shape[0])
-            sm = m._softmax_rows(m._scores(q, k, scale, off, np.arange(q.shape[0])), sink)
+            mv = None if mask is None else np.broadcast_to(m._mask_values(mask), (q.shape[0], k.shape[0]))
+            sm = m._softmax_rows(m._scores(q, k, scale, off, np.arange(q.shape[0]), mv), sink)
             p = sm[0]
             ds = p * (dout @ v.T)
             r = (scale * ds @ k, scale * ds.T @ q, p.T @ dout)
@@ -549,8 +742,8 @@ def _mutant(name):
     elif name == "dk_transposed_operand":
         orig = m.head_backward
 
-        def head_backward(q, k, v, dout, scale, is_causal, row_block=None, sink=None):
-            r = orig(q, k, v, dout, scale, is_causal, row_block, sink)
+        def head_backward(q, k, v, dout, scale, is_causal, row_block=None, sink=None, mask=None):
+            r = orig(q, k, v, dout, scale, is_causal, row_block, sink, mask)
             return (r[0], r[1][::-1].copy()) + tuple(r[2:])
         m.head_backward = head_backward
     elif name == "sink_missing_from_lse":
@@ -563,19 +756,66 @@ def _mutant(name):
     elif name == "sink_gradient_sign":
         orig = m.head_backward
 
-        def head_backward(q, k, v, dout, scale, is_causal, row_block=None, sink=None):
-            r = orig(q, k, v, dout, scale, is_causal, row_block, sink)
+        def head_backward(q, k, v, dout, scale, is_causal, row_block=None, sink=None, mask=None):
+            r = orig(q, k, v, dout, scale, is_causal, row_block, sink, mask)
             return r if sink is None else r[:3] + (-r[3],)
         m.head_backward = head_backward
     elif name == "sink_given_a_value":
         orig = m.head_forward
 
-        def head_forward(q, k, v, scale, is_causal, rows=None, row_block=None, sink=None):
-            o, lse = orig(q, k, v, scale, is_causal, rows, row_block, sink)
+        def head_forward(q, k, v, scale, is_causal, rows=None, row_block=None, sink=None, mask=None):
+            o, lse = orig(q, k, v, scale, is_causal, rows, row_block, sink, mask)
             if sink is not None:
                 o = o + np.exp(sink - lse)[:, None] * np.asarray(v, float)[0][None, :]
             return o, lse
         m.head_forward = head_forward
+    elif name == "mask_scaled":
+        def _scores(q_rows, k, scale, offset, row_idx, mask_rows=None):
+            s = q_rows @ k.T
+            if mask_rows is not None:
+                s = s + mask_rows
+            s = s * scale
+            if offset is not None:
+                j = np.arange(k.shape[0])[None, :]
+                s = np.where(j > np.asarray(row_idx)[:, None] + offset, -np.inf, s)
+            return s
+        m._scores = _scores
+    elif name == "bool_mask_inverted":
+        def _mask_values(mask):
+            mask = np.asarray(mask)
+            if mask.dtype == np.bool_:
+                return np.where(mask, -np.inf, 0.0)
+            return mask.astype(np.float64)
+        m._mask_values = _mask_values
+    elif name == "mask_by_kv_head":
+        def sdpa_forward(q, k, v, scale, is_causal, row_block=None, sinks=None, mask=None):
+            B, Hq, Hkv, G = m._check(q, k, v)
+            mask = m._full_mask(mask, q, k)
+            o = np.empty(q.shape[:3] + (v.shape[3],))
+            lse = np.empty(q.shape[:3])
+            for b in range(B):
+                for h in range(Hq):
+                    g = h // G
+                    o[b, h], lse[b, h] = m.head_forward(
+                        q[b, h], k[b, g], v[b, g], scale, is_causal,
+                        sink=None if sinks is None else float(sinks[h]),
+                        mask=None if mask is None else mask[b, g])
+            return o, lse
+        m.sdpa_forward = sdpa_forward
+    elif name == "masked_row_nan":
+        def _softmax_rows(s, sink=None):
+            mx = s.max(axis=1, keepdims=True)
+            if sink is not None:
+                mx = np.maximum(mx, sink)
+            e = np.exp(s - mx)
+            l = e.sum(axis=1, keepdims=True)
+            if sink is not None:
+                es = np.exp(sink - mx)
+                l = l + es
+            p = e / l
+            lse = (mx + np.log(l))[:, 0]
+            return (p, lse, (es / l)[:, 0]) if sink is not None else (p, lse)
+        m._softmax_rows = _softmax_rows
     else:
         raise KeyError(name)
     return m
@@ -584,7 +824,8 @@ def _mutant(name):
 @pytest.mark.parametrize("name", ["causal_diag_masked", "causal_off_by_one", "lse_log2", "gqa_modulo",
                                   "no_scale_in_dq", "delta_dropped", "dk_transposed_operand",
                                   "bottom_right_offset_off_by_one", "sink_missing_from_lse",
-                                  "sink_gradient_sign", "sink_given_a_value"])
+                                  "sink_gradient_sign", "sink_given_a_value", "mask_scaled",
+                                  "bool_mask_inverted", "mask_by_kv_head", "masked_row_nan"])
 def test_planted_mistakes_are_caught(name):
     mutant = _mutant(name)
     failures = 0
