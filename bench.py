@@ -347,6 +347,7 @@ def main():
     extras = {}
     if rank == 0:
         extras["short_query"] = run_short_query(torch, api, _lib, dev, stream, hbm_peak)
+        extras["masked"] = run_masked(torch, api, dev, stream, bf16_peak)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         heads = 16
@@ -523,6 +524,46 @@ def run_short_query(torch, api, _lib, dev, stream, hbm_peak):
             "bwd_frac_hbm": bwd_bytes / (bms / 1e3) / 1e9 / hbm_peak,
             "fwd_tflops": F / (fms / 1e3) / 1e12, "bwd_tflops": 2.5 * F / (bms / 1e3) / 1e12,
             "algorithmic_bytes": {"fwd": fwd_bytes, "bwd": bwd_bytes}}
+    return res
+
+
+def run_masked(torch, api, dev, stream, bf16_peak):
+    """Attention masks on the headline shape without the causal flag (every key tile is
+    computed): forward + backward with no mask, a boolean key-padding mask [B, 1, 1, Lkv]
+    (the last 10% of each batch's keys hidden) and an additive bf16 [Lq, Lkv] mask shared
+    by every batch and head.  TFLOP/s count the work computed (non-causal FLOPs, backward
+    2.5x the forward)."""
+    from scaled_dot_product_flash_gb300.inputs import Shape, draw
+    S = dict(WORKLOAD)
+    res = {"workload": "bf16 B=2 Hq=32 Hkv=8 Lq=Lkv=4096 D=128, is_causal=False",
+           "timing": "median of 10 forward+backward calls, L2 flushed before each"}
+    q, k, v, do = (t.to(dev) for t in draw(Shape(**S), 5, "bf16"))
+    scale = 1.0 / math.sqrt(S["D"])
+    pad = torch.ones(S["B"], 1, 1, S["Lkv"], dtype=torch.bool, device=dev)
+    pad[..., int(0.9 * S["Lkv"]):] = False
+    gen = torch.Generator(device="cpu").manual_seed(6)
+    add = torch.randn(S["Lq"], S["Lkv"], generator=gen).to(torch.bfloat16).to(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, device=dev, dtype=torch.uint8)
+    F = fwd_flops(**S, causal=False)
+    for name, mask in (("none", None), ("bool_key_padding", pad), ("additive_shared", add)):
+        out, lse = api.attention_forward(q, k, v, scale=scale, attn_mask=mask)
+        grads = api.attention_backward(q, k, v, out, do, lse, scale=scale, attn_mask=mask)
+        times = []
+        for i in range(13):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            api.attention_forward(q, k, v, scale=scale, attn_mask=mask, out=out, lse=lse)
+            api.attention_backward(q, k, v, out, do, lse, scale=scale, attn_mask=mask,
+                                   dq=grads[0], dk=grads[1], dv=grads[2])
+            b.record(stream)
+            if i >= 3:
+                times.append((a, b))
+        torch.cuda.synchronize()
+        api.poll_status()
+        ms = statistics.median(a.elapsed_time(b) for a, b in times)
+        tf = 3.5 * F / (ms / 1e3) / 1e12
+        res[name] = {"ms": ms, "tflops": tf, "frac_of_bf16_peak": tf / bf16_peak}
     return res
 
 

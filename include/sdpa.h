@@ -181,6 +181,53 @@ int sdpa_bwd_sinks(const void* q, const void* k, const void* v, const void* out,
                    size_t workspace_bytes, void* stream);
 
 /*
+ * Attention masks.  The sink calls plus an optional mask M over [B, Hq, Lq, Lkv] (indexed
+ * by the query head), applied to the scores before the softmax:
+ *   SDPA_MASK_BOOL      bytes; a nonzero byte keeps key j for query i, zero hides it (the
+ *                       boolean attn_mask convention of F.scaled_dot_product_attention)
+ *   SDPA_MASK_ADDITIVE  values of `dtype`, added to S = scale·q·k (−inf hides the key)
+ * It combines with is_causal and with sinks.  The pages list masks with sinks among what
+ * the Metal backward leaves to unfused operations ("[Metal] Add Flash Attention VJP for
+ * training", section "Limitations"), and note that the Metal forward of "mps-flash-sdpa
+ * 0.1.0" (section "When MFA Dispatches vs. Falls Back") takes only all-True boolean masks
+ * and hands float masks and boolean masks with False values back; here both kinds are
+ * fused into every kernel, forward and backward (dQ, dK, dV; the mask itself gets no
+ * gradient).
+ *  - A row that sees no key at all (possible only with a mask) gets O = 0, lse = −inf and
+ *    zero gradients; with a sink, the sink alone fills that row's softmax.
+ *  - Layout: element strides for batch, head and row (the keys of a row are contiguous);
+ *    a stride of 0 broadcasts (e.g. {0, 0, Lkv_padded} for one [Lq, Lkv] mask shared by
+ *    all batches and heads, {Lkv_padded, 0, 0} for a per-batch key-padding mask).  ptr and
+ *    every row must be 16-byte aligned (strides in bytes multiples of 16), and each row
+ *    must be readable up to the next multiple of 16 bytes past its Lkv elements (pad
+ *    the key dimension); the padding's values are never used.  Otherwise
+ *    SDPA_ERR_INVALID_ARG.  The mask is read only; it may overlap inputs, not outputs.
+ *  - Cost: the tiles of keys that the causal bound skips are skipped with or without a
+ *    mask; a mask that hides whole tiles still has them computed.
+ * mask = NULL or kind SDPA_MASK_NONE is the sink call.  sdpa_bwd_masked must get the mask
+ * the forward got.
+ */
+typedef enum {
+  SDPA_MASK_NONE = 0,
+  SDPA_MASK_BOOL = 1,
+  SDPA_MASK_ADDITIVE = 2
+} sdpa_mask_kind_t;
+typedef struct {
+  const void* ptr;          /* device pointer, 16-byte aligned */
+  int kind;                 /* sdpa_mask_kind_t */
+  int64_t batch, head, row; /* element strides (>= 0; 0 broadcasts) */
+} sdpa_mask_t;
+int sdpa_fwd_masked(const void* q, const void* k, const void* v, void* out, float* lse,
+                    const float* sinks, const sdpa_mask_t* mask, int B, int Hq, int Hkv, int Lq,
+                    int Lkv, int D, float scale, int is_causal, int dtype,
+                    const sdpa_strides_t* strides, void* stream);
+int sdpa_bwd_masked(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                    const float* lse, const float* sinks, const sdpa_mask_t* mask, void* dq,
+                    void* dk, void* dv, float* dsinks, int B, int Hq, int Hkv, int Lq, int Lkv,
+                    int D, float scale, int is_causal, int dtype, const sdpa_strides_t* strides,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Backward without a workspace argument: sdpa_bwd for callers that cannot allocate device
  * memory.  Such callers include code running inside a host application or framework that
  * owns every device allocation and hands its plugins nothing but their inputs and outputs,

@@ -37,7 +37,15 @@ class Strides(ctypes.Structure):
     _fields_ = [(n, Layout) for n in ("q", "k", "v", "o", "dout", "dq", "dk", "dv")]
 
 
+class Mask(ctypes.Structure):
+    """sdpa_mask_t: device pointer, kind and (batch, head, row) element strides."""
+    _fields_ = [("ptr", ctypes.c_void_p), ("kind", ctypes.c_int), ("batch", ctypes.c_int64),
+                ("head", ctypes.c_int64), ("row", ctypes.c_int64)]
+
+
+MASK_NONE, MASK_BOOL, MASK_ADDITIVE = 0, 1, 2
 _sp = ctypes.POINTER(Strides)
+_mp = ctypes.POINTER(Mask)
 SIGNATURES = {
     "sdpa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
     "sdpa_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i]),
@@ -62,6 +70,10 @@ SIGNATURES = {
                             _sp, _vp]),
     "sdpa_bwd_sinks": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                             _i, _i, _i, _i, _i, _i, _f, _i, _i, _sp, _vp, _sz, _vp]),
+    "sdpa_fwd_masked": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _mp, _i, _i, _i, _i, _i, _i, _f, _i,
+                             _i, _sp, _vp]),
+    "sdpa_bwd_masked": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _mp, _vp, _vp, _vp, _vp,
+                             _i, _i, _i, _i, _i, _i, _f, _i, _i, _sp, _vp, _sz, _vp]),
 }
 BWD_NOALLOC_MAX_ROWS = 1 << 20
 KERNELS = {"fwd": 0, "delta": 1, "dq": 2, "dkdv": 3, "vec_fwd": 4, "vec_bwd": 5, "sink_grad": 6}
@@ -145,6 +157,24 @@ def sdpa_bwd_sinks(q, k, v, out, dout, lse, sinks, dq, dk, dv, dsinks, B, Hq, Hk
     return load().sdpa_bwd_sinks(q, k, v, out, dout, lse, sinks, dq, dk, dv, dsinks, B, Hq, Hkv,
                                  Lq, Lkv, D, scale, is_causal, dtype, ctypes.byref(strides),
                                  workspace, workspace_bytes, stream)
+
+
+def sdpa_fwd_masked(q, k, v, out, lse, sinks, mask, B, Hq, Hkv, Lq, Lkv, D, scale, is_causal,
+                    dtype, strides, stream):
+    """sdpa_fwd_sinks with an attention mask (a ``Mask`` or None)."""
+    return load().sdpa_fwd_masked(q, k, v, out, lse, sinks,
+                                  ctypes.byref(mask) if mask is not None else None, B, Hq, Hkv,
+                                  Lq, Lkv, D, scale, is_causal, dtype, ctypes.byref(strides),
+                                  stream)
+
+
+def sdpa_bwd_masked(q, k, v, out, dout, lse, sinks, mask, dq, dk, dv, dsinks, B, Hq, Hkv, Lq,
+                    Lkv, D, scale, is_causal, dtype, strides, workspace, workspace_bytes, stream):
+    """sdpa_bwd_sinks with the forward's attention mask (a ``Mask`` or None)."""
+    return load().sdpa_bwd_masked(q, k, v, out, dout, lse, sinks,
+                                  ctypes.byref(mask) if mask is not None else None, dq, dk, dv,
+                                  dsinks, B, Hq, Hkv, Lq, Lkv, D, scale, is_causal, dtype,
+                                  ctypes.byref(strides), workspace, workspace_bytes, stream)
 
 
 def sdpa_bwd_noalloc(q, k, v, out, dout, lse, dq, dk, dv, B, Hq, Hkv, Lq, Lkv, D, scale,

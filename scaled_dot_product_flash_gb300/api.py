@@ -70,15 +70,56 @@ def _check_sinks(name, t, Hq):
         raise ValueError(f"{name} must be a 1-D fp32 tensor of Hq = {Hq} sink logits")
 
 
+def _mask_arg(attn_mask, q, Lq, Lkv):
+    """(Mask struct or None, tensor to keep alive) for an attention mask broadcastable to
+    [B, Hq, Lq, Lkv]: boolean (True keeps the key) or floating (added to the scores).
+
+    A mask whose rows are 16-byte aligned, with key stride 1 and a key dimension that
+    fills whole 16-byte pieces, is passed as a view (broadcast dimensions get stride 0).
+    Otherwise its rows are copied into a buffer with the key dimension padded to 16
+    bytes (keeping the broadcast dimensions at size 1); the padding is never read as data.
+    """
+    if attn_mask is None:
+        return None, None
+    if not attn_mask.is_cuda or attn_mask.device != q.device:
+        raise ValueError("attn_mask must be on the device of q")
+    if attn_mask.dim() > 4:
+        raise ValueError("attn_mask must have at most 4 dimensions")
+    m = attn_mask.reshape((1,) * (4 - attn_mask.dim()) + tuple(attn_mask.shape))
+    B, Hq = q.shape[0], q.shape[1]
+    for size, want, name in zip(m.shape, (B, Hq, Lq, Lkv), ("batch", "head", "query", "key")):
+        if size not in (1, want):
+            raise ValueError(f"attn_mask {name} dimension {size} does not broadcast to {want}")
+    if m.dtype == torch.bool:
+        m, kind = m.view(torch.uint8), _lib.MASK_BOOL
+    elif m.is_floating_point():
+        m, kind = m.to(q.dtype), _lib.MASK_ADDITIVE
+    else:
+        raise ValueError("attn_mask must be boolean or floating point")
+    es = m.element_size()
+    direct = (m.shape[3] == Lkv and m.stride(3) == 1 and (Lkv * es) % 16 == 0
+              and m.data_ptr() % 16 == 0
+              and all(m.shape[a] == 1 or (m.stride(a) * es) % 16 == 0 for a in range(3)))
+    if not direct:
+        pad = (Lkv * es + 15) // 16 * 16 // es
+        buf = torch.zeros(tuple(m.shape[:3]) + (pad,), device=m.device, dtype=m.dtype)
+        buf[..., :Lkv] = m
+        m = buf
+    strides = [0 if m.shape[a] == 1 else m.stride(a) for a in range(3)]
+    return _lib.Mask(m.data_ptr(), kind, *strides), m
+
+
 def attention_forward(q, k, v, scale=None, is_causal=False, need_lse=True, out=None,
-                      lse=None, stream=None, sinks=None):
+                      lse=None, stream=None, sinks=None, attn_mask=None):
     """out = softmax(scale·q·kᵀ [causal]) · v; also the fp32 logsumexp when need_lse.
 
     q [B,Hq,Lq,D], k/v [B,Hkv,Lkv,D] CUDA tensors of one dtype (fp32/fp16/bf16), in any
     layout with contiguous rows (e.g. [B,L,H,D] storage seen through .transpose(1, 2));
     the strides go to the library, nothing is copied.  `out` defaults to q's layout.
     ``sinks``: optional fp32 [Hq] sink logits, one extra softmax entry per row of each
-    query head with a zero value vector (the lse then includes it).
+    query head with a zero value vector (the lse then includes it).  ``attn_mask``:
+    optional mask broadcastable to [B, Hq, Lq, Lkv], boolean (True keeps the key) or
+    floating (added to the scaled scores); it combines with ``is_causal``.
     Returns (out, lse or None).
     """
     for n, t in (("q", q), ("k", k), ("v", v)):
@@ -97,11 +138,12 @@ def attention_forward(q, k, v, scale=None, is_causal=False, need_lse=True, out=N
     if sinks is not None:
         _check_sinks("sinks", sinks, Hq)
     strides = _lib.make_strides(q=_layout(q), k=_layout(k), v=_layout(v), o=_layout(out))
-    st = _lib.sdpa_fwd_sinks(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                             lse.data_ptr() if lse is not None else None,
-                             sinks.data_ptr() if sinks is not None else None,
-                             B, Hq, Hkv, Lq, Lkv, D, scale, _causal(is_causal),
-                             DTYPE_CODE[q.dtype], strides, _stream(stream))
+    mask, _keep = _mask_arg(attn_mask, q, Lq, Lkv)
+    st = _lib.sdpa_fwd_masked(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              lse.data_ptr() if lse is not None else None,
+                              sinks.data_ptr() if sinks is not None else None, mask,
+                              B, Hq, Hkv, Lq, Lkv, D, scale, _causal(is_causal),
+                              DTYPE_CODE[q.dtype], strides, _stream(stream))
     if st != _lib.OK:
         raise _lib.SdpaError(st, "sdpa_fwd")
     return out, lse
@@ -113,8 +155,11 @@ def workspace_bytes(q, k):
 
 
 def attention_backward(q, k, v, out, dout, lse, scale=None, is_causal=False, workspace=None,
-                       dq=None, dk=None, dv=None, stream=None, sinks=None, dsinks=None):
+                       dq=None, dk=None, dv=None, stream=None, sinks=None, dsinks=None,
+                       attn_mask=None):
     """(dq, dk, dv) of the forward, from its output ``out`` and logsumexp ``lse``.
+
+    ``attn_mask`` must be the forward's mask (it receives no gradient).
 
     With ``sinks`` (the forward's fp32 [Hq] sink logits), returns (dq, dk, dv, dsinks),
     dsinks being the fp32 [Hq] gradient of the sink logits summed over the batch.
@@ -141,14 +186,15 @@ def attention_backward(q, k, v, out, dout, lse, scale=None, is_causal=False, wor
     strides = _lib.make_strides(q=_layout(q), k=_layout(k), v=_layout(v), o=_layout(out),
                                 dout=_layout(dout), dq=_layout(dq), dk=_layout(dk),
                                 dv=_layout(dv))
-    st = _lib.sdpa_bwd_sinks(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                             dout.data_ptr(), lse.data_ptr(),
-                             sinks.data_ptr() if sinks is not None else None,
-                             dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                             dsinks.data_ptr() if dsinks is not None else None,
-                             B, Hq, Hkv, Lq, Lkv, D, scale, _causal(is_causal),
-                             DTYPE_CODE[q.dtype], strides, workspace.data_ptr(),
-                             workspace.numel(), _stream(stream))
+    mask, _keep = _mask_arg(attn_mask, q, Lq, Lkv)
+    st = _lib.sdpa_bwd_masked(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              dout.data_ptr(), lse.data_ptr(),
+                              sinks.data_ptr() if sinks is not None else None, mask,
+                              dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                              dsinks.data_ptr() if dsinks is not None else None,
+                              B, Hq, Hkv, Lq, Lkv, D, scale, _causal(is_causal),
+                              DTYPE_CODE[q.dtype], strides, workspace.data_ptr(),
+                              workspace.numel(), _stream(stream))
     if st != _lib.OK:
         raise _lib.SdpaError(st, "sdpa_bwd")
     if sinks is not None:

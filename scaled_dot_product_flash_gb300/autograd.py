@@ -11,9 +11,10 @@ the package, this module only marshals tensors; all arithmetic runs in ``libsdpa
 Supported: q [B, Hq, Lq, D], k and v [B, Hkv, Lkv, D] on CUDA (any layout whose rows are
 contiguous, e.g. [B, L, H, D] storage through .transpose(1, 2)), one dtype of fp32/fp16/bf16,
 Hq a multiple of Hkv (grouped-query attention: query head h uses KV head h // (Hq/Hkv)),
-D in {32, 64, 96, 128}, optional top-left causal mask, any finite scale, optional per-head
-attention-sink logits (``sinks``, differentiable).  Attention masks, dropout and other head
-layouts raise ``NotImplementedError``.
+D in {32, 64, 96, 128}, optional top-left causal mask or ``attn_mask`` (boolean: True keeps
+the key; floating: added to the scores; no gradient flows into it), any finite scale,
+optional per-head attention-sink logits (``sinks``, differentiable).  Dropout and other
+head layouts raise ``NotImplementedError``.
 """
 from __future__ import annotations
 
@@ -28,26 +29,27 @@ class SDPAFunction(torch.autograd.Function):
     """out = softmax(scale · q·kᵀ [causal]) · v with a fused backward."""
 
     @staticmethod
-    def forward(ctx, q, k, v, sinks, scale, is_causal):
+    def forward(ctx, q, k, v, sinks, attn_mask, scale, is_causal):
         needs_grad = any(ctx.needs_input_grad[:4])
         out, lse = api.attention_forward(q, k, v, scale=scale, is_causal=is_causal,
-                                         need_lse=needs_grad, sinks=sinks)
+                                         need_lse=needs_grad, sinks=sinks, attn_mask=attn_mask)
         if needs_grad:
-            ctx.save_for_backward(q, k, v, out, lse, sinks)
+            ctx.save_for_backward(q, k, v, out, lse, sinks, attn_mask)
         ctx.scale = scale
         ctx.is_causal = is_causal
         return out
 
     @staticmethod
     def backward(ctx, dout):
-        q, k, v, out, lse, sinks = ctx.saved_tensors
+        q, k, v, out, lse, sinks, attn_mask = ctx.saved_tensors
         if dout.stride(-1) != 1:
             dout = dout.contiguous()
         # The lse already includes the sinks; they are passed only for their own gradient.
         want_ds = sinks is not None and ctx.needs_input_grad[3]
         g = api.attention_backward(q, k, v, out, dout, lse, scale=ctx.scale,
-                                   is_causal=ctx.is_causal, sinks=sinks if want_ds else None)
-        return g[0], g[1], g[2], (g[3] if want_ds else None), None, None
+                                   is_causal=ctx.is_causal, sinks=sinks if want_ds else None,
+                                   attn_mask=attn_mask)
+        return g[0], g[1], g[2], (g[3] if want_ds else None), None, None, None
 
 
 def scaled_dot_product_attention(query, key, value, attn_mask=None, dropout_p=0.0,
@@ -61,7 +63,10 @@ def scaled_dot_product_attention(query, key, value, attn_mask=None, dropout_p=0.
     each query head with a zero value vector; it is used in fp32 and receives a gradient.
     """
     if attn_mask is not None:
-        raise NotImplementedError("attn_mask is not supported (only is_causal)")
+        if attn_mask.requires_grad:
+            raise NotImplementedError("no gradient is computed for attn_mask")
+        if is_causal:
+            raise ValueError("attn_mask and is_causal cannot both be set (as in torch)")
     if dropout_p != 0.0:
         raise NotImplementedError("dropout is not supported")
     if query.dim() != 4 or key.dim() != 4 or value.dim() != 4:
@@ -90,4 +95,4 @@ def scaled_dot_product_attention(query, key, value, attn_mask=None, dropout_p=0.
     # Any layout with contiguous rows is passed through as is (its strides go to the
     # library); others are copied to [B, H, L, D] first.
     q, k, v = (t if t.stride(-1) == 1 else t.contiguous() for t in (query, key, value))
-    return SDPAFunction.apply(q, k, v, sinks, s, bool(is_causal))
+    return SDPAFunction.apply(q, k, v, sinks, attn_mask, s, bool(is_causal))

@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace sdpa {
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -69,6 +71,8 @@ struct Problem {
   float* delta;      // δ = rowsum(dO∘O) [B,Hq,Lq]
   const float* sinks;  // per-query-head sink logits [Hq] (natural log), or null
   float* dsinks;       // their gradients [Hq] (backward), or null
+  const void* mask;    // attention mask [B, Hq, Lq, Lkv] through layout lm, or null
+  int mask_kind;       // MaskKind
   int B, Hq, Hkv, Lq, Lkv, D;
   int G;             // Hq / Hkv
   float scale;
@@ -81,7 +85,12 @@ struct Problem {
   int inject;        // test hook: 1 = the tensor-core forward never delivers its first K tile
   // Layouts of q, k, v, o (forward output / backward input), dout, dq, dk, dv.
   Layout lq, lk, lv, lo, ldo, ldq, ldk, ldv;
+  Layout lm;           // mask strides (batch, query head, row; 0 broadcasts), keys contiguous
 };
+
+// Attention mask kinds: boolean bytes (nonzero keeps the key for that query) or additive
+// values of the element type, added to scale·q·k (−inf hides the key).
+enum MaskKind : int { kMaskNone = 0, kMaskBool = 1, kMaskAdd = 2 };
 
 // Index of query row (b, h, i) in the contiguous [B, Hq, Lq] arrays lse and δ.
 __host__ __device__ __forceinline__ int64_t q_row(const Problem& p, int b, int h, int i) {
@@ -108,6 +117,110 @@ __device__ __forceinline__ float fold_sink(const Problem& p, int h, float& m, fl
   l = fmaf(l, a, 1.f);
   m = s2;
   return a;
+}
+
+__device__ __forceinline__ float minus_inf() { return __int_as_float(0xff800000); }
+
+// Mask term of one (query row, key) pair in the log2 domain: log2e·M, or −inf for a key a
+// boolean mask hides.  `off` is the element offset of the pair in the mask.
+template <typename T>
+__device__ __forceinline__ float mask_log2(const Problem& p, int64_t off) {
+  if (p.mask_kind == kMaskBool) return static_cast<const uint8_t*>(p.mask)[off] ? 0.f : minus_inf();
+  return Elem<T>::to_f(static_cast<const T*>(p.mask)[off]) * kLog2e;
+}
+
+// Raw scores of N consecutive keys k0.. of one query row, held as fp32 bits: replaced by
+// c·s + log2e·M (the log2-domain masked score).  `off` is the mask offset of (row, k0).
+// The mask row is read in 16-byte pieces (the ABI requires 16-byte aligned rows readable
+// up to the next multiple of 16 bytes past Lkv); keys at or past Lkv get values the
+// callers ignore (they hide those keys by their key limit).
+template <typename T, int N>
+__device__ __forceinline__ void mask_scores(uint32_t (&sv)[N], const Problem& p, int64_t off, int k0, float c) {
+  const int n = min(N, p.Lkv - k0);
+  if (p.mask_kind == kMaskBool) {
+    const uint4* m = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.mask) + off);
+    const int pieces = (n + 15) / 16;
+#pragma unroll
+    for (int q = 0; q < N / 16; ++q) {
+      if (q < pieces) {
+        const uint4 w = __ldg(m + q);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const bool keep = ((ws[t / 4] >> (8 * (t % 4))) & 0xffu) != 0u;
+          sv[16 * q + t] = __float_as_uint(keep ? c * __uint_as_float(sv[16 * q + t]) : minus_inf());
+        }
+      }
+    }
+  } else {
+    constexpr int kPer = 16 / sizeof(T);
+    const uint4* m = reinterpret_cast<const uint4*>(static_cast<const T*>(p.mask) + off);
+    const int pieces = (n + kPer - 1) / kPer;
+#pragma unroll
+    for (int q = 0; q < N / kPer; ++q) {
+      if (q < pieces) {
+        union { uint4 u; T e[kPer]; } w;
+        w.u = __ldg(m + q);
+#pragma unroll
+        for (int t = 0; t < kPer; ++t) {
+          const float mv = Elem<T>::to_f(w.e[t]) * kLog2e;
+          const float x = __uint_as_float(sv[kPer * q + t]);
+          sv[kPer * q + t] = __float_as_uint(mv == minus_inf() ? mv : fmaf(c, x, mv));
+        }
+      }
+    }
+  }
+}
+
+// Mask values of N consecutive keys of one query row as packed pairs of the 16-bit element
+// type T (key 2e in the low half of word e): the additive values as stored, or 0 / −inf
+// for a boolean mask.  Only the 16-byte pieces that hold the first n keys are read (the
+// same row padding rule as mask_scores); the other words are 0.
+template <typename T, int N>
+__device__ __forceinline__ void mask_pairs(uint32_t (&mk)[N / 2], const Problem& p, int64_t off, int n) {
+  static_assert(sizeof(T) == 2, "16-bit element types only");
+#pragma unroll
+  for (int e = 0; e < N / 2; ++e) mk[e] = 0u;
+  if (p.mask_kind == kMaskBool) {
+    constexpr uint32_t kHide = std::is_same<T, __nv_bfloat16>::value ? 0xff80u : 0xfc00u;  // −inf
+    const uint4* m = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.mask) + off);
+    const int pieces = (n + 15) / 16;
+#pragma unroll
+    for (int q = 0; q < N / 16; ++q) {
+      if (q < pieces) {
+        const uint4 w = __ldg(m + q);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const uint32_t word = ws[t / 2], sh = 16 * (t % 2);
+          const uint32_t lo = ((word >> sh) & 0xffu) ? 0u : kHide;
+          const uint32_t hi = ((word >> (sh + 8)) & 0xffu) ? 0u : kHide;
+          mk[8 * q + t] = lo | (hi << 16);
+        }
+      }
+    }
+  } else {
+    const uint4* m = reinterpret_cast<const uint4*>(static_cast<const T*>(p.mask) + off);
+    const int pieces = (n + 7) / 8;
+#pragma unroll
+    for (int q = 0; q < N / 8; ++q) {
+      if (q < pieces) {
+        const uint4 w = __ldg(m + q);
+        mk[4 * q] = w.x;
+        mk[4 * q + 1] = w.y;
+        mk[4 * q + 2] = w.z;
+        mk[4 * q + 3] = w.w;
+      }
+    }
+  }
+}
+
+// Hint that the bytes [ptr, ptr + bytes) will be read soon (into L1; bytes <= 256).
+__device__ __forceinline__ void prefetch_l1(const void* ptr, int bytes) {
+  const char* a = static_cast<const char*>(ptr);
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(a));
+  if (bytes > 128) asm volatile("prefetch.global.L1 [%0];" ::"l"(a + 128));
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(a + bytes - 1));
 }
 
 template <typename T>

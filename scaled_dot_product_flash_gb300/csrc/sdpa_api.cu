@@ -82,6 +82,27 @@ bool check_layout(const sdpa_layout_t& l, int B, int H, int L, int D, size_t es,
   return true;
 }
 
+// Validates an attention mask (kind, alignment, strides) and fills p->mask, mask_kind and
+// lm; *bytes is the byte extent the kernels may read (each row up to the next multiple of
+// 16 bytes past Lkv), 0 without a mask.
+bool check_mask(const sdpa_mask_t* m, int dtype, Problem* p, size_t* bytes) {
+  *bytes = 0;
+  if (!m || m->kind == SDPA_MASK_NONE) return true;
+  if (m->kind != SDPA_MASK_BOOL && m->kind != SDPA_MASK_ADDITIVE) return false;
+  if (!m->ptr || !aligned16(m->ptr)) return false;
+  const int64_t es = m->kind == SDPA_MASK_BOOL ? 1 : (int64_t)elem_size(dtype);
+  const int64_t st[3] = {m->batch, m->head, m->row};
+  for (int a = 0; a < 3; ++a)
+    if (st[a] < 0 || (st[a] * es) % 16 != 0 || st[a] > ((int64_t)1 << 40)) return false;
+  const int64_t row_bytes = ((int64_t)p->Lkv * es + 15) / 16 * 16;
+  *bytes = (size_t)(((int64_t)(p->B - 1) * m->batch + (int64_t)(p->Hq - 1) * m->head + (int64_t)(p->Lq - 1) * m->row) * es +
+                    row_bytes);
+  p->mask = m->ptr;
+  p->mask_kind = m->kind;
+  p->lm = Layout{m->batch, m->head, m->row};
+  return true;
+}
+
 // Checks sizes, dtype and scale; fills the size fields of *p.
 int check_sizes(int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale, int dtype,
                 Problem* p) {
@@ -201,10 +222,10 @@ int status_of(cudaError_t e) { return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA
 
 using namespace sdpa;
 
-extern "C" int sdpa_fwd_sinks(const void* q, const void* k, const void* v, void* out, float* lse,
-                              const float* sinks, int B, int Hq, int Hkv, int Lq, int Lkv, int D,
-                              float scale, int is_causal, int dtype, const sdpa_strides_t* strides,
-                              void* stream) {
+extern "C" int sdpa_fwd_masked(const void* q, const void* k, const void* v, void* out, float* lse,
+                               const float* sinks, const sdpa_mask_t* mask, int B, int Hq, int Hkv,
+                               int Lq, int Lkv, int D, float scale, int is_causal, int dtype,
+                               const sdpa_strides_t* strides, void* stream) {
   Problem p;
   int st = check_sizes(B, Hq, Hkv, Lq, Lkv, D, scale, dtype, &p);
   if (st != SDPA_OK) return st;
@@ -224,6 +245,9 @@ extern "C" int sdpa_fwd_sinks(const void* q, const void* k, const void* v, void*
     return SDPA_ERR_INVALID_ARG;
   const size_t sb = (size_t)Hq * sizeof(float);
   if (overlaps(out, ob, sinks, sb) || overlaps(lse, lb, sinks, sb)) return SDPA_ERR_INVALID_ARG;
+  size_t mb;
+  if (!check_mask(mask, dtype, &p, &mb)) return SDPA_ERR_INVALID_ARG;
+  if (overlaps(out, ob, p.mask, mb) || overlaps(lse, lb, p.mask, mb)) return SDPA_ERR_INVALID_ARG;
   p.q = q;
   p.k = k;
   p.v = v;
@@ -253,6 +277,14 @@ extern "C" int sdpa_fwd_sinks(const void* q, const void* k, const void* v, void*
   return status_of(e);
 }
 
+extern "C" int sdpa_fwd_sinks(const void* q, const void* k, const void* v, void* out, float* lse,
+                              const float* sinks, int B, int Hq, int Hkv, int Lq, int Lkv, int D,
+                              float scale, int is_causal, int dtype, const sdpa_strides_t* strides,
+                              void* stream) {
+  return sdpa_fwd_masked(q, k, v, out, lse, sinks, nullptr, B, Hq, Hkv, Lq, Lkv, D, scale, is_causal,
+                         dtype, strides, stream);
+}
+
 extern "C" int sdpa_fwd_strided(const void* q, const void* k, const void* v, void* out, float* lse,
                                 int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale,
                                 int is_causal, int dtype, const sdpa_strides_t* strides, void* stream) {
@@ -276,12 +308,12 @@ extern "C" size_t sdpa_bwd_workspace_size(int B, int Hq, int Hkv, int Lq, int Lk
   return (bytes + 255) / 256 * 256;
 }
 
-extern "C" int sdpa_bwd_sinks(const void* q, const void* k, const void* v, const void* out,
-                              const void* dout, const float* lse, const float* sinks, void* dq,
-                              void* dk, void* dv, float* dsinks, int B, int Hq, int Hkv, int Lq,
-                              int Lkv, int D, float scale, int is_causal, int dtype,
-                              const sdpa_strides_t* strides, void* workspace, size_t workspace_bytes,
-                              void* stream) {
+extern "C" int sdpa_bwd_masked(const void* q, const void* k, const void* v, const void* out,
+                               const void* dout, const float* lse, const float* sinks,
+                               const sdpa_mask_t* mask, void* dq, void* dk, void* dv, float* dsinks,
+                               int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale,
+                               int is_causal, int dtype, const sdpa_strides_t* strides,
+                               void* workspace, size_t workspace_bytes, void* stream) {
   Problem p;
   int st = check_sizes(B, Hq, Hkv, Lq, Lkv, D, scale, dtype, &p);
   if (st != SDPA_OK) return st;
@@ -304,12 +336,14 @@ extern "C" int sdpa_bwd_sinks(const void* q, const void* k, const void* v, const
       !check_layout(strides->dv, B, Hkv, Lkv, D, es, &p.ldv, &dvb))
     return SDPA_ERR_INVALID_ARG;
   const size_t lb = (size_t)B * Hq * Lq * sizeof(float), sb = (size_t)Hq * sizeof(float);
-  const void* ins[] = {q, k, v, out, dout, lse, sinks};
-  const size_t in_bytes[] = {qb, kb, vb, ob, dob, lb, sb};
+  size_t mb;
+  if (!check_mask(mask, dtype, &p, &mb)) return SDPA_ERR_INVALID_ARG;
+  const void* ins[] = {q, k, v, out, dout, lse, sinks, p.mask};
+  const size_t in_bytes[] = {qb, kb, vb, ob, dob, lb, sb, mb};
   void* outs[] = {dq, dk, dv, workspace, dsinks};
   const size_t out_bytes[] = {dqb, dkb, dvb, need, sb};
   for (int a = 0; a < 5; ++a) {
-    for (int c = 0; c < 7; ++c)
+    for (int c = 0; c < 8; ++c)
       if (overlaps(outs[a], out_bytes[a], ins[c], in_bytes[c])) return SDPA_ERR_INVALID_ARG;
     for (int c = a + 1; c < 5; ++c)
       if (overlaps(outs[a], out_bytes[a], outs[c], out_bytes[c])) return SDPA_ERR_INVALID_ARG;
@@ -355,6 +389,16 @@ extern "C" int sdpa_bwd_sinks(const void* q, const void* k, const void* v, const
     return tc ? launch_tc_dq(p, dtype, s) : launch_simt_dq(p, dtype, s);
   });
   return status_of(e);
+}
+
+extern "C" int sdpa_bwd_sinks(const void* q, const void* k, const void* v, const void* out,
+                              const void* dout, const float* lse, const float* sinks, void* dq,
+                              void* dk, void* dv, float* dsinks, int B, int Hq, int Hkv, int Lq,
+                              int Lkv, int D, float scale, int is_causal, int dtype,
+                              const sdpa_strides_t* strides, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  return sdpa_bwd_masked(q, k, v, out, dout, lse, sinks, nullptr, dq, dk, dv, dsinks, B, Hq, Hkv, Lq, Lkv,
+                         D, scale, is_causal, dtype, strides, workspace, workspace_bytes, stream);
 }
 
 extern "C" int sdpa_bwd_strided(const void* q, const void* k, const void* v, const void* out,

@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Problem p) {
   float m = neg_inf(), l = 0.f;
   int kv_end = p.Lkv;
   if (p.causal) kv_end = min(p.Lkv, (int)blockIdx.x * kRows + kRows + p.coff);
+  const int64_t moff = p.mask && valid ? row_off(p.lm, b, h, i) : 0;
 
   for (int j0 = 0; j0 < kv_end; j0 += kTile) {
     __syncthreads();
@@ -78,10 +79,11 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Problem p) {
       const int j = j0 + jj;
       const bool vis = j < p.Lkv && (!p.causal || j <= i + p.coff);
       s[jj] = vis ? acc * p.scale_log2 : neg_inf();
+      if (vis && p.mask && valid) s[jj] += mask_log2<T>(p, moff + j);
       tmax = fmaxf(tmax, s[jj]);
     }
     const float m_new = fmaxf(m, tmax);
-    if (m_new == neg_inf()) continue;  // nothing visible yet (cannot happen for key 0)
+    if (m_new == neg_inf()) continue;  // nothing visible yet (only a mask can do that)
     const float alpha = exp2f(m - m_new);
     l *= alpha;
 #pragma unroll
@@ -97,11 +99,11 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Problem p) {
   }
   if (!valid) return;
   const float a = fold_sink(p, h, m, l);
-  const float inv = a / l;
+  const float inv = l > 0.f ? a / l : 0.f;  // a row that sees no key: O = 0, lse = −inf
   T* op = row_ptr<T>(p.out, p.lo, b, h, i);
 #pragma unroll
   for (int t = 0; t < DPT; ++t) op[sub + kTpr * t] = Elem<T>::from_f(o[t] * inv);
-  if (p.lse && sub == 0) p.lse[q_row(p, b, h, i)] = (m + log2f(l)) * kLn2;
+  if (p.lse && sub == 0) p.lse[q_row(p, b, h, i)] = l > 0.f ? (m + log2f(l)) * kLn2 : neg_inf();
 }
 
 template <typename T, int D>
@@ -126,8 +128,11 @@ __global__ void __launch_bounds__(kThreads) simt_dq_kernel(Problem p) {
     dor[t] = valid ? Elem<T>::to_f(dop[sub + kTpr * t]) : 0.f;
     dq[t] = 0.f;
   }
-  const float lse2 = valid ? p.lse[row] * kLog2e : 0.f;
+  const float lse = valid ? p.lse[row] : neg_inf();
+  const bool live = lse != neg_inf();  // a valid row that sees some key
+  const float lse2 = live ? lse * kLog2e : 0.f;
   const float dl = valid ? p.delta[row] : 0.f;
+  const int64_t moff = p.mask && live ? row_off(p.lm, b, h, i) : 0;
   int kv_end = p.Lkv;
   if (p.causal) kv_end = min(p.Lkv, (int)blockIdx.x * kRows + kRows + p.coff);
 
@@ -147,8 +152,9 @@ __global__ void __launch_bounds__(kThreads) simt_dq_kernel(Problem p) {
       s = reduce4(s);
       dp = reduce4(dp);
       const int j = j0 + jj;
-      const bool vis = valid && j < p.Lkv && (!p.causal || j <= i + p.coff);
-      const float pj = vis ? exp2f(s * p.scale_log2 - lse2) : 0.f;
+      const bool vis = live && j < p.Lkv && (!p.causal || j <= i + p.coff);
+      const float mv = vis && p.mask ? mask_log2<T>(p, moff + j) : 0.f;
+      const float pj = vis ? exp2f(s * p.scale_log2 + mv - lse2) : 0.f;
       const float ds = pj * (dp - dl);
 #pragma unroll
       for (int t = 0; t < DPT; ++t) dq[t] = fmaf(ds, ks[jj][sub + kTpr * t], dq[t]);
@@ -197,7 +203,9 @@ __global__ void __launch_bounds__(kThreads) simt_dkdv_kernel(Problem p) {
       load_tile<T, D>(dos, dop, p.ldo.sl, i0, p.Lq);
       if (threadIdx.x < kTile) {
         const int i = i0 + threadIdx.x;
-        lse2s[threadIdx.x] = i < p.Lq ? lsep[i] * kLog2e : 0.f;
+        // +inf for rows that see no key (lse = −inf): their P is exp2(… − inf) = 0.
+        const float l = i < p.Lq ? lsep[i] : 0.f;
+        lse2s[threadIdx.x] = l == neg_inf() ? -neg_inf() : l * kLog2e;
         dls[threadIdx.x] = i < p.Lq ? dlp[i] : 0.f;
       }
       __syncthreads();
@@ -213,7 +221,8 @@ __global__ void __launch_bounds__(kThreads) simt_dkdv_kernel(Problem p) {
         dp = reduce4(dp);
         const int i = i0 + ii;
         const bool vis = valid && i < p.Lq && (!p.causal || j <= i + p.coff);
-        const float pj = vis ? exp2f(s * p.scale_log2 - lse2s[ii]) : 0.f;
+        const float mv = vis && p.mask ? mask_log2<T>(p, row_off(p.lm, b, h, i) + j) : 0.f;
+        const float pj = vis ? exp2f(s * p.scale_log2 + mv - lse2s[ii]) : 0.f;
         const float ds = pj * (dp - dls[ii]);
 #pragma unroll
         for (int t = 0; t < DPT; ++t) {

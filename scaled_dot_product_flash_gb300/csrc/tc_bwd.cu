@@ -144,7 +144,7 @@ __device__ __forceinline__ void mma_accumulate(uint32_t acc_tmem, uint32_t a_tme
 }
 
 // ================================================================== dK / dV
-template <typename T, int D>
+template <typename T, int D, bool kMasked>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -217,7 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int e = lane; e < kBlk; e += 32) {
         const int i = i0 + e;
-        bars.nlse2[s][e] = i < p.Lq ? -lsep[i] * kLog2e : -pos_inf();
+        const float l = i < p.Lq ? lsep[i] : -pos_inf();  // −inf: the row sees no key, P = 0
+        bars.nlse2[s][e] = l == -pos_inf() ? -pos_inf() : -l * kLog2e;
         bars.ndelta[s][e] = i < p.Lq ? -dlp[i] : 0.f;
       }
       mbar_arrive(&bars.vec_full[s]);
@@ -266,9 +267,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t x_addr = tmem_addr(tbase, quarter * 32, kColX + 64 * w);
     const uint32_t y_addr = tmem_addr(tbase, quarter * 32, kColY + 64 * w);
     const uint64_t cc = f2pack(p.scale_log2, p.scale_log2);
+    constexpr bool masked = kMasked;  // a separate instantiation carries the mask code
+    const int mes = p.mask_kind == kMaskBool ? 1 : (int)sizeof(T);
     bool ok = true;
     for (int n = 0; n < total; ++n) {
       const int s = n % kStages;
+      const int hm = g * p.G + n / nqb;
+      if (masked) {  // this warp's 32 keys of the half's 64 query rows, read after S arrives
+        const int jw = j0 + quarter * 32;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int iq = i_begin + (n % nqb) * kBlk + 64 * w + 32 * t + lane;
+          if (iq < p.Lq && jw < p.Lkv)
+            prefetch_l1(static_cast<const uint8_t*>(p.mask) + (row_off(p.lm, b, hm, iq) + jw) * mes,
+                        min(32, p.Lkv - jw) * mes);
+        }
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[0], n & 1, wc) &&
                                        mbar_wait(&bars.vec_full[s], (n / kStages) & 1, wc));
       if (!ok) break;
@@ -285,12 +299,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sr[64];
         tmem_ld32(x_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
         tmem_ld32(x_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-        tmem_ld_wait();
+        if constexpr (kMasked) tmem_ld_wait(sr);  // the mask code reads sr with plain arithmetic
+        else tmem_ld_wait();
         uint32_t pk[32];
+        if constexpr (masked) {
+          // c·s + log2e·M for this key against the half's queries (mask 0 for queries past
+          // Lq and keys past Lkv: those P are zero or clipped anyway).
+          const bool jv = j < p.Lkv;
+          const int64_t mo = row_off(p.lm, b, hm, 0) + j;
+#pragma unroll
+          for (int e = 0; e < 64; ++e) {
+            const float mv = jv && i0 + e < p.Lq ? mask_log2<T>(p, mo + (int64_t)(i0 + e) * p.lm.sl) : 0.f;
+            sr[e] = __float_as_uint(mv == minus_inf() ? mv : fmaf(p.scale_log2, __uint_as_float(sr[e]), mv));
+          }
+        }
+        const uint64_t ce = masked ? f2pack(1.f, 1.f) : cc;
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           float p0, p1;
-          ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl2[e]), p0, p1);
+          ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), ce, nl2[e]), p0, p1);
           if (diag) {
             if (j > ic + 2 * e) p0 = 0.f;
             if (j > ic + 2 * e + 1) p1 = 0.f;
@@ -409,7 +436,7 @@ struct DqBars {
   int abort;
 };
 
-template <typename T, int D>
+template <typename T, int D, bool kMasked>
 __global__ void __launch_bounds__(kDqThreads, 1)
     tc_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -551,11 +578,19 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const int i = i0 + quarter * 32 + lane;  // this thread's query
     const bool valid = i < p.Lq;
     const int64_t row = q_row(p, b, h, valid ? i : 0);
-    const float lse2 = valid ? p.lse[row] * kLog2e : pos_inf();
+    const float lse = valid ? p.lse[row] : -pos_inf();
+    const float lse2 = lse == -pos_inf() ? pos_inf() : lse * kLog2e;  // no visible key: P = 0
     const float dl = valid ? p.delta[row] : 0.f;
-    const uint64_t cc = f2pack(p.scale_log2, p.scale_log2), nl = f2pack(-lse2, -lse2), nd = f2pack(-dl, -dl);
+    constexpr bool masked = kMasked;  // a separate instantiation carries the mask code
+    const int mes = p.mask_kind == kMaskBool ? 1 : (int)sizeof(T);
+    const int64_t moff = masked && valid ? row_off(p.lm, b, h, i) : 0;
+    const uint64_t cc = f2pack(p.scale_log2, p.scale_log2);
+    const uint64_t nl = f2pack(-lse2, -lse2), nd = f2pack(-dl, -dl);
     bool ok = true;
     for (int n = 0; n < total; ++n) {
+      if (masked && valid && n * kBlk + 64 * w < p.Lkv)  // read after S arrives
+        prefetch_l1(static_cast<const uint8_t*>(p.mask) + (moff + n * kBlk + 64 * w) * mes,
+                    min(64, p.Lkv - (n * kBlk + 64 * w)) * mes);
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[n % 2], (n / 2) & 1, wc) &&
                                        mbar_wait(&bars.dp_full, n & 1, wc));
       if (!ok) break;
@@ -576,11 +611,22 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&bars.dp_free);
+      // Mask terms of this half's keys as 16-bit pairs (0 past the row's mask pieces: those
+      // keys are past Lkv and hidden by lim).
+      uint32_t mk[kMasked ? 32 : 1];
+      if constexpr (kMasked) mask_pairs<T, 64>(mk, p, moff + k0, valid && k0 < p.Lkv ? p.Lkv - k0 : 0);
       uint32_t dsk[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
         float p0, p1;
-        ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl), p0, p1);
+        uint64_t xx = ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl);
+        if constexpr (kMasked) {
+          float x0, x1, m0, m1;
+          f2unpack(xx, x0, x1);
+          unpack2<T>(mk[e], m0, m1);
+          xx = f2pack(x0 + m0 * kLog2e, x1 + m1 * kLog2e);
+        }
+        ex2_pair(xx, p0, p1);
         if (need_mask) {
           if (2 * e >= lim) p0 = 0.f;
           if (2 * e + 1 >= lim) p1 = 0.f;
@@ -665,7 +711,7 @@ cudaError_t dkdv_t(const Problem& p, cudaStream_t s) {
   Maps m;
   if (!make_maps(p, D, &m)) return cudaErrorInvalidValue;
   const int smem = BwdLayout<D>::kBytes + 1024;
-  auto kern = tc_dkdv_kernel<T, D>;
+  auto kern = p.mask ? tc_dkdv_kernel<T, D, true> : tc_dkdv_kernel<T, D, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned nkt = (p.Lkv + kRows - 1) / kRows;
@@ -678,7 +724,7 @@ cudaError_t dq_t(const Problem& p, cudaStream_t s) {
   Maps m;
   if (!make_maps(p, D, &m)) return cudaErrorInvalidValue;
   const int smem = DqLayout<D>::kBytes + 1024;
-  auto kern = tc_dq_kernel<T, D>;
+  auto kern = p.mask ? tc_dq_kernel<T, D, true> : tc_dq_kernel<T, D, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned nqt = (p.Lq + kRows - 1) / kRows;

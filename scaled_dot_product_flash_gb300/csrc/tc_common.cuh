@@ -142,6 +142,21 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// The registers that tcgen05.ld writes are outputs of its asm statement, so the compiler
+// may schedule plain arithmetic on them before the tcgen05.wait::ld that makes them valid.
+// Passing each through an empty volatile asm after the wait ties every later use to a
+// point after the wait.
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int e = 0; e < N; ++e) asm volatile("" : "+r"(r[e]));
+}
+// tcgen05.wait::ld, then reg_fence on the registers loaded.
+template <int N>
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[N]) {
+  tmem_ld_wait();
+  reg_fence(r);
+}
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp gets lane (base + t).

@@ -21,9 +21,10 @@
 // maximum, which keeps the result exact up to rounding.
 // Rows with few visible keys (the first Q tile under the causal mask, or every row when
 // Lkv <= 128) can have |O| near the largest inputs, where rounding P to 16 bits would
-// add an error comparable to the output's own rounding.  For that one KV tile P is split
-// into a 16-bit head and a 16-bit remainder (written to S columns [64, 128)) and both
-// are multiplied into O, so P enters O with ~16 extra bits.
+// add an error comparable to the output's own rounding.  For that one KV tile (for every
+// tile when an attention mask is given) P is split into a 16-bit head and a 16-bit
+// remainder (written to S columns [64, 128)) and both are multiplied into O, so P enters
+// O with ~16 extra bits.
 // Epilogue: O / l rounded to the element type and staged in the tile's (now unused) Q
 // buffer, then written by bulk tensor stores; lse = ln2·(m + log2 l) (natural log).
 #include "launch.h"
@@ -81,9 +82,12 @@ struct IsBf16<__nv_bfloat16> { static constexpr bool value = true; };
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
-// KV tile j of Q tile starting at tile_row0 gets the split (head + remainder) P.
+// KV tile j of Q tile starting at tile_row0 gets the split (head + remainder) P: the first
+// tile of rows that see few keys, and every tile under an attention mask, which can leave
+// any row with few keys of non-negligible weight.
+template <bool kMasked>
 __device__ __forceinline__ bool split_tile(const Problem& p, int j, int tile_row0) {
-  return j == 0 && (tile_row0 == 0 || p.Lkv <= kBN);
+  return kMasked || (j == 0 && (tile_row0 == 0 || p.Lkv <= kBN));
 }
 
 // Number of leading keys of the tile starting at k0 that row i may see: key k0 + e is
@@ -202,7 +206,9 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
   }
 }
 
-template <typename T, int D>
+// kMasked: the call has an attention mask (a separate instantiation, so that the
+// unmasked kernel carries none of the mask code).
+template <typename T, int D, bool kMasked>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to, Problem p) {
@@ -336,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
           mma_ts_w(o_tm, s_tm + kk * 8, sdesc_advance(vd, kk * 2048), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-        if (split_tile(p, j, tile_row0)) {  // remainder of P, columns [64, 128)
+        if (split_tile<kMasked>(p, j, tile_row0)) {  // remainder of P, columns [64, 128)
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
             mma_ts_w(o_tm, s_tm + 64 + kk * 8, sdesc_advance(vd, kk * 2048), kIdO, 1u);
@@ -363,7 +369,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tiles have KV tiles left), so the pass of one tile has the multi-function units to
     // itself while the tensor core works on the other tile's PV and next S.
     const int nboth = min(nkv[0], nkv[1]);
+    constexpr bool masked = kMasked;
+    const int64_t moff = masked && i < p.Lq ? row_off(p.lm, b, h, i) : 0;
     for (int j = 0; j < nkv[w]; ++j) {
+      if (masked && i < p.Lq)  // the mask tile's row is read after S arrives (hint only)
+        prefetch_l1(static_cast<const uint8_t*>(p.mask) + (moff + j * kBN) * (p.mask_kind == kMaskBool ? 1 : sizeof(T)),
+                    min(kBN, p.Lkv - j * kBN) * (p.mask_kind == kMaskBool ? 1 : (int)sizeof(T)));
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[w], j & 1, wc));
       if (!ok) break;
       tc_fence_after();
@@ -374,12 +385,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int q4 = 0; q4 < kBN / 32; ++q4)
         tmem_ld32(s_addr + 32 * q4, *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * q4]));
-      tmem_ld_wait();
+      if constexpr (kMasked) tmem_ld_wait(sv);  // the mask code reads sv with plain arithmetic
+      else tmem_ld_wait();
       const int lim = visible_keys(p, k0, i);
-      const float mt = need_mask ? tile_max<true>(sv, c, lim) : tile_max<false>(sv, c, lim);
+      // With a mask the scores become c·s + log2e·M here and are used with a factor of 1.
+      float cs = c;
+      if constexpr (masked) {
+        if (i < p.Lq) mask_scores<T, kBN>(sv, p, moff + k0, k0, c);
+        cs = 1.f;
+      }
+      const float mt = need_mask ? tile_max<true>(sv, cs, lim) : tile_max<false>(sv, cs, lim);
       const float m_new = fmaxf(m, mt);
       const bool resc = m_new > m + kRescale;  // always true on the first tile (m = -inf)
-      const float alpha = resc ? ex2(m - m_new) : 1.f;
+      const float alpha = resc ? ex2(m - m_new) : 1.f;  // 0 when m was −inf
       if (resc) {
         l *= alpha;
         m = m_new;
@@ -405,12 +423,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
       }
       // Pass 2: P = exp2(c·s − m), row sum, P packed to 16 bits over S's first 64 columns.
-      if (split_tile(p, j, tile_row0))
-        l += exp_pass_split<T>(sv, s_addr, c, -m, lim);
+      // m is −inf only while a mask has hidden every key so far; any finite shift then
+      // gives P = 0 for those keys.
+      const float neg_m = (kMasked && m == neg_inf()) ? 0.f : -m;
+      if (split_tile<kMasked>(p, j, tile_row0))
+        l += exp_pass_split<T>(sv, s_addr, cs, neg_m, lim);
       else if (need_mask)
-        l += exp_pass<T, true>(sv, s_addr, c, -m, lim);
+        l += exp_pass<T, true>(sv, s_addr, cs, neg_m, lim);
       else
-        l += exp_pass<T, false>(sv, s_addr, c, -m, lim);
+        l += exp_pass<T, false>(sv, s_addr, cs, neg_m, lim);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars.p_full[w]);
@@ -429,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) {
         tc_fence_after();
         const float a = fold_sink(p, h, m, l);
-        const float inv = a / l;
+        const float inv = (!kMasked || l > 0.f) ? a / l : 0.f;  // a row that sees no key: O = 0
 #pragma unroll
         for (int c32 = 0; c32 < D / 32; ++c32) {
           uint32_t orr[32];
@@ -446,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 make_uint4(packed[4 * v4], packed[4 * v4 + 1], packed[4 * v4 + 2], packed[4 * v4 + 3]);
         }
         fence_async_smem();
-        if (i < p.Lq && p.lse) p.lse[q_row(p, b, h, i)] = (m + __log2f(l)) * kLn2;
+        if (i < p.Lq && p.lse) p.lse[q_row(p, b, h, i)] = (!kMasked || l > 0.f) ? (m + __log2f(l)) * kLn2 : neg_inf();
       }
       if (named_sync_and(1 + w, kBM, ok) && r == 0) {
         for (int cb = 0; cb < kCB; ++cb) tma_store_4d(&to, stage + cb * 16384, cb * 64, tile_row0, h, b);
@@ -463,20 +484,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <typename T, int D>
-cudaError_t tc_fwd_t(const Problem& p, cudaStream_t s) {
+template <typename T, int D, bool kMasked>
+cudaError_t tc_fwd_m(const Problem& p, cudaStream_t s) {
   CUtensorMap tq, tk, tv, to;
   if (!make_tmap_4d(&tq, p.q, D, p.Lq, p.Hq, p.B, p.lq, kBM) || !make_tmap_4d(&to, p.out, D, p.Lq, p.Hq, p.B, p.lo, kBM) ||
       !make_tmap_4d(&tk, p.k, D, p.Lkv, p.Hkv, p.B, p.lk, kBN) ||
       !make_tmap_4d(&tv, p.v, D, p.Lkv, p.Hkv, p.B, p.lv, kBN))
     return cudaErrorInvalidValue;
   const int smem = FwdLayout<D>::kBytes + 1024;
-  auto kern = tc_fwd_kernel<T, D>;
+  auto kern = tc_fwd_kernel<T, D, kMasked>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned nqb = (p.Lq + kBM * kQTiles - 1) / (kBM * kQTiles);
   kern<<<nqb * p.Hq * p.B, kThreads, smem, s>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t tc_fwd_t(const Problem& p, cudaStream_t s) {
+  return p.mask ? tc_fwd_m<T, D, true>(p, s) : tc_fwd_m<T, D, false>(p, s);
 }
 
 }  // namespace

@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(kThreads) vec_fwd_kernel(Problem p, int chunk)
         const int j = j0 + jj;
         const bool vis = r2 < R && j < j_end && (!p.causal || j <= i2 + p.coff);
         s[e] = vis ? acc * p.scale_log2 : neg_inf();
+        if (vis && p.mask) s[e] += mask_log2<T>(p, row_off(p.lm, b, g * p.G + r2 / p.Lq, i2) + j);
         bmax = fmaxf(bmax, s[e]);
       }
 #pragma unroll
@@ -194,8 +195,9 @@ __global__ void __launch_bounds__(kThreads) vec_fwd_kernel(Problem p, int chunk)
     const int hh2 = r2 / p.Lq, i2 = r2 % p.Lq;
     const int64_t row = q_row(p, b, g * p.G + hh2, i2);
     const float a = fold_sink(p, g * p.G + hh2, M, L);
-    row_ptr<T>(p.out, p.lo, b, g * p.G + hh2, i2)[d] = Elem<T>::from_f(O * a / L);
-    if (p.lse && d == 0) p.lse[row] = (M + log2f(L)) * kLn2;
+    // A row that sees no key (only a mask can do that): O = 0, lse = −inf.
+    row_ptr<T>(p.out, p.lo, b, g * p.G + hh2, i2)[d] = Elem<T>::from_f(L > 0.f ? O * a / L : 0.f);
+    if (p.lse && d == 0) p.lse[row] = L > 0.f ? (M + log2f(L)) * kLn2 : neg_inf();
   }
   cluster.sync();  // peers may still be reading this block's shared memory
 }
@@ -255,7 +257,8 @@ __global__ void __launch_bounds__(kThreads) vec_bwd_kernel(Problem p, int chunk)
       const T* op = row_ptr<T>(p.o, p.lo, b, h2, i2);
       const T* dop = row_ptr<T>(p.dout, p.ldo, b, h2, i2);
       for (int d = lane; d < D; d += 32) acc = fmaf(Elem<T>::to_f(op[d]), Elem<T>::to_f(dop[d]), acc);
-      l2 = p.lse[row] * kLog2e;
+      const float l = p.lse[row];
+      l2 = l == neg_inf() ? -neg_inf() : l * kLog2e;  // no visible key: +inf makes P = 0
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -314,7 +317,8 @@ __global__ void __launch_bounds__(kThreads) vec_bwd_kernel(Problem p, int chunk)
       }
       const int j = j0 + jj;
       const bool vis = r2 < R && j < j_end && (!p.causal || j <= r2 % p.Lq + p.coff);
-      const float pe = vis ? exp2f(s * p.scale_log2 - sm.lse2[r2]) : 0.f;
+      const float mv = vis && p.mask ? mask_log2<T>(p, row_off(p.lm, b, g * p.G + r2 / p.Lq, r2 % p.Lq) + j) : 0.f;
+      const float pe = vis ? exp2f(s * p.scale_log2 + mv - sm.lse2[r2]) : 0.f;
       sm.pr[r2][jj] = pe;
       sm.dsr[r2][jj] = pe * (dp - sm.delta[r2]);
     }

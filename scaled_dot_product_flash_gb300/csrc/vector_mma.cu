@@ -191,6 +191,7 @@ __global__ void __launch_bounds__(128) vec_mma_fwd_kernel(const __grid_constant_
           const int ir = e < 2 ? i0 : i1, rr = e < 2 ? r0 : r1;
           const bool vis = j < j_end && rr < R && (!p.causal || j <= ir + p.coff);
           x[nt][e] = vis ? sc[nt][e] * c2 : ninf();
+          if (vis && p.mask) x[nt][e] += mask_log2<T>(p, row_off(p.lm, b, g * p.G + rr / p.Lq, ir) + j);
         }
       float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
       float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
@@ -332,8 +333,9 @@ __global__ void __launch_bounds__(128) vec_mma_fwd_kernel(const __grid_constant_
     }
     const int64_t row = q_row(p, b, g * p.G + r / p.Lq, r % p.Lq);
     const float a = fold_sink(p, g * p.G + r / p.Lq, M, Lsum);
-    row_ptr<T>(p.out, p.lo, b, g * p.G + r / p.Lq, r % p.Lq)[d] = Elem<T>::from_f(O * a / Lsum);
-    if (p.lse && d == 0) p.lse[row] = (M + __log2f(Lsum)) * kLn2;
+    // A row that sees no key (only a mask can do that): O = 0, lse = −inf.
+    row_ptr<T>(p.out, p.lo, b, g * p.G + r / p.Lq, r % p.Lq)[d] = Elem<T>::from_f(Lsum > 0.f ? O * a / Lsum : 0.f);
+    if (p.lse && d == 0) p.lse[row] = Lsum > 0.f ? (M + __log2f(Lsum)) * kLn2 : ninf();
   }
   cluster.sync();  // peers may still be reading this block's shared memory
   (void)ok;
@@ -469,7 +471,8 @@ __global__ void __launch_bounds__(128) vec_mma_bwd_kernel(const __grid_constant_
         const T* op = row_ptr<T>(p.o, p.lo, b, h2, i2);
         const T* dop = row_ptr<T>(p.dout, p.ldo, b, h2, i2);
         for (int d = lane; d < D; d += 32) acc = fmaf(Elem<T>::to_f(op[d]), Elem<T>::to_f(dop[d]), acc);
-        nl = -p.lse[row] * kLog2e;
+        const float l = p.lse[row];
+        nl = l == ninf() ? ninf() : -l * kLog2e;  // no visible key: P = 0
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -531,7 +534,12 @@ __global__ void __launch_bounds__(128) vec_mma_bwd_kernel(const __grid_constant_
           const int j = tile_key0 + kl + (e & 1);
           const bool first = e < 2;
           const bool vis = j < j_end && (!p.causal || j <= (first ? ia : ib) + p.coff);
-          const float x = fmaf(sc[nt][e], c2, first ? nla : nlb);
+          float x = fmaf(sc[nt][e], c2, first ? nla : nlb);
+          if (vis && p.mask && (first ? ra : rb) < R) {
+            const int rr = first ? ra : rb;
+            const float mv = mask_log2<T>(p, row_off(p.lm, b, g * p.G + rr / p.Lq, rr % p.Lq) + j);
+            x = fmaf(sc[nt][e], c2, mv) + (first ? nla : nlb);
+          }
           pv[e] = vis ? ex2(x) : 0.f;
           dsv[e] = pv[e] * (dp[nt][e] + (first ? nda : ndb));
         }

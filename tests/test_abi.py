@@ -209,3 +209,38 @@ def test_forward_sinks_rejects(lib, sinks):
 ])
 def test_backward_sinks_rejects(lib, sinks, dsinks):
     assert bwd_sinks(sinks, dsinks) == INVALID
+
+
+# ---- masked entry points: every case below is rejected before anything is launched.
+MK = 0x10000000 * 13
+
+
+def fwd_masked(ptr=MK, kind=1, batch=0, head=0, row=64):
+    a = GOOD
+    m = _lib.Mask(ptr, kind, batch, head, row)
+    return _lib.sdpa_fwd_masked(Q, K, V, O, L, None, m, a["B"], a["Hq"], a["Hkv"], a["Lq"],
+                                a["Lkv"], a["D"], a["scale"], a["causal"], a["dtype"],
+                                _all_cont(), None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(kind=3),                  # unknown kind
+    dict(kind=-1),
+    dict(ptr=0),                   # no pointer with a mask kind
+    dict(ptr=MK + 8),              # misaligned
+    dict(row=8),                   # bool row stride of 8 bytes
+    dict(kind=2, row=4),           # additive bf16 row stride of 8 bytes
+    dict(head=-64),                # negative stride
+    dict(ptr=O + 4096),            # inside out
+    dict(ptr=L),                   # inside lse
+])
+def test_forward_masked_rejects(lib, kw):
+    assert fwd_masked(**kw) == INVALID
+
+
+def test_backward_masked_rejects_a_mask_inside_an_output(lib):
+    a = GOOD
+    m = _lib.Mask(DK + 1024, 1, 0, 0, 64)
+    assert _lib.sdpa_bwd_masked(Q, K, V, O, DO, L, None, m, DQ, DK, DV, None, a["B"], a["Hq"],
+                                a["Hkv"], a["Lq"], a["Lkv"], a["D"], a["scale"], a["causal"],
+                                a["dtype"], _all_cont(), WS, 1 << 20, None) == INVALID

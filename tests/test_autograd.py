@@ -21,10 +21,13 @@ def _cpu(shape=(1, 2, 8, 32)):
     return torch.zeros(shape)
 
 
-def test_rejects_masks_and_dropout():
+def test_rejects_mask_gradients_and_dropout():
     q = k = v = _cpu()
     with pytest.raises(NotImplementedError):
-        sa.scaled_dot_product_attention(q, k, v, attn_mask=torch.ones(8, 8, dtype=torch.bool))
+        sa.scaled_dot_product_attention(q, k, v, attn_mask=torch.zeros(8, 8, requires_grad=True))
+    with pytest.raises(ValueError):
+        sa.scaled_dot_product_attention(q, k, v, attn_mask=torch.ones(8, 8, dtype=torch.bool),
+                                        is_causal=True)
     with pytest.raises(NotImplementedError):
         sa.scaled_dot_product_attention(q, k, v, dropout_p=0.1)
     with pytest.raises(NotImplementedError):
