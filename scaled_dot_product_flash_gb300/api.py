@@ -70,6 +70,17 @@ def _check_sinks(name, t, Hq):
         raise ValueError(f"{name} must be a 1-D fp32 tensor of Hq = {Hq} sink logits")
 
 
+def _mask_layout(shape, strides, elem_size, ptr, Lkv):
+    """Whether a 4-D mask view (shape, element strides, element size, address) can be
+    passed to the library as it is, and its (batch, head, row) strides with 0 for the
+    broadcast (size-1) dimensions.  It can if its keys are contiguous and fill whole
+    16-byte pieces and every row starts on a 16-byte boundary."""
+    direct = (shape[3] == Lkv and strides[3] == 1 and (Lkv * elem_size) % 16 == 0
+              and ptr % 16 == 0
+              and all(shape[a] == 1 or (strides[a] * elem_size) % 16 == 0 for a in range(3)))
+    return direct, tuple(0 if shape[a] == 1 else strides[a] for a in range(3))
+
+
 def _mask_arg(attn_mask, q, Lq, Lkv):
     """(Mask struct or None, tensor to keep alive) for an attention mask broadcastable to
     [B, Hq, Lq, Lkv]: boolean (True keeps the key) or floating (added to the scores).
@@ -97,15 +108,13 @@ def _mask_arg(attn_mask, q, Lq, Lkv):
     else:
         raise ValueError("attn_mask must be boolean or floating point")
     es = m.element_size()
-    direct = (m.shape[3] == Lkv and m.stride(3) == 1 and (Lkv * es) % 16 == 0
-              and m.data_ptr() % 16 == 0
-              and all(m.shape[a] == 1 or (m.stride(a) * es) % 16 == 0 for a in range(3)))
+    direct, strides = _mask_layout(m.shape, m.stride(), es, m.data_ptr(), Lkv)
     if not direct:
         pad = (Lkv * es + 15) // 16 * 16 // es
         buf = torch.zeros(tuple(m.shape[:3]) + (pad,), device=m.device, dtype=m.dtype)
         buf[..., :Lkv] = m
         m = buf
-    strides = [0 if m.shape[a] == 1 else m.stride(a) for a in range(3)]
+        _, strides = _mask_layout(m.shape, m.stride(), es, m.data_ptr(), pad)
     return _lib.Mask(m.data_ptr(), kind, *strides), m
 
 
