@@ -44,7 +44,8 @@
  *    return SDPA_ERR_INVALID_ARG or SDPA_ERR_UNSUPPORTED; a failed launch returns
  *    SDPA_ERR_CUDA.  Kernels never trap: a wait that runs out of its iteration limit sets
  *    the device error word and the kernel returns; sdpa_poll_status reports it.
- *  - Supported: dtype in {SDPA_F32, SDPA_F16, SDPA_BF16}; D in {32, 64, 96, 128};
+ *  - Supported: dtype in {SDPA_F32, SDPA_F16, SDPA_BF16}; D in {32, 64, 96, 128, 256}
+ *    (D = 256 runs on the CUDA-core tiled kernels for every dtype);
  *    B, Hq, Hkv, Lq, Lkv >= 1; Hq % Hkv == 0; Hq, B <= 65535; scale finite (0 allowed).
  */
 #ifndef SDPA_GB300_H

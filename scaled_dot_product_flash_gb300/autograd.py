@@ -11,7 +11,7 @@ the package, this module only marshals tensors; all arithmetic runs in ``libsdpa
 Supported: q [B, Hq, Lq, D], k and v [B, Hkv, Lkv, D] on CUDA (any layout whose rows are
 contiguous, e.g. [B, L, H, D] storage through .transpose(1, 2)), one dtype of fp32/fp16/bf16,
 Hq a multiple of Hkv (grouped-query attention: query head h uses KV head h // (Hq/Hkv)),
-D in {32, 64, 96, 128}, optional top-left causal mask or ``attn_mask`` (boolean: True keeps
+D in {32, 64, 96, 128, 256}, optional top-left causal mask or ``attn_mask`` (boolean: True keeps
 the key; floating: added to the scores; no gradient flows into it), any finite scale,
 optional per-head attention-sink logits (``sinks``, differentiable).  Dropout and other
 head layouts raise ``NotImplementedError``.

@@ -110,7 +110,7 @@ int check_sizes(int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale, int
   if (Hq % Hkv != 0) return SDPA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return SDPA_ERR_INVALID_ARG;
   if (dtype != SDPA_F32 && dtype != SDPA_F16 && dtype != SDPA_BF16) return SDPA_ERR_UNSUPPORTED;
-  if (D != 32 && D != 64 && D != 96 && D != 128) return SDPA_ERR_UNSUPPORTED;
+  if (D != 32 && D != 64 && D != 96 && D != 128 && D != 256) return SDPA_ERR_UNSUPPORTED;
   if (B > 65535 || Hq > 65535) return SDPA_ERR_UNSUPPORTED;
   // Keep every element index comfortably inside int64 (and far above any real HBM size).
   const double qe = (double)B * Hq * Lq * D, ke = (double)B * Hkv * Lkv * D;

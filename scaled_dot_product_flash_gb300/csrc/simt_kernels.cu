@@ -19,7 +19,12 @@ namespace {
 constexpr int kRows = 32;
 constexpr int kTpr = 4;
 constexpr int kThreads = kRows * kTpr;
-constexpr int kTile = 32;
+// Rows of K/V (or Q/dO) staged per step: 32, or 16 for D = 256 so that the two fp32 tiles
+// stay within the 48 KB of static shared memory.
+template <int D>
+struct TileRows {
+  static constexpr int value = D > 128 ? 16 : 32;
+};
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
 __device__ __forceinline__ float reduce4(float x) {
@@ -28,11 +33,11 @@ __device__ __forceinline__ float reduce4(float x) {
   return x;
 }
 
-// Cooperative load of rows [r0, r0 + kTile) of a slab of rows `rs` elements apart into
-// fp32 smem; rows at or beyond `nrows` are zero.
+// Cooperative load of rows [r0, r0 + TileRows<D>) of a slab of rows `rs` elements apart
+// into fp32 smem; rows at or beyond `nrows` are zero.
 template <typename T, int D>
 __device__ __forceinline__ void load_tile(float (*dst)[D], const T* src, int64_t rs, int r0, int nrows) {
-  for (int e = threadIdx.x; e < kTile * D; e += kThreads) {
+  for (int e = threadIdx.x; e < TileRows<D>::value * D; e += kThreads) {
     const int rr = e / D, d = e % D;
     const int r = r0 + rr;
     dst[rr][d] = r < nrows ? Elem<T>::to_f(src[(int64_t)r * rs + d]) : 0.f;
@@ -42,6 +47,7 @@ __device__ __forceinline__ void load_tile(float (*dst)[D], const T* src, int64_t
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Problem p) {
   constexpr int DPT = D / kTpr;
+  constexpr int kTile = TileRows<D>::value;
   __shared__ float ks[kTile][D];
   __shared__ float vs[kTile][D];
   const int r = threadIdx.x / kTpr, sub = threadIdx.x % kTpr;
@@ -109,6 +115,7 @@ __global__ void __launch_bounds__(kThreads) simt_fwd_kernel(Problem p) {
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) simt_dq_kernel(Problem p) {
   constexpr int DPT = D / kTpr;
+  constexpr int kTile = TileRows<D>::value;
   __shared__ float ks[kTile][D];
   __shared__ float vs[kTile][D];
   const int r = threadIdx.x / kTpr, sub = threadIdx.x % kTpr;
@@ -169,6 +176,7 @@ __global__ void __launch_bounds__(kThreads) simt_dq_kernel(Problem p) {
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) simt_dkdv_kernel(Problem p) {
   constexpr int DPT = D / kTpr;
+  constexpr int kTile = TileRows<D>::value;
   __shared__ float qs[kTile][D];
   __shared__ float dos[kTile][D];
   __shared__ float lse2s[kTile];
@@ -366,6 +374,7 @@ cudaError_t delta_t(const Problem& p, cudaStream_t s) {
           case 64: return FN<float, 64>(p, s);                                      \
           case 96: return FN<float, 96>(p, s);                                      \
           case 128: return FN<float, 128>(p, s);                                    \
+          case 256: return FN<float, 256>(p, s);                                    \
         }                                                                           \
         break;                                                                      \
       case 1:                                                                       \
@@ -374,6 +383,7 @@ cudaError_t delta_t(const Problem& p, cudaStream_t s) {
           case 64: return FN<__half, 64>(p, s);                                     \
           case 96: return FN<__half, 96>(p, s);                                     \
           case 128: return FN<__half, 128>(p, s);                                   \
+          case 256: return FN<__half, 256>(p, s);                                   \
         }                                                                           \
         break;                                                                      \
       case 2:                                                                       \
@@ -382,6 +392,7 @@ cudaError_t delta_t(const Problem& p, cudaStream_t s) {
           case 64: return FN<__nv_bfloat16, 64>(p, s);                              \
           case 96: return FN<__nv_bfloat16, 96>(p, s);                              \
           case 128: return FN<__nv_bfloat16, 128>(p, s);                            \
+          case 256: return FN<__nv_bfloat16, 256>(p, s);                            \
         }                                                                           \
         break;                                                                      \
     }                                                                               \

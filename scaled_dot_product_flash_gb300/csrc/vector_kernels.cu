@@ -458,7 +458,7 @@ cudaError_t vec_any(const Problem& p, int dtype, cudaStream_t s) {
 
 bool vector_supported(const Problem& p, int dtype) {
   (void)dtype;
-  return p.Lq <= 8 && p.G * p.Lq <= 32;
+  return p.Lq <= 8 && p.G * p.Lq <= 32 && p.D <= 128;  // D = 256 runs on the tiled CUDA-core path
 }
 
 cudaError_t launch_vector_fwd(const Problem& p, int dtype, cudaStream_t s) { return vec_any<true>(p, dtype, s); }

@@ -85,7 +85,7 @@ INVALID, UNSUPPORTED, WORKSPACE = 1, 2, 5
     (dict(scale=float("nan")), INVALID),
     (dict(scale=float("inf")), INVALID),
     (dict(D=48), UNSUPPORTED),
-    (dict(D=256), UNSUPPORTED),
+    (dict(D=512), UNSUPPORTED),
     (dict(dtype=3), UNSUPPORTED),
     (dict(B=70000), UNSUPPORTED),
     (dict(o=Q + 64), INVALID),                # out overlaps q

@@ -148,6 +148,26 @@ def test_forced_family_refuses_what_it_cannot_serve():
         assert e.value.status == 2
 
 
+# ------------------------------------------------------------------ head dim 256
+@pytest.mark.parametrize("shape,dtype,causal", [
+    (Shape(1, 2, 1, 40, 70, 256), "f32", True),        # CUDA cores, GQA, ragged
+    (Shape(1, 4, 2, 100, 130, 256), "bf16", True),     # 16-bit types also run on CUDA cores
+    (Shape(2, 4, 2, 4, 90, 256), "f16", False),        # short query: no short-query kernel
+    (Shape(1, 2, 2, 33, 64, 256), "bf16", 2),          # bottom-right causal
+])
+def test_head_dim_256(shape, dtype, causal):
+    full_parity(shape, dtype, causal, seed=31)
+
+
+def test_head_dim_256_is_refused_by_the_tensor_and_short_query_paths():
+    q = torch.zeros(1, 2, 4, 256, device="cuda", dtype=torch.bfloat16)
+    for path in (_lib.PATH_TENSOR, _lib.PATH_VECTOR):
+        with api.force_path(path):
+            with pytest.raises(_lib.SdpaError) as e:
+                api.attention_forward(q, q, q)
+            assert e.value.status == 2
+
+
 # ------------------------------------------------------------------ properties
 @pytest.mark.parametrize("shape,dtype,causal", [
     (Shape(1, 8, 2, 600, 600, 128), "bf16", True),
