@@ -269,16 +269,17 @@ const char* sdpa_status_string(int status);
 
 /*
  * Kernel family selection, for tests and measurements.  SDPA_PATH_AUTO (the default)
- * picks by shape and dtype: the vector path when Lq <= 8 and (Hq/Hkv)·Lq <= 32, else the
- * tensor-core tiled path for fp16/bf16 with D in {64, 128}, else the CUDA-core tiled path.
+ * picks by shape and dtype: the vector path when Lq <= 8, (Hq/Hkv)·Lq <= 32 and D <= 128, else the
+ * tensor-core tiled path for fp16/bf16 with D in {32, 64, 96, 128}, else the CUDA-core tiled
+ * path (every dtype, D up to 256).
  * A forced path that cannot serve a call makes that call return SDPA_ERR_UNSUPPORTED.
  * Process-wide setting; not thread-safe against concurrent calls.
  */
 typedef enum {
   SDPA_PATH_AUTO = 0,
-  SDPA_PATH_TENSOR = 1,  /* TMA + tcgen05 tiled kernels (fp16/bf16, D in {64,128}) */
+  SDPA_PATH_TENSOR = 1,  /* TMA + tcgen05 tiled kernels (fp16/bf16, D in {32,64,96,128}) */
   SDPA_PATH_SIMT = 2,    /* CUDA-core (FFMA) tiled kernels, every dtype and D */
-  SDPA_PATH_VECTOR = 3   /* short-query kernels (Lq <= 8, (Hq/Hkv)·Lq <= 32) */
+  SDPA_PATH_VECTOR = 3   /* short-query kernels (Lq <= 8, (Hq/Hkv)·Lq <= 32, D <= 128) */
 } sdpa_path_t;
 int sdpa_set_path(int path); /* SDPA_OK, or SDPA_ERR_INVALID_ARG for an unknown path */
 

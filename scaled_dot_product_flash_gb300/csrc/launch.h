@@ -6,7 +6,7 @@
 
 namespace sdpa {
 
-// CUDA-core tiled path: every dtype, D in {32, 64, 96, 128}.
+// CUDA-core tiled path: every dtype, D in {32, 64, 96, 128, 256}.
 cudaError_t launch_simt_fwd(const Problem& p, int dtype, cudaStream_t s);
 cudaError_t launch_simt_dq(const Problem& p, int dtype, cudaStream_t s);
 cudaError_t launch_simt_dkdv(const Problem& p, int dtype, cudaStream_t s);
@@ -26,7 +26,7 @@ bool vector_mma_supported(const Problem& p, int dtype);
 cudaError_t launch_vector_mma_fwd(const Problem& p, int dtype, cudaStream_t s);
 cudaError_t launch_vector_mma_bwd(const Problem& p, int dtype, cudaStream_t s);
 
-// Tensor-core path (TMA + tcgen05), fp16/bf16 with D in {64, 128}.
+// Tensor-core path (TMA + tcgen05), fp16/bf16 with D in {32, 64, 96, 128}.
 bool tensor_supported(const Problem& p, int dtype);
 bool tensor_bwd_supported(const Problem& p, int dtype);
 cudaError_t launch_tc_fwd(const Problem& p, int dtype, cudaStream_t s);

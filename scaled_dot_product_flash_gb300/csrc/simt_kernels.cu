@@ -1,7 +1,7 @@
 // CUDA-core (FFMA) tiled kernels: forward, dQ, dK/dV and the δ pre-pass.
 //
 // These serve fp32 inputs exactly (fp32 products and sums, no reduced-precision
-// operands) and every head dim in {32, 64, 96, 128}.  They follow the same algorithm as
+// operands) and every head dim in {32, 64, 96, 128, 256}.  They follow the same algorithm as
 // the tensor-core path: online softmax in the log2 domain for the forward, P recomputed
 // from the cached logsumexp for the backward, a dQ kernel that loops over KV blocks, and
 // a dK/dV kernel in which each thread block owns its KV rows and loops over the query
@@ -10,7 +10,8 @@
 //
 // Thread mapping: a block of 128 threads owns 32 rows; 4 neighbouring threads share a
 // row, each holding every 4th element of it, and dot products are finished with two
-// xor-shuffles.  K/V (or Q/dO) tiles of 32 rows are staged in shared memory as fp32.
+// xor-shuffles.  K/V (or Q/dO) tiles of 32 rows (16 at D = 256) are staged in shared
+// memory as fp32.
 #include "launch.h"
 
 namespace sdpa {
