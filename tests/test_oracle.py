@@ -52,8 +52,18 @@ def test_closed_form_fixtures(case):
     v = np.array(case["v"])
     do = np.array(case["dout"])
     assert np.allclose(k, np.array(case["k"]), atol=1e-15)
-    o, lse = oracle.sdpa_forward(q, k, v, case["scale"], case["is_causal"])
-    dq, dk, dv = oracle.sdpa_backward(q, k, v, do, case["scale"], case["is_causal"])
+    kw = {}
+    if "sinks_exact" in case:
+        kw["sinks"] = np.array(_exact(case["sinks_exact"]))
+    if "mask_bool" in case:
+        kw["mask"] = np.array(case["mask_bool"], dtype=bool)
+    if "mask_exact" in case:
+        kw["mask"] = np.array(_exact(case["mask_exact"]))
+    o, lse = oracle.sdpa_forward(q, k, v, case["scale"], case["is_causal"], **kw)
+    grads = oracle.sdpa_backward(q, k, v, do, case["scale"], case["is_causal"], **kw)
+    dq, dk, dv = grads[:3]
+    if "dsinks" in case:
+        np.testing.assert_allclose(grads[3], np.array(_exact(case["dsinks"])), atol=1e-13)
     np.testing.assert_allclose(o, np.array(_exact(case["o"])), atol=1e-13)
     np.testing.assert_allclose(lse, np.array(_exact(case["lse"])), atol=1e-13)
     np.testing.assert_allclose(dq, np.array(_exact(case["dq"])), atol=1e-13)
