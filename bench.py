@@ -52,6 +52,22 @@ def fwd_flops(B, Hq, Hkv, Lq, Lkv, D, causal):
     return f / 2 if causal else f
 
 
+def slowest_rank(values, dist, device):
+    """Element-wise maximum over the ranks of a list of times (ms): a job of replicas takes
+    as long as its slowest replica.  Without a process group (dist None) the values come
+    back as they are."""
+    import torch
+    t = torch.tensor(values, device=device, dtype=torch.float64)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_tflops(world, flops_per_step, steps, total_ms):
+    """Whole-job throughput: the work of all `world` replicas over the slowest one's time."""
+    return world * flops_per_step * steps / (total_ms / 1e3) / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -293,15 +309,13 @@ def main():
 
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     fwd_ms = [s.elapsed_time(m) for s, m in zip(starts, mids)]
-    tot = torch.tensor([sum(step_ms), sum(fwd_ms)], device=dev, dtype=torch.float64)
-    if world > 1:
-        dist.all_reduce(tot, op=dist.ReduceOp.MAX)
-    total_ms, total_fwd_ms = float(tot[0]), float(tot[1])
+    total_ms, total_fwd_ms = slowest_rank([sum(step_ms), sum(fwd_ms)],
+                                          dist if world > 1 else None, dev)
     ms_per_step = total_ms / args.steps
     F = fwd_flops(**W, causal=CAUSAL)
     step_flops = 3.5 * F
-    value = world * step_flops * args.steps / (total_ms / 1e3) / 1e12
-    fwd_tflops = world * F * args.steps / (total_fwd_ms / 1e3) / 1e12
+    value = job_tflops(world, step_flops, args.steps, total_ms)
+    fwd_tflops = job_tflops(world, F, args.steps, total_fwd_ms)
 
     peaks, peak_src = load_peaks()
     bf16_peak = peaks["bf16_tflops"]
@@ -467,14 +481,10 @@ def run_e2e(torch, api, dev, stream, host_inputs, scale, steps, step_flops, worl
     run(n, e0, e1)
     torch.cuda.synchronize()
     barrier()
-    ms = e0.elapsed_time(e1)
-    t = torch.tensor([ms], device=dev, dtype=torch.float64)
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms = float(t[0])
+    (ms,) = slowest_rank([e0.elapsed_time(e1)], dist, dev)
     h2d = sum(t.numel() * t.element_size() for t in pin)
     d2h = sum(t.numel() * t.element_size() for t in outs_h)
-    return {"value": world * step_flops * n / (ms / 1e3) / 1e12, "unit": "TFLOP/s",
+    return {"value": job_tflops(world, step_flops, n, ms), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / n,
             "steps": n, "pipelined": "copy-in / compute / copy-out streams, 2 buffer sets"}
 
