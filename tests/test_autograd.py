@@ -46,6 +46,14 @@ def test_rejects_gqa_without_flag_and_bad_groups():
         sa.scaled_dot_product_attention(q, kv, kv, enable_gqa=True, scale=float("inf"))
 
 
+def test_rejects_malformed_sinks():
+    q = k = v = _cpu()
+    with pytest.raises(ValueError):
+        sa.scaled_dot_product_attention(q, k, v, sinks=torch.zeros(3))        # not Hq values
+    with pytest.raises(ValueError):
+        sa.scaled_dot_product_attention(q, k, v, sinks=torch.zeros(2, 1))     # not 1-D
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("shape,dtype,causal", [
     (Shape(2, 8, 2, 200, 200, 128), "bf16", True),    # tensor-core path, GQA, ragged tail
