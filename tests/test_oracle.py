@@ -316,6 +316,32 @@ def test_matches_torch_cpu_float64():
         np.testing.assert_allclose(dv, tv.grad.numpy(), atol=1e-12)
 
 
+def test_masks_match_torch_cpu_float64():
+    """Second opinion for the mask reading: torch's CPU SDPA in float64 with the same
+    boolean and additive attn_mask (no row fully hidden, where torch's conventions vary)."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    rng = np.random.default_rng(14)
+    q, k, v, do = make(rng, B=2, Hq=4, Hkv=2, Lq=7, Lkv=9, D=8)
+    boolean = rng.random((2, 1, 7, 9)) < 0.6
+    boolean[..., 0] = True
+    additive = rng.standard_normal((4, 7, 9))
+    additive[rng.random(additive.shape) < 0.2] = -np.inf
+    additive[..., 1] = 0.0
+    for mask in (boolean, additive):
+        tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+        o = F.scaled_dot_product_attention(tq, tk.repeat_interleave(2, dim=1),
+                                           tv.repeat_interleave(2, dim=1),
+                                           attn_mask=torch.tensor(mask), scale=0.35)
+        o.backward(torch.tensor(do))
+        oo, _ = oracle.sdpa_forward(q, k, v, 0.35, False, mask=mask)
+        dq, dk, dv = oracle.sdpa_backward(q, k, v, do, 0.35, False, mask=mask)
+        np.testing.assert_allclose(oo, o.detach().numpy(), atol=1e-12)
+        np.testing.assert_allclose(dq, tq.grad.numpy(), atol=1e-12)
+        np.testing.assert_allclose(dk, tk.grad.numpy(), atol=1e-12)
+        np.testing.assert_allclose(dv, tv.grad.numpy(), atol=1e-12)
+
+
 # ----------------------------------------------------------------- bottom-right causal
 def test_bottom_right_equals_padded_top_left(impl=None):
     """The bottom-right mask (key j hidden from query i when j > i + Lkv - Lq) is the
