@@ -852,6 +852,36 @@ def _mutant(name):
             lse = (mx + np.log(l))[:, 0]
             return (p, lse, (es / l)[:, 0]) if sink is not None else (p, lse)
         m._softmax_rows = _softmax_rows
+    elif name == "mask_as_large_finite_negative":
+        # hiding keys with -1e9 instead of -inf: a row that sees no key becomes uniform
+        orig = m._mask_values
+
+        def _mask_values(mask):
+            return np.maximum(orig(mask), -1e9)
+        m._mask_values = _mask_values
+    elif name == "mask_subtracted":
+        def _scores(q_rows, k, scale, offset, row_idx, mask_rows=None):
+            s = (q_rows @ k.T) * scale
+            if mask_rows is not None:
+                s = s - np.where(np.isneginf(mask_rows), np.inf, mask_rows)
+            if offset is not None:
+                j = np.arange(k.shape[0])[None, :]
+                s = np.where(j > np.asarray(row_idx)[:, None] + offset, -np.inf, s)
+            return s
+        m._scores = _scores
+    elif name == "sink_gradient_without_delta":
+        orig = m.head_backward
+
+        def head_backward(q, k, v, dout, scale, is_causal, row_block=None, sink=None, mask=None):
+            r = orig(q, k, v, dout, scale, is_causal, row_block, sink, mask)
+            if sink is None:
+                return r
+            q64, k64 = np.asarray(q, float), np.asarray(k, float)
+            off = m._causal_offset(is_causal, q64.shape[0], k64.shape[0])
+            mv = None if mask is None else np.broadcast_to(m._mask_values(mask), (q64.shape[0], k64.shape[0]))
+            sm = m._softmax_rows(m._scores(q64, k64, scale, off, np.arange(q64.shape[0]), mv), sink)
+            return r[:3] + (-float(sm[2].sum()),)
+        m.head_backward = head_backward
     else:
         raise KeyError(name)
     return m
@@ -861,7 +891,9 @@ def _mutant(name):
                                   "no_scale_in_dq", "delta_dropped", "dk_transposed_operand",
                                   "bottom_right_offset_off_by_one", "sink_missing_from_lse",
                                   "sink_gradient_sign", "sink_given_a_value", "mask_scaled",
-                                  "bool_mask_inverted", "mask_by_kv_head", "masked_row_nan"])
+                                  "bool_mask_inverted", "mask_by_kv_head", "masked_row_nan",
+                                  "mask_as_large_finite_negative", "mask_subtracted",
+                                  "sink_gradient_without_delta"])
 def test_planted_mistakes_are_caught(name):
     mutant = _mutant(name)
     failures = 0
