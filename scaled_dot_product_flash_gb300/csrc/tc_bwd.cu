@@ -26,6 +26,12 @@
 // (warpgroup w owns columns [64w, 64w+64) and writes its packed results to its own
 // columns [64w, 64w+32)), warp 8 is the TMA producer, warps 9 and 10 issue the MMAs (two
 // independent chains each) and warp 9 owns the 512 TMEM columns.
+//
+// Attention masks: both kernels have a masked instantiation (kMasked) that adds log2e·M
+// to the log2-domain scores before the exponential (the dK/dV kernel reads one mask value
+// per (query, key), coalesced over the warp's 32 keys; the dQ kernel reads its row's 64
+// values in 16-byte pieces).  A row whose lse is −inf (it saw no key) gets P = 0.  Sinks
+// need no change here: the forward's lse already includes them.
 #include "launch.h"
 #include "tc_common.cuh"
 
