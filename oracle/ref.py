@@ -136,8 +136,12 @@ def _softmax_rows(s, sink=None):
     with np.errstate(divide="ignore", invalid="ignore"):
         p = np.where(l > 0, e / l, 0.0)
         lse = (m + np.log(l))[:, 0]
+        if sink is not None:
+            # A sink of -inf is no sink: with every key hidden too, the row is empty and
+            # the sink's share is 0 like every other entry's.
+            p_sink = np.where(l > 0, es / l, 0.0)[:, 0]
     if sink is not None:
-        return p, lse, (es / l)[:, 0]
+        return p, lse, p_sink
     return p, lse
 
 

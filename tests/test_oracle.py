@@ -645,6 +645,18 @@ def test_fully_masked_row(impl=None):
     o, lse = impl.sdpa_forward(q, k, v, 0.7, False, mask=mask, sinks=sinks)
     np.testing.assert_array_equal(o[:, :, 3], 0.0)
     np.testing.assert_allclose(lse[0, :, 3], sinks, atol=1e-15)
+    # A sink of -inf is no sink, also on the row that sees nothing: every output is the
+    # no-sink one and the sink's gradient is exactly 0 (no 0/0 from the empty row).
+    sinks = np.array([-np.inf, -np.inf])
+    with np.errstate(all="raise"):
+        o, lse = impl.sdpa_forward(q, k, v, 0.7, False, mask=mask, sinks=sinks)
+        r = impl.sdpa_backward(q, k, v, do, 0.7, False, mask=mask, sinks=sinks)
+    np.testing.assert_array_equal(o[:, :, 3], 0.0)
+    assert np.all(lse[:, :, 3] == -np.inf)
+    np.testing.assert_allclose(r[0], dq, atol=1e-14)
+    np.testing.assert_allclose(r[1], dk, atol=1e-14)
+    np.testing.assert_allclose(r[2], dv, atol=1e-14)
+    np.testing.assert_array_equal(r[3], 0.0)
 
 
 MASK_FD_CASES = [
@@ -852,6 +864,24 @@ def _mutant(name):
             lse = (mx + np.log(l))[:, 0]
             return (p, lse, (es / l)[:, 0]) if sink is not None else (p, lse)
         m._softmax_rows = _softmax_rows
+    elif name == "empty_row_sink_share_nan":
+        # the sink's share of a row with no finite entry left as 0/0
+        def _softmax_rows(s, sink=None):
+            mx = s.max(axis=1, keepdims=True)
+            if sink is not None:
+                mx = np.maximum(mx, sink)
+            mx = np.where(np.isfinite(mx), mx, 0.0)
+            e = np.exp(s - mx)
+            l = e.sum(axis=1, keepdims=True)
+            if sink is not None:
+                es = np.exp(sink - mx)
+                l = l + es
+            with np.errstate(divide="ignore", invalid="ignore"):
+                p = np.where(l > 0, e / l, 0.0)
+                lse = (mx + np.log(l))[:, 0]
+                share = (es / l)[:, 0] if sink is not None else None
+            return (p, lse, share) if sink is not None else (p, lse)
+        m._softmax_rows = _softmax_rows
     elif name == "mask_as_large_finite_negative":
         # hiding keys with -1e9 instead of -inf: a row that sees no key becomes uniform
         orig = m._mask_values
@@ -892,7 +922,7 @@ def _mutant(name):
                                   "bottom_right_offset_off_by_one", "sink_missing_from_lse",
                                   "sink_gradient_sign", "sink_given_a_value", "mask_scaled",
                                   "bool_mask_inverted", "mask_by_kv_head", "masked_row_nan",
-                                  "mask_as_large_finite_negative", "mask_subtracted",
+                                  "mask_as_large_finite_negative", "mask_subtracted", "empty_row_sink_share_nan",
                                   "sink_gradient_without_delta"])
 def test_planted_mistakes_are_caught(name):
     mutant = _mutant(name)
