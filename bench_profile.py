@@ -1,20 +1,26 @@
+#!/usr/bin/env python
 """Run one SDPA operation repeatedly on one synthetic case, for profilers (ncu) and quick
 timing.  Every launch goes through the C ABI exactly as in normal use.
 
-  python -m scaled_dot_product_flash_gb300.profile_case --op fwd|bwd|step \\
+  python bench_profile.py --op fwd|bwd|step \\
       --B 2 --Hq 32 --Hkv 8 --L 4096 --D 128 --dtype bf16 --causal --iters 4
 
-Prints the mean CUDA-event time per call (after one warm-up call).
+--L is Lq (and Lkv unless --Lkv is given).  Prints the mean CUDA-event time per call
+(after one warm-up call).
 """
 from __future__ import annotations
 
 import argparse
 import math
+import os
+import sys
 
 import torch
 
-from . import _lib, api
-from .inputs import Shape, draw
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+
+from scaled_dot_product_flash_gb300 import _lib, api  # noqa: E402
+from scaled_dot_product_flash_gb300.inputs import Shape, draw  # noqa: E402
 
 
 def main():

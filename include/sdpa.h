@@ -244,7 +244,9 @@ int sdpa_bwd_masked(const void* q, const void* k, const void* v, const void* out
  *  - Limit: B·Hq·Lq must not exceed SDPA_BWD_NOALLOC_MAX_ROWS; larger problems return
  *    SDPA_ERR_WORKSPACE before anything is launched (use sdpa_bwd with a workspace).
  *  - The first call on each device looks up the array's device address (with that device
- *    current); make that first call before any stream capture begins.
+ *    current); make that first call before any stream capture begins.  The address is
+ *    kept for the life of the process: the call assumes each device's primary context
+ *    (the one the CUDA runtime uses) and no cudaDeviceReset while the library is loaded.
  *  - Every call shares the one array and it keeps the previous call's contents.  The
  *    backward writes every δ it reads before reading it, so nothing needs clearing, but
  *    calls whose work overlaps on the GPU (other streams, other host threads) race on the

@@ -100,15 +100,20 @@ __host__ __device__ __forceinline__ int64_t q_row(const Problem& p, int b, int h
 __host__ __device__ __forceinline__ int64_t row_off(const Layout& l, int b, int h, int64_t i) {
   return (int64_t)b * l.sb + (int64_t)h * l.sh + i * l.sl;
 }
+__device__ __forceinline__ float minus_inf() { return __int_as_float(0xff800000); }
+
+
 // Attention sink of query head h: one more softmax entry per row with logit sinks[h] and
 // a zero value vector.  Folds it into a finished row whose running maximum m and sum l are
 // in the log2 domain (P = exp2(c·s − m)) and returns the factor a by which the row's
 // unnormalised output must be scaled before the division by the updated l (1 without a
 // sink, so the no-sink arithmetic is unchanged).  m and l then describe the row with the
-// sink, so lse = ln2·(m + log2 l) includes it.  A NaN sink gives NaN outputs.
+// sink, so lse = ln2·(m + log2 l) includes it.  A sink of −inf is no sink (also for a row
+// that saw no key, where m = −inf too).  A NaN sink gives NaN outputs.
 __device__ __forceinline__ float fold_sink(const Problem& p, int h, float& m, float& l) {
   if (!p.sinks) return 1.f;
   const float s2 = p.sinks[h] * kLog2e;
+  if (s2 == minus_inf()) return 1.f;
   if (s2 <= m) {
     l += exp2f(s2 - m);
     return 1.f;
@@ -118,8 +123,6 @@ __device__ __forceinline__ float fold_sink(const Problem& p, int h, float& m, fl
   m = s2;
   return a;
 }
-
-__device__ __forceinline__ float minus_inf() { return __int_as_float(0xff800000); }
 
 // Mask term of one (query row, key) pair in the log2 domain: log2e·M, or −inf for a key a
 // boolean mask hides.  `off` is the element offset of the pair in the mask.

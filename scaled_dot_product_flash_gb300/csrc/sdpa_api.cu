@@ -22,18 +22,27 @@ std::atomic<int> g_inject{0};
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 
 constexpr int kMaxDevices = 64;
-unsigned* g_err_ptr[kMaxDevices] = {};
+std::atomic<unsigned*> g_err_ptr[kMaxDevices];
+std::mutex g_err_mu;
 
-// Device address of the error word on the current device (looked up once per device).
+// Device address of the error word on the current device, looked up once per device (the
+// library assumes each device's primary context and no device reset while it is loaded).
+// Several host threads may call this at once.
 int error_word(unsigned** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SDPA_ERR_CUDA;
-  if (!g_err_ptr[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_device_error) != cudaSuccess) return SDPA_ERR_CUDA;
-    g_err_ptr[dev] = static_cast<unsigned*>(ptr);
+  unsigned* ptr = g_err_ptr[dev].load();
+  if (!ptr) {
+    std::lock_guard<std::mutex> lock(g_err_mu);
+    ptr = g_err_ptr[dev].load();
+    if (!ptr) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_device_error) != cudaSuccess || !addr) return SDPA_ERR_CUDA;
+      ptr = static_cast<unsigned*>(addr);
+      g_err_ptr[dev].store(ptr);
+    }
   }
-  *out = g_err_ptr[dev];
+  *out = ptr;
   return SDPA_OK;
 }
 

@@ -305,12 +305,22 @@ __global__ void __launch_bounds__(kDeltaThreads) delta_kernel(Problem p) {
 // −p_sink·δ with p_sink = exp(sink − lse) (lse includes the sink).  Summed over the batch
 // and the rows: dsink_h = −Σ_{b,i} exp(sink_h − lse_bhi)·δ_bhi.  One block per head; the
 // rows are split over the threads in a fixed order and reduced by a fixed tree, so the
-// result is the same bits on every run.
+// result is the same bits on every run.  A sink of −inf is no sink: its gradient is 0
+// (rows that saw no key have lse = −inf too, and exp(−inf − (−inf)) would be NaN).  Rows
+// with lse = −inf contribute nothing.
 constexpr int kSinkThreads = 256;
+
+__device__ __forceinline__ float sink_share(float sk, float lse) {
+  return lse == minus_inf() ? 0.f : expf(sk - lse);
+}
 
 __global__ void __launch_bounds__(kSinkThreads) sink_grad_kernel(Problem p) {
   const int h = blockIdx.x;
   const float sk = p.sinks[h];
+  if (sk == minus_inf()) {
+    if (threadIdx.x == 0) p.dsinks[h] = 0.f;
+    return;
+  }
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   for (int b = 0; b < p.B; ++b) {
     const float* lse = p.lse + q_row(p, b, h, 0);
@@ -319,9 +329,9 @@ __global__ void __launch_bounds__(kSinkThreads) sink_grad_kernel(Problem p) {
     for (; i + 3 * kSinkThreads < p.Lq; i += 4 * kSinkThreads) {
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        acc[u] = fmaf(expf(sk - lse[i + u * kSinkThreads]), dl[i + u * kSinkThreads], acc[u]);
+        acc[u] = fmaf(sink_share(sk, lse[i + u * kSinkThreads]), dl[i + u * kSinkThreads], acc[u]);
     }
-    for (; i < p.Lq; i += kSinkThreads) acc[0] = fmaf(expf(sk - lse[i]), dl[i], acc[0]);
+    for (; i < p.Lq; i += kSinkThreads) acc[0] = fmaf(sink_share(sk, lse[i]), dl[i], acc[0]);
   }
   float t = (acc[0] + acc[1]) + (acc[2] + acc[3]);
 #pragma unroll

@@ -112,6 +112,27 @@ def test_mask_with_sinks_and_causal():
     assert rel_frob(as_f64(g[3]), refs[3]) <= 1e-2
 
 
+@pytest.mark.parametrize("shape,dtype,path", [
+    (Shape(1, 4, 4, 96, 160, 64), "f16", _lib.PATH_AUTO),      # tensor cores
+    (Shape(1, 4, 2, 40, 70, 32), "f32", _lib.PATH_AUTO),       # CUDA cores
+    (Shape(2, 4, 2, 4, 300, 128), "bf16", _lib.PATH_AUTO),     # short query
+])
+def test_minus_infinity_sink_on_a_row_that_sees_no_key(shape, dtype, path):
+    """The additive mask hides one whole row of the last head, whose sink is −inf (no
+    sink): that head's sink gradient is exactly 0 and every sink gradient is finite and
+    matches the oracle."""
+    sinks = torch.tensor([2.5, -1.0, 0.5, -np.inf], dtype=torch.float32)
+    g, refs = run_case(shape, dtype, False, "additive", 131, path, sinks=sinks)
+    got = as_f64(g[3])
+    assert np.all(np.isfinite(got)), got
+    assert got[-1] == 0.0
+    if dtype == "f32":
+        assert float(np.max(np.abs(got - refs[3]))) <= 1e-4
+    else:
+        from parity_util import rel_frob
+        assert rel_frob(got, refs[3]) <= 1e-2
+
+
 def test_masked_autograd_matches_oracle():
     shape = Shape(1, 8, 2, 160, 224, 128)
     q, k, v, do = draw(shape, 125, "bf16")

@@ -40,15 +40,16 @@ def test_workload_fp16_2048(causal):
 
 def test_workload_bf16_gqa_4096_sampled():
     """bf16 GQA 4:1, B=2, Hq=32, Hkv=8, L=4096, D=128, causal, seed 3: full-size run,
-    two whole groups checked."""
+    four whole groups checked (two per batch; every query row of their 16 heads,
+    the last query block of each batch included, and all keys of their 4 KV heads)."""
     sampled_parity(Shape(2, 32, 8, 4096, 4096, 128), "bf16", True, seed=3,
-                   groups=[(0, 0), (1, 7)])
+                   groups=[(0, 0), (0, 5), (1, 2), (1, 7)])
 
 
 def test_workload_bf16_long_context_sampled():
-    """bf16, B=1, H=16, L=16384, D=128, causal, seed 4: full-size run, one head checked."""
+    """bf16, B=1, H=16, L=16384, D=128, causal, seed 4: full-size run, two heads checked."""
     sampled_parity(Shape(1, 16, 16, 16384, 16384, 128), "bf16", True, seed=4,
-                   groups=[(0, 11)])
+                   groups=[(0, 0), (0, 11)])
 
 
 def test_workload_bf16_short_query():
