@@ -10,11 +10,14 @@ FLOPs are algorithmic: 4·B·Hq·Lq·Lkv·D forward, 2.5× that backward, halved
 Timing: W untimed warm-up steps, then exactly K steps, each bracketed by CUDA events on
 the launching stream; L2 is flushed (a 256 MiB write) before every step, outside the
 step's events.  Per-kernel durations come from the library's own event brackets
-(sdpa_timing_*), recorded during the same timed steps.  SM clocks and throttle reasons
-are sampled with nvidia-smi during the timed region.  Also measured in the same run:
-the same step end to end from pinned host buffers (copies inside the timed region), the
-short-query (vector) path and the δ pre-pass against the HBM roofline, and the CPU
-oracle on a bounded sample of the workload (the reported CPU baseline).
+(sdpa_timing_*), recorded during a second pass of K steps (with the brackets on, the
+backward runs its dK/dV and dQ kernels one after the other instead of concurrently).  SM
+clocks and throttle reasons are sampled with nvidia-smi during both passes.  Also
+measured in the same run: the same step end to end from pinned host buffers (copies
+inside the timed region), the short-query (vector) path and the δ pre-pass against the
+HBM roofline, attention masks, one line per (target workload, pass) with the oracle's
+time and the GPU result's maximum errors against it, and the CPU oracle on a bounded
+sample of the workload (the reported CPU baseline).
 
 Multi-GPU (torchrun): every rank runs its own replica of the workload (the path needs no
 exchange between GPUs); value = all ranks' FLOPs / the slowest rank's time; weak scaling.
@@ -66,6 +69,15 @@ def slowest_rank(values, dist, device):
 def job_tflops(world, flops_per_step, steps, total_ms):
     """Whole-job throughput: the work of all `world` replicas over the slowest one's time."""
     return world * flops_per_step * steps / (total_ms / 1e3) / 1e12
+
+
+def headline_config(world):
+    """The `config` object of the headline line, shared by both arms (the GPU arm and the
+    CPU oracle arm time the same workload)."""
+    return {"workload": WORKLOAD_NAME, **WORKLOAD, "causal": CAUSAL,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "flushed before every GPU step (256 MiB write, outside the step's events); "
+                  "not applicable to the CPU oracle arm"}
 
 
 def load_peaks():
@@ -204,7 +216,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_NAME, **W, "causal": CAUSAL, "l2": "n/a (CPU)"},
+        "config": headline_config(args.gpus),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -219,6 +231,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-(config, pass) lines")
     args = ap.parse_args()
     if args.impl == "reference":
         args.steps = args.steps or 20
@@ -288,8 +302,6 @@ def main():
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     mids = []
-    _lib.sdpa_timing_reset()
-    _lib.sdpa_timing_enable(True)
     barrier()
     launches0 = _lib.sdpa_launch_count()
     t0 = time.perf_counter()
@@ -301,11 +313,23 @@ def main():
     barrier()
     t1 = time.perf_counter()
     launches = _lib.sdpa_launch_count() - launches0
-    _lib.sdpa_timing_enable(False)
     api.poll_status()
     clocks = sampler.summary(t0, t1) if sampler else None
-    if sampler:
-        sampler.stop()
+
+    # Per-kernel durations: the same steps again with the library's per-kernel event
+    # brackets on (the backward then runs dK/dV and dQ one after the other, so that each
+    # bracket holds one kernel alone).
+    _lib.sdpa_timing_reset()
+    _lib.sdpa_timing_enable(True)
+    tk0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        step()
+    barrier()
+    tk1 = time.perf_counter()
+    _lib.sdpa_timing_enable(False)
+    api.poll_status()
+    kclocks = sampler.summary(tk0, tk1) if sampler else None
 
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     fwd_ms = [s.elapsed_time(m) for s, m in zip(starts, mids)]
@@ -357,11 +381,16 @@ def main():
     # End to end through the public API from pinned host buffers.
     e2e = run_e2e(torch, api, dev, stream, (q_h, k_h, v_h, do_h), scale, args.steps, step_flops,
                   world, barrier, dist if world > 1 else None)
+    if sampler:
+        sampler.stop()
 
     extras = {}
+    configs = None
     if rank == 0:
         extras["short_query"] = run_short_query(torch, api, _lib, dev, stream, hbm_peak)
         extras["masked"] = run_masked(torch, api, dev, stream, bf16_peak)
+        if not args.no_configs:
+            configs = run_configs(torch, api, dev, stream, peaks, oracle_on=not args.no_cpu_baseline)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         heads = 16
@@ -378,9 +407,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD_NAME, **W, "causal": CAUSAL,
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": "flushed before every step (256 MiB write, outside step events)"},
+            "config": headline_config(world),
             "frac_of_bf16_peak": value / bf16_peak,
             "fwd": {"tflops": fwd_tflops, "ms": total_fwd_ms / args.steps,
                     "frac_of_bf16_peak": fwd_tflops / bf16_peak},
@@ -389,6 +416,10 @@ def main():
             "cpu_baseline": cpu,
             "e2e": e2e,
             "clocks": clocks,
+            "kernel_timing": {"how": "a second pass of the same steps with per-kernel event "
+                                     "brackets on (dK/dV and dQ then serial)",
+                              "clocks": kclocks},
+            "configs": configs,
             "gpu_launches": launches,
             "peaks": {"source": peak_src, "bf16_tflops": bf16_peak, "hbm_gbs": hbm_peak},
             **extras,
@@ -575,6 +606,174 @@ def run_masked(torch, api, dev, stream, bf16_peak):
         tf = 3.5 * F / (ms / 1e3) / 1e12
         res[name] = {"ms": ms, "tflops": tf, "frac_of_bf16_peak": tf / bf16_peak}
     return res
+
+
+# Per-(config, pass) lines: the five target workloads (the short-query one at each Lq).
+# Seeds and the draw order follow the input recipe: one generator per workload; the
+# short-query sub-runs draw one after another from default_rng(4).
+CONFIGS = [
+    ("C1 fp32 tiny", dict(B=1, Hq=2, Hkv=2, Lq=64, Lkv=64, D=32), "f32", False, 0),
+    ("C2 fp32 B=8 H=8 L=128 D=64", dict(B=8, Hq=8, Hkv=8, Lq=128, Lkv=128, D=64), "f32", False, 1),
+    ("C3 fp16 L=2048 D=64", dict(B=1, Hq=8, Hkv=8, Lq=2048, Lkv=2048, D=64), "f16", False, 2),
+    ("C3 fp16 L=2048 D=64 causal", dict(B=1, Hq=8, Hkv=8, Lq=2048, Lkv=2048, D=64), "f16", True, 2),
+    ("C4 bf16 GQA L=4096 D=128 causal", dict(WORKLOAD), "bf16", True, 3),
+    ("C5a bf16 L=16384 D=128 causal", dict(B=1, Hq=16, Hkv=16, Lq=16384, Lkv=16384, D=128), "bf16",
+     True, 4),
+]
+# Oracle sample of the large workloads: whole (batch, KV head) groups.
+ORACLE_GROUPS = {"C4 bf16 GQA L=4096 D=128 causal": [(1, 7)],
+                 "C5a bf16 L=16384 D=128 causal": [(0, 11)]}
+
+
+def _median_ms(torch, stream, fn, flush, n):
+    times = []
+    for i in range(n + 3):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        if i >= 3:
+            times.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(x.elapsed_time(y) for x, y in times)
+
+
+def _errors(dtype, got, ref):
+    """Max errors of one comparison, in the units the tolerances use."""
+    import numpy as np
+    err = {"o_max_abs": float(np.max(np.abs(got["o"] - ref["o"]))),
+           "lse_rel": float(np.max(np.abs(got["lse"] - ref["lse"]) /
+                                   np.maximum(1.0, np.abs(ref["lse"]))))}
+    for n in ("dq", "dk", "dv"):
+        if dtype == "f32":
+            err[n + "_max_abs"] = float(np.max(np.abs(got[n] - ref[n])))
+        else:
+            den = float(np.linalg.norm(ref[n])) or 1.0
+            err[n + "_rel_frob"] = float(np.linalg.norm(got[n] - ref[n]) / den)
+    return err
+
+
+def _oracle_compare(name, S, dtype, causal, host, got, scale, groups):
+    """Oracle on the whole workload (groups None) or on whole (batch, KV-head) groups;
+    returns (seconds, sample description, max errors)."""
+    import numpy as np
+    import oracle
+    from scaled_dot_product_flash_gb300.inputs import as_f64
+    q, k, v, do = host
+    G = S["Hq"] // S["Hkv"]
+    if groups is None:
+        t0 = time.perf_counter()
+        qn, kn, vn, dn = (as_f64(t) for t in host)
+        o, lse = oracle.sdpa_forward(qn, kn, vn, scale, causal)
+        dq, dk, dv = oracle.sdpa_backward(qn, kn, vn, dn, scale, causal)
+        dt = time.perf_counter() - t0
+        ref = dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv)
+        return dt, "whole workload", _errors(dtype, {n: as_f64(t) for n, t in got.items()}, ref)
+    errs = {}
+    dt = 0.0
+    for b, g in groups:
+        hs = slice(g * G, (g + 1) * G)
+        t0 = time.perf_counter()
+        kg, vg = as_f64(k[b, g]), as_f64(v[b, g])
+        o = np.empty((G, S["Lq"], S["D"]))
+        lse = np.empty((G, S["Lq"]))
+        for t, h in enumerate(range(g * G, (g + 1) * G)):
+            o[t], lse[t] = oracle.head_forward(as_f64(q[b, h]), kg, vg, scale, causal, row_block=1024)
+        dq, dk, dv = oracle.group_backward(as_f64(q[b:b + 1]), as_f64(k[b:b + 1]), as_f64(v[b:b + 1]),
+                                           as_f64(do[b:b + 1]), scale, causal, 0, g, row_block=1024)
+        dt += time.perf_counter() - t0
+        part = dict(o=as_f64(got["o"][b, hs]), lse=as_f64(got["lse"][b, hs]),
+                    dq=as_f64(got["dq"][b, hs]), dk=as_f64(got["dk"][b, g]), dv=as_f64(got["dv"][b, g]))
+        e = _errors(dtype, part, dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv))
+        errs = {n: max(errs.get(n, 0.0), x) for n, x in e.items()}
+    heads = G * len(groups)
+    return dt, f"{len(groups)} whole (batch, KV head) group(s) = {heads} of {S['B'] * S['Hq']} query heads", errs
+
+
+def run_configs(torch, api, dev, stream, peaks, oracle_on=True):
+    """One entry per (config, pass): GPU time (median of CUDA-event brackets, L2 flushed
+    before each call), TFLOP/s and the fraction of the bf16 peak (fp32 workloads also
+    against the fp32 FMA peak of the CUDA cores), the oracle's time on this host's cores
+    and the maximum errors of the GPU result against it."""
+    import numpy as np
+    from scaled_dot_product_flash_gb300.inputs import Shape, draw
+    bf16_peak, hbm_peak = peaks["bf16_tflops"], peaks["hbm_gbs"]
+    props = torch.cuda.get_device_properties(dev)
+    sm_mhz = float(peaks.get("sm_max_mhz") or 2070.0)
+    ffma_peak = props.multi_processor_count * 128 * 2 * sm_mhz * 1e6 / 1e12
+    ffma_how = f"{props.multi_processor_count} SMs x 128 fp32 lanes x 2 FLOP (FMA) x {sm_mhz:.0f} MHz"
+    cores = len(os.sched_getaffinity(0))
+    flush = torch.empty(L2_FLUSH_BYTES, device=dev, dtype=torch.uint8)
+    out = []
+    jobs = []
+    for name, S, dtype, causal, seed in CONFIGS:
+        host = draw(Shape(**S), seed, dtype)
+        jobs.append((name, S, dtype, causal, host))
+    rng = np.random.default_rng(4)
+    for lq in (1, 4, 8):
+        S = dict(SHORT_QUERY, Lq=lq)
+        jobs.append((f"C5b bf16 short query Lq={lq}", S, "bf16", False, draw(Shape(**S), 4, "bf16", rng=rng)))
+    results = []
+    for name, S, dtype, causal, host in jobs:
+        q, k, v, do = (t.to(dev) for t in host)
+        scale = 1.0 / math.sqrt(S["D"])
+        o, lse = api.attention_forward(q, k, v, scale=scale, is_causal=causal)
+        dq, dk, dv = api.attention_backward(q, k, v, o, do, lse, scale=scale, is_causal=causal)
+        ws = torch.empty(max(16, api.workspace_bytes(q, k)), device=dev, dtype=torch.uint8)
+        n = 20 if S["Lq"] * S["Lkv"] * S["Hq"] * S["B"] > (1 << 26) else 50
+
+        def fwd():
+            api.attention_forward(q, k, v, scale=scale, is_causal=causal, out=o, lse=lse)
+
+        def both():
+            fwd()
+            api.attention_backward(q, k, v, o, do, lse, scale=scale, is_causal=causal, workspace=ws,
+                                   dq=dq, dk=dk, dv=dv)
+        fwd_ms = _median_ms(torch, stream, fwd, flush, n)
+        both_ms = _median_ms(torch, stream, both, flush, n)
+        api.poll_status()
+        # results of one more clean call, copied to the host for the oracle comparison
+        fwd()
+        api.attention_backward(q, k, v, o, do, lse, scale=scale, is_causal=causal, dq=dq, dk=dk, dv=dv)
+        api.poll_status()
+        got = {n_: t.cpu() for n_, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+        results.append((name, S, dtype, causal, host, got, scale, fwd_ms, both_ms))
+        del q, k, v, do, o, lse, dq, dk, dv, ws
+    del flush
+    torch.cuda.empty_cache()
+    # The oracle runs after every GPU measurement, so it never competes with them.
+    for name, S, dtype, causal, host, got, scale, fwd_ms, both_ms in results:
+        F = fwd_flops(**S, causal=causal)
+        orc = None
+        if oracle_on:
+            groups = ORACLE_GROUPS.get(name)
+            dt, sample, errs = _oracle_compare(name, S, dtype, causal, host, got, scale, groups)
+            full = dt if groups is None else dt * S["B"] * S["Hkv"] / len(groups)
+            orc = {"seconds": dt, "sample": sample, "seconds_whole_workload": full,
+                   "whole_workload_estimate": groups is not None, "cores": cores,
+                   "max_errors": errs}
+        short = name.startswith("C5b")
+        for pas, ms, mult in (("fwd", fwd_ms, 1.0), ("fwd+bwd", both_ms, 3.5)):
+            tf = mult * F / (ms / 1e3) / 1e12
+            e = {"config": name, "shape": S, "dtype": dtype, "causal": bool(causal), "pass": pas,
+                 "ms": ms, "tflops": tf, "frac_of_bf16_peak": tf / bf16_peak}
+            if dtype == "f32":
+                e["frac_of_fp32_ffma_peak"] = tf / ffma_peak
+                e["fp32_ffma_peak_tflops"] = ffma_peak
+                e["fp32_ffma_peak_how"] = ffma_how
+            if short:
+                kv = S["B"] * S["Hkv"] * S["Lkv"] * S["D"] * 2
+                qb = S["B"] * S["Hq"] * S["Lq"] * S["D"] * 2
+                rows = S["B"] * S["Hq"] * S["Lq"] * 4
+                nbytes = (2 * kv + 2 * qb + rows) if pas == "fwd" else (2 * kv + 2 * qb + rows) + (4 * kv + 4 * qb + rows)
+                e["gbs"] = nbytes / (ms / 1e3) / 1e9
+                e["frac_of_hbm"] = e["gbs"] / hbm_peak
+                e["algorithmic_bytes"] = nbytes
+            if orc:
+                e["oracle"] = orc
+            out.append(e)
+    return out
 
 
 if __name__ == "__main__":

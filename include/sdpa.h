@@ -37,7 +37,12 @@
  *  - Ownership: the caller allocates and owns every buffer.  The library keeps only a
  *    static device error word and host-side counters.
  *  - Execution: every call enqueues work on `stream` (a cudaStream_t; NULL = the legacy
- *    default stream) and returns without synchronising, except sdpa_poll_status.
+ *    default stream) and returns without synchronising, except sdpa_poll_status.  The
+ *    tensor-core backward forks its dK/dV kernel onto a library-owned stream of the
+ *    highest priority (one per device, created on first use) and joins it back with
+ *    events, so that its dQ kernel, on `stream`, runs concurrently; work enqueued on
+ *    `stream` after the call still starts only when all of the call's work is done, and
+ *    stream capture follows the fork and the join.
  *  - Outputs are fully overwritten; they need no zeroing.  Inputs must not overlap
  *    outputs.
  *  - Errors: argument errors are detected on the host before anything is launched and
@@ -290,7 +295,9 @@ uint64_t sdpa_launch_count(void);
 
 /*
  * Per-kernel device timing, for measurements.  While enabled, every kernel the library
- * launches is bracketed by two CUDA events recorded on the launch's stream;
+ * launches is bracketed by two CUDA events recorded on the launch's stream, and the
+ * backward runs its dK/dV and dQ kernels one after the other on `stream` (not
+ * concurrently), so that each pair of events brackets one kernel's work alone;
  * sdpa_timing_read waits for the recorded events, adds their elapsed times into
  * per-kernel totals, and returns the total milliseconds and the number of timed launches
  * of one kernel kind since the last sdpa_timing_reset.  Process-wide, guarded by a mutex.

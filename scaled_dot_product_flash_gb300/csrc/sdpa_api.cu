@@ -226,6 +226,45 @@ cudaError_t launch_one(int kernel, cudaStream_t s, Fn fn) {
 
 int status_of(cudaError_t e) { return e == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA; }
 
+// ---- fork / join of the two tiled backward kernels ----
+// The dK/dV and dQ kernels both need only δ, so they run concurrently: the dK/dV kernel on
+// a library-owned stream of the highest priority (its pending blocks are scheduled first),
+// the dQ kernel on the caller's stream, whose blocks fill the SMs that the tail of the
+// dK/dV grid leaves idle.  Events order the side stream after the caller's earlier work
+// and the caller's stream after the dK/dV kernel, so the call stays ordered on the
+// caller's stream like any single-stream launch sequence (graph capture follows the fork
+// into the side stream and back).  One side stream and one event pair per device; the
+// record / wait / launch sequence holds a mutex so that concurrent host threads cannot
+// interleave their events.
+struct Fork {
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+Fork g_fork[kMaxDevices];
+std::mutex g_fork_mu;
+
+// Side stream and events of the current device, created on first use (caller holds
+// g_fork_mu).
+cudaError_t fork_of_device(Fork** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  Fork& f = g_fork[dev];
+  if (!f.side) {
+    int least = 0, greatest = 0;
+    if ((e = cudaDeviceGetStreamPriorityRange(&least, &greatest)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&f.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&f.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithPriority(&f.side, cudaStreamNonBlocking, greatest)) != cudaSuccess) {
+      f.side = nullptr;
+      return e;
+    }
+  }
+  *out = &f;
+  return cudaSuccess;
+}
+
 }  // namespace
 }  // namespace sdpa
 
@@ -390,14 +429,36 @@ extern "C" int sdpa_bwd_masked(const void* q, const void* k, const void* v, cons
       return vector_mma_supported(p, dtype) ? launch_vector_mma_bwd(p, dtype, s) : launch_vector_bwd(p, dtype, s);
     }));
   const bool tc = f == Family::kTensor && tensor_bwd_supported(p, dtype);
-  e = launch_one(SDPA_KERNEL_DKDV, s, [&] {
-    return tc ? launch_tc_dkdv(p, dtype, s) : launch_simt_dkdv(p, dtype, s);
-  });
-  if (e != cudaSuccess) return status_of(e);
-  e = launch_one(SDPA_KERNEL_DQ, s, [&] {
-    return tc ? launch_tc_dq(p, dtype, s) : launch_simt_dq(p, dtype, s);
-  });
-  return status_of(e);
+  auto launch_dkdv = [&](cudaStream_t st) {
+    return launch_one(SDPA_KERNEL_DKDV, st, [&] {
+      return tc ? launch_tc_dkdv(p, dtype, st) : launch_simt_dkdv(p, dtype, st);
+    });
+  };
+  auto launch_dq = [&](cudaStream_t st) {
+    return launch_one(SDPA_KERNEL_DQ, st, [&] {
+      return tc ? launch_tc_dq(p, dtype, st) : launch_simt_dq(p, dtype, st);
+    });
+  };
+  // While per-kernel timing is on, each kernel runs alone so that its events bracket only
+  // its own work.
+  if (!tc || g_timing_on.load()) {
+    if ((e = launch_dkdv(s)) != cudaSuccess) return status_of(e);
+    return status_of(launch_dq(s));
+  }
+  std::lock_guard<std::mutex> lock(g_fork_mu);
+  Fork* fk = nullptr;
+  if ((e = fork_of_device(&fk)) != cudaSuccess) return status_of(e);
+  if ((e = cudaEventRecord(fk->fork, s)) != cudaSuccess) return status_of(e);
+  if ((e = cudaStreamWaitEvent(fk->side, fk->fork, 0)) != cudaSuccess) return status_of(e);
+  const cudaError_t e_kv = launch_dkdv(fk->side);
+  const cudaError_t e_q = launch_dq(s);
+  // The join is recorded and waited for even if a launch failed, so that the side stream
+  // is always joined back (and released from any capture).
+  e = cudaEventRecord(fk->join, fk->side);
+  const cudaError_t e_join = e == cudaSuccess ? cudaStreamWaitEvent(s, fk->join, 0) : e;
+  if (e_kv != cudaSuccess) return status_of(e_kv);
+  if (e_q != cudaSuccess) return status_of(e_q);
+  return status_of(e_join);
 }
 
 extern "C" int sdpa_bwd_sinks(const void* q, const void* k, const void* v, const void* out,
