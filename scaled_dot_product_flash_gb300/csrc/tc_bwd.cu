@@ -11,21 +11,22 @@
 //   dV += Pᵀ·dO, dK += dSᵀ·Q                         (tcgen05, accumulators stay in TMEM)
 // and finally dK·scale and dV are rounded and stored.  The element warps publish Pᵀ as
 // soon as it is ready, so dV runs while dSᵀ is computed, and Sᵀ of the next block starts
-// as soon as dV has consumed Pᵀ.  dSᵀ is formed from Pᵀ in fp32 (dV uses Pᵀ rounded to
-// the element type, as the A operand of a 16-bit MMA must be).
+// as soon as dV has consumed Pᵀ (the MMA order is dV(n), Sᵀ(n+1), dK(n), dPᵀ(n+1)).  dSᵀ
+// is formed from Pᵀ in fp32 (dV uses Pᵀ rounded to the element type, as the A operand of
+// a 16-bit MMA must be).
 //
 // dQ kernel: one block owns 128 query rows of one head and loops over 128-row KV blocks:
 //   S = Q·Kᵀ, dP = dO·Vᵀ, P = exp2(c·S − log2e·lse_i), dS = P∘(dP − δ_i), dQ += dS·K,
 // then dQ·scale is stored.  S alternates between two TMEM buffers, so S of block n+1 is
-// computed while block n's element work runs; dP of block n+1 is issued before dQ of
-// block n so the element warps wait as little as possible.
+// computed while block n's element work runs; S, dP and dQ have an issuer warp each, so
+// that no issuer waits for an MMA it has just issued.
 //
 // All MMAs have M = 128, N = 128 (N = D for the accumulating ones): narrower N would make
 // the shared-memory operand traffic exceed what one SM's shared memory can deliver.
 // Warps 0-3 and 4-7 split each 128-column block of scores into two 64-column halves
 // (warpgroup w owns columns [64w, 64w+64) and writes its packed results to its own
-// columns [64w, 64w+32)), warp 8 is the TMA producer, warps 9 and 10 issue the MMAs (two
-// independent chains each) and warp 9 owns the 512 TMEM columns.
+// columns [64w, 64w+32)), warp 8 is the TMA producer, warps 9 and 10 (and 11 in the dQ
+// kernel) issue the MMAs and warp 9 owns the 512 TMEM columns.
 //
 // Attention masks: both kernels have a masked instantiation (kMasked) that adds log2e·M
 // to the log2-domain scores before the exponential (the dK/dV kernel reads one mask value
@@ -40,7 +41,7 @@ namespace {
 using namespace tc;
 
 constexpr int kThreads = 352;    // dK/dV: warps 0-7 element work, 8 producer, 9-10 MMA issuers
-constexpr int kDqThreads = 384;  // dQ: the same plus an idle warp 11 for the register split
+constexpr int kDqThreads = 384;  // dQ: warps 0-7 element work, 8 producer, 9-11 MMA issuers
 // dQ register split (setmaxnreg): launched at 168 registers a thread (65,536 / 384 rounded
 // down to a multiple of 8, 64,512 in all); warpgroup 2 drops to 56 and the element
 // warpgroups rise to 224: 128·56 + 256·224 = 64,512.
@@ -236,33 +237,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
     // ---------------------------------------------------------------- MMA issuers
-    // Two independent chains, one issuer each: warp 9 issues Sᵀ and dV (TMEM region X),
-    // warp 10 issues dPᵀ and dK (region Y), so Sᵀ of the next block can start as soon as
-    // dV has consumed Pᵀ even while dK still waits for dSᵀ.
+    // Warp 9 issues Sᵀ, dV and dK in the order dV(n), Sᵀ(n+1), dK(n): Sᵀ(n+1) overwrites the
+    // Pᵀ(n) that dV(n) reads, so it waits for dV(n) to finish, and issuing dK(n) only after
+    // it keeps dK(n) from running ahead of Sᵀ(n+1) (the element warps need Sᵀ(n+1) next,
+    // while dK(n) only gates dPᵀ(n+1), which they need a whole exponential pass later).
+    // Warp 10 issues dPᵀ(n) once dK(n-1) has consumed dSᵀ(n-1).
     constexpr unsigned kAll = 0xffffffffu;
     const bool chain_x = __shfl_sync(kAll, warp, 0) == kMmaWarp;
     bool ok = __all_sync(kAll, mbar_wait(&bars.own_full, 0, wc));
     tc_fence_after();
-    const uint32_t own_s = smem_u32(sm + (chain_x ? L::kOwnA : L::kOwnB));  // K or V
-    const uint32_t col = chain_x ? kColX : kColY;
-    const uint32_t acc = chain_x ? kColDv : kColDk;
-    uint64_t* freed = chain_x ? &bars.x_free : &bars.y_free;
-    uint64_t* ready = chain_x ? &bars.p_ready : &bars.ds_ready;
-    uint64_t* scores_done = chain_x ? &bars.s_full[0] : &bars.dp_full;
-    for (int n = 0; ok && n < total; ++n) {
-      const int s = n % kStages;
-      const uint32_t q_s = smem_u32(sm + L::kRing + s * L::kStageBytes), do_s = q_s + L::kTileBytes;
-      if (!(ok = __all_sync(kAll, mbar_wait(&bars.ring_full[s], (n / kStages) & 1, wc)))) break;
-      if (n > 0 && !(ok = __all_sync(kAll, mbar_wait(freed, (n - 1) & 1, wc)))) break;
-      tc_fence_after();
-      mma_scores<D>(tbase + col, own_s, chain_x ? q_s : do_s, kIdS);  // Sᵀ = K·Qᵀ or dPᵀ = V·dOᵀ
-      mma_commit_w(scores_done);
-      if (!(ok = __all_sync(kAll, mbar_wait(ready, n & 1, wc)))) break;
-      tc_fence_after();
-      // dV += Pᵀ·dO or dK += dSᵀ·Q
-      mma_accumulate<D>(tbase + acc, tbase + col, chain_x ? do_s : q_s, kIdAcc, n == 0);
-      mma_commit_w(freed);
-      mma_commit_w(&bars.ring_empty[s]);  // one of the stage's two arrivals
+    const uint32_t k_s = smem_u32(sm + L::kOwnA), v_s = smem_u32(sm + L::kOwnB);
+    auto stage_q = [&](int n) { return smem_u32(sm + L::kRing + (n % kStages) * L::kStageBytes); };
+    if (chain_x) {
+      if (ok && total > 0) {
+        ok = __all_sync(kAll, mbar_wait(&bars.ring_full[0], 0, wc));
+        if (ok) {
+          tc_fence_after();
+          mma_scores<D>(tbase + kColX, k_s, stage_q(0), kIdS);  // Sᵀ(0) = K·Q(0)ᵀ
+          mma_commit_w(&bars.s_full[0]);
+        }
+      }
+      for (int n = 0; ok && n < total; ++n) {
+        const uint32_t q_s = stage_q(n), do_s = q_s + L::kTileBytes;
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.p_ready, n & 1, wc)))) break;
+        tc_fence_after();
+        mma_accumulate<D>(tbase + kColDv, tbase + kColX, do_s, kIdAcc, n == 0);  // dV += Pᵀ·dO
+        mma_commit_w(&bars.x_free);
+        if (n + 1 < total) {
+          if (!(ok = __all_sync(kAll, mbar_wait(&bars.ring_full[(n + 1) % kStages], ((n + 1) / kStages) & 1, wc) &&
+                                          mbar_wait(&bars.x_free, n & 1, wc))))
+            break;
+          tc_fence_after();
+          mma_scores<D>(tbase + kColX, k_s, stage_q(n + 1), kIdS);  // Sᵀ(n+1)
+          mma_commit_w(&bars.s_full[0]);
+        }
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.ds_ready, n & 1, wc)))) break;
+        tc_fence_after();
+        mma_accumulate<D>(tbase + kColDk, tbase + kColY, q_s, kIdAcc, n == 0);  // dK += dSᵀ·Q
+        mma_commit_w(&bars.y_free);
+        mma_commit_w(&bars.ring_empty[n % kStages]);  // one of the stage's two arrivals
+      }
+    } else {
+      for (int n = 0; ok && n < total; ++n) {
+        const uint32_t do_s = stage_q(n) + L::kTileBytes;
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.ring_full[n % kStages], (n / kStages) & 1, wc)))) break;
+        if (n > 0 && !(ok = __all_sync(kAll, mbar_wait(&bars.y_free, (n - 1) & 1, wc)))) break;
+        tc_fence_after();
+        mma_scores<D>(tbase + kColY, v_s, do_s, kIdS);  // dPᵀ = V·dOᵀ
+        mma_commit_w(&bars.dp_full);
+        mma_commit_w(&bars.ring_empty[n % kStages]);
+      }
     }
     mma_commit_w(&bars.acc_done);
     drain_wait(&bars.acc_done, 0, 100000000ull);
@@ -488,7 +512,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     mbar_init(&bars.ds_ready, 256);
     mbar_init(&bars.dq_done[0], 1);
     mbar_init(&bars.dq_done[1], 1);
-    mbar_init(&bars.acc_done, 2);  // one commit per MMA issuer
+    mbar_init(&bars.acc_done, 3);  // one commit per MMA issuer
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -535,38 +559,28 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           drain_wait(&bars.v_full[n % kVStages], (n / kVStages) & 1, 100000000ull);
       }
     }
-  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-    // Two issuers: warp 9 issues S and dQ, warp 10 issues dP, each at its own pace.  All
-    // lanes of an issuer warp run its loop; one elected lane issues.
+  } else if (warp >= kMmaWarp) {
+    // Three issuers, each at its own pace (all lanes of an issuer warp run its loop; one
+    // elected lane issues): warp 9 issues S(n) = Q·K(n)ᵀ into S buffer n % 2 once dQ(n-2)
+    // has read dS(n-2) from it, warp 10 issues dP(n) = dO·V(n)ᵀ once the element warps
+    // have read dP(n-1), and warp 11 issues dQ += dS(n)·K(n) as soon as dS(n) is packed.
+    // Keeping dQ apart from S means no issuer waits for an MMA it has just issued.
     constexpr unsigned kAll = 0xffffffffu;
+    const int role = __shfl_sync(kAll, warp - kMmaWarp, 0);
     bool ok = __all_sync(kAll, mbar_wait(&bars.own_full, 0, wc));
     tc_fence_after();
     const uint32_t q_s = smem_u32(sm + L::kQ), do_s = smem_u32(sm + L::kDo);
     const uint32_t k_s = smem_u32(sm + L::kK), v_s = smem_u32(sm + L::kV);
-    if (__shfl_sync(kAll, warp, 0) == kMmaWarp) {
-      // S(n) = Q·K(n)ᵀ into S buffer n % 2 (free once dQ(n-2) has read dS(n-2) from it).
-      auto issue_s = [&](int n) -> bool {
-        if (!__all_sync(kAll, mbar_wait(&bars.k_full[n % kKStages], (n / kKStages) & 1, wc))) return false;
-        if (n >= 2 && !__all_sync(kAll, mbar_wait(&bars.dq_done[n % 2], ((n - 2) / 2) & 1, wc))) return false;
+    if (role == 0) {
+      for (int n = 0; ok && n < total; ++n) {
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.k_full[n % kKStages], (n / kKStages) & 1, wc)))) break;
+        if (n >= 2 && !(ok = __all_sync(kAll, mbar_wait(&bars.dq_done[n % 2], ((n - 2) / 2) & 1, wc)))) break;
         tc_fence_after();
         mma_scores<D>(tbase + kColS0 + 128 * (n % 2), q_s, k_s + (n % kKStages) * L::kTileBytes, kIdS);
         mma_commit_w(&bars.s_full[n % 2]);
-        return true;
-      };
-      if (ok && total > 0) ok = issue_s(0);
-      if (ok && total > 1) ok = issue_s(1);
-      for (int n = 0; ok && n < total; ++n) {
-        if (!(ok = __all_sync(kAll, mbar_wait(&bars.ds_ready, n & 1, wc)))) break;
-        tc_fence_after();
-        // dQ += dS·K: B = the K block read MN-major.
-        mma_accumulate<D>(tbase + kColDq, tbase + kColS0 + 128 * (n % 2),
-                          k_s + (n % kKStages) * L::kTileBytes, kIdAcc, n == 0);
-        mma_commit_w(&bars.dq_done[n % 2]);
-        mma_commit_w(&bars.k_empty[n % kKStages]);
-        if (n + 2 < total && !(ok = issue_s(n + 2))) break;
       }
-    } else {
-      // dP(n) = dO·V(n)ᵀ into the dP buffer (free once the element warps have read dP(n-1)).
+    } else if (role == 1) {
+      // dP(n) into the dP buffer (free once the element warps have read dP(n-1)).
       for (int n = 0; ok && n < total; ++n) {
         if (!(ok = __all_sync(kAll, mbar_wait(&bars.v_full[n % kVStages], (n / kVStages) & 1, wc)))) break;
         if (n >= 1 && !(ok = __all_sync(kAll, mbar_wait(&bars.dp_free, (n - 1) & 1, wc)))) break;
@@ -574,6 +588,20 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         mma_scores<D>(tbase + kColDp, do_s, v_s + (n % kVStages) * L::kTileBytes, kIdS);
         mma_commit_w(&bars.dp_full);
         mma_commit_w(&bars.v_empty[n % kVStages]);
+      }
+    } else {
+      for (int n = 0; ok && n < total; ++n) {
+        // K(n) is loaded (S(n) read it before dS(n) could exist); waiting on its barrier too
+        // makes the TMA writes visible to this warp's MMA directly.
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.ds_ready, n & 1, wc) &&
+                                        mbar_wait(&bars.k_full[n % kKStages], (n / kKStages) & 1, wc))))
+          break;
+        tc_fence_after();
+        // dQ += dS·K: B = the K block read MN-major.
+        mma_accumulate<D>(tbase + kColDq, tbase + kColS0 + 128 * (n % 2), k_s + (n % kKStages) * L::kTileBytes,
+                          kIdAcc, n == 0);
+        mma_commit_w(&bars.dq_done[n % 2]);
+        mma_commit_w(&bars.k_empty[n % kKStages]);
       }
     }
     mma_commit_w(&bars.acc_done);
