@@ -23,10 +23,12 @@
 //
 // All MMAs have M = 128, N = 128 (N = D for the accumulating ones): narrower N would make
 // the shared-memory operand traffic exceed what one SM's shared memory can deliver.
-// Warps 0-3 and 4-7 split each 128-column block of scores into two 64-column halves
-// (warpgroup w owns columns [64w, 64w+64) and writes its packed results to its own
-// columns [64w, 64w+32)), warp 8 is the TMA producer, warps 9 and 10 (and 11 in the dQ
-// kernel) issue the MMAs and warp 9 owns the 512 TMEM columns.
+// Warps 0-15 do the element work: warp e reads TMEM lane quarter e % 4 and owns the
+// 32 columns [32c, 32c + 32) of each 128-column block of scores (c = e / 4), writing its
+// packed 16-bit results over the first 16 of them; with four warps per SM sub-partition
+// the exponential and dS passes hide each other's latencies.  Warp 16 is the TMA producer,
+// warps 17 and 18 (and 19 in the dQ kernel) issue the MMAs and warp 17 owns the 512 TMEM
+// columns.
 //
 // Attention masks: both kernels have a masked instantiation (kMasked) that adds log2e·M
 // to the log2-domain scores before the exponential (the dK/dV kernel reads one mask value
@@ -40,16 +42,22 @@ namespace sdpa {
 namespace {
 using namespace tc;
 
-constexpr int kThreads = 352;    // dK/dV: warps 0-7 element work, 8 producer, 9-10 MMA issuers
-constexpr int kDqThreads = 384;  // dQ: warps 0-7 element work, 8 producer, 9-11 MMA issuers
-// dQ register split (setmaxnreg): launched at 168 registers a thread (65,536 / 384 rounded
-// down to a multiple of 8, 64,512 in all); warpgroup 2 drops to 56 and the element
-// warpgroups rise to 224: 128·56 + 256·224 = 64,512.
+// dK/dV: warps 0-15 element work (four per TMEM lane quarter, each with 32 of the 128
+// queries of a block), 16 producer, 17-18 MMA issuers.  65,536 / 608 threads leaves 104
+// registers a thread, which the 32-query element work fits.
+constexpr int kKvThreads = 608;
+constexpr int kKvProducerWarp = 16;
+constexpr int kKvMmaWarp = 17;
+// dQ: warps 0-15 element work (four per TMEM lane quarter, each with 32 of the 128 keys of
+// a block), 16 producer, 17-19 MMA issuers.  Register split (setmaxnreg): launched at 96
+// registers a thread (65,536 / 640 rounded down to a multiple of 8, 61,440 in all);
+// warpgroup 4 drops to 56 and the element warpgroups rise to 104: 128·56 + 512·104 = 60,416.
+constexpr int kDqThreads = 640;
 constexpr int kRegsLow = 56;
-constexpr int kRegsHigh = 224;
-static_assert(128 * kRegsLow + 256 * kRegsHigh <= kDqThreads * 168, "register split exceeds the launch");
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kRegsHigh = 104;
+static_assert(128 * kRegsLow + 512 * kRegsHigh <= kDqThreads * 96, "register split exceeds the launch");
+constexpr int kProducerWarp = 16;
+constexpr int kMmaWarp = 17;
 constexpr int kRows = 128;  // rows owned by a block (keys for dK/dV, queries for dQ)
 constexpr int kBlk = 128;   // rows of the streamed operand per iteration
 constexpr int kStages = 2;  // ring depth of the streamed operand
@@ -69,9 +77,15 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
 }
 
 // TMEM column of the packed 16-bit A operand for K-step kk (16 rows of the streamed
-// operand): warpgroup 0 packed rows 0-63 into columns [0, 32), warpgroup 1 rows 64-127
-// into columns [64, 96) of the same buffer.
-__device__ __forceinline__ uint32_t packed_col(int kk) { return kk < 4 ? kk * 8 : 64 + (kk - 4) * 8; }
+// operand) when the element warps own kSplit columns each and pack their results into the
+// first kSplit / 2 of them: dQ (kSplit = 64) packs rows 0-63 into columns [0, 32) and rows
+// 64-127 into [64, 96); dK/dV (kSplit = 32) packs rows [32c, 32c + 32) into columns
+// [32c, 32c + 16).
+template <int kSplit>
+__device__ __forceinline__ uint32_t packed_col(int kk) {
+  constexpr int kSteps = kSplit / 16;  // K-steps per owner
+  return (kk / kSteps) * kSplit + (kk % kSteps) * 8;
+}
 
 // Shared-memory plan (offsets from a 1024-byte aligned base).
 template <int D>
@@ -116,8 +130,8 @@ __device__ __forceinline__ void init_bars(BwdBars& bars) {
   mbar_init(&bars.s_full[0], 1);
   mbar_init(&bars.s_full[1], 1);
   mbar_init(&bars.dp_full, 1);
-  mbar_init(&bars.p_ready, 256);
-  mbar_init(&bars.ds_ready, 256);
+  mbar_init(&bars.p_ready, 512);   // every element thread of the dK/dV kernel
+  mbar_init(&bars.ds_ready, 512);
   mbar_init(&bars.x_free, 1);
   mbar_init(&bars.y_free, 1);
   mbar_init(&bars.dq_done[0], 1);
@@ -140,19 +154,19 @@ __device__ __forceinline__ void mma_scores(uint32_t c_tmem, uint32_t a_s, uint32
 
 // Issues Acc[tmem] (+)= A·B with A = packed 16-bit [128 x 128] in TMEM (see packed_col)
 // and B = a [128 x D] tile in shared memory read MN-major (N = D, K = its 128 rows).
-template <int D>
+template <int D, int kSplit>
 __device__ __forceinline__ void mma_accumulate(uint32_t acc_tmem, uint32_t a_tmem, uint32_t b_s,
                                                uint32_t idesc, bool first) {
   const uint64_t bd = sdesc_sw128(b_s, BwdLayout<D>::kCbStride, 1024);
 #pragma unroll
   for (int kk = 0; kk < kBlk / 16; ++kk)
-    mma_ts_w(acc_tmem, a_tmem + packed_col(kk), sdesc_advance(bd, kk * 2048), idesc,
+    mma_ts_w(acc_tmem, a_tmem + packed_col<kSplit>(kk), sdesc_advance(bd, kk * 2048), idesc,
              (!first || kk > 0) ? 1u : 0u);
 }
 
 // ================================================================== dK / dV
 template <typename T, int D, bool kMasked>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kKvThreads, 1)
     tc_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                    const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv,
@@ -181,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total = p.G * nqb;
 
   if (threadIdx.x == 0) init_bars(bars);
-  if (warp == kMmaWarp) {
+  if (warp == kKvMmaWarp) {
     tmem_alloc(&bars.tmem_base, 512);
     tmem_relinquish();
   }
@@ -191,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = bars.tmem_base;
   const WaitCtx wc{&bars.abort, 0, p.wait_limit_ns, p.err, kKidTcDkdv};
 
-  if (warp == kProducerWarp) {
+  if (warp == kKvProducerWarp) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       prefetch_tmap(&tq);
@@ -235,15 +249,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int n = max(0, issued - kStages); n < issued; ++n)
         drain_wait(&bars.ring_full[n % kStages], (n / kStages) & 1, 100000000ull);
     }
-  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+  } else if (warp == kKvMmaWarp || warp == kKvMmaWarp + 1) {
     // ---------------------------------------------------------------- MMA issuers
-    // Warp 9 issues Sᵀ, dV and dK in the order dV(n), Sᵀ(n+1), dK(n): Sᵀ(n+1) overwrites the
+    // Warp 17 issues Sᵀ, dV and dK in the order dV(n), Sᵀ(n+1), dK(n): Sᵀ(n+1) overwrites the
     // Pᵀ(n) that dV(n) reads, so it waits for dV(n) to finish, and issuing dK(n) only after
     // it keeps dK(n) from running ahead of Sᵀ(n+1) (the element warps need Sᵀ(n+1) next,
     // while dK(n) only gates dPᵀ(n+1), which they need a whole exponential pass later).
-    // Warp 10 issues dPᵀ(n) once dK(n-1) has consumed dSᵀ(n-1).
+    // Warp 18 issues dPᵀ(n) once dK(n-1) has consumed dSᵀ(n-1).
     constexpr unsigned kAll = 0xffffffffu;
-    const bool chain_x = __shfl_sync(kAll, warp, 0) == kMmaWarp;
+    const bool chain_x = __shfl_sync(kAll, warp, 0) == kKvMmaWarp;
     bool ok = __all_sync(kAll, mbar_wait(&bars.own_full, 0, wc));
     tc_fence_after();
     const uint32_t k_s = smem_u32(sm + L::kOwnA), v_s = smem_u32(sm + L::kOwnB);
@@ -261,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t q_s = stage_q(n), do_s = q_s + L::kTileBytes;
         if (!(ok = __all_sync(kAll, mbar_wait(&bars.p_ready, n & 1, wc)))) break;
         tc_fence_after();
-        mma_accumulate<D>(tbase + kColDv, tbase + kColX, do_s, kIdAcc, n == 0);  // dV += Pᵀ·dO
+        mma_accumulate<D, 32>(tbase + kColDv, tbase + kColX, do_s, kIdAcc, n == 0);  // dV += Pᵀ·dO
         mma_commit_w(&bars.x_free);
         if (n + 1 < total) {
           if (!(ok = __all_sync(kAll, mbar_wait(&bars.ring_full[(n + 1) % kStages], ((n + 1) / kStages) & 1, wc) &&
@@ -273,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!(ok = __all_sync(kAll, mbar_wait(&bars.ds_ready, n & 1, wc)))) break;
         tc_fence_after();
-        mma_accumulate<D>(tbase + kColDk, tbase + kColY, q_s, kIdAcc, n == 0);  // dK += dSᵀ·Q
+        mma_accumulate<D, 32>(tbase + kColDk, tbase + kColY, q_s, kIdAcc, n == 0);  // dK += dSᵀ·Q
         mma_commit_w(&bars.y_free);
         mma_commit_w(&bars.ring_empty[n % kStages]);  // one of the stage's two arrivals
       }
@@ -292,10 +306,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     drain_wait(&bars.acc_done, 0, 100000000ull);
   } else {
     // ---------------------------------------------------------------- element warps
-    const int w = warp / 4, quarter = warp % 4;
+    // Warp e: TMEM lane quarter e % 4 (keys), query columns [32c, 32c + 32) with c = e / 4.
+    const int c = warp / 4, quarter = warp % 4;
     const int j = j0 + quarter * 32 + lane;  // this thread's key
-    const uint32_t x_addr = tmem_addr(tbase, quarter * 32, kColX + 64 * w);
-    const uint32_t y_addr = tmem_addr(tbase, quarter * 32, kColY + 64 * w);
+    const uint32_t x_addr = tmem_addr(tbase, quarter * 32, kColX + 32 * c);
+    const uint32_t y_addr = tmem_addr(tbase, quarter * 32, kColY + 32 * c);
     const uint64_t cc = f2pack(p.scale_log2, p.scale_log2);
     constexpr bool masked = kMasked;  // a separate instantiation carries the mask code
     const int mes = p.mask_kind == kMaskBool ? 1 : (int)sizeof(T);
@@ -303,49 +318,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int n = 0; n < total; ++n) {
       const int s = n % kStages;
       const int hm = g * p.G + n / nqb;
-      if (masked) {  // this warp's 32 keys of the half's 64 query rows, read after S arrives
-        const int jw = j0 + quarter * 32;
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const int iq = i_begin + (n % nqb) * kBlk + 64 * w + 32 * t + lane;
-          if (iq < p.Lq && jw < p.Lkv)
-            prefetch_l1(static_cast<const uint8_t*>(p.mask) + (row_off(p.lm, b, hm, iq) + jw) * mes,
-                        min(32, p.Lkv - jw) * mes);
-        }
+      const int i0 = i_begin + (n % nqb) * kBlk + 32 * c;  // first query of this warp's columns
+      if (masked) {  // this warp's 32 keys of its 32 query rows (one row per lane), read after S arrives
+        const int jw = j0 + quarter * 32, iq = i0 + lane;
+        if (iq < p.Lq && jw < p.Lkv)
+          prefetch_l1(static_cast<const uint8_t*>(p.mask) + (row_off(p.lm, b, hm, iq) + jw) * mes,
+                      min(32, p.Lkv - jw) * mes);
       }
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[0], n & 1, wc) &&
                                        mbar_wait(&bars.vec_full[s], (n / kStages) & 1, wc));
       if (!ok) break;
       tc_fence_after();
-      const int i0 = i_begin + (n % nqb) * kBlk + 64 * w;  // first query of this half
       const int ic = i0 + p.coff;  // key j is hidden from query i0 + q when j > ic + q
       const bool diag = p.causal && j0 + kRows - 1 > ic;
-      const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(&bars.nlse2[s][64 * w]);
-      const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(&bars.ndelta[s][64 * w]);
-      // Pᵀ for this half (64 queries) from one TMEM round trip; the packed 16-bit values
-      // are written over Sᵀ for dV, and Pᵀ stays in registers in fp32 for dSᵀ.
-      uint64_t pf[32];  // fp32 pairs
+      const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(&bars.nlse2[s][32 * c]);
+      const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(&bars.ndelta[s][32 * c]);
+      // Pᵀ for this warp's 32 queries from one TMEM load; the packed 16-bit values go over
+      // the first 16 of its own Sᵀ columns for dV, and Pᵀ stays in registers in fp32 for dSᵀ.
+      uint64_t pf[16];  // fp32 pairs
       {
-        uint32_t sr[64];
-        tmem_ld32(x_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-        tmem_ld32(x_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        uint32_t sr[32];
+        tmem_ld32(x_addr, sr);
         if constexpr (kMasked) tmem_ld_wait(sr);  // the mask code reads sr with plain arithmetic
         else tmem_ld_wait();
-        uint32_t pk[32];
+        uint32_t pk[16];
         if constexpr (masked) {
-          // c·s + log2e·M for this key against the half's queries (mask 0 for queries past
+          // c·s + log2e·M for this key against the warp's queries (mask 0 for queries past
           // Lq and keys past Lkv: those P are zero or clipped anyway).
           const bool jv = j < p.Lkv;
           const int64_t mo = row_off(p.lm, b, hm, 0) + j;
 #pragma unroll
-          for (int e = 0; e < 64; ++e) {
+          for (int e = 0; e < 32; ++e) {
             const float mv = jv && i0 + e < p.Lq ? mask_log2<T>(p, mo + (int64_t)(i0 + e) * p.lm.sl) : 0.f;
             sr[e] = __float_as_uint(mv == minus_inf() ? mv : fmaf(p.scale_log2, __uint_as_float(sr[e]), mv));
           }
         }
         const uint64_t ce = masked ? f2pack(1.f, 1.f) : cc;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
+        for (int e = 0; e < 16; ++e) {
           float p0, p1;
           ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), ce, nl2[e]), p0, p1);
           if (diag) {
@@ -355,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pf[e] = f2pack(p0, p1);
           pk[e] = pack2<T>(p0, p1);
         }
-        tmem_st32(x_addr, pk);
+        tmem_st16(x_addr, pk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -363,44 +373,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_full, n & 1, wc));
       if (!ok) break;
       tc_fence_after();
-      // dSᵀ = Pᵀ∘(dPᵀ − δ), one TMEM round trip.
+      // dSᵀ = Pᵀ∘(dPᵀ − δ), one TMEM load.
       {
-        uint32_t dr[64];
-        tmem_ld32(y_addr, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
-        tmem_ld32(y_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+        uint32_t dr[32];
+        tmem_ld32(y_addr, dr);
         tmem_ld_wait();
-        uint32_t dk[32];
+        uint32_t dk[16];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
+        for (int e = 0; e < 16; ++e) {
           float d0, d1;
           f2unpack(fmul2(pf[e], fadd2(f2pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), nd2[e])), d0,
                    d1);
           dk[e] = pack2<T>(d0, d1);
         }
-        tmem_st32(y_addr, dk);
+        tmem_st16(y_addr, dk);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars.ds_ready);
     }
-    // Epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK·scale.  Each is staged in the
-    // block's own V or K buffer (no MMA reads them once acc_done has completed) in the
-    // swizzled tile layout and written by bulk tensor stores (keys past Lkv are clipped).
-    // The staging buffer is one the block's own TMA load fills; with no MMA (total == 0)
+    // Epilogue: dV and dK·scale, each in D/32 chunks of 32 columns; warpgroup wg takes the
+    // chunks whose index is wg modulo 4.  They are staged in the block's own V and K buffers
+    // (no MMA reads them once acc_done has completed) in the swizzled tile layout and written
+    // by bulk tensor stores (keys past Lkv are clipped) once all 16 warps have staged theirs.
+    // The staging buffers are ones the block's own TMA load fills; with no MMA (total == 0)
     // nothing else has waited for that load, so wait for it here too.
     if (ok)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.own_full, 0, wc) && (total == 0 || mbar_wait(&bars.acc_done, 0, wc)));
     const int r = quarter * 32 + lane;
-    uint8_t* stage = sm + (w == 0 ? L::kOwnB : L::kOwnA);
     if (ok) {
       tc_fence_after();
-      const float mul = w == 0 ? 1.f : p.scale;
-      const uint32_t a_addr = tmem_addr(tbase, quarter * 32, w == 0 ? kColDv : kColDk);
+      constexpr int kChunks = D / 32;
 #pragma unroll 1
-      for (int c32 = 0; c32 < D / 32; ++c32) {
+      for (int ch = c; ch < 2 * kChunks; ch += 4) {
+        const bool is_dk = ch >= kChunks;
+        const int c32 = is_dk ? ch - kChunks : ch;
+        const float mul = is_dk ? p.scale : 1.f;
         uint32_t acc[32];
         if (total > 0) {
-          tmem_ld32(a_addr + c32 * 32, acc);
+          tmem_ld32(tmem_addr(tbase, quarter * 32, (is_dk ? kColDk : kColDv) + 32 * c32), acc);
           tmem_ld_wait();
         } else {
 #pragma unroll
@@ -410,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           packed[e] = pack2<T>(__uint_as_float(acc[2 * e]) * mul, __uint_as_float(acc[2 * e + 1]) * mul);
-        uint8_t* blk = stage + (c32 / 2) * L::kCbStride;
+        uint8_t* blk = sm + (is_dk ? L::kOwnA : L::kOwnB) + (c32 / 2) * L::kCbStride;
 #pragma unroll
         for (int v4 = 0; v4 < 4; ++v4)
           *reinterpret_cast<uint4*>(blk + sw128_off(r, (c32 % 2) * 4 + v4)) =
@@ -418,16 +429,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_async_smem();
     }
-    if (named_sync_and(1 + w, 128, ok) && r == 0) {
-      for (int cb = 0; cb < kCB; ++cb)
-        tma_store_4d(w == 0 ? &tdv : &tdk, stage + cb * L::kCbStride, cb * 64, j0, g, b);
+    if (named_sync_and(1, 512, ok) && warp == 0 && lane == 0) {
+      for (int cb = 0; cb < kCB; ++cb) {
+        tma_store_4d(&tdv, sm + L::kOwnB + cb * L::kCbStride, cb * 64, j0, g, b);
+        tma_store_4d(&tdk, sm + L::kOwnA + cb * L::kCbStride, cb * 64, j0, g, b);
+      }
       bulk_commit();
       bulk_wait_read();
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kKvMmaWarp) {
     __syncwarp();
     tmem_dealloc(tbase, 512);
   }
@@ -508,8 +521,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     mbar_init(&bars.s_full[0], 1);
     mbar_init(&bars.s_full[1], 1);
     mbar_init(&bars.dp_full, 1);
-    mbar_init(&bars.dp_free, 256);
-    mbar_init(&bars.ds_ready, 256);
+    mbar_init(&bars.dp_free, 512);   // every element thread
+    mbar_init(&bars.ds_ready, 512);
     mbar_init(&bars.dq_done[0], 1);
     mbar_init(&bars.dq_done[1], 1);
     mbar_init(&bars.acc_done, 3);  // one commit per MMA issuer
@@ -524,7 +537,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   tc_fence_after();
   const uint32_t tbase = bars.tmem_base;
   const WaitCtx wc{&bars.abort, 0, p.wait_limit_ns, p.err, kKidTcDq};
-  if (warp >= 8) regs_dec<kRegsLow>();
+  if (warp >= 16) regs_dec<kRegsLow>();
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
@@ -561,9 +574,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     }
   } else if (warp >= kMmaWarp) {
     // Three issuers, each at its own pace (all lanes of an issuer warp run its loop; one
-    // elected lane issues): warp 9 issues S(n) = Q·K(n)ᵀ into S buffer n % 2 once dQ(n-2)
-    // has read dS(n-2) from it, warp 10 issues dP(n) = dO·V(n)ᵀ once the element warps
-    // have read dP(n-1), and warp 11 issues dQ += dS(n)·K(n) as soon as dS(n) is packed.
+    // elected lane issues): warp 17 issues S(n) = Q·K(n)ᵀ into S buffer n % 2 once dQ(n-2)
+    // has read dS(n-2) from it, warp 18 issues dP(n) = dO·V(n)ᵀ once the element warps
+    // have read dP(n-1), and warp 19 issues dQ += dS(n)·K(n) as soon as dS(n) is packed.
     // Keeping dQ apart from S means no issuer waits for an MMA it has just issued.
     constexpr unsigned kAll = 0xffffffffu;
     const int role = __shfl_sync(kAll, warp - kMmaWarp, 0);
@@ -598,7 +611,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           break;
         tc_fence_after();
         // dQ += dS·K: B = the K block read MN-major.
-        mma_accumulate<D>(tbase + kColDq, tbase + kColS0 + 128 * (n % 2), k_s + (n % kKStages) * L::kTileBytes,
+        mma_accumulate<D, 32>(tbase + kColDq, tbase + kColS0 + 128 * (n % 2), k_s + (n % kKStages) * L::kTileBytes,
                           kIdAcc, n == 0);
         mma_commit_w(&bars.dq_done[n % 2]);
         mma_commit_w(&bars.k_empty[n % kKStages]);
@@ -606,9 +619,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     }
     mma_commit_w(&bars.acc_done);
     drain_wait(&bars.acc_done, 0, 100000000ull);
-  } else if (warp < 8) {
+  } else if (warp < 16) {
     regs_inc<kRegsHigh>();
-    const int w = warp / 4, quarter = warp % 4;
+    // Warp e: TMEM lane quarter e % 4 (queries), key columns [32c, 32c + 32) with c = e / 4.
+    const int c = warp / 4, quarter = warp % 4;
     const int i = i0 + quarter * 32 + lane;  // this thread's query
     const bool valid = i < p.Lq;
     const int64_t row = q_row(p, b, h, valid ? i : 0);
@@ -622,36 +636,33 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const uint64_t nl = f2pack(-lse2, -lse2), nd = f2pack(-dl, -dl);
     bool ok = true;
     for (int n = 0; n < total; ++n) {
-      if (masked && valid && n * kBlk + 64 * w < p.Lkv)  // read after S arrives
-        prefetch_l1(static_cast<const uint8_t*>(p.mask) + (moff + n * kBlk + 64 * w) * mes,
-                    min(64, p.Lkv - (n * kBlk + 64 * w)) * mes);
+      const int k0 = n * kBlk + 32 * c;  // first key of this warp's columns
+      if (masked && valid && k0 < p.Lkv)  // read after S arrives
+        prefetch_l1(static_cast<const uint8_t*>(p.mask) + (moff + k0) * mes, min(32, p.Lkv - k0) * mes);
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[n % 2], (n / 2) & 1, wc) &&
                                        mbar_wait(&bars.dp_full, n & 1, wc));
       if (!ok) break;
       tc_fence_after();
-      const int k0 = n * kBlk + 64 * w;  // first key of this half
-      const bool need_mask = (k0 + 64 > p.Lkv) || (p.causal && k0 + 63 > i0 + p.coff);
+      const bool need_mask = (k0 + 32 > p.Lkv) || (p.causal && k0 + 31 > i0 + p.coff);
       // keys k0 + e with e < lim are visible to this query
-      const int lim = min(p.Lkv - k0, p.causal ? i + p.coff - k0 + 1 : 64);
-      const uint32_t s_addr = tmem_addr(tbase, quarter * 32, kColS0 + 128 * (n % 2) + 64 * w);
-      const uint32_t dp_addr = tmem_addr(tbase, quarter * 32, kColDp + 64 * w);
-      // dP and S of this half in one TMEM round trip; the dP buffer is released at once so
-      // that the next block's dP can be computed during this block's math.
-      uint32_t dr[64], sr[64];
-      tmem_ld32(dp_addr, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
-      tmem_ld32(dp_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
-      tmem_ld32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      const int lim = min(p.Lkv - k0, p.causal ? i + p.coff - k0 + 1 : 32);
+      const uint32_t s_addr = tmem_addr(tbase, quarter * 32, kColS0 + 128 * (n % 2) + 32 * c);
+      const uint32_t dp_addr = tmem_addr(tbase, quarter * 32, kColDp + 32 * c);
+      // dP and S of this warp's columns in one TMEM round trip; the dP buffer is released at
+      // once so that the next block's dP can be computed during this block's math.
+      uint32_t dr[32], sr[32];
+      tmem_ld32(dp_addr, dr);
+      tmem_ld32(s_addr, sr);
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&bars.dp_free);
-      // Mask terms of this half's keys as 16-bit pairs (0 past the row's mask pieces: those
+      // Mask terms of this warp's keys as 16-bit pairs (0 past the row's mask pieces: those
       // keys are past Lkv and hidden by lim).
-      uint32_t mk[kMasked ? 32 : 1];
-      if constexpr (kMasked) mask_pairs<T, 64>(mk, p, moff + k0, valid && k0 < p.Lkv ? p.Lkv - k0 : 0);
-      uint32_t dsk[32];
+      uint32_t mk[kMasked ? 16 : 1];
+      if constexpr (kMasked) mask_pairs<T, 32>(mk, p, moff + k0, valid && k0 < p.Lkv ? p.Lkv - k0 : 0);
+      uint32_t dsk[16];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
+      for (int e = 0; e < 16; ++e) {
         float p0, p1;
         uint64_t xx = ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl);
         if constexpr (kMasked) {
@@ -670,52 +681,47 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                  d0, d1);
         dsk[e] = pack2<T>(d0, d1);
       }
-      tmem_st32(s_addr, dsk);  // dS over this half's first 32 columns (all of it read)
+      tmem_st16(s_addr, dsk);  // dS over the first 16 of this warp's columns (all of them read)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars.ds_ready);
     }
-    // Epilogue: dQ·scale staged in the block's Q buffer (the last S MMA has read it) and
-    // written by bulk tensor stores; warpgroup w handles the 64-column blocks cb ≡ w (mod 2).
-    // The staging buffer is one the block's own TMA load fills; with no MMA (total == 0)
-    // nothing else has waited for that load, so wait for it here too.
+    // Epilogue: dQ·scale in D/32 chunks of 32 columns, warpgroup wg taking the chunks whose
+    // index is wg modulo 4, staged in the block's Q buffer (the last S MMA has read it) and
+    // written by bulk tensor stores once all 16 warps have staged theirs.  The staging buffer
+    // is one the block's own TMA load fills; with no MMA (total == 0) nothing else has
+    // waited for that load, so wait for it here too.
     if (ok)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.own_full, 0, wc) && (total == 0 || mbar_wait(&bars.acc_done, 0, wc)));
-    if (w < kCB) {  // the same for every thread of the warpgroup
-      const int r = quarter * 32 + lane;
-      if (ok) {
-        tc_fence_after();
-        const uint32_t a_addr = tmem_addr(tbase, quarter * 32, kColDq);
+    const int r = quarter * 32 + lane;
+    if (ok) {
+      tc_fence_after();
 #pragma unroll 1
-        for (int cb = w; cb < kCB; cb += 2) {
-          uint8_t* blk = sm + L::kQ + cb * kCbStride;
+      for (int c32 = c; c32 < D / 32; c32 += 4) {
+        uint32_t acc[32];
+        if (total > 0) {
+          tmem_ld32(tmem_addr(tbase, quarter * 32, kColDq + 32 * c32), acc);
+          tmem_ld_wait();
+        } else {
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            uint32_t acc[32];
-            if (total > 0) {
-              tmem_ld32(a_addr + cb * 64 + h2 * 32, acc);
-              tmem_ld_wait();
-            } else {
-#pragma unroll
-              for (int e = 0; e < 32; ++e) acc[e] = 0u;
-            }
-            uint32_t packed[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              packed[e] = pack2<T>(__uint_as_float(acc[2 * e]) * p.scale, __uint_as_float(acc[2 * e + 1]) * p.scale);
-#pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              *reinterpret_cast<uint4*>(blk + sw128_off(r, h2 * 4 + v4)) =
-                  make_uint4(packed[4 * v4], packed[4 * v4 + 1], packed[4 * v4 + 2], packed[4 * v4 + 3]);
-          }
+          for (int e = 0; e < 32; ++e) acc[e] = 0u;
         }
-        fence_async_smem();
+        uint32_t packed[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          packed[e] = pack2<T>(__uint_as_float(acc[2 * e]) * p.scale, __uint_as_float(acc[2 * e + 1]) * p.scale);
+        uint8_t* blk = sm + L::kQ + (c32 / 2) * kCbStride;
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4)
+          *reinterpret_cast<uint4*>(blk + sw128_off(r, (c32 % 2) * 4 + v4)) =
+              make_uint4(packed[4 * v4], packed[4 * v4 + 1], packed[4 * v4 + 2], packed[4 * v4 + 3]);
       }
-      if (named_sync_and(1 + w, 128, ok) && r == 0) {
-        for (int cb = w; cb < kCB; cb += 2) tma_store_4d(&tdq, sm + L::kQ + cb * kCbStride, cb * 64, i0, h, b);
-        bulk_commit();
-        bulk_wait_read();
-      }
+      fence_async_smem();
+    }
+    if (named_sync_and(1, 512, ok) && warp == 0 && lane == 0) {
+      for (int cb = 0; cb < kCB; ++cb) tma_store_4d(&tdq, sm + L::kQ + cb * kCbStride, cb * 64, i0, h, b);
+      bulk_commit();
+      bulk_wait_read();
     }
   }
   tc_fence_before();
@@ -749,7 +755,7 @@ cudaError_t dkdv_t(const Problem& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned nkt = (p.Lkv + kRows - 1) / kRows;
-  kern<<<nkt * p.Hkv * p.B, kThreads, smem, s>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv, p);
+  kern<<<nkt * p.Hkv * p.B, kKvThreads, smem, s>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv, p);
   return cudaGetLastError();
 }
 
