@@ -83,6 +83,7 @@ struct Problem {
   unsigned* err;     // device error word
   uint64_t wait_limit_ns;  // time limit of any single bounded wait inside a kernel
   int inject;        // test hook: 1 = the tensor-core forward never delivers its first K tile
+  int num_sms;       // SMs of the device (blocks resident at once in the one-block-per-SM kernels)
   // Layouts of q, k, v, o (forward output / backward input), dout, dq, dk, dv.
   Layout lq, lk, lv, lo, ldo, ldq, ldk, ldv;
   Layout lm;           // mask strides (batch, query head, row; 0 broadcasts), keys contiguous

@@ -135,6 +135,9 @@ int check_sizes(int B, int Hq, int Hkv, int Lq, int Lkv, int D, float scale, int
   p->scale = scale;
   p->scale_log2 = scale * kLog2e;
   p->wait_limit_ns = g_wait_limit_ns.load();
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    p->num_sms = 0;  // no prefetch hints
   return SDPA_OK;
 }
 

@@ -284,6 +284,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cb = 0; cb < kCB; ++cb)
           tma_load_4d(sm + L::kQOff + w * L::kTileBytes + cb * 16384, &tq, &bars.q_full, cb * 64,
                       row0 + w * kBM, h, b);
+      // The block one wave later (about num_sms blocks on) starts when some block ends:
+      // bring its Q tiles into L2 now, so that its first loads come from L2, not HBM.
+      if (p.num_sms > 0 && blockIdx.x + p.num_sms < gridDim.x) {
+        const int nb = blockIdx.x + p.num_sms;
+        const int nu = nb % units, nrank = nb / units;
+        const int nrow0 = (p.causal ? nqb - 1 - nrank : nrank) * kBM * kQTiles;
+        for (int w = 0; w < kQTiles; ++w)
+          if (nrow0 + w * kBM < p.Lq)
+            for (int cb = 0; cb < kCB; ++cb) tma_prefetch_l2_4d(&tq, cb * 64, nrow0 + w * kBM, nu % p.Hq, nu / p.Hq);
+      }
       int issued = 0;
       bool ok = true;
       for (int j = 0; ok && j < nmax; ++j) {
