@@ -26,7 +26,8 @@ bool vector_mma_supported(const Problem& p, int dtype);
 cudaError_t launch_vector_mma_fwd(const Problem& p, int dtype, cudaStream_t s);
 cudaError_t launch_vector_mma_bwd(const Problem& p, int dtype, cudaStream_t s);
 
-// Tensor-core path (TMA + tcgen05), fp16/bf16 with D in {32, 64, 96, 128}.
+// Tensor-core path (TMA + tcgen05), fp16/bf16: forward with D in {32, 64, 96, 128, 256},
+// backward with D in {32, 64, 96, 128}.
 bool tensor_supported(const Problem& p, int dtype);
 bool tensor_bwd_supported(const Problem& p, int dtype);
 cudaError_t launch_tc_fwd(const Problem& p, int dtype, cudaStream_t s);

@@ -432,6 +432,7 @@ extern "C" int sdpa_bwd_masked(const void* q, const void* k, const void* v, cons
       return vector_mma_supported(p, dtype) ? launch_vector_mma_bwd(p, dtype, s) : launch_vector_bwd(p, dtype, s);
     }));
   const bool tc = f == Family::kTensor && tensor_bwd_supported(p, dtype);
+  if (f == Family::kTensor && !tc && g_path.load() == SDPA_PATH_TENSOR) return SDPA_ERR_UNSUPPORTED;
   auto launch_dkdv = [&](cudaStream_t st) {
     return launch_one(SDPA_KERNEL_DKDV, st, [&] {
       return tc ? launch_tc_dkdv(p, dtype, st) : launch_simt_dkdv(p, dtype, st);

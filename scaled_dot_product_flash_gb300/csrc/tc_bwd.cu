@@ -785,7 +785,9 @@ cudaError_t dq_t(const Problem& p, cudaStream_t s) {
 
 }  // namespace
 
-bool tensor_bwd_supported(const Problem& p, int dtype) { return tensor_supported(p, dtype); }
+// D = 256 has no tensor-core backward: dK and dV of 128 keys would take all 512 TMEM
+// columns, and the block's own K and V plus one Q/dO stage would fill shared memory.
+bool tensor_bwd_supported(const Problem& p, int dtype) { return tensor_supported(p, dtype) && p.D <= 128; }
 
 cudaError_t launch_tc_dkdv(const Problem& p, int dtype, cudaStream_t s) {
   if (dtype == 2) {

@@ -494,6 +494,289 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ================================================================== head dim 256
+// One block computes 128 query rows (one Q tile) of one (batch, head).  Tensor memory: two
+// S buffers (columns [0, 128) and [128, 256)) and O (columns [256, 512), all 256 of D),
+// so S of KV tile j+1 is computed into the other buffer while the softmax of tile j runs,
+// and S never waits for a PV product that reads P from the same buffer except two tiles
+// back.  Per KV tile: S = Q·Kᵀ (16 K-steps of M = N = 128) and O += P·V (8 K-steps of
+// M = 128, N = 256).  Shared memory: Q (64 KB), one 64 KB stage for K tiles and one for V
+// tiles.
+// Warp roles (256 threads): warps 0-3 softmax (one thread per query row, all 128 keys of
+// a tile, as in the D <= 128 kernel), 4 and 7 TMA producers (Q and K; V), 5 S issuer (owns
+// TMEM), 6 PV issuer.
+constexpr int k256Threads = 256;
+constexpr int k256Stages = 2;
+struct Fwd256Layout {
+  static constexpr int kCB = 4;                       // 64-column blocks of D
+  static constexpr int kTileBytes = kBM * kCB * 128;  // [128 rows x 256] 16-bit
+  static constexpr int kQOff = 0;
+  static constexpr int kRingOff = kTileBytes;
+  static constexpr int kBytes = kRingOff + k256Stages * kTileBytes;
+};
+struct Fwd256Bars {
+  uint64_t q_full;
+  uint64_t kv_full[k256Stages];
+  uint64_t kv_empty[k256Stages];
+  uint64_t s_full[2];   // S buffer b holds S of KV tile j with j % 2 == b
+  uint64_t p_full[2];   // its P has been written
+  uint64_t pv_done[2];  // PV of that tile has finished (buffer free, O updated)
+  uint64_t fin;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <typename T, bool kMasked>
+__global__ void __launch_bounds__(k256Threads, 1)
+    tc_fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to, Problem p) {
+  using L = Fwd256Layout;
+  constexpr int D = 256, kCB = L::kCB;
+  constexpr bool kBf16 = IsBf16<T>::value;
+  constexpr uint32_t kIdS = idesc_f16(kBM, kBN, kBf16, false, false);
+  constexpr uint32_t kIdO = idesc_f16(kBM, D, kBf16, false, true);
+  constexpr uint32_t kColO = 256;
+  extern __shared__ unsigned char smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ Fwd256Bars bars;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // Block order: all heads of one query tile, then the next; causal: heaviest first.
+  const int units = p.B * p.Hq;
+  const int unit = blockIdx.x % units, rank = blockIdx.x / units;
+  const int b = unit / p.Hq, h = unit % p.Hq, g = h / p.G;
+  const int nqt = (p.Lq + kBM - 1) / kBM;
+  const int row0 = (p.causal ? nqt - 1 - rank : rank) * kBM;
+  const int kend = p.causal ? min(p.Lkv, min(p.Lq, row0 + kBM) + p.coff) : p.Lkv;
+  const int nkv = (kend + kBN - 1) / kBN;  // >= 1
+
+  if (threadIdx.x == 0) {
+    bars.abort = 0;
+    mbar_init(&bars.q_full, 1);
+    for (int s = 0; s < k256Stages; ++s) {
+      mbar_init(&bars.kv_full[s], 1);
+      mbar_init(&bars.kv_empty[s], 1);
+    }
+    for (int c = 0; c < 2; ++c) {
+      mbar_init(&bars.s_full[c], 1);
+      mbar_init(&bars.p_full[c], kBM);
+      mbar_init(&bars.pv_done[c], 1);
+    }
+    mbar_init(&bars.fin, 2);  // one commit per issuer
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&bars.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = bars.tmem_base;
+  const WaitCtx wc{&bars.abort, 0, p.wait_limit_ns, p.err, kKidTcFwd};
+
+  if (warp == 4 || warp == 7) {
+    // ---------------------------------------------------------------- producers
+    // Warp 4 loads Q, then K(j) into stage 0 as soon as S(j-1) has read K(j-1); warp 7
+    // loads V(j) into stage 1 as soon as PV(j-1) has read V(j-1).  Two producers, so that
+    // neither kind of tile waits behind the other.
+    if (lane == 0) {
+      const int kv = warp == 4 ? 0 : 1;
+      if (kv == 0) {
+        prefetch_tmap(&tq);
+        prefetch_tmap(&tk);
+        prefetch_tmap(&to);
+        mbar_arrive_expect_tx(&bars.q_full, L::kTileBytes);
+        for (int cb = 0; cb < kCB; ++cb)
+          tma_load_4d(sm + L::kQOff + cb * 16384, &tq, &bars.q_full, cb * 64, row0, h, b);
+      } else {
+        prefetch_tmap(&tv);
+      }
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; ok && j < nkv; ++j) {
+        if (!(ok = mbar_wait(&bars.kv_empty[kv], (j & 1) ^ 1, wc))) break;
+        if (p.inject == 1 && kv == 0 && j == 0) continue;  // test hook: never deliver the first K tile
+        mbar_arrive_expect_tx(&bars.kv_full[kv], L::kTileBytes);
+        for (int cb = 0; cb < kCB; ++cb)
+          tma_load_4d(sm + L::kRingOff + kv * L::kTileBytes + cb * 16384, kv ? &tv : &tk, &bars.kv_full[kv],
+                      cb * 64, j * kBN, g, b);
+        issued = j + 1;
+      }
+      if ((!ok || bars.abort) && issued > 0)
+        drain_wait(&bars.kv_full[kv], (issued - 1) & 1, 100000000ull);
+    }
+  } else if (warp == 5 || warp == 6) {
+    // ---------------------------------------------------------------- MMA issuers
+    // Warp 5: S(j) = Q·K(j)ᵀ into buffer j % 2 once PV(j-2) has read P(j-2) from it.
+    // Warp 6: O += P(j)·V(j) once the softmax has written P(j).
+    constexpr unsigned kAll = 0xffffffffu;
+    const bool s_issuer = __shfl_sync(kAll, warp, 0) == 5;
+    bool ok = __all_sync(kAll, mbar_wait(&bars.q_full, 0, wc));
+    tc_fence_after();
+    const uint64_t qd = sdesc_sw128(smem_u32(sm + L::kQOff), 16, 1024);
+    const uint32_t ring_s = smem_u32(sm + L::kRingOff);
+    for (int j = 0; ok && j < nkv; ++j) {
+      const int buf = j % 2;
+      if (s_issuer) {
+        // K(j) is ring item 2j, stage 0.
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.kv_full[0], j & 1, wc)))) break;
+        if (j >= 2 && !(ok = __all_sync(kAll, mbar_wait(&bars.pv_done[buf], ((j - 2) / 2) & 1, wc)))) break;
+        tc_fence_after();
+        const uint64_t kd = sdesc_sw128(ring_s, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+          mma_ss_w(tbase + 128 * buf, sdesc_advance(qd, off), sdesc_advance(kd, off), kIdS, kk > 0);
+        }
+        mma_commit_w(&bars.s_full[buf]);
+        mma_commit_w(&bars.kv_empty[0]);
+      } else {
+        // V(j) is ring item 2j + 1, stage 1.
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.p_full[buf], (j / 2) & 1, wc) &&
+                                        mbar_wait(&bars.kv_full[1], j & 1, wc))))
+          break;
+        tc_fence_after();
+        const uint64_t vd = sdesc_sw128(ring_s + L::kTileBytes, 16384, 1024);
+        const uint32_t s_tm = tbase + 128 * buf;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts_w(tbase + kColO, s_tm + kk * 8, sdesc_advance(vd, kk * 2048), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+        if (split_tile<kMasked>(p, j, row0)) {  // remainder of P, columns [64, 128)
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ts_w(tbase + kColO, s_tm + 64 + kk * 8, sdesc_advance(vd, kk * 2048), kIdO, 1u);
+        }
+        mma_commit_w(&bars.pv_done[buf]);
+        mma_commit_w(&bars.kv_empty[1]);
+      }
+    }
+    mma_commit_w(&bars.fin);
+    drain_wait(&bars.fin, 0, 100000000ull);
+  } else if (warp < 4) {
+    // ---------------------------------------------------------------- softmax
+    const int r = warp * 32 + lane;
+    const int i = row0 + r;
+    const uint32_t o_addr = tmem_addr(tbase, warp * 32, kColO);
+    const float c = p.scale_log2;
+    float m = neg_inf(), l = 0.f;
+    bool ok = true;
+    constexpr bool masked = kMasked;
+    const int64_t moff = masked && i < p.Lq ? row_off(p.lm, b, h, i) : 0;
+    const int mes = p.mask_kind == kMaskBool ? 1 : (int)sizeof(T);
+    for (int j = 0; j < nkv; ++j) {
+      const int buf = j % 2;
+      const int k0 = j * kBN;
+      if (masked && i < p.Lq)  // the mask tile's row is read after S arrives (hint only)
+        prefetch_l1(static_cast<const uint8_t*>(p.mask) + (moff + k0) * mes, min(kBN, p.Lkv - k0) * mes);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[buf], (j / 2) & 1, wc));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t s_addr = tmem_addr(tbase, warp * 32, 128 * buf);
+      const bool need_mask = (k0 + kBN > p.Lkv) || (p.causal && k0 + kBN - 1 > row0 + p.coff);
+      uint32_t sv[kBN];
+#pragma unroll
+      for (int q4 = 0; q4 < kBN / 32; ++q4)
+        tmem_ld32(s_addr + 32 * q4, *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * q4]));
+      if constexpr (kMasked) tmem_ld_wait(sv);
+      else tmem_ld_wait();
+      int lim = min(p.Lkv - k0, kBN);
+      if (p.causal) lim = min(lim, i + p.coff - k0 + 1);
+      float cs = c;
+      if constexpr (masked) {
+        if (i < p.Lq) mask_scores<T, kBN>(sv, p, moff + k0, k0, c);
+        cs = 1.f;
+      }
+      const float mt = need_mask ? tile_max<true>(sv, cs, lim) : tile_max<false>(sv, cs, lim);
+      const float m_new = fmaxf(m, mt);
+      const bool resc = m_new > m + kRescale;  // always true on the first tile (m = -inf)
+      const float alpha = resc ? ex2(m - m_new) : 1.f;
+      if (resc) {
+        l *= alpha;
+        m = m_new;
+      }
+      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        // Rescale O once PV(j-1) has landed.
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars.pv_done[(j - 1) % 2], ((j - 1) / 2) & 1, wc));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c32 = 0; c32 < D / 32; ++c32) {
+          uint32_t orr[32];
+          tmem_ld32(o_addr + c32 * 32, orr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+          tmem_st32(o_addr + c32 * 32, orr);
+        }
+        tmem_st_wait();
+      }
+      const float neg_m = (kMasked && m == neg_inf()) ? 0.f : -m;
+      if (split_tile<kMasked>(p, j, row0))
+        l += exp_pass_split<T>(sv, s_addr, cs, neg_m, lim);
+      else if (need_mask)
+        l += exp_pass<T, true>(sv, s_addr, cs, neg_m, lim);
+      else
+        l += exp_pass<T, false>(sv, s_addr, cs, neg_m, lim);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars.p_full[buf]);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.pv_done[(nkv - 1) % 2], ((nkv - 1) / 2) & 1, wc));
+    // O / l staged in the Q buffer (the last S MMA has read it), then bulk tensor stores.
+    uint8_t* stage = sm + L::kQOff;
+    if (ok) {
+      tc_fence_after();
+      const float a = fold_sink(p, h, m, l);
+      const float inv = (!kMasked || l > 0.f) ? a / l : 0.f;
+#pragma unroll 1
+      for (int c32 = 0; c32 < D / 32; ++c32) {
+        uint32_t orr[32];
+        tmem_ld32(o_addr + c32 * 32, orr);
+        tmem_ld_wait();
+        uint32_t packed[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          packed[e] = pack2<T>(__uint_as_float(orr[2 * e]) * inv, __uint_as_float(orr[2 * e + 1]) * inv);
+        uint8_t* blk = stage + (c32 / 2) * 16384;
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4)
+          *reinterpret_cast<uint4*>(blk + sw128_off(r, (c32 % 2) * 4 + v4)) =
+              make_uint4(packed[4 * v4], packed[4 * v4 + 1], packed[4 * v4 + 2], packed[4 * v4 + 3]);
+      }
+      fence_async_smem();
+      if (i < p.Lq && p.lse) p.lse[q_row(p, b, h, i)] = (!kMasked || l > 0.f) ? (m + __log2f(l)) * kLn2 : neg_inf();
+    }
+    if (named_sync_and(1, kBM, ok) && r == 0) {
+      for (int cb = 0; cb < kCB; ++cb) tma_store_4d(&to, stage + cb * 16384, cb * 64, row0, h, b);
+      bulk_commit();
+      bulk_wait_read();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <typename T, bool kMasked>
+cudaError_t tc_fwd256_m(const Problem& p, cudaStream_t s) {
+  CUtensorMap tq, tk, tv, to;
+  if (!make_tmap_4d(&tq, p.q, 256, p.Lq, p.Hq, p.B, p.lq, kBM) || !make_tmap_4d(&to, p.out, 256, p.Lq, p.Hq, p.B, p.lo, kBM) ||
+      !make_tmap_4d(&tk, p.k, 256, p.Lkv, p.Hkv, p.B, p.lk, kBN) ||
+      !make_tmap_4d(&tv, p.v, 256, p.Lkv, p.Hkv, p.B, p.lv, kBN))
+    return cudaErrorInvalidValue;
+  const int smem = Fwd256Layout::kBytes + 1024;
+  auto kern = tc_fwd256_kernel<T, kMasked>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const unsigned nqt = (p.Lq + kBM - 1) / kBM;
+  kern<<<nqt * p.Hq * p.B, k256Threads, smem, s>>>(tq, tk, tv, to, p);
+  return cudaGetLastError();
+}
+
 template <typename T, int D, bool kMasked>
 cudaError_t tc_fwd_m(const Problem& p, cudaStream_t s) {
   CUtensorMap tq, tk, tv, to;
@@ -512,22 +795,25 @@ cudaError_t tc_fwd_m(const Problem& p, cudaStream_t s) {
 
 template <typename T, int D>
 cudaError_t tc_fwd_t(const Problem& p, cudaStream_t s) {
-  return p.mask ? tc_fwd_m<T, D, true>(p, s) : tc_fwd_m<T, D, false>(p, s);
+  if constexpr (D == 256) return p.mask ? tc_fwd256_m<T, true>(p, s) : tc_fwd256_m<T, false>(p, s);
+  else return p.mask ? tc_fwd_m<T, D, true>(p, s) : tc_fwd_m<T, D, false>(p, s);
 }
 
 }  // namespace
 
 bool tensor_supported(const Problem& p, int dtype) {
-  return (dtype == 1 || dtype == 2) && (p.D == 32 || p.D == 64 || p.D == 96 || p.D == 128);
+  return (dtype == 1 || dtype == 2) && (p.D == 32 || p.D == 64 || p.D == 96 || p.D == 128 || p.D == 256);
 }
 
 cudaError_t launch_tc_fwd(const Problem& p, int dtype, cudaStream_t s) {
   if (dtype == 2) {
+    if (p.D == 256) return tc_fwd_t<__nv_bfloat16, 256>(p, s);
     if (p.D == 128) return tc_fwd_t<__nv_bfloat16, 128>(p, s);
     if (p.D == 96) return tc_fwd_t<__nv_bfloat16, 96>(p, s);
     if (p.D == 32) return tc_fwd_t<__nv_bfloat16, 32>(p, s);
     return tc_fwd_t<__nv_bfloat16, 64>(p, s);
   }
+  if (p.D == 256) return tc_fwd_t<__half, 256>(p, s);
   if (p.D == 128) return tc_fwd_t<__half, 128>(p, s);
   if (p.D == 96) return tc_fwd_t<__half, 96>(p, s);
   if (p.D == 32) return tc_fwd_t<__half, 32>(p, s);

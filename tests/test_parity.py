@@ -160,13 +160,34 @@ def test_head_dim_256(shape, dtype, causal):
     full_parity(shape, dtype, causal, seed=31)
 
 
-def test_head_dim_256_is_refused_by_the_tensor_and_short_query_paths():
+@pytest.mark.parametrize("shape,dtype,causal", [
+    (Shape(1, 8, 2, 700, 900, 256), "bf16", True),     # several Q tiles, GQA, ragged tails
+    (Shape(2, 4, 4, 130, 600, 256), "f16", False),     # five KV tiles: both S buffers reused
+    (Shape(1, 4, 1, 257, 257, 256), "bf16", 2),        # bottom-right causal, Lq = Lkv
+    (Shape(1, 2, 2, 64, 96, 256), "f16", True),        # one KV tile: the split P path only
+])
+def test_head_dim_256_forward_on_tensor_cores(shape, dtype, causal):
+    """The fp16/bf16 forward at D = 256 runs on the tensor-core kernel (forced here); its
+    backward runs on the CUDA-core kernels."""
+    with api.force_path(_lib.PATH_TENSOR):
+        full_parity(shape, dtype, causal, seed=32, backward=False)
+    full_parity(shape, dtype, causal, seed=32)
+
+
+def test_head_dim_256_refusals():
+    """The short-query kernels refuse D = 256; the forced tensor path serves the D = 256
+    forward but refuses its backward."""
     q = torch.zeros(1, 2, 4, 256, device="cuda", dtype=torch.bfloat16)
-    for path in (_lib.PATH_TENSOR, _lib.PATH_VECTOR):
-        with api.force_path(path):
-            with pytest.raises(_lib.SdpaError) as e:
-                api.attention_forward(q, q, q)
-            assert e.value.status == 2
+    with api.force_path(_lib.PATH_VECTOR):
+        with pytest.raises(_lib.SdpaError) as e:
+            api.attention_forward(q, q, q)
+        assert e.value.status == 2
+    with api.force_path(_lib.PATH_TENSOR):
+        out, lse = api.attention_forward(q, q, q)
+        with pytest.raises(_lib.SdpaError) as e:
+            api.attention_backward(q, q, q, out, q, lse)
+        assert e.value.status == 2
+    api.poll_status()
 
 
 # ------------------------------------------------------------------ properties

@@ -51,7 +51,9 @@ CASES = [
     (Shape(2, 8, 2, 4, 300, 128), "bf16", False, _lib.PATH_AUTO),       # short query, warp MMA
     (Shape(1, 4, 2, 5, 90, 96), "f32", 2, _lib.PATH_AUTO),              # short query, CUDA cores
     (Shape(3, 4, 4, 1, 77, 64), "f16", False, _lib.PATH_AUTO),          # single query row
-    (Shape(1, 4, 2, 40, 70, 256), "bf16", True, _lib.PATH_AUTO),        # D = 256, CUDA cores
+    (Shape(1, 4, 2, 40, 70, 256), "bf16", True, _lib.PATH_AUTO),        # D = 256: tensor-core forward
+    (Shape(1, 4, 2, 40, 70, 256), "f32", True, _lib.PATH_AUTO),         # D = 256, CUDA cores
+    (Shape(1, 4, 1, 300, 420, 256), "f16", False, _lib.PATH_AUTO),      # D = 256, several KV tiles
 ]
 
 
