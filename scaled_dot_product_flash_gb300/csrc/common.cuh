@@ -16,7 +16,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Error codes written into the device error word (low 16 bits: code, high: kernel id).
 enum DeviceError : unsigned {
   kDevErrNone = 0,
-  kDevErrTimeout = 1,
+  kDevErrTimeout = 1,  // a bounded wait ran out
+  kDevErrLayout = 2,   // a block found its shared memory placed other than its layout assumes
 };
 
 // Kernel ids for the error word.
@@ -152,7 +153,7 @@ __device__ __forceinline__ void mask_scores(uint32_t (&sv)[N], const Problem& p,
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
           const bool keep = ((ws[t / 4] >> (8 * (t % 4))) & 0xffu) != 0u;
-          sv[16 * q + t] = __float_as_uint(keep ? c * __uint_as_float(sv[16 * q + t]) : minus_inf());
+          sv[16 * q + t] = __float_as_uint(fmaf(c, __uint_as_float(sv[16 * q + t]), keep ? 0.f : minus_inf()));
         }
       }
     }
@@ -167,9 +168,9 @@ __device__ __forceinline__ void mask_scores(uint32_t (&sv)[N], const Problem& p,
         w.u = __ldg(m + q);
 #pragma unroll
         for (int t = 0; t < kPer; ++t) {
+          // c·x is finite, so a −inf mask value passes through the fma unchanged.
           const float mv = Elem<T>::to_f(w.e[t]) * kLog2e;
-          const float x = __uint_as_float(sv[kPer * q + t]);
-          sv[kPer * q + t] = __float_as_uint(mv == minus_inf() ? mv : fmaf(c, x, mv));
+          sv[kPer * q + t] = __float_as_uint(fmaf(c, __uint_as_float(sv[kPer * q + t]), mv));
         }
       }
     }

@@ -113,6 +113,8 @@ struct BwdBars {
   uint64_t y_free;        // dK/dV: dK consumed dSᵀ (dPᵀ region free)
   uint64_t dq_done[2];    // dQ: dQ MMA of the block in S buffer i has finished
   uint64_t acc_done;
+  uint64_t mask_full;     // dK/dV, masked: the query block's mask tile has landed
+  uint64_t mask_free;     // dK/dV, masked: every element warp has read it
   uint32_t tmem_base;
   int abort;
   alignas(16) float nlse2[kStages][kBlk];   // dK/dV: −log2e·lse per query (−inf past Lq)
@@ -137,8 +139,23 @@ __device__ __forceinline__ void init_bars(BwdBars& bars) {
   mbar_init(&bars.dq_done[0], 1);
   mbar_init(&bars.dq_done[1], 1);
   mbar_init(&bars.acc_done, 2);  // one commit per MMA issuer
+  mbar_init(&bars.mask_full, 1);
+  mbar_init(&bars.mask_free, 16);  // one arrival per element warp
   fence_mbar_init();
 }
+
+// dK/dV shared memory: the K, V and Q/dO tiles, then (masked instantiation) one [128 queries
+// x 128 keys] mask tile, then the barriers and per-query vectors.  Everything is dynamic
+// shared memory with no static part, whose base is the start of the block's shared window
+// (1024-byte aligned), so the 224 KB of tiles, mask and barriers need no alignment padding.
+template <int D, bool kMasked>
+struct KvSmem {
+  static constexpr int kMask = BwdLayout<D>::kBytes;
+  static constexpr int kMaskBytes = kMasked ? kBlk * kRows * 2 : 0;  // 16-bit or byte elements
+  static constexpr int kBars = kMask + kMaskBytes;
+  static constexpr int kBytes = kBars + (int)sizeof(BwdBars);
+};
+static_assert(KvSmem<128, true>::kBytes <= 227 * 1024, "dK/dV shared memory exceeds the per-block limit");
 
 // Issues C[tmem] = A·Bᵀ for two [128 x D] K-major tiles in shared memory (N = 128).
 // Called by all 32 lanes of the issuing warp; one elected lane issues.
@@ -170,7 +187,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     tc_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                    const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv,
-                   Problem p) {
+                   const __grid_constant__ CUtensorMap tm, Problem p) {
   using L = BwdLayout<D>;
   constexpr int kCB = L::kCB;
   constexpr bool kBf16 = IsBf16<T>::value;
@@ -178,9 +195,17 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   constexpr uint32_t kIdAcc = idesc_f16(kRows, D, kBf16, false, true);
   // TMEM columns: dV, dK, Sᵀ (→ Pᵀ), dPᵀ (→ dSᵀ)
   constexpr uint32_t kColDv = 0, kColDk = 128, kColX = 256, kColY = 384;
+  using SM = KvSmem<D, kMasked>;
   extern __shared__ unsigned char smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ BwdBars bars;
+  // The layout assumes a 1024-byte aligned base (TMA's 128-byte swizzle and the MMA
+  // descriptors need it); should a launch ever place it elsewhere, the block reports an
+  // error and leaves before touching shared memory.
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) report_error(p.err, kDevErrLayout, kKidTcDkdv);
+    return;
+  }
+  uint8_t* sm = smem_raw;
+  BwdBars& bars = *reinterpret_cast<BwdBars*>(sm + SM::kBars);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // Block order: all (batch, KV head) units of one key tile, then the next tile; under the
@@ -232,6 +257,18 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           tma_load_4d(st + L::kTileBytes + cb * L::kCbStride, &tdo, &bars.ring_full[s], cb * 64, i0, h, b);
         }
       }
+      if (kMasked) {
+        // The query block's mask tile, once every element warp has read the previous one.
+        if (n > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bars.mask_free, (n - 1) & 1, wc));
+        if (!ok) break;
+        if (lane == 0) {
+          const int es = p.mask_kind == kMaskBool ? 1 : 2;
+          const bool row_bc = p.lm.sl == 0;  // one row serves every query
+          mbar_arrive_expect_tx(&bars.mask_full, (row_bc ? 1 : kBlk) * kRows * es);
+          tma_load_4d(sm + SM::kMask, &tm, &bars.mask_full, j0, row_bc ? 0 : i0, p.lm.sh == 0 ? 0 : h,
+                      p.lm.sb == 0 ? 0 : b);
+        }
+      }
       // Per-query vectors, negated for the packed math of the element warps.
       const float* lsep = p.lse + q_row(p, b, h, 0);
       const float* dlp = p.delta + q_row(p, b, h, 0);
@@ -248,6 +285,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     if (lane == 0 && (!ok || bars.abort)) {
       for (int n = max(0, issued - kStages); n < issued; ++n)
         drain_wait(&bars.ring_full[n % kStages], (n / kStages) & 1, 100000000ull);
+      if (kMasked && issued > 0) drain_wait(&bars.mask_full, (issued - 1) & 1, 100000000ull);
     }
   } else if (warp == kKvMmaWarp || warp == kKvMmaWarp + 1) {
     // ---------------------------------------------------------------- MMA issuers
@@ -313,20 +351,13 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     const uint32_t y_addr = tmem_addr(tbase, quarter * 32, kColY + 32 * c);
     const uint64_t cc = f2pack(p.scale_log2, p.scale_log2);
     constexpr bool masked = kMasked;  // a separate instantiation carries the mask code
-    const int mes = p.mask_kind == kMaskBool ? 1 : (int)sizeof(T);
     bool ok = true;
     for (int n = 0; n < total; ++n) {
       const int s = n % kStages;
-      const int hm = g * p.G + n / nqb;
       const int i0 = i_begin + (n % nqb) * kBlk + 32 * c;  // first query of this warp's columns
-      if (masked) {  // this warp's 32 keys of its 32 query rows (one row per lane), read after S arrives
-        const int jw = j0 + quarter * 32, iq = i0 + lane;
-        if (iq < p.Lq && jw < p.Lkv)
-          prefetch_l1(static_cast<const uint8_t*>(p.mask) + (row_off(p.lm, b, hm, iq) + jw) * mes,
-                      min(32, p.Lkv - jw) * mes);
-      }
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[0], n & 1, wc) &&
-                                       mbar_wait(&bars.vec_full[s], (n / kStages) & 1, wc));
+                                       mbar_wait(&bars.vec_full[s], (n / kStages) & 1, wc) &&
+                                       (!masked || mbar_wait(&bars.mask_full, n & 1, wc)));
       if (!ok) break;
       tc_fence_after();
       const int ic = i0 + p.coff;  // key j is hidden from query i0 + q when j > ic + q
@@ -343,15 +374,39 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         else tmem_ld_wait();
         uint32_t pk[16];
         if constexpr (masked) {
-          // c·s + log2e·M for this key against the warp's queries (mask 0 for queries past
-          // Lq and keys past Lkv: those P are zero or clipped anyway).
-          const bool jv = j < p.Lkv;
-          const int64_t mo = row_off(p.lm, b, hm, 0) + j;
+          // c·s + log2e·M for this key against the warp's queries, M read from the block's
+          // mask tile in shared memory (row q, key k at element 128q + k; one row when the
+          // mask is broadcast over queries).  Rows past Lq and keys past Lkv were filled with
+          // zeros by the load: those P are zero or clipped anyway.  c·s is finite, so a
+          // hidden key's −inf passes through the fma unchanged.
+          const int k_local = quarter * 32 + lane;
+          if (p.mask_kind == kMaskBool) {
+            const uint8_t* m8 = sm + SM::kMask + k_local;
+            if (p.lm.sl == 0) {
+              const float mv = m8[0] ? 0.f : minus_inf();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float mv = jv && i0 + e < p.Lq ? mask_log2<T>(p, mo + (int64_t)(i0 + e) * p.lm.sl) : 0.f;
-            sr[e] = __float_as_uint(mv == minus_inf() ? mv : fmaf(p.scale_log2, __uint_as_float(sr[e]), mv));
+              for (int e = 0; e < 32; ++e) sr[e] = __float_as_uint(fmaf(p.scale_log2, __uint_as_float(sr[e]), mv));
+            } else {
+              m8 += 32 * c * kRows;
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                sr[e] = __float_as_uint(fmaf(p.scale_log2, __uint_as_float(sr[e]), m8[e * kRows] ? 0.f : minus_inf()));
+            }
+          } else {
+            const T* m16 = reinterpret_cast<const T*>(sm + SM::kMask) + k_local;
+            if (p.lm.sl == 0) {
+              const float mv = Elem<T>::to_f(m16[0]) * kLog2e;
+#pragma unroll
+              for (int e = 0; e < 32; ++e) sr[e] = __float_as_uint(fmaf(p.scale_log2, __uint_as_float(sr[e]), mv));
+            } else {
+              m16 += 32 * c * kRows;
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                sr[e] = __float_as_uint(fmaf(p.scale_log2, __uint_as_float(sr[e]), Elem<T>::to_f(m16[e * kRows]) * kLog2e));
+            }
           }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars.mask_free);  // this warp is done with the mask tile
         }
         const uint64_t ce = masked ? f2pack(1.f, 1.f) : cc;
 #pragma unroll
@@ -761,12 +816,15 @@ template <typename T, int D>
 cudaError_t dkdv_t(const Problem& p, cudaStream_t s) {
   Maps m;
   if (!make_maps(p, D, &m)) return cudaErrorInvalidValue;
-  const int smem = BwdLayout<D>::kBytes + 1024;
+  CUtensorMap tm = m.k;  // unused without a mask
+  if (p.mask && !make_tmap_mask(&tm, p, p.mask_kind == kMaskBool ? 1 : 2, kRows, p.lm.sl == 0 ? 1 : kBlk))
+    return cudaErrorInvalidValue;
+  const int smem = p.mask ? KvSmem<D, true>::kBytes : KvSmem<D, false>::kBytes;
   auto kern = p.mask ? tc_dkdv_kernel<T, D, true> : tc_dkdv_kernel<T, D, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned nkt = (p.Lkv + kRows - 1) / kRows;
-  kern<<<nkt * p.Hkv * p.B, kKvThreads, smem, s>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv, p);
+  kern<<<nkt * p.Hkv * p.B, kKvThreads, smem, s>>>(m.q, m.k, m.v, m.dout, m.dk, m.dv, tm, p);
   return cudaGetLastError();
 }
 

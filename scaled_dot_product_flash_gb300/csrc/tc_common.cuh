@@ -409,5 +409,10 @@ __device__ __forceinline__ void ex2_pair(uint64_t x, float& p0, float& p1) {
 // false if the driver refuses it.
 bool make_tmap_4d(CUtensorMap* map, const void* base, int D, int rows, int heads, int batch, const Layout& l,
                   int box_rows);
+// 4-D tiled map over the attention mask of p ({Lkv, Lq, Hq, B} with the mask's element
+// strides; broadcast dimensions get extent 1), elements of elem_bytes (1: boolean bytes,
+// 2: 16-bit additive values), box {box_keys, box_rows, 1, 1}, no swizzle (row-major tile),
+// zero fill out of bounds.  Returns false if the driver refuses it.
+bool make_tmap_mask(CUtensorMap* map, const Problem& p, int elem_bytes, int box_keys, int box_rows);
 
 }  // namespace sdpa

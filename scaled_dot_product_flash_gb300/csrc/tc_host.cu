@@ -36,4 +36,25 @@ bool make_tmap_4d(CUtensorMap* map, const void* base, int D, int rows, int heads
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_mask(CUtensorMap* map, const Problem& p, int elem_bytes, int box_keys, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  // A dimension with stride 0 is broadcast: it gets extent 1 (coordinate 0 always) and a
+  // nominal stride, since a tensor map wants every stride to be a positive multiple of 16.
+  const int64_t st[3] = {p.lm.sl, p.lm.sh, p.lm.sb};
+  const int64_t ext[3] = {p.Lq, p.Hq, p.B};
+  cuuint64_t dims[4] = {(cuuint64_t)p.Lkv, 1, 1, 1};
+  cuuint64_t strides[3];
+  for (int a = 0; a < 3; ++a) {
+    dims[a + 1] = st[a] == 0 ? 1 : (cuuint64_t)ext[a];
+    strides[a] = st[a] == 0 ? 16 : (cuuint64_t)(st[a] * elem_bytes);
+  }
+  cuuint32_t box[4] = {(cuuint32_t)box_keys, (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
+                  const_cast<void*>(p.mask), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace sdpa
