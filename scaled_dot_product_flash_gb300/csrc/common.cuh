@@ -134,53 +134,12 @@ __device__ __forceinline__ float mask_log2(const Problem& p, int64_t off) {
   return Elem<T>::to_f(static_cast<const T*>(p.mask)[off]) * kLog2e;
 }
 
-// Raw scores of N consecutive keys k0.. of one query row, held as fp32 bits: replaced by
-// c·s + log2e·M (the log2-domain masked score).  `off` is the mask offset of (row, k0).
-// The mask row is read in 16-byte pieces (the ABI requires 16-byte aligned rows readable
-// up to the next multiple of 16 bytes past Lkv); keys at or past Lkv get values the
-// callers ignore (they hide those keys by their key limit).
-template <typename T, int N>
-__device__ __forceinline__ void mask_scores(uint32_t (&sv)[N], const Problem& p, int64_t off, int k0, float c) {
-  const int n = min(N, p.Lkv - k0);
-  if (p.mask_kind == kMaskBool) {
-    const uint4* m = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.mask) + off);
-    const int pieces = (n + 15) / 16;
-#pragma unroll
-    for (int q = 0; q < N / 16; ++q) {
-      if (q < pieces) {
-        const uint4 w = __ldg(m + q);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const bool keep = ((ws[t / 4] >> (8 * (t % 4))) & 0xffu) != 0u;
-          sv[16 * q + t] = __float_as_uint(fmaf(c, __uint_as_float(sv[16 * q + t]), keep ? 0.f : minus_inf()));
-        }
-      }
-    }
-  } else {
-    constexpr int kPer = 16 / sizeof(T);
-    const uint4* m = reinterpret_cast<const uint4*>(static_cast<const T*>(p.mask) + off);
-    const int pieces = (n + kPer - 1) / kPer;
-#pragma unroll
-    for (int q = 0; q < N / kPer; ++q) {
-      if (q < pieces) {
-        union { uint4 u; T e[kPer]; } w;
-        w.u = __ldg(m + q);
-#pragma unroll
-        for (int t = 0; t < kPer; ++t) {
-          // c·x is finite, so a −inf mask value passes through the fma unchanged.
-          const float mv = Elem<T>::to_f(w.e[t]) * kLog2e;
-          sv[kPer * q + t] = __float_as_uint(fmaf(c, __uint_as_float(sv[kPer * q + t]), mv));
-        }
-      }
-    }
-  }
-}
-
 // Mask values of N consecutive keys of one query row as packed pairs of the 16-bit element
 // type T (key 2e in the low half of word e): the additive values as stored, or 0 / −inf
-// for a boolean mask.  Only the 16-byte pieces that hold the first n keys are read (the
-// same row padding rule as mask_scores); the other words are 0.
+// for a boolean mask.  `off` is the mask offset of the first key.  The row is read in
+// 16-byte pieces, and only the pieces that hold the first n keys (the ABI requires 16-byte
+// aligned rows readable up to the next multiple of 16 bytes past Lkv); the other words
+// are 0.
 template <typename T, int N>
 __device__ __forceinline__ void mask_pairs(uint32_t (&mk)[N / 2], const Problem& p, int64_t off, int n) {
   static_assert(sizeof(T) == 2, "16-bit element types only");

@@ -370,8 +370,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       {
         uint32_t sr[32];
         tmem_ld32(x_addr, sr);
-        if constexpr (kMasked) tmem_ld_wait(sr);  // the mask code reads sr with plain arithmetic
-        else tmem_ld_wait();
+        tmem_ld_wait(sr);
         uint32_t pk[16];
         if constexpr (masked) {
           // c·s + log2e·M for this key against the warp's queries, M read from the block's
@@ -432,7 +431,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       {
         uint32_t dr[32];
         tmem_ld32(y_addr, dr);
-        tmem_ld_wait();
+        tmem_ld_wait(dr);
         uint32_t dk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -467,7 +466,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         uint32_t acc[32];
         if (total > 0) {
           tmem_ld32(tmem_addr(tbase, quarter * 32, (is_dk ? kColDk : kColDv) + 32 * c32), acc);
-          tmem_ld_wait();
+          tmem_ld_wait(acc);
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) acc[e] = 0u;  // no query sees these keys
@@ -527,7 +526,10 @@ struct DqBars {
   uint64_t s_full[2];   // one per S buffer
   uint64_t dp_full;
   uint64_t dp_free;     // the element warps have read dP (its buffer may be refilled)
-  uint64_t ds_ready;    // dS packed
+  // dS of the block in S buffer i packed (one barrier per buffer: an element warp may start
+  // block n+1 while another still packs dS(n), and one barrier could not tell their arrivals
+  // apart; block n+2 starts only after dQ(n) has read buffer n % 2, so two suffice)
+  uint64_t ds_ready[2];
   uint64_t dq_done[2];  // dQ MMA of the block in S buffer i has finished
   uint64_t acc_done;
   uint32_t tmem_base;
@@ -577,7 +579,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     mbar_init(&bars.s_full[1], 1);
     mbar_init(&bars.dp_full, 1);
     mbar_init(&bars.dp_free, 512);   // every element thread
-    mbar_init(&bars.ds_ready, 512);
+    mbar_init(&bars.ds_ready[0], 512);
+    mbar_init(&bars.ds_ready[1], 512);
     mbar_init(&bars.dq_done[0], 1);
     mbar_init(&bars.dq_done[1], 1);
     mbar_init(&bars.acc_done, 3);  // one commit per MMA issuer
@@ -672,7 +675,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       for (int n = 0; ok && n < total; ++n) {
         // K(n) is loaded (S(n) read it before dS(n) could exist); waiting on its barrier too
         // makes the TMA writes visible to this warp's MMA directly.
-        if (!(ok = __all_sync(kAll, mbar_wait(&bars.ds_ready, n & 1, wc) &&
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.ds_ready[n % 2], (n / 2) & 1, wc) &&
                                         mbar_wait(&bars.k_full[n % kKStages], (n / kKStages) & 1, wc))))
           break;
         tc_fence_after();
@@ -696,15 +699,17 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const float lse2 = lse == -pos_inf() ? pos_inf() : lse * kLog2e;  // no visible key: P = 0
     const float dl = valid ? p.delta[row] : 0.f;
     constexpr bool masked = kMasked;  // a separate instantiation carries the mask code
-    const int mes = p.mask_kind == kMaskBool ? 1 : (int)sizeof(T);
     const int64_t moff = masked && valid ? row_off(p.lm, b, h, i) : 0;
     const uint64_t cc = f2pack(p.scale_log2, p.scale_log2);
     const uint64_t nl = f2pack(-lse2, -lse2), nd = f2pack(-dl, -dl);
     bool ok = true;
     for (int n = 0; n < total; ++n) {
       const int k0 = n * kBlk + 32 * c;  // first key of this warp's columns
-      if (masked && valid && k0 < p.Lkv)  // read after S arrives
-        prefetch_l1(static_cast<const uint8_t*>(p.mask) + (moff + k0) * mes, min(32, p.Lkv - k0) * mes);
+      // Mask terms of this warp's keys as 16-bit pairs (0 past the row's mask pieces: those
+      // keys are past Lkv and hidden by lim), read before the waits so that the waits hide
+      // their latency.
+      uint32_t mk[kMasked ? 16 : 1];
+      if constexpr (kMasked) mask_pairs<T, 32>(mk, p, moff + k0, valid && k0 < p.Lkv ? p.Lkv - k0 : 0);
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[n % 2], (n / 2) & 1, wc) &&
                                        mbar_wait(&bars.dp_full, n & 1, wc));
       if (!ok) break;
@@ -719,13 +724,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       uint32_t dr[32], sr[32];
       tmem_ld32(dp_addr, dr);
       tmem_ld32(s_addr, sr);
-      tmem_ld_wait();
+      tmem_ld_wait(dr);
+      reg_fence(sr);
       tc_fence_before();
       mbar_arrive(&bars.dp_free);
-      // Mask terms of this warp's keys as 16-bit pairs (0 past the row's mask pieces: those
-      // keys are past Lkv and hidden by lim).
-      uint32_t mk[kMasked ? 16 : 1];
-      if constexpr (kMasked) mask_pairs<T, 32>(mk, p, moff + k0, valid && k0 < p.Lkv ? p.Lkv - k0 : 0);
       uint32_t dsk[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
@@ -750,7 +752,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       tmem_st16(s_addr, dsk);  // dS over the first 16 of this warp's columns (all of them read)
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars.ds_ready);
+      mbar_arrive(&bars.ds_ready[n % 2]);
     }
     // Epilogue: dQ·scale in D/32 chunks of 32 columns, warpgroup wg taking the chunks whose
     // index is wg modulo 4, staged in the block's Q buffer (the last S MMA has read it) and
@@ -767,7 +769,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         uint32_t acc[32];
         if (total > 0) {
           tmem_ld32(tmem_addr(tbase, quarter * 32, kColDq + 32 * c32), acc);
-          tmem_ld_wait();
+          tmem_ld_wait(acc);
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) acc[e] = 0u;
@@ -817,7 +819,7 @@ cudaError_t dkdv_t(const Problem& p, cudaStream_t s) {
   Maps m;
   if (!make_maps(p, D, &m)) return cudaErrorInvalidValue;
   CUtensorMap tm = m.k;  // unused without a mask
-  if (p.mask && !make_tmap_mask(&tm, p, p.mask_kind == kMaskBool ? 1 : 2, kRows, p.lm.sl == 0 ? 1 : kBlk))
+  if (p.mask && !make_tmap_mask(&tm, p, p.mask_kind == kMaskBool ? 1 : 2, kRows, p.lm.sl == 0 ? 1 : kBlk, false))
     return cudaErrorInvalidValue;
   const int smem = p.mask ? KvSmem<D, true>::kBytes : KvSmem<D, false>::kBytes;
   auto kern = p.mask ? tc_dkdv_kernel<T, D, true> : tc_dkdv_kernel<T, D, false>;

@@ -411,8 +411,9 @@ bool make_tmap_4d(CUtensorMap* map, const void* base, int D, int rows, int heads
                   int box_rows);
 // 4-D tiled map over the attention mask of p ({Lkv, Lq, Hq, B} with the mask's element
 // strides; broadcast dimensions get extent 1), elements of elem_bytes (1: boolean bytes,
-// 2: 16-bit additive values), box {box_keys, box_rows, 1, 1}, no swizzle (row-major tile),
-// zero fill out of bounds.  Returns false if the driver refuses it.
-bool make_tmap_mask(CUtensorMap* map, const Problem& p, int elem_bytes, int box_keys, int box_rows);
+// 2: 16-bit additive values), box {box_keys, box_rows, 1, 1}, the 128-byte swizzle if
+// swizzle128 (box_keys · elem_bytes must then be 128) else a row-major tile, zero fill out
+// of bounds.  Returns false if the driver refuses it.
+bool make_tmap_mask(CUtensorMap* map, const Problem& p, int elem_bytes, int box_keys, int box_rows, bool swizzle128);
 
 }  // namespace sdpa

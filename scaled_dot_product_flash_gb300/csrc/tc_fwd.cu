@@ -37,10 +37,11 @@ using namespace tc;
 constexpr int kBM = 128;      // rows per Q tile
 constexpr int kBN = 128;      // keys per KV tile
 constexpr int kQTiles = 2;    // Q tiles per block
-constexpr int kStages = 4;    // K/V ring stages (each one [kBN x D] tile)
-constexpr int kThreads = 384;    // warps 0-7 softmax, 8 producer, 9-10 MMA issuers, 11 idle
+constexpr int kMaxStages = 4;  // K/V ring stages (each one [kBN x D] tile), unmasked kernel
+constexpr int kThreads = 384;    // warps 0-7 softmax, 8 producer, 9-10 MMA issuers, 11 mask producer
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kMaskWarp = 11;
 // Register split (setmaxnreg): the block launches with 168 registers a thread (65,536 / 384
 // rounded down to a multiple of 8, 64,512 in all); warpgroup 2 (producer, issuers, idle
 // warp) drops to 56 and the softmax warpgroups rise to 224: 128·56 + 256·224 = 64,512.
@@ -48,8 +49,14 @@ constexpr int kRegsLow = 56;
 constexpr int kRegsHigh = 224;
 static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * 168, "register split exceeds the launch");
 constexpr float kRescale = 8.f;  // log2 of the largest exponential allowed before rescaling
+// Under an attention mask a KV tile gets the split P when some row's largest P in it exceeds
+// this share of the weight the row has gathered before it (always on its first visible
+// tile).  Below it no single key carries more than an eighth of a row's weight, so the
+// 16-bit rounding of P (relative 2^-9 per key) moves O by at most about 2^-9·|V|/√8 in
+// the mean over the row's keys, as on the unsplit tiles of the unmasked kernel.
+constexpr float kSplitShare = 1.f / 8.f;
 
-template <int D>
+template <int D, bool kMasked>
 struct FwdLayout {
   // Tiles hold ceil(D/64) 64-column blocks (D = 96 is padded to 128 columns: TMA fills
   // the missing columns with zeros on loads and clips them on stores).
@@ -57,20 +64,29 @@ struct FwdLayout {
   static constexpr int kTileBytes = kBM * kCB * 64 * 2;
   static constexpr int kQOff = 0;
   static constexpr int kRingOff = kQTiles * kTileBytes;
-  static constexpr int kBytes = kRingOff + kStages * kTileBytes;
+  // The masked kernel keeps three ring stages (measured as fast as four) to make room for
+  // one [128 x 128] mask tile per Q tile (16-bit values; a boolean tile uses half).
+  static constexpr int kStages = kMasked ? 3 : kMaxStages;
+  static constexpr int kMaskOff = kRingOff + kStages * kTileBytes;
+  static constexpr int kMaskTile = kBM * kBN * 2;
+  static constexpr int kBytes = kMaskOff + (kMasked ? kQTiles * kMaskTile : 0);
   static constexpr int kSCol = 0;    // S_w at column 128·w
   static constexpr int kOCol = 256;  // O_w at column 256 + 128·w
 };
 
 struct FwdBars {
   uint64_t q_full;
-  uint64_t kv_full[kStages];
-  uint64_t kv_empty[kStages];
+  uint64_t kv_full[kMaxStages];
+  uint64_t kv_empty[kMaxStages];
   uint64_t s_full[kQTiles];
   uint64_t p_full[kQTiles];
   uint64_t o_done[kQTiles];
   uint64_t mma_done[kQTiles];
   uint64_t turn[kQTiles];  // exponential pass of Q tile w may start (alternates 0, 1, 0, ...)
+  uint64_t mask_full[kQTiles];  // masked: Q tile w's mask tile for its next KV tile has landed
+  uint64_t mask_free[kQTiles];  // masked: the four warps of warpgroup w have read it
+  uint64_t vote[kQTiles];       // masked: the four warps of warpgroup w have voted on the split
+  int need[kQTiles][2][4];      // masked: warp q of warpgroup w wants the split P for tile j (at j % 2)
   uint32_t tmem_base;
   int abort;
 };
@@ -85,9 +101,130 @@ __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); 
 // KV tile j of Q tile starting at tile_row0 gets the split (head + remainder) P: the first
 // tile of rows that see few keys, and every tile under an attention mask, which can leave
 // any row with few keys of non-negligible weight.
-template <bool kMasked>
 __device__ __forceinline__ bool split_tile(const Problem& p, int j, int tile_row0) {
-  return kMasked || (j == 0 && (tile_row0 == 0 || p.Lkv <= kBN));
+  return j == 0 && (tile_row0 == 0 || p.Lkv <= kBN);
+}
+
+// The split vote of one KV tile under a mask: set when any warp of the warpgroup voted
+// for it (the flags are written before the warps arrive on the vote and P barriers).
+__device__ __forceinline__ bool split_voted(const int (&need)[4]) {
+  const volatile int* v = need;
+  return (v[0] | v[1] | v[2] | v[3]) != 0;
+}
+
+// One 16-byte piece of shared memory, read in program order with the other such reads
+// (a volatile load: the scheduler may not hoist the whole row's pieces at once).
+__device__ __forceinline__ uint4 lds_ordered(const uint8_t* ptr) {
+  uint4 v;
+  asm volatile("ld.volatile.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_u32(ptr)));
+  return v;
+}
+
+// Replicates the top bit of byte t of x over a 32-bit word (prmt's sign-replicate mode).
+__device__ __forceinline__ uint32_t byte_sign(uint32_t x, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(d) : "r"(x), "r"(sel));
+  return d;
+}
+
+// Applies the Q tile's mask to one query row's raw scores sv (fp32 bits) and returns the
+// factor the softmax then applies to them (log2-domain score = factor · sv[e]).  The mask
+// tile in shared memory holds, for a full mask, the 128 rows in the 128-byte swizzle of its
+// TMA load (16-bit values as two 64-key boxes, 16 KB apart) and, for a mask broadcast over
+// queries, one plain row (16-bit: two 64-key halves, 128 bytes apart) that every thread
+// reads.  Keys past Lkv and rows past Lq were filled with zeros; the callers hide such keys
+// by their key limit and never store such rows.
+//   - A row whose mask keeps every key (boolean) or adds 0 to every key (additive) is left
+//     as it is, with the factor c = scale·log2e.
+//   - Boolean, c > 0: a hidden key's raw score becomes −inf (c·−inf = −inf), factor c.
+//   - Boolean, c <= 0: c·s plus 0 or −inf, factor 1.
+//   - Additive: scale·s + M (natural-log domain, −inf stays −inf), factor log2e.
+template <typename T>
+__device__ __forceinline__ float mask_row(uint32_t (&sv)[kBN], const uint8_t* tile, int r, bool row_bc,
+                                          bool is_bool, float c, float scale) {
+  float factor = c;
+  if (is_bool) {
+    auto piece = [&](int q) { return lds_ordered(tile + (row_bc ? 16 * q : sw128_off(r, q))); };
+    uint32_t hidden = 0;  // a zero byte (a hidden key) anywhere in the row
+#pragma unroll 1
+    for (int q = 0; q < kBN / 16; ++q) {
+      const uint4 w = piece(q);
+      hidden |= __vcmpeq4(w.x, 0u) | __vcmpeq4(w.y, 0u) | __vcmpeq4(w.z, 0u) | __vcmpeq4(w.w, 0u);
+    }
+    if (hidden != 0u && c > 0.f) {
+#pragma unroll
+      for (int q = 0; q < kBN / 16; ++q) {
+        const uint4 w = piece(q);
+        const uint32_t keep[4] = {__vcmpne4(w.x, 0u), __vcmpne4(w.y, 0u), __vcmpne4(w.z, 0u), __vcmpne4(w.w, 0u)};
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const uint32_t m = byte_sign(keep[t / 4], 0x8888u | (0x1111u * (t % 4)));
+          sv[16 * q + t] = (sv[16 * q + t] & m) | (0xff800000u & ~m);
+        }
+      }
+    } else if (hidden != 0u) {
+#pragma unroll
+      for (int q = 0; q < kBN / 16; ++q) {
+        const uint4 w = piece(q);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const bool keep = ((ws[t / 4] >> (8 * (t % 4))) & 0xffu) != 0u;
+          sv[16 * q + t] = __float_as_uint(fmaf(c, __uint_as_float(sv[16 * q + t]), keep ? 0.f : neg_inf()));
+        }
+      }
+      factor = 1.f;
+    }
+  } else {
+    auto piece = [&](int q) {
+      const int x = q / 8, qq = q % 8;
+      return lds_ordered(tile + (row_bc ? 128 * x + 16 * qq : 16384 * x + sw128_off(r, qq)));
+    };
+    uint32_t any = 0;  // a nonzero value (+0 and −0 both add nothing)
+#pragma unroll 1
+    for (int q = 0; q < kBN / 8; ++q) {
+      const uint4 w = piece(q);
+      any |= (w.x | w.y | w.z | w.w) & 0x7fff7fffu;
+    }
+    if (any != 0u) {
+#pragma unroll
+      for (int q = 0; q < kBN / 8; ++q) {
+        union { uint4 u; T e[8]; } w;
+        w.u = piece(q);
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+          sv[8 * q + t] = __float_as_uint(fmaf(scale, __uint_as_float(sv[8 * q + t]), Elem<T>::to_f(w.e[t])));
+      }
+      factor = kLog2e;
+    }
+  }
+  return factor;
+}
+
+// The mask tile of rows [row, row + 128) (row 0 of a mask broadcast over queries) and keys
+// [k0, k0 + 128) into dst (1024-byte aligned), completing on bar.  One 128-key box of a
+// boolean mask, two 64-key boxes of a 16-bit one.
+__device__ __forceinline__ void load_mask_tile(uint8_t* dst, const CUtensorMap* tm, uint64_t* bar, const Problem& p,
+                                               int k0, int row, int h, int b) {
+  const bool row_bc = p.lm.sl == 0;
+  const int es = p.mask_kind == kMaskBool ? 1 : 2;
+  mbar_arrive_expect_tx(bar, (row_bc ? 1 : kBM) * kBN * es);
+  const int hh = p.lm.sh == 0 ? 0 : h, bb = p.lm.sb == 0 ? 0 : b, rr = row_bc ? 0 : row;
+  if (es == 1) {
+    tma_load_4d(dst, tm, bar, k0, rr, hh, bb);
+  } else {
+    tma_load_4d(dst, tm, bar, k0, rr, hh, bb);
+    tma_load_4d(dst + (row_bc ? 128 : 16384), tm, bar, k0 + 64, rr, hh, bb);
+  }
+}
+
+// The tensor map of the forward's mask tiles (box and swizzle as mask_row reads them).
+bool make_fwd_mask_map(CUtensorMap* tm, const Problem& p) {
+  const bool row_bc = p.lm.sl == 0;
+  const int es = p.mask_kind == kMaskBool ? 1 : 2;
+  return make_tmap_mask(tm, p, es, es == 1 ? 128 : 64, row_bc ? 1 : kBM, !row_bc);
 }
 
 // Number of leading keys of the tile starting at k0 that row i may see: key k0 + e is
@@ -211,9 +348,11 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
 template <typename T, int D, bool kMasked>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to, Problem p) {
-  using L = FwdLayout<D>;
+                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                  const __grid_constant__ CUtensorMap tm, Problem p) {
+  using L = FwdLayout<D, kMasked>;
   constexpr int kCB = L::kCB;
+  constexpr int kStages = L::kStages;
   constexpr bool kBf16 = IsBf16<T>::value;
   constexpr uint32_t kIdS = idesc_f16(kBM, kBN, kBf16, false, false);
   constexpr uint32_t kIdO = idesc_f16(kBM, D, kBf16, false, true);
@@ -259,6 +398,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars.mma_done[1], 1);
     mbar_init(&bars.turn[0], 4);  // one arrival per warp of the other warpgroup
     mbar_init(&bars.turn[1], 4);
+    for (int w = 0; w < kQTiles; ++w) {
+      mbar_init(&bars.mask_full[w], 1);
+      mbar_init(&bars.mask_free[w], 4);  // one arrival per warp of warpgroup w
+      mbar_init(&bars.vote[w], 4);
+    }
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -352,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
           mma_ts_w(o_tm, s_tm + kk * 8, sdesc_advance(vd, kk * 2048), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-        if (split_tile<kMasked>(p, j, tile_row0)) {  // remainder of P, columns [64, 128)
+        if (kMasked ? split_voted(bars.need[w][j % 2]) : split_tile(p, j, tile_row0)) {  // remainder of P, columns [64, 128)
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
             mma_ts_w(o_tm, s_tm + 64 + kk * 8, sdesc_advance(vd, kk * 2048), kIdO, 1u);
@@ -363,6 +507,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mma_commit_w(&bars.mma_done[w]);
     drain_wait(&bars.mma_done[w], 0, 100000000ull);
+  } else if (kMasked && warp == kMaskWarp) {
+    // Mask producer: Q tile w's mask tile for KV tile j once its four softmax warps have
+    // read the one for KV tile j-1.
+    if (lane == 0) {
+      prefetch_tmap(&tm);
+      int issued[kQTiles] = {0, 0};
+      bool ok = true;
+      for (int j = 0; ok && j < nmax; ++j)
+        for (int w = 0; w < kQTiles; ++w) {
+          if (j >= nkv[w]) continue;
+          if (j > 0 && !(ok = mbar_wait(&bars.mask_free[w], (j - 1) & 1, wc))) break;
+          load_mask_tile(sm + L::kMaskOff + w * L::kMaskTile, &tm, &bars.mask_full[w], p, j * kBN, row0 + w * kBM, h, b);
+          issued[w] = j + 1;
+        }
+      if (!ok || bars.abort)  // let copies still in flight land before the block exits
+        for (int w = 0; w < kQTiles; ++w)
+          if (issued[w] > 0) drain_wait(&bars.mask_full[w], (issued[w] - 1) & 1, 100000000ull);
+    }
   } else if (warp < 8) {
     // Softmax warpgroups.
     regs_inc<kRegsHigh>();
@@ -380,12 +542,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // itself while the tensor core works on the other tile's PV and next S.
     const int nboth = min(nkv[0], nkv[1]);
     constexpr bool masked = kMasked;
-    const int64_t moff = masked && i < p.Lq ? row_off(p.lm, b, h, i) : 0;
+    const uint8_t* mtile = sm + (masked ? L::kMaskOff + w * L::kMaskTile : 0);
+    const bool row_bc = p.lm.sl == 0, mbool = p.mask_kind == kMaskBool;
     for (int j = 0; j < nkv[w]; ++j) {
-      if (masked && i < p.Lq)  // the mask tile's row is read after S arrives (hint only)
-        prefetch_l1(static_cast<const uint8_t*>(p.mask) + (moff + j * kBN) * (p.mask_kind == kMaskBool ? 1 : sizeof(T)),
-                    min(kBN, p.Lkv - j * kBN) * (p.mask_kind == kMaskBool ? 1 : (int)sizeof(T)));
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[w], j & 1, wc));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[w], j & 1, wc) &&
+                                       (!masked || mbar_wait(&bars.mask_full[w], j & 1, wc)));
       if (!ok) break;
       tc_fence_after();
       const int k0 = j * kBN;
@@ -395,14 +556,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int q4 = 0; q4 < kBN / 32; ++q4)
         tmem_ld32(s_addr + 32 * q4, *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * q4]));
-      if constexpr (kMasked) tmem_ld_wait(sv);  // the mask code reads sv with plain arithmetic
-      else tmem_ld_wait();
+      tmem_ld_wait(sv);
       const int lim = visible_keys(p, k0, i);
-      // With a mask the scores become c·s + log2e·M here and are used with a factor of 1.
+      // Under a mask, mask_row applies it and gives the factor the scores are used with.
       float cs = c;
       if constexpr (masked) {
-        if (i < p.Lq) mask_scores<T, kBN>(sv, p, moff + k0, k0, c);
-        cs = 1.f;
+        cs = mask_row<T>(sv, mtile, r, row_bc, mbool, c, p.scale);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.mask_free[w]);  // this warp is done with the mask tile
       }
       const float mt = need_mask ? tile_max<true>(sv, cs, lim) : tile_max<false>(sv, cs, lim);
       const float m_new = fmaxf(m, mt);
@@ -411,6 +572,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (resc) {
         l *= alpha;
         m = m_new;
+      }
+      if constexpr (masked) {
+        // Split vote: this tile's largest P against the weight the row has so far (0 before
+        // its first visible key, so that tile always votes for the split).
+        const float pmax = ex2(mt + (m == neg_inf() ? 0.f : -m));
+        const bool wn = __any_sync(0xffffffffu, pmax > l * kSplitShare);
+        if (lane == 0) {
+          bars.need[w][j % 2][quarter] = wn;
+          mbar_arrive(&bars.vote[w]);
+        }
       }
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
         // Some row of this warp raised its maximum: rescale O once PV(j-1) has landed.
@@ -421,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c32 = 0; c32 < D / 32; ++c32) {
           uint32_t orr[32];
           tmem_ld32(o_addr + c32 * 32, orr);
-          tmem_ld_wait();
+          tmem_ld_wait(orr);
 #pragma unroll
           for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
           tmem_st32(o_addr + c32 * 32, orr);
@@ -436,7 +607,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // m is −inf only while a mask has hidden every key so far; any finite shift then
       // gives P = 0 for those keys.
       const float neg_m = (kMasked && m == neg_inf()) ? 0.f : -m;
-      if (split_tile<kMasked>(p, j, tile_row0))
+      bool split;
+      if constexpr (masked) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars.vote[w], j & 1, wc));
+        if (!ok) break;
+        split = split_voted(bars.need[w][j % 2]);
+      } else {
+        split = split_tile(p, j, tile_row0);
+      }
+      if (split)
         l += exp_pass_split<T>(sv, s_addr, cs, neg_m, lim);
       else if (need_mask)
         l += exp_pass<T, true>(sv, s_addr, cs, neg_m, lim);
@@ -444,11 +623,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         l += exp_pass<T, false>(sv, s_addr, cs, neg_m, lim);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars.p_full[w]);
-      if (j < nboth - w) {  // hand the turn to the other tile
+      // Hand the turn to the other tile before arriving on p_full: P(j) complete then implies
+      // that every warp of this warpgroup has also arrived on the turn barrier for tile j, so
+      // no warp's arrival for tile j+1 can count toward tile j.
+      if (j < nboth - w) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.turn[1 - w]);
       }
+      mbar_arrive(&bars.p_full[w]);
     }
     if (ok && nkv[w] > 0)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_done[w], (nkv[w] - 1) & 1, wc));
@@ -465,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c32 = 0; c32 < D / 32; ++c32) {
           uint32_t orr[32];
           tmem_ld32(o_addr + c32 * 32, orr);
-          tmem_ld_wait();
+          tmem_ld_wait(orr);
           uint32_t packed[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
@@ -501,18 +683,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 // and S never waits for a PV product that reads P from the same buffer except two tiles
 // back.  Per KV tile: S = Q·Kᵀ (16 K-steps of M = N = 128) and O += P·V (8 K-steps of
 // M = 128, N = 256).  Shared memory: Q (64 KB), one 64 KB stage for K tiles and one for V
-// tiles.
+// tiles, and under an attention mask one [128 x 128] mask tile.
 // Warp roles (256 threads): warps 0-3 softmax (one thread per query row, all 128 keys of
-// a tile, as in the D <= 128 kernel), 4 and 7 TMA producers (Q and K; V), 5 S issuer (owns
-// TMEM), 6 PV issuer.
+// a tile, as in the D <= 128 kernel), 4 and 7 TMA producers (Q and K; mask and V), 5 S
+// issuer (owns TMEM), 6 PV issuer.
 constexpr int k256Threads = 256;
 constexpr int k256Stages = 2;
+template <bool kMasked>
 struct Fwd256Layout {
   static constexpr int kCB = 4;                       // 64-column blocks of D
   static constexpr int kTileBytes = kBM * kCB * 128;  // [128 rows x 256] 16-bit
   static constexpr int kQOff = 0;
   static constexpr int kRingOff = kTileBytes;
-  static constexpr int kBytes = kRingOff + k256Stages * kTileBytes;
+  static constexpr int kMaskOff = kRingOff + k256Stages * kTileBytes;
+  static constexpr int kBytes = kMaskOff + (kMasked ? kBM * kBN * 2 : 0);
 };
 struct Fwd256Bars {
   uint64_t q_full;
@@ -522,6 +706,12 @@ struct Fwd256Bars {
   uint64_t p_full[2];   // its P has been written
   uint64_t pv_done[2];  // PV of that tile has finished (buffer free, O updated)
   uint64_t fin;
+  uint64_t mask_full;   // masked: the mask tile of the next KV tile has landed
+  uint64_t mask_free;   // masked: the four softmax warps have read it
+  uint64_t vote;        // masked: the four softmax warps have voted on the split
+  // masked: softmax warp q wants the split P for KV tile j (at j % 2: a warp may vote on
+  // tile j+1 before another warp or the PV issuer has read the votes on tile j)
+  int need[2][4];
   uint32_t tmem_base;
   int abort;
 };
@@ -529,8 +719,9 @@ struct Fwd256Bars {
 template <typename T, bool kMasked>
 __global__ void __launch_bounds__(k256Threads, 1)
     tc_fwd256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to, Problem p) {
-  using L = Fwd256Layout;
+                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                     const __grid_constant__ CUtensorMap tm, Problem p) {
+  using L = Fwd256Layout<kMasked>;
   constexpr int D = 256, kCB = L::kCB;
   constexpr bool kBf16 = IsBf16<T>::value;
   constexpr uint32_t kIdS = idesc_f16(kBM, kBN, kBf16, false, false);
@@ -563,6 +754,9 @@ __global__ void __launch_bounds__(k256Threads, 1)
       mbar_init(&bars.pv_done[c], 1);
     }
     mbar_init(&bars.fin, 2);  // one commit per issuer
+    mbar_init(&bars.mask_full, 1);
+    mbar_init(&bars.mask_free, 4);  // one arrival per softmax warp
+    mbar_init(&bars.vote, 4);
     fence_mbar_init();
   }
   if (warp == 5) {
@@ -578,8 +772,9 @@ __global__ void __launch_bounds__(k256Threads, 1)
   if (warp == 4 || warp == 7) {
     // ---------------------------------------------------------------- producers
     // Warp 4 loads Q, then K(j) into stage 0 as soon as S(j-1) has read K(j-1); warp 7
-    // loads V(j) into stage 1 as soon as PV(j-1) has read V(j-1).  Two producers, so that
-    // neither kind of tile waits behind the other.
+    // loads V(j) into stage 1 as soon as PV(j-1) has read V(j-1), and before it (masked)
+    // the mask tile of KV tile j once the softmax warps have read that of tile j-1.  Two
+    // producers, so that neither kind of tile waits behind the other.
     if (lane == 0) {
       const int kv = warp == 4 ? 0 : 1;
       if (kv == 0) {
@@ -591,10 +786,16 @@ __global__ void __launch_bounds__(k256Threads, 1)
           tma_load_4d(sm + L::kQOff + cb * 16384, &tq, &bars.q_full, cb * 64, row0, h, b);
       } else {
         prefetch_tmap(&tv);
+        if (kMasked) prefetch_tmap(&tm);
       }
-      int issued = 0;
+      int issued = 0, m_issued = 0;
       bool ok = true;
       for (int j = 0; ok && j < nkv; ++j) {
+        if (kMasked && kv == 1) {
+          if (j > 0 && !(ok = mbar_wait(&bars.mask_free, (j - 1) & 1, wc))) break;
+          load_mask_tile(sm + L::kMaskOff, &tm, &bars.mask_full, p, j * kBN, row0, h, b);
+          m_issued = j + 1;
+        }
         if (!(ok = mbar_wait(&bars.kv_empty[kv], (j & 1) ^ 1, wc))) break;
         if (p.inject == 1 && kv == 0 && j == 0) continue;  // test hook: never deliver the first K tile
         mbar_arrive_expect_tx(&bars.kv_full[kv], L::kTileBytes);
@@ -605,6 +806,8 @@ __global__ void __launch_bounds__(k256Threads, 1)
       }
       if ((!ok || bars.abort) && issued > 0)
         drain_wait(&bars.kv_full[kv], (issued - 1) & 1, 100000000ull);
+      if ((!ok || bars.abort) && m_issued > 0)
+        drain_wait(&bars.mask_full, (m_issued - 1) & 1, 100000000ull);
     }
   } else if (warp == 5 || warp == 6) {
     // ---------------------------------------------------------------- MMA issuers
@@ -642,7 +845,7 @@ __global__ void __launch_bounds__(k256Threads, 1)
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
           mma_ts_w(tbase + kColO, s_tm + kk * 8, sdesc_advance(vd, kk * 2048), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-        if (split_tile<kMasked>(p, j, row0)) {  // remainder of P, columns [64, 128)
+        if (kMasked ? split_voted(bars.need[j % 2]) : split_tile(p, j, row0)) {  // remainder of P, columns [64, 128)
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
             mma_ts_w(tbase + kColO, s_tm + 64 + kk * 8, sdesc_advance(vd, kk * 2048), kIdO, 1u);
@@ -662,14 +865,12 @@ __global__ void __launch_bounds__(k256Threads, 1)
     float m = neg_inf(), l = 0.f;
     bool ok = true;
     constexpr bool masked = kMasked;
-    const int64_t moff = masked && i < p.Lq ? row_off(p.lm, b, h, i) : 0;
-    const int mes = p.mask_kind == kMaskBool ? 1 : (int)sizeof(T);
+    const bool row_bc = p.lm.sl == 0, mbool = p.mask_kind == kMaskBool;
     for (int j = 0; j < nkv; ++j) {
       const int buf = j % 2;
       const int k0 = j * kBN;
-      if (masked && i < p.Lq)  // the mask tile's row is read after S arrives (hint only)
-        prefetch_l1(static_cast<const uint8_t*>(p.mask) + (moff + k0) * mes, min(kBN, p.Lkv - k0) * mes);
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[buf], (j / 2) & 1, wc));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[buf], (j / 2) & 1, wc) &&
+                                       (!masked || mbar_wait(&bars.mask_full, j & 1, wc)));
       if (!ok) break;
       tc_fence_after();
       const uint32_t s_addr = tmem_addr(tbase, warp * 32, 128 * buf);
@@ -678,14 +879,14 @@ __global__ void __launch_bounds__(k256Threads, 1)
 #pragma unroll
       for (int q4 = 0; q4 < kBN / 32; ++q4)
         tmem_ld32(s_addr + 32 * q4, *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * q4]));
-      if constexpr (kMasked) tmem_ld_wait(sv);
-      else tmem_ld_wait();
+      tmem_ld_wait(sv);
       int lim = min(p.Lkv - k0, kBN);
       if (p.causal) lim = min(lim, i + p.coff - k0 + 1);
       float cs = c;
       if constexpr (masked) {
-        if (i < p.Lq) mask_scores<T, kBN>(sv, p, moff + k0, k0, c);
-        cs = 1.f;
+        cs = mask_row<T>(sv, sm + L::kMaskOff, r, row_bc, mbool, c, p.scale);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.mask_free);  // this warp is done with the mask tile
       }
       const float mt = need_mask ? tile_max<true>(sv, cs, lim) : tile_max<false>(sv, cs, lim);
       const float m_new = fmaxf(m, mt);
@@ -694,6 +895,14 @@ __global__ void __launch_bounds__(k256Threads, 1)
       if (resc) {
         l *= alpha;
         m = m_new;
+      }
+      if constexpr (masked) {  // split vote, as in the D <= 128 kernel
+        const float pmax = ex2(mt + (m == neg_inf() ? 0.f : -m));
+        const bool wn = __any_sync(0xffffffffu, pmax > l * kSplitShare);
+        if (lane == 0) {
+          bars.need[j % 2][warp] = wn;
+          mbar_arrive(&bars.vote);
+        }
       }
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
         // Rescale O once PV(j-1) has landed.
@@ -704,7 +913,7 @@ __global__ void __launch_bounds__(k256Threads, 1)
         for (int c32 = 0; c32 < D / 32; ++c32) {
           uint32_t orr[32];
           tmem_ld32(o_addr + c32 * 32, orr);
-          tmem_ld_wait();
+          tmem_ld_wait(orr);
 #pragma unroll
           for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
           tmem_st32(o_addr + c32 * 32, orr);
@@ -712,7 +921,15 @@ __global__ void __launch_bounds__(k256Threads, 1)
         tmem_st_wait();
       }
       const float neg_m = (kMasked && m == neg_inf()) ? 0.f : -m;
-      if (split_tile<kMasked>(p, j, row0))
+      bool split;
+      if constexpr (masked) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars.vote, j & 1, wc));
+        if (!ok) break;
+        split = split_voted(bars.need[j % 2]);
+      } else {
+        split = split_tile(p, j, row0);
+      }
+      if (split)
         l += exp_pass_split<T>(sv, s_addr, cs, neg_m, lim);
       else if (need_mask)
         l += exp_pass<T, true>(sv, s_addr, cs, neg_m, lim);
@@ -733,7 +950,7 @@ __global__ void __launch_bounds__(k256Threads, 1)
       for (int c32 = 0; c32 < D / 32; ++c32) {
         uint32_t orr[32];
         tmem_ld32(o_addr + c32 * 32, orr);
-        tmem_ld_wait();
+        tmem_ld_wait(orr);
         uint32_t packed[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
@@ -768,12 +985,14 @@ cudaError_t tc_fwd256_m(const Problem& p, cudaStream_t s) {
       !make_tmap_4d(&tk, p.k, 256, p.Lkv, p.Hkv, p.B, p.lk, kBN) ||
       !make_tmap_4d(&tv, p.v, 256, p.Lkv, p.Hkv, p.B, p.lv, kBN))
     return cudaErrorInvalidValue;
-  const int smem = Fwd256Layout::kBytes + 1024;
+  CUtensorMap tm = tq;  // unused without a mask
+  if (kMasked && !make_fwd_mask_map(&tm, p)) return cudaErrorInvalidValue;
+  const int smem = Fwd256Layout<kMasked>::kBytes + 1024;
   auto kern = tc_fwd256_kernel<T, kMasked>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned nqt = (p.Lq + kBM - 1) / kBM;
-  kern<<<nqt * p.Hq * p.B, k256Threads, smem, s>>>(tq, tk, tv, to, p);
+  kern<<<nqt * p.Hq * p.B, k256Threads, smem, s>>>(tq, tk, tv, to, tm, p);
   return cudaGetLastError();
 }
 
@@ -784,12 +1003,14 @@ cudaError_t tc_fwd_m(const Problem& p, cudaStream_t s) {
       !make_tmap_4d(&tk, p.k, D, p.Lkv, p.Hkv, p.B, p.lk, kBN) ||
       !make_tmap_4d(&tv, p.v, D, p.Lkv, p.Hkv, p.B, p.lv, kBN))
     return cudaErrorInvalidValue;
-  const int smem = FwdLayout<D>::kBytes + 1024;
+  CUtensorMap tm = tq;  // unused without a mask
+  if (kMasked && !make_fwd_mask_map(&tm, p)) return cudaErrorInvalidValue;
+  const int smem = FwdLayout<D, kMasked>::kBytes + 1024;
   auto kern = tc_fwd_kernel<T, D, kMasked>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned nqb = (p.Lq + kBM * kQTiles - 1) / (kBM * kQTiles);
-  kern<<<nqb * p.Hq * p.B, kThreads, smem, s>>>(tq, tk, tv, to, p);
+  kern<<<nqb * p.Hq * p.B, kThreads, smem, s>>>(tq, tk, tv, to, tm, p);
   return cudaGetLastError();
 }
 

@@ -36,7 +36,7 @@ bool make_tmap_4d(CUtensorMap* map, const void* base, int D, int rows, int heads
   return r == CUDA_SUCCESS;
 }
 
-bool make_tmap_mask(CUtensorMap* map, const Problem& p, int elem_bytes, int box_keys, int box_rows) {
+bool make_tmap_mask(CUtensorMap* map, const Problem& p, int elem_bytes, int box_keys, int box_rows, bool swizzle128) {
   auto fn = encode_fn();
   if (!fn) return false;
   // A dimension with stride 0 is broadcast: it gets extent 1 (coordinate 0 always) and a
@@ -53,7 +53,8 @@ bool make_tmap_mask(CUtensorMap* map, const Problem& p, int elem_bytes, int box_
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(map, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 4,
                   const_cast<void*>(p.mask), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 

@@ -5,10 +5,12 @@ mask gradients among what the Metal backward leaves unfused; "mps-flash-sdpa 0.1
 section "When MFA Dispatches vs. Falls Back", hands every mask with a False entry back).
 GPU results are compared element by element with the CPU oracle at the parity tolerances.
 
-Masks are drawn from fixed seeds in four shapes: a random boolean mask per (batch, head)
+Masks are drawn from fixed seeds in five shapes: a random boolean mask per (batch, head)
 keeping 70% of the keys, an additive N(0, 2²) mask per head with 20% −inf entries, a
-per-batch key-padding mask, and one additive [Lq, Lkv] mask shared by every batch and
-head.  The first two each hide one whole row (O = 0, lse = −inf, zero gradients).
+per-batch key-padding mask, one additive [Lq, Lkv] mask shared by every batch and head,
+and a sparse boolean mask keeping about three keys a row (the output of such a row rests
+on a few weights).  The first two each hide one whole row (O = 0, lse = −inf, zero
+gradients).
 """
 import math
 
@@ -33,6 +35,12 @@ def make_mask(kind, shape, seed, dtype):
         m[0, 0, min(3, Lq - 1)] = False
         t = torch.from_numpy(m)
         return t, m
+    if kind == "sparse":
+        # about three visible keys per row, spread over the KV tiles: the rows whose output
+        # rests on a few weights, where rounding P to 16 bits shows most
+        m = rng.random((B, Hq, Lq, Lkv)) < 3.0 / Lkv
+        m[..., 0] |= ~m.any(axis=-1)
+        return torch.from_numpy(m), m
     if kind == "padding":
         m = np.zeros((B, 1, 1, Lkv), dtype=bool)
         for b in range(B):
@@ -98,6 +106,8 @@ CASES = [
     (Shape(1, 4, 2, 50, 77, 256), "f16", False, _lib.PATH_AUTO, "additive"),     # D = 256: tensor-core forward
     (Shape(1, 4, 2, 200, 330, 256), "bf16", True, _lib.PATH_AUTO, "bool"),       # D = 256, several KV tiles
     (Shape(1, 4, 2, 50, 77, 256), "f32", False, _lib.PATH_AUTO, "padding"),      # D = 256, CUDA cores
+    (Shape(2, 4, 2, 260, 520, 128), "bf16", False, _lib.PATH_AUTO, "sparse"),    # few keys a row, MMA
+    (Shape(1, 4, 2, 130, 400, 256), "bf16", False, _lib.PATH_AUTO, "sparse"),    # few keys a row, D = 256
 ]
 
 
