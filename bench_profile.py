@@ -3,10 +3,13 @@
 timing.  Every launch goes through the C ABI exactly as in normal use.
 
   python bench_profile.py --op fwd|bwd|step \\
-      --B 2 --Hq 32 --Hkv 8 --L 4096 --D 128 --dtype bf16 --causal --iters 4
+      --B 2 --Hq 32 --Hkv 8 --L 4096 --D 128 --dtype bf16 --causal --iters 4 \\
+      [--mask padding|additive]
 
---L is Lq (and Lkv unless --Lkv is given).  Prints the mean CUDA-event time per call
-(after one warm-up call).
+--L is Lq (and Lkv unless --Lkv is given).  --mask padding passes a boolean key-padding
+mask [B, 1, 1, Lkv] hiding the last 10% of the keys; --mask additive passes one N(0, 1)
+[Lq, Lkv] mask in the element type, shared by every batch and head (seed 6).  Prints the
+mean CUDA-event time per call (after one warm-up call).
 """
 from __future__ import annotations
 
@@ -36,23 +39,33 @@ def main():
     ap.add_argument("--causal", action="store_true")
     ap.add_argument("--path", default="auto", choices=["auto", "tensor", "simt", "vector"])
     ap.add_argument("--iters", type=int, default=4)
+    ap.add_argument("--mask", default="none", choices=["none", "padding", "additive"])
     a = ap.parse_args()
     shape = Shape(a.B, a.Hq, a.Hkv, a.L, a.Lkv or a.L, a.D)
     q, k, v, do = (t.cuda() for t in draw(shape, 3, a.dtype))
     scale = 1.0 / math.sqrt(a.D)
+    Lkv = a.Lkv or a.L
+    mask = None
+    if a.mask == "padding":
+        mask = torch.ones(a.B, 1, 1, Lkv, dtype=torch.bool, device="cuda")
+        mask[..., int(0.9 * Lkv):] = False
+    elif a.mask == "additive":
+        gen = torch.Generator(device="cpu").manual_seed(6)
+        mask = torch.randn(a.L, Lkv, generator=gen).to(q.dtype).cuda()
     path = {"auto": _lib.PATH_AUTO, "tensor": _lib.PATH_TENSOR, "simt": _lib.PATH_SIMT,
             "vector": _lib.PATH_VECTOR}[a.path]
     with api.force_path(path):
-        out, lse = api.attention_forward(q, k, v, scale=scale, is_causal=a.causal)
+        out, lse = api.attention_forward(q, k, v, scale=scale, is_causal=a.causal, attn_mask=mask)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         ws = torch.empty(max(16, api.workspace_bytes(q, k)), device="cuda", dtype=torch.uint8)
 
         def once():
             if a.op in ("fwd", "step"):
-                api.attention_forward(q, k, v, scale=scale, is_causal=a.causal, out=out, lse=lse)
+                api.attention_forward(q, k, v, scale=scale, is_causal=a.causal, out=out, lse=lse,
+                                      attn_mask=mask)
             if a.op in ("bwd", "step"):
                 api.attention_backward(q, k, v, out, do, lse, scale=scale, is_causal=a.causal,
-                                       workspace=ws, dq=dq, dk=dk, dv=dv)
+                                       workspace=ws, dq=dq, dk=dk, dv=dv, attn_mask=mask)
 
         once()
         api.poll_status()

@@ -51,10 +51,11 @@ static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * 168, "register spli
 constexpr float kRescale = 8.f;  // log2 of the largest exponential allowed before rescaling
 // Under an attention mask a KV tile gets the split P when some row's largest P in it exceeds
 // this share of the weight the row has gathered before it (always on its first visible
-// tile).  Below it no single key carries more than an eighth of a row's weight, so the
-// 16-bit rounding of P (relative 2^-9 per key) moves O by at most about 2^-9·|V|/√8 in
-// the mean over the row's keys, as on the unsplit tiles of the unmasked kernel.
-constexpr float kSplitShare = 1.f / 8.f;
+// tile).  On the other tiles no key holds more than a quarter of its row's weight when its
+// tile arrives, so rounding P to 16 bits (relative 2^-9 per key) moves O by at most
+// 2^-9·max|V| over all such keys together, the bound the unmasked kernel has on every tile
+// after its first; a row resting on a few keys still gets the split on their tiles.
+constexpr float kSplitShare = 1.f / 4.f;
 
 template <int D, bool kMasked>
 struct FwdLayout {
@@ -122,6 +123,13 @@ __device__ __forceinline__ uint4 lds_ordered(const uint8_t* ptr) {
   return v;
 }
 
+// Bit 7 of each byte of the result is set iff that byte of w is nonzero (the low seven
+// bits plus 0x7f carry into bit 7 when any of them is set, without crossing into the next
+// byte; or-ing w adds bit 7 itself); the other bits are zero.
+__device__ __forceinline__ uint32_t nonzero_bytes(uint32_t w) {
+  return (((w & 0x7f7f7f7fu) + 0x7f7f7f7fu) | w) & 0x80808080u;
+}
+
 // Replicates the top bit of byte t of x over a 32-bit word (prmt's sign-replicate mode).
 __device__ __forceinline__ uint32_t byte_sign(uint32_t x, uint32_t sel) {
   uint32_t d;
@@ -133,74 +141,79 @@ __device__ __forceinline__ uint32_t byte_sign(uint32_t x, uint32_t sel) {
 // factor the softmax then applies to them (log2-domain score = factor · sv[e]).  The mask
 // tile in shared memory holds, for a full mask, the 128 rows in the 128-byte swizzle of its
 // TMA load (16-bit values as two 64-key boxes, 16 KB apart) and, for a mask broadcast over
-// queries, one plain row (16-bit: two 64-key halves, 128 bytes apart) that every thread
-// reads.  Keys past Lkv and rows past Lq were filled with zeros; the callers hide such keys
-// by their key limit and never store such rows.
-//   - A row whose mask keeps every key (boolean) or adds 0 to every key (additive) is left
-//     as it is, with the factor c = scale·log2e.
+// queries, one plain row (128 bytes boolean, 256 bytes 16-bit) that every thread reads.
+// Keys past Lkv and rows past Lq were filled with zeros; the callers hide such keys by
+// their key limit and never store such rows.
+//   - A broadcast row that keeps every key (boolean) or adds 0 to every key (additive) is
+//     left as it is, with the factor c = scale·log2e; the warp checks it together (each
+//     lane one slice of the row, then a vote).
 //   - Boolean, c > 0: a hidden key's raw score becomes −inf (c·−inf = −inf), factor c.
 //   - Boolean, c <= 0: c·s plus 0 or −inf, factor 1.
 //   - Additive: scale·s + M (natural-log domain, −inf stays −inf), factor log2e.
-template <typename T>
-__device__ __forceinline__ float mask_row(uint32_t (&sv)[kBN], const uint8_t* tile, int r, bool row_bc,
+// kOrdered reads the pieces with ordered (volatile) loads, which keeps the scheduler from
+// hoisting them all at once where registers are short (the D = 256 kernel).
+template <typename T, bool kOrdered>
+__device__ __forceinline__ float mask_row(uint32_t (&sv)[kBN], const uint8_t* tile, int r, int lane, bool row_bc,
                                           bool is_bool, float c, float scale) {
-  float factor = c;
-  if (is_bool) {
-    auto piece = [&](int q) { return lds_ordered(tile + (row_bc ? 16 * q : sw128_off(r, q))); };
-    uint32_t hidden = 0;  // a zero byte (a hidden key) anywhere in the row
-#pragma unroll 1
+  if (row_bc) {
+    bool any;
+    if (is_bool) {
+      const uint32_t w = *reinterpret_cast<const volatile uint32_t*>(tile + 4 * lane);
+      any = __any_sync(0xffffffffu, nonzero_bytes(w) != 0x80808080u);  // some key hidden
+    } else {
+      const volatile uint32_t* v = reinterpret_cast<const volatile uint32_t*>(tile + 8 * lane);
+      any = __any_sync(0xffffffffu, ((v[0] | v[1]) & 0x7fff7fffu) != 0u);  // some value nonzero
+    }
+    if (!any) return c;
+  }
+  auto piece = [&](int q) {  // the q-th 16-byte piece of the row
+    const int x = q / 8, qq = q % 8;
+    const uint8_t* a = is_bool ? tile + (row_bc ? 16 * q : sw128_off(r, q))
+                               : tile + (row_bc ? 128 * x + 16 * qq : 16384 * x + sw128_off(r, qq));
+    return kOrdered ? lds_ordered(a) : *reinterpret_cast<const uint4*>(a);
+  };
+  if (is_bool && c > 0.f) {
+#pragma unroll
     for (int q = 0; q < kBN / 16; ++q) {
       const uint4 w = piece(q);
-      hidden |= __vcmpeq4(w.x, 0u) | __vcmpeq4(w.y, 0u) | __vcmpeq4(w.z, 0u) | __vcmpeq4(w.w, 0u);
-    }
-    if (hidden != 0u && c > 0.f) {
+      const uint32_t keep[4] = {nonzero_bytes(w.x), nonzero_bytes(w.y), nonzero_bytes(w.z), nonzero_bytes(w.w)};
 #pragma unroll
-      for (int q = 0; q < kBN / 16; ++q) {
-        const uint4 w = piece(q);
-        const uint32_t keep[4] = {__vcmpne4(w.x, 0u), __vcmpne4(w.y, 0u), __vcmpne4(w.z, 0u), __vcmpne4(w.w, 0u)};
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const uint32_t m = byte_sign(keep[t / 4], 0x8888u | (0x1111u * (t % 4)));
-          sv[16 * q + t] = (sv[16 * q + t] & m) | (0xff800000u & ~m);
-        }
+      for (int t = 0; t < 16; ++t) {
+        const uint32_t m = byte_sign(keep[t / 4], 0x8888u | (0x1111u * (t % 4)));
+        sv[16 * q + t] = (sv[16 * q + t] & m) | (0xff800000u & ~m);
       }
-    } else if (hidden != 0u) {
-#pragma unroll
-      for (int q = 0; q < kBN / 16; ++q) {
-        const uint4 w = piece(q);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const bool keep = ((ws[t / 4] >> (8 * (t % 4))) & 0xffu) != 0u;
-          sv[16 * q + t] = __float_as_uint(fmaf(c, __uint_as_float(sv[16 * q + t]), keep ? 0.f : neg_inf()));
-        }
-      }
-      factor = 1.f;
     }
-  } else {
-    auto piece = [&](int q) {
-      const int x = q / 8, qq = q % 8;
-      return lds_ordered(tile + (row_bc ? 128 * x + 16 * qq : 16384 * x + sw128_off(r, qq)));
-    };
-    uint32_t any = 0;  // a nonzero value (+0 and −0 both add nothing)
-#pragma unroll 1
-    for (int q = 0; q < kBN / 8; ++q) {
+    return c;
+  }
+  if (is_bool) {
+#pragma unroll
+    for (int q = 0; q < kBN / 16; ++q) {
       const uint4 w = piece(q);
-      any |= (w.x | w.y | w.z | w.w) & 0x7fff7fffu;
-    }
-    if (any != 0u) {
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int q = 0; q < kBN / 8; ++q) {
-        union { uint4 u; T e[8]; } w;
-        w.u = piece(q);
-#pragma unroll
-        for (int t = 0; t < 8; ++t)
-          sv[8 * q + t] = __float_as_uint(fmaf(scale, __uint_as_float(sv[8 * q + t]), Elem<T>::to_f(w.e[t])));
+      for (int t = 0; t < 16; ++t) {
+        const bool keep = ((ws[t / 4] >> (8 * (t % 4))) & 0xffu) != 0u;
+        sv[16 * q + t] = __float_as_uint(fmaf(c, __uint_as_float(sv[16 * q + t]), keep ? 0.f : neg_inf()));
       }
-      factor = kLog2e;
+    }
+    return 1.f;
+  }
+  const uint64_t sc = f2pack(scale, scale);
+#pragma unroll
+  for (int q = 0; q < kBN / 8; ++q) {
+    union { uint4 u; T e[8]; } w;
+    w.u = piece(q);
+#pragma unroll
+    for (int t = 0; t < 8; t += 2) {
+      float a, b;
+      f2unpack(ffma2(sc, f2pack(__uint_as_float(sv[8 * q + t]), __uint_as_float(sv[8 * q + t + 1])),
+                     f2pack(Elem<T>::to_f(w.e[t]), Elem<T>::to_f(w.e[t + 1]))),
+               a, b);
+      sv[8 * q + t] = __float_as_uint(a);
+      sv[8 * q + t + 1] = __float_as_uint(b);
     }
   }
-  return factor;
+  return kLog2e;
 }
 
 // The mask tile of rows [row, row + 128) (row 0 of a mask broadcast over queries) and keys
@@ -561,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Under a mask, mask_row applies it and gives the factor the scores are used with.
       float cs = c;
       if constexpr (masked) {
-        cs = mask_row<T>(sv, mtile, r, row_bc, mbool, c, p.scale);
+        cs = mask_row<T, false>(sv, mtile, r, lane, row_bc, mbool, c, p.scale);
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.mask_free[w]);  // this warp is done with the mask tile
       }
@@ -884,7 +897,7 @@ __global__ void __launch_bounds__(k256Threads, 1)
       if (p.causal) lim = min(lim, i + p.coff - k0 + 1);
       float cs = c;
       if constexpr (masked) {
-        cs = mask_row<T>(sv, sm + L::kMaskOff, r, row_bc, mbool, c, p.scale);
+        cs = mask_row<T, true>(sv, sm + L::kMaskOff, r, lane, row_bc, mbool, c, p.scale);
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars.mask_free);  // this warp is done with the mask tile
       }
