@@ -84,6 +84,7 @@ struct FwdBars {
   uint64_t o_done[kQTiles];
   uint64_t mma_done[kQTiles];
   uint64_t turn[kQTiles];  // exponential pass of Q tile w may start (alternates 0, 1, 0, ...)
+  uint64_t p_half[kQTiles];  // unmasked: P_w of keys [0, 64) has been written
   uint64_t mask_full[kQTiles];  // masked: Q tile w's mask tile for its next KV tile has landed
   uint64_t mask_free[kQTiles];  // masked: the four warps of warpgroup w have read it
   uint64_t vote[kQTiles];       // masked: the four warps of warpgroup w have voted on the split
@@ -278,9 +279,11 @@ __device__ __forceinline__ float tile_max(const uint32_t (&sv)[kBN], float c, in
 
 // Exponentials of a 128-key tile held in registers: returns their sum and writes P packed
 // to 16 bits into TMEM columns [0, 64) of the S tile (column q holds keys 2q and 2q + 1).
+// With `half`, arrives on it once P of keys [0, 64) is in TMEM, so that the PV product of
+// those keys can start while the other half is computed.
 template <typename T, bool kMask>
 __device__ __forceinline__ float exp_pass(const uint32_t (&sv)[kBN], uint32_t s_addr, float c, float neg_m,
-                                          int lim) {
+                                          int lim, uint64_t* half) {
   const uint64_t cc = f2pack(c, c), nm = f2pack(neg_m, neg_m);
   uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
@@ -304,6 +307,11 @@ __device__ __forceinline__ float exp_pass(const uint32_t (&sv)[kBN], uint32_t s_
       pk[e] = pack2<T>(p0, p1);
     }
     tmem_st32(s_addr + 32 * h, pk);
+    if (h == 0 && half != nullptr) {
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(half);
+    }
   }
   float a, b, c2, d;
   f2unpack(acc0, a, b);
@@ -406,6 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars.s_full[w], 1);
       mbar_init(&bars.p_full[w], kBM);
       mbar_init(&bars.o_done[w], 1);
+      mbar_init(&bars.p_half[w], kBM);
     }
     mbar_init(&bars.mma_done[0], 1);
     mbar_init(&bars.mma_done[1], 1);
@@ -483,40 +492,108 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t ring_s = smem_u32(sm + L::kRingOff);
     const uint32_t s_tm = tbase + L::kSCol + w * 128, o_tm = tbase + L::kOCol + w * 128;
     const int tile_row0 = row0 + w * kBM;
-    for (int j = 0; ok && j < nmax; ++j) {
-      const int sk = (2 * j) % kStages, sv = (2 * j + 1) % kStages;
-      const uint32_t phk = ((2 * j) / kStages) & 1, phv = ((2 * j + 1) / kStages) & 1;
-      // Every stage use gets exactly one arrival from each issuer, made only after the
-      // stage was filled for this use, even by an issuer whose tile needs no MMA here.
-      if (!(ok = __all_sync(kAll, mbar_wait(&bars.kv_full[sk], phk, wc)))) break;
-      if (j < nkv_w) {
-        if (j > 0 && !(ok = __all_sync(kAll, mbar_wait(&bars.o_done[w], (j - 1) & 1, wc)))) break;
-        tc_fence_after();  // P_w(j-1) consumed: S_w may be overwritten
-        const uint64_t kd = sdesc_sw128(ring_s + sk * L::kTileBytes, 16, 1024);
+    if constexpr (!kMasked) {
+      // PV_w(j) in two K = 64 halves: the half over keys 0..63 starts once the softmax has
+      // written that half of P(j), so it runs while the other half is computed and the chain
+      // S → softmax → PV → S only waits for the second half.  (S(j+1) stays one N = 128
+      // product: N = 64 halves issued early measured slower, the MMA count doubling.)  Every
+      // ring stage still gets exactly one kv_empty arrival per use, in order.
+      auto s_full_product = [&](int stage) {
+        const uint64_t kd = sdesc_sw128(ring_s + stage * L::kTileBytes, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
           mma_ss_w(s_tm, sdesc_advance(qd, off), sdesc_advance(kd, off), kIdS, kk > 0);
         }
+      };
+      auto pv_half = [&](int stage, int hi, bool first) {  // keys [64·hi, 64·hi + 64) of P·V
+        const uint64_t vd = sdesc_sw128(ring_s + stage * L::kTileBytes, 16384, 1024);
+#pragma unroll
+        for (int kk = 4 * hi; kk < 4 * hi + 4; ++kk)
+          mma_ts_w(o_tm, s_tm + kk * 8, sdesc_advance(vd, kk * 2048), kIdO, (!first || kk > 0) ? 1u : 0u);
+      };
+      // K(0) and S(0).
+      ok = __all_sync(kAll, mbar_wait(&bars.kv_full[0], 0, wc));
+      if (ok && nkv_w > 0) {
+        tc_fence_after();
+        s_full_product(0);
         mma_commit_w(&bars.s_full[w]);
       }
-      mma_commit_w(&bars.kv_empty[sk]);  // one of the stage's two arrivals
-      if (!(ok = __all_sync(kAll, mbar_wait(&bars.kv_full[sv], phv, wc)))) break;
-      if (j < nkv_w) {
-        if (!(ok = __all_sync(kAll, mbar_wait(&bars.p_full[w], j & 1, wc)))) break;
-        tc_fence_after();
-        const uint64_t vd = sdesc_sw128(ring_s + sv * L::kTileBytes, 16384, 1024);
+      if (ok) mma_commit_w(&bars.kv_empty[0]);
+      for (int j = 0; ok && j < nmax; ++j) {
+        const int itv = 2 * j + 1, itk = 2 * j + 2;  // V(j), K(j+1)
+        const int sv = itv % kStages, sk = itk % kStages;
+        const uint32_t phv = (itv / kStages) & 1, phk = (itk / kStages) & 1;
+        const bool act = j < nkv_w, act1 = j + 1 < nkv_w, nxt = j + 1 < nmax;
+        const bool spl = act && split_tile(p, j, tile_row0);
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.kv_full[sv], phv, wc)))) break;
+        if (act) {
+          if (!(ok = __all_sync(kAll, mbar_wait(spl ? &bars.p_full[w] : &bars.p_half[w], j & 1, wc)))) break;
+          tc_fence_after();
+          pv_half(sv, 0, j == 0);
+          if (spl) {  // the whole P and its remainder (columns [64, 128))
+            pv_half(sv, 1, false);
+            const uint64_t vd = sdesc_sw128(ring_s + sv * L::kTileBytes, 16384, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts_w(o_tm, s_tm + kk * 8, sdesc_advance(vd, kk * 2048), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-        if (kMasked ? split_voted(bars.need[w][j % 2]) : split_tile(p, j, tile_row0)) {  // remainder of P, columns [64, 128)
-#pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
-            mma_ts_w(o_tm, s_tm + 64 + kk * 8, sdesc_advance(vd, kk * 2048), kIdO, 1u);
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              mma_ts_w(o_tm, s_tm + 64 + kk * 8, sdesc_advance(vd, kk * 2048), kIdO, 1u);
+          }
         }
-        mma_commit_w(&bars.o_done[w]);
+        if (act && !spl) {
+          if (!(ok = __all_sync(kAll, mbar_wait(&bars.p_full[w], j & 1, wc)))) break;
+          tc_fence_after();
+          pv_half(sv, 1, false);
+        }
+        if (act) mma_commit_w(&bars.o_done[w]);
+        mma_commit_w(&bars.kv_empty[sv]);
+        if (nxt) {
+          if (!(ok = __all_sync(kAll, mbar_wait(&bars.kv_full[sk], phk, wc)))) break;
+          if (act1) {
+            // P(j) consumed: S(j+1) may overwrite S_w.
+            if (!(ok = __all_sync(kAll, mbar_wait(&bars.o_done[w], j & 1, wc)))) break;
+            tc_fence_after();
+            s_full_product(sk);
+            mma_commit_w(&bars.s_full[w]);
+          }
+          mma_commit_w(&bars.kv_empty[sk]);
+        }
       }
-      mma_commit_w(&bars.kv_empty[sv]);
+    } else {
+      for (int j = 0; ok && j < nmax; ++j) {
+        const int sk = (2 * j) % kStages, sv = (2 * j + 1) % kStages;
+        const uint32_t phk = ((2 * j) / kStages) & 1, phv = ((2 * j + 1) / kStages) & 1;
+        // Every stage use gets exactly one arrival from each issuer, made only after the
+        // stage was filled for this use, even by an issuer whose tile needs no MMA here.
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.kv_full[sk], phk, wc)))) break;
+        if (j < nkv_w) {
+          if (j > 0 && !(ok = __all_sync(kAll, mbar_wait(&bars.o_done[w], (j - 1) & 1, wc)))) break;
+          tc_fence_after();  // P_w(j-1) consumed: S_w may be overwritten
+          const uint64_t kd = sdesc_sw128(ring_s + sk * L::kTileBytes, 16, 1024);
+  #pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+            mma_ss_w(s_tm, sdesc_advance(qd, off), sdesc_advance(kd, off), kIdS, kk > 0);
+          }
+          mma_commit_w(&bars.s_full[w]);
+        }
+        mma_commit_w(&bars.kv_empty[sk]);  // one of the stage's two arrivals
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.kv_full[sv], phv, wc)))) break;
+        if (j < nkv_w) {
+          if (!(ok = __all_sync(kAll, mbar_wait(&bars.p_full[w], j & 1, wc)))) break;
+          tc_fence_after();
+          const uint64_t vd = sdesc_sw128(ring_s + sv * L::kTileBytes, 16384, 1024);
+  #pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ts_w(o_tm, s_tm + kk * 8, sdesc_advance(vd, kk * 2048), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+          if (kMasked ? split_voted(bars.need[w][j % 2]) : split_tile(p, j, tile_row0)) {  // remainder of P, columns [64, 128)
+  #pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              mma_ts_w(o_tm, s_tm + 64 + kk * 8, sdesc_advance(vd, kk * 2048), kIdO, 1u);
+          }
+          mma_commit_w(&bars.o_done[w]);
+        }
+        mma_commit_w(&bars.kv_empty[sv]);
+      }
     }
     mma_commit_w(&bars.mma_done[w]);
     drain_wait(&bars.mma_done[w], 0, 100000000ull);
@@ -628,14 +705,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         split = split_tile(p, j, tile_row0);
       }
+      uint64_t* half = kMasked ? nullptr : &bars.p_half[w];
       if (split)
         l += exp_pass_split<T>(sv, s_addr, cs, neg_m, lim);
       else if (need_mask)
-        l += exp_pass<T, true>(sv, s_addr, cs, neg_m, lim);
+        l += exp_pass<T, true>(sv, s_addr, cs, neg_m, lim, half);
       else
-        l += exp_pass<T, false>(sv, s_addr, cs, neg_m, lim);
+        l += exp_pass<T, false>(sv, s_addr, cs, neg_m, lim, half);
       tmem_st_wait();
       tc_fence_before();
+      if (!kMasked && split) mbar_arrive(&bars.p_half[w]);  // one p_half phase per tile
       // Hand the turn to the other tile before arriving on p_full: P(j) complete then implies
       // that every warp of this warpgroup has also arrived on the turn barrier for tile j, so
       // no warp's arrival for tile j+1 can count toward tile j.
@@ -945,9 +1024,9 @@ __global__ void __launch_bounds__(k256Threads, 1)
       if (split)
         l += exp_pass_split<T>(sv, s_addr, cs, neg_m, lim);
       else if (need_mask)
-        l += exp_pass<T, true>(sv, s_addr, cs, neg_m, lim);
+        l += exp_pass<T, true>(sv, s_addr, cs, neg_m, lim, nullptr);
       else
-        l += exp_pass<T, false>(sv, s_addr, cs, neg_m, lim);
+        l += exp_pass<T, false>(sv, s_addr, cs, neg_m, lim, nullptr);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars.p_full[buf]);
