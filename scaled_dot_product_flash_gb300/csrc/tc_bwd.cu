@@ -107,6 +107,7 @@ struct BwdBars {
   uint64_t vec_full[kStages];
   uint64_t s_full[2];     // dK/dV: [0] only.  dQ: one per S buffer
   uint64_t dp_full;
+  uint64_t p_half;        // dK/dV: Pᵀ of each warp's first 16 queries packed
   uint64_t p_ready;       // dK/dV: Pᵀ packed
   uint64_t ds_ready;      // dSᵀ / dS packed
   uint64_t x_free;        // dK/dV: dV consumed Pᵀ (Sᵀ region free)
@@ -132,7 +133,8 @@ __device__ __forceinline__ void init_bars(BwdBars& bars) {
   mbar_init(&bars.s_full[0], 1);
   mbar_init(&bars.s_full[1], 1);
   mbar_init(&bars.dp_full, 1);
-  mbar_init(&bars.p_ready, 512);   // every element thread of the dK/dV kernel
+  mbar_init(&bars.p_half, 512);    // every element thread of the dK/dV kernel
+  mbar_init(&bars.p_ready, 512);
   mbar_init(&bars.ds_ready, 512);
   mbar_init(&bars.x_free, 1);
   mbar_init(&bars.y_free, 1);
@@ -177,6 +179,18 @@ __device__ __forceinline__ void mma_accumulate(uint32_t acc_tmem, uint32_t a_tme
   const uint64_t bd = sdesc_sw128(b_s, BwdLayout<D>::kCbStride, 1024);
 #pragma unroll
   for (int kk = 0; kk < kBlk / 16; ++kk)
+    mma_ts_w(acc_tmem, a_tmem + packed_col<kSplit>(kk), sdesc_advance(bd, kk * 2048), idesc,
+             (!first || kk > 0) ? 1u : 0u);
+}
+
+// The K-steps kk = odd, odd + 2, ... of mma_accumulate (odd = 0: the even steps, which
+// read each owner's first 16 rows of A; odd = 1: the others).
+template <int D, int kSplit>
+__device__ __forceinline__ void mma_accumulate_half(uint32_t acc_tmem, uint32_t a_tmem, uint32_t b_s,
+                                                    uint32_t idesc, bool first, int odd) {
+  const uint64_t bd = sdesc_sw128(b_s, BwdLayout<D>::kCbStride, 1024);
+#pragma unroll
+  for (int kk = odd; kk < kBlk / 16; kk += 2)
     mma_ts_w(acc_tmem, a_tmem + packed_col<kSplit>(kk), sdesc_advance(bd, kk * 2048), idesc,
              (!first || kk > 0) ? 1u : 0u);
 }
@@ -311,9 +325,14 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       }
       for (int n = 0; ok && n < total; ++n) {
         const uint32_t q_s = stage_q(n), do_s = q_s + L::kTileBytes;
+        // dV += Pᵀ·dO in two halves: the K-steps of the queries whose Pᵀ the element warps
+        // write first, then the rest, so that dV(n) is half done when the Pᵀ pass ends.
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.p_half, n & 1, wc)))) break;
+        tc_fence_after();
+        mma_accumulate_half<D, 32>(tbase + kColDv, tbase + kColX, do_s, kIdAcc, n == 0, 0);
         if (!(ok = __all_sync(kAll, mbar_wait(&bars.p_ready, n & 1, wc)))) break;
         tc_fence_after();
-        mma_accumulate<D, 32>(tbase + kColDv, tbase + kColX, do_s, kIdAcc, n == 0);  // dV += Pᵀ·dO
+        mma_accumulate_half<D, 32>(tbase + kColDv, tbase + kColX, do_s, kIdAcc, n == 0, 1);
         mma_commit_w(&bars.x_free);
         if (n + 1 < total) {
           if (!(ok = __all_sync(kAll, mbar_wait(&bars.ring_full[(n + 1) % kStages], ((n + 1) / kStages) & 1, wc) &&
@@ -371,7 +390,6 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         uint32_t sr[32];
         tmem_ld32(x_addr, sr);
         tmem_ld_wait(sr);
-        uint32_t pk[16];
         if constexpr (masked) {
           // c·s + log2e·M for this key against the warp's queries, M read from the block's
           // mask tile in shared memory (row q, key k at element 128q + k; one row when the
@@ -408,18 +426,30 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           if (lane == 0) mbar_arrive(&bars.mask_free);  // this warp is done with the mask tile
         }
         const uint64_t ce = masked ? f2pack(1.f, 1.f) : cc;
+        // Two halves of 16 queries, each stored as soon as it is packed: the first half
+        // lets the dV product start (p_half) while the second is computed.
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float p0, p1;
-          ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), ce, nl2[e]), p0, p1);
-          if (diag) {
-            if (j > ic + 2 * e) p0 = 0.f;
-            if (j > ic + 2 * e + 1) p1 = 0.f;
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int e8 = 0; e8 < 8; ++e8) {
+            const int e = 8 * hf + e8;
+            float p0, p1;
+            ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), ce, nl2[e]), p0, p1);
+            if (diag) {
+              if (j > ic + 2 * e) p0 = 0.f;
+              if (j > ic + 2 * e + 1) p1 = 0.f;
+            }
+            pf[e] = f2pack(p0, p1);
+            pk[e8] = pack2<T>(p0, p1);
           }
-          pf[e] = f2pack(p0, p1);
-          pk[e] = pack2<T>(p0, p1);
+          tmem_st8(x_addr + 8 * hf, pk);
+          if (hf == 0) {
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bars.p_half);
+          }
         }
-        tmem_st16(x_addr, pk);
       }
       tmem_st_wait();
       tc_fence_before();
