@@ -9,9 +9,11 @@
 //   Pᵀ = exp2(c·Sᵀ − log2e·lse), dSᵀ = Pᵀ∘(dPᵀ − δ)  (element warps; written back over
 //                                                     Sᵀ and dPᵀ as 16-bit A operands)
 //   dV += Pᵀ·dO, dK += dSᵀ·Q                         (tcgen05, accumulators stay in TMEM)
-// and finally dK·scale and dV are rounded and stored.  The element warps publish Pᵀ as
-// soon as it is ready, so dV runs while dSᵀ is computed, and Sᵀ of the next block starts
-// as soon as dV has consumed Pᵀ (the MMA order is dV(n), Sᵀ(n+1), dK(n), dPᵀ(n+1)).  dSᵀ
+// and finally dK·scale and dV are rounded and stored.  The element warps publish Pᵀ in
+// two halves (each warp's first 16 queries, then the rest), so dV starts over the first
+// half while the second is computed and runs while dSᵀ is computed, and Sᵀ of the next
+// block starts as soon as dV has consumed Pᵀ (the MMA order is dV(n), Sᵀ(n+1), dK(n),
+// dPᵀ(n+1)).  dSᵀ
 // is formed from Pᵀ in fp32 (dV uses Pᵀ rounded to the element type, as the A operand of
 // a 16-bit MMA must be).
 //
@@ -31,10 +33,12 @@
 // columns.
 //
 // Attention masks: both kernels have a masked instantiation (kMasked) that adds log2e·M
-// to the log2-domain scores before the exponential (the dK/dV kernel reads one mask value
-// per (query, key), coalesced over the warp's 32 keys; the dQ kernel reads its row's 64
-// values in 16-byte pieces).  A row whose lse is −inf (it saw no key) gets P = 0.  Sinks
-// need no change here: the forward's lse already includes them.
+// to the log2-domain scores before the exponential.  The dK/dV kernel's producer loads
+// each query block's [128 x 128] mask tile by TMA into shared memory, from which each
+// element warp reads its keys' column; the dQ kernel (no shared memory left at D = 128)
+// reads its row's 32 mask values from global memory in 16-byte pieces before its barrier
+// waits.  A row whose lse is −inf (it saw no key) gets P = 0.  Sinks need no change here:
+// the forward's lse already includes them.
 #include "launch.h"
 #include "tc_common.cuh"
 

@@ -6,9 +6,11 @@
 //                    lane; online softmax in the log2 domain ("[Metal] Add Flash Attention
 //                    VJP for training", section "Implementation Notes": log2 domain)
 //   warp 8           TMA producer: Q tiles once, then K_j, V_j tiles into a 4-stage ring
+//                    (3 stages with a mask, whose tiles take the room of the fourth)
 //   warps 9 / 10     tcgen05 issuers for Q tile 0 / 1 (whole warp runs the loop, one
 //                    elected lane issues); warp 9 owns TMEM
-//   warp 11          idle (completes warpgroup 2 for the register split)
+//   warp 11          mask tile producer with a mask; otherwise idle (it completes
+//                    warpgroup 2 for the register split)
 // setmaxnreg moves registers from warpgroup 2 to the softmax warpgroups, so a softmax
 // thread holds its row's 128 scores in registers after one TMEM round trip and computes
 // the row maximum and the exponentials from there.  The two softmax warpgroups take turns
@@ -16,15 +18,17 @@
 // Tensor memory (512 columns, fp32): S_w = Q_w·K_jᵀ at columns [128w, 128w+128); P_w is
 // written back over the first 64 columns of S_w as packed 16-bit pairs and read from TMEM
 // as the A operand of O_w += P_w·V_j, with O_w at columns [256 + 128w, 256 + 128w + D).
+// Without a mask PV is issued in two halves of 64 keys, the first as soon as the softmax
+// has written that half of P, so the next S waits only for the second half.
 // The running maximum is raised lazily: O and l are rescaled only when a row's maximum
 // grows by more than 2^8, so exponentials stay <= 256 while O and l use one consistent
 // maximum, which keeps the result exact up to rounding.
 // Rows with few visible keys (the first Q tile under the causal mask, or every row when
 // Lkv <= 128) can have |O| near the largest inputs, where rounding P to 16 bits would
-// add an error comparable to the output's own rounding.  For that one KV tile (for every
-// tile when an attention mask is given) P is split into a 16-bit head and a 16-bit
-// remainder (written to S columns [64, 128)) and both are multiplied into O, so P enters
-// O with ~16 extra bits.
+// add an error comparable to the output's own rounding.  For that one KV tile (under an
+// attention mask, for every tile the softmax warps vote to split, see kSplitShare) P is
+// split into a 16-bit head and a 16-bit remainder (written to S columns [64, 128)) and
+// both are multiplied into O, so P enters O with ~16 extra bits.
 // Epilogue: O / l rounded to the element type and staged in the tile's (now unused) Q
 // buffer, then written by bulk tensor stores; lse = ln2·(m + log2 l) (natural log).
 #include "launch.h"
