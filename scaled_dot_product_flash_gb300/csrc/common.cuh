@@ -179,14 +179,6 @@ __device__ __forceinline__ void mask_pairs(uint32_t (&mk)[N / 2], const Problem&
   }
 }
 
-// Hint that the bytes [ptr, ptr + bytes) will be read soon (into L1; bytes <= 256).
-__device__ __forceinline__ void prefetch_l1(const void* ptr, int bytes) {
-  const char* a = static_cast<const char*>(ptr);
-  asm volatile("prefetch.global.L1 [%0];" ::"l"(a));
-  if (bytes > 128) asm volatile("prefetch.global.L1 [%0];" ::"l"(a + 128));
-  asm volatile("prefetch.global.L1 [%0];" ::"l"(a + bytes - 1));
-}
-
 template <typename T>
 __host__ __device__ __forceinline__ const T* row_ptr(const void* base, const Layout& l, int b, int h, int64_t i) {
   return static_cast<const T*>(base) + row_off(l, b, h, i);
