@@ -346,6 +346,7 @@ def main():
 
     peaks, peak_src = load_peaks()
     bf16_peak = peaks["bf16_tflops"]
+    bf16_sustained = peaks.get("bf16_tflops_sustained") or bf16_peak
     hbm_peak = peaks["hbm_gbs"]
 
     # Per-kernel achieved rates from the library's event brackets (same timed steps).
@@ -372,9 +373,15 @@ def main():
         if path_is_tensor else "simt_kernels.cu"
     traffic = ncu_traffic(f"{dom}:{dom_src}")
     if path_is_tensor:
-        roof = {"bound": "tensor", "achieved": kern[dom]["tflops"], "peak": bf16_peak,
-                "unit": "TFLOP/s", "frac": kern[dom]["tflops"] / bf16_peak, "traffic": traffic,
-                "kernel": dom, "peak_source": f"{peak_src} (burst bf16)"}
+        # The dominant kernel's rate comes from the bracketed pass over the same seconds-long
+        # run of back-to-back steps (the clock record shows the power cap engaged), so its
+        # denominator is the sustained bf16 figure; the burst one is given beside it.
+        roof = {"bound": "tensor", "achieved": kern[dom]["tflops"], "peak": bf16_sustained,
+                "unit": "TFLOP/s", "frac": kern[dom]["tflops"] / bf16_sustained, "traffic": traffic,
+                "kernel": dom,
+                "peak_source": f"{peak_src} (sustained bf16: the kernel is timed inside a "
+                               f"seconds-long run of steps)",
+                "frac_of_burst_peak": kern[dom]["tflops"] / bf16_peak}
     else:
         alu_peak = alu_peak_tflops(clocks)
         roof = {"bound": "alu", "achieved": kern[dom]["tflops"], "peak": alu_peak,
@@ -414,6 +421,8 @@ def main():
             "data": "synthetic",
             "config": headline_config(world),
             "frac_of_bf16_peak": value / bf16_peak,
+            # the headline steps run back to back for seconds under the power cap
+            "frac_of_bf16_sustained_peak": value / bf16_sustained,
             "fwd": {"tflops": fwd_tflops, "ms": total_fwd_ms / args.steps,
                     "frac_of_bf16_peak": fwd_tflops / bf16_peak},
             "roofline": roof,
@@ -426,7 +435,8 @@ def main():
                               "clocks": kclocks},
             "configs": configs,
             "gpu_launches": launches,
-            "peaks": {"source": peak_src, "bf16_tflops": bf16_peak, "hbm_gbs": hbm_peak},
+            "peaks": {"source": peak_src, "bf16_tflops": bf16_peak,
+                      "bf16_tflops_sustained": bf16_sustained, "hbm_gbs": hbm_peak},
             **extras,
         }
         print(json.dumps(line))
