@@ -145,6 +145,34 @@ def test_minus_infinity_sink_on_a_row_that_sees_no_key(shape, dtype, path):
         assert rel_frob(got, refs[3]) <= 1e-2
 
 
+@pytest.mark.parametrize("shape,dtype", [
+    (Shape(1, 4, 2, 300, 384, 128), "bf16"),   # D = 128: Q tile 1 of the first block hidden
+    (Shape(1, 2, 1, 260, 300, 256), "f16"),    # D = 256
+])
+def test_mask_hiding_whole_query_tiles(shape, dtype):
+    """A boolean mask per (batch, head) that hides every key of query rows [128, 256) (a
+    whole 128-row Q tile) of the first head and keeps a random 70% elsewhere: those rows
+    give O = 0, lse = −inf and zero dQ, and everything matches the oracle."""
+    rng = np.random.default_rng(140)
+    m = rng.random((shape.B, shape.Hq, shape.Lq, shape.Lkv)) < 0.7
+    m[:, 0, 128:256, :] = False
+    q, k, v, do = draw(shape, 141, dtype)
+    scale = 1.0 / math.sqrt(shape.D)
+    qd, kd, vd, dod, md = (t.cuda() for t in (q, k, v, do, torch.from_numpy(m)))
+    o, lse = api.attention_forward(qd, kd, vd, scale=scale, attn_mask=md)
+    g = api.attention_backward(qd, kd, vd, o, dod, lse, scale=scale, attn_mask=md)
+    api.poll_status()
+    qn, kn, vn, don = (as_f64(t) for t in (q, k, v, do))
+    o_ref, lse_ref = oracle.sdpa_forward(qn, kn, vn, scale, False, mask=m)
+    check_forward_masked(dtype, as_f64(o), as_f64(lse), o_ref, lse_ref, "whole tiles")
+    assert np.all(as_f64(o)[:, 0, 128:256] == 0.0)
+    assert np.all(np.isneginf(as_f64(lse)[:, 0, 128:256]))
+    assert np.all(as_f64(g[0])[:, 0, 128:256] == 0.0)
+    refs = oracle.sdpa_backward(qn, kn, vn, don, scale, False, mask=m)
+    for name, got, ref in zip(("dq", "dk", "dv"), g[:3], refs[:3]):
+        check_grad(dtype, name, as_f64(got), ref, "whole tiles")
+
+
 def test_masked_autograd_matches_oracle():
     shape = Shape(1, 8, 2, 160, 224, 128)
     q, k, v, do = draw(shape, 125, "bf16")
