@@ -431,16 +431,19 @@ extern "C" int sdpa_bwd_masked(const void* q, const void* k, const void* v, cons
     return status_of(launch_one(SDPA_KERNEL_VEC_BWD, s, [&] {
       return vector_mma_supported(p, dtype) ? launch_vector_mma_bwd(p, dtype, s) : launch_vector_bwd(p, dtype, s);
     }));
-  const bool tc = f == Family::kTensor && tensor_bwd_supported(p, dtype);
+  const bool tc256 = f == Family::kTensor && tensor_bwd256_supported(p, dtype);
+  const bool tc = tc256 || (f == Family::kTensor && tensor_bwd_supported(p, dtype));
   if (f == Family::kTensor && !tc && g_path.load() == SDPA_PATH_TENSOR) return SDPA_ERR_UNSUPPORTED;
   auto launch_dkdv = [&](cudaStream_t st) {
     return launch_one(SDPA_KERNEL_DKDV, st, [&] {
-      return tc ? launch_tc_dkdv(p, dtype, st) : launch_simt_dkdv(p, dtype, st);
+      if (!tc) return launch_simt_dkdv(p, dtype, st);
+      return tc256 ? launch_tc_dkdv256(p, dtype, st) : launch_tc_dkdv(p, dtype, st);
     });
   };
   auto launch_dq = [&](cudaStream_t st) {
     return launch_one(SDPA_KERNEL_DQ, st, [&] {
-      return tc ? launch_tc_dq(p, dtype, st) : launch_simt_dq(p, dtype, st);
+      if (!tc) return launch_simt_dq(p, dtype, st);
+      return tc256 ? launch_tc_dq256(p, dtype, st) : launch_tc_dq(p, dtype, st);
     });
   };
   // While per-kernel timing is on, each kernel runs alone so that its events bracket only

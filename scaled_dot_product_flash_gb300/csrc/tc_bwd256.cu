@@ -1,0 +1,690 @@
+// Tensor-core backward at head dim 256 (fp16/bf16, no attention mask): a dQ kernel and a
+// dK/dV kernel on TMA + tcgen05 + TMEM, recomputing P from the forward's logsumexp as the
+// D <= 128 kernels do ("[Metal] Add Flash Attention VJP for training", sections
+// "Implementation Notes" and "Limitations").  At D = 256 one SM's budgets (512 TMEM
+// columns, 227 KB of shared memory) shape them differently:
+//   dQ: a block owns 128 query rows of one head and streams 64-key blocks.  TMEM: dQ in
+//       256 columns, S in two 64-column buffers (→ dS), dP in 64 columns.  Shared memory:
+//       Q and dO (64 KB each), two 32 KB K stages (K lives through S and dQ) and one 32 KB
+//       V stage (224 KB).  S = Q·Kᵀ and dP = dO·Vᵀ are M = 128, N = 64 products over 16
+//       K-steps; dQ += dS·K is one M = 128, N = 256 product over 4 K-steps.
+//   dK/dV: D is split in two halves over two passes, whose blocks run side by side: a
+//       block owns 128 keys of one KV head, accumulates dV and dK of its half of D (128
+//       TMEM columns each) and streams 64-row query blocks of the G query heads of its
+//       group.  Sᵀ = K·Qᵀ and dPᵀ = V·dOᵀ (64 columns each) are recomputed over the full D
+//       in each pass (1.5x the MMA work of one pass).  Shared memory: K and V whole
+//       (128 KB), two 32 KB Q slots (Q lives through Sᵀ and dK) and one 32 KB dO slot.
+// Warp roles as in the D <= 128 kernels: warps 0-15 element work (warp e takes TMEM lane
+// quarter e % 4 and the 16 streamed columns [16c, 16c + 16), c = e / 4, and writes its
+// packed 16-bit results over the first 8 of them), warp 16 the TMA producer, warps 17-19
+// (dQ: S, dP, dQ) or 17-18 (dK/dV) the MMA issuers; warp 17 owns the TMEM.  Every wait is
+// bounded, as everywhere in the library.
+#include "launch.h"
+#include "tc_common.cuh"
+
+namespace sdpa {
+namespace {
+using namespace tc;
+
+constexpr int kD = 256;
+constexpr int kOwn = 128;                   // rows owned by a block
+constexpr int kStr = 64;                    // rows of a streamed block
+constexpr int kOwnBytes = kOwn * kD * 2;    // [128 x 256] 16-bit: 64 KB
+constexpr int kOwnCb = kOwn * 128;          // one 64-column block of an own tile
+constexpr int kStrBytes = kStr * kD * 2;    // [64 x 256] 16-bit: 32 KB
+constexpr int kStrCb = kStr * 128;          // one 64-column block of a streamed tile
+constexpr int kProducer = 16;
+constexpr int kIssuer = 17;
+// dQ: launched at 96 registers a thread (65,536 / 640 rounded down to a multiple of 8);
+// warpgroup 4 drops to 56 and the element warpgroups rise to 104.
+constexpr int kDqThreads = 640;
+constexpr int kRegsLow = 56;
+constexpr int kRegsHigh = 104;
+static_assert(128 * kRegsLow + 512 * kRegsHigh <= kDqThreads * 96, "register split exceeds the launch");
+constexpr int kKvThreads = 608;
+
+template <typename T>
+struct IsBf16 { static constexpr bool value = false; };
+template <>
+struct IsBf16<__nv_bfloat16> { static constexpr bool value = true; };
+
+__device__ __forceinline__ float pos_inf() { return __int_as_float(0x7f800000); }
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > 100000000ull) return;
+  }
+}
+
+// S (or Sᵀ) = A·Bᵀ over D = 256: A an own [128 x 256] tile and B a streamed [64 x 256]
+// tile, both K-major in the 128-byte swizzle as four 64-column blocks; M = 128, N = 64,
+// 16 K-steps.  Called by all 32 lanes of the issuing warp; one elected lane issues.
+__device__ __forceinline__ void mma_scores256(uint32_t c_tmem, uint32_t a_s, uint32_t b_s, uint32_t idesc) {
+  const uint64_t ad = sdesc_sw128(a_s, 16, 1024), bd = sdesc_sw128(b_s, 16, 1024);
+#pragma unroll
+  for (int kk = 0; kk < kD / 16; ++kk) {
+    const uint32_t ka = (kk / 4) * kOwnCb + (kk % 4) * 32, kb = (kk / 4) * kStrCb + (kk % 4) * 32;
+    mma_ss_w(c_tmem, sdesc_advance(ad, ka), sdesc_advance(bd, kb), idesc, kk > 0);
+  }
+}
+
+// Acc (+)= A·B: A the packed 16-bit [128 x 64] in TMEM (K-step kk, rows [16kk, 16kk + 16)
+// of the streamed block, is element warp group kk's first 8 columns, at a_tmem + 16kk) and
+// B the columns of a streamed [64 x 256] tile from b_s on (as many 64-column blocks as the
+// instruction's N), read MN-major with K = its 64 rows.
+__device__ __forceinline__ void mma_acc256(uint32_t acc_tmem, uint32_t a_tmem, uint32_t b_s, uint32_t idesc,
+                                           bool first) {
+  const uint64_t bd = sdesc_sw128(b_s, kStrCb, 1024);
+#pragma unroll
+  for (int kk = 0; kk < kStr / 16; ++kk)
+    mma_ts_w(acc_tmem, a_tmem + 16 * kk, sdesc_advance(bd, kk * 2048), idesc, (!first || kk > 0) ? 1u : 0u);
+}
+
+// ================================================================== dQ
+constexpr int kDqQ = 0;
+constexpr int kDqDo = kOwnBytes;
+constexpr int kDqK = 2 * kOwnBytes;             // two K stages
+constexpr int kDqV = kDqK + 2 * kStrBytes;      // one V stage
+constexpr int kDqBytes = kDqV + kStrBytes;      // 224 KB
+
+struct Dq256Bars {
+  uint64_t own_full;
+  uint64_t k_full[2];
+  uint64_t k_empty[2];
+  uint64_t v_full;
+  uint64_t v_empty;
+  uint64_t s_full[2];    // one per S buffer
+  uint64_t dp_full;
+  uint64_t dp_free;      // every element thread has read dP
+  uint64_t ds_ready[2];  // dS of the block in S buffer i packed (one per buffer, as at D <= 128)
+  uint64_t dq_done[2];   // the dQ product of the block in S buffer i has finished
+  uint64_t acc_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kDqThreads, 1)
+    tc_dq256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                    const __grid_constant__ CUtensorMap tdq, Problem p) {
+  constexpr bool kBf16 = IsBf16<T>::value;
+  constexpr uint32_t kIdS = idesc_f16(kOwn, kStr, kBf16, false, false);  // M = 128, N = 64
+  constexpr uint32_t kIdAcc = idesc_f16(kOwn, kD, kBf16, false, true);   // M = 128, N = 256, B MN-major
+  // TMEM columns: dQ [0, 256), S buffer i at [256 + 64i, 320 + 64i), dP [384, 448).
+  constexpr uint32_t kColDq = 0, kColS = 256, kColDp = 384;
+  extern __shared__ unsigned char smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ Dq256Bars bars;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // Block order: all heads of one query tile, then the next; causal: heaviest tiles first.
+  const int units = p.B * p.Hq;
+  const int unit = blockIdx.x % units, rank = blockIdx.x / units;
+  const int b = unit / p.Hq, h = unit % p.Hq, g = h / p.G;
+  const int nqt = (p.Lq + kOwn - 1) / kOwn;
+  const int i0 = (p.causal ? nqt - 1 - rank : rank) * kOwn;
+  const int kend = p.causal ? min(p.Lkv, min(p.Lq, i0 + kOwn) + p.coff) : p.Lkv;
+  const int total = (kend + kStr - 1) / kStr;  // key blocks visited
+
+  if (threadIdx.x == 0) {
+    bars.abort = 0;
+    mbar_init(&bars.own_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars.k_full[s], 1);
+      mbar_init(&bars.k_empty[s], 1);
+      mbar_init(&bars.s_full[s], 1);
+      mbar_init(&bars.ds_ready[s], 512);
+      mbar_init(&bars.dq_done[s], 1);
+    }
+    mbar_init(&bars.v_full, 1);
+    mbar_init(&bars.v_empty, 1);
+    mbar_init(&bars.dp_full, 1);
+    mbar_init(&bars.dp_free, 512);
+    mbar_init(&bars.acc_done, 3);  // one commit per MMA issuer
+    fence_mbar_init();
+  }
+  if (warp == kIssuer) {
+    tmem_alloc(&bars.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = bars.tmem_base;
+  const WaitCtx wc{&bars.abort, 0, p.wait_limit_ns, p.err, kKidTcDq};
+  if (warp >= 16) regs_dec<kRegsLow>();
+
+  if (warp == kProducer) {
+    // Q and dO once; then K(n) into stage n % 2 once dQ(n-2) has read that stage, and V(n)
+    // into the V stage once dP(n-1) has read it.
+    if (lane == 0) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      prefetch_tmap(&tdo);
+      mbar_arrive_expect_tx(&bars.own_full, 2 * kOwnBytes);
+      for (int cb = 0; cb < 4; ++cb) {
+        tma_load_4d(sm + kDqQ + cb * kOwnCb, &tq, &bars.own_full, cb * 64, i0, h, b);
+        tma_load_4d(sm + kDqDo + cb * kOwnCb, &tdo, &bars.own_full, cb * 64, i0, h, b);
+      }
+      int k_issued = 0, v_issued = 0;
+      bool ok = true;
+      for (int n = 0; ok && n < total; ++n) {
+        const int sk = n % 2;
+        if (!(ok = mbar_wait(&bars.k_empty[sk], ((n / 2) & 1) ^ 1, wc))) break;
+        mbar_arrive_expect_tx(&bars.k_full[sk], kStrBytes);
+        for (int cb = 0; cb < 4; ++cb)
+          tma_load_4d(sm + kDqK + sk * kStrBytes + cb * kStrCb, &tk, &bars.k_full[sk], cb * 64, n * kStr, g, b);
+        k_issued = n + 1;
+        if (!(ok = mbar_wait(&bars.v_empty, (n & 1) ^ 1, wc))) break;
+        mbar_arrive_expect_tx(&bars.v_full, kStrBytes);
+        for (int cb = 0; cb < 4; ++cb)
+          tma_load_4d(sm + kDqV + cb * kStrCb, &tv, &bars.v_full, cb * 64, n * kStr, g, b);
+        v_issued = n + 1;
+      }
+      if (!ok || bars.abort) {  // let copies still in flight land before the block exits
+        for (int n = max(0, k_issued - 2); n < k_issued; ++n) drain_wait(&bars.k_full[n % 2], (n / 2) & 1);
+        if (v_issued > 0) drain_wait(&bars.v_full, (v_issued - 1) & 1);
+      }
+    }
+  } else if (warp >= kIssuer) {
+    // Warp 17: S(n) = Q·K(n)ᵀ into S buffer n % 2 once dQ(n-2) has read dS(n-2) from it.
+    // Warp 18: dP(n) = dO·V(n)ᵀ once the element warps have read dP(n-1).
+    // Warp 19: dQ += dS(n)·K(n) once dS(n) is packed.
+    constexpr unsigned kAll = 0xffffffffu;
+    const int role = __shfl_sync(kAll, warp - kIssuer, 0);
+    bool ok = __all_sync(kAll, mbar_wait(&bars.own_full, 0, wc));
+    tc_fence_after();
+    const uint32_t q_s = smem_u32(sm + kDqQ), do_s = smem_u32(sm + kDqDo);
+    const uint32_t k_s = smem_u32(sm + kDqK), v_s = smem_u32(sm + kDqV);
+    if (role == 0) {
+      for (int n = 0; ok && n < total; ++n) {
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.k_full[n % 2], (n / 2) & 1, wc)))) break;
+        if (n >= 2 && !(ok = __all_sync(kAll, mbar_wait(&bars.dq_done[n % 2], ((n - 2) / 2) & 1, wc)))) break;
+        tc_fence_after();
+        mma_scores256(tbase + kColS + 64 * (n % 2), q_s, k_s + (n % 2) * kStrBytes, kIdS);
+        mma_commit_w(&bars.s_full[n % 2]);
+      }
+    } else if (role == 1) {
+      for (int n = 0; ok && n < total; ++n) {
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.v_full, n & 1, wc)))) break;
+        if (n >= 1 && !(ok = __all_sync(kAll, mbar_wait(&bars.dp_free, (n - 1) & 1, wc)))) break;
+        tc_fence_after();
+        mma_scores256(tbase + kColDp, do_s, v_s, kIdS);
+        mma_commit_w(&bars.dp_full);
+        mma_commit_w(&bars.v_empty);
+      }
+    } else {
+      for (int n = 0; ok && n < total; ++n) {
+        // K(n) is loaded (S(n) read it before dS(n) could exist); waiting on its barrier too
+        // makes the TMA writes visible to this warp's MMA directly.
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.ds_ready[n % 2], (n / 2) & 1, wc) &&
+                                        mbar_wait(&bars.k_full[n % 2], (n / 2) & 1, wc))))
+          break;
+        tc_fence_after();
+        mma_acc256(tbase + kColDq, tbase + kColS + 64 * (n % 2), k_s + (n % 2) * kStrBytes, kIdAcc, n == 0);
+        mma_commit_w(&bars.dq_done[n % 2]);
+        mma_commit_w(&bars.k_empty[n % 2]);
+      }
+    }
+    mma_commit_w(&bars.acc_done);
+    drain_wait(&bars.acc_done, 0);
+  } else {
+    regs_inc<kRegsHigh>();
+    // Warp e: TMEM lane quarter e % 4 (queries), key columns [16c, 16c + 16) with c = e / 4.
+    const int c = warp / 4, quarter = warp % 4;
+    const int i = i0 + quarter * 32 + lane;  // this thread's query
+    const bool valid = i < p.Lq;
+    const int64_t row = q_row(p, b, h, valid ? i : 0);
+    const float lse = valid ? p.lse[row] : -pos_inf();
+    const float lse2 = lse == -pos_inf() ? pos_inf() : lse * kLog2e;  // no visible key: P = 0
+    const float dl = valid ? p.delta[row] : 0.f;
+    const uint64_t cc = f2pack(p.scale_log2, p.scale_log2);
+    const uint64_t nl = f2pack(-lse2, -lse2), nd = f2pack(-dl, -dl);
+    bool ok = true;
+    for (int n = 0; n < total; ++n) {
+      const int k0 = n * kStr + 16 * c;  // first key of this warp's columns
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[n % 2], (n / 2) & 1, wc) &&
+                                       mbar_wait(&bars.dp_full, n & 1, wc));
+      if (!ok) break;
+      tc_fence_after();
+      const bool need_mask = (k0 + 16 > p.Lkv) || (p.causal && k0 + 15 > i0 + p.coff);
+      const int lim = min(p.Lkv - k0, p.causal ? i + p.coff - k0 + 1 : 16);  // keys k0 + e, e < lim
+      const uint32_t s_addr = tmem_addr(tbase, quarter * 32, kColS + 64 * (n % 2) + 16 * c);
+      const uint32_t dp_addr = tmem_addr(tbase, quarter * 32, kColDp + 16 * c);
+      // dP and S of this warp's columns; the dP buffer is released at once.
+      uint32_t dr[16], sr[16];
+      tmem_ld16(dp_addr, dr);
+      tmem_ld16(s_addr, sr);
+      tmem_ld_wait(dr);
+      reg_fence(sr);
+      tc_fence_before();
+      mbar_arrive(&bars.dp_free);
+      uint32_t dsk[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float p0, p1;
+        ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl), p0, p1);
+        if (need_mask) {
+          if (2 * e >= lim) p0 = 0.f;
+          if (2 * e + 1 >= lim) p1 = 0.f;
+        }
+        float d0, d1;
+        f2unpack(fmul2(f2pack(p0, p1), fadd2(f2pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), nd)),
+                 d0, d1);
+        dsk[e] = pack2<T>(d0, d1);
+      }
+      tmem_st8(s_addr, dsk);  // dS over the first 8 of this warp's 16 columns
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars.ds_ready[n % 2]);
+    }
+    // Epilogue: dQ·scale in 8 chunks of 32 columns (warps of group c take chunks c and
+    // c + 4), staged in the Q buffer (the last S product has read it) and written by bulk
+    // tensor stores once all 16 warps have staged theirs (rows past Lq are clipped).  With
+    // no key block (total == 0) nothing else has waited for the Q load, so wait for it here.
+    if (ok)
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.own_full, 0, wc) && (total == 0 || mbar_wait(&bars.acc_done, 0, wc)));
+    const int r = quarter * 32 + lane;
+    if (ok) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int c32 = c; c32 < kD / 32; c32 += 4) {
+        uint32_t acc[32];
+        if (total > 0) {
+          tmem_ld32(tmem_addr(tbase, quarter * 32, kColDq + 32 * c32), acc);
+          tmem_ld_wait(acc);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) acc[e] = 0u;
+        }
+        uint32_t packed[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          packed[e] = pack2<T>(__uint_as_float(acc[2 * e]) * p.scale, __uint_as_float(acc[2 * e + 1]) * p.scale);
+        uint8_t* blk = sm + kDqQ + (c32 / 2) * kOwnCb;
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4)
+          *reinterpret_cast<uint4*>(blk + sw128_off(r, (c32 % 2) * 4 + v4)) =
+              make_uint4(packed[4 * v4], packed[4 * v4 + 1], packed[4 * v4 + 2], packed[4 * v4 + 3]);
+      }
+      fence_async_smem();
+    }
+    if (named_sync_and(1, 512, ok) && warp == 0 && lane == 0) {
+      for (int cb = 0; cb < 4; ++cb) tma_store_4d(&tdq, sm + kDqQ + cb * kOwnCb, cb * 64, i0, h, b);
+      bulk_commit();
+      bulk_wait_read();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kIssuer) {
+    __syncwarp();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+// ================================================================== dK / dV
+struct Kv256Bars {
+  uint64_t own_full;
+  uint64_t q_full[2];
+  uint64_t q_empty[2];  // dK of the block in Q slot i has read it
+  uint64_t do_full;
+  uint64_t do_empty;    // both dPᵀ and dV of the block have read the dO slot
+  uint64_t vec_full[2];
+  uint64_t s_full;
+  uint64_t dp_full;
+  uint64_t p_ready;     // Pᵀ packed
+  uint64_t ds_ready;    // dSᵀ packed
+  uint64_t x_free;      // dV consumed Pᵀ (Sᵀ region free)
+  uint64_t y_free;      // dK consumed dSᵀ (dPᵀ region free)
+  uint64_t acc_done;
+  uint32_t tmem_base;
+  int abort;
+  alignas(16) float nlse2[2][kStr];   // −log2e·lse per query of the block in Q slot i
+  alignas(16) float ndelta[2][kStr];  // −δ per query
+};
+constexpr int kKvK = 0;
+constexpr int kKvV = kOwnBytes;
+constexpr int kKvQ = 2 * kOwnBytes;        // two Q slots
+constexpr int kKvDo = kKvQ + 2 * kStrBytes;  // one dO slot
+constexpr int kKvBars = kKvDo + kStrBytes;   // 224 KB of tiles, then the barriers
+constexpr int kKvBytes = kKvBars + (int)sizeof(Kv256Bars);
+static_assert(kKvBytes <= 227 * 1024, "dK/dV shared memory exceeds the per-block limit");
+
+template <typename T>
+__global__ void __launch_bounds__(kKvThreads, 1)
+    tc_dkdv256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                      const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv, Problem p) {
+  constexpr bool kBf16 = IsBf16<T>::value;
+  constexpr uint32_t kIdS = idesc_f16(kOwn, kStr, kBf16, false, false);   // M = 128, N = 64
+  constexpr uint32_t kIdAcc = idesc_f16(kOwn, 128, kBf16, false, true);   // M = 128, N = 128 (half of D)
+  // TMEM columns: dV and dK of this pass's half of D, Sᵀ (→ Pᵀ), dPᵀ (→ dSᵀ).
+  constexpr uint32_t kColDv = 0, kColDk = 128, kColX = 256, kColY = 320;
+  extern __shared__ unsigned char smem_raw[];
+  // The layout assumes a 1024-byte aligned base (TMA's 128-byte swizzle and the MMA
+  // descriptors need it); should a launch place it elsewhere, the block reports an error
+  // and leaves before touching shared memory.
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) report_error(p.err, kDevErrLayout, kKidTcDkdv);
+    return;
+  }
+  uint8_t* sm = smem_raw;
+  Kv256Bars& bars = *reinterpret_cast<Kv256Bars*>(sm + kKvBars);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // Block order: the two passes (halves of D) of one (batch, KV head) unit next to each
+  // other, all units of one key tile, then the next tile; under the causal mask the first
+  // key tiles see the most queries, so the heavy blocks go first.
+  const int half = blockIdx.x & 1;
+  const int rest = blockIdx.x >> 1;
+  const int units = p.B * p.Hkv;
+  const int unit = rest % units;
+  const int b = unit / p.Hkv, g = unit % p.Hkv;
+  const int j0 = (rest / units) * kOwn;  // first key of this block
+  // Queries before j0 - coff see none of these keys.
+  const int i_begin = p.causal ? max(0, j0 - p.coff) : 0;
+  const int nqb = i_begin < p.Lq ? (p.Lq - i_begin + kStr - 1) / kStr : 0;
+  const int total = p.G * nqb;
+
+  if (threadIdx.x == 0) {
+    bars.abort = 0;
+    mbar_init(&bars.own_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars.q_full[s], 1);
+      mbar_init(&bars.q_empty[s], 1);
+      mbar_init(&bars.vec_full[s], 32);  // every lane of the producer warp
+    }
+    mbar_init(&bars.do_full, 1);
+    mbar_init(&bars.do_empty, 2);  // dPᵀ (warp 18) and dV (warp 17)
+    mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.dp_full, 1);
+    mbar_init(&bars.p_ready, 512);
+    mbar_init(&bars.ds_ready, 512);
+    mbar_init(&bars.x_free, 1);
+    mbar_init(&bars.y_free, 1);
+    mbar_init(&bars.acc_done, 2);  // one commit per MMA issuer
+    fence_mbar_init();
+  }
+  if (warp == kIssuer) {
+    tmem_alloc(&bars.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = bars.tmem_base;
+  const WaitCtx wc{&bars.abort, 0, p.wait_limit_ns, p.err, kKidTcDkdv};
+
+  if (warp == kProducer) {
+    // K and V once; per query block n: Q(n) into slot n % 2 once dK(n-2) has read it, the
+    // per-query vectors beside it, then dO(n) once dPᵀ(n-1) and dV(n-1) have read the slot.
+    if (lane == 0) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tdo);
+      mbar_arrive_expect_tx(&bars.own_full, 2 * kOwnBytes);
+      for (int cb = 0; cb < 4; ++cb) {
+        tma_load_4d(sm + kKvK + cb * kOwnCb, &tk, &bars.own_full, cb * 64, j0, g, b);
+        tma_load_4d(sm + kKvV + cb * kOwnCb, &tv, &bars.own_full, cb * 64, j0, g, b);
+      }
+    }
+    int q_issued = 0, do_issued = 0;
+    bool ok = true;
+    for (int n = 0; ok && n < total; ++n) {
+      const int s = n % 2;
+      const int h = g * p.G + n / nqb;
+      const int i0 = i_begin + (n % nqb) * kStr;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.q_empty[s], ((n / 2) & 1) ^ 1, wc)))) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars.q_full[s], kStrBytes);
+        for (int cb = 0; cb < 4; ++cb)
+          tma_load_4d(sm + kKvQ + s * kStrBytes + cb * kStrCb, &tq, &bars.q_full[s], cb * 64, i0, h, b);
+      }
+      q_issued = n + 1;
+      // Per-query vectors, negated for the packed math of the element warps.
+      const float* lsep = p.lse + q_row(p, b, h, 0);
+      const float* dlp = p.delta + q_row(p, b, h, 0);
+#pragma unroll
+      for (int e = lane; e < kStr; e += 32) {
+        const int i = i0 + e;
+        const float l = i < p.Lq ? lsep[i] : -pos_inf();  // −inf: the row sees no key, P = 0
+        bars.nlse2[s][e] = l == -pos_inf() ? -pos_inf() : -l * kLog2e;
+        bars.ndelta[s][e] = i < p.Lq ? -dlp[i] : 0.f;
+      }
+      mbar_arrive(&bars.vec_full[s]);
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.do_empty, (n & 1) ^ 1, wc)))) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars.do_full, kStrBytes);
+        for (int cb = 0; cb < 4; ++cb)
+          tma_load_4d(sm + kKvDo + cb * kStrCb, &tdo, &bars.do_full, cb * 64, i0, h, b);
+      }
+      do_issued = n + 1;
+    }
+    if (lane == 0 && (!ok || bars.abort)) {
+      for (int n = max(0, q_issued - 2); n < q_issued; ++n) drain_wait(&bars.q_full[n % 2], (n / 2) & 1);
+      if (do_issued > 0) drain_wait(&bars.do_full, (do_issued - 1) & 1);
+    }
+  } else if (warp == kIssuer || warp == kIssuer + 1) {
+    // Warp 17 issues in the order dV(n), Sᵀ(n+1), dK(n), as at D <= 128 (Sᵀ(n+1) overwrites
+    // the Pᵀ(n) that dV(n) reads); warp 18 issues dPᵀ(n) once dK(n-1) has consumed dSᵀ(n-1).
+    constexpr unsigned kAll = 0xffffffffu;
+    const bool chain_x = __shfl_sync(kAll, warp, 0) == kIssuer;
+    bool ok = __all_sync(kAll, mbar_wait(&bars.own_full, 0, wc));
+    tc_fence_after();
+    const uint32_t k_s = smem_u32(sm + kKvK), v_s = smem_u32(sm + kKvV), do_s = smem_u32(sm + kKvDo);
+    auto q_slot = [&](int n) { return smem_u32(sm + kKvQ + (n % 2) * kStrBytes); };
+    const uint32_t dcol = 2 * half * kStrCb;  // this pass's half of D in a streamed tile
+    if (chain_x) {
+      if (ok && total > 0) {
+        ok = __all_sync(kAll, mbar_wait(&bars.q_full[0], 0, wc));
+        if (ok) {
+          tc_fence_after();
+          mma_scores256(tbase + kColX, k_s, q_slot(0), kIdS);  // Sᵀ(0) = K·Q(0)ᵀ
+          mma_commit_w(&bars.s_full);
+        }
+      }
+      for (int n = 0; ok && n < total; ++n) {
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.p_ready, n & 1, wc) && mbar_wait(&bars.do_full, n & 1, wc))))
+          break;
+        tc_fence_after();
+        mma_acc256(tbase + kColDv, tbase + kColX, do_s + dcol, kIdAcc, n == 0);  // dV += Pᵀ·dO
+        mma_commit_w(&bars.x_free);
+        mma_commit_w(&bars.do_empty);  // one of the slot's two arrivals
+        if (n + 1 < total) {
+          if (!(ok = __all_sync(kAll, mbar_wait(&bars.q_full[(n + 1) % 2], ((n + 1) / 2) & 1, wc) &&
+                                          mbar_wait(&bars.x_free, n & 1, wc))))
+            break;
+          tc_fence_after();
+          mma_scores256(tbase + kColX, k_s, q_slot(n + 1), kIdS);  // Sᵀ(n+1)
+          mma_commit_w(&bars.s_full);
+        }
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.ds_ready, n & 1, wc)))) break;
+        tc_fence_after();
+        mma_acc256(tbase + kColDk, tbase + kColY, q_slot(n) + dcol, kIdAcc, n == 0);  // dK += dSᵀ·Q
+        mma_commit_w(&bars.y_free);
+        mma_commit_w(&bars.q_empty[n % 2]);
+      }
+    } else {
+      for (int n = 0; ok && n < total; ++n) {
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.do_full, n & 1, wc)))) break;
+        if (n > 0 && !(ok = __all_sync(kAll, mbar_wait(&bars.y_free, (n - 1) & 1, wc)))) break;
+        tc_fence_after();
+        mma_scores256(tbase + kColY, v_s, do_s, kIdS);  // dPᵀ = V·dOᵀ
+        mma_commit_w(&bars.dp_full);
+        mma_commit_w(&bars.do_empty);
+      }
+    }
+    mma_commit_w(&bars.acc_done);
+    drain_wait(&bars.acc_done, 0);
+  } else {
+    // Warp e: TMEM lane quarter e % 4 (keys), query columns [16c, 16c + 16) with c = e / 4.
+    const int c = warp / 4, quarter = warp % 4;
+    const int j = j0 + quarter * 32 + lane;  // this thread's key
+    const uint32_t x_addr = tmem_addr(tbase, quarter * 32, kColX + 16 * c);
+    const uint32_t y_addr = tmem_addr(tbase, quarter * 32, kColY + 16 * c);
+    const uint64_t cc = f2pack(p.scale_log2, p.scale_log2);
+    bool ok = true;
+    for (int n = 0; n < total; ++n) {
+      const int s = n % 2;
+      const int i0 = i_begin + (n % nqb) * kStr + 16 * c;  // first query of this warp's columns
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, n & 1, wc) &&
+                                       mbar_wait(&bars.vec_full[s], (n / 2) & 1, wc));
+      if (!ok) break;
+      tc_fence_after();
+      const int ic = i0 + p.coff;  // key j is hidden from query i0 + q when j > ic + q
+      const bool diag = p.causal && j0 + kOwn - 1 > ic;
+      const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(&bars.nlse2[s][16 * c]);
+      const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(&bars.ndelta[s][16 * c]);
+      // Pᵀ for this warp's 16 queries: packed over the first 8 of its Sᵀ columns for dV,
+      // kept in registers in fp32 for dSᵀ.
+      uint64_t pf[8];
+      {
+        uint32_t sr[16];
+        tmem_ld16(x_addr, sr);
+        tmem_ld_wait(sr);
+        uint32_t pk[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float p0, p1;
+          ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl2[e]), p0, p1);
+          if (diag) {
+            if (j > ic + 2 * e) p0 = 0.f;
+            if (j > ic + 2 * e + 1) p1 = 0.f;
+          }
+          pf[e] = f2pack(p0, p1);
+          pk[e] = pack2<T>(p0, p1);
+        }
+        tmem_st8(x_addr, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars.p_ready);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_full, n & 1, wc));
+      if (!ok) break;
+      tc_fence_after();
+      // dSᵀ = Pᵀ∘(dPᵀ − δ), one TMEM load.
+      {
+        uint32_t dr[16];
+        tmem_ld16(y_addr, dr);
+        tmem_ld_wait(dr);
+        uint32_t dk[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float d0, d1;
+          f2unpack(fmul2(pf[e], fadd2(f2pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), nd2[e])), d0,
+                   d1);
+          dk[e] = pack2<T>(d0, d1);
+        }
+        tmem_st8(y_addr, dk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars.ds_ready);
+    }
+    // Epilogue: dV and dK·scale of this pass's half of D, each in 4 chunks of 32 columns
+    // (warps of group c take dV chunk c and dK chunk c), staged in the first two column
+    // blocks of the block's own V and K buffers (no MMA reads them once acc_done has
+    // completed) and written by bulk tensor stores at columns [128·half, 128·half + 128)
+    // once all 16 warps have staged theirs (keys past Lkv are clipped).  With no query
+    // block (total == 0) nothing else has waited for the K and V load, so wait for it here.
+    if (ok)
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.own_full, 0, wc) && (total == 0 || mbar_wait(&bars.acc_done, 0, wc)));
+    const int r = quarter * 32 + lane;
+    if (ok) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int ch = c; ch < 8; ch += 4) {
+        const bool is_dk = ch >= 4;
+        const int c32 = ch % 4;
+        const float mul = is_dk ? p.scale : 1.f;
+        uint32_t acc[32];
+        if (total > 0) {
+          tmem_ld32(tmem_addr(tbase, quarter * 32, (is_dk ? kColDk : kColDv) + 32 * c32), acc);
+          tmem_ld_wait(acc);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) acc[e] = 0u;  // no query sees these keys
+        }
+        uint32_t packed[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          packed[e] = pack2<T>(__uint_as_float(acc[2 * e]) * mul, __uint_as_float(acc[2 * e + 1]) * mul);
+        uint8_t* blk = sm + (is_dk ? kKvK : kKvV) + (c32 / 2) * kOwnCb;
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4)
+          *reinterpret_cast<uint4*>(blk + sw128_off(r, (c32 % 2) * 4 + v4)) =
+              make_uint4(packed[4 * v4], packed[4 * v4 + 1], packed[4 * v4 + 2], packed[4 * v4 + 3]);
+      }
+      fence_async_smem();
+    }
+    if (named_sync_and(1, 512, ok) && warp == 0 && lane == 0) {
+      for (int cb = 0; cb < 2; ++cb) {
+        tma_store_4d(&tdv, sm + kKvV + cb * kOwnCb, 128 * half + cb * 64, j0, g, b);
+        tma_store_4d(&tdk, sm + kKvK + cb * kOwnCb, 128 * half + cb * 64, j0, g, b);
+      }
+      bulk_commit();
+      bulk_wait_read();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kIssuer) {
+    __syncwarp();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <typename T>
+cudaError_t dq256_t(const Problem& p, cudaStream_t s) {
+  CUtensorMap tq, tk, tv, tdo, tdq;
+  if (!make_tmap_4d(&tq, p.q, kD, p.Lq, p.Hq, p.B, p.lq, kOwn) ||
+      !make_tmap_4d(&tdo, p.dout, kD, p.Lq, p.Hq, p.B, p.ldo, kOwn) ||
+      !make_tmap_4d(&tdq, p.dq, kD, p.Lq, p.Hq, p.B, p.ldq, kOwn) ||
+      !make_tmap_4d(&tk, p.k, kD, p.Lkv, p.Hkv, p.B, p.lk, kStr) ||
+      !make_tmap_4d(&tv, p.v, kD, p.Lkv, p.Hkv, p.B, p.lv, kStr))
+    return cudaErrorInvalidValue;
+  const int smem = kDqBytes + 1024;
+  auto kern = tc_dq256_kernel<T>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const unsigned nqt = (p.Lq + kOwn - 1) / kOwn;
+  kern<<<nqt * p.Hq * p.B, kDqThreads, smem, s>>>(tq, tk, tv, tdo, tdq, p);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t dkdv256_t(const Problem& p, cudaStream_t s) {
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+  if (!make_tmap_4d(&tk, p.k, kD, p.Lkv, p.Hkv, p.B, p.lk, kOwn) ||
+      !make_tmap_4d(&tv, p.v, kD, p.Lkv, p.Hkv, p.B, p.lv, kOwn) ||
+      !make_tmap_4d(&tdk, p.dk, kD, p.Lkv, p.Hkv, p.B, p.ldk, kOwn) ||
+      !make_tmap_4d(&tdv, p.dv, kD, p.Lkv, p.Hkv, p.B, p.ldv, kOwn) ||
+      !make_tmap_4d(&tq, p.q, kD, p.Lq, p.Hq, p.B, p.lq, kStr) ||
+      !make_tmap_4d(&tdo, p.dout, kD, p.Lq, p.Hq, p.B, p.ldo, kStr))
+    return cudaErrorInvalidValue;
+  auto kern = tc_dkdv256_kernel<T>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kKvBytes);
+  if (e != cudaSuccess) return e;
+  const unsigned nkt = (p.Lkv + kOwn - 1) / kOwn;
+  kern<<<2 * nkt * p.Hkv * p.B, kKvThreads, kKvBytes, s>>>(tq, tk, tv, tdo, tdk, tdv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tensor_bwd256_supported(const Problem& p, int dtype) {
+  return tensor_supported(p, dtype) && p.D == kD && p.mask == nullptr;
+}
+
+cudaError_t launch_tc_dq256(const Problem& p, int dtype, cudaStream_t s) {
+  return dtype == 2 ? dq256_t<__nv_bfloat16>(p, s) : dq256_t<__half>(p, s);
+}
+
+cudaError_t launch_tc_dkdv256(const Problem& p, int dtype, cudaStream_t s) {
+  return dtype == 2 ? dkdv256_t<__nv_bfloat16>(p, s) : dkdv256_t<__half>(p, s);
+}
+
+}  // namespace sdpa

@@ -166,26 +166,42 @@ def test_head_dim_256(shape, dtype, causal):
     (Shape(1, 4, 1, 257, 257, 256), "bf16", 2),        # bottom-right causal, Lq = Lkv
     (Shape(1, 2, 2, 64, 96, 256), "f16", True),        # one KV tile: the split P path only
 ])
-def test_head_dim_256_forward_on_tensor_cores(shape, dtype, causal):
-    """The fp16/bf16 forward at D = 256 runs on the tensor-core kernel (forced here); its
-    backward runs on the CUDA-core kernels."""
+def test_head_dim_256_on_tensor_cores(shape, dtype, causal):
+    """The fp16/bf16 forward and backward at D = 256 on the tensor-core kernels (forced)."""
     with api.force_path(_lib.PATH_TENSOR):
-        full_parity(shape, dtype, causal, seed=32, backward=False)
-    full_parity(shape, dtype, causal, seed=32)
+        full_parity(shape, dtype, causal, seed=32)
+
+
+@pytest.mark.parametrize("shape,dtype,causal", [
+    (Shape(1, 4, 1, 200, 330, 256), "bf16", False),    # G = 4: each dK/dV block streams 4 heads
+    (Shape(1, 2, 2, 1, 150, 256), "f16", False),       # one query row
+    (Shape(1, 2, 1, 100, 300, 256), "bf16", 2),        # bottom-right, offset 200: key tiles start mid-query-range
+    (Shape(2, 2, 2, 129, 65, 256), "f16", True),       # top-left causal, one row past a tile
+    (Shape(1, 2, 2, 70, 1, 256), "bf16", False),       # a single key
+])
+def test_head_dim_256_backward_edges(shape, dtype, causal):
+    """Edge cases of the D = 256 tensor-core backward: query blocks of 64 rows streamed per
+    head of a group, key and query tails, a causal offset, a single key."""
+    with api.force_path(_lib.PATH_TENSOR):
+        full_parity(shape, dtype, causal, seed=33)
 
 
 def test_head_dim_256_refusals():
     """The short-query kernels refuse D = 256; the forced tensor path serves the D = 256
-    forward but refuses its backward."""
+    backward without a mask but refuses it with one."""
     q = torch.zeros(1, 2, 4, 256, device="cuda", dtype=torch.bfloat16)
     with api.force_path(_lib.PATH_VECTOR):
         with pytest.raises(_lib.SdpaError) as e:
             api.attention_forward(q, q, q)
         assert e.value.status == 2
+    mask = torch.ones(4, 4, dtype=torch.bool, device="cuda")
     with api.force_path(_lib.PATH_TENSOR):
         out, lse = api.attention_forward(q, q, q)
+        dq, dk, dv = api.attention_backward(q, q, q, out, q, lse)
+        assert torch.count_nonzero(dq) == 0 and torch.count_nonzero(dv) == 0
+        out, lse = api.attention_forward(q, q, q, attn_mask=mask)
         with pytest.raises(_lib.SdpaError) as e:
-            api.attention_backward(q, q, q, out, q, lse)
+            api.attention_backward(q, q, q, out, q, lse, attn_mask=mask)
         assert e.value.status == 2
     api.poll_status()
 
