@@ -8,17 +8,15 @@
 //       Q and dO (64 KB each), two 32 KB K stages (K lives through S and dQ) and one 32 KB
 //       V stage (224 KB).  S = Q·Kᵀ and dP = dO·Vᵀ are M = 128, N = 64 products over 16
 //       K-steps; dQ += dS·K is one M = 128, N = 256 product over 4 K-steps.
-//   dK/dV: D is split in two halves over two passes, whose blocks run side by side: a
-//       block owns 128 keys of one KV head, accumulates dV and dK of its half of D (128
-//       TMEM columns each) and streams 64-row query blocks of the G query heads of its
-//       group.  Sᵀ = K·Qᵀ and dPᵀ = V·dOᵀ (64 columns each) are recomputed over the full D
-//       in each pass (1.5x the MMA work of one pass).  Shared memory: K and V whole
-//       (128 KB), two 32 KB Q slots (Q lives through Sᵀ and dK) and one 32 KB dO slot.
+//   dK/dV: a block owns 128 keys of one KV head and streams 64-row query blocks of the G
+//       query heads of its group; one block of a neighbouring pair accumulates dK, the
+//       other dV, each over the full D in 256 TMEM columns.  Both compute Sᵀ = K·Qᵀ; the dK
+//       block also dPᵀ = V·dOᵀ (2.5F of MMA work in all against 3F for a split of D).
 // Warp roles as in the D <= 128 kernels: warps 0-15 element work (warp e takes TMEM lane
 // quarter e % 4 and the 16 streamed columns [16c, 16c + 16), c = e / 4, and writes its
 // packed 16-bit results over the first 8 of them), warp 16 the TMA producer, warps 17-19
-// (dQ: S, dP, dQ) or 17-18 (dK/dV) the MMA issuers; warp 17 owns the TMEM.  Every wait is
-// bounded, as everywhere in the library.
+// the MMA issuers; warp 17 owns the TMEM.  Every wait is bounded, as everywhere in the
+// library.
 #include "launch.h"
 #include "tc_common.cuh"
 
@@ -41,7 +39,6 @@ constexpr int kDqThreads = 640;
 constexpr int kRegsLow = 56;
 constexpr int kRegsHigh = 104;
 static_assert(128 * kRegsLow + 512 * kRegsHigh <= kDqThreads * 96, "register split exceeds the launch");
-constexpr int kKvThreads = 608;
 
 template <typename T>
 struct IsBf16 { static constexpr bool value = false; };
@@ -327,19 +324,32 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 }
 
 // ================================================================== dK / dV
+// Two kinds of block, neighbours in the grid (blockIdx.x & 1): a dK block computes
+// Sᵀ = K·Qᵀ, dPᵀ = V·dOᵀ and dK += dSᵀ·Q; a dV block computes Sᵀ and dV += Pᵀ·dO.  Each
+// accumulates its gradient over the full D in 256 TMEM columns; Sᵀ is computed by both
+// (2.5F of MMA work in all where a split of D into halves would take 3F).
+//   dK block: TMEM dK [0, 256), Sᵀ [256, 320), dPᵀ → dSᵀ in two buffers [320, 448).  Shared
+//     memory: K, V (64 KB each), two Q slots, one dO slot (32 KB each).  Warp 17 issues
+//     Sᵀ(n) once every element thread has read Sᵀ(n-1) (P stays in registers), warp 18
+//     dPᵀ(n) into buffer n % 2 once dK(n-2) has read it, warp 19 dK += dSᵀ(n)·Q(n).
+//   dV block: TMEM dV [0, 256), Sᵀ → Pᵀ in two buffers [256, 384).  Shared memory: K, two
+//     dO slots in the place of V, two Q slots.  Warp 17 issues Sᵀ(n) into buffer n % 2 once
+//     dV(n-2) has read it, warp 18 dV += Pᵀ(n)·dO(n); warp 19 has nothing to issue.
 struct Kv256Bars {
   uint64_t own_full;
   uint64_t q_full[2];
-  uint64_t q_empty[2];  // dK of the block in Q slot i has read it
-  uint64_t do_full;
-  uint64_t do_empty;    // both dPᵀ and dV of the block have read the dO slot
-  uint64_t vec_full[2];
-  uint64_t s_full;
-  uint64_t dp_full;
-  uint64_t p_ready;     // Pᵀ packed
-  uint64_t ds_ready;    // dSᵀ packed
-  uint64_t x_free;      // dV consumed Pᵀ (Sᵀ region free)
-  uint64_t y_free;      // dK consumed dSᵀ (dPᵀ region free)
+  uint64_t q_empty[2];    // the last MMA reading Q slot i has finished
+  uint64_t do_full[2];
+  uint64_t do_empty[2];   // the MMA reading dO slot i has finished
+  uint64_t vec_full[2];   // per-query vectors of slot i written (32 producer lanes)
+  uint64_t vec_empty[2];  // every element thread is done with them
+  uint64_t s_full[2];     // Sᵀ in buffer i (dK blocks: buffer 0 only)
+  uint64_t s_read;        // dK blocks: every element thread has read Sᵀ
+  uint64_t p_ready[2];    // dV blocks: Pᵀ packed in buffer i
+  uint64_t x_free[2];     // dV blocks: dV has read buffer i
+  uint64_t dp_full[2];    // dK blocks: dPᵀ in buffer i
+  uint64_t ds_ready[2];   // dK blocks: dSᵀ packed in buffer i
+  uint64_t y_free[2];     // dK blocks: dK has read buffer i
   uint64_t acc_done;
   uint32_t tmem_base;
   int abort;
@@ -347,12 +357,13 @@ struct Kv256Bars {
   alignas(16) float ndelta[2][kStr];  // −δ per query
 };
 constexpr int kKvK = 0;
-constexpr int kKvV = kOwnBytes;
+constexpr int kKvV = kOwnBytes;            // V (dK blocks) or two dO slots (dV blocks)
 constexpr int kKvQ = 2 * kOwnBytes;        // two Q slots
-constexpr int kKvDo = kKvQ + 2 * kStrBytes;  // one dO slot
+constexpr int kKvDo = kKvQ + 2 * kStrBytes;  // the dO slot of dK blocks
 constexpr int kKvBars = kKvDo + kStrBytes;   // 224 KB of tiles, then the barriers
 constexpr int kKvBytes = kKvBars + (int)sizeof(Kv256Bars);
 static_assert(kKvBytes <= 227 * 1024, "dK/dV shared memory exceeds the per-block limit");
+constexpr int kKvThreads = 640;
 
 template <typename T>
 __global__ void __launch_bounds__(kKvThreads, 1)
@@ -360,10 +371,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                       const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv, Problem p) {
   constexpr bool kBf16 = IsBf16<T>::value;
-  constexpr uint32_t kIdS = idesc_f16(kOwn, kStr, kBf16, false, false);   // M = 128, N = 64
-  constexpr uint32_t kIdAcc = idesc_f16(kOwn, 128, kBf16, false, true);   // M = 128, N = 128 (half of D)
-  // TMEM columns: dV and dK of this pass's half of D, Sᵀ (→ Pᵀ), dPᵀ (→ dSᵀ).
-  constexpr uint32_t kColDv = 0, kColDk = 128, kColX = 256, kColY = 320;
+  constexpr uint32_t kIdS = idesc_f16(kOwn, kStr, kBf16, false, false);  // M = 128, N = 64
+  constexpr uint32_t kIdAcc = idesc_f16(kOwn, kD, kBf16, false, true);   // M = 128, N = 256, B MN-major
+  constexpr uint32_t kColAcc = 0, kColX = 256, kColY = 320;
   extern __shared__ unsigned char smem_raw[];
   // The layout assumes a 1024-byte aligned base (TMA's 128-byte swizzle and the MMA
   // descriptors need it); should a launch place it elsewhere, the block reports an error
@@ -376,10 +386,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   Kv256Bars& bars = *reinterpret_cast<Kv256Bars*>(sm + kKvBars);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // Block order: the two passes (halves of D) of one (batch, KV head) unit next to each
+  // Block order: the dK and the dV block of one (batch, KV head, key tile) next to each
   // other, all units of one key tile, then the next tile; under the causal mask the first
   // key tiles see the most queries, so the heavy blocks go first.
-  const int half = blockIdx.x & 1;
+  const bool dv = (blockIdx.x & 1) != 0;
   const int rest = blockIdx.x >> 1;
   const int units = p.B * p.Hkv;
   const int unit = rest % units;
@@ -389,6 +399,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   const int i_begin = p.causal ? max(0, j0 - p.coff) : 0;
   const int nqb = i_begin < p.Lq ? (p.Lq - i_begin + kStr - 1) / kStr : 0;
   const int total = p.G * nqb;
+  // dO slot of query block n and the parity of its use: two slots in dV blocks, one in dK.
+  auto do_slot = [&](int n) { return dv ? (n & 1) : 0; };
+  auto do_par = [&](int n) { return static_cast<uint32_t>(dv ? (n >> 1) & 1 : n & 1); };
+  auto do_off = [&](int n) { return dv ? kKvV + (n & 1) * kStrBytes : kKvDo; };
 
   if (threadIdx.x == 0) {
     bars.abort = 0;
@@ -396,17 +410,19 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars.q_full[s], 1);
       mbar_init(&bars.q_empty[s], 1);
+      mbar_init(&bars.do_full[s], 1);
+      mbar_init(&bars.do_empty[s], 1);
       mbar_init(&bars.vec_full[s], 32);  // every lane of the producer warp
+      mbar_init(&bars.vec_empty[s], 512);
+      mbar_init(&bars.s_full[s], 1);
+      mbar_init(&bars.p_ready[s], 512);
+      mbar_init(&bars.x_free[s], 1);
+      mbar_init(&bars.dp_full[s], 1);
+      mbar_init(&bars.ds_ready[s], 512);
+      mbar_init(&bars.y_free[s], 1);
     }
-    mbar_init(&bars.do_full, 1);
-    mbar_init(&bars.do_empty, 2);  // dPᵀ (warp 18) and dV (warp 17)
-    mbar_init(&bars.s_full, 1);
-    mbar_init(&bars.dp_full, 1);
-    mbar_init(&bars.p_ready, 512);
-    mbar_init(&bars.ds_ready, 512);
-    mbar_init(&bars.x_free, 1);
-    mbar_init(&bars.y_free, 1);
-    mbar_init(&bars.acc_done, 2);  // one commit per MMA issuer
+    mbar_init(&bars.s_read, 512);
+    mbar_init(&bars.acc_done, 3);  // one commit per MMA issuer warp
     fence_mbar_init();
   }
   if (warp == kIssuer) {
@@ -418,17 +434,20 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   tc_fence_after();
   const uint32_t tbase = bars.tmem_base;
   const WaitCtx wc{&bars.abort, 0, p.wait_limit_ns, p.err, kKidTcDkdv};
+  constexpr unsigned kAll = 0xffffffffu;
 
   if (warp == kProducer) {
-    // K and V once; per query block n: Q(n) into slot n % 2 once dK(n-2) has read it, the
-    // per-query vectors beside it, then dO(n) once dPᵀ(n-1) and dV(n-1) have read the slot.
+    // K (and V in dK blocks) once; per query block n: Q(n) into slot n % 2 once its last
+    // reader of n-2 has finished, the per-query vectors beside it once the element threads
+    // are done with those of n-2, then dO(n) once the reader of its slot's previous block
+    // has finished.
     if (lane == 0) {
       prefetch_tmap(&tq);
       prefetch_tmap(&tdo);
-      mbar_arrive_expect_tx(&bars.own_full, 2 * kOwnBytes);
+      mbar_arrive_expect_tx(&bars.own_full, (dv ? 1 : 2) * kOwnBytes);
       for (int cb = 0; cb < 4; ++cb) {
         tma_load_4d(sm + kKvK + cb * kOwnCb, &tk, &bars.own_full, cb * 64, j0, g, b);
-        tma_load_4d(sm + kKvV + cb * kOwnCb, &tv, &bars.own_full, cb * 64, j0, g, b);
+        if (!dv) tma_load_4d(sm + kKvV + cb * kOwnCb, &tv, &bars.own_full, cb * 64, j0, g, b);
       }
     }
     int q_issued = 0, do_issued = 0;
@@ -437,7 +456,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       const int s = n % 2;
       const int h = g * p.G + n / nqb;
       const int i0 = i_begin + (n % nqb) * kStr;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.q_empty[s], ((n / 2) & 1) ^ 1, wc)))) break;
+      if (!(ok = __all_sync(kAll, mbar_wait(&bars.q_empty[s], ((n / 2) & 1) ^ 1, wc)))) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(&bars.q_full[s], kStrBytes);
         for (int cb = 0; cb < 4; ++cb)
@@ -445,6 +464,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       }
       q_issued = n + 1;
       // Per-query vectors, negated for the packed math of the element warps.
+      if (!(ok = __all_sync(kAll, mbar_wait(&bars.vec_empty[s], ((n / 2) & 1) ^ 1, wc)))) break;
       const float* lsep = p.lse + q_row(p, b, h, 0);
       const float* dlp = p.delta + q_row(p, b, h, 0);
 #pragma unroll
@@ -452,69 +472,77 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         const int i = i0 + e;
         const float l = i < p.Lq ? lsep[i] : -pos_inf();  // −inf: the row sees no key, P = 0
         bars.nlse2[s][e] = l == -pos_inf() ? -pos_inf() : -l * kLog2e;
-        bars.ndelta[s][e] = i < p.Lq ? -dlp[i] : 0.f;
+        bars.ndelta[s][e] = (!dv && i < p.Lq) ? -dlp[i] : 0.f;
       }
       mbar_arrive(&bars.vec_full[s]);
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&bars.do_empty, (n & 1) ^ 1, wc)))) break;
+      if (!(ok = __all_sync(kAll, mbar_wait(&bars.do_empty[do_slot(n)], do_par(n) ^ 1, wc)))) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars.do_full, kStrBytes);
+        mbar_arrive_expect_tx(&bars.do_full[do_slot(n)], kStrBytes);
         for (int cb = 0; cb < 4; ++cb)
-          tma_load_4d(sm + kKvDo + cb * kStrCb, &tdo, &bars.do_full, cb * 64, i0, h, b);
+          tma_load_4d(sm + do_off(n) + cb * kStrCb, &tdo, &bars.do_full[do_slot(n)], cb * 64, i0, h, b);
       }
       do_issued = n + 1;
     }
-    if (lane == 0 && (!ok || bars.abort)) {
+    if (lane == 0 && (!ok || bars.abort)) {  // let copies still in flight land before the block exits
       for (int n = max(0, q_issued - 2); n < q_issued; ++n) drain_wait(&bars.q_full[n % 2], (n / 2) & 1);
-      if (do_issued > 0) drain_wait(&bars.do_full, (do_issued - 1) & 1);
+      for (int n = max(0, do_issued - (dv ? 2 : 1)); n < do_issued; ++n)
+        drain_wait(&bars.do_full[do_slot(n)], do_par(n));
     }
-  } else if (warp == kIssuer || warp == kIssuer + 1) {
-    // Warp 17 issues in the order dV(n), Sᵀ(n+1), dK(n), as at D <= 128 (Sᵀ(n+1) overwrites
-    // the Pᵀ(n) that dV(n) reads); warp 18 issues dPᵀ(n) once dK(n-1) has consumed dSᵀ(n-1).
-    constexpr unsigned kAll = 0xffffffffu;
-    const bool chain_x = __shfl_sync(kAll, warp, 0) == kIssuer;
+  } else if (warp >= kIssuer) {
+    const int role = __shfl_sync(kAll, warp - kIssuer, 0);
     bool ok = __all_sync(kAll, mbar_wait(&bars.own_full, 0, wc));
     tc_fence_after();
-    const uint32_t k_s = smem_u32(sm + kKvK), v_s = smem_u32(sm + kKvV), do_s = smem_u32(sm + kKvDo);
-    auto q_slot = [&](int n) { return smem_u32(sm + kKvQ + (n % 2) * kStrBytes); };
-    const uint32_t dcol = 2 * half * kStrCb;  // this pass's half of D in a streamed tile
-    if (chain_x) {
-      if (ok && total > 0) {
-        ok = __all_sync(kAll, mbar_wait(&bars.q_full[0], 0, wc));
-        if (ok) {
-          tc_fence_after();
-          mma_scores256(tbase + kColX, k_s, q_slot(0), kIdS);  // Sᵀ(0) = K·Q(0)ᵀ
-          mma_commit_w(&bars.s_full);
-        }
-      }
+    const uint32_t k_s = smem_u32(sm + kKvK), v_s = smem_u32(sm + kKvV);
+    auto q_s = [&](int n) { return smem_u32(sm + kKvQ + (n % 2) * kStrBytes); };
+    if (role == 0) {
+      // Sᵀ(n) = K·Q(n)ᵀ.
       for (int n = 0; ok && n < total; ++n) {
-        if (!(ok = __all_sync(kAll, mbar_wait(&bars.p_ready, n & 1, wc) && mbar_wait(&bars.do_full, n & 1, wc))))
+        const int s = n % 2;
+        bool w = mbar_wait(&bars.q_full[s], (n / 2) & 1, wc);
+        if (dv) w = w && mbar_wait(&bars.x_free[s], ((n / 2) & 1) ^ 1, wc);
+        else if (n > 0) w = w && mbar_wait(&bars.s_read, (n - 1) & 1, wc);
+        if (!(ok = __all_sync(kAll, w))) break;
+        tc_fence_after();
+        mma_scores256(tbase + kColX + (dv ? 64 * s : 0), k_s, q_s(n), kIdS);
+        mma_commit_w(&bars.s_full[dv ? s : 0]);
+        if (dv) mma_commit_w(&bars.q_empty[s]);
+      }
+    } else if (role == 1 && dv) {
+      // dV += Pᵀ(n)·dO(n).
+      for (int n = 0; ok && n < total; ++n) {
+        const int s = n % 2;
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.p_ready[s], (n / 2) & 1, wc) &&
+                                        mbar_wait(&bars.do_full[do_slot(n)], do_par(n), wc))))
           break;
         tc_fence_after();
-        mma_acc256(tbase + kColDv, tbase + kColX, do_s + dcol, kIdAcc, n == 0);  // dV += Pᵀ·dO
-        mma_commit_w(&bars.x_free);
-        mma_commit_w(&bars.do_empty);  // one of the slot's two arrivals
-        if (n + 1 < total) {
-          if (!(ok = __all_sync(kAll, mbar_wait(&bars.q_full[(n + 1) % 2], ((n + 1) / 2) & 1, wc) &&
-                                          mbar_wait(&bars.x_free, n & 1, wc))))
-            break;
-          tc_fence_after();
-          mma_scores256(tbase + kColX, k_s, q_slot(n + 1), kIdS);  // Sᵀ(n+1)
-          mma_commit_w(&bars.s_full);
-        }
-        if (!(ok = __all_sync(kAll, mbar_wait(&bars.ds_ready, n & 1, wc)))) break;
-        tc_fence_after();
-        mma_acc256(tbase + kColDk, tbase + kColY, q_slot(n) + dcol, kIdAcc, n == 0);  // dK += dSᵀ·Q
-        mma_commit_w(&bars.y_free);
-        mma_commit_w(&bars.q_empty[n % 2]);
+        mma_acc256(tbase + kColAcc, tbase + kColX + 64 * s, smem_u32(sm + do_off(n)), kIdAcc, n == 0);
+        mma_commit_w(&bars.x_free[s]);
+        mma_commit_w(&bars.do_empty[do_slot(n)]);
       }
-    } else {
+    } else if (role == 1) {
+      // dPᵀ(n) = V·dO(n)ᵀ into buffer n % 2.
       for (int n = 0; ok && n < total; ++n) {
-        if (!(ok = __all_sync(kAll, mbar_wait(&bars.do_full, n & 1, wc)))) break;
-        if (n > 0 && !(ok = __all_sync(kAll, mbar_wait(&bars.y_free, (n - 1) & 1, wc)))) break;
+        const int s = n % 2;
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.do_full[0], n & 1, wc) &&
+                                        mbar_wait(&bars.y_free[s], ((n / 2) & 1) ^ 1, wc))))
+          break;
         tc_fence_after();
-        mma_scores256(tbase + kColY, v_s, do_s, kIdS);  // dPᵀ = V·dOᵀ
-        mma_commit_w(&bars.dp_full);
-        mma_commit_w(&bars.do_empty);
+        mma_scores256(tbase + kColY + 64 * s, v_s, smem_u32(sm + kKvDo), kIdS);
+        mma_commit_w(&bars.dp_full[s]);
+        mma_commit_w(&bars.do_empty[0]);
+      }
+    } else if (!dv) {
+      // dK += dSᵀ(n)·Q(n).  Q(n) is loaded (Sᵀ(n) read it before dSᵀ(n) could exist);
+      // waiting on its barrier too makes the TMA writes visible to this warp's MMA directly.
+      for (int n = 0; ok && n < total; ++n) {
+        const int s = n % 2;
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.ds_ready[s], (n / 2) & 1, wc) &&
+                                        mbar_wait(&bars.q_full[s], (n / 2) & 1, wc))))
+          break;
+        tc_fence_after();
+        mma_acc256(tbase + kColAcc, tbase + kColY + 64 * s, q_s(n), kIdAcc, n == 0);
+        mma_commit_w(&bars.y_free[s]);
+        mma_commit_w(&bars.q_empty[s]);
       }
     }
     mma_commit_w(&bars.acc_done);
@@ -523,86 +551,91 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     // Warp e: TMEM lane quarter e % 4 (keys), query columns [16c, 16c + 16) with c = e / 4.
     const int c = warp / 4, quarter = warp % 4;
     const int j = j0 + quarter * 32 + lane;  // this thread's key
-    const uint32_t x_addr = tmem_addr(tbase, quarter * 32, kColX + 16 * c);
-    const uint32_t y_addr = tmem_addr(tbase, quarter * 32, kColY + 16 * c);
     const uint64_t cc = f2pack(p.scale_log2, p.scale_log2);
     bool ok = true;
     for (int n = 0; n < total; ++n) {
       const int s = n % 2;
       const int i0 = i_begin + (n % nqb) * kStr + 16 * c;  // first query of this warp's columns
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, n & 1, wc) &&
-                                       mbar_wait(&bars.vec_full[s], (n / 2) & 1, wc));
+      ok = __all_sync(kAll, mbar_wait(&bars.s_full[dv ? s : 0], dv ? (n / 2) & 1 : n & 1, wc) &&
+                                mbar_wait(&bars.vec_full[s], (n / 2) & 1, wc));
       if (!ok) break;
       tc_fence_after();
       const int ic = i0 + p.coff;  // key j is hidden from query i0 + q when j > ic + q
       const bool diag = p.causal && j0 + kOwn - 1 > ic;
       const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(&bars.nlse2[s][16 * c]);
       const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(&bars.ndelta[s][16 * c]);
-      // Pᵀ for this warp's 16 queries: packed over the first 8 of its Sᵀ columns for dV,
-      // kept in registers in fp32 for dSᵀ.
+      const uint32_t x_addr = tmem_addr(tbase, quarter * 32, kColX + (dv ? 64 * s : 0) + 16 * c);
+      uint32_t sr[16];
+      tmem_ld16(x_addr, sr);
+      tmem_ld_wait(sr);
+      if (!dv) {
+        tc_fence_before();
+        mbar_arrive(&bars.s_read);
+      }
+      // Pᵀ of this warp's 16 queries, in fp32 pairs.
       uint64_t pf[8];
-      {
-        uint32_t sr[16];
-        tmem_ld16(x_addr, sr);
-        tmem_ld_wait(sr);
-        uint32_t pk[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float p0, p1;
+        ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl2[e]), p0, p1);
+        if (diag) {
+          if (j > ic + 2 * e) p0 = 0.f;
+          if (j > ic + 2 * e + 1) p1 = 0.f;
+        }
+        pf[e] = f2pack(p0, p1);
+      }
+      uint32_t pk[8];
+      if (dv) {
+        mbar_arrive(&bars.vec_empty[s]);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           float p0, p1;
-          ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl2[e]), p0, p1);
-          if (diag) {
-            if (j > ic + 2 * e) p0 = 0.f;
-            if (j > ic + 2 * e + 1) p1 = 0.f;
-          }
-          pf[e] = f2pack(p0, p1);
+          f2unpack(pf[e], p0, p1);
           pk[e] = pack2<T>(p0, p1);
         }
-        tmem_st8(x_addr, pk);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bars.p_ready);
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_full, n & 1, wc));
-      if (!ok) break;
-      tc_fence_after();
-      // dSᵀ = Pᵀ∘(dPᵀ − δ), one TMEM load.
-      {
+        tmem_st8(x_addr, pk);  // Pᵀ over the first 8 of this warp's 16 columns
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars.p_ready[s]);
+      } else {
+        // dSᵀ = Pᵀ∘(dPᵀ − δ).
+        ok = __all_sync(kAll, mbar_wait(&bars.dp_full[s], (n / 2) & 1, wc));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t y_addr = tmem_addr(tbase, quarter * 32, kColY + 64 * s + 16 * c);
         uint32_t dr[16];
         tmem_ld16(y_addr, dr);
         tmem_ld_wait(dr);
-        uint32_t dk[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           float d0, d1;
           f2unpack(fmul2(pf[e], fadd2(f2pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), nd2[e])), d0,
                    d1);
-          dk[e] = pack2<T>(d0, d1);
+          pk[e] = pack2<T>(d0, d1);
         }
-        tmem_st8(y_addr, dk);
+        mbar_arrive(&bars.vec_empty[s]);
+        tmem_st8(y_addr, pk);  // dSᵀ over the first 8 of this warp's 16 columns
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars.ds_ready[s]);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bars.ds_ready);
     }
-    // Epilogue: dV and dK·scale of this pass's half of D, each in 4 chunks of 32 columns
-    // (warps of group c take dV chunk c and dK chunk c), staged in the first two column
-    // blocks of the block's own V and K buffers (no MMA reads them once acc_done has
-    // completed) and written by bulk tensor stores at columns [128·half, 128·half + 128)
-    // once all 16 warps have staged theirs (keys past Lkv are clipped).  With no query
-    // block (total == 0) nothing else has waited for the K and V load, so wait for it here.
+    // Epilogue: the gradient (dK·scale or dV) in 8 chunks of 32 columns (warps of group c
+    // take chunks c and c + 4), staged in the K buffer (no MMA reads it once acc_done has
+    // completed) and written by bulk tensor stores once all 16 warps have staged theirs
+    // (keys past Lkv are clipped).  With no query block (total == 0) nothing else has
+    // waited for the K load, so wait for it here.
     if (ok)
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars.own_full, 0, wc) && (total == 0 || mbar_wait(&bars.acc_done, 0, wc)));
+      ok = __all_sync(kAll, mbar_wait(&bars.own_full, 0, wc) && (total == 0 || mbar_wait(&bars.acc_done, 0, wc)));
     const int r = quarter * 32 + lane;
     if (ok) {
       tc_fence_after();
+      const float mul = dv ? 1.f : p.scale;
 #pragma unroll 1
-      for (int ch = c; ch < 8; ch += 4) {
-        const bool is_dk = ch >= 4;
-        const int c32 = ch % 4;
-        const float mul = is_dk ? p.scale : 1.f;
+      for (int c32 = c; c32 < kD / 32; c32 += 4) {
         uint32_t acc[32];
         if (total > 0) {
-          tmem_ld32(tmem_addr(tbase, quarter * 32, (is_dk ? kColDk : kColDv) + 32 * c32), acc);
+          tmem_ld32(tmem_addr(tbase, quarter * 32, kColAcc + 32 * c32), acc);
           tmem_ld_wait(acc);
         } else {
 #pragma unroll
@@ -612,7 +645,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           packed[e] = pack2<T>(__uint_as_float(acc[2 * e]) * mul, __uint_as_float(acc[2 * e + 1]) * mul);
-        uint8_t* blk = sm + (is_dk ? kKvK : kKvV) + (c32 / 2) * kOwnCb;
+        uint8_t* blk = sm + kKvK + (c32 / 2) * kOwnCb;
 #pragma unroll
         for (int v4 = 0; v4 < 4; ++v4)
           *reinterpret_cast<uint4*>(blk + sw128_off(r, (c32 % 2) * 4 + v4)) =
@@ -621,10 +654,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       fence_async_smem();
     }
     if (named_sync_and(1, 512, ok) && warp == 0 && lane == 0) {
-      for (int cb = 0; cb < 2; ++cb) {
-        tma_store_4d(&tdv, sm + kKvV + cb * kOwnCb, 128 * half + cb * 64, j0, g, b);
-        tma_store_4d(&tdk, sm + kKvK + cb * kOwnCb, 128 * half + cb * 64, j0, g, b);
-      }
+      for (int cb = 0; cb < 4; ++cb) tma_store_4d(dv ? &tdv : &tdk, sm + kKvK + cb * kOwnCb, cb * 64, j0, g, b);
       bulk_commit();
       bulk_wait_read();
     }
