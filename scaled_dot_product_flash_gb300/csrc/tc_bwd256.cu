@@ -47,6 +47,27 @@ struct IsBf16<__nv_bfloat16> { static constexpr bool value = true; };
 
 __device__ __forceinline__ float pos_inf() { return __int_as_float(0x7f800000); }
 
+// Thread-block cluster helpers: rank of this block in its cluster, a barrier over every
+// thread of the cluster (release / acquire at cluster scope), the address of a shared-memory
+// location in the block of another rank, and a 16-byte store there.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
@@ -324,10 +345,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 }
 
 // ================================================================== dK / dV
-// Two kinds of block, neighbours in the grid (blockIdx.x & 1): a dK block computes
-// Sᵀ = K·Qᵀ, dPᵀ = V·dOᵀ and dK += dSᵀ·Q; a dV block computes Sᵀ and dV += Pᵀ·dO.  Each
-// accumulates its gradient over the full D in 256 TMEM columns; Sᵀ is computed by both
-// (2.5F of MMA work in all where a split of D into halves would take 3F).
+// Two kinds of block: a dK block computes Sᵀ = K·Qᵀ, dPᵀ = V·dOᵀ and dK += dSᵀ·Q; a dV
+// block computes Sᵀ and dV += Pᵀ·dO.  Each accumulates its gradient over the full D in 256
+// TMEM columns; Sᵀ is computed by both (2.5F of MMA work in all where a split of D into
+// halves would take 3F).  Each runs as a cluster of two blocks that take the first and the
+// second half of the query blocks: the heaviest causal key tile (every query of every
+// head of the group) would otherwise set the kernel's time alone.  At the end the second
+// block writes its fp32 partial sum into the first block's shared memory, which adds it
+// to its own and stores the result.
 //   dK block: TMEM dK [0, 256), Sᵀ [256, 320), dPᵀ → dSᵀ in two buffers [320, 448).  Shared
 //     memory: K, V (64 KB each), two Q slots, one dO slot (32 KB each).  Warp 17 issues
 //     Sᵀ(n) once every element thread has read Sᵀ(n-1) (P stays in registers), warp 18
@@ -361,12 +386,16 @@ constexpr int kKvV = kOwnBytes;            // V (dK blocks) or two dO slots (dV 
 constexpr int kKvQ = 2 * kOwnBytes;        // two Q slots
 constexpr int kKvDo = kKvQ + 2 * kStrBytes;  // the dO slot of dK blocks
 constexpr int kKvBars = kKvDo + kStrBytes;   // 224 KB of tiles, then the barriers
+// The partner's fp32 partial sum [128 x 256] in the first block of a cluster, once no MMA
+// reads V, dO or Q any more: 16-byte pieces ordered (32-column chunk, piece, row).
+constexpr int kKvRed = kOwnBytes;
+static_assert(kKvRed + kOwn * kD * 4 <= kKvBars, "partial sum overlaps the barriers");
 constexpr int kKvBytes = kKvBars + (int)sizeof(Kv256Bars);
 static_assert(kKvBytes <= 227 * 1024, "dK/dV shared memory exceeds the per-block limit");
 constexpr int kKvThreads = 640;
 
 template <typename T>
-__global__ void __launch_bounds__(kKvThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
     tc_dkdv256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                       const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv, Problem p) {
@@ -386,11 +415,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   Kv256Bars& bars = *reinterpret_cast<Kv256Bars*>(sm + kKvBars);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // Block order: the dK and the dV block of one (batch, KV head, key tile) next to each
-  // other, all units of one key tile, then the next tile; under the causal mask the first
-  // key tiles see the most queries, so the heavy blocks go first.
-  const bool dv = (blockIdx.x & 1) != 0;
-  const int rest = blockIdx.x >> 1;
+  // Block order: the two blocks of a cluster, then the dK and the dV cluster of one (batch,
+  // KV head, key tile), all units of one key tile, then the next tile; under the causal mask
+  // the first key tiles see the most queries, so the heavy blocks go first.
+  const uint32_t rank = cluster_rank();
+  const bool dv = ((blockIdx.x >> 1) & 1) != 0;
+  const int rest = blockIdx.x >> 2;
   const int units = p.B * p.Hkv;
   const int unit = rest % units;
   const int b = unit / p.Hkv, g = unit % p.Hkv;
@@ -398,7 +428,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   // Queries before j0 - coff see none of these keys.
   const int i_begin = p.causal ? max(0, j0 - p.coff) : 0;
   const int nqb = i_begin < p.Lq ? (p.Lq - i_begin + kStr - 1) / kStr : 0;
-  const int total = p.G * nqb;
+  // This block's share of the G·nqb query blocks: [n_begin, n_begin + total).
+  const int n_half = (p.G * nqb + 1) / 2;
+  const int n_begin = rank == 0 ? 0 : n_half;
+  const int total = rank == 0 ? n_half : p.G * nqb - n_half;
+  // Loops below count n from 0 (barrier phases and slots follow it); query block n of this
+  // block is block n_begin + n of the key tile's list.
   // dO slot of query block n and the parity of its use: two slots in dV blocks, one in dK.
   auto do_slot = [&](int n) { return dv ? (n & 1) : 0; };
   auto do_par = [&](int n) { return static_cast<uint32_t>(dv ? (n >> 1) & 1 : n & 1); };
@@ -435,6 +470,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   const uint32_t tbase = bars.tmem_base;
   const WaitCtx wc{&bars.abort, 0, p.wait_limit_ns, p.err, kKidTcDkdv};
   constexpr unsigned kAll = 0xffffffffu;
+  bool el_ok = true;  // element threads: every wait of the loop and of acc_done succeeded
 
   if (warp == kProducer) {
     // K (and V in dK blocks) once; per query block n: Q(n) into slot n % 2 once its last
@@ -454,8 +490,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     bool ok = true;
     for (int n = 0; ok && n < total; ++n) {
       const int s = n % 2;
-      const int h = g * p.G + n / nqb;
-      const int i0 = i_begin + (n % nqb) * kStr;
+      const int h = g * p.G + (n_begin + n) / nqb;
+      const int i0 = i_begin + ((n_begin + n) % nqb) * kStr;
       if (!(ok = __all_sync(kAll, mbar_wait(&bars.q_empty[s], ((n / 2) & 1) ^ 1, wc)))) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(&bars.q_full[s], kStrBytes);
@@ -555,7 +591,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     bool ok = true;
     for (int n = 0; n < total; ++n) {
       const int s = n % 2;
-      const int i0 = i_begin + (n % nqb) * kStr + 16 * c;  // first query of this warp's columns
+      const int i0 = i_begin + ((n_begin + n) % nqb) * kStr + 16 * c;  // first query of this warp's columns
       ok = __all_sync(kAll, mbar_wait(&bars.s_full[dv ? s : 0], dv ? (n / 2) & 1 : n & 1, wc) &&
                                 mbar_wait(&bars.vec_full[s], (n / 2) & 1, wc));
       if (!ok) break;
@@ -620,15 +656,44 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         mbar_arrive(&bars.ds_ready[s]);
       }
     }
-    // Epilogue: the gradient (dK·scale or dV) in 8 chunks of 32 columns (warps of group c
-    // take chunks c and c + 4), staged in the K buffer (no MMA reads it once acc_done has
-    // completed) and written by bulk tensor stores once all 16 warps have staged theirs
-    // (keys past Lkv are clipped).  With no query block (total == 0) nothing else has
-    // waited for the K load, so wait for it here.
+    // With no query block (total == 0) nothing else has waited for the K load; the
+    // epilogue overwrites K, so wait for it here.
     if (ok)
       ok = __all_sync(kAll, mbar_wait(&bars.own_full, 0, wc) && (total == 0 || mbar_wait(&bars.acc_done, 0, wc)));
-    const int r = quarter * 32 + lane;
-    if (ok) {
+    el_ok = ok;
+  }
+  // Epilogue, every thread of both blocks.  After the first cluster barrier no MMA of
+  // either block runs any more (the element threads waited for acc_done; the issuers
+  // drained it), so the second block writes its partial sum into the first block's V/dO
+  // and Q space; after the second the first block adds it to its own, scales (dK by the
+  // softmax scale), packs the result in 8 chunks of 32 columns (warps of group c take
+  // chunks c and c + 4), stages it in its K buffer and writes it by bulk tensor stores
+  // once all 16 warps have staged theirs (keys past Lkv are clipped).
+  cluster_sync();
+  const bool elem = warp < 16;
+  const int c = warp / 4, quarter = warp % 4, r = quarter * 32 + lane;
+  if (elem && rank != 0 && el_ok) {
+    tc_fence_after();
+    const uint32_t red = map_to_rank(smem_u32(sm + kKvRed), 0);
+#pragma unroll 1
+    for (int c32 = c; c32 < kD / 32; c32 += 4) {
+      uint32_t acc[32];
+      if (total > 0) {
+        tmem_ld32(tmem_addr(tbase, quarter * 32, kColAcc + 32 * c32), acc);
+        tmem_ld_wait(acc);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) acc[e] = 0u;  // no query block in this half
+      }
+#pragma unroll
+      for (int e4 = 0; e4 < 8; ++e4)
+        st_cluster_v4(red + ((c32 * 8 + e4) * kOwn + r) * 16, acc[4 * e4], acc[4 * e4 + 1], acc[4 * e4 + 2],
+                      acc[4 * e4 + 3]);
+    }
+  }
+  cluster_sync();
+  if (elem && rank == 0) {
+    if (el_ok) {
       tc_fence_after();
       const float mul = dv ? 1.f : p.scale;
 #pragma unroll 1
@@ -643,8 +708,15 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         }
         uint32_t packed[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          packed[e] = pack2<T>(__uint_as_float(acc[2 * e]) * mul, __uint_as_float(acc[2 * e + 1]) * mul);
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const uint4 o = *reinterpret_cast<const uint4*>(sm + kKvRed + ((c32 * 8 + e4) * kOwn + r) * 16);
+          const float a0 = (__uint_as_float(acc[4 * e4]) + __uint_as_float(o.x)) * mul;
+          const float a1 = (__uint_as_float(acc[4 * e4 + 1]) + __uint_as_float(o.y)) * mul;
+          const float a2 = (__uint_as_float(acc[4 * e4 + 2]) + __uint_as_float(o.z)) * mul;
+          const float a3 = (__uint_as_float(acc[4 * e4 + 3]) + __uint_as_float(o.w)) * mul;
+          packed[2 * e4] = pack2<T>(a0, a1);
+          packed[2 * e4 + 1] = pack2<T>(a2, a3);
+        }
         uint8_t* blk = sm + kKvK + (c32 / 2) * kOwnCb;
 #pragma unroll
         for (int v4 = 0; v4 < 4; ++v4)
@@ -653,7 +725,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       }
       fence_async_smem();
     }
-    if (named_sync_and(1, 512, ok) && warp == 0 && lane == 0) {
+    if (named_sync_and(1, 512, el_ok) && warp == 0 && lane == 0) {
       for (int cb = 0; cb < 4; ++cb) tma_store_4d(dv ? &tdv : &tdk, sm + kKvK + cb * kOwnCb, cb * 64, j0, g, b);
       bulk_commit();
       bulk_wait_read();
@@ -699,7 +771,7 @@ cudaError_t dkdv256_t(const Problem& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kKvBytes);
   if (e != cudaSuccess) return e;
   const unsigned nkt = (p.Lkv + kOwn - 1) / kOwn;
-  kern<<<2 * nkt * p.Hkv * p.B, kKvThreads, kKvBytes, s>>>(tq, tk, tv, tdo, tdk, tdv, p);
+  kern<<<4 * nkt * p.Hkv * p.B, kKvThreads, kKvBytes, s>>>(tq, tk, tv, tdo, tdk, tdv, p);
   return cudaGetLastError();
 }
 
