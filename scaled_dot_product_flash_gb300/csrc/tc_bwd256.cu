@@ -87,6 +87,16 @@ __device__ __forceinline__ void mma_scores256(uint32_t c_tmem, uint32_t a_s, uin
   }
 }
 
+// The same product with A = the own tile held in TMEM (row r in lane r, elements (2i, 2i+1)
+// of D in column a_tmem + i): only B is read from shared memory, so the N = 64 product is
+// no longer bound by shared-memory bandwidth.
+__device__ __forceinline__ void mma_scores256_ts(uint32_t c_tmem, uint32_t a_tmem, uint32_t b_s, uint32_t idesc) {
+  const uint64_t bd = sdesc_sw128(b_s, 16, 1024);
+#pragma unroll
+  for (int kk = 0; kk < kD / 16; ++kk)
+    mma_ts_w(c_tmem, a_tmem + 8 * kk, sdesc_advance(bd, (kk / 4) * kStrCb + (kk % 4) * 32), idesc, kk > 0);
+}
+
 // Acc (+)= A·B: A the packed 16-bit [128 x 64] in TMEM (K-step kk, rows [16kk, 16kk + 16)
 // of the streamed block, is element warp group kk's first 8 columns, at a_tmem + 16kk) and
 // B the columns of a streamed [64 x 256] tile from b_s on (as many 64-column blocks as the
@@ -348,18 +358,20 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 // Two kinds of block: a dK block computes Sᵀ = K·Qᵀ, dPᵀ = V·dOᵀ and dK += dSᵀ·Q; a dV
 // block computes Sᵀ and dV += Pᵀ·dO.  Each accumulates its gradient over the full D in 256
 // TMEM columns; Sᵀ is computed by both (2.5F of MMA work in all where a split of D into
-// halves would take 3F).  Each runs as a cluster of two blocks that take the first and the
+// halves would take 3F).  Each block copies one owned tile into TMEM columns [384, 512)
+// (the dV block K, the dK block V) and runs that score product with A from TMEM.  Each runs as a cluster of two blocks that take the first and the
 // second half of the query blocks: the heaviest causal key tile (every query of every
 // head of the group) would otherwise set the kernel's time alone.  At the end the second
 // block writes its fp32 partial sum into the first block's shared memory, which adds it
 // to its own and stores the result.
-//   dK block: TMEM dK [0, 256), Sᵀ [256, 320), dPᵀ → dSᵀ in two buffers [320, 448).  Shared
-//     memory: K, V (64 KB each), two Q slots, one dO slot (32 KB each).  Warp 17 issues
-//     Sᵀ(n) once every element thread has read Sᵀ(n-1) (P stays in registers), warp 18
-//     dPᵀ(n) into buffer n % 2 once dK(n-2) has read it, warp 19 dK += dSᵀ(n)·Q(n).
-//   dV block: TMEM dV [0, 256), Sᵀ → Pᵀ in two buffers [256, 384).  Shared memory: K, two
-//     dO slots in the place of V, two Q slots.  Warp 17 issues Sᵀ(n) into buffer n % 2 once
-//     dV(n-2) has read it, warp 18 dV += Pᵀ(n)·dO(n); warp 19 has nothing to issue.
+//   dK block: TMEM dK [0, 256), Sᵀ [256, 320), dPᵀ → dSᵀ [320, 384), V [384, 512).  Shared
+//     memory: K, two dO slots in the place of V once V is in TMEM, two Q slots.  Warp 17
+//     issues Sᵀ(n) once every element thread has read Sᵀ(n-1) (P stays in registers),
+//     warp 18 dPᵀ(n) once dK(n-1) has read dSᵀ(n-1), warp 19 dK += dSᵀ(n)·Q(n).
+//   dV block: TMEM dV [0, 256), Sᵀ → Pᵀ in two buffers [256, 384), K [384, 512).  Shared
+//     memory: K (read once, into TMEM), two dO slots, two Q slots.  Warp 17 issues Sᵀ(n)
+//     into buffer n % 2 once dV(n-2) has read it, warp 18 dV += Pᵀ(n)·dO(n); warp 19 has
+//     nothing to issue.
 struct Kv256Bars {
   uint64_t own_full;
   uint64_t q_full[2];
@@ -372,9 +384,10 @@ struct Kv256Bars {
   uint64_t s_read;        // dK blocks: every element thread has read Sᵀ
   uint64_t p_ready[2];    // dV blocks: Pᵀ packed in buffer i
   uint64_t x_free[2];     // dV blocks: dV has read buffer i
-  uint64_t dp_full[2];    // dK blocks: dPᵀ in buffer i
-  uint64_t ds_ready[2];   // dK blocks: dSᵀ packed in buffer i
-  uint64_t y_free[2];     // dK blocks: dK has read buffer i
+  uint64_t dp_full;       // dK blocks: dPᵀ computed
+  uint64_t ds_ready;      // dK blocks: dSᵀ packed
+  uint64_t y_free;        // dK blocks: dK has read dSᵀ
+  uint64_t opnd_ready;    // the TMEM copy of the owned operand is complete (512 threads)
   uint64_t acc_done;
   uint32_t tmem_base;
   int abort;
@@ -382,10 +395,9 @@ struct Kv256Bars {
   alignas(16) float ndelta[2][kStr];  // −δ per query
 };
 constexpr int kKvK = 0;
-constexpr int kKvV = kOwnBytes;            // V (dK blocks) or two dO slots (dV blocks)
+constexpr int kKvV = kOwnBytes;            // V (dK blocks, until it is in TMEM), then two dO slots
 constexpr int kKvQ = 2 * kOwnBytes;        // two Q slots
-constexpr int kKvDo = kKvQ + 2 * kStrBytes;  // the dO slot of dK blocks
-constexpr int kKvBars = kKvDo + kStrBytes;   // 224 KB of tiles, then the barriers
+constexpr int kKvBars = kKvQ + 2 * kStrBytes;  // 192 KB of tiles, then the barriers
 // The partner's fp32 partial sum [128 x 256] in the first block of a cluster, once no MMA
 // reads V, dO or Q any more: 16-byte pieces ordered (32-column chunk, piece, row).
 constexpr int kKvRed = kOwnBytes;
@@ -402,7 +414,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
   constexpr bool kBf16 = IsBf16<T>::value;
   constexpr uint32_t kIdS = idesc_f16(kOwn, kStr, kBf16, false, false);  // M = 128, N = 64
   constexpr uint32_t kIdAcc = idesc_f16(kOwn, kD, kBf16, false, true);   // M = 128, N = 256, B MN-major
-  constexpr uint32_t kColAcc = 0, kColX = 256, kColY = 320;
+  constexpr uint32_t kColAcc = 0, kColX = 256, kColY = 320, kColOp = 384;
   extern __shared__ unsigned char smem_raw[];
   // The layout assumes a 1024-byte aligned base (TMA's 128-byte swizzle and the MMA
   // descriptors need it); should a launch place it elsewhere, the block reports an error
@@ -434,10 +446,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
   const int total = rank == 0 ? n_half : p.G * nqb - n_half;
   // Loops below count n from 0 (barrier phases and slots follow it); query block n of this
   // block is block n_begin + n of the key tile's list.
-  // dO slot of query block n and the parity of its use: two slots in dV blocks, one in dK.
-  auto do_slot = [&](int n) { return dv ? (n & 1) : 0; };
-  auto do_par = [&](int n) { return static_cast<uint32_t>(dv ? (n >> 1) & 1 : n & 1); };
-  auto do_off = [&](int n) { return dv ? kKvV + (n & 1) * kStrBytes : kKvDo; };
+  // dO slot of query block n, the parity of its use and its place.
+  auto do_slot = [&](int n) { return n & 1; };
+  auto do_par = [&](int n) { return static_cast<uint32_t>((n >> 1) & 1); };
+  auto do_off = [&](int n) { return kKvV + (n & 1) * kStrBytes; };
 
   if (threadIdx.x == 0) {
     bars.abort = 0;
@@ -452,10 +464,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
       mbar_init(&bars.s_full[s], 1);
       mbar_init(&bars.p_ready[s], 512);
       mbar_init(&bars.x_free[s], 1);
-      mbar_init(&bars.dp_full[s], 1);
-      mbar_init(&bars.ds_ready[s], 512);
-      mbar_init(&bars.y_free[s], 1);
     }
+    mbar_init(&bars.dp_full, 1);
+    mbar_init(&bars.ds_ready, 512);
+    mbar_init(&bars.y_free, 1);
+    mbar_init(&bars.opnd_ready, 512);
     mbar_init(&bars.s_read, 512);
     mbar_init(&bars.acc_done, 3);  // one commit per MMA issuer warp
     fence_mbar_init();
@@ -475,8 +488,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
   if (warp == kProducer) {
     // K (and V in dK blocks) once; per query block n: Q(n) into slot n % 2 once its last
     // reader of n-2 has finished, the per-query vectors beside it once the element threads
-    // are done with those of n-2, then dO(n) once the reader of its slot's previous block
-    // has finished.
+    // are done with those of n-2, then dO(n) into slot n % 2 once the reader of n-2 has
+    // finished (in dK blocks the first dO load waits for V to be copied out of its place).
     if (lane == 0) {
       prefetch_tmap(&tq);
       prefetch_tmap(&tdo);
@@ -511,7 +524,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
         bars.ndelta[s][e] = (!dv && i < p.Lq) ? -dlp[i] : 0.f;
       }
       mbar_arrive(&bars.vec_full[s]);
-      if (!(ok = __all_sync(kAll, mbar_wait(&bars.do_empty[do_slot(n)], do_par(n) ^ 1, wc)))) break;
+      if (!(ok = __all_sync(kAll, mbar_wait(&bars.do_empty[do_slot(n)], do_par(n) ^ 1, wc) &&
+                                      (dv || n > 0 || mbar_wait(&bars.opnd_ready, 0, wc)))))
+        break;
       if (lane == 0) {
         mbar_arrive_expect_tx(&bars.do_full[do_slot(n)], kStrBytes);
         for (int cb = 0; cb < 4; ++cb)
@@ -521,15 +536,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
     }
     if (lane == 0 && (!ok || bars.abort)) {  // let copies still in flight land before the block exits
       for (int n = max(0, q_issued - 2); n < q_issued; ++n) drain_wait(&bars.q_full[n % 2], (n / 2) & 1);
-      for (int n = max(0, do_issued - (dv ? 2 : 1)); n < do_issued; ++n)
+      for (int n = max(0, do_issued - 2); n < do_issued; ++n)
         drain_wait(&bars.do_full[do_slot(n)], do_par(n));
     }
   } else if (warp >= kIssuer) {
     const int role = __shfl_sync(kAll, warp - kIssuer, 0);
     bool ok = __all_sync(kAll, mbar_wait(&bars.own_full, 0, wc));
     tc_fence_after();
-    const uint32_t k_s = smem_u32(sm + kKvK), v_s = smem_u32(sm + kKvV);
+    const uint32_t k_s = smem_u32(sm + kKvK);
     auto q_s = [&](int n) { return smem_u32(sm + kKvQ + (n % 2) * kStrBytes); };
+    // The TS score product of the block (dV: Sᵀ; dK: dPᵀ) reads the TMEM copy of K or V.
+    if (role < 2 && (role == 0) == dv && ok) ok = __all_sync(kAll, mbar_wait(&bars.opnd_ready, 0, wc));
     if (role == 0) {
       // Sᵀ(n) = K·Q(n)ᵀ.
       for (int n = 0; ok && n < total; ++n) {
@@ -539,7 +556,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
         else if (n > 0) w = w && mbar_wait(&bars.s_read, (n - 1) & 1, wc);
         if (!(ok = __all_sync(kAll, w))) break;
         tc_fence_after();
-        mma_scores256(tbase + kColX + (dv ? 64 * s : 0), k_s, q_s(n), kIdS);
+        if (dv) mma_scores256_ts(tbase + kColX + 64 * s, tbase + kColOp, q_s(n), kIdS);
+        else mma_scores256(tbase + kColX, k_s, q_s(n), kIdS);
         mma_commit_w(&bars.s_full[dv ? s : 0]);
         if (dv) mma_commit_w(&bars.q_empty[s]);
       }
@@ -556,28 +574,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
         mma_commit_w(&bars.do_empty[do_slot(n)]);
       }
     } else if (role == 1) {
-      // dPᵀ(n) = V·dO(n)ᵀ into buffer n % 2.
+      // dPᵀ(n) = V·dO(n)ᵀ once dK(n-1) has read dSᵀ(n-1) from the same columns.
       for (int n = 0; ok && n < total; ++n) {
-        const int s = n % 2;
-        if (!(ok = __all_sync(kAll, mbar_wait(&bars.do_full[0], n & 1, wc) &&
-                                        mbar_wait(&bars.y_free[s], ((n / 2) & 1) ^ 1, wc))))
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.do_full[do_slot(n)], do_par(n), wc) &&
+                                        mbar_wait(&bars.y_free, (n & 1) ^ 1, wc))))
           break;
         tc_fence_after();
-        mma_scores256(tbase + kColY + 64 * s, v_s, smem_u32(sm + kKvDo), kIdS);
-        mma_commit_w(&bars.dp_full[s]);
-        mma_commit_w(&bars.do_empty[0]);
+        mma_scores256_ts(tbase + kColY, tbase + kColOp, smem_u32(sm + do_off(n)), kIdS);
+        mma_commit_w(&bars.dp_full);
+        mma_commit_w(&bars.do_empty[do_slot(n)]);
       }
     } else if (!dv) {
       // dK += dSᵀ(n)·Q(n).  Q(n) is loaded (Sᵀ(n) read it before dSᵀ(n) could exist);
       // waiting on its barrier too makes the TMA writes visible to this warp's MMA directly.
       for (int n = 0; ok && n < total; ++n) {
         const int s = n % 2;
-        if (!(ok = __all_sync(kAll, mbar_wait(&bars.ds_ready[s], (n / 2) & 1, wc) &&
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.ds_ready, n & 1, wc) &&
                                         mbar_wait(&bars.q_full[s], (n / 2) & 1, wc))))
           break;
         tc_fence_after();
-        mma_acc256(tbase + kColAcc, tbase + kColY + 64 * s, q_s(n), kIdAcc, n == 0);
-        mma_commit_w(&bars.y_free[s]);
+        mma_acc256(tbase + kColAcc, tbase + kColY, q_s(n), kIdAcc, n == 0);
+        mma_commit_w(&bars.y_free);
         mma_commit_w(&bars.q_empty[s]);
       }
     }
@@ -588,8 +605,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
     const int c = warp / 4, quarter = warp % 4;
     const int j = j0 + quarter * 32 + lane;  // this thread's key
     const uint64_t cc = f2pack(p.scale_log2, p.scale_log2);
-    bool ok = true;
-    for (int n = 0; n < total; ++n) {
+    // The owned tile the TS score product reads (dV blocks: K for Sᵀ; dK blocks: V for dPᵀ)
+    // into TMEM columns [384, 512): row r in lane r, elements (2i, 2i+1) of D in column
+    // 384 + i.  Warp e copies rows [32(e % 4), +32) of D columns [64c, 64c + 64); the 16-byte
+    // pieces of a swizzled row hold consecutive element pairs, so they go over as they are.
+    bool ok = __all_sync(kAll, mbar_wait(&bars.own_full, 0, wc));
+    if (ok) {
+      const uint8_t* src = sm + (dv ? kKvK : kKvV) + c * kOwnCb;
+      const int r = quarter * 32 + lane;
+      uint32_t w[32];
+#pragma unroll
+      for (int pc = 0; pc < 8; ++pc) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + sw128_off(r, pc));
+        w[4 * pc] = v.x;
+        w[4 * pc + 1] = v.y;
+        w[4 * pc + 2] = v.z;
+        w[4 * pc + 3] = v.w;
+      }
+      tmem_st32(tmem_addr(tbase, quarter * 32, kColOp + 32 * c), w);
+      tmem_st_wait();
+      tc_fence_before();
+    }
+    mbar_arrive(&bars.opnd_ready);
+    for (int n = 0; ok && n < total; ++n) {
       const int s = n % 2;
       const int i0 = i_begin + ((n_begin + n) % nqb) * kStr + 16 * c;  // first query of this warp's columns
       ok = __all_sync(kAll, mbar_wait(&bars.s_full[dv ? s : 0], dv ? (n / 2) & 1 : n & 1, wc) &&
@@ -635,10 +673,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
         mbar_arrive(&bars.p_ready[s]);
       } else {
         // dSᵀ = Pᵀ∘(dPᵀ − δ).
-        ok = __all_sync(kAll, mbar_wait(&bars.dp_full[s], (n / 2) & 1, wc));
+        ok = __all_sync(kAll, mbar_wait(&bars.dp_full, n & 1, wc));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t y_addr = tmem_addr(tbase, quarter * 32, kColY + 64 * s + 16 * c);
+        const uint32_t y_addr = tmem_addr(tbase, quarter * 32, kColY + 16 * c);
         uint32_t dr[16];
         tmem_ld16(y_addr, dr);
         tmem_ld_wait(dr);
@@ -653,7 +691,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
         tmem_st8(y_addr, pk);  // dSᵀ over the first 8 of this warp's 16 columns
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars.ds_ready[s]);
+        mbar_arrive(&bars.ds_ready);
       }
     }
     // With no query block (total == 0) nothing else has waited for the K load; the
