@@ -364,29 +364,34 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 // head of the group) would otherwise set the kernel's time alone.  At the end the second
 // block writes its fp32 partial sum into the first block's shared memory, which adds it
 // to its own and stores the result.
-//   dK block: TMEM dK [0, 256), Sᵀ [256, 320), dPᵀ → dSᵀ [320, 384), V [384, 512).  Shared
-//     memory: K, two dO slots in the place of V once V is in TMEM, two Q slots.  Warp 17
-//     issues Sᵀ(n) once every element thread has read Sᵀ(n-1) (P stays in registers),
-//     warp 18 dPᵀ(n) once dK(n-1) has read dSᵀ(n-1), warp 19 dK += dSᵀ(n)·Q(n).
-//   dV block: TMEM dV [0, 256), Sᵀ → Pᵀ in two buffers [256, 384), K [384, 512).  Shared
-//     memory: K (read once, into TMEM), two dO slots, two Q slots.  Warp 17 issues Sᵀ(n)
+//   dK block: TMEM dK [0, 256), two 64-column buffers [256, 384) that take Sᵀ(n), then
+//     dPᵀ(n) over it once every element thread has read Sᵀ(n) (Pᵀ stays in registers), then
+//     dSᵀ(n) over that; V [384, 512).  Shared memory: K, two dO slots in the place of V once
+//     V is in TMEM, three Q slots (Q(n) is read until dK(n), late in the iteration).  Warp
+//     17 issues Sᵀ(n) into buffer n % 2 once dK(n-2) has read it, warp 18 dPᵀ(n), warp 19
+//     dK += dSᵀ(n)·Q(n).
+//   dV block: TMEM dV [0, 256), Sᵀ → Pᵀ in the two buffers [256, 384), K [384, 512).  Shared
+//     memory: K (read once, into TMEM), two dO slots, three Q slots.  Warp 17 issues Sᵀ(n)
 //     into buffer n % 2 once dV(n-2) has read it, warp 18 dV += Pᵀ(n)·dO(n); warp 19 has
 //     nothing to issue.
+// Every ring is deep enough that a load is issued about two iterations before its data is
+// needed: a TMA load of a 32 KB tile takes 1500-2000 cycles to land under this kernel's
+// load, longer than one iteration.
 struct Kv256Bars {
   uint64_t own_full;
-  uint64_t q_full[2];
-  uint64_t q_empty[2];    // the last MMA reading Q slot i has finished
+  uint64_t q_full[3];
+  uint64_t q_empty[3];    // the last MMA reading Q slot i has finished
   uint64_t do_full[2];
   uint64_t do_empty[2];   // the MMA reading dO slot i has finished
   uint64_t vec_full[2];   // per-query vectors of slot i written (32 producer lanes)
   uint64_t vec_empty[2];  // every element thread is done with them
-  uint64_t s_full[2];     // Sᵀ in buffer i (dK blocks: buffer 0 only)
-  uint64_t s_read;        // dK blocks: every element thread has read Sᵀ
+  uint64_t s_full[2];     // Sᵀ in buffer i
+  uint64_t s_read[2];     // dK blocks: every element thread has read Sᵀ from buffer i
   uint64_t p_ready[2];    // dV blocks: Pᵀ packed in buffer i
   uint64_t x_free[2];     // dV blocks: dV has read buffer i
-  uint64_t dp_full;       // dK blocks: dPᵀ computed
-  uint64_t ds_ready;      // dK blocks: dSᵀ packed
-  uint64_t y_free;        // dK blocks: dK has read dSᵀ
+  uint64_t dp_full[2];    // dK blocks: dPᵀ in buffer i
+  uint64_t ds_ready[2];   // dK blocks: dSᵀ packed in buffer i
+  uint64_t y_free[2];     // dK blocks: dK has read buffer i
   uint64_t opnd_ready;    // the TMEM copy of the owned operand is complete (512 threads)
   uint64_t acc_done;
   uint32_t tmem_base;
@@ -396,8 +401,8 @@ struct Kv256Bars {
 };
 constexpr int kKvK = 0;
 constexpr int kKvV = kOwnBytes;            // V (dK blocks, until it is in TMEM), then two dO slots
-constexpr int kKvQ = 2 * kOwnBytes;        // two Q slots
-constexpr int kKvBars = kKvQ + 2 * kStrBytes;  // 192 KB of tiles, then the barriers
+constexpr int kKvQ = 2 * kOwnBytes;        // three Q slots
+constexpr int kKvBars = kKvQ + 3 * kStrBytes;  // 224 KB of tiles, then the barriers
 // The partner's fp32 partial sum [128 x 256] in the first block of a cluster, once no MMA
 // reads V, dO or Q any more: 16-byte pieces ordered (32-column chunk, piece, row).
 constexpr int kKvRed = kOwnBytes;
@@ -414,7 +419,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
   constexpr bool kBf16 = IsBf16<T>::value;
   constexpr uint32_t kIdS = idesc_f16(kOwn, kStr, kBf16, false, false);  // M = 128, N = 64
   constexpr uint32_t kIdAcc = idesc_f16(kOwn, kD, kBf16, false, true);   // M = 128, N = 256, B MN-major
-  constexpr uint32_t kColAcc = 0, kColX = 256, kColY = 320, kColOp = 384;
+  constexpr uint32_t kColAcc = 0, kColX = 256, kColOp = 384;
   extern __shared__ unsigned char smem_raw[];
   // The layout assumes a 1024-byte aligned base (TMA's 128-byte swizzle and the MMA
   // descriptors need it); should a launch place it elsewhere, the block reports an error
@@ -454,22 +459,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
   if (threadIdx.x == 0) {
     bars.abort = 0;
     mbar_init(&bars.own_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < 3; ++s) {
       mbar_init(&bars.q_full[s], 1);
       mbar_init(&bars.q_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&bars.do_full[s], 1);
       mbar_init(&bars.do_empty[s], 1);
       mbar_init(&bars.vec_full[s], 32);  // every lane of the producer warp
-      mbar_init(&bars.vec_empty[s], 512);
+      mbar_init(&bars.vec_empty[s], 256);  // the element group of buffer s (8 warps)
       mbar_init(&bars.s_full[s], 1);
-      mbar_init(&bars.p_ready[s], 512);
+      mbar_init(&bars.p_ready[s], 256);
       mbar_init(&bars.x_free[s], 1);
+      mbar_init(&bars.s_read[s], 256);
+      mbar_init(&bars.dp_full[s], 1);
+      mbar_init(&bars.ds_ready[s], 256);
+      mbar_init(&bars.y_free[s], 1);
     }
-    mbar_init(&bars.dp_full, 1);
-    mbar_init(&bars.ds_ready, 512);
-    mbar_init(&bars.y_free, 1);
     mbar_init(&bars.opnd_ready, 512);
-    mbar_init(&bars.s_read, 512);
     mbar_init(&bars.acc_done, 3);  // one commit per MMA issuer warp
     fence_mbar_init();
   }
@@ -483,13 +490,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
   const uint32_t tbase = bars.tmem_base;
   const WaitCtx wc{&bars.abort, 0, p.wait_limit_ns, p.err, kKidTcDkdv};
   constexpr unsigned kAll = 0xffffffffu;
+  if (warp >= 16) regs_dec<kRegsLow>();
   bool el_ok = true;  // element threads: every wait of the loop and of acc_done succeeded
 
   if (warp == kProducer) {
-    // K (and V in dK blocks) once; per query block n: Q(n) into slot n % 2 once its last
-    // reader of n-2 has finished, the per-query vectors beside it once the element threads
-    // are done with those of n-2, then dO(n) into slot n % 2 once the reader of n-2 has
-    // finished (in dK blocks the first dO load waits for V to be copied out of its place).
+    // K (and V in dK blocks) once; per query block n: Q(n) into slot n % 3 once its last
+    // reader of n-3 has finished, dO(n) into slot n % 2 once the reader of n-2 has finished
+    // (in dK blocks the first dO load waits for V to be copied out of its place), then the
+    // per-query vectors into slot n % 2 once the element threads are done with those of n-2.
     if (lane == 0) {
       prefetch_tmap(&tq);
       prefetch_tmap(&tdo);
@@ -499,31 +507,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
         if (!dv) tma_load_4d(sm + kKvV + cb * kOwnCb, &tv, &bars.own_full, cb * 64, j0, g, b);
       }
     }
+    // The per-query lse and δ of query block n (lane e holds queries e and e + 32) are read
+    // from global memory one block ahead, so their latency overlaps the loop's waits
+    // instead of holding back the next TMA loads.
+    float lv[2], dl[2];
+    auto fetch = [&](int n) {
+      const int h = g * p.G + (n_begin + n) / nqb;
+      const int i0 = i_begin + ((n_begin + n) % nqb) * kStr;
+      const float* lsep = p.lse + q_row(p, b, h, 0);
+      const float* dlp = p.delta + q_row(p, b, h, 0);
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int i = i0 + lane + 32 * t;
+        lv[t] = i < p.Lq ? lsep[i] : -pos_inf();  // −inf: the row sees no key, P = 0
+        dl[t] = (!dv && i < p.Lq) ? dlp[i] : 0.f;
+      }
+    };
+    if (total > 0) fetch(0);
     int q_issued = 0, do_issued = 0;
     bool ok = true;
     for (int n = 0; ok && n < total; ++n) {
       const int s = n % 2;
       const int h = g * p.G + (n_begin + n) / nqb;
       const int i0 = i_begin + ((n_begin + n) % nqb) * kStr;
-      if (!(ok = __all_sync(kAll, mbar_wait(&bars.q_empty[s], ((n / 2) & 1) ^ 1, wc)))) break;
+      const int qs = n % 3;
+      if (!(ok = __all_sync(kAll, mbar_wait(&bars.q_empty[qs], ((n / 3) & 1) ^ 1, wc)))) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars.q_full[s], kStrBytes);
+        mbar_arrive_expect_tx(&bars.q_full[qs], kStrBytes);
         for (int cb = 0; cb < 4; ++cb)
-          tma_load_4d(sm + kKvQ + s * kStrBytes + cb * kStrCb, &tq, &bars.q_full[s], cb * 64, i0, h, b);
+          tma_load_4d(sm + kKvQ + qs * kStrBytes + cb * kStrCb, &tq, &bars.q_full[qs], cb * 64, i0, h, b);
       }
       q_issued = n + 1;
-      // Per-query vectors, negated for the packed math of the element warps.
-      if (!(ok = __all_sync(kAll, mbar_wait(&bars.vec_empty[s], ((n / 2) & 1) ^ 1, wc)))) break;
-      const float* lsep = p.lse + q_row(p, b, h, 0);
-      const float* dlp = p.delta + q_row(p, b, h, 0);
-#pragma unroll
-      for (int e = lane; e < kStr; e += 32) {
-        const int i = i0 + e;
-        const float l = i < p.Lq ? lsep[i] : -pos_inf();  // −inf: the row sees no key, P = 0
-        bars.nlse2[s][e] = l == -pos_inf() ? -pos_inf() : -l * kLog2e;
-        bars.ndelta[s][e] = (!dv && i < p.Lq) ? -dlp[i] : 0.f;
-      }
-      mbar_arrive(&bars.vec_full[s]);
       if (!(ok = __all_sync(kAll, mbar_wait(&bars.do_empty[do_slot(n)], do_par(n) ^ 1, wc) &&
                                       (dv || n > 0 || mbar_wait(&bars.opnd_ready, 0, wc)))))
         break;
@@ -533,9 +547,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
           tma_load_4d(sm + do_off(n) + cb * kStrCb, &tdo, &bars.do_full[do_slot(n)], cb * 64, i0, h, b);
       }
       do_issued = n + 1;
+      // Per-query vectors, negated for the packed math of the element warps.
+      if (!(ok = __all_sync(kAll, mbar_wait(&bars.vec_empty[s], ((n / 2) & 1) ^ 1, wc)))) break;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        bars.nlse2[s][lane + 32 * t] = lv[t] == -pos_inf() ? -pos_inf() : -lv[t] * kLog2e;
+        bars.ndelta[s][lane + 32 * t] = -dl[t];
+      }
+      mbar_arrive(&bars.vec_full[s]);
+      if (n + 1 < total) fetch(n + 1);
     }
     if (lane == 0 && (!ok || bars.abort)) {  // let copies still in flight land before the block exits
-      for (int n = max(0, q_issued - 2); n < q_issued; ++n) drain_wait(&bars.q_full[n % 2], (n / 2) & 1);
+      for (int n = max(0, q_issued - 3); n < q_issued; ++n) drain_wait(&bars.q_full[n % 3], (n / 3) & 1);
       for (int n = max(0, do_issued - 2); n < do_issued; ++n)
         drain_wait(&bars.do_full[do_slot(n)], do_par(n));
     }
@@ -544,22 +567,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
     bool ok = __all_sync(kAll, mbar_wait(&bars.own_full, 0, wc));
     tc_fence_after();
     const uint32_t k_s = smem_u32(sm + kKvK);
-    auto q_s = [&](int n) { return smem_u32(sm + kKvQ + (n % 2) * kStrBytes); };
+    auto q_s = [&](int n) { return smem_u32(sm + kKvQ + (n % 3) * kStrBytes); };
     // The TS score product of the block (dV: Sᵀ; dK: dPᵀ) reads the TMEM copy of K or V.
     if (role < 2 && (role == 0) == dv && ok) ok = __all_sync(kAll, mbar_wait(&bars.opnd_ready, 0, wc));
     if (role == 0) {
-      // Sᵀ(n) = K·Q(n)ᵀ.
+      // Sᵀ(n) = K·Q(n)ᵀ into buffer n % 2 once dV(n-2) or dK(n-2) has read it.
       for (int n = 0; ok && n < total; ++n) {
         const int s = n % 2;
-        bool w = mbar_wait(&bars.q_full[s], (n / 2) & 1, wc);
-        if (dv) w = w && mbar_wait(&bars.x_free[s], ((n / 2) & 1) ^ 1, wc);
-        else if (n > 0) w = w && mbar_wait(&bars.s_read, (n - 1) & 1, wc);
-        if (!(ok = __all_sync(kAll, w))) break;
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.q_full[n % 3], (n / 3) & 1, wc) &&
+                                        mbar_wait(dv ? &bars.x_free[s] : &bars.y_free[s], ((n / 2) & 1) ^ 1, wc))))
+          break;
         tc_fence_after();
         if (dv) mma_scores256_ts(tbase + kColX + 64 * s, tbase + kColOp, q_s(n), kIdS);
-        else mma_scores256(tbase + kColX, k_s, q_s(n), kIdS);
-        mma_commit_w(&bars.s_full[dv ? s : 0]);
-        if (dv) mma_commit_w(&bars.q_empty[s]);
+        else mma_scores256(tbase + kColX + 64 * s, k_s, q_s(n), kIdS);
+        mma_commit_w(&bars.s_full[s]);
+        if (dv) mma_commit_w(&bars.q_empty[n % 3]);
       }
     } else if (role == 1 && dv) {
       // dV += Pᵀ(n)·dO(n).
@@ -574,14 +596,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
         mma_commit_w(&bars.do_empty[do_slot(n)]);
       }
     } else if (role == 1) {
-      // dPᵀ(n) = V·dO(n)ᵀ once dK(n-1) has read dSᵀ(n-1) from the same columns.
+      // dPᵀ(n) = V·dO(n)ᵀ over Sᵀ(n) in buffer n % 2 once every element thread has read it.
       for (int n = 0; ok && n < total; ++n) {
+        const int s = n % 2;
         if (!(ok = __all_sync(kAll, mbar_wait(&bars.do_full[do_slot(n)], do_par(n), wc) &&
-                                        mbar_wait(&bars.y_free, (n & 1) ^ 1, wc))))
+                                        mbar_wait(&bars.s_read[s], (n / 2) & 1, wc))))
           break;
         tc_fence_after();
-        mma_scores256_ts(tbase + kColY, tbase + kColOp, smem_u32(sm + do_off(n)), kIdS);
-        mma_commit_w(&bars.dp_full);
+        mma_scores256_ts(tbase + kColX + 64 * s, tbase + kColOp, smem_u32(sm + do_off(n)), kIdS);
+        mma_commit_w(&bars.dp_full[s]);
         mma_commit_w(&bars.do_empty[do_slot(n)]);
       }
     } else if (!dv) {
@@ -589,19 +612,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
       // waiting on its barrier too makes the TMA writes visible to this warp's MMA directly.
       for (int n = 0; ok && n < total; ++n) {
         const int s = n % 2;
-        if (!(ok = __all_sync(kAll, mbar_wait(&bars.ds_ready, n & 1, wc) &&
-                                        mbar_wait(&bars.q_full[s], (n / 2) & 1, wc))))
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.ds_ready[s], (n / 2) & 1, wc) &&
+                                        mbar_wait(&bars.q_full[n % 3], (n / 3) & 1, wc))))
           break;
         tc_fence_after();
-        mma_acc256(tbase + kColAcc, tbase + kColY, q_s(n), kIdAcc, n == 0);
-        mma_commit_w(&bars.y_free);
-        mma_commit_w(&bars.q_empty[s]);
+        mma_acc256(tbase + kColAcc, tbase + kColX + 64 * s, q_s(n), kIdAcc, n == 0);
+        mma_commit_w(&bars.y_free[s]);
+        mma_commit_w(&bars.q_empty[n % 3]);
       }
     }
     mma_commit_w(&bars.acc_done);
     drain_wait(&bars.acc_done, 0);
   } else {
-    // Warp e: TMEM lane quarter e % 4 (keys), query columns [16c, 16c + 16) with c = e / 4.
+    regs_inc<kRegsHigh>();
     const int c = warp / 4, quarter = warp % 4;
     const int j = j0 + quarter * 32 + lane;  // this thread's key
     const uint64_t cc = f2pack(p.scale_log2, p.scale_log2);
@@ -627,71 +650,90 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
       tc_fence_before();
     }
     mbar_arrive(&bars.opnd_ready);
-    for (int n = 0; ok && n < total; ++n) {
+    // The element warps form two groups of 8 that take turns: group gq = e / 8 takes the
+    // query blocks n with n % 2 == gq (TMEM buffer n % 2), so one group's TMEM round trips,
+    // exponentials and barrier hand-offs overlap the other's block.  Warp e of a group has
+    // lane quarter e % 4 (keys) and query columns [32h, 32h + 32), h = (e / 4) % 2; it packs
+    // the 16-bit results of queries [32h, 32h + 16) over columns [32h, 32h + 8) and those of
+    // [32h + 16, 32h + 32) over [32h + 16, 32h + 24), where the K-steps 2h and 2h + 1 of the
+    // dV / dK products read them.
+    const int gq = warp / 8, h2 = (warp / 4) % 2;
+    for (int n = gq; ok && n < total; n += 2) {
       const int s = n % 2;
-      const int i0 = i_begin + ((n_begin + n) % nqb) * kStr + 16 * c;  // first query of this warp's columns
-      ok = __all_sync(kAll, mbar_wait(&bars.s_full[dv ? s : 0], dv ? (n / 2) & 1 : n & 1, wc) &&
+      const int i0 = i_begin + ((n_begin + n) % nqb) * kStr + 32 * h2;  // first query of this warp's columns
+      ok = __all_sync(kAll, mbar_wait(&bars.s_full[s], (n / 2) & 1, wc) &&
                                 mbar_wait(&bars.vec_full[s], (n / 2) & 1, wc));
       if (!ok) break;
       tc_fence_after();
       const int ic = i0 + p.coff;  // key j is hidden from query i0 + q when j > ic + q
       const bool diag = p.causal && j0 + kOwn - 1 > ic;
-      const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(&bars.nlse2[s][16 * c]);
-      const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(&bars.ndelta[s][16 * c]);
-      const uint32_t x_addr = tmem_addr(tbase, quarter * 32, kColX + (dv ? 64 * s : 0) + 16 * c);
-      uint32_t sr[16];
-      tmem_ld16(x_addr, sr);
-      tmem_ld_wait(sr);
-      if (!dv) {
-        tc_fence_before();
-        mbar_arrive(&bars.s_read);
-      }
-      // Pᵀ of this warp's 16 queries, in fp32 pairs.
-      uint64_t pf[8];
+      const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(&bars.nlse2[s][32 * h2]);
+      const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(&bars.ndelta[s][32 * h2]);
+      const uint32_t x_addr = tmem_addr(tbase, quarter * 32, kColX + 64 * s + 32 * h2);
+      // Pᵀ of this warp's 32 queries, in fp32 pairs.
+      uint64_t pf[16];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        float p0, p1;
-        ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl2[e]), p0, p1);
-        if (diag) {
-          if (j > ic + 2 * e) p0 = 0.f;
-          if (j > ic + 2 * e + 1) p1 = 0.f;
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t sr[16];
+        tmem_ld16(x_addr + 16 * hf, sr);
+        tmem_ld_wait(sr);
+        if (!dv && hf == 1) {  // dPᵀ(n) may now overwrite Sᵀ(n)
+          tc_fence_before();
+          mbar_arrive(&bars.s_read[s]);
         }
-        pf[e] = f2pack(p0, p1);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int x = 8 * hf + e;
+          float p0, p1;
+          ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl2[x]), p0, p1);
+          if (diag) {
+            if (j > ic + 2 * x) p0 = 0.f;
+            if (j > ic + 2 * x + 1) p1 = 0.f;
+          }
+          pf[x] = f2pack(p0, p1);
+        }
       }
       uint32_t pk[8];
       if (dv) {
         mbar_arrive(&bars.vec_empty[s]);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float p0, p1;
-          f2unpack(pf[e], p0, p1);
-          pk[e] = pack2<T>(p0, p1);
+        for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float p0, p1;
+            f2unpack(pf[8 * hf + e], p0, p1);
+            pk[e] = pack2<T>(p0, p1);
+          }
+          tmem_st8(x_addr + 16 * hf, pk);  // Pᵀ over the first 8 of each 16 columns
         }
-        tmem_st8(x_addr, pk);  // Pᵀ over the first 8 of this warp's 16 columns
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars.p_ready[s]);
       } else {
         // dSᵀ = Pᵀ∘(dPᵀ − δ).
-        ok = __all_sync(kAll, mbar_wait(&bars.dp_full, n & 1, wc));
+        ok = __all_sync(kAll, mbar_wait(&bars.dp_full[s], (n / 2) & 1, wc));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t y_addr = tmem_addr(tbase, quarter * 32, kColY + 16 * c);
-        uint32_t dr[16];
-        tmem_ld16(y_addr, dr);
-        tmem_ld_wait(dr);
+        // In two halves of 16 columns (the half-0 store does not touch half 1's columns).
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float d0, d1;
-          f2unpack(fmul2(pf[e], fadd2(f2pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), nd2[e])), d0,
-                   d1);
-          pk[e] = pack2<T>(d0, d1);
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t dr[16];
+          tmem_ld16(x_addr + 16 * hf, dr);
+          tmem_ld_wait(dr);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int x = 8 * hf + e;
+            float d0, d1;
+            f2unpack(fmul2(pf[x], fadd2(f2pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), nd2[x])),
+                     d0, d1);
+            pk[e] = pack2<T>(d0, d1);
+          }
+          tmem_st8(x_addr + 16 * hf, pk);  // dSᵀ over the first 8 of each 16 columns
         }
         mbar_arrive(&bars.vec_empty[s]);
-        tmem_st8(y_addr, pk);  // dSᵀ over the first 8 of this warp's 16 columns
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars.ds_ready);
+        mbar_arrive(&bars.ds_ready[s]);
       }
     }
     // With no query block (total == 0) nothing else has waited for the K load; the
