@@ -623,7 +623,8 @@ def run_masked(torch, api, dev, stream, bf16_peak):
     return res
 
 
-# Per-(config, pass) lines: the five target workloads (the short-query one at each Lq).
+# Per-(config, pass) lines: the five target workloads (the short-query one at each Lq) and a
+# head-dim-256 case.
 # Seeds and the draw order follow the input recipe: one generator per workload; the
 # short-query sub-runs draw one after another from default_rng(4).
 CONFIGS = [
@@ -634,10 +635,13 @@ CONFIGS = [
     ("C4 bf16 GQA L=4096 D=128 causal", dict(WORKLOAD), "bf16", True, 3),
     ("C5a bf16 L=16384 D=128 causal", dict(B=1, Hq=16, Hkv=16, Lq=16384, Lkv=16384, D=128), "bf16",
      True, 4),
+    # head dim 256 (the widest head the library serves; tensor-core forward and backward)
+    ("D256 bf16 GQA L=4096 causal", dict(B=1, Hq=16, Hkv=4, Lq=4096, Lkv=4096, D=256), "bf16", True, 5),
 ]
 # Oracle sample of the large workloads: whole (batch, KV head) groups.
 ORACLE_GROUPS = {"C4 bf16 GQA L=4096 D=128 causal": [(1, 7)],
-                 "C5a bf16 L=16384 D=128 causal": [(0, 11)]}
+                 "C5a bf16 L=16384 D=128 causal": [(0, 11)],
+                 "D256 bf16 GQA L=4096 causal": [(0, 3)]}
 
 
 def _median_ms(torch, stream, fn, flush, n):

@@ -50,8 +50,7 @@
  *    SDPA_ERR_CUDA.  Kernels never trap: a wait that runs out of its iteration limit sets
  *    the device error word and the kernel returns; sdpa_poll_status reports it.
  *  - Supported: dtype in {SDPA_F32, SDPA_F16, SDPA_BF16}; D in {32, 64, 96, 128, 256}
- *    (at D = 256 the fp16/bf16 forward and the unmasked fp16/bf16 backward run on tensor
- *    cores, the masked backward and every fp32 call on the CUDA-core tiled kernels);
+ *    (fp16/bf16 run on tensor cores at every D, fp32 on the CUDA-core tiled kernels);
  *    B, Hq, Hkv, Lq, Lkv >= 1; Hq % Hkv == 0; Hq, B <= 65535; scale finite (0 allowed).
  */
 #ifndef SDPA_GB300_H
@@ -278,16 +277,14 @@ const char* sdpa_status_string(int status);
 /*
  * Kernel family selection, for tests and measurements.  SDPA_PATH_AUTO (the default)
  * picks by shape and dtype: the vector path when Lq <= 8, (Hq/Hkv)·Lq <= 32 and D <= 128, else the
- * tensor-core tiled path for fp16/bf16 with D in {32, 64, 96, 128, 256} (a backward at
- * D = 256 with an attention mask then runs on the CUDA-core kernels), else the CUDA-core
+ * tensor-core tiled path for fp16/bf16 with D in {32, 64, 96, 128, 256}, else the CUDA-core
  * tiled path (every dtype, D up to 256).
  * A forced path that cannot serve a call makes that call return SDPA_ERR_UNSUPPORTED.
  * Process-wide setting; not thread-safe against concurrent calls.
  */
 typedef enum {
   SDPA_PATH_AUTO = 0,
-  SDPA_PATH_TENSOR = 1,  /* TMA + tcgen05 tiled kernels (fp16/bf16, D in {32,64,96,128};
-                            also D = 256, except a backward with a mask) */
+  SDPA_PATH_TENSOR = 1,  /* TMA + tcgen05 tiled kernels (fp16/bf16, D in {32,64,96,128,256}) */
   SDPA_PATH_SIMT = 2,    /* CUDA-core (FFMA) tiled kernels, every dtype and D */
   SDPA_PATH_VECTOR = 3   /* short-query kernels (Lq <= 8, (Hq/Hkv)·Lq <= 32, D <= 128) */
 } sdpa_path_t;

@@ -27,7 +27,7 @@ cudaError_t launch_vector_mma_fwd(const Problem& p, int dtype, cudaStream_t s);
 cudaError_t launch_vector_mma_bwd(const Problem& p, int dtype, cudaStream_t s);
 
 // Tensor-core path (TMA + tcgen05), fp16/bf16: forward with D in {32, 64, 96, 128, 256},
-// backward with D in {32, 64, 96, 128}, and at D = 256 without an attention mask.
+// backward with D in {32, 64, 96, 128} (tc_bwd.cu) and 256 (tc_bwd256.cu).
 bool tensor_supported(const Problem& p, int dtype);
 bool tensor_bwd_supported(const Problem& p, int dtype);
 bool tensor_bwd256_supported(const Problem& p, int dtype);

@@ -1,4 +1,4 @@
-// Tensor-core backward at head dim 256 (fp16/bf16, no attention mask): a dQ kernel and a
+// Tensor-core backward at head dim 256 (fp16/bf16): a dQ kernel and a
 // dK/dV kernel on TMA + tcgen05 + TMEM, recomputing P from the forward's logsumexp as the
 // D <= 128 kernels do ("[Metal] Add Flash Attention VJP for training", sections
 // "Implementation Notes" and "Limitations").  At D = 256 one SM's budgets (512 TMEM
@@ -17,6 +17,13 @@
 // packed 16-bit results over the first 8 of them), warp 16 the TMA producer, warps 17-19
 // the MMA issuers; warp 17 owns the TMEM.  Every wait is bounded, as everywhere in the
 // library.
+// Attention masks: each kernel has a masked instantiation (kMasked) that adds log2e·M to
+// the log2-domain scores before the exponential, as the D <= 128 kernels do.  Neither has
+// shared memory left for a mask tile: the dQ kernel reads its row's 16 mask values from
+// global memory in 16-byte pieces before its barrier waits, the dK/dV kernel reads its
+// key's column for 16 queries at a time (one byte or element per query, coalesced across
+// the warp's 32 keys) while its TMEM load is in flight.  Keys past Lkv and rows past Lq
+// are not read.
 #include "launch.h"
 #include "tc_common.cuh"
 
@@ -132,7 +139,7 @@ struct Dq256Bars {
   int abort;
 };
 
-template <typename T>
+template <typename T, bool kMasked>
 __global__ void __launch_bounds__(kDqThreads, 1)
     tc_dq256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -269,11 +276,17 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const float lse = valid ? p.lse[row] : -pos_inf();
     const float lse2 = lse == -pos_inf() ? pos_inf() : lse * kLog2e;  // no visible key: P = 0
     const float dl = valid ? p.delta[row] : 0.f;
+    const int64_t moff = kMasked && valid ? row_off(p.lm, b, h, i) : 0;
     const uint64_t cc = f2pack(p.scale_log2, p.scale_log2);
     const uint64_t nl = f2pack(-lse2, -lse2), nd = f2pack(-dl, -dl);
     bool ok = true;
     for (int n = 0; n < total; ++n) {
       const int k0 = n * kStr + 16 * c;  // first key of this warp's columns
+      // Mask terms of this warp's keys as 16-bit pairs (0 past the row's mask pieces: those
+      // keys are past Lkv and hidden by lim), read before the waits so that they hide the
+      // loads' latency.
+      uint32_t mk[kMasked ? 8 : 1];
+      if constexpr (kMasked) mask_pairs<T, 16>(mk, p, moff + k0, valid && k0 < p.Lkv ? p.Lkv - k0 : 0);
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[n % 2], (n / 2) & 1, wc) &&
                                        mbar_wait(&bars.dp_full, n & 1, wc));
       if (!ok) break;
@@ -294,7 +307,14 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         float p0, p1;
-        ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl), p0, p1);
+        uint64_t xx = ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl);
+        if constexpr (kMasked) {
+          float x0, x1, m0, m1;
+          f2unpack(xx, x0, x1);
+          unpack2<T>(mk[e], m0, m1);
+          xx = f2pack(x0 + m0 * kLog2e, x1 + m1 * kLog2e);
+        }
+        ex2_pair(xx, p0, p1);
         if (need_mask) {
           if (2 * e >= lim) p0 = 0.f;
           if (2 * e + 1 >= lim) p1 = 0.f;
@@ -411,7 +431,7 @@ constexpr int kKvBytes = kKvBars + (int)sizeof(Kv256Bars);
 static_assert(kKvBytes <= 227 * 1024, "dK/dV shared memory exceeds the per-block limit");
 constexpr int kKvThreads = 640;
 
-template <typename T>
+template <typename T, bool kMasked>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
     tc_dkdv256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -670,12 +690,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
       const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(&bars.nlse2[s][32 * h2]);
       const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(&bars.ndelta[s][32 * h2]);
       const uint32_t x_addr = tmem_addr(tbase, quarter * 32, kColX + 64 * s + 32 * h2);
+      // Mask element (this block's head, query 0, key j); keys past Lkv are not read.
+      const int64_t mcol = kMasked ? row_off(p.lm, b, g * p.G + (n_begin + n) / nqb, 0) + j : 0;
       // Pᵀ of this warp's 32 queries, in fp32 pairs.
       uint64_t pf[16];
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         uint32_t sr[16];
         tmem_ld16(x_addr + 16 * hf, sr);
+        float mv[kMasked ? 16 : 1];  // log2e·M of query i0 + 16hf + e
+        if constexpr (kMasked) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int q = i0 + 16 * hf + e;
+            mv[e] = (j < p.Lkv && q < p.Lq) ? mask_log2<T>(p, mcol + (int64_t)q * p.lm.sl) : 0.f;
+          }
+        }
         tmem_ld_wait(sr);
         if (!dv && hf == 1) {  // dPᵀ(n) may now overwrite Sᵀ(n)
           tc_fence_before();
@@ -685,7 +715,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
         for (int e = 0; e < 8; ++e) {
           const int x = 8 * hf + e;
           float p0, p1;
-          ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl2[x]), p0, p1);
+          if constexpr (kMasked) {  // c·s is finite, so a hidden key's −inf passes through the fma
+            ex2_pair(fadd2(f2pack(fmaf(p.scale_log2, __uint_as_float(sr[2 * e]), mv[2 * e]),
+                                  fmaf(p.scale_log2, __uint_as_float(sr[2 * e + 1]), mv[2 * e + 1])),
+                           nl2[x]),
+                     p0, p1);
+          } else {
+            ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl2[x]), p0, p1);
+          }
           if (diag) {
             if (j > ic + 2 * x) p0 = 0.f;
             if (j > ic + 2 * x + 1) p1 = 0.f;
@@ -819,7 +856,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
   }
 }
 
-template <typename T>
+template <typename T, bool kMasked>
 cudaError_t dq256_t(const Problem& p, cudaStream_t s) {
   CUtensorMap tq, tk, tv, tdo, tdq;
   if (!make_tmap_4d(&tq, p.q, kD, p.Lq, p.Hq, p.B, p.lq, kOwn) ||
@@ -829,7 +866,7 @@ cudaError_t dq256_t(const Problem& p, cudaStream_t s) {
       !make_tmap_4d(&tv, p.v, kD, p.Lkv, p.Hkv, p.B, p.lv, kStr))
     return cudaErrorInvalidValue;
   const int smem = kDqBytes + 1024;
-  auto kern = tc_dq256_kernel<T>;
+  auto kern = tc_dq256_kernel<T, kMasked>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned nqt = (p.Lq + kOwn - 1) / kOwn;
@@ -837,7 +874,7 @@ cudaError_t dq256_t(const Problem& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <typename T>
+template <typename T, bool kMasked>
 cudaError_t dkdv256_t(const Problem& p, cudaStream_t s) {
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   if (!make_tmap_4d(&tk, p.k, kD, p.Lkv, p.Hkv, p.B, p.lk, kOwn) ||
@@ -847,7 +884,7 @@ cudaError_t dkdv256_t(const Problem& p, cudaStream_t s) {
       !make_tmap_4d(&tq, p.q, kD, p.Lq, p.Hq, p.B, p.lq, kStr) ||
       !make_tmap_4d(&tdo, p.dout, kD, p.Lq, p.Hq, p.B, p.ldo, kStr))
     return cudaErrorInvalidValue;
-  auto kern = tc_dkdv256_kernel<T>;
+  auto kern = tc_dkdv256_kernel<T, kMasked>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kKvBytes);
   if (e != cudaSuccess) return e;
   const unsigned nkt = (p.Lkv + kOwn - 1) / kOwn;
@@ -857,16 +894,16 @@ cudaError_t dkdv256_t(const Problem& p, cudaStream_t s) {
 
 }  // namespace
 
-bool tensor_bwd256_supported(const Problem& p, int dtype) {
-  return tensor_supported(p, dtype) && p.D == kD && p.mask == nullptr;
-}
+bool tensor_bwd256_supported(const Problem& p, int dtype) { return tensor_supported(p, dtype) && p.D == kD; }
 
 cudaError_t launch_tc_dq256(const Problem& p, int dtype, cudaStream_t s) {
-  return dtype == 2 ? dq256_t<__nv_bfloat16>(p, s) : dq256_t<__half>(p, s);
+  if (p.mask) return dtype == 2 ? dq256_t<__nv_bfloat16, true>(p, s) : dq256_t<__half, true>(p, s);
+  return dtype == 2 ? dq256_t<__nv_bfloat16, false>(p, s) : dq256_t<__half, false>(p, s);
 }
 
 cudaError_t launch_tc_dkdv256(const Problem& p, int dtype, cudaStream_t s) {
-  return dtype == 2 ? dkdv256_t<__nv_bfloat16>(p, s) : dkdv256_t<__half>(p, s);
+  if (p.mask) return dtype == 2 ? dkdv256_t<__nv_bfloat16, true>(p, s) : dkdv256_t<__half, true>(p, s);
+  return dtype == 2 ? dkdv256_t<__nv_bfloat16, false>(p, s) : dkdv256_t<__half, false>(p, s);
 }
 
 }  // namespace sdpa

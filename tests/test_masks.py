@@ -103,8 +103,11 @@ CASES = [
     (Shape(2, 8, 2, 4, 300, 64), "bf16", True, _lib.PATH_AUTO, "shared"),        # short query, MMA, D = 64
     (Shape(1, 4, 2, 5, 90, 96), "f32", False, _lib.PATH_AUTO, "additive"),       # short query, CUDA cores
     (Shape(3, 4, 4, 1, 77, 64), "f16", False, _lib.PATH_AUTO, "padding"),        # single query row
-    (Shape(1, 4, 2, 50, 77, 256), "f16", False, _lib.PATH_AUTO, "additive"),     # D = 256: tensor-core forward
+    (Shape(1, 4, 2, 50, 77, 256), "f16", False, _lib.PATH_AUTO, "additive"),     # D = 256 on tensor cores
     (Shape(1, 4, 2, 200, 330, 256), "bf16", True, _lib.PATH_AUTO, "bool"),       # D = 256, several KV tiles
+    (Shape(1, 4, 2, 200, 330, 256), "f16", 2, _lib.PATH_TENSOR, "padding"),      # D = 256 forced, one row, bottom-right
+    (Shape(2, 4, 4, 70, 200, 256), "bf16", True, _lib.PATH_TENSOR, "shared"),    # D = 256 forced, one mask for all
+    (Shape(1, 4, 1, 129, 150, 256), "bf16", False, _lib.PATH_TENSOR, "additive"),  # D = 256 forced, G = 4
     (Shape(1, 4, 2, 50, 77, 256), "f32", False, _lib.PATH_AUTO, "padding"),      # D = 256, CUDA cores
     (Shape(2, 4, 2, 260, 520, 128), "bf16", False, _lib.PATH_AUTO, "sparse"),    # few keys a row, MMA
     (Shape(1, 4, 2, 130, 400, 256), "bf16", False, _lib.PATH_AUTO, "sparse"),    # few keys a row, D = 256
