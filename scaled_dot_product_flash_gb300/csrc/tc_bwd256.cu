@@ -117,23 +117,27 @@ __device__ __forceinline__ void mma_acc256(uint32_t acc_tmem, uint32_t a_tmem, u
 }
 
 // ================================================================== dQ
-constexpr int kDqQ = 0;
-constexpr int kDqDo = kOwnBytes;
-constexpr int kDqK = 2 * kOwnBytes;             // two K stages
-constexpr int kDqV = kDqK + 2 * kStrBytes;      // one V stage
-constexpr int kDqBytes = kDqV + kStrBytes;      // 224 KB
+// Shared memory: dO (64 KB, read by every dP), three K stages (K(n) is read by S(n) and by
+// dQ += dS(n)·K(n), late in the iteration) and two V stages, 32 KB each (224 KB).  Q is
+// loaded once into the V stages and copied into TMEM, where S = Q·Kᵀ reads it as the A
+// operand; the V stages are filled only after the copy.
+constexpr int kDqDo = 0;
+constexpr int kDqK = kOwnBytes;                 // three K stages
+constexpr int kDqV = kDqK + 3 * kStrBytes;      // two V stages (first holding Q)
+constexpr int kDqBytes = kDqV + 2 * kStrBytes;  // 224 KB
 
 struct Dq256Bars {
-  uint64_t own_full;
-  uint64_t k_full[2];
-  uint64_t k_empty[2];
-  uint64_t v_full;
-  uint64_t v_empty;
-  uint64_t s_full[2];    // one per S buffer
-  uint64_t dp_full;
-  uint64_t dp_free;      // every element thread has read dP
-  uint64_t ds_ready[2];  // dS of the block in S buffer i packed (one per buffer, as at D <= 128)
-  uint64_t dq_done[2];   // the dQ product of the block in S buffer i has finished
+  uint64_t own_full;      // Q and dO
+  uint64_t k_full[3];
+  uint64_t k_empty[3];    // dQ(n) has read K stage n % 3
+  uint64_t v_full[2];
+  uint64_t v_empty[2];    // dP(n) has read V stage n % 2
+  uint64_t opnd_ready;    // Q is in TMEM (512 element threads): the V stages are free
+  uint64_t s_full[2];     // S(n) in buffer n % 2
+  uint64_t s_read[2];     // every thread of the buffer's element group has read S(n)
+  uint64_t dp_full[2];    // dP(n) over S(n) in buffer n % 2
+  uint64_t ds_ready[2];   // dS(n) packed in buffer n % 2
+  uint64_t dq_done[2];    // dQ(n) has read buffer n % 2
   uint64_t acc_done;
   uint32_t tmem_base;
   int abort;
@@ -147,8 +151,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   constexpr bool kBf16 = IsBf16<T>::value;
   constexpr uint32_t kIdS = idesc_f16(kOwn, kStr, kBf16, false, false);  // M = 128, N = 64
   constexpr uint32_t kIdAcc = idesc_f16(kOwn, kD, kBf16, false, true);   // M = 128, N = 256, B MN-major
-  // TMEM columns: dQ [0, 256), S buffer i at [256 + 64i, 320 + 64i), dP [384, 448).
-  constexpr uint32_t kColDq = 0, kColS = 256, kColDp = 384;
+  // TMEM columns: dQ [0, 256), two buffers [256, 384) that take S(n), then dP(n) over it
+  // once the element group has read S(n), then dS(n) over that; Q [384, 512).
+  constexpr uint32_t kColDq = 0, kColX = 256, kColQ = 384;
   extern __shared__ unsigned char smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ Dq256Bars bars;
@@ -166,17 +171,20 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   if (threadIdx.x == 0) {
     bars.abort = 0;
     mbar_init(&bars.own_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < 3; ++s) {
       mbar_init(&bars.k_full[s], 1);
       mbar_init(&bars.k_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars.v_full[s], 1);
+      mbar_init(&bars.v_empty[s], 1);
       mbar_init(&bars.s_full[s], 1);
-      mbar_init(&bars.ds_ready[s], 512);
+      mbar_init(&bars.s_read[s], 256);  // the element group of buffer s (8 warps)
+      mbar_init(&bars.dp_full[s], 1);
+      mbar_init(&bars.ds_ready[s], 256);
       mbar_init(&bars.dq_done[s], 1);
     }
-    mbar_init(&bars.v_full, 1);
-    mbar_init(&bars.v_empty, 1);
-    mbar_init(&bars.dp_full, 1);
-    mbar_init(&bars.dp_free, 512);
+    mbar_init(&bars.opnd_ready, 512);
     mbar_init(&bars.acc_done, 3);  // one commit per MMA issuer
     fence_mbar_init();
   }
@@ -192,8 +200,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   if (warp >= 16) regs_dec<kRegsLow>();
 
   if (warp == kProducer) {
-    // Q and dO once; then K(n) into stage n % 2 once dQ(n-2) has read that stage, and V(n)
-    // into the V stage once dP(n-1) has read it.
+    // Q (into the V stages) and dO once; then K(n) into stage n % 3 once dQ(n-3) has read
+    // it, and V(n) into stage n % 2 once dP(n-2) has read it (the first two once Q is in
+    // TMEM).
     if (lane == 0) {
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
@@ -201,74 +210,79 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       prefetch_tmap(&tdo);
       mbar_arrive_expect_tx(&bars.own_full, 2 * kOwnBytes);
       for (int cb = 0; cb < 4; ++cb) {
-        tma_load_4d(sm + kDqQ + cb * kOwnCb, &tq, &bars.own_full, cb * 64, i0, h, b);
+        tma_load_4d(sm + kDqV + cb * kOwnCb, &tq, &bars.own_full, cb * 64, i0, h, b);
         tma_load_4d(sm + kDqDo + cb * kOwnCb, &tdo, &bars.own_full, cb * 64, i0, h, b);
       }
       int k_issued = 0, v_issued = 0;
       bool ok = true;
       for (int n = 0; ok && n < total; ++n) {
-        const int sk = n % 2;
-        if (!(ok = mbar_wait(&bars.k_empty[sk], ((n / 2) & 1) ^ 1, wc))) break;
-        mbar_arrive_expect_tx(&bars.k_full[sk], kStrBytes);
+        const int ks = n % 3, vs = n % 2;
+        if (!(ok = mbar_wait(&bars.k_empty[ks], ((n / 3) & 1) ^ 1, wc))) break;
+        mbar_arrive_expect_tx(&bars.k_full[ks], kStrBytes);
         for (int cb = 0; cb < 4; ++cb)
-          tma_load_4d(sm + kDqK + sk * kStrBytes + cb * kStrCb, &tk, &bars.k_full[sk], cb * 64, n * kStr, g, b);
+          tma_load_4d(sm + kDqK + ks * kStrBytes + cb * kStrCb, &tk, &bars.k_full[ks], cb * 64, n * kStr, g, b);
         k_issued = n + 1;
-        if (!(ok = mbar_wait(&bars.v_empty, (n & 1) ^ 1, wc))) break;
-        mbar_arrive_expect_tx(&bars.v_full, kStrBytes);
+        if (!(ok = mbar_wait(&bars.v_empty[vs], ((n / 2) & 1) ^ 1, wc) &&
+                   (n >= 2 || mbar_wait(&bars.opnd_ready, 0, wc))))
+          break;
+        mbar_arrive_expect_tx(&bars.v_full[vs], kStrBytes);
         for (int cb = 0; cb < 4; ++cb)
-          tma_load_4d(sm + kDqV + cb * kStrCb, &tv, &bars.v_full, cb * 64, n * kStr, g, b);
+          tma_load_4d(sm + kDqV + vs * kStrBytes + cb * kStrCb, &tv, &bars.v_full[vs], cb * 64, n * kStr, g, b);
         v_issued = n + 1;
       }
       if (!ok || bars.abort) {  // let copies still in flight land before the block exits
-        for (int n = max(0, k_issued - 2); n < k_issued; ++n) drain_wait(&bars.k_full[n % 2], (n / 2) & 1);
-        if (v_issued > 0) drain_wait(&bars.v_full, (v_issued - 1) & 1);
+        for (int n = max(0, k_issued - 3); n < k_issued; ++n) drain_wait(&bars.k_full[n % 3], (n / 3) & 1);
+        for (int n = max(0, v_issued - 2); n < v_issued; ++n) drain_wait(&bars.v_full[n % 2], (n / 2) & 1);
       }
     }
   } else if (warp >= kIssuer) {
-    // Warp 17: S(n) = Q·K(n)ᵀ into S buffer n % 2 once dQ(n-2) has read dS(n-2) from it.
-    // Warp 18: dP(n) = dO·V(n)ᵀ once the element warps have read dP(n-1).
+    // Warp 17: S(n) = Q·K(n)ᵀ into buffer n % 2 once dQ(n-2) has read it.
+    // Warp 18: dP(n) = dO·V(n)ᵀ over S(n) once the element group has read S(n).
     // Warp 19: dQ += dS(n)·K(n) once dS(n) is packed.
     constexpr unsigned kAll = 0xffffffffu;
     const int role = __shfl_sync(kAll, warp - kIssuer, 0);
     bool ok = __all_sync(kAll, mbar_wait(&bars.own_full, 0, wc));
+    if (role == 0 && ok) ok = __all_sync(kAll, mbar_wait(&bars.opnd_ready, 0, wc));
     tc_fence_after();
-    const uint32_t q_s = smem_u32(sm + kDqQ), do_s = smem_u32(sm + kDqDo);
-    const uint32_t k_s = smem_u32(sm + kDqK), v_s = smem_u32(sm + kDqV);
+    const uint32_t do_s = smem_u32(sm + kDqDo);
+    auto k_s = [&](int n) { return smem_u32(sm + kDqK + (n % 3) * kStrBytes); };
+    auto v_s = [&](int n) { return smem_u32(sm + kDqV + (n % 2) * kStrBytes); };
     if (role == 0) {
       for (int n = 0; ok && n < total; ++n) {
-        if (!(ok = __all_sync(kAll, mbar_wait(&bars.k_full[n % 2], (n / 2) & 1, wc)))) break;
-        if (n >= 2 && !(ok = __all_sync(kAll, mbar_wait(&bars.dq_done[n % 2], ((n - 2) / 2) & 1, wc)))) break;
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.k_full[n % 3], (n / 3) & 1, wc) &&
+                                        mbar_wait(&bars.dq_done[n % 2], ((n / 2) & 1) ^ 1, wc))))
+          break;
         tc_fence_after();
-        mma_scores256(tbase + kColS + 64 * (n % 2), q_s, k_s + (n % 2) * kStrBytes, kIdS);
+        mma_scores256_ts(tbase + kColX + 64 * (n % 2), tbase + kColQ, k_s(n), kIdS);
         mma_commit_w(&bars.s_full[n % 2]);
       }
     } else if (role == 1) {
       for (int n = 0; ok && n < total; ++n) {
-        if (!(ok = __all_sync(kAll, mbar_wait(&bars.v_full, n & 1, wc)))) break;
-        if (n >= 1 && !(ok = __all_sync(kAll, mbar_wait(&bars.dp_free, (n - 1) & 1, wc)))) break;
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.v_full[n % 2], (n / 2) & 1, wc) &&
+                                        mbar_wait(&bars.s_read[n % 2], (n / 2) & 1, wc))))
+          break;
         tc_fence_after();
-        mma_scores256(tbase + kColDp, do_s, v_s, kIdS);
-        mma_commit_w(&bars.dp_full);
-        mma_commit_w(&bars.v_empty);
+        mma_scores256(tbase + kColX + 64 * (n % 2), do_s, v_s(n), kIdS);
+        mma_commit_w(&bars.dp_full[n % 2]);
+        mma_commit_w(&bars.v_empty[n % 2]);
       }
     } else {
       for (int n = 0; ok && n < total; ++n) {
         // K(n) is loaded (S(n) read it before dS(n) could exist); waiting on its barrier too
         // makes the TMA writes visible to this warp's MMA directly.
         if (!(ok = __all_sync(kAll, mbar_wait(&bars.ds_ready[n % 2], (n / 2) & 1, wc) &&
-                                        mbar_wait(&bars.k_full[n % 2], (n / 2) & 1, wc))))
+                                        mbar_wait(&bars.k_full[n % 3], (n / 3) & 1, wc))))
           break;
         tc_fence_after();
-        mma_acc256(tbase + kColDq, tbase + kColS + 64 * (n % 2), k_s + (n % 2) * kStrBytes, kIdAcc, n == 0);
+        mma_acc256(tbase + kColDq, tbase + kColX + 64 * (n % 2), k_s(n), kIdAcc, n == 0);
         mma_commit_w(&bars.dq_done[n % 2]);
-        mma_commit_w(&bars.k_empty[n % 2]);
+        mma_commit_w(&bars.k_empty[n % 3]);
       }
     }
     mma_commit_w(&bars.acc_done);
     drain_wait(&bars.acc_done, 0);
   } else {
     regs_inc<kRegsHigh>();
-    // Warp e: TMEM lane quarter e % 4 (queries), key columns [16c, 16c + 16) with c = e / 4.
     const int c = warp / 4, quarter = warp % 4;
     const int i = i0 + quarter * 32 + lane;  // this thread's query
     const bool valid = i < p.Lq;
@@ -279,62 +293,104 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const int64_t moff = kMasked && valid ? row_off(p.lm, b, h, i) : 0;
     const uint64_t cc = f2pack(p.scale_log2, p.scale_log2);
     const uint64_t nl = f2pack(-lse2, -lse2), nd = f2pack(-dl, -dl);
-    bool ok = true;
-    for (int n = 0; n < total; ++n) {
-      const int k0 = n * kStr + 16 * c;  // first key of this warp's columns
-      // Mask terms of this warp's keys as 16-bit pairs (0 past the row's mask pieces: those
-      // keys are past Lkv and hidden by lim), read before the waits so that they hide the
-      // loads' latency.
-      uint32_t mk[kMasked ? 8 : 1];
-      if constexpr (kMasked) mask_pairs<T, 16>(mk, p, moff + k0, valid && k0 < p.Lkv ? p.Lkv - k0 : 0);
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[n % 2], (n / 2) & 1, wc) &&
-                                       mbar_wait(&bars.dp_full, n & 1, wc));
-      if (!ok) break;
-      tc_fence_after();
-      const bool need_mask = (k0 + 16 > p.Lkv) || (p.causal && k0 + 15 > i0 + p.coff);
-      const int lim = min(p.Lkv - k0, p.causal ? i + p.coff - k0 + 1 : 16);  // keys k0 + e, e < lim
-      const uint32_t s_addr = tmem_addr(tbase, quarter * 32, kColS + 64 * (n % 2) + 16 * c);
-      const uint32_t dp_addr = tmem_addr(tbase, quarter * 32, kColDp + 16 * c);
-      // dP and S of this warp's columns; the dP buffer is released at once.
-      uint32_t dr[16], sr[16];
-      tmem_ld16(dp_addr, dr);
-      tmem_ld16(s_addr, sr);
-      tmem_ld_wait(dr);
-      reg_fence(sr);
-      tc_fence_before();
-      mbar_arrive(&bars.dp_free);
-      uint32_t dsk[8];
+    // Q into TMEM columns [384, 512): row r in lane r, elements (2i, 2i+1) of D in column
+    // 384 + i.  Warp e copies rows [32(e % 4), +32) of D columns [64c, 64c + 64); the 16-byte
+    // pieces of a swizzled row hold consecutive element pairs, so they go over as they are.
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars.own_full, 0, wc));
+    if (ok) {
+      const uint8_t* src = sm + kDqV + c * kOwnCb;
+      const int r = quarter * 32 + lane;
+      uint32_t w[32];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        float p0, p1;
-        uint64_t xx = ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl);
-        if constexpr (kMasked) {
-          float x0, x1, m0, m1;
-          f2unpack(xx, x0, x1);
-          unpack2<T>(mk[e], m0, m1);
-          xx = f2pack(x0 + m0 * kLog2e, x1 + m1 * kLog2e);
-        }
-        ex2_pair(xx, p0, p1);
-        if (need_mask) {
-          if (2 * e >= lim) p0 = 0.f;
-          if (2 * e + 1 >= lim) p1 = 0.f;
-        }
-        float d0, d1;
-        f2unpack(fmul2(f2pack(p0, p1), fadd2(f2pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), nd)),
-                 d0, d1);
-        dsk[e] = pack2<T>(d0, d1);
+      for (int pc = 0; pc < 8; ++pc) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + sw128_off(r, pc));
+        w[4 * pc] = v.x;
+        w[4 * pc + 1] = v.y;
+        w[4 * pc + 2] = v.z;
+        w[4 * pc + 3] = v.w;
       }
-      tmem_st8(s_addr, dsk);  // dS over the first 8 of this warp's 16 columns
+      tmem_st32(tmem_addr(tbase, quarter * 32, kColQ + 32 * c), w);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars.ds_ready[n % 2]);
+    }
+    mbar_arrive(&bars.opnd_ready);
+    // The element warps form two groups of 8 that take turns: group gq = e / 8 takes the
+    // key blocks n with n % 2 == gq (TMEM buffer n % 2).  Warp e of a group has lane quarter
+    // e % 4 (queries) and key columns [32h, 32h + 32), h = (e / 4) % 2; it packs the 16-bit
+    // dS of keys [32h, 32h + 16) over columns [32h, 32h + 8) and those of [32h + 16, 32h + 32)
+    // over [32h + 16, 32h + 24), where the K-steps 2h and 2h + 1 of the dQ product read them.
+    const int gq = warp / 8, h2 = (warp / 4) % 2;
+    for (int n = gq; ok && n < total; n += 2) {
+      const int s = n % 2;
+      const int k0 = n * kStr + 32 * h2;  // first key of this warp's columns
+      // Mask terms of this warp's keys as 16-bit pairs (0 past the row's mask pieces: those
+      // keys are past Lkv and hidden by lim), read before the wait so that it hides the
+      // loads' latency.
+      uint32_t mk[kMasked ? 16 : 1];
+      if constexpr (kMasked) mask_pairs<T, 32>(mk, p, moff + k0, valid && k0 < p.Lkv ? p.Lkv - k0 : 0);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[s], (n / 2) & 1, wc));
+      if (!ok) break;
+      tc_fence_after();
+      const bool need_mask = (k0 + 32 > p.Lkv) || (p.causal && k0 + 31 > i0 + p.coff);
+      const int lim = min(p.Lkv - k0, p.causal ? i + p.coff - k0 + 1 : 32);  // keys k0 + e, e < lim
+      const uint32_t x_addr = tmem_addr(tbase, quarter * 32, kColX + 64 * s + 32 * h2);
+      // P of this warp's 32 keys, in fp32 pairs.
+      uint64_t pf[16];
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t sr[16];
+        tmem_ld16(x_addr + 16 * hf, sr);
+        tmem_ld_wait(sr);
+        if (hf == 1) {  // dP(n) may now overwrite S(n)
+          tc_fence_before();
+          mbar_arrive(&bars.s_read[s]);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int x = 8 * hf + e;
+          float p0, p1;
+          uint64_t xx = ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl);
+          if constexpr (kMasked) {
+            float x0, x1, m0, m1;
+            f2unpack(xx, x0, x1);
+            unpack2<T>(mk[x], m0, m1);
+            xx = f2pack(x0 + m0 * kLog2e, x1 + m1 * kLog2e);
+          }
+          ex2_pair(xx, p0, p1);
+          if (need_mask) {
+            if (2 * x >= lim) p0 = 0.f;
+            if (2 * x + 1 >= lim) p1 = 0.f;
+          }
+          pf[x] = f2pack(p0, p1);
+        }
+      }
+      // dS = P∘(dP − δ), in two halves of 16 columns.
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_full[s], (n / 2) & 1, wc));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t dr[16];
+        tmem_ld16(x_addr + 16 * hf, dr);
+        tmem_ld_wait(dr);
+        uint32_t pk[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float d0, d1;
+          f2unpack(fmul2(pf[8 * hf + e], fadd2(f2pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), nd)),
+                   d0, d1);
+          pk[e] = pack2<T>(d0, d1);
+        }
+        tmem_st8(x_addr + 16 * hf, pk);  // dS over the first 8 of each 16 columns
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars.ds_ready[s]);
     }
     // Epilogue: dQ·scale in 8 chunks of 32 columns (warps of group c take chunks c and
-    // c + 4), staged in the Q buffer (the last S product has read it) and written by bulk
-    // tensor stores once all 16 warps have staged theirs (rows past Lq are clipped).  With
-    // no key block (total == 0) nothing else has waited for the Q load, so wait for it here.
-    if (ok)
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars.own_full, 0, wc) && (total == 0 || mbar_wait(&bars.acc_done, 0, wc)));
+    // c + 4), staged in the dO buffer (the last dP product has read it) and written by bulk
+    // tensor stores once all 16 warps have staged theirs (rows past Lq are clipped).
+    if (ok) ok = __all_sync(0xffffffffu, total == 0 || mbar_wait(&bars.acc_done, 0, wc));
     const int r = quarter * 32 + lane;
     if (ok) {
       tc_fence_after();
@@ -352,7 +408,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           packed[e] = pack2<T>(__uint_as_float(acc[2 * e]) * p.scale, __uint_as_float(acc[2 * e + 1]) * p.scale);
-        uint8_t* blk = sm + kDqQ + (c32 / 2) * kOwnCb;
+        uint8_t* blk = sm + kDqDo + (c32 / 2) * kOwnCb;
 #pragma unroll
         for (int v4 = 0; v4 < 4; ++v4)
           *reinterpret_cast<uint4*>(blk + sw128_off(r, (c32 % 2) * 4 + v4)) =
@@ -361,7 +417,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       fence_async_smem();
     }
     if (named_sync_and(1, 512, ok) && warp == 0 && lane == 0) {
-      for (int cb = 0; cb < 4; ++cb) tma_store_4d(&tdq, sm + kDqQ + cb * kOwnCb, cb * 64, i0, h, b);
+      for (int cb = 0; cb < 4; ++cb) tma_store_4d(&tdq, sm + kDqDo + cb * kOwnCb, cb * 64, i0, h, b);
       bulk_commit();
       bulk_wait_read();
     }

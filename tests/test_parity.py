@@ -52,6 +52,13 @@ def test_workload_bf16_long_context_sampled():
                    groups=[(0, 0), (0, 11)])
 
 
+def test_workload_bf16_head_dim_256_sampled():
+    """bf16 GQA 4:1, B=1, Hq=16, Hkv=4, L=4096, D=256, causal, seed 5 (the bench's D = 256
+    case): full-size run on the tensor-core kernels, two whole groups checked (the first
+    and the last KV head, every query row of their 8 heads)."""
+    sampled_parity(Shape(1, 16, 4, 4096, 4096, 256), "bf16", True, seed=5, groups=[(0, 0), (0, 3)])
+
+
 def test_workload_bf16_short_query():
     """bf16, B=4, Hq=32, Hkv=8, Lq in {1, 4, 8}, Lkv=8192, D=128, non-causal, seed 4:
     drawn one after another from one generator; every output compared."""
