@@ -334,22 +334,20 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const bool need_mask = (k0 + 32 > p.Lkv) || (p.causal && k0 + 31 > i0 + p.coff);
       const int lim = min(p.Lkv - k0, p.causal ? i + p.coff - k0 + 1 : 32);  // keys k0 + e, e < lim
       const uint32_t x_addr = tmem_addr(tbase, quarter * 32, kColX + 64 * s + 32 * h2);
-      // P of this warp's 32 keys, in fp32 pairs.
+      // P of this warp's 32 keys, in fp32 pairs (one TMEM round trip for S).
       uint64_t pf[16];
+      uint32_t sr[32];
+      tmem_ld32(x_addr, sr);
+      tmem_ld_wait(sr);
+      tc_fence_before();  // dP(n) may now overwrite S(n)
+      mbar_arrive(&bars.s_read[s]);
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        uint32_t sr[16];
-        tmem_ld16(x_addr + 16 * hf, sr);
-        tmem_ld_wait(sr);
-        if (hf == 1) {  // dP(n) may now overwrite S(n)
-          tc_fence_before();
-          mbar_arrive(&bars.s_read[s]);
-        }
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int x = 8 * hf + e;
           float p0, p1;
-          uint64_t xx = ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), cc, nl);
+          uint64_t xx = ffma2(f2pack(__uint_as_float(sr[2 * x]), __uint_as_float(sr[2 * x + 1])), cc, nl);
           if constexpr (kMasked) {
             float x0, x1, m0, m1;
             f2unpack(xx, x0, x1);
@@ -364,21 +362,21 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           pf[x] = f2pack(p0, p1);
         }
       }
-      // dS = P∘(dP − δ), in two halves of 16 columns.
+      // dS = P∘(dP − δ) (one TMEM round trip for dP).
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.dp_full[s], (n / 2) & 1, wc));
       if (!ok) break;
       tc_fence_after();
+      uint32_t dr[32];
+      tmem_ld32(x_addr, dr);
+      tmem_ld_wait(dr);
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        uint32_t dr[16];
-        tmem_ld16(x_addr + 16 * hf, dr);
-        tmem_ld_wait(dr);
         uint32_t pk[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
+          const int x = 8 * hf + e;
           float d0, d1;
-          f2unpack(fmul2(pf[8 * hf + e], fadd2(f2pack(__uint_as_float(dr[2 * e]), __uint_as_float(dr[2 * e + 1])), nd)),
-                   d0, d1);
+          f2unpack(fmul2(pf[x], fadd2(f2pack(__uint_as_float(dr[2 * x]), __uint_as_float(dr[2 * x + 1])), nd)), d0, d1);
           pk[e] = pack2<T>(d0, d1);
         }
         tmem_st8(x_addr + 16 * hf, pk);  // dS over the first 8 of each 16 columns
