@@ -485,7 +485,9 @@ constexpr int kKvBytes = kKvBars + (int)sizeof(Kv256Bars);
 static_assert(kKvBytes <= 227 * 1024, "dK/dV shared memory exceeds the per-block limit");
 constexpr int kKvThreads = 640;
 
-template <typename T, bool kMasked>
+// kRowBc: the mask has one row for every query (row stride 0, e.g. key padding), read once
+// per key instead of once per query.
+template <typename T, bool kMasked, bool kRowBc>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
     tc_dkdv256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -754,10 +756,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
         tmem_ld16(x_addr + 16 * hf, sr);
         float mv[kMasked ? 16 : 1];  // log2e·M of query i0 + 16hf + e
         if constexpr (kMasked) {
+          if constexpr (kRowBc) {
+            const float m = j < p.Lkv ? mask_log2<T>(p, mcol) : 0.f;
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int q = i0 + 16 * hf + e;
-            mv[e] = (j < p.Lkv && q < p.Lq) ? mask_log2<T>(p, mcol + (int64_t)q * p.lm.sl) : 0.f;
+            for (int e = 0; e < 16; ++e) mv[e] = i0 + 16 * hf + e < p.Lq ? m : 0.f;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int q = i0 + 16 * hf + e;
+              mv[e] = (j < p.Lkv && q < p.Lq) ? mask_log2<T>(p, mcol + (int64_t)q * p.lm.sl) : 0.f;
+            }
           }
         }
         tmem_ld_wait(sr);
@@ -928,7 +936,7 @@ cudaError_t dq256_t(const Problem& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <typename T, bool kMasked>
+template <typename T, bool kMasked, bool kRowBc>
 cudaError_t dkdv256_t(const Problem& p, cudaStream_t s) {
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   if (!make_tmap_4d(&tk, p.k, kD, p.Lkv, p.Hkv, p.B, p.lk, kOwn) ||
@@ -938,7 +946,7 @@ cudaError_t dkdv256_t(const Problem& p, cudaStream_t s) {
       !make_tmap_4d(&tq, p.q, kD, p.Lq, p.Hq, p.B, p.lq, kStr) ||
       !make_tmap_4d(&tdo, p.dout, kD, p.Lq, p.Hq, p.B, p.ldo, kStr))
     return cudaErrorInvalidValue;
-  auto kern = tc_dkdv256_kernel<T, kMasked>;
+  auto kern = tc_dkdv256_kernel<T, kMasked, kRowBc>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kKvBytes);
   if (e != cudaSuccess) return e;
   const unsigned nkt = (p.Lkv + kOwn - 1) / kOwn;
@@ -956,8 +964,10 @@ cudaError_t launch_tc_dq256(const Problem& p, int dtype, cudaStream_t s) {
 }
 
 cudaError_t launch_tc_dkdv256(const Problem& p, int dtype, cudaStream_t s) {
-  if (p.mask) return dtype == 2 ? dkdv256_t<__nv_bfloat16, true>(p, s) : dkdv256_t<__half, true>(p, s);
-  return dtype == 2 ? dkdv256_t<__nv_bfloat16, false>(p, s) : dkdv256_t<__half, false>(p, s);
+  if (p.mask && p.lm.sl == 0)
+    return dtype == 2 ? dkdv256_t<__nv_bfloat16, true, true>(p, s) : dkdv256_t<__half, true, true>(p, s);
+  if (p.mask) return dtype == 2 ? dkdv256_t<__nv_bfloat16, true, false>(p, s) : dkdv256_t<__half, true, false>(p, s);
+  return dtype == 2 ? dkdv256_t<__nv_bfloat16, false, false>(p, s) : dkdv256_t<__half, false, false>(p, s);
 }
 
 }  // namespace sdpa

@@ -215,6 +215,7 @@ def test_head_dim_256_refusals():
     (Shape(1, 8, 2, 600, 600, 128), "bf16", True),
     (Shape(2, 8, 2, 4, 900, 64), "f16", False),
     (Shape(1, 2, 2, 100, 100, 64), "f32", True),
+    (Shape(1, 8, 2, 300, 460, 256), "bf16", True),  # D = 256: two-CTA partial sums in fixed order
 ])
 def test_bitwise_deterministic(shape, dtype, causal):
     q, k, v, do = draw(shape, 21, dtype)

@@ -37,6 +37,8 @@ CASES = [
     (Shape(1, 2, 2, 5, 90, 96), "f32", False, _lib.PATH_AUTO),         # short query, CUDA cores
     (Shape(1, 4, 2, 130, 130, 64), "bf16", True, _lib.PATH_SIMT),      # forced CUDA cores, bf16
     (Shape(1, 4, 2, 200, 330, 96), "bf16", True, _lib.PATH_AUTO),      # tensor cores, D = 96
+    (Shape(1, 4, 2, 150, 200, 256), "bf16", True, _lib.PATH_AUTO),     # tensor cores, D = 256
+    (Shape(2, 4, 4, 70, 130, 256), "f16", False, _lib.PATH_AUTO),      # D = 256, MHA
 ]
 
 

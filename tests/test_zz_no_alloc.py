@@ -42,6 +42,7 @@ def test_noalloc_matches_workspace_backward_twice():
     # reuses the same static scratch (stale contents from the first call in its tail).
     _run_pair(Shape(2, 8, 2, 384, 384, 128), "bf16", True, seed=41)
     _run_pair(Shape(1, 4, 4, 200, 260, 64), "f16", False, seed=42)
+    _run_pair(Shape(1, 4, 1, 300, 330, 256), "bf16", True, seed=43)  # D = 256 kernels
 
 
 def test_noalloc_refuses_problems_larger_than_its_scratch():
