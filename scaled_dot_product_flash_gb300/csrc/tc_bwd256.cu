@@ -18,12 +18,11 @@
 // the MMA issuers; warp 17 owns the TMEM.  Every wait is bounded, as everywhere in the
 // library.
 // Attention masks: each kernel has a masked instantiation (kMasked) that adds log2e·M to
-// the log2-domain scores before the exponential, as the D <= 128 kernels do.  Neither has
-// shared memory left for a mask tile: the dQ kernel reads its row's 16 mask values from
-// global memory in 16-byte pieces before its barrier waits, the dK/dV kernel reads its
-// key's column for 16 queries at a time (one byte or element per query, coalesced across
-// the warp's 32 keys) while its TMEM load is in flight.  Keys past Lkv and rows past Lq
-// are not read.
+// the log2-domain scores before the exponential, as the D <= 128 kernels do.  The dQ
+// kernel has no shared memory left for a mask tile and reads its row's 32 mask values
+// from global memory in 16-byte pieces before its barrier wait; the dK/dV kernel reads a
+// mask with one row for every query once per key from global memory and stages any other
+// mask's [64 x 128] tiles by TMA in the place of its third Q slot.
 #include "launch.h"
 #include "tc_common.cuh"
 
@@ -467,6 +466,8 @@ struct Kv256Bars {
   uint64_t ds_ready[2];   // dK blocks: dSᵀ packed in buffer i
   uint64_t y_free[2];     // dK blocks: dK has read buffer i
   uint64_t opnd_ready;    // the TMEM copy of the owned operand is complete (512 threads)
+  uint64_t mask_full[2];  // staged-mask variant: the mask tile of query block n in slot n % 2
+  uint64_t mask_empty[2]; // the element group of slot i has read it
   uint64_t acc_done;
   uint32_t tmem_base;
   int abort;
@@ -475,8 +476,13 @@ struct Kv256Bars {
 };
 constexpr int kKvK = 0;
 constexpr int kKvV = kOwnBytes;            // V (dK blocks, until it is in TMEM), then two dO slots
-constexpr int kKvQ = 2 * kOwnBytes;        // three Q slots
+constexpr int kKvQ = 2 * kOwnBytes;        // three Q slots (two with a staged mask)
 constexpr int kKvBars = kKvQ + 3 * kStrBytes;  // 224 KB of tiles, then the barriers
+// Staged-mask variant: two mask tiles [64 queries x 128 keys] of at most 16-bit elements in
+// the place of the third Q slot.
+constexpr int kKvMaskTile = kStr * kOwn * 2;
+constexpr int kKvMask = kKvQ + 2 * kStrBytes;
+static_assert(kKvMask + 2 * kKvMaskTile <= kKvBars, "mask tiles overlap the barriers");
 // The partner's fp32 partial sum [128 x 256] in the first block of a cluster, once no MMA
 // reads V, dO or Q any more: 16-byte pieces ordered (32-column chunk, piece, row).
 constexpr int kKvRed = kOwnBytes;
@@ -486,12 +492,17 @@ static_assert(kKvBytes <= 227 * 1024, "dK/dV shared memory exceeds the per-block
 constexpr int kKvThreads = 640;
 
 // kRowBc: the mask has one row for every query (row stride 0, e.g. key padding), read once
-// per key instead of once per query.
+// per key from global memory.  Any other mask is staged: the producer loads each query
+// block's [64 x 128] mask tile by TMA (map tm) into one of two slots, from which each
+// element thread reads its key's column; the third Q slot gives way to the two tiles.
 template <typename T, bool kMasked, bool kRowBc>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
     tc_dkdv256_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                      const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv, Problem p) {
+                      const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv,
+                      const __grid_constant__ CUtensorMap tm, Problem p) {
+  constexpr bool kTileMask = kMasked && !kRowBc;
+  constexpr int kQs = kTileMask ? 2 : 3;  // Q slots
   constexpr bool kBf16 = IsBf16<T>::value;
   constexpr uint32_t kIdS = idesc_f16(kOwn, kStr, kBf16, false, false);  // M = 128, N = 64
   constexpr uint32_t kIdAcc = idesc_f16(kOwn, kD, kBf16, false, true);   // M = 128, N = 256, B MN-major
@@ -551,6 +562,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
       mbar_init(&bars.dp_full[s], 1);
       mbar_init(&bars.ds_ready[s], 256);
       mbar_init(&bars.y_free[s], 1);
+      mbar_init(&bars.mask_full[s], 1);
+      mbar_init(&bars.mask_empty[s], 256);
     }
     mbar_init(&bars.opnd_ready, 512);
     mbar_init(&bars.acc_done, 3);  // one commit per MMA issuer warp
@@ -570,7 +583,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
   bool el_ok = true;  // element threads: every wait of the loop and of acc_done succeeded
 
   if (warp == kProducer) {
-    // K (and V in dK blocks) once; per query block n: Q(n) into slot n % 3 once its last
+    // K (and V in dK blocks) once; per query block n: Q(n) into slot n % kQs once its last
     // reader of n-3 has finished, dO(n) into slot n % 2 once the reader of n-2 has finished
     // (in dK blocks the first dO load waits for V to be copied out of its place), then the
     // per-query vectors into slot n % 2 once the element threads are done with those of n-2.
@@ -600,14 +613,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
       }
     };
     if (total > 0) fetch(0);
-    int q_issued = 0, do_issued = 0;
+    int q_issued = 0, do_issued = 0, mask_issued = 0;
     bool ok = true;
     for (int n = 0; ok && n < total; ++n) {
       const int s = n % 2;
       const int h = g * p.G + (n_begin + n) / nqb;
       const int i0 = i_begin + ((n_begin + n) % nqb) * kStr;
-      const int qs = n % 3;
-      if (!(ok = __all_sync(kAll, mbar_wait(&bars.q_empty[qs], ((n / 3) & 1) ^ 1, wc)))) break;
+      const int qs = n % kQs;
+      if (!(ok = __all_sync(kAll, mbar_wait(&bars.q_empty[qs], ((n / kQs) & 1) ^ 1, wc)))) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(&bars.q_full[qs], kStrBytes);
         for (int cb = 0; cb < 4; ++cb)
@@ -631,33 +644,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
         bars.ndelta[s][lane + 32 * t] = -dl[t];
       }
       mbar_arrive(&bars.vec_full[s]);
+      if constexpr (kTileMask) {  // the query block's mask tile, once its slot's readers are done
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.mask_empty[s], ((n / 2) & 1) ^ 1, wc)))) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars.mask_full[s], kStr * kOwn * (p.mask_kind == kMaskBool ? 1 : 2));
+          tma_load_4d(sm + kKvMask + s * kKvMaskTile, &tm, &bars.mask_full[s], j0, i0, p.lm.sh == 0 ? 0 : h,
+                      p.lm.sb == 0 ? 0 : b);
+        }
+        mask_issued = n + 1;
+      }
       if (n + 1 < total) fetch(n + 1);
     }
     if (lane == 0 && (!ok || bars.abort)) {  // let copies still in flight land before the block exits
-      for (int n = max(0, q_issued - 3); n < q_issued; ++n) drain_wait(&bars.q_full[n % 3], (n / 3) & 1);
+      for (int n = max(0, q_issued - kQs); n < q_issued; ++n) drain_wait(&bars.q_full[n % kQs], (n / kQs) & 1);
       for (int n = max(0, do_issued - 2); n < do_issued; ++n)
         drain_wait(&bars.do_full[do_slot(n)], do_par(n));
+      for (int n = max(0, mask_issued - 2); n < mask_issued; ++n) drain_wait(&bars.mask_full[n % 2], (n / 2) & 1);
     }
   } else if (warp >= kIssuer) {
     const int role = __shfl_sync(kAll, warp - kIssuer, 0);
     bool ok = __all_sync(kAll, mbar_wait(&bars.own_full, 0, wc));
     tc_fence_after();
     const uint32_t k_s = smem_u32(sm + kKvK);
-    auto q_s = [&](int n) { return smem_u32(sm + kKvQ + (n % 3) * kStrBytes); };
+    auto q_s = [&](int n) { return smem_u32(sm + kKvQ + (n % kQs) * kStrBytes); };
     // The TS score product of the block (dV: Sᵀ; dK: dPᵀ) reads the TMEM copy of K or V.
     if (role < 2 && (role == 0) == dv && ok) ok = __all_sync(kAll, mbar_wait(&bars.opnd_ready, 0, wc));
     if (role == 0) {
       // Sᵀ(n) = K·Q(n)ᵀ into buffer n % 2 once dV(n-2) or dK(n-2) has read it.
       for (int n = 0; ok && n < total; ++n) {
         const int s = n % 2;
-        if (!(ok = __all_sync(kAll, mbar_wait(&bars.q_full[n % 3], (n / 3) & 1, wc) &&
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.q_full[n % kQs], (n / kQs) & 1, wc) &&
                                         mbar_wait(dv ? &bars.x_free[s] : &bars.y_free[s], ((n / 2) & 1) ^ 1, wc))))
           break;
         tc_fence_after();
         if (dv) mma_scores256_ts(tbase + kColX + 64 * s, tbase + kColOp, q_s(n), kIdS);
         else mma_scores256(tbase + kColX + 64 * s, k_s, q_s(n), kIdS);
         mma_commit_w(&bars.s_full[s]);
-        if (dv) mma_commit_w(&bars.q_empty[n % 3]);
+        if (dv) mma_commit_w(&bars.q_empty[n % kQs]);
       }
     } else if (role == 1 && dv) {
       // dV += Pᵀ(n)·dO(n).
@@ -689,12 +712,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
       for (int n = 0; ok && n < total; ++n) {
         const int s = n % 2;
         if (!(ok = __all_sync(kAll, mbar_wait(&bars.ds_ready[s], (n / 2) & 1, wc) &&
-                                        mbar_wait(&bars.q_full[n % 3], (n / 3) & 1, wc))))
+                                        mbar_wait(&bars.q_full[n % kQs], (n / kQs) & 1, wc))))
           break;
         tc_fence_after();
         mma_acc256(tbase + kColAcc, tbase + kColX + 64 * s, q_s(n), kIdAcc, n == 0);
         mma_commit_w(&bars.y_free[s]);
-        mma_commit_w(&bars.q_empty[n % 3]);
+        mma_commit_w(&bars.q_empty[n % kQs]);
       }
     }
     mma_commit_w(&bars.acc_done);
@@ -738,7 +761,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
       const int s = n % 2;
       const int i0 = i_begin + ((n_begin + n) % nqb) * kStr + 32 * h2;  // first query of this warp's columns
       ok = __all_sync(kAll, mbar_wait(&bars.s_full[s], (n / 2) & 1, wc) &&
-                                mbar_wait(&bars.vec_full[s], (n / 2) & 1, wc));
+                                mbar_wait(&bars.vec_full[s], (n / 2) & 1, wc) &&
+                                (!kTileMask || mbar_wait(&bars.mask_full[s], (n / 2) & 1, wc)));
       if (!ok) break;
       tc_fence_after();
       const int ic = i0 + p.coff;  // key j is hidden from query i0 + q when j > ic + q
@@ -747,7 +771,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
       const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(&bars.ndelta[s][32 * h2]);
       const uint32_t x_addr = tmem_addr(tbase, quarter * 32, kColX + 64 * s + 32 * h2);
       // Mask element (this block's head, query 0, key j); keys past Lkv are not read.
-      const int64_t mcol = kMasked ? row_off(p.lm, b, g * p.G + (n_begin + n) / nqb, 0) + j : 0;
+      const int64_t mcol = kRowBc ? row_off(p.lm, b, g * p.G + (n_begin + n) / nqb, 0) + j : 0;
       // Pᵀ of this warp's 32 queries, in fp32 pairs.
       uint64_t pf[16];
 #pragma unroll
@@ -761,10 +785,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
 #pragma unroll
             for (int e = 0; e < 16; ++e) mv[e] = i0 + 16 * hf + e < p.Lq ? m : 0.f;
           } else {
+            // Row q of the tile holds query i0 - 32h + q, key k at element 128q + k; rows
+            // past Lq and keys past Lkv were filled with zeros by the load (those P are zero
+            // or clipped anyway).
+            const int kl = quarter * 32 + lane, q0 = 32 * h2 + 16 * hf;
+            const uint8_t* tile = sm + kKvMask + s * kKvMaskTile;
+            if (p.mask_kind == kMaskBool) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int q = i0 + 16 * hf + e;
-              mv[e] = (j < p.Lkv && q < p.Lq) ? mask_log2<T>(p, mcol + (int64_t)q * p.lm.sl) : 0.f;
+              for (int e = 0; e < 16; ++e) mv[e] = tile[(q0 + e) * kOwn + kl] ? 0.f : minus_inf();
+            } else {
+              const T* t16 = reinterpret_cast<const T*>(tile);
+#pragma unroll
+              for (int e = 0; e < 16; ++e) mv[e] = Elem<T>::to_f(t16[(q0 + e) * kOwn + kl]) * kLog2e;
             }
           }
         }
@@ -792,6 +824,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
           pf[x] = f2pack(p0, p1);
         }
       }
+      if constexpr (kTileMask) mbar_arrive(&bars.mask_empty[s]);  // done with the mask tile
       uint32_t pk[8];
       if (dv) {
         mbar_arrive(&bars.vec_empty[s]);
@@ -938,7 +971,10 @@ cudaError_t dq256_t(const Problem& p, cudaStream_t s) {
 
 template <typename T, bool kMasked, bool kRowBc>
 cudaError_t dkdv256_t(const Problem& p, cudaStream_t s) {
-  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv, tm;
+  memset(&tm, 0, sizeof(tm));  // not read unless the mask is staged
+  if (kMasked && !kRowBc && !make_tmap_mask(&tm, p, p.mask_kind == kMaskBool ? 1 : 2, kOwn, kStr, false))
+    return cudaErrorInvalidValue;
   if (!make_tmap_4d(&tk, p.k, kD, p.Lkv, p.Hkv, p.B, p.lk, kOwn) ||
       !make_tmap_4d(&tv, p.v, kD, p.Lkv, p.Hkv, p.B, p.lv, kOwn) ||
       !make_tmap_4d(&tdk, p.dk, kD, p.Lkv, p.Hkv, p.B, p.ldk, kOwn) ||
@@ -950,7 +986,7 @@ cudaError_t dkdv256_t(const Problem& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kKvBytes);
   if (e != cudaSuccess) return e;
   const unsigned nkt = (p.Lkv + kOwn - 1) / kOwn;
-  kern<<<4 * nkt * p.Hkv * p.B, kKvThreads, kKvBytes, s>>>(tq, tk, tv, tdo, tdk, tdv, p);
+  kern<<<4 * nkt * p.Hkv * p.B, kKvThreads, kKvBytes, s>>>(tq, tk, tv, tdo, tdk, tdv, tm, p);
   return cudaGetLastError();
 }
 
