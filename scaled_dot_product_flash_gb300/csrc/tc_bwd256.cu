@@ -4,19 +4,19 @@
 // "Implementation Notes" and "Limitations").  At D = 256 one SM's budgets (512 TMEM
 // columns, 227 KB of shared memory) shape them differently:
 //   dQ: a block owns 128 query rows of one head and streams 64-key blocks.  TMEM: dQ in
-//       256 columns, S in two 64-column buffers (→ dS), dP in 64 columns.  Shared memory:
-//       Q and dO (64 KB each), two 32 KB K stages (K lives through S and dQ) and one 32 KB
-//       V stage (224 KB).  S = Q·Kᵀ and dP = dO·Vᵀ are M = 128, N = 64 products over 16
-//       K-steps; dQ += dS·K is one M = 128, N = 256 product over 4 K-steps.
+//       256 columns, Q in 128 (the A operand of S = Q·Kᵀ) and two 64-column buffers that
+//       take S, then dP = dO·Vᵀ over it, then dS over that.  Shared memory: dO (64 KB),
+//       three K stages and two V stages (32 KB each).  S and dP are M = 128, N = 64
+//       products over 16 K-steps; dQ += dS·K is one M = 128, N = 256 product over 4.
 //   dK/dV: a block owns 128 keys of one KV head and streams 64-row query blocks of the G
 //       query heads of its group; one block of a neighbouring pair accumulates dK, the
 //       other dV, each over the full D in 256 TMEM columns.  Both compute Sᵀ = K·Qᵀ; the dK
 //       block also dPᵀ = V·dOᵀ (2.5F of MMA work in all against 3F for a split of D).
-// Warp roles as in the D <= 128 kernels: warps 0-15 element work (warp e takes TMEM lane
-// quarter e % 4 and the 16 streamed columns [16c, 16c + 16), c = e / 4, and writes its
-// packed 16-bit results over the first 8 of them), warp 16 the TMA producer, warps 17-19
-// the MMA issuers; warp 17 owns the TMEM.  Every wait is bounded, as everywhere in the
-// library.
+// Warp roles as in the D <= 128 kernels: warps 0-15 element work, warp 16 the TMA
+// producer, warps 17-19 the MMA issuers; warp 17 owns the TMEM.  The element warps form two
+// groups of 8 that take the even and the odd streamed blocks (TMEM buffer n % 2); warp e of
+// a group takes TMEM lane quarter e % 4 and 32 streamed columns, and packs its 16-bit
+// results over the first 8 of each 16.  Every wait is bounded, as everywhere in the library.
 // Attention masks: each kernel has a masked instantiation (kMasked) that adds log2e·M to
 // the log2-domain scores before the exponential, as the D <= 128 kernels do.  The dQ
 // kernel has no shared memory left for a mask tile and reads its row's 32 mask values
@@ -39,8 +39,9 @@ constexpr int kStrBytes = kStr * kD * 2;    // [64 x 256] 16-bit: 32 KB
 constexpr int kStrCb = kStr * 128;          // one 64-column block of a streamed tile
 constexpr int kProducer = 16;
 constexpr int kIssuer = 17;
-// dQ: launched at 96 registers a thread (65,536 / 640 rounded down to a multiple of 8);
-// warpgroup 4 drops to 56 and the element warpgroups rise to 104.
+// Both kernels: launched at 96 registers a thread (65,536 / 640 rounded down to a multiple
+// of 8); warpgroup 4 (producer and issuers) drops to 56 and the element warpgroups rise to
+// 104.
 constexpr int kDqThreads = 640;
 constexpr int kRegsLow = 56;
 constexpr int kRegsHigh = 104;
@@ -94,8 +95,7 @@ __device__ __forceinline__ void mma_scores256(uint32_t c_tmem, uint32_t a_s, uin
 }
 
 // The same product with A = the own tile held in TMEM (row r in lane r, elements (2i, 2i+1)
-// of D in column a_tmem + i): only B is read from shared memory, so the N = 64 product is
-// no longer bound by shared-memory bandwidth.
+// of D in column a_tmem + i): only B is read from shared memory.
 __device__ __forceinline__ void mma_scores256_ts(uint32_t c_tmem, uint32_t a_tmem, uint32_t b_s, uint32_t idesc) {
   const uint64_t bd = sdesc_sw128(b_s, 16, 1024);
 #pragma unroll
@@ -104,9 +104,9 @@ __device__ __forceinline__ void mma_scores256_ts(uint32_t c_tmem, uint32_t a_tme
 }
 
 // Acc (+)= A·B: A the packed 16-bit [128 x 64] in TMEM (K-step kk, rows [16kk, 16kk + 16)
-// of the streamed block, is element warp group kk's first 8 columns, at a_tmem + 16kk) and
-// B the columns of a streamed [64 x 256] tile from b_s on (as many 64-column blocks as the
-// instruction's N), read MN-major with K = its 64 rows.
+// of the streamed block, in columns [a_tmem + 16kk, a_tmem + 16kk + 8)) and B the columns
+// of a streamed [64 x 256] tile from b_s on (as many 64-column blocks as the instruction's
+// N), read MN-major with K = its 64 rows.
 __device__ __forceinline__ void mma_acc256(uint32_t acc_tmem, uint32_t a_tmem, uint32_t b_s, uint32_t idesc,
                                            bool first) {
   const uint64_t bd = sdesc_sw128(b_s, kStrCb, 1024);
@@ -432,24 +432,24 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 // block computes Sᵀ and dV += Pᵀ·dO.  Each accumulates its gradient over the full D in 256
 // TMEM columns; Sᵀ is computed by both (2.5F of MMA work in all where a split of D into
 // halves would take 3F).  Each block copies one owned tile into TMEM columns [384, 512)
-// (the dV block K, the dK block V) and runs that score product with A from TMEM.  Each runs as a cluster of two blocks that take the first and the
-// second half of the query blocks: the heaviest causal key tile (every query of every
-// head of the group) would otherwise set the kernel's time alone.  At the end the second
-// block writes its fp32 partial sum into the first block's shared memory, which adds it
-// to its own and stores the result.
+// (the dV block K, the dK block V) and runs that score product with A from TMEM.  Each
+// runs as a cluster of two blocks that take the first and the second half of the query
+// blocks: the heaviest causal key tile (every query of every head of the group) would
+// otherwise set the kernel's time alone.  At the end the second block writes its fp32
+// partial sum into the first block's shared memory, which adds it to its own and stores
+// the result.
 //   dK block: TMEM dK [0, 256), two 64-column buffers [256, 384) that take Sᵀ(n), then
-//     dPᵀ(n) over it once every element thread has read Sᵀ(n) (Pᵀ stays in registers), then
-//     dSᵀ(n) over that; V [384, 512).  Shared memory: K, two dO slots in the place of V once
-//     V is in TMEM, three Q slots (Q(n) is read until dK(n), late in the iteration).  Warp
-//     17 issues Sᵀ(n) into buffer n % 2 once dK(n-2) has read it, warp 18 dPᵀ(n), warp 19
-//     dK += dSᵀ(n)·Q(n).
+//     dPᵀ(n) over it once the buffer's element group has read Sᵀ(n) (Pᵀ stays in
+//     registers), then dSᵀ(n) over that; V [384, 512).  Shared memory: K, two dO slots in
+//     the place of V once V is in TMEM, three Q slots (Q(n) is read until dK(n), late in
+//     the iteration; two when mask tiles are staged).  Warp 17 issues Sᵀ(n) into buffer
+//     n % 2 once dK(n-2) has read it, warp 18 dPᵀ(n), warp 19 dK += dSᵀ(n)·Q(n).
 //   dV block: TMEM dV [0, 256), Sᵀ → Pᵀ in the two buffers [256, 384), K [384, 512).  Shared
-//     memory: K (read once, into TMEM), two dO slots, three Q slots.  Warp 17 issues Sᵀ(n)
-//     into buffer n % 2 once dV(n-2) has read it, warp 18 dV += Pᵀ(n)·dO(n); warp 19 has
-//     nothing to issue.
-// Every ring is deep enough that a load is issued about two iterations before its data is
-// needed: a TMA load of a 32 KB tile takes 1500-2000 cycles to land under this kernel's
-// load, longer than one iteration.
+//     memory: K (read once, into TMEM), two dO slots, three (or two) Q slots.  Warp 17
+//     issues Sᵀ(n) into buffer n % 2 once dV(n-2) has read it, warp 18 dV += Pᵀ(n)·dO(n);
+//     warp 19 has nothing to issue.
+// The rings let a load be issued about two iterations before its data is needed: a TMA
+// load of a 32 KB tile took 750-2000 cycles to land under this kernel's load.
 struct Kv256Bars {
   uint64_t own_full;
   uint64_t q_full[3];
@@ -457,9 +457,9 @@ struct Kv256Bars {
   uint64_t do_full[2];
   uint64_t do_empty[2];   // the MMA reading dO slot i has finished
   uint64_t vec_full[2];   // per-query vectors of slot i written (32 producer lanes)
-  uint64_t vec_empty[2];  // every element thread is done with them
+  uint64_t vec_empty[2];  // the element group of slot i is done with them
   uint64_t s_full[2];     // Sᵀ in buffer i
-  uint64_t s_read[2];     // dK blocks: every element thread has read Sᵀ from buffer i
+  uint64_t s_read[2];     // dK blocks: the element group of buffer i has read Sᵀ
   uint64_t p_ready[2];    // dV blocks: Pᵀ packed in buffer i
   uint64_t x_free[2];     // dV blocks: dV has read buffer i
   uint64_t dp_full[2];    // dK blocks: dPᵀ in buffer i
@@ -695,7 +695,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kKvThreads, 1)
         mma_commit_w(&bars.do_empty[do_slot(n)]);
       }
     } else if (role == 1) {
-      // dPᵀ(n) = V·dO(n)ᵀ over Sᵀ(n) in buffer n % 2 once every element thread has read it.
+      // dPᵀ(n) = V·dO(n)ᵀ over Sᵀ(n) in buffer n % 2 once its element group has read it.
       for (int n = 0; ok && n < total; ++n) {
         const int s = n % 2;
         if (!(ok = __all_sync(kAll, mbar_wait(&bars.do_full[do_slot(n)], do_par(n), wc) &&
