@@ -779,7 +779,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // and S never waits for a PV product that reads P from the same buffer except two tiles
 // back.  Per KV tile: S = Q·Kᵀ (16 K-steps of M = N = 128) and O += P·V (8 K-steps of
 // M = 128, N = 256).  Shared memory: Q (64 KB), one 64 KB stage for K tiles and one for V
-// tiles, and under an attention mask one [128 x 128] mask tile.
+// tiles, and under an attention mask one [128 x 128] mask tile.  The K stage is handed
+// back in its four 64-column blocks (S reads block kk / 4 in K-step kk) and the V stage in
+// its two 64-row halves (PV reads rows [16kk, 16kk + 16) in K-step kk), so the next tile's
+// first pieces are on their way while the current product still reads the rest.
 // Warp roles (256 threads): warps 0-3 softmax (one thread per query row, all 128 keys of
 // a tile, as in the D <= 128 kernel), 4 and 7 TMA producers (Q and K; mask and V), 5 S
 // issuer (owns TMEM), 6 PV issuer.
@@ -796,8 +799,10 @@ struct Fwd256Layout {
 };
 struct Fwd256Bars {
   uint64_t q_full;
-  uint64_t kv_full[k256Stages];
-  uint64_t kv_empty[k256Stages];
+  uint64_t k_full[4];   // column block cb of K(j) has landed
+  uint64_t k_empty[4];  // S(j) has read column block cb
+  uint64_t v_full[2];   // rows [64h, 64h + 64) of V(j) have landed
+  uint64_t v_empty[2];  // PV(j) has read them
   uint64_t s_full[2];   // S buffer b holds S of KV tile j with j % 2 == b
   uint64_t p_full[2];   // its P has been written
   uint64_t pv_done[2];  // PV of that tile has finished (buffer free, O updated)
@@ -840,9 +845,13 @@ __global__ void __launch_bounds__(k256Threads, 1)
   if (threadIdx.x == 0) {
     bars.abort = 0;
     mbar_init(&bars.q_full, 1);
-    for (int s = 0; s < k256Stages; ++s) {
-      mbar_init(&bars.kv_full[s], 1);
-      mbar_init(&bars.kv_empty[s], 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&bars.k_full[s], 1);
+      mbar_init(&bars.k_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars.v_full[s], 1);
+      mbar_init(&bars.v_empty[s], 1);
     }
     for (int c = 0; c < 2; ++c) {
       mbar_init(&bars.s_full[c], 1);
@@ -867,10 +876,11 @@ __global__ void __launch_bounds__(k256Threads, 1)
 
   if (warp == 4 || warp == 7) {
     // ---------------------------------------------------------------- producers
-    // Warp 4 loads Q, then K(j) into stage 0 as soon as S(j-1) has read K(j-1); warp 7
-    // loads V(j) into stage 1 as soon as PV(j-1) has read V(j-1), and before it (masked)
-    // the mask tile of KV tile j once the softmax warps have read that of tile j-1.  Two
-    // producers, so that neither kind of tile waits behind the other.
+    // Warp 4 loads Q, then each column block of K(j) into stage 0 as soon as S(j-1) has
+    // read that block of K(j-1); warp 7 loads each 64-row half of V(j) into stage 1 as
+    // soon as PV(j-1) has read that half of V(j-1), and before it (masked) the mask tile
+    // of KV tile j once the softmax warps have read that of tile j-1.  Two producers, so
+    // that neither kind of tile waits behind the other.
     if (lane == 0) {
       const int kv = warp == 4 ? 0 : 1;
       if (kv == 0) {
@@ -884,7 +894,7 @@ __global__ void __launch_bounds__(k256Threads, 1)
         prefetch_tmap(&tv);
         if (kMasked) prefetch_tmap(&tm);
       }
-      int issued = 0, m_issued = 0;
+      int piece_issued[kCB] = {0, 0, 0, 0}, m_issued = 0;  // tiles issued per K block / V half
       bool ok = true;
       for (int j = 0; ok && j < nkv; ++j) {
         if (kMasked && kv == 1) {
@@ -892,16 +902,31 @@ __global__ void __launch_bounds__(k256Threads, 1)
           load_mask_tile(sm + L::kMaskOff, &tm, &bars.mask_full, p, j * kBN, row0, h, b);
           m_issued = j + 1;
         }
-        if (!(ok = mbar_wait(&bars.kv_empty[kv], (j & 1) ^ 1, wc))) break;
         if (p.inject == 1 && kv == 0 && j == 0) continue;  // test hook: never deliver the first K tile
-        mbar_arrive_expect_tx(&bars.kv_full[kv], L::kTileBytes);
-        for (int cb = 0; cb < kCB; ++cb)
-          tma_load_4d(sm + L::kRingOff + kv * L::kTileBytes + cb * 16384, kv ? &tv : &tk, &bars.kv_full[kv],
-                      cb * 64, j * kBN, g, b);
-        issued = j + 1;
+        uint8_t* stage = sm + L::kRingOff + kv * L::kTileBytes;
+        if (kv == 0) {
+          for (int cb = 0; cb < kCB && ok; ++cb) {
+            if (!(ok = mbar_wait(&bars.k_empty[cb], (j & 1) ^ 1, wc))) break;
+            mbar_arrive_expect_tx(&bars.k_full[cb], L::kTileBytes / kCB);
+            tma_load_4d(stage + cb * 16384, &tk, &bars.k_full[cb], cb * 64, j * kBN, g, b);
+            piece_issued[cb] = j + 1;
+          }
+        } else {
+          // rows [64h, 64h + 64) of every column block: a 64-row box at row offset 64h
+          for (int hr = 0; hr < 2 && ok; ++hr) {
+            if (!(ok = mbar_wait(&bars.v_empty[hr], (j & 1) ^ 1, wc))) break;
+            mbar_arrive_expect_tx(&bars.v_full[hr], L::kTileBytes / 2);
+            for (int cb = 0; cb < kCB; ++cb)
+              tma_load_4d(stage + cb * 16384 + hr * 8192, &tv, &bars.v_full[hr], cb * 64, j * kBN + 64 * hr, g, b);
+            piece_issued[hr] = j + 1;
+          }
+        }
       }
-      if ((!ok || bars.abort) && issued > 0)
-        drain_wait(&bars.kv_full[kv], (issued - 1) & 1, 100000000ull);
+      if (!ok || bars.abort) {  // let copies still in flight land before the block exits
+        for (int x = 0; x < (kv == 0 ? kCB : 2); ++x)
+          if (piece_issued[x] > 0)
+            drain_wait(kv == 0 ? &bars.k_full[x] : &bars.v_full[x], (piece_issued[x] - 1) & 1, 100000000ull);
+      }
       if ((!ok || bars.abort) && m_issued > 0)
         drain_wait(&bars.mask_full, (m_issued - 1) & 1, 100000000ull);
     }
@@ -918,36 +943,51 @@ __global__ void __launch_bounds__(k256Threads, 1)
     for (int j = 0; ok && j < nkv; ++j) {
       const int buf = j % 2;
       if (s_issuer) {
-        // K(j) is ring item 2j, stage 0.
-        if (!(ok = __all_sync(kAll, mbar_wait(&bars.kv_full[0], j & 1, wc)))) break;
+        // K(j) in stage 0, one 64-column block at a time: K-steps 4cb .. 4cb + 3 read block
+        // cb, which is handed back as soon as they are done.
         if (j >= 2 && !(ok = __all_sync(kAll, mbar_wait(&bars.pv_done[buf], ((j - 2) / 2) & 1, wc)))) break;
-        tc_fence_after();
         const uint64_t kd = sdesc_sw128(ring_s, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-          mma_ss_w(tbase + 128 * buf, sdesc_advance(qd, off), sdesc_advance(kd, off), kIdS, kk > 0);
+        for (int cb = 0; cb < kCB; ++cb) {
+          if (!(ok = __all_sync(kAll, mbar_wait(&bars.k_full[cb], j & 1, wc)))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const uint32_t off = cb * 16384 + k4 * 32;
+            mma_ss_w(tbase + 128 * buf, sdesc_advance(qd, off), sdesc_advance(kd, off), kIdS, cb + k4 > 0);
+          }
+          mma_commit_w(&bars.k_empty[cb]);
         }
+        if (!ok) break;
         mma_commit_w(&bars.s_full[buf]);
-        mma_commit_w(&bars.kv_empty[0]);
       } else {
-        // V(j) is ring item 2j + 1, stage 1.
-        if (!(ok = __all_sync(kAll, mbar_wait(&bars.p_full[buf], (j / 2) & 1, wc) &&
-                                        mbar_wait(&bars.kv_full[1], j & 1, wc))))
-          break;
-        tc_fence_after();
+        // V(j) in stage 1, one 64-row half at a time: K-steps 4h .. 4h + 3 (and those of the
+        // remainder of P, columns [64, 128), when the tile is split) read rows [64h, 64h + 64),
+        // which are handed back as soon as they are done.
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.p_full[buf], (j / 2) & 1, wc)))) break;
+        const bool split = kMasked ? split_voted(bars.need[j % 2]) : split_tile(p, j, row0);
         const uint64_t vd = sdesc_sw128(ring_s + L::kTileBytes, 16384, 1024);
         const uint32_t s_tm = tbase + 128 * buf;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts_w(tbase + kColO, s_tm + kk * 8, sdesc_advance(vd, kk * 2048), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-        if (kMasked ? split_voted(bars.need[j % 2]) : split_tile(p, j, row0)) {  // remainder of P, columns [64, 128)
+        for (int hr = 0; hr < 2; ++hr) {
+          if (!(ok = __all_sync(kAll, mbar_wait(&bars.v_full[hr], j & 1, wc)))) break;
+          tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
-            mma_ts_w(tbase + kColO, s_tm + 64 + kk * 8, sdesc_advance(vd, kk * 2048), kIdO, 1u);
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int kk = 4 * hr + k4;
+            mma_ts_w(tbase + kColO, s_tm + kk * 8, sdesc_advance(vd, kk * 2048), kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (split) {
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+              const int kk = 4 * hr + k4;
+              mma_ts_w(tbase + kColO, s_tm + 64 + kk * 8, sdesc_advance(vd, kk * 2048), kIdO, 1u);
+            }
+          }
+          mma_commit_w(&bars.v_empty[hr]);
         }
+        if (!ok) break;
         mma_commit_w(&bars.pv_done[buf]);
-        mma_commit_w(&bars.kv_empty[1]);
       }
     }
     mma_commit_w(&bars.fin);
@@ -1079,7 +1119,7 @@ cudaError_t tc_fwd256_m(const Problem& p, cudaStream_t s) {
   CUtensorMap tq, tk, tv, to;
   if (!make_tmap_4d(&tq, p.q, 256, p.Lq, p.Hq, p.B, p.lq, kBM) || !make_tmap_4d(&to, p.out, 256, p.Lq, p.Hq, p.B, p.lo, kBM) ||
       !make_tmap_4d(&tk, p.k, 256, p.Lkv, p.Hkv, p.B, p.lk, kBN) ||
-      !make_tmap_4d(&tv, p.v, 256, p.Lkv, p.Hkv, p.B, p.lv, kBN))
+      !make_tmap_4d(&tv, p.v, 256, p.Lkv, p.Hkv, p.B, p.lv, kBN / 2))  // V in 64-row halves
     return cudaErrorInvalidValue;
   CUtensorMap tm = tq;  // unused without a mask
   if (kMasked && !make_fwd_mask_map(&tm, p)) return cudaErrorInvalidValue;
