@@ -64,7 +64,7 @@ constexpr int kProducerWarp = 16;
 constexpr int kMmaWarp = 17;
 constexpr int kRows = 128;  // rows owned by a block (keys for dK/dV, queries for dQ)
 constexpr int kBlk = 128;   // rows of the streamed operand per iteration
-constexpr int kStages = 2;  // ring depth of the streamed operand
+constexpr int kStages = 2;  // dK/dV: depth of the dO ring and of the per-query vector ring
 
 template <typename T>
 struct IsBf16 { static constexpr bool value = false; };
@@ -98,17 +98,17 @@ struct BwdLayout {
   static constexpr int kTileBytes = kRows * kCB * 64 * 2;  // one [128 x D] tile
   static constexpr int kOwnA = 0;                      // K (dK/dV) or Q (dQ)
   static constexpr int kOwnB = kTileBytes;             // V (dK/dV) or dO (dQ)
-  static constexpr int kRing = 2 * kTileBytes;         // stages of {A block, B block}
-  static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kBytes = kRing + kStages * kStageBytes;
   static constexpr int kCbStride = kRows * 128;        // one 64-column block of a tile
 };
 
 struct BwdBars {
   uint64_t own_full;
-  uint64_t ring_full[kStages];
-  uint64_t ring_empty[kStages];
+  uint64_t q_full[3];
+  uint64_t q_empty[3];        // dK(n) has read the Q slot of query block n
+  uint64_t do_full[kStages];
+  uint64_t do_empty[kStages]; // dPᵀ(n) and dV(n) have read the dO slot of block n
   uint64_t vec_full[kStages];
+  uint64_t vec_empty[kStages];  // every element thread is done with the slot's vectors
   uint64_t s_full[2];     // dK/dV: [0] only.  dQ: one per S buffer
   uint64_t dp_full;
   uint64_t p_half;        // dK/dV: Pᵀ of each warp's first 16 queries packed
@@ -129,10 +129,15 @@ struct BwdBars {
 __device__ __forceinline__ void init_bars(BwdBars& bars) {
   bars.abort = 0;
   mbar_init(&bars.own_full, 1);
+  for (int s = 0; s < 3; ++s) {
+    mbar_init(&bars.q_full[s], 1);
+    mbar_init(&bars.q_empty[s], 1);
+  }
   for (int s = 0; s < kStages; ++s) {
-    mbar_init(&bars.ring_full[s], 1);
-    mbar_init(&bars.ring_empty[s], 2);  // released by both MMA issuers
+    mbar_init(&bars.do_full[s], 1);
+    mbar_init(&bars.do_empty[s], 2);  // released by both MMA issuers
     mbar_init(&bars.vec_full[s], 32);
+    mbar_init(&bars.vec_empty[s], 512);
   }
   mbar_init(&bars.s_full[0], 1);
   mbar_init(&bars.s_full[1], 1);
@@ -150,18 +155,24 @@ __device__ __forceinline__ void init_bars(BwdBars& bars) {
   fence_mbar_init();
 }
 
-// dK/dV shared memory: the K, V and Q/dO tiles, then (masked instantiation) one [128 queries
-// x 128 keys] mask tile, then the barriers and per-query vectors.  Everything is dynamic
+// dK/dV shared memory: the K and V tiles, a ring of Q slots (three, or two in the masked
+// instantiation: Q(n) is read until dK(n), late in the iteration), two dO slots (dO(n) is
+// free once dPᵀ(n) and dV(n) have read it), then (masked instantiation) one [128 queries x
+// 128 keys] mask tile, then the barriers and per-query vectors.  Everything is dynamic
 // shared memory with no static part, whose base is the start of the block's shared window
 // (1024-byte aligned), so the 224 KB of tiles, mask and barriers need no alignment padding.
 template <int D, bool kMasked>
 struct KvSmem {
-  static constexpr int kMask = BwdLayout<D>::kBytes;
+  static constexpr int kQSlots = kMasked ? 2 : 3;
+  static constexpr int kQ = 2 * BwdLayout<D>::kTileBytes;
+  static constexpr int kDo = kQ + kQSlots * BwdLayout<D>::kTileBytes;
+  static constexpr int kMask = kDo + kStages * BwdLayout<D>::kTileBytes;
   static constexpr int kMaskBytes = kMasked ? kBlk * kRows * 2 : 0;  // 16-bit or byte elements
   static constexpr int kBars = kMask + kMaskBytes;
   static constexpr int kBytes = kBars + (int)sizeof(BwdBars);
 };
 static_assert(KvSmem<128, true>::kBytes <= 227 * 1024, "dK/dV shared memory exceeds the per-block limit");
+static_assert(KvSmem<128, false>::kBytes <= 227 * 1024, "dK/dV shared memory exceeds the per-block limit");
 
 // Issues C[tmem] = A·Bᵀ for two [128 x D] K-major tiles in shared memory (N = 128).
 // Called by all 32 lanes of the issuing warp; one elected lane issues.
@@ -259,22 +270,33 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         tma_load_4d(sm + L::kOwnB + cb * L::kCbStride, &tv, &bars.own_full, cb * 64, j0, g, b);
       }
     }
-    int issued = 0;
+    // Per query block n: Q(n) into its slot once dK of the block that last used it has read
+    // it, dO(n) into its slot once dPᵀ and dV of that block have, the mask tile (masked),
+    // then the per-query vectors once the element threads are done with those of n - 2.
+    int q_issued = 0, do_issued = 0, m_issued = 0;
     bool ok = true;
     for (int n = 0; ok && n < total; ++n) {
-      const int s = n % kStages;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars.ring_empty[s], ((n / kStages) & 1) ^ 1, wc));
-      if (!ok) break;
+      const int s = n % kStages, qs = n % SM::kQSlots;
       const int h = g * p.G + n / nqb;
       const int i0 = i_begin + (n % nqb) * kBlk;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.q_empty[qs], ((n / SM::kQSlots) & 1) ^ 1, wc));
+      if (!ok) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars.ring_full[s], 2 * L::kTileBytes);
-        uint8_t* st = sm + L::kRing + s * L::kStageBytes;
-        for (int cb = 0; cb < kCB; ++cb) {
-          tma_load_4d(st + cb * L::kCbStride, &tq, &bars.ring_full[s], cb * 64, i0, h, b);
-          tma_load_4d(st + L::kTileBytes + cb * L::kCbStride, &tdo, &bars.ring_full[s], cb * 64, i0, h, b);
-        }
+        mbar_arrive_expect_tx(&bars.q_full[qs], L::kTileBytes);
+        for (int cb = 0; cb < kCB; ++cb)
+          tma_load_4d(sm + SM::kQ + qs * L::kTileBytes + cb * L::kCbStride, &tq, &bars.q_full[qs], cb * 64, i0, h,
+                      b);
       }
+      q_issued = n + 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.do_empty[s], ((n / kStages) & 1) ^ 1, wc));
+      if (!ok) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars.do_full[s], L::kTileBytes);
+        for (int cb = 0; cb < kCB; ++cb)
+          tma_load_4d(sm + SM::kDo + s * L::kTileBytes + cb * L::kCbStride, &tdo, &bars.do_full[s], cb * 64, i0,
+                      h, b);
+      }
+      do_issued = n + 1;
       if (kMasked) {
         // The query block's mask tile, once every element warp has read the previous one.
         if (n > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bars.mask_free, (n - 1) & 1, wc));
@@ -286,8 +308,11 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           tma_load_4d(sm + SM::kMask, &tm, &bars.mask_full, j0, row_bc ? 0 : i0, p.lm.sh == 0 ? 0 : h,
                       p.lm.sb == 0 ? 0 : b);
         }
+        m_issued = n + 1;
       }
       // Per-query vectors, negated for the packed math of the element warps.
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars.vec_empty[s], ((n / kStages) & 1) ^ 1, wc));
+      if (!ok) break;
       const float* lsep = p.lse + q_row(p, b, h, 0);
       const float* dlp = p.delta + q_row(p, b, h, 0);
 #pragma unroll
@@ -298,12 +323,13 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         bars.ndelta[s][e] = i < p.Lq ? -dlp[i] : 0.f;
       }
       mbar_arrive(&bars.vec_full[s]);
-      issued = n + 1;
     }
-    if (lane == 0 && (!ok || bars.abort)) {
-      for (int n = max(0, issued - kStages); n < issued; ++n)
-        drain_wait(&bars.ring_full[n % kStages], (n / kStages) & 1, 100000000ull);
-      if (kMasked && issued > 0) drain_wait(&bars.mask_full, (issued - 1) & 1, 100000000ull);
+    if (lane == 0 && (!ok || bars.abort)) {  // let copies still in flight land before the block exits
+      for (int n = max(0, q_issued - SM::kQSlots); n < q_issued; ++n)
+        drain_wait(&bars.q_full[n % SM::kQSlots], (n / SM::kQSlots) & 1, 100000000ull);
+      for (int n = max(0, do_issued - kStages); n < do_issued; ++n)
+        drain_wait(&bars.do_full[n % kStages], (n / kStages) & 1, 100000000ull);
+      if (kMasked && m_issued > 0) drain_wait(&bars.mask_full, (m_issued - 1) & 1, 100000000ull);
     }
   } else if (warp == kKvMmaWarp || warp == kKvMmaWarp + 1) {
     // ---------------------------------------------------------------- MMA issuers
@@ -317,50 +343,55 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     bool ok = __all_sync(kAll, mbar_wait(&bars.own_full, 0, wc));
     tc_fence_after();
     const uint32_t k_s = smem_u32(sm + L::kOwnA), v_s = smem_u32(sm + L::kOwnB);
-    auto stage_q = [&](int n) { return smem_u32(sm + L::kRing + (n % kStages) * L::kStageBytes); };
+    constexpr int kQs = SM::kQSlots;
+    auto q_slot = [&](int n) { return smem_u32(sm + SM::kQ + (n % kQs) * L::kTileBytes); };
+    auto do_slot = [&](int n) { return smem_u32(sm + SM::kDo + (n % kStages) * L::kTileBytes); };
     if (chain_x) {
       if (ok && total > 0) {
-        ok = __all_sync(kAll, mbar_wait(&bars.ring_full[0], 0, wc));
+        ok = __all_sync(kAll, mbar_wait(&bars.q_full[0], 0, wc));
         if (ok) {
           tc_fence_after();
-          mma_scores<D>(tbase + kColX, k_s, stage_q(0), kIdS);  // Sᵀ(0) = K·Q(0)ᵀ
+          mma_scores<D>(tbase + kColX, k_s, q_slot(0), kIdS);  // Sᵀ(0) = K·Q(0)ᵀ
           mma_commit_w(&bars.s_full[0]);
         }
       }
       for (int n = 0; ok && n < total; ++n) {
-        const uint32_t q_s = stage_q(n), do_s = q_s + L::kTileBytes;
+        const uint32_t q_s = q_slot(n), do_s = do_slot(n);
         // dV += Pᵀ·dO in two halves: the K-steps of the queries whose Pᵀ the element warps
         // write first, then the rest, so that dV(n) is half done when the Pᵀ pass ends.
-        if (!(ok = __all_sync(kAll, mbar_wait(&bars.p_half, n & 1, wc)))) break;
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.p_half, n & 1, wc) &&
+                                        mbar_wait(&bars.do_full[n % kStages], (n / kStages) & 1, wc))))
+          break;
         tc_fence_after();
         mma_accumulate_half<D, 32>(tbase + kColDv, tbase + kColX, do_s, kIdAcc, n == 0, 0);
         if (!(ok = __all_sync(kAll, mbar_wait(&bars.p_ready, n & 1, wc)))) break;
         tc_fence_after();
         mma_accumulate_half<D, 32>(tbase + kColDv, tbase + kColX, do_s, kIdAcc, n == 0, 1);
         mma_commit_w(&bars.x_free);
+        mma_commit_w(&bars.do_empty[n % kStages]);  // one of the slot's two arrivals
         if (n + 1 < total) {
-          if (!(ok = __all_sync(kAll, mbar_wait(&bars.ring_full[(n + 1) % kStages], ((n + 1) / kStages) & 1, wc) &&
+          if (!(ok = __all_sync(kAll, mbar_wait(&bars.q_full[(n + 1) % kQs], ((n + 1) / kQs) & 1, wc) &&
                                           mbar_wait(&bars.x_free, n & 1, wc))))
             break;
           tc_fence_after();
-          mma_scores<D>(tbase + kColX, k_s, stage_q(n + 1), kIdS);  // Sᵀ(n+1)
+          mma_scores<D>(tbase + kColX, k_s, q_slot(n + 1), kIdS);  // Sᵀ(n+1)
           mma_commit_w(&bars.s_full[0]);
         }
         if (!(ok = __all_sync(kAll, mbar_wait(&bars.ds_ready, n & 1, wc)))) break;
         tc_fence_after();
         mma_accumulate<D, 32>(tbase + kColDk, tbase + kColY, q_s, kIdAcc, n == 0);  // dK += dSᵀ·Q
         mma_commit_w(&bars.y_free);
-        mma_commit_w(&bars.ring_empty[n % kStages]);  // one of the stage's two arrivals
+        mma_commit_w(&bars.q_empty[n % kQs]);
       }
     } else {
       for (int n = 0; ok && n < total; ++n) {
-        const uint32_t do_s = stage_q(n) + L::kTileBytes;
-        if (!(ok = __all_sync(kAll, mbar_wait(&bars.ring_full[n % kStages], (n / kStages) & 1, wc)))) break;
+        const uint32_t do_s = do_slot(n);
+        if (!(ok = __all_sync(kAll, mbar_wait(&bars.do_full[n % kStages], (n / kStages) & 1, wc)))) break;
         if (n > 0 && !(ok = __all_sync(kAll, mbar_wait(&bars.y_free, (n - 1) & 1, wc)))) break;
         tc_fence_after();
         mma_scores<D>(tbase + kColY, v_s, do_s, kIdS);  // dPᵀ = V·dOᵀ
         mma_commit_w(&bars.dp_full);
-        mma_commit_w(&bars.ring_empty[n % kStages]);
+        mma_commit_w(&bars.do_empty[n % kStages]);  // one of the slot's two arrivals
       }
     }
     mma_commit_w(&bars.acc_done);
@@ -476,6 +507,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         }
         tmem_st16(y_addr, dk);
       }
+      mbar_arrive(&bars.vec_empty[s]);  // done with this block's lse and δ
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars.ds_ready);
