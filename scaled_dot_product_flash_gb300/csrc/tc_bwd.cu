@@ -13,9 +13,11 @@
 // two halves (each warp's first 16 queries, then the rest), so dV starts over the first
 // half while the second is computed and runs while dSᵀ is computed, and Sᵀ of the next
 // block starts as soon as dV has consumed Pᵀ (the MMA order is dV(n), Sᵀ(n+1), dK(n),
-// dPᵀ(n+1)).  dSᵀ
-// is formed from Pᵀ in fp32 (dV uses Pᵀ rounded to the element type, as the A operand of
-// a 16-bit MMA must be).
+// dPᵀ(n+1)).  dSᵀ is formed from Pᵀ in fp32 (dV uses Pᵀ rounded to the element type, as
+// the A operand of a 16-bit MMA must be).  Q and dO tiles stream through separate rings:
+// Q(n) is read until dK(n), late in the iteration, dO(n) only until dPᵀ(n) and dV(n), so
+// Q has three slots (two in the masked instantiation, whose mask tile takes the third's
+// place) and dO two.
 //
 // dQ kernel: one block owns 128 query rows of one head and loops over 128-row KV blocks:
 //   S = Q·Kᵀ, dP = dO·Vᵀ, P = exp2(c·S − log2e·lse_i), dS = P∘(dP − δ_i), dQ += dS·K,
