@@ -212,6 +212,17 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         tma_load_4d(sm + kDqV + cb * kOwnCb, &tq, &bars.own_full, cb * 64, i0, h, b);
         tma_load_4d(sm + kDqDo + cb * kOwnCb, &tdo, &bars.own_full, cb * 64, i0, h, b);
       }
+      // The block one wave later (about num_sms blocks on) starts when some block ends:
+      // bring its Q and dO tiles into L2 now, so that its first loads come from L2.
+      if (p.num_sms > 0 && blockIdx.x + p.num_sms < gridDim.x) {
+        const int nb = blockIdx.x + p.num_sms;
+        const int nu = nb % units, nrank = nb / units;
+        const int ni0 = (p.causal ? nqt - 1 - nrank : nrank) * kOwn;
+        for (int cb = 0; cb < 4; ++cb) {
+          tma_prefetch_l2_4d(&tq, cb * 64, ni0, nu % p.Hq, nu / p.Hq);
+          tma_prefetch_l2_4d(&tdo, cb * 64, ni0, nu % p.Hq, nu / p.Hq);
+        }
+      }
       int k_issued = 0, v_issued = 0;
       bool ok = true;
       for (int n = 0; ok && n < total; ++n) {

@@ -890,6 +890,14 @@ __global__ void __launch_bounds__(k256Threads, 1)
         mbar_arrive_expect_tx(&bars.q_full, L::kTileBytes);
         for (int cb = 0; cb < kCB; ++cb)
           tma_load_4d(sm + L::kQOff + cb * 16384, &tq, &bars.q_full, cb * 64, row0, h, b);
+        // The block one wave later (about num_sms blocks on) starts when some block ends:
+        // bring its Q tile into L2 now, so that its first load comes from L2, not HBM.
+        if (p.num_sms > 0 && blockIdx.x + p.num_sms < gridDim.x) {
+          const int nb = blockIdx.x + p.num_sms;
+          const int nu = nb % units, nrank = nb / units;
+          const int nrow0 = (p.causal ? nqt - 1 - nrank : nrank) * kBM;
+          for (int cb = 0; cb < kCB; ++cb) tma_prefetch_l2_4d(&tq, cb * 64, nrow0, nu % p.Hq, nu / p.Hq);
+        }
       } else {
         prefetch_tmap(&tv);
         if (kMasked) prefetch_tmap(&tm);
