@@ -163,18 +163,20 @@ __device__ __forceinline__ void init_bars(BwdBars& bars) {
 // 128 keys] mask tile, then the barriers and per-query vectors.  Everything is dynamic
 // shared memory with no static part, whose base is the start of the block's shared window
 // (1024-byte aligned), so the 224 KB of tiles, mask and barriers need no alignment padding.
-template <int D, bool kMasked>
+template <int D, bool kMasked, bool kRowBc = false>
 struct KvSmem {
-  static constexpr int kQSlots = kMasked ? 2 : 3;
+  static constexpr bool kTileMask = kMasked && !kRowBc;  // a staged mask tile
+  static constexpr int kQSlots = kTileMask ? 2 : 3;
   static constexpr int kQ = 2 * BwdLayout<D>::kTileBytes;
   static constexpr int kDo = kQ + kQSlots * BwdLayout<D>::kTileBytes;
   static constexpr int kMask = kDo + kStages * BwdLayout<D>::kTileBytes;
-  static constexpr int kMaskBytes = kMasked ? kBlk * kRows * 2 : 0;  // 16-bit or byte elements
+  static constexpr int kMaskBytes = kTileMask ? kBlk * kRows * 2 : 0;  // 16-bit or byte elements
   static constexpr int kBars = kMask + kMaskBytes;
   static constexpr int kBytes = kBars + (int)sizeof(BwdBars);
 };
 static_assert(KvSmem<128, true>::kBytes <= 227 * 1024, "dK/dV shared memory exceeds the per-block limit");
 static_assert(KvSmem<128, false>::kBytes <= 227 * 1024, "dK/dV shared memory exceeds the per-block limit");
+static_assert(KvSmem<128, true, true>::kBytes <= 227 * 1024, "dK/dV shared memory exceeds the per-block limit");
 
 // Issues C[tmem] = A·Bᵀ for two [128 x D] K-major tiles in shared memory (N = 128).
 // Called by all 32 lanes of the issuing warp; one elected lane issues.
@@ -213,7 +215,10 @@ __device__ __forceinline__ void mma_accumulate_half(uint32_t acc_tmem, uint32_t 
 }
 
 // ================================================================== dK / dV
-template <typename T, int D, bool kMasked>
+// kRowBc (with kMasked): the mask has one row for every query (row stride 0, the
+// [B, 1, 1, Lkv] key-padding form); each element thread reads its key's value from global
+// memory once per query block, so no mask tile is staged and Q keeps three slots.
+template <typename T, int D, bool kMasked, bool kRowBc>
 __global__ void __launch_bounds__(kKvThreads, 1)
     tc_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -226,7 +231,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   constexpr uint32_t kIdAcc = idesc_f16(kRows, D, kBf16, false, true);
   // TMEM columns: dV, dK, Sᵀ (→ Pᵀ), dPᵀ (→ dSᵀ)
   constexpr uint32_t kColDv = 0, kColDk = 128, kColX = 256, kColY = 384;
-  using SM = KvSmem<D, kMasked>;
+  using SM = KvSmem<D, kMasked, kRowBc>;
+  constexpr bool kTileMask = SM::kTileMask;
   extern __shared__ unsigned char smem_raw[];
   // The layout assumes a 1024-byte aligned base (TMA's 128-byte swizzle and the MMA
   // descriptors need it); should a launch ever place it elsewhere, the block reports an
@@ -299,7 +305,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                       h, b);
       }
       do_issued = n + 1;
-      if (kMasked) {
+      if (kTileMask) {
         // The query block's mask tile, once every element warp has read the previous one.
         if (n > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bars.mask_free, (n - 1) & 1, wc));
         if (!ok) break;
@@ -331,7 +337,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         drain_wait(&bars.q_full[n % SM::kQSlots], (n / SM::kQSlots) & 1, 100000000ull);
       for (int n = max(0, do_issued - kStages); n < do_issued; ++n)
         drain_wait(&bars.do_full[n % kStages], (n / kStages) & 1, 100000000ull);
-      if (kMasked && m_issued > 0) drain_wait(&bars.mask_full, (m_issued - 1) & 1, 100000000ull);
+      if (kTileMask && m_issued > 0) drain_wait(&bars.mask_full, (m_issued - 1) & 1, 100000000ull);
     }
   } else if (warp == kKvMmaWarp || warp == kKvMmaWarp + 1) {
     // ---------------------------------------------------------------- MMA issuers
@@ -413,7 +419,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       const int i0 = i_begin + (n % nqb) * kBlk + 32 * c;  // first query of this warp's columns
       ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[0], n & 1, wc) &&
                                        mbar_wait(&bars.vec_full[s], (n / kStages) & 1, wc) &&
-                                       (!masked || mbar_wait(&bars.mask_full, n & 1, wc)));
+                                       (!kTileMask || mbar_wait(&bars.mask_full, n & 1, wc)));
       if (!ok) break;
       tc_fence_after();
       const int ic = i0 + p.coff;  // key j is hidden from query i0 + q when j > ic + q
@@ -423,11 +429,17 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       // Pᵀ for this warp's 32 queries from one TMEM load; the packed 16-bit values go over
       // the first 16 of its own Sᵀ columns for dV, and Pᵀ stays in registers in fp32 for dSᵀ.
       uint64_t pf[16];  // fp32 pairs
+      uint64_t mrow = 0;  // one-row mask: log2e·M of this key, in both halves
       {
         uint32_t sr[32];
         tmem_ld32(x_addr, sr);
         tmem_ld_wait(sr);
-        if constexpr (masked) {
+        if constexpr (masked && kRowBc) {
+          // The one mask value of this key for every query (0 past Lkv: those keys' rows
+          // are clipped) goes into the per-query constant below: c·s + (−log2e·lse + log2e·M).
+          const float mv = j < p.Lkv ? mask_log2<T>(p, row_off(p.lm, b, g * p.G + n / nqb, 0) + j) : 0.f;
+          mrow = f2pack(mv, mv);
+        } else if constexpr (masked) {
           // c·s + log2e·M for this key against the warp's queries, M read from the block's
           // mask tile in shared memory (row q, key k at element 128q + k; one row when the
           // mask is broadcast over queries).  Rows past Lq and keys past Lkv were filled with
@@ -462,7 +474,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars.mask_free);  // this warp is done with the mask tile
         }
-        const uint64_t ce = masked ? f2pack(1.f, 1.f) : cc;
+        const uint64_t ce = kTileMask ? f2pack(1.f, 1.f) : cc;
         // Two halves of 16 queries, each stored as soon as it is packed: the first half
         // lets the dV product start (p_half) while the second is computed.
 #pragma unroll
@@ -472,7 +484,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           for (int e8 = 0; e8 < 8; ++e8) {
             const int e = 8 * hf + e8;
             float p0, p1;
-            ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), ce, nl2[e]), p0, p1);
+            const uint64_t nle = kRowBc ? fadd2(nl2[e], mrow) : nl2[e];
+            ex2_pair(ffma2(f2pack(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), ce, nle), p0, p1);
             if (diag) {
               if (j > ic + 2 * e) p0 = 0.f;
               if (j > ic + 2 * e + 1) p1 = 0.f;
@@ -886,11 +899,18 @@ template <typename T, int D>
 cudaError_t dkdv_t(const Problem& p, cudaStream_t s) {
   Maps m;
   if (!make_maps(p, D, &m)) return cudaErrorInvalidValue;
-  CUtensorMap tm = m.k;  // unused without a mask
-  if (p.mask && !make_tmap_mask(&tm, p, p.mask_kind == kMaskBool ? 1 : 2, kRows, p.lm.sl == 0 ? 1 : kBlk, false))
+  // A mask with one row for every query is read from global memory (no tile); any other
+  // mask is staged in [128 x 128] tiles.
+  const bool row_mask = p.mask && p.lm.sl == 0;
+  CUtensorMap tm = m.k;  // unused without a staged mask
+  if (p.mask && !row_mask && !make_tmap_mask(&tm, p, p.mask_kind == kMaskBool ? 1 : 2, kRows, kBlk, false))
     return cudaErrorInvalidValue;
-  const int smem = p.mask ? KvSmem<D, true>::kBytes : KvSmem<D, false>::kBytes;
-  auto kern = p.mask ? tc_dkdv_kernel<T, D, true> : tc_dkdv_kernel<T, D, false>;
+  const int smem = row_mask ? KvSmem<D, true, true>::kBytes
+                   : p.mask ? KvSmem<D, true>::kBytes
+                            : KvSmem<D, false>::kBytes;
+  auto kern = row_mask ? tc_dkdv_kernel<T, D, true, true>
+              : p.mask ? tc_dkdv_kernel<T, D, true, false>
+                       : tc_dkdv_kernel<T, D, false, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned nkt = (p.Lkv + kRows - 1) / kRows;
