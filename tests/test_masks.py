@@ -46,7 +46,16 @@ def make_mask(kind, shape, seed, dtype):
         for b in range(B):
             m[b, :, :, :max(1, Lkv - 37 * (b + 1))] = True
         return torch.from_numpy(m), m
-    if kind == "additive":
+    if kind == "headrow":
+        # one row per (batch, head), every query sees it: row stride 0, head stride nonzero
+        m = rng.random((B, Hq, 1, Lkv)) < 0.8
+        m[..., 0] = True
+        return torch.from_numpy(m), m
+    if kind == "addrow":
+        m = (rng.standard_normal((1, Hq, 1, Lkv)) * 2.0).astype(np.float32)
+        m[rng.random(m.shape) < 0.2] = -np.inf
+        m[..., 0] = 0.0
+    elif kind == "additive":
         m = (rng.standard_normal((1, Hq, Lq, Lkv)) * 2.0).astype(np.float32)
         m[rng.random(m.shape) < 0.2] = -np.inf
         m[0, Hq - 1, Lq // 2] = -np.inf
@@ -111,6 +120,11 @@ CASES = [
     (Shape(1, 4, 2, 50, 77, 256), "f32", False, _lib.PATH_AUTO, "padding"),      # D = 256, CUDA cores
     (Shape(2, 4, 2, 260, 520, 128), "bf16", False, _lib.PATH_AUTO, "sparse"),    # few keys a row, MMA
     (Shape(1, 4, 2, 130, 400, 256), "bf16", False, _lib.PATH_AUTO, "sparse"),    # few keys a row, D = 256
+    # one mask row for every query (row stride 0): dK/dV reads it per key, no mask tile
+    (Shape(2, 4, 2, 300, 300, 128), "bf16", False, _lib.PATH_AUTO, "padding"),   # key padding, D = 128
+    (Shape(2, 8, 2, 200, 330, 128), "bf16", True, _lib.PATH_AUTO, "headrow"),    # one row per head
+    (Shape(1, 4, 1, 150, 260, 64), "f16", False, _lib.PATH_AUTO, "addrow"),      # additive row, G = 4
+    (Shape(1, 4, 2, 130, 200, 256), "bf16", True, _lib.PATH_AUTO, "headrow"),    # D = 256
 ]
 
 
