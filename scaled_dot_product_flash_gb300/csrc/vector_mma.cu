@@ -375,46 +375,81 @@ cudaError_t vec_mma_fwd_any(const Problem& p, cudaStream_t s) {
 
 
 // ------------------------------------------------------------------ backward
-// Per 64-key tile (keys owned by this block; all G·Lq rows of the group):
-//   phase A (warp w: keys [16w, 16w+16)): S = Q·Kᵀ, dP = dO·Vᵀ on mma.sync;
-//            P = exp2(c·S − log2e·lse), dS = P∘(dP − δ) → shared memory (16-bit)
-//   phase C (warp w): dV = Pᵀ·dO and dK = scale·dSᵀ·Q for keys [16w, 16w+16), complete
-//            for these keys (every row of the group is here) and stored at once;
-//            dQ[:, w·D/4 : (w+1)·D/4) += dS·K accumulated in registers across tiles.
-// The dQ partials of the cluster's blocks are summed through distributed shared memory.
-constexpr int kBwdRing = 2;
+// Eight warps; warp w takes key slice q = w % 4 (keys [16q, 16q+16) of every tile) and
+// half h = w / 4.  Per 64-key tile (keys owned by this block; all G·Lq rows of the group):
+//   phase A: warp (q, 1) computes dP = dO·Vᵀ and hands its fp32 fragments to warp (q, 0)
+//            through shared memory (a 64-thread named barrier; the hand-off buffer lies
+//            over the P and dS buffers, so the four (q, 0) warps meet at a 128-thread
+//            barrier before they write P and dS); warp (q, 0) computes S = Q·Kᵀ and
+//            P = exp2(c·S − log2e·lse) meanwhile, then dS = P∘(dP − δ), and writes P and
+//            dS (16-bit) to shared memory;
+//   phase C: warp (q, 0) computes dV = Pᵀ·dO and warp (q, 1) dK = scale·dSᵀ·Q for the
+//            slice's keys, complete (every row of the group is here) and stored at once;
+//            warp (q, h) adds dS·K over keys [32h, 32h+32) of the tile to its dQ partial
+//            for dims [q·D/4, (q+1)·D/4), kept in registers across tiles.
+// The two key halves' dQ partials and the cluster's blocks are summed through distributed
+// shared memory, in a fixed order.  Splitting each slice over two warps doubles the warps
+// that hide the shared-memory and MMA latencies of a tile.  The K/V ring has three stages
+// with up to 16 rows and two with 32, the most that keeps two blocks on an SM.
+constexpr int kBwdWarps = 8;
+
+// Named barrier 1 + q (immediate ids, so the block reserves six barriers, not sixteen)
+// between the two warps of key slice q: the dP warp arrives, the P warp waits.
+template <bool kSync>
+__device__ __forceinline__ void pair_bar(int q) {
+#define SDPA_PAIR_BAR(ID)                                                  \
+  if (kSync) asm volatile("bar.sync " #ID ", 64;" ::: "memory");           \
+  else asm volatile("bar.arrive " #ID ", 64;" ::: "memory");
+  switch (q) {
+    case 0: SDPA_PAIR_BAR(1) break;
+    case 1: SDPA_PAIR_BAR(2) break;
+    case 2: SDPA_PAIR_BAR(3) break;
+    default: SDPA_PAIR_BAR(4) break;
+  }
+#undef SDPA_PAIR_BAR
+}
+// Named barrier 5: the four P warps (w < 4).
+__device__ __forceinline__ void p_warps_bar() { asm volatile("bar.sync 5, 128;" ::: "memory"); }
 
 template <int D, int MT>
 struct VbLayout {
+  static constexpr int kRing = MT == 1 ? 3 : 2;           // K/V ring stages
   static constexpr int kTileBytes = kKeys * D * 2;
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kRows = 16 * MT;
   static constexpr int kRowStride = (D + 8) * 2;          // padded: conflict-free ldmatrix
   static constexpr int kPStride = (kKeys + 8) * 2;
-  static constexpr int kQ = kBwdRing * kStageBytes;       // [rows][D+8] 16-bit
+  static constexpr int kQ = kRing * kStageBytes;          // [rows][D+8] 16-bit
   static constexpr int kDo = kQ + kRows * kRowStride;
   static constexpr int kP = kDo + kRows * kRowStride;     // [rows][64+8] 16-bit
   static constexpr int kDs = kP + kRows * kPStride;
   static constexpr int kVec = kDs + kRows * kPStride;     // nlse2[rows], ndelta[rows]
   static constexpr int kBytes = kVec + 2 * kRows * 4;
-  static constexpr int kDq = 0;                           // after the loop: [rows][D] fp32
-  static_assert(kRows * D * 4 <= kBwdRing * kStageBytes, "dQ merge buffer must fit in the ring");
+  static constexpr int kDpFrag = MT * 2 * 4 * 32;         // fp32 dP fragments of one key slice
+  static constexpr int kDp = kP;                          // [4 slices][MT][2][4][32 lanes] fp32, over P and dS
+  static constexpr int kDq = 0;                           // after the loop: [2 halves][rows][D] fp32
+  static_assert(4 * kDpFrag * 4 <= 2 * kRows * kPStride, "dP hand-off must fit over P and dS");
+  static_assert(2 * kRows * D * 4 <= kRing * kStageBytes, "dQ merge buffer must fit in the ring");
+  // dynamic bytes + alignment slack + the 1 KB the SM reserves per block + static barriers
+  static_assert(2 * (kBytes + 1024 + 1024 + 64) <= 233472, "two blocks per SM");
 };
 
 template <typename T, int D, int MT>
-__global__ void __launch_bounds__(128) vec_mma_bwd_kernel(const __grid_constant__ CUtensorMap tk,
+__global__ void __launch_bounds__(256, 2) vec_mma_bwd_kernel(const __grid_constant__ CUtensorMap tk,
                                                          const __grid_constant__ CUtensorMap tv, Problem p,
                                                          int chunk) {
   using L = VbLayout<D, MT>;
-  constexpr int kWarps = 4;
+  constexpr int kWarps = kBwdWarps;
   extern __shared__ unsigned char smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int kBwdRing = L::kRing;
   __shared__ uint64_t full[kBwdRing], empty[kBwdRing];
   __shared__ int abort_flag;
   cg::cluster_group cluster = cg::this_cluster();
   const int c = (int)cluster.block_rank();
   const int b = blockIdx.z, g = blockIdx.y;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int q4 = warp % 4, half = warp / 4;  // key slice, and S/P/dV (0) or dP/dK (1)
   const int R = p.G * p.Lq;
   const int kv_end = p.causal ? min(p.Lkv, p.Lq + p.coff) : p.Lkv;
   const int j_begin = c * chunk, j_own_end = min(p.Lkv, j_begin + chunk);
@@ -499,60 +534,102 @@ __global__ void __launch_bounds__(128) vec_mma_bwd_kernel(const __grid_constant_
   for (int t = 0; t < ntiles; ++t) {
     const int s = t % kBwdRing;
     ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (t / kBwdRing) & 1, wc));
-    if (!ok) break;
+    // every warp leaves together: a warp of a key slice must not wait at the pair barrier
+    // for a partner that gave up
+    if (__syncthreads_or(!ok)) {
+      ok = false;
+      break;
+    }
     const uint32_t kt = ring + s * L::kStageBytes, vt = kt + L::kTileBytes;
     const int tile_key0 = j_begin + t * kKeys;
-    // ---- phase A: S, dP for keys [16w, 16w+16) of the tile, all rows
+    // ---- phase A: warp (q, 0) S and P, warp (q, 1) dP, for keys [16q, 16q+16), all rows
+    float* dpf = reinterpret_cast<float*>(sm + L::kDp) + q4 * L::kDpFrag;
+    float acc2[MT][2][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
-      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      float dp[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) acc2[mt][nt][0] = acc2[mt][nt][1] = acc2[mt][nt][2] = acc2[mt][nt][3] = 0.f;
+      const uint32_t a_s = half == 0 ? qs : dos, b_t = half == 0 ? kt : vt;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const int arow = 16 * mt + (mm % 2) * 8 + (lane % 8), acol = 16 * kk + (mm / 2) * 8;
-        uint32_t qa[4], da[4];
-        ldsm_x4(qs + arow * L::kRowStride + acol * 2, qa[0], qa[1], qa[2], qa[3]);
-        ldsm_x4(dos + arow * L::kRowStride + acol * 2, da[0], da[1], da[2], da[3]);
-        const int key = 16 * warp + (mm / 2) * 8 + (lane % 8);
+        uint32_t a[4];
+        ldsm_x4(a_s + arow * L::kRowStride + acol * 2, a[0], a[1], a[2], a[3]);
+        const int key = 16 * q4 + (mm / 2) * 8 + (lane % 8);
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(swz<D>(kt, key, 2 * kk + (mm % 2)), b0, b1, b2, b3);
-        mma16816<T>(sc[0], qa, b0, b1);
-        mma16816<T>(sc[1], qa, b2, b3);
-        ldsm_x4(swz<D>(vt, key, 2 * kk + (mm % 2)), b0, b1, b2, b3);
-        mma16816<T>(dp[0], da, b0, b1);
-        mma16816<T>(dp[1], da, b2, b3);
+        ldsm_x4(swz<D>(b_t, key, 2 * kk + (mm % 2)), b0, b1, b2, b3);
+        mma16816<T>(acc2[mt][0], a, b0, b1);
+        mma16816<T>(acc2[mt][1], a, b2, b3);
       }
-      const int ra = 16 * mt + lane / 4, rb = ra + 8;
-      const float nla = nlse2[ra], nlb = nlse2[rb], nda = ndelta[ra], ndb = ndelta[rb];
-      const int ia = ra < R ? ra % p.Lq : 0, ib = rb < R ? rb % p.Lq : 0;
+    }
+    if (half == 1) {
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int kl = 16 * warp + 8 * nt + 2 * (lane % 4);  // key within the tile
-        float pv[4], dsv[4];
+      for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = tile_key0 + kl + (e & 1);
-          const bool first = e < 2;
-          const bool vis = j < j_end && (!p.causal || j <= (first ? ia : ib) + p.coff);
-          float x = fmaf(sc[nt][e], c2, first ? nla : nlb);
-          if (vis && p.mask && (first ? ra : rb) < R) {
-            const int rr = first ? ra : rb;
-            const float mv = mask_log2<T>(p, row_off(p.lm, b, g * p.G + rr / p.Lq, rr % p.Lq) + j);
-            x = fmaf(sc[nt][e], c2, mv) + (first ? nla : nlb);
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dpf[((mt * 2 + nt) * 4 + e) * 32 + lane] = acc2[mt][nt][e];
+      pair_bar<false>(q4);
+    } else {
+      // P from S in place, while the partner warp finishes dP
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const int ra = 16 * mt + lane / 4, rb = ra + 8;
+        const float nla = nlse2[ra], nlb = nlse2[rb];
+        const int ia = ra < R ? ra % p.Lq : 0, ib = rb < R ? rb % p.Lq : 0;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int kl = 16 * q4 + 8 * nt + 2 * (lane % 4);  // key within the tile
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = tile_key0 + kl + (e & 1);
+            const bool first = e < 2;
+            const bool vis = j < j_end && (!p.causal || j <= (first ? ia : ib) + p.coff);
+            const float sc = acc2[mt][nt][e];
+            float x = fmaf(sc, c2, first ? nla : nlb);
+            if (vis && p.mask && (first ? ra : rb) < R) {
+              const int rr = first ? ra : rb;
+              const float mv = mask_log2<T>(p, row_off(p.lm, b, g * p.G + rr / p.Lq, rr % p.Lq) + j);
+              x = fmaf(sc, c2, mv) + (first ? nla : nlb);
+            }
+            acc2[mt][nt][e] = vis ? ex2(x) : 0.f;
           }
-          pv[e] = vis ? ex2(x) : 0.f;
-          dsv[e] = pv[e] * (dp[nt][e] + (first ? nda : ndb));
         }
-        *reinterpret_cast<uint32_t*>(sm + L::kP + ra * L::kPStride + kl * 2) = pack2<T>(pv[0], pv[1]);
-        *reinterpret_cast<uint32_t*>(sm + L::kP + rb * L::kPStride + kl * 2) = pack2<T>(pv[2], pv[3]);
-        *reinterpret_cast<uint32_t*>(sm + L::kDs + ra * L::kPStride + kl * 2) = pack2<T>(dsv[0], dsv[1]);
-        *reinterpret_cast<uint32_t*>(sm + L::kDs + rb * L::kPStride + kl * 2) = pack2<T>(dsv[2], dsv[3]);
+      }
+      pair_bar<true>(q4);
+      float dsv[MT][2][4];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const int ra = 16 * mt + lane / 4, rb = ra + 8;
+        const float nda = ndelta[ra], ndb = ndelta[rb];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dsv[mt][nt][e] =
+                acc2[mt][nt][e] * (dpf[((mt * 2 + nt) * 4 + e) * 32 + lane] + (e < 2 ? nda : ndb));
+      }
+      p_warps_bar();  // every P warp has read its dP: P and dS may now overwrite the hand-off
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        const int ra = 16 * mt + lane / 4, rb = ra + 8;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int kl = 16 * q4 + 8 * nt + 2 * (lane % 4);
+          const float* pv = acc2[mt][nt];
+          const float* ds = dsv[mt][nt];
+          *reinterpret_cast<uint32_t*>(sm + L::kP + ra * L::kPStride + kl * 2) = pack2<T>(pv[0], pv[1]);
+          *reinterpret_cast<uint32_t*>(sm + L::kP + rb * L::kPStride + kl * 2) = pack2<T>(pv[2], pv[3]);
+          *reinterpret_cast<uint32_t*>(sm + L::kDs + ra * L::kPStride + kl * 2) = pack2<T>(ds[0], ds[1]);
+          *reinterpret_cast<uint32_t*>(sm + L::kDs + rb * L::kPStride + kl * 2) = pack2<T>(ds[2], ds[3]);
+        }
       }
     }
     __syncthreads();
-    // ---- phase C (i): dV = Pᵀ·dO and dK = scale·dSᵀ·Q for keys [16w, 16w+16)
-#pragma unroll 1
-    for (int which = 0; which < 2; ++which) {
+    // ---- phase C (i): warp (q, 0) dV = Pᵀ·dO, warp (q, 1) dK = scale·dSᵀ·Q, keys [16q, 16q+16)
+    uint32_t pk[D / 8][2];  // the result as 16-bit pairs: [8-dim block][key row lane/4, +8]
+    {
+      const int which = half;
       const uint32_t a_s = which == 0 ? ps : dss;
       const uint32_t b_s = which == 0 ? dos : qs;
       float acc[D / 8][4];
@@ -561,7 +638,7 @@ __global__ void __launch_bounds__(128) vec_mma_bwd_kernel(const __grid_constant_
 #pragma unroll
       for (int ks = 0; ks < MT; ++ks) {
         uint32_t a[4];
-        const int prow = 16 * ks + (mm / 2) * 8 + (lane % 8), pcol = 16 * warp + (mm % 2) * 8;
+        const int prow = 16 * ks + (mm / 2) * 8 + (lane % 8), pcol = 16 * q4 + (mm % 2) * 8;
         ldsm_x4_t(a_s + prow * L::kPStride + pcol * 2, a[0], a[1], a[2], a[3]);
 #pragma unroll
         for (int dn2 = 0; dn2 < D / 16; ++dn2) {
@@ -573,23 +650,18 @@ __global__ void __launch_bounds__(128) vec_mma_bwd_kernel(const __grid_constant_
         }
       }
       const float mul = which == 0 ? 1.f : p.scale;
-      T* dst = which == 0 ? dvg : dkg;
-      const int64_t rs = which == 0 ? p.ldv.sl : p.ldk.sl;
-      const int ja = tile_key0 + 16 * warp + lane / 4, jb = ja + 8;
 #pragma unroll
       for (int dn = 0; dn < D / 8; ++dn) {
-        const int d = 8 * dn + 2 * (lane % 4);
-        if (ja < j_own_end)
-          *reinterpret_cast<uint32_t*>(dst + (int64_t)ja * rs + d) = pack2<T>(acc[dn][0] * mul, acc[dn][1] * mul);
-        if (jb < j_own_end)
-          *reinterpret_cast<uint32_t*>(dst + (int64_t)jb * rs + d) = pack2<T>(acc[dn][2] * mul, acc[dn][3] * mul);
+        pk[dn][0] = pack2<T>(acc[dn][0] * mul, acc[dn][1] * mul);
+        pk[dn][1] = pack2<T>(acc[dn][2] * mul, acc[dn][3] * mul);
       }
     }
-    // ---- phase C (ii): dQ[:, w·D/4 : (w+1)·D/4) += dS·K over this tile's 64 keys
+    // ---- phase C (ii): dQ[:, q·D/4 : (q+1)·D/4) += dS·K over keys [32h, 32h+32) of the tile
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
-      for (int kk = 0; kk < kKeys / 16; ++kk) {
+      for (int k2 = 0; k2 < kKeys / 32; ++k2) {
+        const int kk = (kKeys / 32) * half + k2;
         uint32_t a[4];
         const int arow = 16 * mt + (mm % 2) * 8 + (lane % 8), acol = 16 * kk + (mm / 2) * 8;
         ldsm_x4(dss + arow * L::kPStride + acol * 2, a[0], a[1], a[2], a[3]);
@@ -597,11 +669,37 @@ __global__ void __launch_bounds__(128) vec_mma_bwd_kernel(const __grid_constant_
         for (int np = 0; np < kDqTiles / 2; ++np) {
           const int key = 16 * kk + (mm % 2) * 8 + (lane % 8);
           uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(swz<D>(kt, key, (warp * D / 4) / 8 + 2 * np + mm / 2), b0, b1, b2, b3);
+          ldsm_x4_t(swz<D>(kt, key, (q4 * D / 4) / 8 + 2 * np + mm / 2), b0, b1, b2, b3);
           mma16816<T>(dq[mt][2 * np], a, b0, b1);
           mma16816<T>(dq[mt][2 * np + 1], a, b2, b3);
         }
       }
+    }
+    // ---- phase C (iii): once every warp is done with this stage's K and V, each warp
+    // stages its 16 rows of dV (over V) or dK (over K), 16-byte block c of row r at block
+    // c ^ (r % 8) (conflict-free fragment writes), and stores whole rows with 16-byte stores.
+    __syncthreads();
+    {
+      uint8_t* stg = sm + s * L::kStageBytes + (half == 0 ? L::kTileBytes : 0) + q4 * 16 * (D * 2);
+      const int r0 = lane / 4, r1 = r0 + 8, cb = (lane % 4) * 4;
+#pragma unroll
+      for (int dn = 0; dn < D / 8; ++dn) {
+        *reinterpret_cast<uint32_t*>(stg + r0 * (D * 2) + ((dn ^ (r0 & 7)) * 16) + cb) = pk[dn][0];
+        *reinterpret_cast<uint32_t*>(stg + r1 * (D * 2) + ((dn ^ (r1 & 7)) * 16) + cb) = pk[dn][1];
+      }
+      __syncwarp();
+      T* dst = half == 0 ? dvg : dkg;
+      const int64_t rs = half == 0 ? p.ldv.sl : p.ldk.sl;
+      constexpr int kBlocks = D / 8;        // 16-byte blocks per row
+      constexpr int kRowsPer = 32 / kBlocks;
+      const int ch = lane % kBlocks;
+#pragma unroll
+      for (int r = lane / kBlocks; r < 16; r += kRowsPer) {
+        const int j = tile_key0 + 16 * q4 + r;
+        const uint4 v = *reinterpret_cast<const uint4*>(stg + r * (D * 2) + ((ch ^ (r & 7)) * 16));
+        if (j < j_own_end) *reinterpret_cast<uint4*>(dst + (int64_t)j * rs + ch * 8) = v;
+      }
+      fence_async_smem();  // these generic-proxy writes come before the next tile's TMA write here
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
@@ -609,7 +707,8 @@ __global__ void __launch_bounds__(128) vec_mma_bwd_kernel(const __grid_constant_
       if (!mbar_wait(&empty[s], (t / kBwdRing) & 1, wc)) ok = false;
       else issue(issued++);
     }
-    __syncthreads();  // phase A of the next tile rewrites P and dS
+    // no barrier here: the last reads of P and dS came before the staging barrier, and the
+    // next tile starts with a block-wide vote
   }
   if (threadIdx.x == 0 && (!ok || abort_flag)) {  // let copies still in flight land
     for (int t = max(0, issued - kBwdRing); t < issued; ++t) {
@@ -625,24 +724,29 @@ __global__ void __launch_bounds__(128) vec_mma_bwd_kernel(const __grid_constant_
     dkg[jj * p.ldk.sl + d] = Elem<T>::from_f(0.f);
     dvg[jj * p.ldv.sl + d] = Elem<T>::from_f(0.f);
   }
-  __syncthreads();  // the ring is free: reuse it for the dQ partial of this block
+  __syncthreads();  // the ring is free: reuse it for the two dQ partials of this block
   float* cta_dq = reinterpret_cast<float*>(sm + L::kDq);
+  float* my_dq = cta_dq + half * (L::kRows * D);
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
     for (int nt = 0; nt < kDqTiles; ++nt) {
-      const int r = 16 * mt + lane / 4, d = warp * D / 4 + 8 * nt + 2 * (lane % 4);
-      cta_dq[r * D + d] = dq[mt][nt][0];
-      cta_dq[r * D + d + 1] = dq[mt][nt][1];
-      cta_dq[(r + 8) * D + d] = dq[mt][nt][2];
-      cta_dq[(r + 8) * D + d + 1] = dq[mt][nt][3];
+      const int r = 16 * mt + lane / 4, d = q4 * D / 4 + 8 * nt + 2 * (lane % 4);
+      my_dq[r * D + d] = dq[mt][nt][0];
+      my_dq[r * D + d + 1] = dq[mt][nt][1];
+      my_dq[(r + 8) * D + d] = dq[mt][nt][2];
+      my_dq[(r + 8) * D + d + 1] = dq[mt][nt][3];
     }
   cluster.sync();
   constexpr int kSlice = D / kCs;
   for (int e = threadIdx.x; e < R * kSlice; e += blockDim.x) {
     const int r = e / kSlice, d = c * kSlice + e % kSlice;
     float acc = 0.f;
-    for (int cc = 0; cc < kCs; ++cc) acc += cluster.map_shared_rank(cta_dq, cc)[r * D + d];
+    for (int cc = 0; cc < kCs; ++cc) {
+      const float* src = cluster.map_shared_rank(cta_dq, cc);
+      acc += src[r * D + d];
+      acc += src[L::kRows * D + r * D + d];
+    }
     row_ptr<T>(p.dq, p.ldq, b, g * p.G + r / p.Lq, r % p.Lq)[d] = Elem<T>::from_f(acc * p.scale);
   }
   cluster.sync();
@@ -660,7 +764,7 @@ cudaError_t vec_mma_bwd_t(const Problem& p, cudaStream_t s) {
   const int chunk = ((p.Lkv + kCs - 1) / kCs + kKeys - 1) / kKeys * kKeys;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kCs, p.Hkv, p.B);
-  cfg.blockDim = dim3(128, 1, 1);
+  cfg.blockDim = dim3(32 * kBwdWarps, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
