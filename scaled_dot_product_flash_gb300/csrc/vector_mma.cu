@@ -11,9 +11,10 @@
 //
 // One cluster of 8 blocks per (batch, KV head); block c owns a contiguous chunk of keys,
 // streamed by TMA in 64-key tiles through a 3-stage ring (each K/V byte read once).
-// A block has four warps; with MT row blocks of 16 (MT = 1 or 2), warp (mt, kq) takes rows
-// [16mt, 16mt+16) of the group and the 64/(4/MT)-key slice kq of every tile, in 16-key
-// steps, keeping its own online-softmax state (row maximum, row sum, O).  At the end the
+// A forward block has four warps; with MT row blocks of 16 (MT = 1 or 2), warp (mt, kq)
+// takes rows [16mt, 16mt+16) of the group and the 64/(4/MT)-key slice kq of every tile, in
+// 16-key steps, keeping its own online-softmax state (row maximum, row sum, O).  (The
+// backward's eight-warp layout is described above its kernel.)  At the end the
 // key slices are merged in shared memory and the eight blocks of the cluster through
 // distributed shared memory (log-sum-exp merge), so no workspace is needed.  Row r of the
 // group is query r % Lq of head g·G + r / Lq.
